@@ -1,0 +1,242 @@
+"""fp64 CPU oracle for the speculative-verify weight stream (TEST INFRASTRUCTURE ONLY).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import
+this package.  The product library never loads it and shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, one thread per output row); this module only
+builds it with gcc and marshals numpy arrays through ctypes.  Every function cites, in the C source,
+the passage of the pages it follows:
+
+* "lithos-metal: per-layer megakernels for Qwen3.8-27B on an M5 Max" -- "What one token costs the
+  bus" (byte table), "Formats, and what runs where" (NVFP4 = E2M1 code x E4M3 block scale per 16 x
+  FP32 tensor-scale multiplier; scale codes top out at 448; BF16 activations, wide accumulation),
+  "The megakernel is per layer, not per step" (greedy acceptance, 1..8 tokens per round).
+* "144 tok/s needs 502 GB/s" (Splash) -- "The engine hard-codes the model" (geometry).
+* "Beating Splash on an M5 Max" -- "The bugs a second reviewer found" (one argmax tie rule).
+
+Parity status: every function here is pinned by a ``-m "not gpu"`` test against page values,
+closed forms, library routines or brute force, except the 64-layer surrogate chain, whose
+end-to-end fp64 result is only pinned through its parts and a small independent re-composition.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+NVFP4 = 0
+FP8 = 1
+PTRS_PER_LAYER = 9
+SCALES_PER_LAYER = 6
+
+
+def build(force: bool = False) -> str:
+    """Compiles oracle.c into liboracle.so with gcc (portable flags, no FMA contraction)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off",
+           "-D_DEFAULT_SOURCE", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+class Geom(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int), ("hidden", ctypes.c_int), ("inter", ctypes.c_int),
+                ("vocab", ctypes.c_int), ("period", ctypes.c_int), ("gdn_in", ctypes.c_int),
+                ("gdn_z", ctypes.c_int), ("attn_q", ctypes.c_int), ("attn_kv", ctypes.c_int),
+                ("attn_z", ctypes.c_int), ("eps", ctypes.c_double)]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            L.orc_e2m1.restype = ctypes.c_double
+            L.orc_e2m1.argtypes = [ctypes.c_int]
+            L.orc_e4m3.restype = ctypes.c_double
+            L.orc_e4m3.argtypes = [ctypes.c_int]
+            L.orc_tables.argtypes = [P, P]
+            L.orc_bf16_value.restype = ctypes.c_double
+            L.orc_bf16_value.argtypes = [ctypes.c_uint16]
+            L.orc_bf16_values.argtypes = [P, P, ctypes.c_int64]
+            L.orc_bf16_round1.restype = ctypes.c_uint16
+            L.orc_bf16_round1.argtypes = [ctypes.c_double]
+            L.orc_bf16_round.argtypes = [P, P, ctypes.c_int64]
+            L.orc_linear.restype = ctypes.c_int
+            L.orc_linear.argtypes = [ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
+                                     ctypes.c_double, P, ctypes.c_int64, P, P, ctypes.c_int]
+            L.orc_silu_mul.argtypes = [P, P, ctypes.c_int64, P]
+            L.orc_rmsnorm.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
+            L.orc_argmax.restype = ctypes.c_int64
+            L.orc_argmax.argtypes = [P, ctypes.c_int64]
+            L.orc_accept.argtypes = [P, P, ctypes.c_int, P, P]
+            L.orc_verify_pass.restype = ctypes.c_int
+            L.orc_verify_pass.argtypes = [ctypes.POINTER(Geom), P, P, P, P, ctypes.c_double, P,
+                                          ctypes.c_int, P, P, P, P, P, P, P, ctypes.c_int]
+            L.orc_pass_bytes.argtypes = [ctypes.POINTER(Geom), P]
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def e2m1_table() -> np.ndarray:
+    a = np.zeros(16, np.float64)
+    b = np.zeros(256, np.float64)
+    lib().orc_tables(_p(a), _p(b))
+    return a
+
+
+def e4m3_table() -> np.ndarray:
+    a = np.zeros(16, np.float64)
+    b = np.zeros(256, np.float64)
+    lib().orc_tables(_p(a), _p(b))
+    return b
+
+
+def bf16_value(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64 values."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, np.float64)
+    lib().orc_bf16_values(_p(bits), _p(out), bits.size)
+    return out
+
+
+def bf16_round(v: np.ndarray) -> np.ndarray:
+    """fp64 -> bf16 bit patterns, round to nearest even, rounding once."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    lib().orc_bf16_round(_p(v), _p(out), v.size)
+    return out
+
+
+def linear(fmt: int, x_bf16: np.ndarray, codes: np.ndarray, scales: np.ndarray | None, ts: float,
+           N: int, rows: np.ndarray | None = None, with_abs: bool = True, nthreads: int | None = None):
+    """y[m][i] = sum_k x[m][k] w[rows[i]][k] (fp64) and a = sum_k |x w| (tolerance scale).
+
+    x_bf16: uint16 [M][K]; codes: NVFP4 uint8 [N][K/2] or FP8 uint8 [N][K]; scales: NVFP4 uint8
+    [N][K/16].  rows: optional int32 subset of output rows (codes/scales still hold all N rows, or
+    exactly the listed rows when ``rows`` indexes into a row-sampled array)."""
+    x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x_bf16.shape
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint8) if scales is not None else None
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        n_rows = rows.size
+    else:
+        n_rows = N
+    y = np.zeros((M, n_rows), np.float64)
+    a = np.zeros((M, n_rows), np.float64) if with_abs else None
+    rc = lib().orc_linear(fmt, _p(x_bf16), M, K, N, _p(codes), _p(sc) if sc is not None else None,
+                          float(ts), _p(rows) if rows is not None else None, n_rows, _p(y),
+                          _p(a) if a is not None else None, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("orc_linear rejected its arguments")
+    return (y, a) if with_abs else y
+
+
+def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    out = np.empty_like(g)
+    lib().orc_silu_mul(_p(g), _p(u), g.size, _p(out))
+    return out
+
+
+def rmsnorm(h_bf16: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    h = np.ascontiguousarray(h_bf16, dtype=np.uint16)
+    M, D = h.shape
+    out = np.empty_like(h)
+    lib().orc_rmsnorm(_p(h), M, D, float(eps), _p(out))
+    return out
+
+
+def argmax(v: np.ndarray) -> int:
+    v = np.ascontiguousarray(v, dtype=np.float64).reshape(-1)
+    return int(lib().orc_argmax(_p(v), v.size))
+
+
+def accept(t: np.ndarray, pending: np.ndarray):
+    t = np.ascontiguousarray(t, dtype=np.int32)
+    pending = np.ascontiguousarray(pending, dtype=np.int32)
+    lanes = t.size // 8
+    nc = np.zeros(lanes, np.int32)
+    cm = np.zeros((lanes, 8), np.int32)
+    lib().orc_accept(_p(t), _p(pending), lanes, _p(nc), _p(cm))
+    return nc, cm
+
+
+def geom(n_layers=64, hidden=5120, inter=17408, vocab=248320, period=4, gdn_in=16384, gdn_z=6144,
+         attn_q=12288, attn_kv=2048, attn_z=6144, eps=1e-6) -> Geom:
+    return Geom(n_layers, hidden, inter, vocab, period, gdn_in, gdn_z, attn_q, attn_kv, attn_z, eps)
+
+
+def pass_bytes(g: Geom) -> np.ndarray:
+    out = np.zeros(6, np.int64)
+    lib().orc_pass_bytes(ctypes.byref(g), _p(out))
+    return out
+
+
+def verify_pass(g: Geom, layers: list, head: tuple, x0_bf16: np.ndarray, pending: np.ndarray,
+                want_trace: bool = False, want_logits: bool = False, nthreads: int | None = None):
+    """Runs the surrogate pass.  ``layers[l]`` is a dict with keys in, kv (None on GDN layers), out,
+    gate_c, gate_s, up_c, up_s, down_c, down_s (canonical uint8 arrays) and s_in, s_kv, s_out,
+    ts_gate, ts_up, ts_down (floats).  ``head`` = (codes, scales, ts)."""
+    L = g.n_layers
+    keep = []
+    ptrs = (ctypes.c_void_p * (L * PTRS_PER_LAYER))()
+    scs = np.zeros(L * SCALES_PER_LAYER, np.float64)
+    names = ["in", "kv", "out", "gate_c", "gate_s", "up_c", "up_s", "down_c", "down_s"]
+    snames = ["s_in", "s_kv", "s_out", "ts_gate", "ts_up", "ts_down"]
+    for l, d in enumerate(layers):
+        for j, nm in enumerate(names):
+            a = d.get(nm)
+            if a is None:
+                ptrs[l * PTRS_PER_LAYER + j] = None
+            else:
+                a = np.ascontiguousarray(a, dtype=np.uint8)
+                keep.append(a)
+                ptrs[l * PTRS_PER_LAYER + j] = a.ctypes.data
+        for j, nm in enumerate(snames):
+            scs[l * SCALES_PER_LAYER + j] = float(d.get(nm, 1.0))
+    hc = np.ascontiguousarray(head[0], dtype=np.uint8)
+    hs = np.ascontiguousarray(head[1], dtype=np.uint8)
+    x0 = np.ascontiguousarray(x0_bf16, dtype=np.uint16)
+    M = x0.shape[0]
+    pend = np.ascontiguousarray(pending, dtype=np.int32)
+    am = np.zeros(M, np.int32)
+    nc = np.zeros(M // 8, np.int32)
+    cm = np.zeros((M // 8, 8), np.int32)
+    trace = np.zeros((2 * L, M, g.hidden), np.uint16) if want_trace else None
+    logits = np.zeros((M, g.vocab), np.float64) if want_logits else None
+    final_r = np.zeros((M, g.hidden), np.uint16)
+    rc = lib().orc_verify_pass(ctypes.byref(g), ctypes.cast(ptrs, ctypes.c_void_p), _p(scs), _p(hc),
+                               _p(hs), float(head[2]), _p(x0), M, _p(pend), _p(am), _p(nc), _p(cm),
+                               _p(trace) if trace is not None else None,
+                               _p(logits) if logits is not None else None, _p(final_r),
+                               nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("orc_verify_pass rejected its arguments")
+    return {"argmax": am, "n_commit": nc, "committed": cm, "trace": trace, "logits": logits,
+            "final_r": final_r}

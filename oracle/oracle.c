@@ -1,0 +1,389 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU reference for the speculative-verify weight stream.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call this file;
+ * only the tests, the package smoke check and the bench's CPU-baseline leg use it.  It shares no
+ * code, header, table or constant generator with the CUDA library.
+ *
+ * Sources (web pages, cited by title and section):
+ *  - "lithos-metal: per-layer megakernels for Qwen3.8-27B on an M5 Max", section "What one token
+ *    costs the bus" (the NVFP4/FP8 byte table) and section "Formats, and what runs where": NVFP4 is an
+ *    E2M1 code, one FP8 E4M3 block scale per 16 weights and an FP32 tensor scale used as a
+ *    MULTIPLIER; block-scale codes top out at exactly 448 (so E4M3 is the finite-only "FN" variant);
+ *    arithmetic is weight-only with BF16 activations/residuals and FP32 (here: fp64) accumulation.
+ *  - same page, section "The megakernel is per layer, not per step": the greedy acceptance scan
+ *    (accept the longest prefix of drafts that equal the target's tokens, then commit the target's
+ *    own token after it; a round commits 1..8 tokens).
+ *  - "144 tok/s needs 502 GB/s" (Splash engine), section "The engine hard-codes the model": the
+ *    geometry (64 layers, hidden 5120, vocab 248320, intermediate 17408, fullAttentionPeriod = 4).
+ *  - "Beating Splash on an M5 Max", section "The bugs a second reviewer found": the argmax tie
+ *    rule must be the same everywhere (here: lowest index among equal maxima).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *  - E2M1 bit layout: bit 3 = sign, bits 2..1 = exponent (bias 1), bit 0 = mantissa (OCP MX).
+ *  - Packing of two E2M1 codes per byte: element 2j is the LOW nibble of byte j.
+ *  - Block scales run along K: scale[n][k/16].
+ *  - Argmax: NaN is treated as -inf; -0 == +0; the lowest index among equal maxima wins.
+ *  - The verify-pass surrogate (mixer cores replaced by slices) -- see orc_verify_pass().
+ *
+ * Everything is computed in fp64 from the plain definitions, with no blocking or reordering:
+ * w[n][k] = e2m1(code) * e4m3(scale) * ts, y[m][n] = sum_k x[m][k] * w[n][k].
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ formats */
+
+/* E2M1 magnitudes for codes 0..7; codes 8..15 are their negatives (code 8 is -0). */
+static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1(int code) {
+    code &= 15;
+    double v = E2M1_MAG[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+/* E4M3 "FN": 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0 is subnormal (m/8 * 2^-6);
+ * S.1111.111 is NaN; there are no infinities, so the largest finite value is 1.75 * 2^8 = 448. */
+double orc_e4m3(int byte) {
+    byte &= 255;
+    int s = byte >> 7, e = (byte >> 3) & 15, m = byte & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+void orc_tables(double* e2m1_16, double* e4m3_256) {
+    for (int c = 0; c < 16; ++c) e2m1_16[c] = orc_e2m1(c);
+    for (int b = 0; b < 256; ++b) e4m3_256[b] = orc_e4m3(b);
+}
+
+/* bf16 bits -> value (exact). */
+double orc_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+void orc_bf16_values(const uint16_t* in, double* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_value(in[i]);
+}
+
+/* fp64 -> bf16 with round-to-nearest-even, rounding once, directly from fp64. */
+uint16_t orc_bf16_round1(double v) {
+    if (isnan(v)) return 0x7FC0;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e;
+    frexp(a, &e);           /* a in [2^(e-1), 2^e) */
+    int q = e - 8;          /* 8 significant bits -> quantum 2^(e-8) */
+    if (q < -133) q = -133; /* bf16 subnormal quantum */
+    double r = nearbyint(ldexp(a, -q)); /* default rounding mode: to nearest, ties to even */
+    double rv = ldexp(r, q);
+    if (rv >= 0x1p128) return sign | 0x7F80;
+    float f = (float)rv; /* exact: rv has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return sign | (uint16_t)((u >> 16) & 0x7FFF);
+}
+
+void orc_bf16_round(const double* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_round1(in[i]);
+}
+
+/* ------------------------------------------------------------------ threading */
+
+typedef struct {
+    void (*fn)(void* ctx, int64_t i);
+    void* ctx;
+    int64_t n;
+    int tid, nthreads;
+} orc_job;
+
+static void* orc_job_run(void* p) {
+    orc_job* j = (orc_job*)p;
+    for (int64_t i = j->tid; i < j->n; i += j->nthreads) j->fn(j->ctx, i);
+    return NULL;
+}
+
+/* Runs fn(ctx, i) for i in [0, n) on up to nthreads threads (rows are independent). */
+static void orc_parallel(int nthreads, int64_t n, void (*fn)(void*, int64_t), void* ctx) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if ((int64_t)nthreads > n) nthreads = (int)(n > 0 ? n : 1);
+    pthread_t th[256];
+    orc_job jobs[256];
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].fn = fn; jobs[t].ctx = ctx; jobs[t].n = n; jobs[t].tid = t; jobs[t].nthreads = nthreads;
+    }
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, orc_job_run, &jobs[t]) != 0) break;
+        started = t;
+    }
+    orc_job_run(&jobs[0]);
+    for (int t = started + 1; t < nthreads; ++t) orc_job_run(&jobs[t]); /* threads that failed to start */
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+}
+
+/* ------------------------------------------------------------------ linear layers */
+
+/* Weight formats handled by orc_linear. */
+enum { ORC_NVFP4 = 0, ORC_FP8 = 1 };
+
+typedef struct {
+    int fmt;
+    const double* x; /* [M][K] activation values (bf16 values widened to fp64) */
+    int M, K, N;
+    const uint8_t* codes;  /* NVFP4: [N][K/2], element 2j = low nibble of byte j.  FP8: [N][K] */
+    const uint8_t* scales; /* NVFP4: [N][K/16] E4M3 block scales; unused for FP8 */
+    double ts;             /* NVFP4 tensor scale / FP8 per-tensor scale (a multiplier) */
+    const int32_t* rows;   /* rows to compute (NULL = all N) */
+    double* y;             /* [M][n_rows] */
+    double* a;             /* [M][n_rows] sum |x*w| (may be NULL) */
+    int64_t n_rows;
+} orc_lin_ctx;
+
+/* Dequantizes weight row n to fp64 by the definition, then forms the M dot products. */
+static void orc_lin_row(void* p, int64_t i) {
+    orc_lin_ctx* c = (orc_lin_ctx*)p;
+    int64_t n = c->rows ? c->rows[i] : i;
+    int K = c->K;
+    double* w = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!w) return;
+    if (c->fmt == ORC_NVFP4) {
+        const uint8_t* cr = c->codes + n * (int64_t)(K / 2);
+        const uint8_t* sr = c->scales + n * (int64_t)(K / 16);
+        for (int k = 0; k < K; ++k) {
+            int byte = cr[k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            w[k] = orc_e2m1(code) * orc_e4m3(sr[k / 16]) * c->ts;
+        }
+    } else {
+        const uint8_t* wr = c->codes + n * (int64_t)K;
+        for (int k = 0; k < K; ++k) w[k] = orc_e4m3(wr[k]) * c->ts;
+    }
+    for (int m = 0; m < c->M; ++m) {
+        const double* xr = c->x + (int64_t)m * K;
+        double s = 0.0, sa = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double p2 = xr[k] * w[k];
+            s += p2;
+            sa += fabs(p2);
+        }
+        c->y[(int64_t)m * c->n_rows + i] = s;
+        if (c->a) c->a[(int64_t)m * c->n_rows + i] = sa;
+    }
+    free(w);
+}
+
+/* y[m][i] = sum_k x[m][k] * w[rows[i]][k] in fp64; a[m][i] = sum_k |x[m][k] * w[rows[i]][k]|.
+ * x holds bf16 bit patterns [M][K].  Returns 0, or -1 on bad arguments. */
+int orc_linear(int fmt, const uint16_t* x_bf16, int M, int K, int N, const uint8_t* codes,
+               const uint8_t* scales, double ts, const int32_t* rows, int64_t n_rows, double* y,
+               double* a, int nthreads) {
+    if (M < 0 || K <= 0 || N <= 0 || !x_bf16 || !codes || !y) return -1;
+    if (fmt == ORC_NVFP4 && (K % 16 != 0 || !scales)) return -1;
+    if (fmt != ORC_NVFP4 && fmt != ORC_FP8) return -1;
+    if (!rows) n_rows = N;
+    for (int64_t i = 0; rows && i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= N) return -1;
+    double* x = (double*)malloc(sizeof(double) * (size_t)M * (size_t)K + 8);
+    if (!x) return -1;
+    for (int64_t i = 0; i < (int64_t)M * K; ++i) x[i] = orc_bf16_value(x_bf16[i]);
+    orc_lin_ctx c = {fmt, x, M, K, N, codes, scales, ts, rows, y, a, n_rows};
+    orc_parallel(nthreads, n_rows, orc_lin_row, &c);
+    free(x);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ glue */
+
+/* silu(g) = g / (1 + exp(-g)); out = silu(g) * u, fp64. */
+void orc_silu_mul(const double* g, const double* u, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}
+
+/* RMSNorm with unit weight: r = bf16( h / sqrt(mean(h^2) + eps) ), per row, fp64 inside. */
+void orc_rmsnorm(const uint16_t* h, int M, int D, double eps, uint16_t* r) {
+    for (int m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int k = 0; k < D; ++k) {
+            double v = orc_bf16_value(h[(int64_t)m * D + k]);
+            ss += v * v;
+        }
+        double denom = sqrt(ss / (double)D + eps);
+        for (int k = 0; k < D; ++k)
+            r[(int64_t)m * D + k] = orc_bf16_round1(orc_bf16_value(h[(int64_t)m * D + k]) / denom);
+    }
+}
+
+/* Lowest index of the maximum; NaN counts as -inf, and -0 == +0 (IEEE compare). */
+int64_t orc_argmax(const double* v, int64_t n) {
+    int64_t best = 0;
+    double bv = -INFINITY;
+    for (int64_t i = 0; i < n; ++i) {
+        double x = isnan(v[i]) ? -INFINITY : v[i];
+        if (i == 0 || x > bv) {
+            bv = x;
+            best = i;
+        }
+    }
+    return best;
+}
+
+/* Greedy acceptance per lane (8 rows: the committed anchor token + 7 drafts).
+ * t[8l + j] is the target's token at verify row j; pending[8l + j + 1] is draft j.
+ * acc = number of leading drafts equal to the target's tokens (0..7);
+ * n_commit = acc + 1 and committed[l][0..acc] = t[8l .. 8l + acc] (accepted drafts, then the
+ * target's own token); committed[l][acc+1..7] = -1. */
+void orc_accept(const int32_t* t, const int32_t* pending, int lanes, int32_t* n_commit,
+                int32_t* committed) {
+    for (int l = 0; l < lanes; ++l) {
+        int base = 8 * l, acc = 0;
+        while (acc < 7 && t[base + acc] == pending[base + acc + 1]) acc++;
+        n_commit[l] = acc + 1;
+        for (int j = 0; j < 8; ++j) committed[8 * l + j] = (j <= acc) ? t[base + j] : -1;
+    }
+}
+
+/* ------------------------------------------------------------------ verify-pass surrogate */
+
+/* Geometry of the pass.  Layer l is an attention layer when l % period == period - 1, otherwise a
+ * Gated DeltaNet layer (fullAttentionPeriod = 4 on the Splash page). */
+typedef struct {
+    int n_layers, hidden, inter, vocab, period;
+    int gdn_in, gdn_z;            /* GDN in-projection width (16384) and out-projection K (6144) */
+    int attn_q, attn_kv, attn_z;  /* attention q (12288), kv (2048) widths, o-projection K (6144) */
+    double eps;
+} orc_geom;
+
+/* Per layer, pointers in this order (canonical layouts, see orc_linear):
+ *   [0] mixer in-projection  FP8 [gdn_in or attn_q][hidden]
+ *   [1] attention kv         FP8 [attn_kv][hidden] (NULL on GDN layers; streamed, unused here)
+ *   [2] mixer out-projection FP8 [hidden][gdn_z or attn_z]
+ *   [3] gate codes [inter][hidden/2]  [4] gate scales [inter][hidden/16]
+ *   [5] up codes                      [6] up scales
+ *   [7] down codes [hidden][inter/2]  [8] down scales [hidden][inter/16]
+ * and per layer the scales in this order: s_in, s_kv, s_out, ts_gate, ts_up, ts_down. */
+#define ORC_PTRS_PER_LAYER 9
+#define ORC_SCALES_PER_LAYER 6
+
+static int orc_lin_bf16(int fmt, const uint16_t* x, int M, int K, int N, const uint8_t* codes,
+                        const uint8_t* scales, double ts, double* y, int nthreads) {
+    return orc_linear(fmt, x, M, K, N, codes, scales, ts, NULL, N, y, NULL, nthreads);
+}
+
+/*
+ * The surrogate pass (mixer cores are outside the weight stream; the plainest shape-consistent
+ * stand-in keeps every weight GEMM and replaces each core by a slice):
+ *   h = x0
+ *   for l in layers:
+ *     r = RMSNorm(h)
+ *     GDN:  u = FP8(in, r);  z = bf16(u[:, :gdn_z]);   h = bf16(h + FP8(out, z))
+ *     attn: q = FP8(q, r);   (kv = FP8(kv, r) is streamed but unused);
+ *           z = bf16(q[:, :attn_z]);                   h = bf16(h + FP8(o, z))
+ *     r = RMSNorm(h);  a = bf16(silu(NVFP4(gate, r)) * NVFP4(up, r));  h = bf16(h + NVFP4(down, a))
+ *   r = RMSNorm(h); logits = NVFP4(head, r); t = argmax per row; accept per lane.
+ * Optional outputs: trace [2*n_layers][M][hidden] bf16 (h after each mixer block and each MLP
+ * block), logits [M][vocab] fp64, final_r [M][hidden] bf16 (the head's input).
+ */
+int orc_verify_pass(const orc_geom* G, const uint8_t* const* layer_ptrs, const double* layer_scales,
+                    const uint8_t* head_codes, const uint8_t* head_scales, double head_ts,
+                    const uint16_t* x0, int M, const int32_t* pending, int32_t* argmax,
+                    int32_t* n_commit, int32_t* committed, uint16_t* trace, double* logits_out,
+                    uint16_t* final_r, int nthreads) {
+    if (!G || M <= 0 || M % 8 != 0 || G->hidden % 16 || G->inter % 16) return -1;
+    int H = G->hidden, I = G->inter, V = G->vocab;
+    int wmax = G->gdn_in > G->attn_q ? G->gdn_in : G->attn_q;
+    if (I > wmax) wmax = I;
+    if (H > wmax) wmax = H;
+    if (V > wmax) wmax = V;
+    uint16_t* h = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)M * H);
+    uint16_t* r = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)M * H);
+    uint16_t* z = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)M * wmax);
+    double* y = (double*)malloc(sizeof(double) * (size_t)M * wmax);
+    double* y2 = (double*)malloc(sizeof(double) * (size_t)M * wmax);
+    int rc = -1;
+    if (!h || !r || !z || !y || !y2) goto done;
+    memcpy(h, x0, sizeof(uint16_t) * (size_t)M * H);
+    for (int l = 0; l < G->n_layers; ++l) {
+        const uint8_t* const* P = layer_ptrs + (int64_t)l * ORC_PTRS_PER_LAYER;
+        const double* S = layer_scales + (int64_t)l * ORC_SCALES_PER_LAYER;
+        int attn = (l % G->period) == G->period - 1;
+        int n_in = attn ? G->attn_q : G->gdn_in;
+        int kz = attn ? G->attn_z : G->gdn_z;
+        /* mixer block */
+        orc_rmsnorm(h, M, H, G->eps, r);
+        if (orc_lin_bf16(ORC_FP8, r, M, H, n_in, P[0], NULL, S[0], y, nthreads)) goto done;
+        for (int m = 0; m < M; ++m)
+            for (int k = 0; k < kz; ++k) z[(int64_t)m * kz + k] = orc_bf16_round1(y[(int64_t)m * n_in + k]);
+        if (orc_lin_bf16(ORC_FP8, z, M, kz, H, P[2], NULL, S[2], y, nthreads)) goto done;
+        for (int64_t i = 0; i < (int64_t)M * H; ++i) h[i] = orc_bf16_round1(orc_bf16_value(h[i]) + y[i]);
+        if (trace) memcpy(trace + (int64_t)(2 * l) * M * H, h, sizeof(uint16_t) * (size_t)M * H);
+        /* MLP block */
+        orc_rmsnorm(h, M, H, G->eps, r);
+        if (orc_lin_bf16(ORC_NVFP4, r, M, H, I, P[3], P[4], S[3], y, nthreads)) goto done;
+        if (orc_lin_bf16(ORC_NVFP4, r, M, H, I, P[5], P[6], S[4], y2, nthreads)) goto done;
+        orc_silu_mul(y, y2, (int64_t)M * I, y);
+        orc_bf16_round(y, z, (int64_t)M * I);
+        if (orc_lin_bf16(ORC_NVFP4, z, M, I, H, P[7], P[8], S[5], y, nthreads)) goto done;
+        for (int64_t i = 0; i < (int64_t)M * H; ++i) h[i] = orc_bf16_round1(orc_bf16_value(h[i]) + y[i]);
+        if (trace) memcpy(trace + (int64_t)(2 * l + 1) * M * H, h, sizeof(uint16_t) * (size_t)M * H);
+    }
+    orc_rmsnorm(h, M, H, G->eps, r);
+    if (final_r) memcpy(final_r, r, sizeof(uint16_t) * (size_t)M * H);
+    {
+        double* lg = logits_out ? logits_out : (double*)malloc(sizeof(double) * (size_t)M * V);
+        if (!lg) goto done;
+        if (orc_lin_bf16(ORC_NVFP4, r, M, H, V, head_codes, head_scales, head_ts, lg, nthreads)) {
+            if (!logits_out) free(lg);
+            goto done;
+        }
+        int32_t* t = (int32_t*)malloc(sizeof(int32_t) * (size_t)M);
+        for (int m = 0; m < M; ++m) t[m] = (int32_t)orc_argmax(lg + (int64_t)m * V, V);
+        for (int m = 0; m < M; ++m) argmax[m] = t[m];
+        orc_accept(t, pending, M / 8, n_commit, committed);
+        free(t);
+        if (!logits_out) free(lg);
+    }
+    rc = 0;
+done:
+    free(h); free(r); free(z); free(y); free(y2);
+    return rc;
+}
+
+/* ------------------------------------------------------------------ byte counts */
+
+/* Bytes one NVFP4 matrix streams: N*K/2 code bytes + N*K/16 scale bytes (9 bytes per 16 weights). */
+int64_t orc_nvfp4_code_bytes(int64_t N, int64_t K) { return N * K / 2; }
+int64_t orc_nvfp4_scale_bytes(int64_t N, int64_t K) { return N * K / 16; }
+int64_t orc_fp8_bytes(int64_t N, int64_t K) { return N * K; }
+
+/* Per-pass byte groups of the pass geometry, in the page's table order:
+ * out[0] MLP codes, out[1] MLP block scales, out[2] GDN FP8, out[3] attention FP8, out[4] head
+ * (codes + scales), out[5] total. */
+void orc_pass_bytes(const orc_geom* G, int64_t* out) {
+    int64_t H = G->hidden, I = G->inter;
+    int64_t n_attn = 0, n_gdn = 0;
+    for (int l = 0; l < G->n_layers; ++l) {
+        if ((l % G->period) == G->period - 1) n_attn++;
+        else n_gdn++;
+    }
+    int64_t L = G->n_layers;
+    out[0] = L * (2 * orc_nvfp4_code_bytes(I, H) + orc_nvfp4_code_bytes(H, I));
+    out[1] = L * (2 * orc_nvfp4_scale_bytes(I, H) + orc_nvfp4_scale_bytes(H, I));
+    out[2] = n_gdn * (orc_fp8_bytes(G->gdn_in, H) + orc_fp8_bytes(H, G->gdn_z));
+    out[3] = n_attn * (orc_fp8_bytes(G->attn_q, H) + orc_fp8_bytes(G->attn_kv, H) +
+                       orc_fp8_bytes(H, G->attn_z));
+    out[4] = orc_nvfp4_code_bytes(G->vocab, H) + orc_nvfp4_scale_bytes(G->vocab, H);
+    out[5] = out[0] + out[1] + out[2] + out[3] + out[4];
+}

@@ -1,0 +1,395 @@
+"""Pins the fp64 oracle to facts that do not come from the oracle itself.
+
+Each test checks one oracle function against values the pages print, a closed form, an independent
+library routine (torch / numpy), or brute force on tiny inputs.  A plausible slip in the oracle
+(a dropped term, a wrong nibble, sign or index, a transposed operand) fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "page_values.json")))
+
+
+# ------------------------------------------------------------------ independent decoders
+
+def e4m3_torch(codes):
+    """E4M3 values from torch's float8_e4m3fn conversion (a library routine)."""
+    t = torch.as_tensor(np.asarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn)
+    return t.to(torch.float64).numpy()
+
+
+def e2m1_formula(code):
+    """Generic minifloat decode: sign bit 3, 2-bit exponent (bias 1), 1-bit mantissa."""
+    s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
+    v = (m / 2.0) if e == 0 else (2.0 ** (e - 1)) * (1.0 + m / 2.0)
+    return -v if s else v
+
+
+def dequant_nvfp4_indep(codes, scales, ts):
+    """Dequantizes canonical NVFP4 with torch's E4M3 and the formula decode (not the oracle)."""
+    lo = codes & 15
+    hi = codes >> 4
+    N, K2 = codes.shape
+    q = np.empty((N, 2 * K2), np.int64)
+    q[:, 0::2] = lo
+    q[:, 1::2] = hi
+    lut = np.array([e2m1_formula(c) for c in range(16)])
+    sv = np.repeat(e4m3_torch(scales), 16, axis=1)
+    return lut[q] * sv * ts
+
+
+def bf16_vals_torch(bits):
+    return torch.from_numpy(np.asarray(bits, np.uint16).view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rand_bf16(rng, shape, scale=1.0):
+    x = torch.from_numpy(rng.standard_normal(shape) * scale).to(torch.bfloat16)
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ formats
+
+def test_e2m1_value_set_matches_page():
+    t = oracle.e2m1_table()
+    assert sorted(set(t.tolist())) == sorted(set(GOLD["e2m1_value_set"]["values"]))
+    assert t[8] == 0.0 and math.copysign(1.0, t[8]) == -1.0  # code 8 is -0
+
+
+def test_e2m1_bit_layout_matches_minifloat_formula():
+    t = oracle.e2m1_table()
+    for c in range(16):
+        assert t[c] == e2m1_formula(c), c
+    # codes 8..15 are the negatives of 0..7, and each half is increasing in magnitude
+    assert np.all(t[8:] == -t[:8])
+    assert np.all(np.diff(t[:8]) > 0)
+
+
+def test_e4m3_table_matches_torch_and_page_max():
+    t = oracle.e4m3_table()
+    ref = e4m3_torch(np.arange(256))
+    nan_o = np.isnan(t)
+    assert np.array_equal(nan_o, np.isnan(ref))
+    assert np.array_equal(np.flatnonzero(nan_o), [0x7F, 0xFF])
+    assert np.array_equal(t[~nan_o], ref[~nan_o])
+    assert np.nanmax(t) == GOLD["e4m3_block_scale_max"]["value"] == t[0x7E]
+    assert t[0x01] == 2.0 ** -9  # smallest subnormal
+    assert t[0x08] == 2.0 ** -6 and t[0x38] == 1.0
+
+
+def test_bf16_round_matches_torch_on_float32_inputs():
+    rng = np.random.default_rng(0)
+    v = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.integers(-40, 38, 20000),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 3.4e38, 1e-40, -1e-41, 9.2e-41]),
+    ]).astype(np.float32)
+    # exact ties between two bf16 neighbours (round half to even)
+    base = rng.integers(0, 0x7F00, 2000).astype(np.uint32) << 16
+    ties = (base | 0x8000).view(np.float32)
+    v = np.concatenate([v, ties]).astype(np.float32)
+    ours = oracle.bf16_round(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+def test_bf16_round_is_single_rounding_from_fp64():
+    # x = 1 + 2^-8 + 2^-40: just above the bf16 tie 1 + 2^-8, so it must round UP to 1 + 2^-7.
+    # Rounding through fp32 first would land exactly on the tie and round down to 1.0.
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    bits = int(oracle.bf16_round(np.array([x]))[0])
+    assert Fraction(float(bf16_vals_torch([bits])[0])) == 1 + Fraction(1, 128)
+    # brute force: nearest bf16 by exact rational distance over a neighbourhood
+    rng = np.random.default_rng(1)
+    xs = rng.standard_normal(300) * 2.0 ** rng.integers(-20, 20, 300)
+    got = oracle.bf16_round(xs)
+    for x, b in zip(xs, got):
+        cands = [int(b) + d for d in (-1, 0, 1)]
+        dist = [abs(Fraction(float(bf16_vals_torch([c & 0xFFFF])[0])) - Fraction(float(x))) for c in cands]
+        assert dist[1] <= min(dist), (x, b)
+
+
+# ------------------------------------------------------------------ linear layers
+
+def test_nvfp4_one_hot_probes_cover_all_codes_and_scales():
+    """x = e_k reproduces w[n][k] = e2m1(code) * e4m3(scale) * ts exactly, for all 16 codes and all
+    127 finite non-negative scale codes 0x00..0x7E."""
+    N, G = 16, 128
+    K = 16 * G
+    codes = np.zeros((N, K // 2), np.uint8)
+    for n in range(N):
+        codes[n, :] = n | (n << 4)
+    scales = np.tile(np.arange(G, dtype=np.uint8), (N, 1))
+    scales[:, 127] = 0x7E  # 0x7F is NaN; keep the last group finite
+    ts = 0.75
+    M = G
+    x = np.zeros((M, K), np.uint16)
+    for m in range(M):
+        x[m, 16 * m + (m % 16)] = 0x3F80  # bf16 1.0
+    y, a = oracle.linear(oracle.NVFP4, x, codes, scales, ts, N)
+    val = np.array(GOLD["e2m1_value_set"]["values"])  # noqa: F841 (the set is pinned above)
+    for m in range(M):
+        sc = e4m3_torch([scales[0, m]])[0]
+        for n in range(N):
+            assert y[m, n] == e2m1_formula(n) * sc * ts
+            assert a[m, n] == abs(e2m1_formula(n) * sc * ts)
+
+
+def test_nvfp4_dyadic_inputs_match_integer_matmul():
+    """Integer x and power-of-two scales make every product an integer multiple of 2^-10, so the
+    exact result is an int64 matmul (numpy) scaled by 2^-10."""
+    rng = np.random.default_rng(2)
+    M, N, K = 5, 24, 128
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    pow2_codes = np.array([0x30, 0x38, 0x40, 0x28], np.uint8)  # 0.5, 1, 2, 0.25
+    scales = pow2_codes[rng.integers(0, 4, (N, K // 16))]
+    xi = rng.integers(-3, 4, (M, K))
+    x = torch.from_numpy(xi.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y = oracle.linear(oracle.NVFP4, x, codes, scales, 1.0, N, with_abs=False)
+    w = dequant_nvfp4_indep(codes, scales, 1.0)
+    wi = np.rint(w * 1024).astype(np.int64)
+    assert np.array_equal(wi / 1024.0, w)
+    exact = (xi.astype(np.int64) @ wi.T) / 1024.0
+    assert np.array_equal(y, exact)
+
+
+def test_nvfp4_matches_numpy_matmul_random():
+    rng = np.random.default_rng(3)
+    M, N, K = 7, 40, 256
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, (N, K // 16), dtype=np.uint8)
+    x = rand_bf16(rng, (M, K))
+    ts = 1.3
+    y, a = oracle.linear(oracle.NVFP4, x, codes, scales, ts, N)
+    w = dequant_nvfp4_indep(codes, scales, ts)
+    xv = bf16_vals_torch(x)
+    np.testing.assert_allclose(y, xv @ w.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a, np.abs(xv) @ np.abs(w).T, rtol=1e-12, atol=1e-12)
+    rows = np.array([39, 0, 17], np.int32)
+    y2, a2 = oracle.linear(oracle.NVFP4, x, codes, scales, ts, N, rows=rows)
+    assert np.array_equal(y2, y[:, rows]) and np.array_equal(a2, a[:, rows])
+
+
+def test_nvfp4_nibble_order_low_first():
+    """Element 2j is the low nibble: a code byte 0x10 (low 0, high 1 = 0.5) only reaches x[2j+1]."""
+    K = 32
+    codes = np.zeros((1, K // 2), np.uint8)
+    codes[0, 3] = 0x10
+    scales = np.full((1, K // 16), 0x38, np.uint8)
+    x = np.zeros((2, K), np.uint16)
+    x[0, 6] = 0x3F80
+    x[1, 7] = 0x3F80
+    y = oracle.linear(oracle.NVFP4, x, codes, scales, 1.0, 1, with_abs=False)
+    assert y[0, 0] == 0.0 and y[1, 0] == 0.5
+
+
+def test_fp8_matches_numpy_matmul_random():
+    rng = np.random.default_rng(4)
+    M, N, K = 9, 33, 96
+    w8 = rng.integers(0, 256, (N, K), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x11  # no NaN codes
+    x = rand_bf16(rng, (M, K))
+    s = 0.37
+    y, a = oracle.linear(oracle.FP8, x, w8, None, s, N)
+    w = e4m3_torch(w8) * s
+    xv = bf16_vals_torch(x)
+    np.testing.assert_allclose(y, xv @ w.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a, np.abs(xv) @ np.abs(w).T, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_rejects_bad_arguments():
+    x = np.zeros((2, 16), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.linear(oracle.NVFP4, x, np.zeros((4, 8), np.uint8), np.zeros((4, 1), np.uint8), 1.0, 4,
+                      rows=np.array([4], np.int32))
+
+
+# ------------------------------------------------------------------ glue
+
+def test_silu_mul_matches_torch_and_closed_forms():
+    rng = np.random.default_rng(5)
+    g = rng.standard_normal(1000) * 20
+    u = rng.standard_normal(1000) * 5
+    out = oracle.silu_mul(g, u)
+    ref = (torch.nn.functional.silu(torch.from_numpy(g)) * torch.from_numpy(u)).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-14, atol=1e-300)
+    z = oracle.silu_mul(np.array([0.0, 50.0, -50.0]), np.array([3.0, 1.0, 1.0]))
+    assert z[0] == 0.0 and abs(z[1] - 50.0) < 1e-18 and abs(z[2]) < 1e-19
+    # silu(-x) = silu(x) - x
+    xs = rng.standard_normal(50)
+    np.testing.assert_allclose(oracle.silu_mul(-xs, np.ones(50)), oracle.silu_mul(xs, np.ones(50)) - xs,
+                               rtol=1e-12, atol=1e-14)
+
+
+def _round_bf16_numpy(v):
+    """Independent fp64 -> bf16 RNE (numpy frexp/rint), values only."""
+    v = np.asarray(v, np.float64)
+    m, e = np.frexp(v)
+    q = np.maximum(e - 8, -133).astype(np.float64)
+    return np.rint(v / 2.0 ** q) * 2.0 ** q
+
+
+def test_rmsnorm_matches_torch_formula():
+    rng = np.random.default_rng(6)
+    h = rand_bf16(rng, (6, 320), 7.0)
+    r = oracle.rmsnorm(h, 1e-6)
+    hv = torch.from_numpy(bf16_vals_torch(h))
+    ref = torch.nn.functional.rms_norm(hv, (320,), eps=1e-6).numpy()
+    assert np.array_equal(bf16_vals_torch(r), _round_bf16_numpy(ref))
+    # closed form: a constant row c maps to c / sqrt(c^2 + eps)
+    c = np.full((1, 64), 0x4040, np.uint16)  # 3.0
+    rc = bf16_vals_torch(oracle.rmsnorm(c, 1e-6))
+    assert np.all(rc == _round_bf16_numpy(3.0 / math.sqrt(9.0 + 1e-6)))
+
+
+def test_argmax_lowest_index_ties_and_nan():
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        v = rng.integers(-3, 4, 50).astype(np.float64)
+        assert oracle.argmax(v) == int(np.argmax(v))  # numpy returns the first maximum
+    assert oracle.argmax(np.array([-0.0, 0.0, -1.0])) == 0
+    assert oracle.argmax(np.array([0.0, -0.0])) == 0
+    assert oracle.argmax(np.array([-1.0, np.nan, 2.0, 2.0])) == 2
+    assert oracle.argmax(np.array([np.nan, -1.0])) == 1
+    assert oracle.argmax(np.array([np.nan, np.nan])) == 0
+    assert oracle.argmax(np.array([-np.inf, -np.inf])) == 0
+
+
+# ------------------------------------------------------------------ acceptance
+
+def _accept_by_definition(t, drafts):
+    """1 + length of the longest common prefix of drafts[0..6] and t[0..6]."""
+    n = 0
+    for a, b in zip(t[:7], drafts):
+        if a != b:
+            break
+        n += 1
+    return n + 1
+
+
+def test_accept_brute_force_binary_vocab():
+    # every target pattern (8 tokens) x every draft pattern (7 tokens) over V = 2
+    tp = np.array(list(itertools.product([0, 1], repeat=8)), np.int32)
+    dp = np.array(list(itertools.product([0, 1], repeat=7)), np.int32)
+    T = np.repeat(tp, len(dp), axis=0)
+    D = np.tile(dp, (len(tp), 1))
+    anchor = np.full((T.shape[0], 1), 5, np.int32)
+    pending = np.concatenate([anchor, D], axis=1)
+    nc, cm = oracle.accept(T.reshape(-1), pending.reshape(-1))
+    eq = (T[:, :7] == D)
+    lcp = np.cumprod(eq, axis=1).sum(axis=1)
+    assert np.array_equal(nc, lcp + 1)
+    lo, hi = GOLD["accept_commit_range"]["min"], GOLD["accept_commit_range"]["max"]
+    assert nc.min() == lo and nc.max() == hi
+    j = np.arange(8)[None, :]
+    expect = np.where(j <= lcp[:, None], T, -1)
+    assert np.array_equal(cm, expect)
+
+
+def test_accept_random_vocab3_against_definition():
+    rng = np.random.default_rng(8)
+    n = 20000
+    T = rng.integers(0, 3, (n, 8)).astype(np.int32)
+    D = rng.integers(0, 3, (n, 7)).astype(np.int32)
+    pending = np.concatenate([rng.integers(0, 3, (n, 1)).astype(np.int32), D], axis=1)
+    nc, cm = oracle.accept(T.reshape(-1), pending.reshape(-1))
+    for i in range(0, n, 97):
+        assert nc[i] == _accept_by_definition(T[i], D[i])
+        assert list(cm[i][:nc[i]]) == list(T[i][:nc[i]])
+        assert all(v == -1 for v in cm[i][nc[i]:])
+
+
+# ------------------------------------------------------------------ byte counts
+
+def test_pass_bytes_match_page_table():
+    g = GOLD["geometry"]
+    G = oracle.geom(n_layers=g["layers"], hidden=g["hidden"], inter=g["intermediate"], vocab=g["vocab"],
+                    period=g["full_attention_period"], attn_kv=2 * g["kv_heads"] * g["head_dim"])
+    b = oracle.pass_bytes(G)
+    pb = GOLD["pass_bytes_gb"]
+    for i, key in enumerate(["mlp_codes", "mlp_scales", "gdn_fp8", "attn_fp8", "head"]):
+        assert round(b[i] / 1e9, 3) == pb[key], key
+    assert round(b[5] / 1e9, 3) == pb["weight_gemm_total"]
+    assert b[5] == 17_555_292_160
+    # 9 bytes per 16 NVFP4 weights
+    assert (b[0] + b[1]) * 16 == 9 * (64 * 3 * 17408 * 5120)
+    assert (b[4]) * 16 == 9 * (248320 * 5120)
+
+
+def test_arithmetic_intensity_matches_page():
+    ai = GOLD["arithmetic_intensity_flop_per_byte"]
+    for M, key in ((8, "M8"), (32, "M32")):
+        flop_per_byte = 2 * M / (GOLD["bytes_per_16_weights_nvfp4"]["value"] / 16)
+        assert round(flop_per_byte) == ai[key]
+
+
+# ------------------------------------------------------------------ the surrogate pass
+
+def _tiny_model(seed=11, L=4, H=64, I=96, V=200, gdn_in=80, gdn_z=48, aq=72, akv=16, az=40):
+    import synth
+    rng = np.random.default_rng(seed)
+    layers = []
+    for l in range(L):
+        attn = (l % 4) == 3
+        d = {}
+        n_in = aq if attn else gdn_in
+        kz = az if attn else gdn_z
+        d["in"] = synth.fp8_matrix(seed, l, synth.T_IN, n_in, H)
+        d["kv"] = synth.fp8_matrix(seed, l, synth.T_KV, akv, H) if attn else None
+        d["out"] = synth.fp8_matrix(seed, l, synth.T_OUT, H, kz)
+        d["gate_c"], d["gate_s"] = synth.nvfp4_matrix(seed, l, synth.T_GATE_C, synth.T_GATE_S, I, H)
+        d["up_c"], d["up_s"] = synth.nvfp4_matrix(seed, l, synth.T_UP_C, synth.T_UP_S, I, H)
+        d["down_c"], d["down_s"] = synth.nvfp4_matrix(seed, l, synth.T_DOWN_C, synth.T_DOWN_S, H, I)
+        d.update(s_in=float(rng.uniform(0.5, 1.5)), s_kv=1.0, s_out=float(rng.uniform(0.5, 1.5)),
+                 ts_gate=float(rng.uniform(0.5, 1.5)), ts_up=float(rng.uniform(0.5, 1.5)),
+                 ts_down=float(rng.uniform(0.5, 1.5)))
+        layers.append(d)
+    hc, hs = synth.nvfp4_matrix(seed, synth.HEAD_LAYER, synth.T_HEAD_C, synth.T_HEAD_S, V, H)
+    G = oracle.geom(n_layers=L, hidden=H, inter=I, vocab=V, period=4, gdn_in=gdn_in, gdn_z=gdn_z,
+                    attn_q=aq, attn_kv=akv, attn_z=az)
+    return G, layers, (hc, hs, 0.9)
+
+
+def test_verify_pass_matches_independent_torch_composition():
+    """Re-composes the surrogate pass with torch fp64 ops, numpy RNE and the independent decoders,
+    and compares every traced residual state and the final logits."""
+    import synth
+    G, layers, head = _tiny_model()
+    M = 16
+    x0 = synth.normal_bf16(3, synth.stream_id(0, synth.T_X0), (M, G.hidden))
+    pending = np.zeros(M, np.int32)
+    out = oracle.verify_pass(G, layers, head, x0, pending, want_trace=True, want_logits=True)
+
+    def fp8(codes, s):
+        return torch.from_numpy(e4m3_torch(codes) * s)
+
+    def rms(hv):
+        return torch.from_numpy(_round_bf16_numpy(torch.nn.functional.rms_norm(hv, (G.hidden,), eps=1e-6).numpy()))
+
+    h = torch.from_numpy(bf16_vals_torch(x0))
+    for l, d in enumerate(layers):
+        attn = (l % 4) == 3
+        kz = G.attn_z if attn else G.gdn_z
+        r = rms(h)
+        u = r @ fp8(d["in"], d["s_in"]).T
+        z = torch.from_numpy(_round_bf16_numpy(u[:, :kz].numpy()))
+        h = torch.from_numpy(_round_bf16_numpy((h + z @ fp8(d["out"], d["s_out"]).T).numpy()))
+        assert np.array_equal(h.numpy(), bf16_vals_torch(out["trace"][2 * l])), l
+        r = rms(h)
+        g = r @ torch.from_numpy(dequant_nvfp4_indep(d["gate_c"], d["gate_s"], d["ts_gate"])).T
+        u = r @ torch.from_numpy(dequant_nvfp4_indep(d["up_c"], d["up_s"], d["ts_up"])).T
+        a = torch.from_numpy(_round_bf16_numpy((torch.nn.functional.silu(g) * u).numpy()))
+        dn = a @ torch.from_numpy(dequant_nvfp4_indep(d["down_c"], d["down_s"], d["ts_down"])).T
+        h = torch.from_numpy(_round_bf16_numpy((h + dn).numpy()))
+        assert np.array_equal(h.numpy(), bf16_vals_torch(out["trace"][2 * l + 1])), l
+    r = rms(h)
+    logits = (r @ torch.from_numpy(dequant_nvfp4_indep(head[0], head[1], head[2])).T).numpy()
+    np.testing.assert_allclose(out["logits"], logits, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(out["argmax"], np.argmax(out["logits"], axis=1))
