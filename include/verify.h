@@ -1,0 +1,212 @@
+/*
+ * verify.h -- C ABI of libverify: the weight-streaming verify pass of speculative decoding on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * One verify pass streams every weight of a 64-layer hybrid target once for M = 8 * lanes rows
+ * (per lane: the committed anchor token and 7 draft tokens; 1..4 lanes).  Sources, by page title and
+ * section:
+ *   [LM-bus]     "lithos-metal: per-layer megakernels for Qwen3.8-27B on an M5 Max",
+ *                section "What one token costs the bus" (NVFP4 MLP + FP8 E4M3 mixer projections +
+ *                NVFP4 head = the bytes read on every pass; tensor-group table).
+ *   [LM-formats] same page, section "Formats, and what runs where" (NVFP4 = E2M1 codes, one E4M3
+ *                scale per 16 weights, an FP32 tensor scale that MULTIPLIES; scale codes top out at
+ *                448; weight-only arithmetic: BF16 activations, FP32 accumulation).
+ *   [LM-accept]  same page, section "The megakernel is per layer, not per step" (greedy acceptance:
+ *                accept the longest prefix of drafts equal to the target's tokens, commit the
+ *                target's token after it; 1..8 tokens per round).
+ *   [SP-geom]    "144 tok/s needs 502 GB/s" (Splash), sections "The engine hard-codes the model"
+ *                (geometry; nine bytes per sixteen weights) and "The decode step is one command
+ *                buffer" (8 verify rows per lane, up to 4 lanes, one submission per step).
+ *   [BS-ties]    "Beating Splash on an M5 Max", section "The bugs a second reviewer found" (GPU and
+ *                CPU must break argmax ties the same way) and "The kernels were not the gap"
+ *                (split-K for narrow projections).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are plain CUDA device addresses owned by the caller; the library never
+ *     allocates or frees device memory and never keeps a pointer beyond the call, except a
+ *     vp_model, which stores the weight pointers given to vp_model_create (the caller keeps them
+ *     alive and unchanged while the model is used).
+ *   - All work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *     stream); no call synchronises the host.  vp_verify_pass issues no host synchronisation and
+ *     no allocation, so it can be captured into a CUDA graph.
+ *   - Arguments are validated on the host before any launch; an invalid call returns an error and
+ *     enqueues nothing.  The library never aborts, throws or prints.
+ *   - Workspace: `ws` is caller-owned device memory of at least vp_*_workspace_bytes() bytes,
+ *     256-byte aligned.  Each call resets the workspace parts it needs; its first 4 bytes hold a
+ *     device status word (vp_status), written VP_OK by the call and VP_ERR_TIMEOUT if a bounded
+ *     device-side wait gave up.  Read it after the stream has synchronised (vp_read_status).
+ *     Calls that share a workspace must be ordered on one stream.
+ *   - Inputs are read-only; outputs are fully overwritten.
+ */
+#ifndef VERIFY_H_
+#define VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  VP_OK = 0,
+  VP_ERR_INVALID_ARG = 1, /* null pointer, negative size, unknown enum */
+  VP_ERR_SHAPE = 2,       /* unsupported M, N or K (see each call) */
+  VP_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  VP_ERR_WORKSPACE = 4,   /* ws_bytes smaller than the matching vp_*_workspace_bytes() */
+  VP_ERR_CUDA = 5,        /* a CUDA runtime call failed; vp_get_last_cuda_error() has the code */
+  VP_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up (reported in the status word) */
+  VP_ERR_UNSUPPORTED = 7  /* no sm_103a device, or an unsupported configuration */
+} vp_status;
+
+/* Human-readable name of a status code (static string). */
+const char* vp_status_string(int status);
+
+/* The CUDA error code of the most recent VP_ERR_CUDA on the calling thread (0 if none). */
+int vp_get_last_cuda_error(void);
+
+/* Copies the device status word at the start of `ws` to *status (synchronous: it waits for
+ * `stream`).  Returns VP_OK or VP_ERR_CUDA. */
+vp_status vp_read_status(const void* ws, int* status, void* stream);
+
+/* ------------------------------------------------------------------ packed weight layouts
+ *
+ * Canonical (logical) layouts, row-major [N][K] as in nn.Linear:
+ *   NVFP4: codes [N][K/2] bytes, element 2j of a row is the LOW nibble of byte j; each nibble is an
+ *          E2M1 code (bit 3 sign, bits 2..1 exponent, bit 0 mantissa); scales [N][K/16] E4M3 (FN)
+ *          bytes, scale[n][k/16] applies to weights k..k+15 of row n.  [LM-formats]
+ *   FP8:   [N][K] E4M3 (FN) bytes, one fp32 scale per tensor.  [LM-bus]
+ * The kernels read a packed copy whose size is exactly the canonical size (9 bytes per 16 NVFP4
+ * weights [SP-geom]; 1 byte per FP8 weight): rows are cut into 256-row slabs; within a slab,
+ * 64-wide K chunks of every 16-row block are stored contiguously so that one bulk copy moves a
+ * slab's K chunk and every thread's MMA operand is one aligned 16/32-byte read.
+ * Requirements: N % 16 == 0, K % 64 == 0.  */
+
+/* Packed size in bytes: N*K/16*9 (NVFP4) and N*K (FP8); 0 if N or K is unsupported. */
+size_t vp_packed_bytes_nvfp4(int N, int K);
+size_t vp_packed_bytes_fp8(int N, int K);
+
+/* Device-to-device repack from the canonical layout.  codes: [N][K/2], scales: [N][K/16],
+ * packed: vp_packed_bytes_nvfp4(N, K) bytes, all 16-byte aligned and not overlapping. */
+vp_status vp_pack_nvfp4(const void* codes, const void* scales, int N, int K, void* packed,
+                        size_t packed_bytes, void* stream);
+/* w: [N][K] E4M3 bytes -> packed (vp_packed_bytes_fp8(N, K) bytes). */
+vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_bytes, void* stream);
+
+/* ------------------------------------------------------------------ skinny linear layers
+ *
+ * y[m][n] = scale * sum_k x[m][k] * w[n][k], m < M, n < N, fp32 accumulation.  [LM-formats]
+ *   NVFP4: w[n][k] = e2m1(code[n][k]) * e4m3(block_scale[n][k/16]); scale = the fp32 tensor
+ *          scale (a multiplier).
+ *   FP8:   w[n][k] = e4m3(w8[n][k]); scale = the fp32 per-tensor scale.
+ * x: bf16 [M][K] row-major (device, 16-byte aligned); y: fp32 [M][N] row-major (device).
+ * Shapes: 1 <= M <= 32, N % 16 == 0, K % 64 == 0, N*K < 2^40.
+ * The K dimension is split across CTAs (split-K) with a fixed-order reduction, so results are
+ * bit-identical from run to run.  [BS-ties] (split-K).  */
+enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3 };
+
+/* Workspace bytes for one call of op (VP_OP_*) at the given shape; 0 if the shape is invalid. */
+size_t vp_workspace_bytes(int op, int M, int N, int K);
+
+vp_status vp_linear_nvfp4(const void* w_packed, float tensor_scale, const void* x, float* y, int M,
+                          int N, int K, void* ws, size_t ws_bytes, void* stream);
+vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float* y, int M, int N,
+                        int K, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ head + argmax + accept
+ *
+ * logits[m][v] = tensor_scale * sum_k x[m][k] * w[v][k] (NVFP4 head [V][K]), never materialised
+ * unless `logits` is non-NULL; argmax[m] = the lowest index v with the largest logit (NaN counts
+ * as -inf, -0 == +0) [BS-ties]; then per lane l (M = 8 * lanes, lanes 1..4) [LM-accept]:
+ *   acc = 0; while (acc < 7 && argmax[8l + acc] == pending[8l + acc + 1]) acc++;
+ *   n_commit[l] = acc + 1 (1..8);  committed[l][j] = argmax[8l + j] for j <= acc, -1 after.
+ * pending[8l] is the lane's anchor (already committed) token and is not compared.
+ * x: bf16 [M][K]; pending: int32 [M]; argmax: int32 [M]; n_commit: int32 [M/8];
+ * committed: int32 [M/8][8]; logits: optional fp32 [M][V] (debug).  V % 16 == 0, K % 64 == 0. */
+vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const void* x, int M,
+                                int V, int K, const int32_t* pending, int32_t* argmax,
+                                int32_t* n_commit, int32_t* committed, float* logits, void* ws,
+                                size_t ws_bytes, void* stream);
+
+/* The argmax + accept stage alone, over given fp32 logits [M][V] (any V >= 1; M = 8 * lanes).
+ * It runs the same device reduction and acceptance code as vp_head_argmax_accept. */
+vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending,
+                           int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ the verify pass
+ *
+ * The pass chains, for each layer l (attention when layer.kind == VP_LAYER_ATTN, else Gated
+ * DeltaNet; the Splash geometry has every fourth layer attention [SP-geom]):
+ *   r = RMSNorm(h)                                  (unit weight, eps; bf16 result)
+ *   GDN:  u = FP8(in, r) [M][n_in];  z = bf16(u[:, :k_out]);  h = bf16(h + FP8(out, z))
+ *   attn: q = FP8(q, r) [M][n_in], kv = FP8(kv, r) [M][n_kv] (streamed; unused by the stand-in
+ *         mixer);  z = bf16(q[:, :k_out]);  h = bf16(h + FP8(o, z))
+ *   r = RMSNorm(h);  a = bf16(silu(NVFP4(gate, r)) * NVFP4(up, r));  h = bf16(h + NVFP4(down, a))
+ * and then r = RMSNorm(h); head + argmax + accept as vp_head_argmax_accept.
+ * The mixer cores (Gated DeltaNet recurrence, attention over a KV cache) are outside the weight
+ * stream and are replaced by the slice z = u[:, :k_out]; every weight GEMM of the pass
+ * (17,555,292,160 bytes at the Qwen3.8-27B shapes [LM-bus]) is streamed.  */
+enum { VP_LAYER_GDN = 0, VP_LAYER_ATTN = 1 };
+
+typedef struct {
+  int kind;          /* VP_LAYER_GDN or VP_LAYER_ATTN */
+  const void* w_in;  /* FP8 packed [n_in][hidden]: GDN in-projection or attention q */
+  float s_in;
+  int n_in;
+  const void* w_kv;  /* FP8 packed [n_kv][hidden] (attention only; NULL and 0 on GDN layers) */
+  float s_kv;
+  int n_kv;
+  const void* w_out; /* FP8 packed [hidden][k_out]; k_out <= n_in */
+  float s_out;
+  int k_out;
+  const void* w_gate; /* NVFP4 packed [inter][hidden] */
+  float ts_gate;
+  const void* w_up;   /* NVFP4 packed [inter][hidden] */
+  float ts_up;
+  const void* w_down; /* NVFP4 packed [hidden][inter] */
+  float ts_down;
+} vp_layer_desc;
+
+typedef struct {
+  const void* w; /* NVFP4 packed [vocab][hidden] */
+  float ts;
+  int vocab;
+} vp_head_desc;
+
+typedef struct vp_model vp_model;
+
+/* Validates the descriptors (shapes as for the linear calls; hidden % 64 == 0, inter % 64 == 0,
+ * k_out % 64 == 0) and stores them (host memory, owned by the model). */
+vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_desc* layers,
+                          int n_layers, const vp_head_desc* head, vp_model** out);
+void vp_model_destroy(vp_model* model);
+
+/* Workspace bytes for vp_verify_pass at M rows (0 if invalid). */
+size_t vp_pass_workspace_bytes(const vp_model* model, int M);
+
+/* One verify pass.  x0: bf16 [M][hidden] (the rows' input hidden states, read-only); pending,
+ * argmax, n_commit, committed as for vp_head_argmax_accept; M = 8 * lanes, lanes 1..4.
+ * trace: optional bf16 [2 * n_layers][M][hidden], the residual stream h after every mixer block
+ * and every MLP block (debug; adds one device copy per block).  logits: optional fp32 [M][vocab].
+ * No host synchronisation, no allocation: capturable into a CUDA graph. */
+vp_status vp_verify_pass(const vp_model* model, const void* x0, int M, const int32_t* pending,
+                         int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace,
+                         float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16
+ * [M][hidden], updated in place); block 2l is the mixer block of layer l and block 2l + 1 its MLP
+ * block, computed exactly as inside vp_verify_pass (the same kernels), preceded by the 1/rms of h's
+ * rows.  trace: optional bf16 [block_end - block_begin][M][hidden], h after each block.  Lets a
+ * caller run part of the stream, or check one block against a reference from a known input. */
+vp_status vp_verify_blocks(const vp_model* model, void* h, int M, int block_begin, int block_end, void* trace,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Kernel launches that vp_verify_pass enqueues for a model (for launch accounting). */
+int vp_pass_launch_count(const vp_model* model);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_H_ */

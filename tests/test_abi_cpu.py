@@ -1,0 +1,119 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol, and rejects bad
+arguments before touching the GPU (so these run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def V():
+    from weight_streaming_gb300 import build
+    build()
+    from weight_streaming_gb300 import _lib
+    return _lib
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "verify.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(vp_[a-z0-9_]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(V):
+    decl = declared_functions()
+    assert len(decl) >= 18
+    lib = ctypes.CDLL(V.LIB_PATH)
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert sorted(V.EXPORTS) == decl
+
+
+def test_status_strings(V):
+    assert V.status_string(0) == "VP_OK"
+    assert V.status_string(6) == "VP_ERR_TIMEOUT"
+    assert V.status_string(99) == "VP_ERR_UNKNOWN"
+
+
+def test_packed_and_workspace_sizes(V):
+    assert V.vp_packed_bytes_nvfp4(17408, 5120) == 17408 * 5120 * 9 // 16
+    assert V.vp_packed_bytes_fp8(16384, 5120) == 16384 * 5120
+    assert V.vp_packed_bytes_nvfp4(17, 64) == 0 and V.vp_packed_bytes_nvfp4(16, 48) == 0
+    assert V.vp_workspace_bytes(V.VP_OP_NVFP4, 8, 5120, 17408) > 0
+    assert V.vp_workspace_bytes(V.VP_OP_NVFP4, 33, 5120, 17408) == 0
+    assert V.vp_workspace_bytes(V.VP_OP_NVFP4, 0, 5120, 17408) == 0
+    assert V.vp_workspace_bytes(V.VP_OP_HEAD, 12, 1024, 1024) == 0  # head needs M % 8 == 0
+    assert V.vp_workspace_bytes(V.VP_OP_ARGMAX, 8, 248320, 0) > 0
+    assert V.vp_workspace_bytes(7, 8, 64, 64) == 0
+
+
+FAKE = 0x10000000  # an aligned address that is never dereferenced: every call below fails validation first
+
+
+def test_linear_validation_without_gpu(V):
+    L = V.lib()
+    ws = V.vp_workspace_bytes(V.VP_OP_NVFP4, 8, 256, 1024)
+    ok = (FAKE, 1.0, FAKE, FAKE, 8, 256, 1024, FAKE, ws, None)
+    for fn in (L.vp_linear_nvfp4, L.vp_linear_fp8):
+        assert fn(None, *ok[1:]) == V.VP_ERR_INVALID_ARG
+        assert fn(*ok[:2], None, *ok[3:]) == V.VP_ERR_INVALID_ARG
+        assert fn(*ok[:7], None, *ok[8:]) == V.VP_ERR_INVALID_ARG
+        for M, N, K in ((0, 256, 1024), (33, 256, 1024), (8, 250, 1024), (8, 256, 1000), (8, 0, 1024)):
+            assert fn(FAKE, 1.0, FAKE, FAKE, M, N, K, FAKE, 1 << 30, None) == V.VP_ERR_SHAPE
+        assert fn(FAKE + 8, *ok[1:]) == V.VP_ERR_ALIGNMENT
+        assert fn(*ok[:2], FAKE + 2, *ok[3:]) == V.VP_ERR_ALIGNMENT
+        assert fn(*ok[:7], FAKE + 16, *ok[8:]) == V.VP_ERR_ALIGNMENT
+        assert fn(*ok[:8], ws - 1, None) == V.VP_ERR_WORKSPACE
+
+
+def test_head_and_argmax_validation_without_gpu(V):
+    L = V.lib()
+    ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)
+    args = [FAKE, 1.0, FAKE, 8, 1024, 512, FAKE, FAKE, FAKE, FAKE, None, FAKE, ws, None]
+    a = list(args)
+    a[3] = 12
+    assert L.vp_head_argmax_accept(*a) == V.VP_ERR_SHAPE
+    a = list(args)
+    a[6] = None
+    assert L.vp_head_argmax_accept(*a) == V.VP_ERR_INVALID_ARG
+    a = list(args)
+    a[12] = ws - 256
+    assert L.vp_head_argmax_accept(*a) == V.VP_ERR_WORKSPACE
+    assert L.vp_argmax_accept(FAKE, 9, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == V.VP_ERR_SHAPE
+    assert L.vp_argmax_accept(FAKE, 8, 0, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == V.VP_ERR_SHAPE
+    assert L.vp_argmax_accept(FAKE + 2, 8, 100, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20, None) == V.VP_ERR_ALIGNMENT
+
+
+def _layer(V, kind=0, n_in=512, k_out=256, n_kv=0):
+    d = V.vp_layer_desc()
+    d.kind = kind
+    d.w_in, d.s_in, d.n_in = FAKE, 1.0, n_in
+    d.w_kv, d.s_kv, d.n_kv = (FAKE, 1.0, n_kv) if kind == 1 else (None, 1.0, 0)
+    d.w_out, d.s_out, d.k_out = FAKE, 1.0, k_out
+    d.w_gate, d.ts_gate = FAKE, 1.0
+    d.w_up, d.ts_up = FAKE, 1.0
+    d.w_down, d.ts_down = FAKE, 1.0
+    return d
+
+
+def test_model_create_validation_without_gpu(V):
+    head = V.vp_head_desc(FAKE, 1.0, 2048)
+    m = V.vp_model(256, 512, 1e-6, [_layer(V), _layer(V, 1, 384, 256, 128)], head)
+    assert V.vp_pass_launch_count(m) == 2 + 4 * 2
+    assert V.vp_pass_workspace_bytes(m, 8) > 0
+    assert V.vp_pass_workspace_bytes(m, 12) == 0
+    m.close()
+    with pytest.raises(V.VerifyError):
+        V.vp_model(256, 512, 1e-6, [_layer(V, k_out=1024)], head)  # k_out > n_in
+    with pytest.raises(V.VerifyError):
+        V.vp_model(250, 512, 1e-6, [_layer(V)], head)
+    with pytest.raises(V.VerifyError):
+        V.vp_model(256, 512, 1e-6, [_layer(V, kind=1, n_kv=0)], head)
+    bad = _layer(V)
+    bad.w_up = FAKE + 4
+    with pytest.raises(V.VerifyError):
+        V.vp_model(256, 512, 1e-6, [bad], head)

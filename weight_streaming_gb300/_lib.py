@@ -1,0 +1,220 @@
+"""ctypes binding of libverify (include/verify.h): argument marshalling only.
+
+Every function keeps its C name.  Pointer arguments accept a torch tensor (its data_ptr), a plain
+integer address, or None (NULL).  Workspace sizes are taken from the tensor when not given.  The
+stream defaults to torch's current CUDA stream.  A non-VP_OK status raises VerifyError.  There is no
+fallback: if libverify.so has not been built, importing fails with an explicit message.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libverify.so")
+
+VP_OK, VP_ERR_INVALID_ARG, VP_ERR_SHAPE, VP_ERR_ALIGNMENT, VP_ERR_WORKSPACE, VP_ERR_CUDA, VP_ERR_TIMEOUT, \
+    VP_ERR_UNSUPPORTED = range(8)
+VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX = range(4)
+VP_LAYER_GDN, VP_LAYER_ATTN = 0, 1
+
+# Every symbol include/verify.h declares.
+EXPORTS = [
+    "vp_status_string", "vp_get_last_cuda_error", "vp_read_status", "vp_packed_bytes_nvfp4",
+    "vp_packed_bytes_fp8", "vp_pack_nvfp4", "vp_pack_fp8", "vp_workspace_bytes", "vp_linear_nvfp4",
+    "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
+    "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
+]
+
+
+class VerifyError(RuntimeError):
+    def __init__(self, name: str, status: int):
+        self.status = status
+        msg = f"{name} failed: {status_string(status)}"
+        if status == VP_ERR_CUDA:
+            msg += f" (cuda error {_L.vp_get_last_cuda_error()})"
+        super().__init__(msg)
+
+
+class vp_layer_desc(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int),
+                ("w_in", ctypes.c_void_p), ("s_in", ctypes.c_float), ("n_in", ctypes.c_int),
+                ("w_kv", ctypes.c_void_p), ("s_kv", ctypes.c_float), ("n_kv", ctypes.c_int),
+                ("w_out", ctypes.c_void_p), ("s_out", ctypes.c_float), ("k_out", ctypes.c_int),
+                ("w_gate", ctypes.c_void_p), ("ts_gate", ctypes.c_float),
+                ("w_up", ctypes.c_void_p), ("ts_up", ctypes.c_float),
+                ("w_down", ctypes.c_void_p), ("ts_down", ctypes.c_float)]
+
+
+class vp_head_desc(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("ts", ctypes.c_float), ("vocab", ctypes.c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libverify.so is not built ({LIB_PATH}); run weight_streaming_gb300.build.build() "
+                          "(nvcc, sm_103a) first -- there is no fallback implementation")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "vp_status_string": (ctypes.c_char_p, [I]),
+        "vp_get_last_cuda_error": (I, []),
+        "vp_read_status": (I, [P, ctypes.POINTER(I), P]),
+        "vp_packed_bytes_nvfp4": (S, [I, I]),
+        "vp_packed_bytes_fp8": (S, [I, I]),
+        "vp_pack_nvfp4": (I, [P, P, I, I, P, S, P]),
+        "vp_pack_fp8": (I, [P, I, I, P, S, P]),
+        "vp_workspace_bytes": (S, [I, I, I, I]),
+        "vp_linear_nvfp4": (I, [P, F, P, P, I, I, I, P, S, P]),
+        "vp_linear_fp8": (I, [P, F, P, P, I, I, I, P, S, P]),
+        "vp_head_argmax_accept": (I, [P, F, P, I, I, I, P, P, P, P, P, P, S, P]),
+        "vp_argmax_accept": (I, [P, I, I, P, P, P, P, P, S, P]),
+        "vp_model_create": (I, [I, I, F, ctypes.POINTER(vp_layer_desc), I, ctypes.POINTER(vp_head_desc),
+                                ctypes.POINTER(P)]),
+        "vp_model_destroy": (None, [P]),
+        "vp_pass_workspace_bytes": (S, [P, I]),
+        "vp_verify_pass": (I, [P, P, I, P, P, P, P, P, P, P, S, P]),
+        "vp_verify_blocks": (I, [P, P, I, I, I, P, P, S, P]),
+        "vp_pass_launch_count": (I, [P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+_L = _load()
+
+
+def lib():
+    return _L
+
+
+def status_string(s: int) -> str:
+    return _L.vp_status_string(int(s)).decode()
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(name, st):
+    if st != VP_OK:
+        raise VerifyError(name, st)
+
+
+def vp_packed_bytes_nvfp4(N: int, K: int) -> int:
+    return _L.vp_packed_bytes_nvfp4(N, K)
+
+
+def vp_packed_bytes_fp8(N: int, K: int) -> int:
+    return _L.vp_packed_bytes_fp8(N, K)
+
+
+def vp_workspace_bytes(op: int, M: int, N: int, K: int) -> int:
+    return _L.vp_workspace_bytes(op, M, N, K)
+
+
+def vp_pack_nvfp4(codes, scales, N: int, K: int, packed, stream=None, packed_bytes=None):
+    pb = packed_bytes if packed_bytes is not None else _nbytes(packed)
+    _check("vp_pack_nvfp4", _L.vp_pack_nvfp4(_ptr(codes), _ptr(scales), N, K, _ptr(packed), pb, _stream(stream)))
+
+
+def vp_pack_fp8(w, N: int, K: int, packed, stream=None, packed_bytes=None):
+    pb = packed_bytes if packed_bytes is not None else _nbytes(packed)
+    _check("vp_pack_fp8", _L.vp_pack_fp8(_ptr(w), N, K, _ptr(packed), pb, _stream(stream)))
+
+
+def vp_linear_nvfp4(w_packed, tensor_scale: float, x, y, M: int, N: int, K: int, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_linear_nvfp4", _L.vp_linear_nvfp4(_ptr(w_packed), tensor_scale, _ptr(x), _ptr(y), M, N, K, _ptr(ws),
+                                                 wb, _stream(stream)))
+
+
+def vp_linear_fp8(w_packed, scale: float, x, y, M: int, N: int, K: int, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_linear_fp8", _L.vp_linear_fp8(_ptr(w_packed), scale, _ptr(x), _ptr(y), M, N, K, _ptr(ws), wb,
+                                             _stream(stream)))
+
+
+def vp_head_argmax_accept(w_packed, tensor_scale: float, x, M: int, V: int, K: int, pending, argmax, n_commit,
+                          committed, logits, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_head_argmax_accept",
+           _L.vp_head_argmax_accept(_ptr(w_packed), tensor_scale, _ptr(x), M, V, K, _ptr(pending), _ptr(argmax),
+                                    _ptr(n_commit), _ptr(committed), _ptr(logits), _ptr(ws), wb, _stream(stream)))
+
+
+def vp_argmax_accept(logits, M: int, V: int, pending, argmax, n_commit, committed, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_argmax_accept", _L.vp_argmax_accept(_ptr(logits), M, V, _ptr(pending), _ptr(argmax), _ptr(n_commit),
+                                                   _ptr(committed), _ptr(ws), wb, _stream(stream)))
+
+
+def vp_read_status(ws, stream=None) -> int:
+    out = ctypes.c_int(-1)
+    _check("vp_read_status", _L.vp_read_status(_ptr(ws), ctypes.byref(out), _stream(stream)))
+    return out.value
+
+
+class vp_model:
+    """Owns a vp_model handle (vp_model_create / vp_model_destroy).  ``layers`` is a list of
+    vp_layer_desc; the device weights they point to must stay alive while the model is used."""
+
+    def __init__(self, hidden: int, inter: int, rms_eps: float, layers, head: vp_head_desc):
+        arr = (vp_layer_desc * len(layers))(*layers)
+        self._layers = arr
+        self._head = head
+        h = ctypes.c_void_p()
+        _check("vp_model_create", _L.vp_model_create(hidden, inter, rms_eps, arr, len(layers), ctypes.byref(head),
+                                                     ctypes.byref(h)))
+        self.handle = h
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _L.vp_model_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+
+def vp_pass_workspace_bytes(model: vp_model, M: int) -> int:
+    return _L.vp_pass_workspace_bytes(model.handle, M)
+
+
+def vp_pass_launch_count(model: vp_model) -> int:
+    return _L.vp_pass_launch_count(model.handle)
+
+
+def vp_verify_pass(model: vp_model, x0, M: int, pending, argmax, n_commit, committed, trace, logits, ws, stream=None,
+                   ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_verify_pass", _L.vp_verify_pass(model.handle, _ptr(x0), M, _ptr(pending), _ptr(argmax),
+                                               _ptr(n_commit), _ptr(committed), _ptr(trace), _ptr(logits), _ptr(ws),
+                                               wb, _stream(stream)))
+
+
+def vp_verify_blocks(model: vp_model, h, M: int, block_begin: int, block_end: int, trace, ws, stream=None,
+                     ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_verify_blocks", _L.vp_verify_blocks(model.handle, _ptr(h), M, block_begin, block_end, _ptr(trace),
+                                                   _ptr(ws), wb, _stream(stream)))

@@ -1,0 +1,139 @@
+"""Device-resident packed weights and the verify-pass model handle.
+
+Canonical weights (NVFP4 codes [N][K/2] + E4M3 scales [N][K/16], or FP8 E4M3 [N][K]) are packed on
+the device by vp_pack_nvfp4 / vp_pack_fp8 into the layout the kernels stream, then described to
+vp_model_create.  `SyntheticModel` fills the canonical tensors with the seeded synthetic recipe
+(synth) directly in HBM, one tensor at a time, so a full 17.6 GB pass fits next to a single
+canonical scratch tensor.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import _lib as V
+
+
+@dataclass
+class Geometry:
+    n_layers: int = 64
+    hidden: int = 5120
+    inter: int = 17408
+    vocab: int = 248320
+    period: int = 4          # every `period`-th layer (index % period == period - 1) is attention
+    gdn_in: int = 16384
+    gdn_z: int = 6144
+    attn_q: int = 12288
+    attn_kv: int = 2048
+    attn_z: int = 6144
+    eps: float = 1e-6
+
+    def is_attn(self, l: int) -> bool:
+        return (l % self.period) == self.period - 1
+
+    def pass_bytes(self) -> int:
+        H, I = self.hidden, self.inter
+        b = 0
+        for l in range(self.n_layers):
+            if self.is_attn(l):
+                b += self.attn_q * H + self.attn_kv * H + H * self.attn_z
+            else:
+                b += self.gdn_in * H + H * self.gdn_z
+            b += (2 * I * H + H * I) * 9 // 16
+        b += self.vocab * H * 9 // 16
+        return b
+
+
+def pack_nvfp4(codes: torch.Tensor, scales: torch.Tensor, stream=None) -> torch.Tensor:
+    N, K2 = codes.shape
+    K = 2 * K2
+    out = torch.empty(V.vp_packed_bytes_nvfp4(N, K), dtype=torch.uint8, device=codes.device)
+    V.vp_pack_nvfp4(codes, scales, N, K, out, stream)
+    return out
+
+
+def pack_fp8(w: torch.Tensor, stream=None) -> torch.Tensor:
+    N, K = w.shape
+    out = torch.empty(V.vp_packed_bytes_fp8(N, K), dtype=torch.uint8, device=w.device)
+    V.vp_pack_fp8(w, N, K, out, stream)
+    return out
+
+
+class SyntheticModel:
+    """A verify-pass model whose weights come from the seeded synthetic recipe:
+    NVFP4 code bytes uniform, E4M3 block scales 2^U(-6,0), FP8 weights E4M3(N(0,1)); tensor scales
+    are drawn uniformly in [0.5, 1.5] (``unit_scales=True`` sets them all to 1)."""
+
+    def __init__(self, geom: Geometry, seed: int = 0, device="cuda", unit_scales: bool = True):
+        import numpy as np
+
+        import synth
+        self.geom, self.seed = geom, seed
+        H, I = geom.hidden, geom.inter
+        rng = np.random.default_rng(seed + 12345)
+        self.scales = []
+        self.packed = []
+        layers = []
+
+        def sc():
+            return 1.0 if unit_scales else float(rng.uniform(0.5, 1.5))
+
+        def fp8(l, t, N, K):
+            w = torch.empty((N, K), dtype=torch.uint8, device=device)
+            synth.gpu_fp8_normal_codes(w, seed, synth.stream_id(l, t))
+            p = pack_fp8(w)
+            del w
+            self.packed.append(p)
+            return p
+
+        def nvfp4(l, tc, ts, N, K):
+            c = torch.empty((N, K // 2), dtype=torch.uint8, device=device)
+            s = torch.empty((N, K // 16), dtype=torch.uint8, device=device)
+            synth.gpu_uniform_bytes(c, seed, synth.stream_id(l, tc))
+            synth.gpu_scale_codes(s, seed, synth.stream_id(l, ts))
+            p = pack_nvfp4(c, s)
+            del c, s
+            self.packed.append(p)
+            return p
+
+        for l in range(geom.n_layers):
+            attn = geom.is_attn(l)
+            d = V.vp_layer_desc()
+            d.kind = V.VP_LAYER_ATTN if attn else V.VP_LAYER_GDN
+            n_in = geom.attn_q if attn else geom.gdn_in
+            kz = geom.attn_z if attn else geom.gdn_z
+            d.w_in = fp8(l, synth.T_IN, n_in, H).data_ptr()
+            d.s_in, d.n_in = sc(), n_in
+            if attn:
+                d.w_kv = fp8(l, synth.T_KV, geom.attn_kv, H).data_ptr()
+                d.s_kv, d.n_kv = sc(), geom.attn_kv
+            else:
+                d.w_kv, d.s_kv, d.n_kv = None, 1.0, 0
+            d.w_out = fp8(l, synth.T_OUT, H, kz).data_ptr()
+            d.s_out, d.k_out = sc(), kz
+            d.w_gate = nvfp4(l, synth.T_GATE_C, synth.T_GATE_S, I, H).data_ptr()
+            d.ts_gate = sc()
+            d.w_up = nvfp4(l, synth.T_UP_C, synth.T_UP_S, I, H).data_ptr()
+            d.ts_up = sc()
+            d.w_down = nvfp4(l, synth.T_DOWN_C, synth.T_DOWN_S, H, I).data_ptr()
+            d.ts_down = sc()
+            self.scales.append(dict(s_in=d.s_in, s_kv=d.s_kv, s_out=d.s_out, ts_gate=d.ts_gate, ts_up=d.ts_up,
+                                    ts_down=d.ts_down))
+            layers.append(d)
+        hp = nvfp4(synth.HEAD_LAYER, synth.T_HEAD_C, synth.T_HEAD_S, geom.vocab, H)
+        self.head_ts = sc()
+        head = V.vp_head_desc(hp.data_ptr(), self.head_ts, geom.vocab)
+        torch.cuda.synchronize()
+        self.model = V.vp_model(H, I, geom.eps, layers, head)
+
+    def workspace(self, M: int) -> torch.Tensor:
+        n = V.vp_pass_workspace_bytes(self.model, M)
+        return torch.empty(n, dtype=torch.uint8, device="cuda")
+
+    def launch_count(self) -> int:
+        return V.vp_pass_launch_count(self.model)
+
+    def run(self, x0, pending, argmax, n_commit, committed, ws, trace=None, logits=None, stream=None):
+        M = x0.shape[0]
+        V.vp_verify_pass(self.model, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, stream)
