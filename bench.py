@@ -1,0 +1,402 @@
+"""Benchmark of the verify-pass weight stream on GB300.
+
+One step = one full verify pass (64 layers + vocabulary head with argmax and greedy acceptance,
+17,555,292,160 weight bytes at the Qwen3.8-27B shapes) over M = 8 rows (one lane), captured once into
+a CUDA graph and replayed; weights and inputs are resident in HBM and far larger than L2, so every
+replay streams the weights from DRAM.  The JSON line reports verify-pass GB/s (weight bytes / pass
+time), ms per pass, the same at M = 16/24/32, the dominant kernel's roofline, an end-to-end figure
+through the C ABI with host buffers, and the fp64 oracle on the host cores as the CPU baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU: the pass does not shard in this build (replicas only): under torchrun every rank runs its
+own replica on its own GPU; value = total bytes streamed by all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify-pass HBM GB/s (% of GB300 roofline) and ms/pass at M=8 and M=32"
+UNIT = "GB/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=64)
+    return ap.parse_args()
+
+
+def aggregate(bytes_per_rank: float, times_s: list) -> tuple:
+    """Whole-job GB/s over ranks that each stream `bytes_per_rank`: total bytes / slowest time."""
+    t = max(times_s)
+    return bytes_per_rank * len(times_s) / t / 1e9, t
+
+
+def dist_setup(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    world = int(os.environ["WORLD_SIZE"])
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+    dist.init_process_group("nccl")
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return [x]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    out = [torch.zeros_like(t) for _ in range(world)]
+    dist.all_gather(out, t)
+    return [float(o.item()) for o in out]
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.Q}", "--format=csv,noheader",
+                                       "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.p:
+            time.sleep(0.2)
+            self.p.terminate()
+            try:
+                self.out, _ = self.p.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+                self.out, _ = self.p.communicate()
+
+    def summary(self):
+        rows = []
+        for r in csv.reader(io.StringIO(self.out or "")):
+            if len(r) < 9:
+                continue
+            try:
+                rows.append({"sm": float(r[1].split()[0]), "max": float(r[2].split()[0]),
+                             "hw": r[5].strip(), "hwt": r[6].strip(), "swt": r[7].strip(), "pcap": r[8].strip()})
+            except (ValueError, IndexError):
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        import statistics
+        reasons = set()
+        for r in rows:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ CPU baseline (the oracle)
+
+def oracle_sample(geom, seed: int, M: int, target_s: float = 12.0):
+    """Times the fp64 oracle (as it stands, all host cores) on whole MLP blocks of layers 0, 1, ...
+    (RMSNorm, gate, up, SiLU*up, down) at M rows until about target_s seconds of work, and returns
+    (weight bytes processed, seconds, threads, description)."""
+    import numpy as np
+
+    import oracle
+    import synth
+    H, I = geom.hidden, geom.inter
+    x = synth.normal_bf16(seed, synth.stream_id(0, synth.T_X0), (M, H))
+    nbytes, secs, l = 0, 0.0, 0
+    threads = oracle.default_threads()
+    while (l == 0 or secs < target_s) and l < geom.n_layers:
+        gc, gs = synth.nvfp4_matrix(seed, l, synth.T_GATE_C, synth.T_GATE_S, I, H)
+        uc, us = synth.nvfp4_matrix(seed, l, synth.T_UP_C, synth.T_UP_S, I, H)
+        dc, ds = synth.nvfp4_matrix(seed, l, synth.T_DOWN_C, synth.T_DOWN_S, H, I)
+        t0 = time.perf_counter()
+        r = oracle.rmsnorm(x, geom.eps)
+        g = oracle.linear(oracle.NVFP4, r, gc, gs, 1.0, I, with_abs=False, nthreads=threads)
+        u = oracle.linear(oracle.NVFP4, r, uc, us, 1.0, I, with_abs=False, nthreads=threads)
+        a = oracle.bf16_round(oracle.silu_mul(g, u))
+        y = oracle.linear(oracle.NVFP4, a, dc, ds, 1.0, H, with_abs=False, nthreads=threads)
+        x = oracle.bf16_round(oracle.bf16_value(x) + y)
+        secs += time.perf_counter() - t0
+        nbytes += 3 * I * H * 9 // 16
+        l += 1
+    desc = f"fp64 oracle, MLP blocks of layers 0..{l - 1} ({l} x 150.4 MB NVFP4) at M={M}, all host cores"
+    return nbytes, secs, threads, desc
+
+
+def run_reference(args):
+    """The oracle arm: the same metric (weight GB/s of the verify pass) for the fp64 CPU oracle."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from weight_streaming_gb300.model import Geometry
+    geom = Geometry(n_layers=args.layers)
+    for _ in range(args.warmup):
+        oracle_sample(geom, 0, 8, target_s=0.0)
+    tot_b, tot_s, thr, desc = 0, 0.0, 1, ""
+    for _ in range(args.steps):
+        b, s, thr, desc = oracle_sample(geom, 0, 8, target_s=0.0)
+        tot_b += b
+        tot_s += s
+    v = tot_b / tot_s / 1e9
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "verify-pass weight stream, M=8 (bounded sample: one MLP block per step)"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import numpy as np
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    from weight_streaming_gb300.model import Geometry, SyntheticModel
+
+    rank, world = dist_setup(args.gpus)
+    dev = torch.cuda.current_device()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+    geom = Geometry(n_layers=args.layers)
+    pass_bytes = geom.pass_bytes()
+    sm = SyntheticModel(geom, seed=0)
+    H = geom.hidden
+
+    def make_io(M, seed):
+        x0 = torch.from_numpy(synth.normal_bf16(seed, synth.stream_id(0, synth.T_X0), (M, H)).view(np.int16))
+        x0 = x0.cuda().view(torch.bfloat16)
+        t = synth.uniform_ints(seed, synth.stream_id(0, synth.T_PENDING) + 7, 0, M, geom.vocab)
+        pending, _ = synth.planted_pending(seed, t, geom.vocab)
+        pend = torch.from_numpy(pending).cuda()
+        am = torch.empty(M, dtype=torch.int32, device="cuda")
+        nc = torch.empty(M // 8, dtype=torch.int32, device="cuda")
+        cm = torch.empty((M // 8, 8), dtype=torch.int32, device="cuda")
+        ws = sm.workspace(M)
+        return x0, pend, am, nc, cm, ws
+
+    def graph_for(M, seed):
+        io_ = make_io(M, seed)
+        x0, pend, am, nc, cm, ws = io_
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                sm.run(x0, pend, am, nc, cm, ws, stream=s)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                sm.run(x0, pend, am, nc, cm, ws, stream=s)
+        torch.cuda.synchronize()
+        assert V.vp_read_status(ws) == V.VP_OK
+        return g, s, io_
+
+    def time_graph(g, s, steps, warmup):
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                g.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(steps):
+                g.replay()
+        e1.record(s)
+        torch.cuda.synchronize()
+        barrier(world)
+        return e0.elapsed_time(e1) / 1e3
+
+    # ---- headline: M = 8
+    g8, s8, io8 = graph_for(8, 0)
+    with Clocks(dev) as clk:
+        t8 = time_graph(g8, s8, args.steps, args.warmup)
+    times = max_over_ranks(t8, world)
+    value, tmax = aggregate(pass_bytes * args.steps, times)
+    ms8 = 1e3 * tmax / args.steps
+
+    # ---- the other widths (1 graph each)
+    also = {}
+    for M in (16, 24, 32):
+        g, s, _ = graph_for(M, M)
+        t = time_graph(g, s, max(3, args.steps // 2), 3)
+        steps_m = max(3, args.steps // 2)
+        gbs = pass_bytes * steps_m / t / 1e9
+        also[f"M{M}"] = {"gbps": gbs, "ms_per_pass": 1e3 * t / steps_m,
+                         "implied_tok_s": (M // 8) * 4.8 / (t / steps_m)}
+        del g
+    also["M8"] = {"gbps": value / world, "ms_per_pass": ms8, "implied_tok_s": 4.8 / (ms8 / 1e3)}
+
+    # ---- dominant kernel: the NVFP4 GEMM (MLP gate, 17408 x 5120, 50.1 MB per launch) alone, launched
+    # back to back through the C ABI while rotating over the 64 layers' gate matrices, so every launch
+    # streams its weights from DRAM; CUDA events on the launching stream.
+    I = geom.inter
+    gate_ptrs = [d.w_gate for d in sm.model._layers]
+    Mk = 8
+    xk = io8[0]
+    yk = torch.empty((Mk, I), dtype=torch.float32, device="cuda")
+    wsk = torch.zeros(V.vp_workspace_bytes(V.VP_OP_NVFP4, Mk, I, H), dtype=torch.uint8, device="cuda")
+    sk = torch.cuda.Stream()
+    reps = 3
+    with torch.cuda.stream(sk):
+        for p in gate_ptrs[:8]:
+            V.vp_linear_nvfp4(p, 1.0, xk, yk, Mk, I, H, wsk, stream=sk)
+        sk.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(sk)
+        for _ in range(reps):
+            for p in gate_ptrs:
+                V.vp_linear_nvfp4(p, 1.0, xk, yk, Mk, I, H, wsk, stream=sk)
+        e1.record(sk)
+    torch.cuda.synchronize()
+    n_launch = reps * len(gate_ptrs)
+    t_kern = e0.elapsed_time(e1) / 1e3 / n_launch
+    gate_bytes = I * H * 9 // 16
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = gate_bytes / t_kern / 1e9
+
+    # ---- copy roofline re-measured in this run (torch copy, read + write bytes)
+    a = torch.empty(1 << 30, dtype=torch.bfloat16, device="cuda")
+    b = torch.empty_like(a)
+    b.copy_(a)
+    best = 1e9
+    for _ in range(5):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record()
+        b.copy_(a)
+        c1.record()
+        torch.cuda.synchronize()
+        best = min(best, c0.elapsed_time(c1) / 1e3)
+    copy_gbs = 2 * a.numel() * 2 / best / 1e9
+    del a, b
+    nominal = None
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={dev}", "--query-gpu=clocks.max.memory", "--format=csv,noheader"],
+                             capture_output=True, text=True, timeout=10).stdout
+        mem_mhz = float(out.split()[0])
+        nominal = 2 * mem_mhz * 1e6 * 7936 / 8 / 1e9  # double data rate x bus width (bits)
+    except Exception:
+        pass
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    x0d, pend, am, nc, cm, ws = io8
+    x0h = x0d.cpu().pin_memory()
+    pendh = pend.cpu().pin_memory()
+    amh = torch.empty_like(am, device="cpu").pin_memory()
+    nch = torch.empty_like(nc, device="cpu").pin_memory()
+    cmh = torch.empty_like(cm, device="cpu").pin_memory()
+    se = torch.cuda.Stream()
+    with torch.cuda.stream(se):
+        for it in range(args.warmup + args.steps):
+            if it == args.warmup:
+                se.synchronize()
+                ee0 = torch.cuda.Event(enable_timing=True)
+                ee0.record(se)
+                w0 = time.perf_counter()
+            x0d.copy_(x0h, non_blocking=True)
+            pend.copy_(pendh, non_blocking=True)
+            sm.run(x0d, pend, am, nc, cm, ws, stream=se)
+            amh.copy_(am, non_blocking=True)
+            nch.copy_(nc, non_blocking=True)
+            cmh.copy_(cm, non_blocking=True)
+        ee1 = torch.cuda.Event(enable_timing=True)
+        ee1.record(se)
+        se.synchronize()
+        wall = time.perf_counter() - w0
+    t_e2e = max(ee0.elapsed_time(ee1) / 1e3, 0.0)
+    t_e2e = max(t_e2e, wall)
+    e2e_times = max_over_ranks(t_e2e, world)
+    e2e_val, _ = aggregate(pass_bytes * args.steps, e2e_times)
+    h2d = x0h.numel() * 2 + pendh.numel() * 4
+    d2h = amh.numel() * 4 + nch.numel() * 4 + cmh.numel() * 4
+    assert int(nch.min()) >= 1 and int(nch.max()) <= 8
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world >= 1:
+        b, s, thr, desc = oracle_sample(geom, 0, 8)
+        cpu = {"value": b / s / 1e9, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc}
+    frac = achieved / peak
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms8, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 mma (nvfp4/fp8 weights exact in f16), f32 accumulate", "data": "synthetic",
+        "config": {"workload": f"full verify pass: {geom.n_layers} layers (48 GDN + 16 attention FP8 projections, "
+                               "NVFP4 MLP) + NVFP4 head + argmax + greedy accept, Qwen3.8-27B shapes, M=8 (1 lane)",
+                   "bytes_per_pass": pass_bytes, "M": 8, "graph": "one CUDA graph per pass",
+                   "l2": "no flush needed: 17.6 GB of weights per pass >> 129 MB L2",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": frac,
+                     "traffic": None, "kernel": "gemm_kernel<NVFP4,MT=1> (MLP gate 17408x5120, 50.1 MB/launch)",
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sm.launch_count() * args.steps,
+        "clocks": clk.summary(),
+        "also": {**also, "pass_pct_of_measured_copy": 100 * (value / world) / peak,
+                 "copy_gbs_this_run": copy_gbs, "pass_pct_of_this_run_copy": 100 * (value / world) / copy_gbs,
+                 "nominal_hbm_gbs": nominal, "dominant_kernel_ms": t_kern * 1e3},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

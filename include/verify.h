@@ -32,10 +32,13 @@
  *   - Arguments are validated on the host before any launch; an invalid call returns an error and
  *     enqueues nothing.  The library never aborts, throws or prints.
  *   - Workspace: `ws` is caller-owned device memory of at least vp_*_workspace_bytes() bytes,
- *     256-byte aligned.  Each call resets the workspace parts it needs; its first 4 bytes hold a
- *     device status word (vp_status), written VP_OK by the call and VP_ERR_TIMEOUT if a bounded
- *     device-side wait gave up.  Read it after the stream has synchronised (vp_read_status).
- *     Calls that share a workspace must be ordered on one stream.
+ *     256-byte aligned, zero-filled once before its first use (vp_workspace_init).  The kernels
+ *     leave the counters they use back at zero, so a call that completes normally leaves the
+ *     workspace ready for the next call without any per-call reset (each call is a pure sequence
+ *     of kernel launches).  The first 4 bytes hold a sticky device status word: 0, or
+ *     VP_ERR_TIMEOUT once a bounded device-side wait gave up (then re-initialise the workspace).
+ *     Read it after the stream has synchronised (vp_read_status).  Calls that share a workspace
+ *     must be ordered on one stream.
  *   - Inputs are read-only; outputs are fully overwritten.
  */
 #ifndef VERIFY_H_
@@ -64,6 +67,10 @@ const char* vp_status_string(int status);
 
 /* The CUDA error code of the most recent VP_ERR_CUDA on the calling thread (0 if none). */
 int vp_get_last_cuda_error(void);
+
+/* Zero-fills ws_bytes of the workspace on `stream` (required once before first use, and after
+ * an error). */
+vp_status vp_workspace_init(void* ws, size_t ws_bytes, void* stream);
 
 /* Copies the device status word at the start of `ws` to *status (synchronous: it waits for
  * `stream`).  Returns VP_OK or VP_ERR_CUDA. */

@@ -31,7 +31,7 @@ def host_bf16_bits(t) -> np.ndarray:
 
 def workspace(nbytes: int):
     import torch
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device="cuda")
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device="cuda")
 
 
 def assert_linear_close(y_gpu: np.ndarray, y_ref: np.ndarray, a_ref: np.ndarray, what: str = ""):

@@ -20,7 +20,7 @@ VP_LAYER_GDN, VP_LAYER_ATTN = 0, 1
 
 # Every symbol include/verify.h declares.
 EXPORTS = [
-    "vp_status_string", "vp_get_last_cuda_error", "vp_read_status", "vp_packed_bytes_nvfp4",
+    "vp_status_string", "vp_get_last_cuda_error", "vp_workspace_init", "vp_read_status", "vp_packed_bytes_nvfp4",
     "vp_packed_bytes_fp8", "vp_pack_nvfp4", "vp_pack_fp8", "vp_workspace_bytes", "vp_linear_nvfp4",
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
@@ -59,6 +59,7 @@ def _load():
     sig = {
         "vp_status_string": (ctypes.c_char_p, [I]),
         "vp_get_last_cuda_error": (I, []),
+        "vp_workspace_init": (I, [P, S, P]),
         "vp_read_status": (I, [P, ctypes.POINTER(I), P]),
         "vp_packed_bytes_nvfp4": (S, [I, I]),
         "vp_packed_bytes_fp8": (S, [I, I]),
@@ -167,6 +168,11 @@ def vp_argmax_accept(logits, M: int, V: int, pending, argmax, n_commit, committe
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check("vp_argmax_accept", _L.vp_argmax_accept(_ptr(logits), M, V, _ptr(pending), _ptr(argmax), _ptr(n_commit),
                                                    _ptr(committed), _ptr(ws), wb, _stream(stream)))
+
+
+def vp_workspace_init(ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_workspace_init", _L.vp_workspace_init(_ptr(ws), wb, _stream(stream)))
 
 
 def vp_read_status(ws, stream=None) -> int:

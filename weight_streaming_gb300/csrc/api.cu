@@ -271,6 +271,13 @@ const char* vp_status_string(int s) {
 
 int vp_get_last_cuda_error(void) { return g_last_cuda_error; }
 
+vp_status vp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return VP_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return VP_ERR_ALIGNMENT;
+  cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream);
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
 vp_status vp_read_status(const void* ws, int* status, void* stream) {
   if (!ws || !status) return VP_ERR_INVALID_ARG;
   cudaError_t e = cudaMemcpyAsync(status, ws, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
@@ -346,10 +353,7 @@ static vp_status linear_common(int fmt, const void* w, float scale, const void* 
   p.epi = kEpiF32;
   p.y = y;
   p.y_ld = N;
-  const GemmWs g = carve_gemm_ws(ws, p.n_groups, (M + 7) / 8);
-  fill_ws(p, g);
-  cudaError_t e = cudaMemsetAsync(ws, 0, g.L.group_aux, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e);
+  fill_ws(p, carve_gemm_ws(ws, p.n_groups, (M + 7) / 8));
   return launch(fmt, p, sms, (cudaStream_t)stream, false);
 }
 
@@ -385,10 +389,7 @@ vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const 
   p.committed = committed;
   p.logits = logits;
   p.logits_ld = V;
-  const GemmWs g = carve_gemm_ws(ws, p.n_groups, (M + 7) / 8);
-  fill_ws(p, g);
-  cudaError_t e = cudaMemsetAsync(ws, 0, g.L.group_aux, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e);
+  fill_ws(p, carve_gemm_ws(ws, p.n_groups, (M + 7) / 8));
   return launch(kFmtNvfp4, p, sms, (cudaStream_t)stream, false);
 }
 
@@ -404,13 +405,11 @@ vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pen
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
   const int n_chunks = ceil_div(V, kArgmaxChunk);
-  cudaError_t e = cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e);
   uint8_t* b = (uint8_t*)ws;
   argmax_accept_kernel<<<dim3(n_chunks, M), 256, 0, (cudaStream_t)stream>>>(
       logits, M, V, kArgmaxChunk, n_chunks, pending, argmax, n_commit, committed, (float*)(b + 256),
       (unsigned*)(b + 64));
-  e = cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
@@ -624,8 +623,7 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
   cudaStream_t s = (cudaStream_t)stream;
   const int H = md->hidden;
   const PassWs w = carve_pass_ws(md, M, ws);
-  cudaError_t e = cudaMemsetAsync(ws, 0, w.counters_bytes, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  cudaError_t e;
   pass_prep_kernel<<<M, 256, 0, s>>>((const uint16_t*)x0, w.h, H, md->eps, w.inv_rms);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
   if ((st = enqueue_blocks(md, w, w.h, M, 0, 2 * (int)md->layers.size(), trace, sms, s)) != VP_OK) return st;
@@ -657,8 +655,7 @@ vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, 
   if ((st = device_sms(&sms)) != VP_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   const PassWs w = carve_pass_ws(md, M, ws);
-  cudaError_t e = cudaMemsetAsync(ws, 0, w.counters_bytes, s);
-  if (e != cudaSuccess) return cuda_fail(e);
+  cudaError_t e;
   // 1/rms of the incoming rows (the copy onto itself is a no-op)
   pass_prep_kernel<<<M, 256, 0, s>>>((const uint16_t*)h, (uint16_t*)h, md->hidden, md->eps, w.inv_rms);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);

@@ -65,6 +65,7 @@ struct SmemMisc {
   uint64_t full[16];
   uint64_t empty[16];
   int xexp[kMaxM];
+  int xmax[kMaxM];
   float red_v[kConsumerWarps][kMaxM];
   int red_i[kConsumerWarps][kMaxM];
   int tok[kMaxM];
@@ -143,60 +144,76 @@ __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(_
 // slot (q - origin).  Each row m is scaled by 2^-xexp[m], chosen from the row's largest magnitude
 // over the staged quads so that it lies in [2^14, 2^15): every bf16 value then converts to f16
 // exactly (f16 has more significand bits) unless it is over 2^31 times smaller than that maximum.
+// Pass 1 reads X once (16-byte loads, all consumer threads), applies the optional row multiplier
+// (bf16-rounded, as RMSNorm's output), stores the bf16 pairs straight into their fragment slots and
+// takes the row maxima; pass 2 rescales every fragment word in place to f16.
 template <int MT>
 __device__ void stage_x(const GemmParams& p, uint32_t* xbuf, SmemMisc& sm, int origin, int qa0, int qb0,
-                        int qa1, int qb1, int warp, int lane) {
-  for (int m = warp; m < MT * 8; m += kConsumerWarps) {
-    const int nt = m >> 3, gq = m & 7;
-    const bool live = m < p.M;
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(p.x + (size_t)(live ? m : 0) * p.x_ld);
-    const float rs = (live && p.x_rowscale) ? p.x_rowscale[m] : 1.0f;
-    const bool use_rs = p.x_rowscale != nullptr;
-    float mx = 0.0f;
-    if (live) {
-      for (int iv = 0; iv < 2; ++iv) {
-        const int qa = iv ? qa1 : qa0, qb = iv ? qb1 : qb0;
+                        int qa1, int qb1, int ctid) {
+  if (ctid < MT * 8) sm.xmax[ctid] = 0;
+  named_bar_sync(1, kConsumerThreads);
+  const int n0 = (qb0 - qa0) * 8, n1 = (qb1 - qa1) * 8;  // 8-element chunks per row
+  const int per_row = n0 + n1;
+  const int total = MT * 8 * per_row;
+  const bool use_rs = p.x_rowscale != nullptr;
 #pragma unroll 4
-        for (int pi = qa * 32 + lane; pi < qb * 32; pi += 32) {
-          const uint32_t w = __ldcg(xr + pi);
-          float v0 = bf16_bits_to_float(w & 0xFFFFu), v1 = bf16_bits_to_float(w >> 16);
-          if (use_rs) {
-            v0 = round_bf16(v0 * rs);
-            v1 = round_bf16(v1 * rs);
-          }
-          mx = fmaxf(mx, fmaxf(fabsf(v0), fabsf(v1)));
-        }
-      }
+  for (int c = ctid; c < total; c += kConsumerThreads) {
+    const int m = c / per_row, jj = c - m * per_row;
+    const int kc = jj < n0 ? qa0 * 8 + jj : qa1 * 8 + (jj - n0);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (m < p.M) {
+      const uint4 raw = ldcg128(p.x + (size_t)m * p.x_ld + (size_t)kc * 8);
+      w[0] = raw.x;
+      w[1] = raw.y;
+      w[2] = raw.z;
+      w[3] = raw.w;
+      float mx = 0.0f;
+      const float rs = use_rs ? p.x_rowscale[m] : 1.0f;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      for (int i = 0; i < 4; ++i) {
+        float v0 = bf16_bits_to_float(w[i] & 0xFFFFu), v1 = bf16_bits_to_float(w[i] >> 16);
+        if (use_rs) {
+          v0 = round_bf16(v0 * rs);
+          v1 = round_bf16(v1 * rs);
+          w[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v0)) |
+                 ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v1)) << 16);
+        }
+        mx = fmaxf(mx, fmaxf(fabsf(v0), fabsf(v1)));
+      }
+      atomicMax(&sm.xmax[m], __float_as_int(mx));  // non-negative floats order like their bits
     }
+    const int k0 = kc * 8, q = k0 >> 6, kl = k0 & 63;
+    const int slot = q - origin, j16 = kl >> 4, reg = (kl & 15) >> 3;
+    const int nt = m >> 3, g = m & 7;
+    uint32_t* dst = xbuf + (((slot * 4 + j16) * MT + nt) * 32 + g * 4) * 2 + reg;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[2 * i] = w[i];
+  }
+  named_bar_sync(1, kConsumerThreads);
+  if (ctid < MT * 8) {
+    const float mx = __int_as_float(sm.xmax[ctid]);
     int e = 0;
     if (mx > 0.0f) {
       const int ef = (__float_as_uint(mx) >> 23) & 0xFF;
-      const int fl = ef ? ef - 127 : -127;  // floor(log2(mx)) (subnormal maxima: -127)
-      e = fl - 14;
+      e = (ef ? ef - 127 : -127) - 14;  // floor(log2(mx)) - 14 (subnormal maxima: -127 - 14)
     }
-    if (lane == 0) sm.xexp[m] = e;
-    for (int iv = 0; iv < 2; ++iv) {
-      const int qa = iv ? qa1 : qa0, qb = iv ? qb1 : qb0;
+    sm.xexp[ctid] = e;
+  }
+  named_bar_sync(1, kConsumerThreads);
+  for (int iv = 0; iv < 2; ++iv) {
+    const int qa = iv ? qa1 : qa0, qb = iv ? qb1 : qb0;
+    if (qb <= qa) continue;
+    uint32_t* base = xbuf + (size_t)(qa - origin) * (256 * MT);
+    const int nwords = (qb - qa) * 256 * MT;
 #pragma unroll 4
-      for (int pi = qa * 32 + lane; pi < qb * 32; pi += 32) {
-        uint32_t h2 = 0;
-        if (live) {
-          const uint32_t w = __ldcg(xr + pi);
-          float v0 = bf16_bits_to_float(w & 0xFFFFu), v1 = bf16_bits_to_float(w >> 16);
-          if (use_rs) {
-            v0 = round_bf16(v0 * rs);
-            v1 = round_bf16(v1 * rs);
-          }
-          const __half2 h = __floats2half2_rn(mul_pow2(v0, -e), mul_pow2(v1, -e));
-          h2 = *reinterpret_cast<const uint32_t*>(&h);
-        }
-        const int q = pi >> 5, pl = pi & 31;
-        const int slot = q - origin;
-        const int word = (((slot * 4 + (pl >> 3)) * MT + nt) * 32 + gq * 4 + (pl & 3)) * 2 + ((pl & 7) >> 2);
-        xbuf[word] = h2;
-      }
+    for (int wi = ctid; wi < nwords; wi += kConsumerThreads) {
+      const int nt = (wi >> 6) % MT, m = nt * 8 + ((wi >> 3) & 7);
+      if (m >= p.M) continue;
+      const uint32_t wv = base[wi];
+      const int e = sm.xexp[m];
+      const __half2 h = __floats2half2_rn(mul_pow2(bf16_bits_to_float(wv & 0xFFFFu), -e),
+                                          mul_pow2(bf16_bits_to_float(wv >> 16), -e));
+      base[wi] = *reinterpret_cast<const uint32_t*>(&h);
     }
   }
 }
@@ -634,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       qb0 = origin + (int)(ub - u);
     }
     named_bar_sync(1, kConsumerThreads);
-    stage_x<MT>(p, xbuf, sm, origin, qa0, qb0, qa1, qb1, warp, lane);
+    stage_x<MT>(p, xbuf, sm, origin, qa0, qb0, qa1, qb1, warp * 32 + lane);
     named_bar_sync(1, kConsumerThreads);
 
     int cur_g = -1;

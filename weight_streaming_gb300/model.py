@@ -129,7 +129,7 @@ class SyntheticModel:
 
     def workspace(self, M: int) -> torch.Tensor:
         n = V.vp_pass_workspace_bytes(self.model, M)
-        return torch.empty(n, dtype=torch.uint8, device="cuda")
+        return torch.zeros(n, dtype=torch.uint8, device="cuda")
 
     def launch_count(self) -> int:
         return V.vp_pass_launch_count(self.model)
