@@ -38,6 +38,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=64)
+    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head"],
+                    help="time one GEMM shape alone (for profiling) instead of the pass")
+    ap.add_argument("--M", type=int, default=8)
     return ap.parse_args()
 
 
@@ -199,10 +202,58 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ the GPU arm
 
+def run_kernel(args):
+    """One GEMM of the pass alone through the C ABI, rotating over 4 weight copies (> L2) so every
+    launch streams from DRAM; prints one JSON line with the average launch time and GB/s."""
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    from weight_streaming_gb300.model import pack_fp8, pack_nvfp4
+    shapes = {"gate": ("nvfp4", 17408, 5120), "down": ("nvfp4", 5120, 17408), "gdn_in": ("fp8", 16384, 5120),
+              "head": ("nvfp4", 248320, 5120)}
+    fmt, N, K = shapes[args.kernel]
+    M = args.M
+    copies = 1 if args.kernel == "head" else 4
+    ws_list = []
+    for c in range(copies):
+        if fmt == "nvfp4":
+            cc = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+            sc = torch.empty((N, K // 16), dtype=torch.uint8, device="cuda")
+            synth.gpu_uniform_bytes(cc, 0, synth.stream_id(c, synth.T_GATE_C))
+            synth.gpu_scale_codes(sc, 0, synth.stream_id(c, synth.T_GATE_S))
+            ws_list.append(pack_nvfp4(cc, sc))
+        else:
+            w = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+            synth.gpu_fp8_normal_codes(w, 0, synth.stream_id(c, synth.T_IN))
+            ws_list.append(pack_fp8(w))
+    x = torch.randn((M, K), device="cuda").to(torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(V.vp_workspace_bytes(V.VP_OP_NVFP4, M, N, K), dtype=torch.uint8, device="cuda")
+    fn = V.vp_linear_nvfp4 if fmt == "nvfp4" else V.vp_linear_fp8
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        fn(ws_list[i % copies], 1.0, x, y, M, N, K, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        fn(ws_list[i % copies], 1.0, x, y, M, N, K, ws)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    nbytes = N * K * 9 // 16 if fmt == "nvfp4" else N * K
+    print(json.dumps({"kernel": args.kernel, "fmt": fmt, "M": M, "N": N, "K": K, "us_per_launch": t * 1e6,
+                      "gbps": nbytes / t / 1e9, "bytes_per_launch": nbytes}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.kernel:
+        run_kernel(args)
         return
     import numpy as np
     import torch

@@ -84,10 +84,12 @@ vp_status vp_read_status(const void* ws, int* status, void* stream);
  *          bytes, scale[n][k/16] applies to weights k..k+15 of row n.  [LM-formats]
  *   FP8:   [N][K] E4M3 (FN) bytes, one fp32 scale per tensor.  [LM-bus]
  * The kernels read a packed copy whose size is exactly the canonical size (9 bytes per 16 NVFP4
- * weights [SP-geom]; 1 byte per FP8 weight): rows are cut into 256-row slabs; within a slab,
- * 64-wide K chunks of every 16-row block are stored contiguously so that one bulk copy moves a
- * slab's K chunk and every thread's MMA operand is one aligned 16/32-byte read.
- * Requirements: N % 16 == 0, K % 64 == 0.  */
+ * weights [SP-geom]; 1 byte per FP8 weight): 16-row blocks, each cut along K into chunks (256
+ * weights wide for NVFP4, 128 for FP8) of two 8-row strips, stored row-block major so that one
+ * row block's stream along K is contiguous and one chunk (2304 / 2048 bytes) is one bulk copy;
+ * inside a strip the bytes follow the warp MMA's operand order (every thread's share of a 16-wide
+ * k step is one aligned 16-byte read).
+ * Requirements: N % 16 == 0; NVFP4 K % 256 == 0, FP8 K % 128 == 0; K <= 65536.  */
 
 /* Packed size in bytes: N*K/16*9 (NVFP4) and N*K (FP8); 0 if N or K is unsupported. */
 size_t vp_packed_bytes_nvfp4(int N, int K);
@@ -107,9 +109,9 @@ vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_b
  *          scale (a multiplier).
  *   FP8:   w[n][k] = e4m3(w8[n][k]); scale = the fp32 per-tensor scale.
  * x: bf16 [M][K] row-major (device, 16-byte aligned); y: fp32 [M][N] row-major (device).
- * Shapes: 1 <= M <= 32, N % 16 == 0, K % 64 == 0, N*K < 2^40.
- * The K dimension is split across CTAs (split-K) with a fixed-order reduction, so results are
- * bit-identical from run to run.  [BS-ties] (split-K).  */
+ * Shapes: 1 <= M <= 32, N % 16 == 0, K as for the packed layout, N*K < 2^40.
+ * Work is split along K across warps and CTAs (split-K) with a fixed-order reduction, so results
+ * are bit-identical from run to run.  [BS-ties] (split-K).  */
 enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3 };
 
 /* Workspace bytes for one call of op (VP_OP_*) at the given shape; 0 if the shape is invalid. */
@@ -129,7 +131,7 @@ vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float*
  *   n_commit[l] = acc + 1 (1..8);  committed[l][j] = argmax[8l + j] for j <= acc, -1 after.
  * pending[8l] is the lane's anchor (already committed) token and is not compared.
  * x: bf16 [M][K]; pending: int32 [M]; argmax: int32 [M]; n_commit: int32 [M/8];
- * committed: int32 [M/8][8]; logits: optional fp32 [M][V] (debug).  V % 16 == 0, K % 64 == 0. */
+ * committed: int32 [M/8][8]; logits: optional fp32 [M][V] (debug).  V % 16 == 0, K % 256 == 0. */
 vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const void* x, int M,
                                 int V, int K, const int32_t* pending, int32_t* argmax,
                                 int32_t* n_commit, int32_t* committed, float* logits, void* ws,
@@ -183,8 +185,9 @@ typedef struct {
 
 typedef struct vp_model vp_model;
 
-/* Validates the descriptors (shapes as for the linear calls; hidden % 64 == 0, inter % 64 == 0,
- * k_out % 64 == 0) and stores them (host memory, owned by the model). */
+/* Validates the descriptors (shapes as for the linear calls: hidden % 256 == 0, inter % 256 == 0,
+ * k_out % 128 == 0, row counts % 16 == 0) and stores them with the pass's phase program (host
+ * memory, owned by the model). */
 vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_desc* layers,
                           int n_layers, const vp_head_desc* head, vp_model** out);
 void vp_model_destroy(vp_model* model);
@@ -195,21 +198,23 @@ size_t vp_pass_workspace_bytes(const vp_model* model, int M);
 /* One verify pass.  x0: bf16 [M][hidden] (the rows' input hidden states, read-only); pending,
  * argmax, n_commit, committed as for vp_head_argmax_accept; M = 8 * lanes, lanes 1..4.
  * trace: optional bf16 [2 * n_layers][M][hidden], the residual stream h after every mixer block
- * and every MLP block (debug; adds one device copy per block).  logits: optional fp32 [M][vocab].
- * No host synchronisation, no allocation: capturable into a CUDA graph. */
+ * and every MLP block (debug; written by the residual epilogues).  logits: optional fp32
+ * [M][vocab].  No host synchronisation, no allocation: capturable into a CUDA graph. */
 vp_status vp_verify_pass(const vp_model* model, const void* x0, int M, const int32_t* pending,
                          int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace,
                          float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16
  * [M][hidden], updated in place); block 2l is the mixer block of layer l and block 2l + 1 its MLP
- * block, computed exactly as inside vp_verify_pass (the same kernels), preceded by the 1/rms of h's
- * rows.  trace: optional bf16 [block_end - block_begin][M][hidden], h after each block.  Lets a
+ * block, computed exactly as inside vp_verify_pass (the same phases of the same kernel).
+ * trace: optional bf16 [block_end - block_begin][M][hidden], h after each block.  Lets a
  * caller run part of the stream, or check one block against a reference from a known input. */
 vp_status vp_verify_blocks(const vp_model* model, void* h, int M, int block_begin, int block_end, void* trace,
                            void* ws, size_t ws_bytes, void* stream);
 
-/* Kernel launches that vp_verify_pass enqueues for a model (for launch accounting). */
+/* Kernel launches that vp_verify_pass enqueues for a model (for launch accounting): the pass runs
+ * as one persistent program of 4 phases per layer plus the head, at most 160 phases per launch,
+ * after one device-to-device copy of x0. */
 int vp_pass_launch_count(const vp_model* model);
 
 #ifdef __cplusplus

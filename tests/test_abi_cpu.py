@@ -42,7 +42,8 @@ def test_status_strings(V):
 def test_packed_and_workspace_sizes(V):
     assert V.vp_packed_bytes_nvfp4(17408, 5120) == 17408 * 5120 * 9 // 16
     assert V.vp_packed_bytes_fp8(16384, 5120) == 16384 * 5120
-    assert V.vp_packed_bytes_nvfp4(17, 64) == 0 and V.vp_packed_bytes_nvfp4(16, 48) == 0
+    assert V.vp_packed_bytes_nvfp4(17, 256) == 0 and V.vp_packed_bytes_nvfp4(16, 128) == 0
+    assert V.vp_packed_bytes_fp8(16, 128) == 16 * 128 and V.vp_packed_bytes_fp8(16, 64) == 0
     assert V.vp_workspace_bytes(V.VP_OP_NVFP4, 8, 5120, 17408) > 0
     assert V.vp_workspace_bytes(V.VP_OP_NVFP4, 33, 5120, 17408) == 0
     assert V.vp_workspace_bytes(V.VP_OP_NVFP4, 0, 5120, 17408) == 0
@@ -62,7 +63,8 @@ def test_linear_validation_without_gpu(V):
         assert fn(None, *ok[1:]) == V.VP_ERR_INVALID_ARG
         assert fn(*ok[:2], None, *ok[3:]) == V.VP_ERR_INVALID_ARG
         assert fn(*ok[:7], None, *ok[8:]) == V.VP_ERR_INVALID_ARG
-        for M, N, K in ((0, 256, 1024), (33, 256, 1024), (8, 250, 1024), (8, 256, 1000), (8, 0, 1024)):
+        for M, N, K in ((0, 256, 1024), (33, 256, 1024), (8, 250, 1024), (8, 256, 1000), (8, 0, 1024),
+                        (8, 256, 65536 + 256)):
             assert fn(FAKE, 1.0, FAKE, FAKE, M, N, K, FAKE, 1 << 30, None) == V.VP_ERR_SHAPE
         assert fn(FAKE + 8, *ok[1:]) == V.VP_ERR_ALIGNMENT
         assert fn(*ok[:2], FAKE + 2, *ok[3:]) == V.VP_ERR_ALIGNMENT
@@ -103,7 +105,7 @@ def _layer(V, kind=0, n_in=512, k_out=256, n_kv=0):
 def test_model_create_validation_without_gpu(V):
     head = V.vp_head_desc(FAKE, 1.0, 2048)
     m = V.vp_model(256, 512, 1e-6, [_layer(V), _layer(V, 1, 384, 256, 128)], head)
-    assert V.vp_pass_launch_count(m) == 2 + 4 * 2
+    assert V.vp_pass_launch_count(m) == 1  # 9 phases: one executor launch
     assert V.vp_pass_workspace_bytes(m, 8) > 0
     assert V.vp_pass_workspace_bytes(m, 12) == 0
     m.close()
@@ -113,6 +115,10 @@ def test_model_create_validation_without_gpu(V):
         V.vp_model(250, 512, 1e-6, [_layer(V)], head)
     with pytest.raises(V.VerifyError):
         V.vp_model(256, 512, 1e-6, [_layer(V, kind=1, n_kv=0)], head)
+    m64 = V.vp_model(256, 512, 1e-6, [_layer(V, 1 if l % 4 == 3 else 0, 384 if l % 4 == 3 else 512, 256,
+                                             128 if l % 4 == 3 else 0) for l in range(64)], head)
+    assert V.vp_pass_launch_count(m64) == 2  # 257 phases, at most 160 per launch
+    m64.close()
     bad = _layer(V)
     bad.w_up = FAKE + 4
     with pytest.raises(V.VerifyError):

@@ -122,7 +122,7 @@ def check_head(am, nc, cm, lg, y_ref, a_ref, pending, what):
     return unique
 
 
-@pytest.mark.parametrize("M,Vv,K", [(8, 5136, 1024), (16, 4096, 640), (32, 2064, 2048)])
+@pytest.mark.parametrize("M,Vv,K", [(8, 5136, 1024), (16, 4096, 768), (32, 2064, 2048), (8, 2048, 5120)])
 def test_head_matches_oracle(V, M, Vv, K):
     codes = synth.uniform_bytes(M + Vv, 1, 0, Vv * K // 2).reshape(Vv, K // 2)
     scales = synth.scale_codes(M + Vv, 2, 0, Vv * K // 16).reshape(Vv, K // 16)

@@ -1,6 +1,6 @@
 """GPU parity of the skinny NVFP4 / FP8 linear layers (vp_linear_*) and the packers against the
 fp64 oracle, through the C ABI.  Sizes span several 256-row groups, several CTAs per group
-(split-K), ragged M, partial last groups and both activation-staging modes."""
+(split-K), ragged M, one to four n-tiles, and phases cut into K slices."""
 import numpy as np
 import pytest
 import torch
@@ -60,77 +60,68 @@ def run_fp8(V, w, x, s):
 # ------------------------------------------------------------------ packers
 
 def expected_packed_nvfp4(codes, scales):
-    """The documented packed layout, built independently in numpy."""
+    """The documented packed layout, built independently in numpy: 16-row blocks, 256-wide K chunks,
+    two 8-row strips per chunk; a strip holds, for half h, row g and quarter c, the bytes of steps
+    8h .. 8h+7 that cover k = 16s + 4c .. +3, then the rows' 16 block scales."""
     N, K = codes.shape[0], codes.shape[1] * 2
-    nq = K // 64
     out = []
-    for slab in range((N + 255) // 256):
-        nrb = min(16, N // 16 - 16 * slab)
-        for q in range(nq):
-            for rbi in range(nrb):
-                rb = 16 * slab + rbi
-                blk = np.zeros(576, np.uint8)
-                for L in range(32):
-                    g, t = L // 4, L % 4
-                    for j in range(4):
-                        for i in range(4):
-                            row = rb * 16 + g + 8 * (i & 1)
-                            k = 64 * q + 16 * j + 2 * t + 8 * (i >> 1)
-                            blk[16 * L + 4 * j + i] = codes[row, k // 2]
-                for g in range(8):
-                    for j in range(4):
-                        for h in range(2):
-                            blk[512 + 8 * g + 2 * j + h] = scales[rb * 16 + g + 8 * h, 4 * q + j]
-                out.append(blk)
+    for rb in range(N // 16):
+        for kc in range(K // 256):
+            for t in range(2):
+                r0 = 16 * rb + 8 * t
+                c = codes[r0:r0 + 8, 128 * kc:128 * kc + 128].reshape(8, 2, 8, 4, 2)  # [g][h][ss][c][b]
+                out.append(c.transpose(1, 0, 3, 2, 4).reshape(-1))
+                out.append(scales[r0:r0 + 8, 16 * kc:16 * kc + 16].reshape(-1))
+    return np.concatenate(out)
+
+
+def expected_packed_fp8(w):
+    N, K = w.shape
+    out = []
+    for rb in range(N // 16):
+        for kc in range(K // 128):
+            for t in range(2):
+                r0 = 16 * rb + 8 * t
+                q = w[r0:r0 + 8, 128 * kc:128 * kc + 128].reshape(8, 2, 4, 4, 4)  # [g][h][ss][c][b]
+                out.append(q.transpose(1, 0, 3, 2, 4).reshape(-1))
     return np.concatenate(out)
 
 
 def test_pack_nvfp4_layout(V):
-    N, K = 288, 128  # one full slab + a partial one
+    N, K = 48, 512  # three row blocks, two chunks
     codes, scales, _ = nvfp4_case(7, 1, N, K)
     packed = torch.empty(V.vp_packed_bytes_nvfp4(N, K), dtype=torch.uint8, device="cuda")
     V.vp_pack_nvfp4(dev_u8(codes), dev_u8(scales), N, K, packed)
     torch.cuda.synchronize()
-    assert np.array_equal(packed.cpu().numpy(), expected_packed_nvfp4(codes, scales))
+    exp = expected_packed_nvfp4(codes, scales)
+    assert exp.size == N * K * 9 // 16
+    assert np.array_equal(packed.cpu().numpy(), exp)
 
 
 def test_pack_fp8_layout(V):
-    N, K = 272, 128
+    N, K = 48, 384
     w, _ = fp8_case(8, 1, N, K)
     packed = torch.empty(V.vp_packed_bytes_fp8(N, K), dtype=torch.uint8, device="cuda")
     V.vp_pack_fp8(dev_u8(w), N, K, packed)
     torch.cuda.synchronize()
-    got = packed.cpu().numpy()
-    nq = K // 64
-    pos = 0
-    for slab in range((N + 255) // 256):
-        nrb = min(16, N // 16 - 16 * slab)
-        for q in range(nq):
-            for rbi in range(nrb):
-                rb = 16 * slab + rbi
-                for L in range(32):
-                    g, t = L // 4, L % 4
-                    for j in range(4):
-                        for i in range(4):
-                            for e in range(2):
-                                row = rb * 16 + g + 8 * (i & 1)
-                                k = 64 * q + 16 * j + 2 * t + 8 * (i >> 1) + e
-                                assert got[pos + 32 * L + 8 * j + 2 * i + e] == w[row, k]
-                pos += 1024
-    assert pos == got.size
+    exp = expected_packed_fp8(w)
+    assert exp.size == N * K
+    assert np.array_equal(packed.cpu().numpy(), exp)
 
 
 # ------------------------------------------------------------------ parity
 
 SHAPES = [
     (8, 1024, 1024),   # tiny NVFP4 linear of the synthetic recipe
-    (1, 16, 64),       # smallest
-    (3, 272, 192),     # partial group, odd M
-    (13, 1040, 1024),  # several groups + ragged last group
-    (24, 528, 640),
-    (32, 4096, 512),   # many groups, all K staged at once
-    (32, 256, 4096),   # activation window larger than shared memory: staged in batches
-    (8, 4112, 2048),   # split-K over many CTAs + ragged group
+    (1, 16, 256),      # smallest: one row block, one chunk
+    (3, 272, 256),     # odd M, odd row-block count
+    (13, 1040, 1024),  # ragged M in the second n-tile
+    (24, 528, 768),    # three n-tiles
+    (32, 4096, 512),   # four n-tiles, many row blocks per warp
+    (32, 256, 4096),   # activations wider than shared memory: three K slices
+    (16, 512, 8192),   # the same with two n-tiles
+    (8, 4112, 2048),   # fewer units than warps: row blocks split across warps
+    (8, 512, 17408),   # MLP-down width at M = 8: three K slices
 ]
 
 
@@ -148,6 +139,15 @@ def test_linear_fp8_matches_oracle(V, M, N, K):
     w, x = fp8_case(200 + M + N + K, M, N, K)
     y = run_fp8(V, w, x, 0.625)
     y_ref, a_ref = oracle.linear(oracle.FP8, x, w, None, 0.625, N)
+    assert_linear_close(y, y_ref, a_ref, f"fp8 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(5, 64, 384), (8, 1024, 6144)])
+def test_linear_fp8_half_chunks(V, M, N, K):
+    """FP8 reduction widths that are a multiple of 128 but not of 256 (mixer out-projection)."""
+    w, x = fp8_case(300 + M + N + K, M, N, K)
+    y = run_fp8(V, w, x, 1.25)
+    y_ref, a_ref = oracle.linear(oracle.FP8, x, w, None, 1.25, N)
     assert_linear_close(y, y_ref, a_ref, f"fp8 {M}x{N}x{K}")
 
 

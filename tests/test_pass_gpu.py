@@ -16,7 +16,7 @@ from passutil import DeviceModel, make_layers, mixer_block_ref, mlp_block_ref
 
 pytestmark = pytest.mark.gpu
 
-SMALL = dict(n_layers=4, hidden=256, inter=512, vocab=2064, period=4, gdn_in=512, gdn_z=320, attn_q=384, attn_kv=128,
+SMALL = dict(n_layers=4, hidden=256, inter=512, vocab=2064, period=4, gdn_in=512, gdn_z=384, attn_q=384, attn_kv=128,
              attn_z=256)
 
 

@@ -1,7 +1,8 @@
 """Builds libverify.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Three translation units are compiled in parallel (host API + packers, NVFP4 GEMM instantiations,
-FP8 GEMM instantiations) and linked against the shared CUDA runtime.
+Three translation units are compiled in parallel (host API + packers, the streaming executor for
+8/16 token columns, the executor for 24/32 token columns) and linked against the shared CUDA
+runtime.
 """
 from __future__ import annotations
 
@@ -15,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libverify.so")
-SOURCES = ["api.cu", "gemm_nvfp4.cu", "gemm_fp8.cu"]
+SOURCES = ["api.cu", "exec_nt12.cu", "exec_nt34.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -1,5 +1,6 @@
-// Host side of libverify: argument validation, packers, workspace carving and the verify-pass
-// driver.  Every entry point is declared (with its source passage) in include/verify.h.
+// Host side of libverify: argument validation, packers, workspace carving, the phase programs of
+// the linear / head calls and of the verify pass, and the argmax + accept kernel over given logits.
+// Every entry point is declared (with its source passage) in include/verify.h.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -7,10 +8,10 @@
 #include <new>
 #include <vector>
 
-#include "verify.h"
-#include "gemm.cuh"
+#include "exec.cuh"
+#include "exec_launch.h"
 #include "internal.h"
-#include "launch_decl.h"
+#include "verify.h"
 
 using namespace vp;
 
@@ -22,9 +23,6 @@ vp_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = (int)e;
   return VP_ERR_CUDA;
 }
-
-constexpr int kMaxGrid = 256;  // workspace is sized for grids up to this many CTAs
-constexpr int kArgmaxChunk = 8192;
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -49,118 +47,161 @@ vp_status device_sms(int* sms) {
   return VP_OK;
 }
 
-bool linear_shape_ok(int M, int N, int K) {
-  return M >= 1 && M <= kMaxM && N >= 16 && N % kRowsPerBlock == 0 && K >= kQuadK && K % kQuadK == 0 &&
+constexpr int kMaxK = 65536;
+
+bool weight_shape_ok(int fmt, int N, int K) {
+  const int ck = chunk_k(fmt);
+  return N >= kRowBlock && N % kRowBlock == 0 && K >= ck && K % ck == 0 && K <= kMaxK &&
          (long long)N * K < (1LL << 40);
 }
 
-int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+int nt_of(int M) { return (M + 7) / 8; }
 
-struct GemmWs {
-  WsLayout L;
-  int* status;
-  unsigned* task_cnt;
-  unsigned* group_cnt;
-  float* group_aux;
-  float* partials;
+// ------------------------------------------------------------------ phases
+struct PhaseSpec {
+  int fmt = kFmtNvfp4, layout = kPlain;
+  const void* w0 = nullptr;
+  const void* w1 = nullptr;
+  float s0 = 1.0f, s1 = 1.0f;
+  int rows0 = 0, rows1 = 0, K = 0;
+  int epi = kEpiF32, x_src = kBufX, x_ld = 0, x_rms = 0, out = kBufY, out_ld = 0, out_cols = 0, trace_slot = -1;
 };
 
-GemmWs carve_gemm_ws(void* ws, int n_groups, int mt) {
-  GemmWs w;
-  w.L = gemm_ws_layout(n_groups, kMaxGrid, mt);
-  uint8_t* b = (uint8_t*)ws;
-  w.status = (int*)(b + w.L.status);
-  w.task_cnt = (unsigned*)(b + w.L.task_cnt);
-  w.group_cnt = (unsigned*)(b + w.L.group_cnt);
-  w.group_aux = (float*)(b + w.L.group_aux);
-  w.partials = (float*)(b + w.L.partials);
-  return w;
+Phase make_phase(const PhaseSpec& s, int NT) {
+  Phase ph;
+  memset(&ph, 0, sizeof(ph));
+  ph.w0 = static_cast<const uint8_t*>(s.w0);
+  ph.w1 = static_cast<const uint8_t*>(s.w1);
+  ph.s0 = s.s0;
+  ph.s1 = s.s1;
+  ph.K = s.K;
+  ph.KC = s.K / chunk_k(s.fmt);
+  if (s.layout == kPlain) {
+    ph.RB = (s.rows0 + s.rows1) / kRowBlock;
+    ph.rb1 = s.rows0 / kRowBlock;
+  } else {
+    ph.RB = s.rows0 / kStripRows;
+    ph.rb1 = ph.RB;
+  }
+  const int per = ks_max(NT) / chunk_k(s.fmt);
+  ph.ks = (int8_t)((ph.KC + per - 1) / per);
+  ph.cmax = phase_cmax(ph.RB, ph.KC, ph.ks);
+  ph.fmt = (int8_t)s.fmt;
+  ph.layout = (int8_t)s.layout;
+  ph.epi = (int8_t)s.epi;
+  ph.x_src = (int8_t)s.x_src;
+  ph.x_rms = (int8_t)s.x_rms;
+  ph.out = (int8_t)s.out;
+  ph.x_ld = s.x_ld;
+  ph.out_ld = s.out_ld;
+  ph.out_cols = s.out_cols;
+  ph.trace_slot = s.trace_slot;
+  return ph;
 }
 
-void fill_ws(GemmParams& p, const GemmWs& w) {
-  p.status = w.status;
-  p.task_cnt = w.task_cnt;
-  p.group_cnt = w.group_cnt;
-  p.group_aux = w.group_aux;
-  p.partials = w.partials;
+// Every K slice gets at least one CTA (the same integer formula as the device's slice_geom).
+bool slices_ok(const Phase& ph, int G) {
+  int prev = 0;
+  for (int s = 1; s <= ph.ks; ++s) {
+    const int kc = (int)((long long)s * ph.KC / ph.ks);
+    const int c = s == ph.ks ? G : (int)(((long long)G * kc + ph.KC / 2) / ph.KC);
+    if (c <= prev) return false;
+    prev = c;
+  }
+  return true;
 }
 
-// Plain single-matrix GEMM parameters.
-GemmParams single(const void* w, int N, int K, int M, float scale) {
-  GemmParams p;
-  memset(&p, 0, sizeof(p));
-  p.w[0] = (const uint8_t*)w;
-  p.seg_rows[0] = N;
-  p.wscale[0] = scale;
-  p.wscale[1] = 1.0f;
-  p.K = K;
-  p.M = M;
-  p.nq = K / kQuadK;
-  p.n_groups = ceil_div(N, kSlabRows);
-  p.seg0_groups = p.n_groups;
-  p.units = (long long)p.n_groups * p.nq;
-  return p;
+struct Needs {
+  size_t max_rb = 1, max_slots = 1;
+  void add(const Phase& ph) {
+    max_rb = std::max(max_rb, (size_t)ph.RB);
+    max_slots = std::max(max_slots, (size_t)ph.RB * ph.ks * ph.cmax);
+  }
+};
+
+Io make_io(void* ws, const WsLayout& L) {
+  Io io;
+  memset(&io, 0, sizeof(io));
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  io.status = reinterpret_cast<int*>(b + L.status);
+  io.bar = reinterpret_cast<unsigned*>(b + L.bar);
+  io.head_cnt = reinterpret_cast<unsigned*>(b + L.head_cnt);
+  io.head_aux = reinterpret_cast<float*>(b + L.head_aux);
+  io.rb_cnt = reinterpret_cast<unsigned*>(b + L.rb_cnt);
+  io.partials = reinterpret_cast<float*>(b + L.partials);
+  return io;
 }
 
-vp_status launch(int fmt, const GemmParams& p, int sms, cudaStream_t s, bool pdl) {
-  const int mt = (p.M + 7) / 8;
-  const int grid = (int)((p.units < (long long)sms) ? p.units : (long long)sms);
-  cudaError_t e = fmt == kFmtNvfp4 ? launch_gemm_nvfp4(p, mt, grid, s, pdl) : launch_gemm_fp8(p, mt, grid, s, pdl);
-  if (e != cudaSuccess) return cuda_fail(e);
+// Launches phases [0, n) of `phases` as programs of at most kMaxPhases phases each.
+vp_status run_phases(const std::vector<Phase>& phases, int M, float eps, const Io& io, int G, cudaStream_t s) {
+  const int n = (int)phases.size();
+  const int launches = (n + kMaxPhases - 1) / kMaxPhases;
+  static thread_local Program prog;  // ~12 KB: kept off the stack
+  for (int l = 0; l < launches; ++l) {
+    const int p0 = (int)((long long)l * n / launches), p1 = (int)((long long)(l + 1) * n / launches);
+    prog.n = p1 - p0;
+    prog.M = M;
+    prog.eps = eps;
+    prog.pad = 0;
+    for (int i = p0; i < p1; ++i) prog.ph[i - p0] = phases[i];
+    cudaError_t e = launch_exec(prog, io, G, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   return VP_OK;
 }
 
+int program_launches(int n_phases) { return (n_phases + kMaxPhases - 1) / kMaxPhases; }
+
 // ------------------------------------------------------------------ packers
-// Packed NVFP4 block (16 rows x 64 K, 576 bytes) of row-block rb, quad q:
-//   byte 16*L + 4*j + i (L = lane 0..31, g = L/4, t = L%4, j = k16 step, i = MMA A register):
-//     the canonical code byte holding weights (row rb*16 + g + 8*(i&1), k = 64q + 16j + 2t + 8*(i>>1))
-//     and k + 1 (low nibble = k).
-//   byte 512 + 8*g + 2*j + h: block scale of row rb*16 + g + 8h for k16 step j (scale column 4q + j).
-// Blocks are ordered slab by slab (256 rows); within a slab, quad-major then row-block.
+// Canonical row-major weights -> the packed layout of internal.h.  One thread per 16-byte piece of
+// a strip: NVFP4 strips have 64 code pieces ([h][g][c]) and 8 scale pieces ([g]); FP8 strips 64.
 __global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int N, int K,
-                                  uint8_t* __restrict__ out, long long total) {
-  const int nq = K / kQuadK;
-  const int nrb_total = N / kRowsPerBlock;
-  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total; o += (long long)gridDim.x * blockDim.x) {
-    const long long b = o / kNvfp4BlockBytes;
-    const int bb = (int)(o % kNvfp4BlockBytes);
-    const long long slab = b / ((long long)kBlocksPerSlab * nq);
-    const long long r = b % ((long long)kBlocksPerSlab * nq);
-    const int nrb_s = min(kBlocksPerSlab, nrb_total - (int)slab * kBlocksPerSlab);
-    const int q = (int)(r / nrb_s), rb = (int)slab * kBlocksPerSlab + (int)(r % nrb_s);
-    uint8_t v;
-    if (bb < 512) {
-      const int L = bb >> 4, j = (bb >> 2) & 3, i = bb & 3;
-      const int g = L >> 2, t = L & 3;
-      const long long row = (long long)rb * kRowsPerBlock + g + 8 * (i & 1);
-      const int k = q * kQuadK + 16 * j + 2 * t + 8 * (i >> 1);
-      v = codes[row * (K / 2) + k / 2];
+                                  uint8_t* __restrict__ out) {
+  const int KC = K / 256;
+  const long long pieces = (long long)(N / 8) * KC * 72;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pieces;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long strip = i / 72;
+    const int piece = (int)(i % 72);
+    const int t = (int)(strip & 1), kc = (int)((strip >> 1) % KC);
+    const long long rb = (strip >> 1) / KC;
+    uint8_t b[16];
+    if (piece < 64) {
+      const int h = piece >> 5, g = (piece >> 2) & 7, c = piece & 3;
+      const uint8_t* src = codes + (size_t)(rb * 16 + t * 8 + g) * (K / 2) + (size_t)kc * 128;
+#pragma unroll
+      for (int ss = 0; ss < 8; ++ss) {
+        const int s = 8 * h + ss;
+        b[2 * ss] = src[8 * s + 2 * c];
+        b[2 * ss + 1] = src[8 * s + 2 * c + 1];
+      }
     } else {
-      const int x = bb - 512, g = x >> 3, j = (x >> 1) & 3, h = x & 1;
-      const long long row = (long long)rb * kRowsPerBlock + g + 8 * h;
-      v = scales[row * (K / 16) + 4 * q + j];
+      const int g = piece - 64;
+      const uint8_t* src = scales + (size_t)(rb * 16 + t * 8 + g) * (K / 16) + (size_t)kc * 16;
+#pragma unroll
+      for (int s = 0; s < 16; ++s) b[s] = src[s];
     }
-    out[o] = v;
+    uint4 v;
+    memcpy(&v, b, 16);
+    *reinterpret_cast<uint4*>(out + strip * 1152 + piece * 16) = v;
   }
 }
 
-// Packed FP8 block (16 rows x 64 K, 1024 bytes): byte 32*L + 8*j + 2*i + e holds
-// w[rb*16 + g + 8*(i&1)][64q + 16j + 2t + 8*(i>>1) + e] (g = L/4, t = L%4).
-__global__ void pack_fp8_kernel(const uint8_t* __restrict__ w, int N, int K, uint8_t* __restrict__ out, long long total) {
-  const int nq = K / kQuadK;
-  const int nrb_total = N / kRowsPerBlock;
-  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < total; o += (long long)gridDim.x * blockDim.x) {
-    const long long b = o / kFp8BlockBytes;
-    const int bb = (int)(o % kFp8BlockBytes);
-    const long long slab = b / ((long long)kBlocksPerSlab * nq);
-    const long long r = b % ((long long)kBlocksPerSlab * nq);
-    const int nrb_s = min(kBlocksPerSlab, nrb_total - (int)slab * kBlocksPerSlab);
-    const int q = (int)(r / nrb_s), rb = (int)slab * kBlocksPerSlab + (int)(r % nrb_s);
-    const int L = bb >> 5, j = (bb >> 3) & 3, i = (bb >> 1) & 3, e = bb & 1;
-    const int g = L >> 2, t = L & 3;
-    const long long row = (long long)rb * kRowsPerBlock + g + 8 * (i & 1);
-    const int k = q * kQuadK + 16 * j + 2 * t + 8 * (i >> 1) + e;
-    out[o] = w[row * K + k];
+__global__ void pack_fp8_kernel(const uint8_t* __restrict__ w, int N, int K, uint8_t* __restrict__ out) {
+  const int KC = K / 128;
+  const long long pieces = (long long)(N / 8) * KC * 64;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pieces;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long strip = i / 64;
+    const int piece = (int)(i % 64);
+    const int t = (int)(strip & 1), kc = (int)((strip >> 1) % KC);
+    const long long rb = (strip >> 1) / KC;
+    const int h = piece >> 5, g = (piece >> 2) & 7, c = piece & 3;
+    const uint8_t* src = w + (size_t)(rb * 16 + t * 8 + g) * K + (size_t)kc * 128;
+    uint32_t q[4];
+#pragma unroll
+    for (int ss = 0; ss < 4; ++ss) q[ss] = *reinterpret_cast<const uint32_t*>(src + 16 * (4 * h + ss) + 4 * c);
+    *reinterpret_cast<uint4*>(out + strip * 1024 + piece * 16) = make_uint4(q[0], q[1], q[2], q[3]);
   }
 }
 
@@ -171,12 +212,14 @@ int pack_grid(long long total) {
 }
 
 // ------------------------------------------------------------------ argmax + accept over given logits
+// Grid (chunks, M): each CTA reduces one chunk of one row, the last CTA reduces the chunks in order
+// and runs the acceptance.
 __global__ void __launch_bounds__(256) argmax_accept_kernel(const float* __restrict__ logits, int M, int V, int chunk,
                                                             int n_chunks, const int32_t* pending, int32_t* argmax,
                                                             int32_t* n_commit, int32_t* committed, float* aux,
-                                                            unsigned* task_cnt) {
-  __shared__ float red_v[256];
-  __shared__ int red_i[256];
+                                                            unsigned* cnt) {
+  __shared__ float red_v[8];
+  __shared__ int red_i[8];
   __shared__ int tok[kMaxM];
   __shared__ int last;
   const int c = blockIdx.x, m = blockIdx.y;
@@ -192,7 +235,7 @@ __global__ void __launch_bounds__(256) argmax_accept_kernel(const float* __restr
       bi = i;
     }
   }
-  am_shfl_reduce(bv, bi, 1, 16);
+  for (int o = 1; o < 32; o <<= 1) am_shfl_xor(bv, bi, o);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
     red_v[warp] = bv;
@@ -202,7 +245,7 @@ __global__ void __launch_bounds__(256) argmax_accept_kernel(const float* __restr
   if (threadIdx.x == 0) {
     float v0 = -INFINITY;
     int i0 = 0x7fffffff;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w)
+    for (int w = 0; w < 8; ++w)
       if (am_better(red_v[w], red_i[w], v0, i0)) {
         v0 = red_v[w];
         i0 = red_i[w];
@@ -210,43 +253,39 @@ __global__ void __launch_bounds__(256) argmax_accept_kernel(const float* __restr
     aux[((size_t)c * kMaxM + m) * 2] = v0;
     aux[((size_t)c * kMaxM + m) * 2 + 1] = __int_as_float(i0);
     __threadfence();
-    const unsigned old = atomicAdd(task_cnt, 1u);
-    last = (old == (unsigned)(n_chunks * M) - 1u);
+    last = atomicAdd(cnt, 1u) + 1 == (unsigned)(n_chunks * M);
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
-  argmax_accept_finish(aux, n_chunks, M, pending, argmax, n_commit, committed, red_v, red_i, tok, threadIdx.x, 256, 1);
-  if (threadIdx.x == 0) *task_cnt = 0u;
-}
-
-// ------------------------------------------------------------------ pass prologue
-// h = x0 and inv_rms[m] = 1 / sqrt(mean(h[m]^2) + eps), one CTA per row.
-__global__ void __launch_bounds__(256) pass_prep_kernel(const uint16_t* __restrict__ x0, uint16_t* __restrict__ h, int H,
-                                                        float eps, float* __restrict__ inv_rms) {
-  pdl_trigger();
-  __shared__ float red[8];
-  const int m = blockIdx.x;
-  float s = 0.0f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    const uint16_t b = x0[(size_t)m * H + k];
-    h[(size_t)m * H + k] = b;
-    const float v = __uint_as_float((uint32_t)b << 16);
-    s += v * v;
+  if (threadIdx.x < M) {
+    float v0 = -INFINITY;
+    int i0 = 0x7fffffff;
+    for (int cc = 0; cc < n_chunks; ++cc) {
+      const float2 e = __ldcg(reinterpret_cast<const float2*>(aux) + (size_t)cc * kMaxM + threadIdx.x);
+      if (am_better(e.x, __float_as_int(e.y), v0, i0)) {
+        v0 = e.x;
+        i0 = __float_as_int(e.y);
+      }
+    }
+    if (i0 == 0x7fffffff) i0 = 0;
+    tok[threadIdx.x] = i0;
+    argmax[threadIdx.x] = i0;
   }
-  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = 0.0f;
-    for (int w = 0; w < 8; ++w) t += red[w];
-    inv_rms[m] = 1.0f / sqrtf(t / (float)H + eps);
-  }
+  if ((int)threadIdx.x < M / 8) accept_lane(threadIdx.x, tok, pending, n_commit, committed);
+  if (threadIdx.x == 0) *cnt = 0u;
 }
 
-size_t argmax_ws_bytes(int V) {
-  const int n_chunks = ceil_div(V, kArgmaxChunk);
-  return align_up(256 + sizeof(float) * 2 * kMaxM * (size_t)n_chunks, 256);
+void argmax_chunking(int V, int* chunk, int* n_chunks) {
+  int ch = 8192;
+  if ((V + ch - 1) / ch > kMaxGrid) ch = (V + kMaxGrid - 1) / kMaxGrid;
+  *chunk = ch;
+  *n_chunks = (V + ch - 1) / ch;
+}
+
+size_t single_ws_bytes(const Phase& ph, int NT) {
+  return ws_layout((size_t)ph.RB, (size_t)ph.RB * ph.ks * ph.cmax, NT).total;
 }
 
 }  // namespace
@@ -286,12 +325,12 @@ vp_status vp_read_status(const void* ws, int* status, void* stream) {
 }
 
 size_t vp_packed_bytes_nvfp4(int N, int K) {
-  if (N < 16 || N % 16 || K < 64 || K % 64) return 0;
+  if (!weight_shape_ok(kFmtNvfp4, N, K)) return 0;
   return (size_t)N * (size_t)K / 16 * 9;
 }
 
 size_t vp_packed_bytes_fp8(int N, int K) {
-  if (N < 16 || N % 16 || K < 64 || K % 64) return 0;
+  if (!weight_shape_ok(kFmtFp8, N, K)) return 0;
   return (size_t)N * (size_t)K;
 }
 
@@ -305,8 +344,8 @@ vp_status vp_pack_nvfp4(const void* codes, const void* scales, int N, int K, voi
   int sms = 0;
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
-  pack_nvfp4_kernel<<<pack_grid((long long)need), 256, 0, (cudaStream_t)stream>>>(
-      (const uint8_t*)codes, (const uint8_t*)scales, N, K, (uint8_t*)packed, (long long)need);
+  pack_nvfp4_kernel<<<pack_grid((long long)(N / 8) * (K / 256) * 72), 256, 0, (cudaStream_t)stream>>>(
+      (const uint8_t*)codes, (const uint8_t*)scales, N, K, (uint8_t*)packed);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
@@ -320,8 +359,8 @@ vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_b
   int sms = 0;
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
-  pack_fp8_kernel<<<pack_grid((long long)need), 256, 0, (cudaStream_t)stream>>>((const uint8_t*)w, N, K,
-                                                                               (uint8_t*)packed, (long long)need);
+  pack_fp8_kernel<<<pack_grid((long long)(N / 8) * (K / 128) * 64), 256, 0, (cudaStream_t)stream>>>(
+      (const uint8_t*)w, N, K, (uint8_t*)packed);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
@@ -329,32 +368,60 @@ vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_b
 size_t vp_workspace_bytes(int op, int M, int N, int K) {
   if (op == VP_OP_ARGMAX) {
     if (M < 8 || M > kMaxM || M % 8 || N < 1) return 0;
-    return argmax_ws_bytes(N);
+    return ws_layout(1, 1, 1).rb_cnt;  // the counter and the per-chunk maxima
   }
   if (op != VP_OP_NVFP4 && op != VP_OP_FP8 && op != VP_OP_HEAD) return 0;
-  if (!linear_shape_ok(M, N, K)) return 0;
+  const int fmt = op == VP_OP_FP8 ? kFmtFp8 : kFmtNvfp4;
+  if (M < 1 || M > kMaxM || !weight_shape_ok(fmt, N, K)) return 0;
   if (op == VP_OP_HEAD && M % 8) return 0;
-  return gemm_ws_layout(ceil_div(N, kSlabRows), kMaxGrid, (M + 7) / 8).total;
+  PhaseSpec s;
+  s.fmt = fmt;
+  s.rows0 = N;
+  s.K = K;
+  return single_ws_bytes(make_phase(s, nt_of(M)), nt_of(M));
+}
+
+static vp_status run_single(const PhaseSpec& s, int M, const void* x, void* ws, size_t ws_bytes, Io io_extra,
+                            cudaStream_t stream) {
+  const int NT = nt_of(M);
+  const Phase ph = make_phase(s, NT);
+  const WsLayout L = ws_layout((size_t)ph.RB, (size_t)ph.RB * ph.ks * ph.cmax, NT);
+  if (ws_bytes < L.total) return VP_ERR_WORKSPACE;
+  int sms = 0;
+  vp_status st = device_sms(&sms);
+  if (st != VP_OK) return st;
+  if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
+  Io io = make_io(ws, L);
+  for (int b = 0; b < kNumBufs; ++b) io.buf[b] = io_extra.buf[b];
+  io.buf[kBufX] = const_cast<void*>(x);
+  io.pending = io_extra.pending;
+  io.argmax = io_extra.argmax;
+  io.n_commit = io_extra.n_commit;
+  io.committed = io_extra.committed;
+  std::vector<Phase> phases(1, ph);
+  return run_phases(phases, M, 0.0f, io, sms, stream);
 }
 
 static vp_status linear_common(int fmt, const void* w, float scale, const void* x, float* y, int M, int N, int K,
                                void* ws, size_t ws_bytes, void* stream) {
   if (!w || !x || !y || !ws) return VP_ERR_INVALID_ARG;
-  if (!linear_shape_ok(M, N, K)) return VP_ERR_SHAPE;
+  if (M < 1 || M > kMaxM || !weight_shape_ok(fmt, N, K)) return VP_ERR_SHAPE;
   if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(ws, 256)) return VP_ERR_ALIGNMENT;
-  const size_t need = vp_workspace_bytes(fmt == kFmtNvfp4 ? VP_OP_NVFP4 : VP_OP_FP8, M, N, K);
-  if (ws_bytes < need) return VP_ERR_WORKSPACE;
-  int sms = 0;
-  vp_status st = device_sms(&sms);
-  if (st != VP_OK) return st;
-  GemmParams p = single(w, N, K, M, scale);
-  p.x = (const uint16_t*)x;
-  p.x_ld = K;
-  p.epi = kEpiF32;
-  p.y = y;
-  p.y_ld = N;
-  fill_ws(p, carve_gemm_ws(ws, p.n_groups, (M + 7) / 8));
-  return launch(fmt, p, sms, (cudaStream_t)stream, false);
+  PhaseSpec s;
+  s.fmt = fmt;
+  s.w0 = w;
+  s.s0 = scale;
+  s.rows0 = N;
+  s.K = K;
+  s.epi = kEpiF32;
+  s.x_src = kBufX;
+  s.x_ld = K;
+  s.out = kBufY;
+  s.out_ld = N;
+  Io extra;
+  memset(&extra, 0, sizeof(extra));
+  extra.buf[kBufY] = y;
+  return run_single(s, M, x, ws, ws_bytes, extra, (cudaStream_t)stream);
 }
 
 vp_status vp_linear_nvfp4(const void* w_packed, float tensor_scale, const void* x, float* y, int M, int N, int K,
@@ -371,26 +438,29 @@ vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const 
                                 const int32_t* pending, int32_t* argmax, int32_t* n_commit, int32_t* committed,
                                 float* logits, void* ws, size_t ws_bytes, void* stream) {
   if (!w_packed || !x || !pending || !argmax || !n_commit || !committed || !ws) return VP_ERR_INVALID_ARG;
-  if (!linear_shape_ok(M, V, K) || M % 8) return VP_ERR_SHAPE;
+  if (M < 8 || M > kMaxM || M % 8 || !weight_shape_ok(kFmtNvfp4, V, K)) return VP_ERR_SHAPE;
   if (!aligned(w_packed, 16) || !aligned(x, 16) || !aligned(ws, 256) || !aligned(pending, 4) || !aligned(argmax, 4) ||
       !aligned(n_commit, 4) || !aligned(committed, 4) || (logits && !aligned(logits, 4)))
     return VP_ERR_ALIGNMENT;
-  if (ws_bytes < vp_workspace_bytes(VP_OP_HEAD, M, V, K)) return VP_ERR_WORKSPACE;
-  int sms = 0;
-  vp_status st = device_sms(&sms);
-  if (st != VP_OK) return st;
-  GemmParams p = single(w_packed, V, K, M, tensor_scale);
-  p.x = (const uint16_t*)x;
-  p.x_ld = K;
-  p.epi = kEpiHead;
-  p.pending = pending;
-  p.argmax = argmax;
-  p.n_commit = n_commit;
-  p.committed = committed;
-  p.logits = logits;
-  p.logits_ld = V;
-  fill_ws(p, carve_gemm_ws(ws, p.n_groups, (M + 7) / 8));
-  return launch(kFmtNvfp4, p, sms, (cudaStream_t)stream, false);
+  PhaseSpec s;
+  s.fmt = kFmtNvfp4;
+  s.w0 = w_packed;
+  s.s0 = tensor_scale;
+  s.rows0 = V;
+  s.K = K;
+  s.epi = kEpiHead;
+  s.x_src = kBufX;
+  s.x_ld = K;
+  s.out = kBufLogits;
+  s.out_ld = V;
+  Io extra;
+  memset(&extra, 0, sizeof(extra));
+  extra.buf[kBufLogits] = logits;
+  extra.pending = pending;
+  extra.argmax = argmax;
+  extra.n_commit = n_commit;
+  extra.committed = committed;
+  return run_single(s, M, x, ws, ws_bytes, extra, (cudaStream_t)stream);
 }
 
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending, int32_t* argmax,
@@ -400,15 +470,17 @@ vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pen
   if (!aligned(logits, 4) || !aligned(ws, 256) || !aligned(pending, 4) || !aligned(argmax, 4) ||
       !aligned(n_commit, 4) || !aligned(committed, 4))
     return VP_ERR_ALIGNMENT;
-  if (ws_bytes < argmax_ws_bytes(V)) return VP_ERR_WORKSPACE;
+  if (ws_bytes < vp_workspace_bytes(VP_OP_ARGMAX, M, V, 0)) return VP_ERR_WORKSPACE;
   int sms = 0;
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
-  const int n_chunks = ceil_div(V, kArgmaxChunk);
+  int chunk = 0, n_chunks = 0;
+  argmax_chunking(V, &chunk, &n_chunks);
+  const WsLayout L = ws_layout(1, 1, 1);
   uint8_t* b = (uint8_t*)ws;
   argmax_accept_kernel<<<dim3(n_chunks, M), 256, 0, (cudaStream_t)stream>>>(
-      logits, M, V, kArgmaxChunk, n_chunks, pending, argmax, n_commit, committed, (float*)(b + 256),
-      (unsigned*)(b + 64));
+      logits, M, V, chunk, n_chunks, pending, argmax, n_commit, committed, (float*)(b + L.head_aux),
+      (unsigned*)(b + L.head_cnt));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
@@ -422,47 +494,131 @@ struct vp_model {
   float eps;
   std::vector<vp_layer_desc> layers;
   vp_head_desc head;
-  int max_groups;
   int zmax;
+  std::vector<Phase> phases[4];  // per NT: 4 phases per layer (in, out, gate+up, down), then the head
+  Needs needs[4];
 };
 
 namespace {
 
+// The pass's phases at NT n-tiles.  Block 2l (mixer of layer l) = phases 4l, 4l + 1; block 2l + 1
+// (its MLP) = phases 4l + 2, 4l + 3; the head is the last phase.
+void build_pass(vp_model* md, int NT) {
+  const int H = md->hidden, I = md->inter;
+  std::vector<Phase>& out = md->phases[NT - 1];
+  Needs& nd = md->needs[NT - 1];
+  out.clear();
+  for (int l = 0; l < (int)md->layers.size(); ++l) {
+    const vp_layer_desc& d = md->layers[l];
+    PhaseSpec in;  // mixer in-projection (GDN in, or attention q + kv): z = bf16(u[:, :k_out])
+    in.fmt = kFmtFp8;
+    in.w0 = d.w_in;
+    in.s0 = d.s_in;
+    in.rows0 = d.n_in;
+    if (d.kind == VP_LAYER_ATTN) {
+      in.w1 = d.w_kv;
+      in.s1 = d.s_kv;
+      in.rows1 = d.n_kv;
+    }
+    in.K = H;
+    in.epi = kEpiZ;
+    in.x_src = kBufH;
+    in.x_ld = H;
+    in.x_rms = 1;
+    in.out = kBufZ;
+    in.out_ld = d.k_out;
+    in.out_cols = d.k_out;
+    out.push_back(make_phase(in, NT));
+    PhaseSpec o;  // mixer out-projection + residual
+    o.fmt = kFmtFp8;
+    o.w0 = d.w_out;
+    o.s0 = d.s_out;
+    o.rows0 = H;
+    o.K = d.k_out;
+    o.epi = kEpiResid;
+    o.x_src = kBufZ;
+    o.x_ld = d.k_out;
+    o.out = kBufH;
+    o.out_ld = H;
+    o.trace_slot = 2 * l;
+    out.push_back(make_phase(o, NT));
+    PhaseSpec gu;  // MLP gate + up, interleaved strips -> a = bf16(silu(gate) * up)
+    gu.fmt = kFmtNvfp4;
+    gu.layout = kInterleaved;
+    gu.w0 = d.w_gate;
+    gu.s0 = d.ts_gate;
+    gu.w1 = d.w_up;
+    gu.s1 = d.ts_up;
+    gu.rows0 = I;
+    gu.K = H;
+    gu.epi = kEpiSilu;
+    gu.x_src = kBufH;
+    gu.x_ld = H;
+    gu.x_rms = 1;
+    gu.out = kBufA;
+    gu.out_ld = I;
+    out.push_back(make_phase(gu, NT));
+    PhaseSpec dn;  // MLP down + residual
+    dn.fmt = kFmtNvfp4;
+    dn.w0 = d.w_down;
+    dn.s0 = d.ts_down;
+    dn.rows0 = H;
+    dn.K = I;
+    dn.epi = kEpiResid;
+    dn.x_src = kBufA;
+    dn.x_ld = I;
+    dn.out = kBufH;
+    dn.out_ld = H;
+    dn.trace_slot = 2 * l + 1;
+    out.push_back(make_phase(dn, NT));
+  }
+  PhaseSpec hd;
+  hd.fmt = kFmtNvfp4;
+  hd.w0 = md->head.w;
+  hd.s0 = md->head.ts;
+  hd.rows0 = md->head.vocab;
+  hd.K = H;
+  hd.epi = kEpiHead;
+  hd.x_src = kBufH;
+  hd.x_ld = H;
+  hd.x_rms = 1;
+  hd.out = kBufLogits;
+  hd.out_ld = md->head.vocab;
+  out.push_back(make_phase(hd, NT));
+  nd = Needs();
+  for (const Phase& ph : out) nd.add(ph);
+}
+
 struct PassWs {
-  GemmWs g;
-  float* inv_rms;
-  uint16_t* h;
-  uint16_t* z;
-  uint16_t* a;
-  size_t counters_bytes;
-  size_t total;
+  WsLayout L;
+  size_t h, z, a, total;
 };
 
-PassWs carve_pass_ws(const vp_model* md, int M, void* ws) {
+PassWs pass_ws(const vp_model* md, int M) {
+  const int NT = nt_of(M);
   PassWs w;
-  const int mt = (M + 7) / 8;
-  w.g = carve_gemm_ws(ws, md->max_groups, mt);
-  size_t off = w.g.L.total;
-  const size_t inv_off = off;
-  off = align_up(off + sizeof(float) * kMaxM, 256);
-  const size_t h_off = off;
+  w.L = ws_layout(md->needs[NT - 1].max_rb, md->needs[NT - 1].max_slots, NT);
+  size_t off = w.L.total;
+  w.h = off;
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->hidden, 256);
-  const size_t z_off = off;
+  w.z = off;
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->zmax, 256);
-  const size_t a_off = off;
+  w.a = off;
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->inter, 256);
-  uint8_t* b = (uint8_t*)ws;
-  w.inv_rms = (float*)(b + inv_off);
-  w.h = (uint16_t*)(b + h_off);
-  w.z = (uint16_t*)(b + z_off);
-  w.a = (uint16_t*)(b + a_off);
-  w.counters_bytes = w.g.L.group_aux;
   w.total = off;
   return w;
 }
 
 bool fp8_ok(const void* w, int N, int K) { return w && aligned(w, 16) && vp_packed_bytes_fp8(N, K) > 0; }
 bool nvfp4_ok(const void* w, int N, int K) { return w && aligned(w, 16) && vp_packed_bytes_nvfp4(N, K) > 0; }
+
+vp_status pass_args_ok(const vp_model* md, int M, void* ws, size_t ws_bytes) {
+  if (!md || !ws) return VP_ERR_INVALID_ARG;
+  if (M < 8 || M > kMaxM || M % 8) return VP_ERR_SHAPE;
+  if (!aligned(ws, 256)) return VP_ERR_ALIGNMENT;
+  if (ws_bytes < pass_ws(md, M).total) return VP_ERR_WORKSPACE;
+  return VP_OK;
+}
 
 }  // namespace
 
@@ -471,9 +627,8 @@ extern "C" {
 vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_desc* layers, int n_layers,
                           const vp_head_desc* head, vp_model** out) {
   if (!layers || !head || !out || n_layers < 1 || !(rms_eps >= 0.0f)) return VP_ERR_INVALID_ARG;
-  if (hidden < 64 || hidden % 64 || inter < 64 || inter % 64) return VP_ERR_SHAPE;
-  int max_groups = ceil_div(head->vocab, kSlabRows);
-  int zmax = 64;
+  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return VP_ERR_SHAPE;
+  int zmax = 128;
   for (int l = 0; l < n_layers; ++l) {
     const vp_layer_desc& d = layers[l];
     if (d.kind != VP_LAYER_GDN && d.kind != VP_LAYER_ATTN) return VP_ERR_INVALID_ARG;
@@ -483,13 +638,9 @@ vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_d
     if (d.kind == VP_LAYER_GDN && (d.w_kv || d.n_kv)) return VP_ERR_INVALID_ARG;
     if (!nvfp4_ok(d.w_gate, inter, hidden) || !nvfp4_ok(d.w_up, inter, hidden) || !nvfp4_ok(d.w_down, hidden, inter))
       return VP_ERR_SHAPE;
-    int gin = ceil_div(d.n_in, kSlabRows) + (d.kind == VP_LAYER_ATTN ? ceil_div(d.n_kv, kSlabRows) : 0);
-    if (gin > max_groups) max_groups = gin;
     if (d.k_out > zmax) zmax = d.k_out;
   }
   if (!nvfp4_ok(head->w, head->vocab, hidden)) return VP_ERR_SHAPE;
-  max_groups = std::max(max_groups, ceil_div(inter, 128));
-  max_groups = std::max(max_groups, ceil_div(hidden, kSlabRows));
   vp_model* m = new (std::nothrow) vp_model;
   if (!m) return VP_ERR_INVALID_ARG;
   m->hidden = hidden;
@@ -497,8 +648,8 @@ vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_d
   m->eps = rms_eps;
   m->layers.assign(layers, layers + n_layers);
   m->head = *head;
-  m->max_groups = max_groups;
   m->zmax = zmax;
+  for (int nt = 1; nt <= 4; ++nt) build_pass(m, nt);
   *out = m;
   return VP_OK;
 }
@@ -507,107 +658,12 @@ void vp_model_destroy(vp_model* model) { delete model; }
 
 size_t vp_pass_workspace_bytes(const vp_model* model, int M) {
   if (!model || M < 8 || M > kMaxM || M % 8) return 0;
-  return carve_pass_ws(model, M, nullptr).total;
+  return pass_ws(model, M).total;
 }
 
-int vp_pass_launch_count(const vp_model* model) { return model ? 2 + 4 * (int)model->layers.size() : 0; }
-
-}  // extern "C"
-
-namespace {
-
-// Enqueues blocks [b0, b1) of the pass (block 2l = mixer of layer l, 2l + 1 = MLP of layer l) on
-// the residual stream h (bf16 [M][hidden], updated in place).  inv_rms must hold 1/rms of h's rows
-// on entry and holds 1/rms of the result on exit.  Optional trace: h after each block.
-vp_status enqueue_blocks(const vp_model* md, const PassWs& w, uint16_t* h, int M, int b0, int b1, void* trace,
-                         int sms, cudaStream_t s) {
-  const int H = md->hidden, I = md->inter;
-  const size_t hbytes = sizeof(uint16_t) * (size_t)M * H;
-  vp_status st;
-  cudaError_t e;
-  for (int b = b0; b < b1; ++b) {
-    const vp_layer_desc& d = md->layers[b / 2];
-    if ((b & 1) == 0) {
-      // mixer in-projection (GDN in, or attention q + kv): z = bf16(first k_out columns of RMSNorm(h) W^T)
-      GemmParams p = single(d.w_in, d.n_in, H, M, d.s_in);
-      if (d.kind == VP_LAYER_ATTN) {
-        p.w[1] = (const uint8_t*)d.w_kv;
-        p.seg_rows[1] = d.n_kv;
-        p.wscale[1] = d.s_kv;
-        p.n_groups = p.seg0_groups + ceil_div(d.n_kv, kSlabRows);
-        p.units = (long long)p.n_groups * p.nq;
-      }
-      p.x = h;
-      p.x_ld = H;
-      p.x_rowscale = w.inv_rms;
-      p.epi = kEpiBf16Prefix;
-      p.out = w.z;
-      p.out_ld = d.k_out;
-      p.out_cols = d.k_out;
-      fill_ws(p, w.g);
-      if ((st = launch(kFmtFp8, p, sms, s, true)) != VP_OK) return st;
-      // mixer out-projection + residual: h = bf16(h + z W_out^T); 1/rms(h) for the next block
-      p = single(d.w_out, H, d.k_out, M, d.s_out);
-      p.x = w.z;
-      p.x_ld = d.k_out;
-      p.epi = kEpiResid;
-      p.resid = h;
-      p.resid_ld = H;
-      p.resid_cols = H;
-      p.rms_out = w.inv_rms;
-      p.rms_eps = md->eps;
-      fill_ws(p, w.g);
-      if ((st = launch(kFmtFp8, p, sms, s, true)) != VP_OK) return st;
-    } else {
-      // MLP gate + up (interleaved row-blocks) -> a = bf16(silu(gate) * up)
-      GemmParams p = single(d.w_gate, I, H, M, d.ts_gate);
-      p.w[1] = (const uint8_t*)d.w_up;
-      p.seg_rows[1] = I;
-      p.wscale[1] = d.ts_up;
-      p.interleave = 1;
-      p.n_groups = ceil_div(I, 128);
-      p.seg0_groups = p.n_groups;
-      p.units = (long long)p.n_groups * p.nq;
-      p.x = h;
-      p.x_ld = H;
-      p.x_rowscale = w.inv_rms;
-      p.epi = kEpiSiluMul;
-      p.out = w.a;
-      p.out_ld = I;
-      fill_ws(p, w.g);
-      if ((st = launch(kFmtNvfp4, p, sms, s, true)) != VP_OK) return st;
-      // MLP down + residual
-      p = single(d.w_down, H, I, M, d.ts_down);
-      p.x = w.a;
-      p.x_ld = I;
-      p.epi = kEpiResid;
-      p.resid = h;
-      p.resid_ld = H;
-      p.resid_cols = H;
-      p.rms_out = w.inv_rms;
-      p.rms_eps = md->eps;
-      fill_ws(p, w.g);
-      if ((st = launch(kFmtNvfp4, p, sms, s, true)) != VP_OK) return st;
-    }
-    if (trace &&
-        (e = cudaMemcpyAsync((uint8_t*)trace + (size_t)(b - b0) * hbytes, h, hbytes, cudaMemcpyDeviceToDevice, s)) !=
-            cudaSuccess)
-      return cuda_fail(e);
-  }
-  return VP_OK;
+int vp_pass_launch_count(const vp_model* model) {
+  return model ? program_launches((int)model->phases[0].size()) : 0;
 }
-
-vp_status pass_args_ok(const vp_model* md, int M, void* ws, size_t ws_bytes) {
-  if (!md || !ws) return VP_ERR_INVALID_ARG;
-  if (M < 8 || M > kMaxM || M % 8) return VP_ERR_SHAPE;
-  if (!aligned(ws, 256)) return VP_ERR_ALIGNMENT;
-  if (ws_bytes < vp_pass_workspace_bytes(md, M)) return VP_ERR_WORKSPACE;
-  return VP_OK;
-}
-
-}  // namespace
-
-extern "C" {
 
 vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
                          int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, size_t ws_bytes,
@@ -620,27 +676,27 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
     return VP_ERR_ALIGNMENT;
   int sms = 0;
   if ((st = device_sms(&sms)) != VP_OK) return st;
+  const std::vector<Phase>& phases = md->phases[nt_of(M) - 1];
+  for (const Phase& ph : phases)
+    if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
   cudaStream_t s = (cudaStream_t)stream;
-  const int H = md->hidden;
-  const PassWs w = carve_pass_ws(md, M, ws);
-  cudaError_t e;
-  pass_prep_kernel<<<M, 256, 0, s>>>((const uint16_t*)x0, w.h, H, md->eps, w.inv_rms);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  if ((st = enqueue_blocks(md, w, w.h, M, 0, 2 * (int)md->layers.size(), trace, sms, s)) != VP_OK) return st;
-  // head + argmax + acceptance on RMSNorm(h)
-  GemmParams p = single(md->head.w, md->head.vocab, H, M, md->head.ts);
-  p.x = w.h;
-  p.x_ld = H;
-  p.x_rowscale = w.inv_rms;
-  p.epi = kEpiHead;
-  p.pending = pending;
-  p.argmax = argmax;
-  p.n_commit = n_commit;
-  p.committed = committed;
-  p.logits = logits;
-  p.logits_ld = md->head.vocab;
-  fill_ws(p, w.g);
-  return launch(kFmtNvfp4, p, sms, s, true);
+  const PassWs w = pass_ws(md, M);
+  uint8_t* b = (uint8_t*)ws;
+  Io io = make_io(ws, w.L);
+  io.buf[kBufH] = b + w.h;
+  io.buf[kBufZ] = b + w.z;
+  io.buf[kBufA] = b + w.a;
+  io.buf[kBufLogits] = logits;
+  io.buf[kBufTrace] = trace;
+  io.trace_stride = (size_t)M * md->hidden;
+  io.pending = pending;
+  io.argmax = argmax;
+  io.n_commit = n_commit;
+  io.committed = committed;
+  cudaError_t e = cudaMemcpyAsync(io.buf[kBufH], x0, sizeof(uint16_t) * (size_t)M * md->hidden,
+                                  cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return run_phases(phases, M, md->eps, io, sms, s);
 }
 
 vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, int block_end, void* trace, void* ws,
@@ -651,15 +707,24 @@ vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, 
   const int nb = 2 * (int)md->layers.size();
   if (block_begin < 0 || block_end > nb || block_begin > block_end) return VP_ERR_INVALID_ARG;
   if (!aligned(h, 16) || (trace && !aligned(trace, 16))) return VP_ERR_ALIGNMENT;
+  if (block_begin == block_end) return VP_OK;
   int sms = 0;
   if ((st = device_sms(&sms)) != VP_OK) return st;
-  cudaStream_t s = (cudaStream_t)stream;
-  const PassWs w = carve_pass_ws(md, M, ws);
-  cudaError_t e;
-  // 1/rms of the incoming rows (the copy onto itself is a no-op)
-  pass_prep_kernel<<<M, 256, 0, s>>>((const uint16_t*)h, (uint16_t*)h, md->hidden, md->eps, w.inv_rms);
-  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-  return enqueue_blocks(md, w, (uint16_t*)h, M, block_begin, block_end, trace, sms, s);
+  const std::vector<Phase>& all = md->phases[nt_of(M) - 1];
+  std::vector<Phase> phases(all.begin() + 2 * block_begin, all.begin() + 2 * block_end);
+  for (Phase& ph : phases) {
+    if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
+    if (ph.trace_slot >= 0) ph.trace_slot -= block_begin;
+  }
+  const PassWs w = pass_ws(md, M);
+  uint8_t* b = (uint8_t*)ws;
+  Io io = make_io(ws, w.L);
+  io.buf[kBufH] = h;
+  io.buf[kBufZ] = b + w.z;
+  io.buf[kBufA] = b + w.a;
+  io.buf[kBufTrace] = trace;
+  io.trace_stride = (size_t)M * md->hidden;
+  return run_phases(phases, M, md->eps, io, sms, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,725 @@
+// The streaming executor of the verify pass: one persistent kernel that runs a program of
+// weight-streaming GEMM phases  Y = X W^T  (M = 1..32 activation rows, NVFP4 or FP8 weights, fp32
+// accumulation) with their fused epilogues, separated by grid-wide barriers.
+//
+// Sources: "lithos-metal: per-layer megakernels for Qwen3.8-27B on an M5 Max" -- "What one token
+// costs the bus" (the NVFP4/FP8 weight groups a pass streams), "Formats, and what runs where"
+// (NVFP4 = E2M1 code x E4M3 scale per 16 weights x fp32 tensor scale; weight-only arithmetic with
+// BF16 activations and wide accumulation) and "The megakernel is per layer, not per step" (greedy
+// acceptance); "Beating Splash on an M5 Max" -- "The kernels were not the gap" (split-K for narrow
+// projections) and "The bugs a second reviewer found" (one argmax tie rule everywhere).
+//
+// GB300 design (not the pages' Metal tiles):
+//  * One CTA per SM, 16 independent warps.  Each phase's units (16-row block x one K chunk, 2304 B
+//    NVFP4 / 2048 B FP8) are split into equal contiguous ranges, one per warp.  A warp streams its
+//    range through a private 3-slot ring with 1-D bulk copies that its lane 0 issues (evict-first),
+//    so no warp ever waits for another inside a phase, and it keeps prefetching across phase ends:
+//    the next phase's first units are in flight while the grid barrier and the activation staging
+//    of the phase boundary run.
+//  * Dequantisation is exact in f16 (E2M1 x E4M3 products have <= 5 significant bits), done in
+//    registers straight into mma.sync.m16n8k16 A fragments; the activations (B) are staged once per
+//    phase as f16 fragments scaled per row by an exact power of two, which un-scales the fp32
+//    accumulators.  At M <= 8 a 16x16 weight tile costs one MMA per 8 tokens, so the SM's issue
+//    slots, not the tensor pipe, carry the dequantisation (about 8 TB/s-equivalent per GPU).
+//  * K slices: when a phase's activations do not fit shared memory, its K chunks are cut into ks
+//    slices with CTAs assigned in proportion.  Row blocks that several warps share are reduced by
+//    the last contributor (atomic counter, no waiting) in a fixed order, so every result is
+//    bit-reproducible; it then runs the epilogue.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace vp {
+
+enum : int { kStatusTimeout = 6 };
+
+struct SmemMisc {
+  uint64_t full[kWarps][kSlots];
+  float red[kThreads / 16];
+  int xexp[kMaxM];
+  float xscale[kMaxM];
+  int tok[kMaxM];
+  int abort;
+  int flag;
+};
+static_assert(sizeof(SmemMisc) <= (size_t)kMiscBytes, "SmemMisc exceeds its shared-memory budget");
+static_assert(kSlotBytes >= 2 * 1152 && kSlotBytes >= 2 * 1024, "a slot holds one unit");
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+__device__ __forceinline__ uint16_t bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// ---------------------------------------------------------------- argmax helpers
+// Lowest index among the largest values; callers map NaN to -inf first, and -0 == +0.
+__device__ __forceinline__ bool am_better(float v, int i, float bv, int bi) { return v > bv || (v == bv && i < bi); }
+__device__ __forceinline__ void am_shfl_xor(float& v, int& i, int off) {
+  const float v2 = __shfl_xor_sync(0xffffffffu, v, off);
+  const int i2 = __shfl_xor_sync(0xffffffffu, i, off);
+  if (am_better(v2, i2, v, i)) {
+    v = v2;
+    i = i2;
+  }
+}
+// Greedy acceptance of lane l given the target tokens tok[8l .. 8l + 7] (the anchor pending[8l] is
+// not compared): the longest prefix of drafts equal to the target's tokens plus the target's token
+// after it.
+__device__ __forceinline__ void accept_lane(int l, const int* tok, const int32_t* pending, int32_t* n_commit,
+                                            int32_t* committed) {
+  int acc = 0;
+  while (acc < 7 && tok[8 * l + acc] == pending[8 * l + acc + 1]) ++acc;
+  n_commit[l] = acc + 1;
+  for (int j = 0; j < 8; ++j) committed[8 * l + j] = j <= acc ? tok[8 * l + j] : -1;
+}
+
+// ---------------------------------------------------------------- phase geometry
+// K slice s of a phase: chunks [kc0, kc0 + kcn), CTAs [cta0, cta0 + ctan) in proportion to the
+// chunks, U = RB * kcn units (row-block major) over W = min(16 ctan, U) warps, so that every warp
+// with a range owns at least one unit (the owners of a row block's units are then exactly its
+// contributors, and consecutive); the slice's other warps idle.
+struct Slice {
+  int kc0, kcn, cta0, ctan, U, W;
+};
+__device__ __forceinline__ Slice slice_geom(const Phase& ph, int G, int s) {
+  Slice S;
+  const int kc0 = (int)((long long)s * ph.KC / ph.ks), kc1 = (int)((long long)(s + 1) * ph.KC / ph.ks);
+  const int c0 = (int)(((long long)G * kc0 + ph.KC / 2) / ph.KC);
+  const int c1 = s + 1 == ph.ks ? G : (int)(((long long)G * kc1 + ph.KC / 2) / ph.KC);
+  S.kc0 = kc0;
+  S.kcn = kc1 - kc0;
+  S.cta0 = c0;
+  S.ctan = c1 - c0;
+  S.U = ph.RB * S.kcn;
+  S.W = min(kWarps * S.ctan, S.U);
+  return S;
+}
+__device__ __forceinline__ int slice_of_cta(const Phase& ph, int G, int cta, Slice& S) {
+  for (int s = 0; s < ph.ks; ++s) {
+    S = slice_geom(ph, G, s);
+    if (cta < S.cta0 + S.ctan) return s;
+  }
+  return ph.ks - 1;
+}
+// Warp w of a slice owns units [range_begin(w), range_begin(w + 1)); owner(u) inverts it.
+__device__ __forceinline__ int range_begin(const Slice& S, int w) {
+  return w >= S.W ? S.U : (int)((long long)w * S.U / S.W);
+}
+__device__ __forceinline__ int owner(const Slice& S, int u) { return (int)(((long long)(u + 1) * S.W - 1) / S.U); }
+
+// ---------------------------------------------------------------- weight producer (lane 0 of a warp)
+// Walks the warp's units across all phases of the program, in consumption order.
+struct Cursor {
+  int p, u, ue, kc0, kcn;
+};
+__device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, int G, int cta, int warp) {
+  while (c.p < prog.n) {
+    const Phase& ph = prog.ph[c.p];
+    Slice S;
+    slice_of_cta(ph, G, cta, S);
+    const int w = (cta - S.cta0) * kWarps + warp;
+    c.u = range_begin(S, w);
+    c.ue = range_begin(S, w + 1);
+    c.kc0 = S.kc0;
+    c.kcn = S.kcn;
+    if (c.u < c.ue) return;
+    ++c.p;
+  }
+}
+__device__ __forceinline__ void cursor_next(Cursor& c, const Program& prog, int G, int cta, int warp) {
+  if (++c.u == c.ue) {
+    ++c.p;
+    cursor_seek(c, prog, G, cta, warp);
+  }
+}
+// Global address and size of the cursor's unit: one contiguous copy (plain), or two strips.
+struct UnitSrc {
+  const uint8_t* a;
+  const uint8_t* b;  // second strip (interleaved), else nullptr
+  uint32_t bytes;    // per source
+};
+__device__ __forceinline__ UnitSrc unit_src(const Program& prog, const Cursor& c) {
+  const Phase& ph = prog.ph[c.p];
+  const int rb = c.u / c.kcn, kc = c.kc0 + c.u % c.kcn;
+  const int sb = strip_bytes(ph.fmt);
+  UnitSrc r;
+  if (ph.layout == kPlain) {
+    const bool s1 = rb >= ph.rb1;
+    r.a = (s1 ? ph.w1 : ph.w0) + strip_offset(ph.fmt, ph.KC, s1 ? rb - ph.rb1 : rb, kc, 0);
+    r.b = nullptr;
+    r.bytes = 2u * sb;
+  } else {
+    const size_t off = strip_offset(ph.fmt, ph.KC, rb >> 1, kc, rb & 1);
+    r.a = ph.w0 + off;
+    r.b = ph.w1 + off;
+    r.bytes = (uint32_t)sb;
+  }
+  return r;
+}
+// Bulk copy of the cursor's unit into the slot at shared address dst, completing on bar.
+__device__ __forceinline__ void issue_unit(const Program& prog, const Cursor& c, uint32_t dst, uint64_t* bar,
+                                           uint64_t pol) {
+  const UnitSrc r = unit_src(prog, c);
+  const uint32_t b = smem_addr(bar);
+  mbar_arrive_expect_tx(bar, r.b ? 2u * r.bytes : r.bytes);
+  bulk_g2s(dst, r.a, r.bytes, b, pol);
+  if (r.b) bulk_g2s(dst + r.bytes, r.b, r.bytes, b, pol);
+}
+
+// ---------------------------------------------------------------- activation staging
+// Shared layout of the K slice's activations: for every pair of 16-wide k steps p, n-tile j and lane
+// (g, c): 16 bytes = the f16 values of token 8j + g at k = 32p + 4c .. +3 (step 2p) and
+// 32p + 16 + 4c .. +3 (step 2p + 1) -- exactly the thread's two B fragments.
+template <int NT>
+__device__ __forceinline__ uint32_t xfrag_offset(int p, int n, int c) {
+  return (uint32_t)((((p * NT + (n >> 3)) * 32 + (n & 7) * 4 + c) * 16));
+}
+
+__device__ __forceinline__ float sumsq8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = bf16_bits_to_float(w[i] & 0xFFFFu), b = bf16_bits_to_float(w[i] >> 16);
+    s = fmaf(a, a, s);
+    s = fmaf(b, b, s);
+  }
+  return s;
+}
+
+// Reduces x over the T consecutive threads of each row (T a multiple of 16) in a fixed order; every
+// thread of the row gets the result.
+__device__ __forceinline__ float row_reduce(float x, int T, bool is_max, float* red) {
+#pragma unroll
+  for (int o = 8; o; o >>= 1) {
+    const float y = __shfl_xor_sync(0xffffffffu, x, o);
+    x = is_max ? fmaxf(x, y) : x + y;
+  }
+  const int tid = threadIdx.x;
+  if ((tid & 15) == 0) red[tid >> 4] = x;
+  __syncthreads();
+  const int segs = T >> 4, s0 = (tid / T) * segs;
+  float r = red[s0];
+  for (int s = 1; s < segs; ++s) r = is_max ? fmaxf(r, red[s0 + s]) : r + red[s0 + s];
+  __syncthreads();
+  return r;
+}
+
+// Exponent e of a row whose largest magnitude is mx: the row enters the tensor core as x * 2^-e,
+// below 2^15 (f16 holds every bf16 value exactly there, down to 2^-24 of that scale).
+__device__ __forceinline__ int exp_of_max(float mx) {
+  if (!(mx > 0.0f) || !(mx < INFINITY)) return 0;
+  int ex;
+  frexpf(mx, &ex);  // mx in [2^(ex-1), 2^ex)
+  return ex - 1 - 14;
+}
+
+// Stages the CTA's K slice [kbase, kbase + Ks) of the phase's activation rows: x, or
+// bf16(RMSNorm(x)) (unit weight) when the phase asks for it, with the row statistics taken over
+// the whole row.  Thread t handles row n = t / T, 16-byte chunks i, i + T, ... of the slice.
+template <int NT>
+__device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, const Io& io, int kbase, int Ks,
+                                     uint8_t* xs, SmemMisc& sm) {
+  const int tid = threadIdx.x, M = prog.M;
+  const int Mp = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32;
+  const int T = kThreads / Mp, n = tid / T, i = tid % T;
+  const bool active = n < M;
+  const uint16_t* row = static_cast<const uint16_t*>(io.buf[ph.x_src]) + (size_t)(active ? n : 0) * ph.x_ld;
+  const int nch = Ks >> 3;
+  const uint32_t xb = smem_addr(xs);
+
+  if (M < 8 * NT) {  // token rows M .. 8 NT - 1 are zero
+    const int per_row = Ks >> 3, zrows = 8 * NT - M;
+    for (int e = tid; e < zrows * per_row; e += kThreads) {
+      const int r = M + e / per_row, q = e % per_row;
+      sts128(xb + xfrag_offset<NT>(q >> 2, r, q & 3), make_uint4(0u, 0u, 0u, 0u));
+    }
+  }
+  // All of the thread's chunks are loaded at once (one memory round trip).
+  uint4 v[16];
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const int q = i + T * m;
+    v[m] = (active && q < nch) ? ldcg128(row + kbase + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  // Row exponent e (the row enters the tensor core as x * 2^-e, below 2^15).  RMSNorm output has
+  // |r| <= sqrt(K) (no element exceeds the root of the row's sum of squares; 1% covers the fp32
+  // 1/rms and the bf16 rounding), so those rows take the exponent of that bound and only their sum
+  // of squares is reduced; other rows take the exponent of their largest magnitude.
+  const bool rms = ph.x_rms != 0;
+  float stat = 0.0f;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float a = __uint_as_float(w[k] << 16), b = __uint_as_float(w[k] & 0xFFFF0000u);
+      stat = rms ? fmaf(b, b, fmaf(a, a, stat)) : fmaxf(stat, fmaxf(fabsf(a), fabsf(b)));
+    }
+  }
+  float inv = 1.0f;
+  int e;
+  if (rms) {
+    if (Ks < ph.K && active)
+      for (int q = i; q < (ph.K >> 3); q += T) {
+        const int k = 8 * q;
+        if (k < kbase || k >= kbase + Ks) stat += sumsq8(ldcg128(row + k));
+      }
+    const float tot = row_reduce(stat, T, false, sm.red);
+    inv = 1.0f / sqrtf(tot / (float)ph.K + prog.eps);
+    e = exp_of_max(1.01f * sqrtf((float)ph.K));
+  } else {
+    e = exp_of_max(row_reduce(stat, T, true, sm.red));
+  }
+  if (active && i == 0) {
+    sm.xexp[n] = e;
+    sm.xscale[n] = pow2f(e);
+  }
+  if (tid >= M && tid < kMaxM) sm.xscale[tid] = 0.0f;
+  // x * 2^-e exactly (two power-of-two steps when 2^-e is not a normal float); for RMSNorm the
+  // 2^-e folds into 1/rms: bf16(x * inv) * 2^-e == bf16(x * (inv * 2^-e)) (no under/overflow).
+  const int ne = -e;
+  float sc1 = ne > 127 ? pow2f(127) : ne < -126 ? pow2f(-126) : pow2f(ne);
+  const float sc2 = ne > 127 ? pow2f(ne - 127) : ne < -126 ? pow2f(ne + 126) : 1.0f;
+  if (rms) sc1 *= inv;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) {
+    const int q = i + T * m;
+    if (!(active && q < nch)) continue;
+    const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+    uint32_t h[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float a = __uint_as_float(w[k] << 16) * sc1, b = __uint_as_float(w[k] & 0xFFFF0000u) * sc1;
+      if (rms) {
+        const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);  // the RMSNorm output, rounded once
+        a = __low2float(r);
+        b = __high2float(r);
+      } else {
+        a *= sc2;
+        b *= sc2;
+      }
+      const __half2 hh = __floats2half2_rn(a, b);
+      h[k] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    const int k0 = 8 * q, st = k0 >> 4, hf = (k0 >> 3) & 1;
+    const uint32_t ad = xb + xfrag_offset<NT>(st >> 1, n, 2 * hf) + (st & 1) * 8;
+    sts64(ad, h[0], h[1]);
+    sts64(ad + 16, h[2], h[3]);
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- one unit of a warp
+// acc[j] (16 rows x 8 tokens, the mma.sync C fragment): rows g, g + 8 of the row block, tokens
+// 8j + 2c, 8j + 2c + 1.  With one n-tile, odd k steps accumulate into acc2 (two independent MMA
+// chains); with more, the n-tiles are the independent chains.  ua: the unit's slot; xa: this lane's fragments of the unit's first k-step pair.
+template <int NT>
+__device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4], float (&acc2)[NT][4]) {
+  const int g = lane >> 2;
+  const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
+  const uint4 c1a = lds128(ua + 1152 + lane * 16), c1b = lds128(ua + 1152 + 512 + lane * 16);
+  const uint4 s0 = lds128(ua + 1024 + g * 16), s1 = lds128(ua + 1152 + 1024 + g * 16);
+  const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+  const uint32_t w1[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
+  const uint32_t sw0[4] = {s0.x, s0.y, s0.z, s0.w}, sw1[4] = {s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    uint4 b[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) b[j] = lds128(xa + (p * NT + j) * 512);
+    // block scales of steps 2p, 2p + 1 for rows g and g + 8
+    const uint32_t sc0 = e4m3x2_to_f16x2((p & 1) ? (sw0[p >> 1] >> 16) : sw0[p >> 1]);
+    const uint32_t sc1 = e4m3x2_to_f16x2((p & 1) ? (sw1[p >> 1] >> 16) : sw1[p >> 1]);
+    uint32_t o0[4], o1[4];
+    e2m1x8_to_f16x2x4(w0[p], o0);
+    e2m1x8_to_f16x2x4(w1[p], o1);
+    {
+      const uint32_t d0 = dup_lo16(sc0), d1 = dup_lo16(sc1);
+      const uint32_t a0 = hmul2_u32(o0[0], d0), a1 = hmul2_u32(o1[0], d1);
+      const uint32_t a2 = hmul2_u32(o0[1], d0), a3 = hmul2_u32(o1[1], d1);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) mma_f16_16816(acc[j], a0, a1, a2, a3, b[j].x, b[j].y);
+    }
+    {
+      const uint32_t d0 = dup_hi16(sc0), d1 = dup_hi16(sc1);
+      const uint32_t a0 = hmul2_u32(o0[2], d0), a1 = hmul2_u32(o1[2], d1);
+      const uint32_t a2 = hmul2_u32(o0[3], d0), a3 = hmul2_u32(o1[3], d1);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) mma_f16_16816(NT == 1 ? acc2[j] : acc[j], a0, a1, a2, a3, b[j].z, b[j].w);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void unit_fp8(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4], float (&acc2)[NT][4]) {
+  const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
+  const uint4 c1a = lds128(ua + 1024 + lane * 16), c1b = lds128(ua + 1024 + 512 + lane * 16);
+  const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+  const uint32_t w1[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    uint4 b[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) b[j] = lds128(xa + (p * NT + j) * 512);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t a0, a1, a2, a3;
+      e4m3x4_to_f16x2x2(w0[2 * p + h], a0, a2);
+      e4m3x4_to_f16x2x2(w1[2 * p + h], a1, a3);
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+        mma_f16_16816((NT == 1 && h) ? acc2[j] : acc[j], a0, a1, a2, a3, h ? b[j].z : b[j].x, h ? b[j].w : b[j].y);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- epilogues
+template <int NT>
+struct HeadBest {
+  float v[NT][2];
+  int i[NT][2];
+};
+
+// Residual inputs h[t][n] of the thread's elements of row block rb (plain layout), element
+// [j][2r + h] = row g + 8r, token 8j + 2c + h.
+template <int NT>
+__device__ __forceinline__ void load_resid(const Phase& ph, const Io& io, int M, int rb, uint16_t (&hold)[NT][4],
+                                           int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  const uint16_t* hp = static_cast<const uint16_t*>(io.buf[ph.out]);
+  const int nb = rb * kRowBlock + g;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int t = 8 * j + 2 * c + h;
+        unsigned short b = 0;
+        if (t < M) asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(b) : "l"(hp + (size_t)t * ph.out_ld + nb + 8 * r));
+        hold[j][2 * r + h] = b;
+      }
+}
+
+// v: the finished row block (fp32, un-scaled activations, before the weight scale).
+template <int NT>
+__device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const float (&v)[NT][4],
+                         const uint16_t (&hold)[NT][4], HeadBest<NT>& hb, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  if (ph.layout == kInterleaved) {  // a = bf16(silu(s0 * gate) * s1 * up)
+    uint16_t* out = static_cast<uint16_t*>(io.buf[ph.out]);
+    const int f = rb * kStripRows + g;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = 8 * j + 2 * c + h;
+        if (t >= M) continue;
+        const float gt = ph.s0 * v[j][h], up = ph.s1 * v[j][2 + h];
+        out[(size_t)t * ph.out_ld + f] = bf16_bits(gt / (1.0f + expf(-gt)) * up);
+      }
+    return;
+  }
+  const bool seg1 = rb >= ph.rb1;
+  const float s = seg1 ? ph.s1 : ph.s0;
+  const int nb = (seg1 ? rb - ph.rb1 : rb) * kRowBlock + g;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = 8 * j + 2 * c + h;
+      if (t >= M) continue;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int n = nb + 8 * r;
+        const float val = s * v[j][2 * r + h];
+        const size_t o = (size_t)t * ph.out_ld + n;
+        switch (ph.epi) {
+          case kEpiF32:
+            static_cast<float*>(io.buf[ph.out])[o] = val;
+            break;
+          case kEpiZ:
+            if (!seg1 && n < ph.out_cols) static_cast<uint16_t*>(io.buf[ph.out])[o] = bf16_bits(val);
+            break;
+          case kEpiResid: {
+            uint16_t* hp = static_cast<uint16_t*>(io.buf[ph.out]);
+            const uint16_t nv = bf16_bits(bf16_bits_to_float(hold[j][2 * r + h]) + val);
+            hp[o] = nv;
+            if (ph.trace_slot >= 0 && io.buf[kBufTrace])
+              static_cast<uint16_t*>(io.buf[kBufTrace])[(size_t)ph.trace_slot * io.trace_stride + o] = nv;
+            break;
+          }
+          case kEpiHead: {
+            if (io.buf[kBufLogits]) static_cast<float*>(io.buf[kBufLogits])[o] = val;
+            const float key = isnan(val) ? -INFINITY : val;
+            if (am_better(key, n, hb.v[j][h], hb.i[j][h])) {
+              hb.v[j][h] = key;
+              hb.i[j][h] = n;
+            }
+            break;
+          }
+          default:
+            break;
+        }
+      }
+    }
+}
+
+// Finishes row block rb of the warp's range: directly when the warp computed all of it, else
+// through the fixup slots (the last of its contributors sums them in a fixed order).
+template <int NT>
+__device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, const Slice& S, int w, int ub, int ue,
+                      int rb, const float (&acc)[NT][4], const float (&acc2)[NT][4], const float (&tsc)[NT][2],
+                      HeadBest<NT>& hb, int lane) {
+  float v[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    v[j][0] = (acc[j][0] + acc2[j][0]) * tsc[j][0];
+    v[j][1] = (acc[j][1] + acc2[j][1]) * tsc[j][1];
+    v[j][2] = (acc[j][2] + acc2[j][2]) * tsc[j][0];
+    v[j][3] = (acc[j][3] + acc2[j][3]) * tsc[j][1];
+  }
+  uint16_t hold[NT][4];  // residual inputs, loaded before the fixup round trips
+  if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
+  const int uf = rb * S.kcn;
+  if (ph.ks == 1 && uf >= ub && uf + S.kcn <= ue) {
+    epilogue<NT>(ph, io, M, rb, v, hold, hb, lane);
+    return;
+  }
+  const size_t slot_floats = 32 * 4 * NT;
+  {
+    const int i = w - owner(S, uf);
+    float* slot = io.partials + (((size_t)rb * ph.ks + sidx) * ph.cmax + i) * slot_floats + lane * 4 * NT;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) *reinterpret_cast<float4*>(slot + 4 * j) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+  }
+  __syncwarp();
+  int total = 0;
+  for (int s = 0; s < ph.ks; ++s) {
+    const Slice T = slice_geom(ph, G, s);
+    total += owner(T, rb * T.kcn + T.kcn - 1) - owner(T, rb * T.kcn) + 1;
+  }
+  // Release: the warp's partial (ordered before by the warp barrier) is visible to the CTA that
+  // finishes the row block; acquire: that CTA then sees every contributor's partial.
+  unsigned old = 0;
+  if (lane == 0) old = atom_add_acq_rel_gpu(io.rb_cnt + rb, 1u);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old + 1 != (unsigned)total) return;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+  for (int s = 0; s < ph.ks; ++s) {
+    const Slice T = slice_geom(ph, G, s);
+    const int a = owner(T, rb * T.kcn), nc = owner(T, rb * T.kcn + T.kcn - 1) - a + 1;
+    for (int ii = 0; ii < nc; ++ii) {
+      const float* sl = io.partials + (((size_t)rb * ph.ks + s) * ph.cmax + ii) * slot_floats + lane * 4 * NT;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const float4 q = ldcg_f4(sl + 4 * j);
+        v[j][0] += q.x;
+        v[j][1] += q.y;
+        v[j][2] += q.z;
+        v[j][3] += q.w;
+      }
+    }
+  }
+  if (lane == 0) io.rb_cnt[rb] = 0u;
+  epilogue<NT>(ph, io, M, rb, v, hold, hb, lane);
+}
+
+// Head phase end: per-token argmax of the CTA, then the last CTA to finish reduces all CTAs in a
+// fixed order and runs the acceptance.
+template <int NT>
+__device__ __noinline__ void head_finish(const Program& prog, const Io& io, int G, HeadBest<NT>& hb, uint8_t* xs,
+                                         SmemMisc& sm, int warp, int lane) {
+  const int M = prog.M, tid = threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      am_shfl_xor(hb.v[j][h], hb.i[j][h], 4);
+      am_shfl_xor(hb.v[j][h], hb.i[j][h], 8);
+      am_shfl_xor(hb.v[j][h], hb.i[j][h], 16);
+    }
+  __syncthreads();  // every warp is done with the activation fragments: reuse that space
+  float* rv = reinterpret_cast<float*>(xs);
+  int* ri = reinterpret_cast<int*>(xs + kWarps * kMaxM * sizeof(float));
+  if (lane < 4)
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = 8 * j + 2 * lane + h;
+        rv[warp * kMaxM + t] = hb.v[j][h];
+        ri[warp * kMaxM + t] = hb.i[j][h];
+      }
+  __syncthreads();
+  if (tid < M) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int w = 0; w < kWarps; ++w)
+      if (am_better(rv[w * kMaxM + tid], ri[w * kMaxM + tid], bv, bi)) {
+        bv = rv[w * kMaxM + tid];
+        bi = ri[w * kMaxM + tid];
+      }
+    io.head_aux[((size_t)blockIdx.x * kMaxM + tid) * 2] = bv;
+    io.head_aux[((size_t)blockIdx.x * kMaxM + tid) * 2 + 1] = __int_as_float(bi);
+    __threadfence();
+  }
+  __syncthreads();
+  if (tid == 0) sm.flag = atomicAdd(io.head_cnt, 1u) + 1 == (unsigned)G;
+  __syncthreads();
+  if (!sm.flag) return;
+  __threadfence();
+  if (tid < M) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = 0; c < G; ++c) {
+      const float2 e = __ldcg(reinterpret_cast<const float2*>(io.head_aux) + (size_t)c * kMaxM + tid);
+      const int ei = __float_as_int(e.y);
+      if (am_better(e.x, ei, bv, bi)) {
+        bv = e.x;
+        bi = ei;
+      }
+    }
+    if (bi == 0x7fffffff) bi = 0;
+    sm.tok[tid] = bi;
+    io.argmax[tid] = bi;
+  }
+  __syncthreads();
+  if (tid < M / 8) accept_lane(tid, sm.tok, io.pending, io.n_commit, io.committed);
+  if (tid == 0) *io.head_cnt = 0u;
+}
+
+// ---------------------------------------------------------------- grid barrier
+// Sense-free generation barrier on two workspace words (arrivals, generation): the last CTA to
+// arrive resets the count and bumps the generation; the others poll it (bounded).
+__device__ __forceinline__ void grid_barrier(const Io& io, int G, SmemMisc& sm) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned gen = ld_acquire_gpu(io.bar + 1);
+    __threadfence();
+    const unsigned arrived = atomicAdd(io.bar, 1u);
+    if (arrived + 1 == (unsigned)G) {
+      atomicExch(io.bar, 0u);
+      __threadfence();
+      st_release_gpu(io.bar + 1, gen + 1u);
+    } else if (!sm.abort) {
+      uint32_t n = 0;
+      while (ld_acquire_gpu(io.bar + 1) == gen) {
+        if (++n > (1u << 21)) {  // about 1-2 s
+          sm.abort = 1;
+          atomicExch(io.status, kStatusTimeout);
+          break;
+        }
+        if (n > 64) __nanosleep(64);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant__ Program prog,
+                                                           const __grid_constant__ Io io) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* xs = smem + kRingBytes;
+  SmemMisc& sm = *reinterpret_cast<SmemMisc*>(smem + kRingBytes + kXBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
+  const int G = gridDim.x, cta = blockIdx.x;
+
+  if (lane == 0)
+    for (int s = 0; s < kSlots; ++s) mbar_init(&sm.full[warp][s], 1);
+  if (threadIdx.x == 0) sm.abort = 0;
+  fence_mbar_init();
+  __syncthreads();
+
+  const uint32_t ring_w = smem_addr(smem) + warp * kSlots * kSlotBytes;
+  uint64_t pol = 0;
+  Cursor pc;  // next unit to copy into the ring
+  pc.p = 0;
+  unsigned issued = 0;
+  if (lane == 0) {
+    pol = l2_evict_first_policy();
+    cursor_seek(pc, prog, G, cta, warp);
+    for (; issued < (unsigned)kSlots && pc.p < prog.n; ++issued) {
+      issue_unit(prog, pc, ring_w + issued * kSlotBytes, &sm.full[warp][issued], pol);
+      cursor_next(pc, prog, G, cta, warp);
+    }
+  }
+
+  unsigned seq = 0;
+  for (int p = 0; p < prog.n; ++p) {
+    const Phase& ph = prog.ph[p];
+    Slice S;
+    const int sidx = slice_of_cta(ph, G, cta, S);
+    const int ck = chunk_k(ph.fmt);
+    stage_x<NT>(prog, ph, io, S.kc0 * ck, S.kcn * ck, xs, sm);
+    float tsc[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      tsc[j][0] = sm.xscale[8 * j + 2 * c];
+      tsc[j][1] = sm.xscale[8 * j + 2 * c + 1];
+    }
+    HeadBest<NT> hb;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        hb.v[j][h] = -INFINITY;
+        hb.i[j][h] = 0x7fffffff;
+      }
+    const int w = (cta - S.cta0) * kWarps + warp;
+    const int ub = range_begin(S, w), ue = range_begin(S, w + 1);
+    const uint32_t xlane = smem_addr(xs) + lane * 16;
+    const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
+    float acc[NT][4], acc2[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
+    int cur = -1;
+    for (int u = ub; u < ue; ++u) {
+      const int rb = u / S.kcn, kcl = u - rb * S.kcn;
+      if (rb != cur) {
+        if (cur >= 0) {
+          flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
+#pragma unroll
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
+        }
+        cur = rb;
+      }
+      const int slot = (int)(seq % kSlots);
+      if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
+        sm.abort = 1;
+        atomicExch(io.status, kStatusTimeout);
+      }
+      const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kcl * pair_stride;
+      if (ph.fmt == kFmtNvfp4)
+        unit_nvfp4<NT>(ua, xa, lane, acc, acc2);
+      else
+        unit_fp8<NT>(ua, xa, lane, acc, acc2);
+      __syncwarp();
+      if (lane == 0 && pc.p < prog.n && !sm.abort) {
+        fence_proxy_async_smem();
+        issue_unit(prog, pc, ua, &sm.full[warp][slot], pol);
+        cursor_next(pc, prog, G, cta, warp);
+        ++issued;
+      }
+      ++seq;
+    }
+    if (cur >= 0) flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
+    if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
+    if (p + 1 < prog.n) grid_barrier(io, G, sm);
+  }
+  // Copies still in flight (only after a timeout): wait for them before the CTA's memory goes away.
+  if (lane == 0)
+    for (unsigned k = seq; k < issued; ++k) mbar_wait_bounded(&sm.full[warp][k % kSlots], (k / kSlots) & 1u);
+}
+
+}  // namespace vp

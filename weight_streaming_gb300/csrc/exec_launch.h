@@ -1,0 +1,20 @@
+// Host-side entry of the streaming executor (exec.cuh), instantiated in exec_nt12.cu / exec_nt34.cu.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace vp {
+
+cudaError_t launch_exec_nt12(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
+cudaError_t launch_exec_nt34(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
+
+// Runs `prog` (NT = ceil(M / 8) n-tiles of 8 tokens) on `grid` CTAs; cooperative when the program
+// has grid barriers (more than one phase), so that every CTA is resident.
+inline cudaError_t launch_exec(const Program& prog, const Io& io, int grid, cudaStream_t s) {
+  const int NT = (prog.M + 7) / 8;
+  const bool coop = prog.n > 1;
+  return NT <= 2 ? launch_exec_nt12(prog, io, NT, grid, s, coop) : launch_exec_nt34(prog, io, NT, grid, s, coop);
+}
+
+}  // namespace vp

@@ -1,84 +1,141 @@
-// Internal definitions shared by the host API (api.cu) and the kernels (gemm.cuh).
+// Definitions shared by the host API (api.cu) and the streaming executor (exec.cuh): the packed
+// weight layout, the phase program the executor runs, and the workspace carving.
 #pragma once
 #include <cstddef>
 #include <cstdint>
 
 namespace vp {
 
-// ---------------------------------------------------------------- packed layout constants
-constexpr int kRowsPerBlock = 16;   // one MMA A tile: 16 weight rows
-constexpr int kBlocksPerSlab = 16;  // 256 rows per slab (one stage of the copy ring)
-constexpr int kSlabRows = kRowsPerBlock * kBlocksPerSlab;
-constexpr int kQuadK = 64;          // K chunk of one packed block (four k16 MMA steps)
-constexpr int kNvfp4BlockBytes = 576;  // 512 code bytes + 64 scale bytes (9 bytes per 16 weights)
-constexpr int kFp8BlockBytes = 1024;   // 16 x 64 E4M3 bytes
+// ---------------------------------------------------------------- packed weight layout
+// A matrix [N][K] (N % 16 == 0) is stored as row blocks of 16 rows; each row block as K chunks
+// (256 weights wide for NVFP4, 128 for FP8); each chunk as two 8-row strips (rows 0-7, then 8-15 of
+// the block).  Row block rb, chunk kc, strip t starts at ((rb * KC + kc) * 2 + t) * strip bytes, so
+// a row block's stream along K is contiguous and one chunk of a row block (a "unit") is one
+// 2304-byte (NVFP4) or 2048-byte (FP8) copy.
+//
+// Inside a strip, thread (g = lane / 4, c = lane % 4) of a warp owns row g and, in every 16-wide k
+// step s of the chunk, the four weights k = 16 s + 4 c .. + 3 (the mma.sync A fragment with the k
+// order permuted inside each step; the activations are staged with the same permutation):
+//   NVFP4 strip (1152 B): codes [half h = 0..1][g][c][16 B] -- the 16 bytes are steps 8h .. 8h + 7,
+//                         two bytes per step (k, k+1 in the first byte, low nibble first; k+2, k+3
+//                         in the second) -- then block scales [g][16 B], byte s = E4M3 scale of step s.
+//   FP8 strip (1024 B):   [half h = 0..1][g][c][16 B] -- steps 4h .. 4h + 3, four bytes per step.
+// Every warp-wide 16-byte shared-memory read of a strip is one contiguous 512-byte row.
+constexpr int kRowBlock = 16;
+constexpr int kStripRows = 8;
+constexpr int kMaxM = 32;
 
 enum Fmt : int { kFmtNvfp4 = 0, kFmtFp8 = 1 };
 
-// ---------------------------------------------------------------- kernel geometry
-constexpr int kConsumerWarps = 8;                      // each owns 2 row-blocks of a 256-row group
-constexpr int kThreads = (kConsumerWarps + 1) * 32;    // + one bulk-copy producer warp
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-constexpr int kXBufBytes = 104 * 1024;                 // staged activation fragments
-constexpr int kNvfp4Stages = 12;                       // 12 x 9216 B ring
-constexpr int kFp8Stages = 7;                          // 7 x 16384 B ring
-constexpr int kMaxM = 32;
+__host__ __device__ constexpr int chunk_k(int fmt) { return fmt == kFmtNvfp4 ? 256 : 128; }
+__host__ __device__ constexpr int strip_bytes(int fmt) { return fmt == kFmtNvfp4 ? 1152 : 1024; }
+__host__ __device__ inline size_t strip_offset(int fmt, int KC, int rb, int kc, int t) {
+  return (((size_t)rb * KC + kc) * 2 + t) * (size_t)strip_bytes(fmt);
+}
 
+// ---------------------------------------------------------------- executor geometry
+// One persistent CTA per SM, 16 warps.  Every warp streams its own contiguous range of units
+// through a private 3-slot shared-memory ring filled by bulk copies it issues itself, and runs the
+// dequantisation + warp MMAs of each unit from there.  The rest of shared memory holds the
+// activations of the CTA's K slice as f16 MMA fragments.
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kSlots = 3;
+constexpr int kSlotBytes = 2304;
+constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;  // 110,592
+constexpr int kMiscBytes = 4096;
+constexpr int kSmemBytes = 232448;                        // 227 KB: the per-CTA maximum
+constexpr int kXBytes = kSmemBytes - kRingBytes - kMiscBytes;
+constexpr int kMaxGrid = 256;
+constexpr int kWarpsBound = kMaxGrid * kWarps;  // bound on the warps of any slice (fixup slot count)
+
+// Widest K slice whose activations fit in kXBytes as NT n-tiles of 8 tokens (and that the staging
+// threads hold in registers): a multiple of both chunk widths.
+__host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 7168 : NT == 2 ? 3584 : NT == 3 ? 2048 : 1792; }
+
+enum Layout : int {
+  kPlain = 0,        // virtual row blocks = the row blocks of w0, then of w1 (from row block rb1)
+  kInterleaved = 1,  // virtual row block rb = 8-row strip rb of w0 (rows 0-7) + strip rb of w1 (rows 8-15)
+};
 enum Epi : int {
-  kEpiF32 = 0,        // y[m][n] = scale * acc (fp32)
-  kEpiBf16Prefix = 1, // out[m][n] = bf16(scale * acc) for n < out_cols (segment 0 only)
-  kEpiSiluMul = 2,    // out[m][f] = bf16(silu(ts0 * gate) * ts1 * up)  (interleaved segments)
-  kEpiResid = 3,      // h[m][n] = bf16(h[m][n] + scale * acc); finisher writes 1/rms(h) per row
-  kEpiHead = 4,       // per-row argmax over n, then greedy acceptance per lane
+  kEpiF32 = 0,    // y[m][n] = s * acc
+  kEpiZ = 1,      // z[m][n] = bf16(s * acc) for segment-0 rows n < out_cols (the rest is computed, unused)
+  kEpiSilu = 2,   // a[m][f] = bf16(silu(s0 * gate) * s1 * up) (interleaved)
+  kEpiResid = 3,  // h[m][n] = bf16(h[m][n] + s * acc) (and the trace copy)
+  kEpiHead = 4,   // logits -> per-row argmax -> greedy acceptance
+};
+// Buffers a phase reads or writes, resolved per launch through Io::buf.
+enum Buf : int { kBufX = 0, kBufY, kBufH, kBufZ, kBufA, kBufLogits, kBufTrace, kNumBufs };
+
+struct Phase {
+  const uint8_t* w0;
+  const uint8_t* w1;
+  float s0, s1;     // fp32 scale of w0 / w1 (NVFP4 tensor scale or FP8 per-tensor scale)
+  int K, KC;        // reduction length and its chunk count
+  int RB, rb1;      // virtual row blocks; first row block of w1 (plain; RB if none)
+  int cmax;         // fixup slots per (row block, K slice)
+  int8_t fmt, layout, epi, ks;  // ks: K slices
+  int8_t x_src, x_rms, out, pad;
+  int x_ld, out_ld, out_cols, trace_slot;
 };
 
-struct GemmParams {
-  // weights: one or two packed matrices ("segments") forming the virtual output rows
-  const uint8_t* w[2];
-  int seg_rows[2];    // rows of each segment (multiple of 16; seg_rows[1] = 0 if unused)
-  float wscale[2];    // fp32 scale (NVFP4 tensor scale / FP8 per-tensor scale) per segment
-  int interleave;     // 1: each 256-row group = 8 row-blocks of seg 0 + the same 8 of seg 1
-  int K, M;
-  int nq;             // K / 64
-  int n_groups;       // virtual 256-row groups
-  int seg0_groups;    // groups belonging to segment 0 (non-interleaved)
-  long long units;    // n_groups * nq
-  // activation source: bf16 [M][ld]; optional per-row multiplier (RMSNorm: 1/rms)
-  const uint16_t* x;
-  int x_ld;
-  const float* x_rowscale;
-  // epilogue
-  int epi;
-  float* y;  int y_ld;                 // kEpiF32
-  uint16_t* out; int out_ld; int out_cols;  // kEpiBf16Prefix / kEpiSiluMul
-  uint16_t* resid; int resid_ld; int resid_cols;  // kEpiResid (in/out)
-  float* rms_out; float rms_eps;       // kEpiResid finisher
-  const int32_t* pending; int32_t* argmax; int32_t* n_commit; int32_t* committed;  // kEpiHead
-  float* logits; int logits_ld;        // kEpiHead (optional)
+constexpr int kMaxPhases = 160;
+struct Program {
+  int n, M;
+  float eps;
+  int pad;
+  Phase ph[kMaxPhases];
+};
+
+struct Io {
+  void* buf[kNumBufs];
+  const int32_t* pending;
+  int32_t* argmax;
+  int32_t* n_commit;
+  int32_t* committed;
+  size_t trace_stride;  // elements between trace slots
   // workspace
   int* status;
-  unsigned* task_cnt;
-  unsigned* group_cnt;  // [n_groups]
-  float* group_aux;     // [n_groups][kMaxM][2]
-  float* partials;      // [grid][2][kConsumerThreads][8 * MT]
+  unsigned* bar;       // [0] arrivals, [1] generation
+  unsigned* head_cnt;
+  float* head_aux;     // [kMaxGrid][kMaxM][2]
+  unsigned* rb_cnt;    // [max RB]
+  float* partials;     // fixup slots: [RB][ks][cmax][32 lanes][4 NT]
 };
 
-// Workspace carving shared by the host-side size query and the launch code.
-struct WsLayout {
-  size_t status, task_cnt, group_cnt, group_aux, partials, total;
-};
-
+// ---------------------------------------------------------------- workspace carving
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout gemm_ws_layout(int n_groups, int grid, int mt) {
+struct WsLayout {
+  size_t status, bar, head_cnt, head_aux, rb_cnt, partials, total;
+};
+
+// max_rb: largest RB of the program's phases; max_slots: largest RB * ks * cmax.
+inline WsLayout ws_layout(size_t max_rb, size_t max_slots, int NT) {
   WsLayout L;
   L.status = 0;
-  L.task_cnt = 64;
-  L.group_cnt = 256;
-  L.group_aux = align_up(L.group_cnt + sizeof(unsigned) * (size_t)n_groups, 256);
-  L.partials = align_up(L.group_aux + sizeof(float) * 2 * kMaxM * (size_t)n_groups, 256);
-  L.total = align_up(L.partials + sizeof(float) * (size_t)grid * 2 * kConsumerThreads * 8 * mt, 256);
+  L.bar = 64;
+  L.head_cnt = 128;
+  L.head_aux = 256;
+  L.rb_cnt = align_up(L.head_aux + sizeof(float) * 2 * kMaxM * kMaxGrid, 256);
+  L.partials = align_up(L.rb_cnt + sizeof(unsigned) * max_rb, 256);
+  L.total = align_up(L.partials + sizeof(float) * 32 * 4 * (size_t)NT * max_slots, 256);
   return L;
+}
+
+// Fixup slots a phase needs per (row block, K slice): the most warps whose unit ranges can meet one
+// row block's kcn units, for any grid of at most kMaxGrid CTAs (every non-empty warp range holds at
+// least floor(U / kWarpsBound) units).
+inline int phase_cmax(int RB, int KC, int ks) {
+  int cm = 1;
+  for (int s = 0; s < ks; ++s) {
+    const int kcn = (int)((long long)(s + 1) * KC / ks - (long long)s * KC / ks);
+    const long long ufl = (long long)RB * kcn / kWarpsBound;
+    int c = ufl == 0 ? kcn : (int)((kcn + ufl - 1) / ufl) + 1;
+    if (c > kcn) c = kcn;
+    if (c > cm) cm = c;
+  }
+  return cm;
 }
 
 }  // namespace vp
