@@ -122,6 +122,25 @@ vp_status vp_linear_nvfp4(const void* w_packed, float tensor_scale, const void* 
 vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float* y, int M, int N,
                         int K, void* ws, size_t ws_bytes, void* stream);
 
+/* vp_linear_nvfp4 without a caller-provided workspace.  The pages describe no such call: it is
+ * a convenience of this library for callers that cannot pass scratch memory -- a plugin or custom-
+ * op interface whose fixed signature has no workspace argument, or a decode loop that must not
+ * stall, where allocating device memory is not allowed (cudaMalloc / cudaFree synchronise the
+ * device).  The call allocates nothing: it uses a fixed 8 MiB scratch array inside the library,
+ * one per device, and computes exactly what vp_linear_nvfp4 computes (same kernel, same order of
+ * reduction, so the same bits).
+ *   - The first call on a device does the set-up (it looks up the scratch array's address, which
+ *     may initialise the CUDA context); make it before any stream capture.
+ *   - Every call clears the scratch's status word and counters on `stream` before its launch.
+ *   - Shapes whose split-K bookkeeping needs more than the 8 MiB scratch (roughly: many rows times
+ *     a long K, e.g. a 248320 x 5120 head) return VP_ERR_WORKSPACE; use vp_linear_nvfp4 for them.
+ *   - The scratch is shared by all calls on a device: calls that overlap in time (on different
+ *     streams, or from different host threads) race and corrupt each other's results.  Order them
+ *     on one stream.
+ * Arguments, shapes and errors otherwise as for vp_linear_nvfp4. */
+vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, const void* x, float* y, int M,
+                                  int N, int K, void* stream);
+
 /* ------------------------------------------------------------------ head + argmax + accept
  *
  * logits[m][v] = tensor_scale * sum_k x[m][k] * w[v][k] (NVFP4 head [V][K]), never materialised

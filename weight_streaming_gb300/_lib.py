@@ -24,6 +24,7 @@ EXPORTS = [
     "vp_packed_bytes_fp8", "vp_pack_nvfp4", "vp_pack_fp8", "vp_workspace_bytes", "vp_linear_nvfp4",
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
+    "vp_linear_nvfp4_noalloc",
 ]
 
 
@@ -77,6 +78,7 @@ def _load():
         "vp_verify_pass": (I, [P, P, I, P, P, P, P, P, P, P, S, P]),
         "vp_verify_blocks": (I, [P, P, I, I, I, P, P, S, P]),
         "vp_pass_launch_count": (I, [P]),
+        "vp_linear_nvfp4_noalloc": (I, [P, F, P, P, I, I, I, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -148,6 +150,13 @@ def vp_linear_nvfp4(w_packed, tensor_scale: float, x, y, M: int, N: int, K: int,
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check("vp_linear_nvfp4", _L.vp_linear_nvfp4(_ptr(w_packed), tensor_scale, _ptr(x), _ptr(y), M, N, K, _ptr(ws),
                                                  wb, _stream(stream)))
+
+
+def vp_linear_nvfp4_noalloc(w_packed, tensor_scale: float, x, y, M: int, N: int, K: int, stream=None):
+    """vp_linear_nvfp4 on the library's own fixed scratch (no workspace argument, nothing allocated);
+    calls must not overlap in time (see include/verify.h)."""
+    _check("vp_linear_nvfp4_noalloc", _L.vp_linear_nvfp4_noalloc(_ptr(w_packed), tensor_scale, _ptr(x), _ptr(y), M,
+                                                                 N, K, _stream(stream)))
 
 
 def vp_linear_fp8(w_packed, scale: float, x, y, M: int, N: int, K: int, ws, stream=None, ws_bytes=None):

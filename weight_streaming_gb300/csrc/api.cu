@@ -463,6 +463,86 @@ vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const 
   return run_single(s, M, x, ws, ws_bytes, extra, (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------ linear layer without a workspace
+// Some callers cannot hand the library a workspace: a plugin hook or a custom-op interface with a
+// fixed signature that has no scratch argument, or a decode loop that must never stall, where a
+// device allocation is ruled out because cudaMalloc and cudaFree synchronise the device.  For them
+// vp_linear_nvfp4_noalloc runs the same streaming executor as vp_linear_nvfp4 on a scratch area
+// that lives in the library itself: a fixed-size device array, zero at load time, whose address is
+// looked up once per device.
+namespace {
+
+constexpr size_t kNoallocScratchBytes = (size_t)8 << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+
+// Address of the scratch array on the current device, looked up on the first call per device (with
+// that device current) and kept.
+vp_status noalloc_scratch(void** out) {
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return VP_ERR_UNSUPPORTED;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return VP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, const void* x, float* y, int M, int N,
+                                  int K, void* stream) {
+  if (!w_packed || !x || !y) return VP_ERR_INVALID_ARG;
+  if (M < 1 || M > kMaxM || !weight_shape_ok(kFmtNvfp4, N, K)) return VP_ERR_SHAPE;
+  if (!aligned(w_packed, 16) || !aligned(x, 16) || !aligned(y, 4)) return VP_ERR_ALIGNMENT;
+  PhaseSpec s;
+  s.fmt = kFmtNvfp4;
+  s.w0 = w_packed;
+  s.s0 = tensor_scale;
+  s.rows0 = N;
+  s.K = K;
+  s.epi = kEpiF32;
+  s.x_src = kBufX;
+  s.x_ld = K;
+  s.out = kBufY;
+  s.out_ld = N;
+  const int NT = nt_of(M);
+  const Phase ph = make_phase(s, NT);
+  const WsLayout L = ws_layout((size_t)ph.RB, (size_t)ph.RB * ph.ks * ph.cmax, NT);
+  if (L.total > kNoallocScratchBytes) return VP_ERR_WORKSPACE;  // the shape needs more than the fixed scratch
+  int sms = 0;
+  vp_status st = device_sms(&sms);
+  if (st != VP_OK) return st;
+  if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != VP_OK) return st;
+  cudaStream_t cs = (cudaStream_t)stream;
+  // The status word, the barrier and the counters must start at zero: clear them on every call
+  // (the fixup slots and the head maxima are written before they are read).
+  cudaError_t e = cudaMemsetAsync(scratch, 0, L.partials, cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  Io io = make_io(scratch, L);
+  io.buf[kBufX] = const_cast<void*>(x);
+  io.buf[kBufY] = y;
+  static thread_local Program prog;
+  prog.n = 1;
+  prog.M = M;
+  prog.eps = 0.0f;
+  prog.pad = 0;
+  prog.ph[0] = ph;
+  e = launch_exec(prog, io, sms, cs);
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending, int32_t* argmax,
                            int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes, void* stream) {
   if (!logits || !pending || !argmax || !n_commit || !committed || !ws) return VP_ERR_INVALID_ARG;
