@@ -37,16 +37,6 @@ namespace vp {
 
 enum : int { kStatusTimeout = 6 };
 
-struct SmemMisc {
-  uint64_t full[kWarps][kSlots];
-  float red[kThreads / 16];
-  int xexp[kMaxM];
-  float xscale[kMaxM];
-  int tok[kMaxM];
-  int abort;
-  int flag;
-};
-static_assert(sizeof(SmemMisc) <= (size_t)kMiscBytes, "SmemMisc exceeds its shared-memory budget");
 static_assert(kSlotBytes >= 2 * 1152 && kSlotBytes >= 2 * 1024, "a slot holds one unit");
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
@@ -110,62 +100,85 @@ __device__ __forceinline__ int range_begin(const Slice& S, int w) {
 __device__ __forceinline__ int owner(const Slice& S, int u) { return (int)(((long long)(u + 1) * S.W - 1) / S.U); }
 
 // ---------------------------------------------------------------- weight producer (lane 0 of a warp)
-// Walks the warp's units across all phases of the program, in consumption order.
+// Walks the warp's units across all phases of the program, in consumption order, keeping the
+// source addresses of the current unit: within a row block the next unit is the next K chunk
+// (2 strips further on), so a step is two pointer increments; the phase descriptor is read only
+// when the row block or the phase changes.
 struct Cursor {
-  int p, u, ue, kc0, kcn;
+  int p;           // phase (== prog.n when done)
+  int left;        // units left in the phase's range, including the current one
+  int rb, kcl;     // row block and chunk position within the slice of the current unit
+  int kc0, kcn;    // the slice's chunks
+  const uint8_t* a;
+  const uint8_t* b;  // second strip (interleaved layout), else nullptr
+  uint32_t bytes;    // per source
+  uint32_t step;     // bytes from one K chunk to the next of the same row block
 };
+__device__ __forceinline__ void cursor_locate(Cursor& c, const Program& prog) {
+  const Phase& ph = prog.ph[c.p];
+  const int sb = strip_bytes(ph.fmt), kc = c.kc0 + c.kcl;
+  c.step = 2u * sb;
+  if (ph.layout == kPlain) {
+    const bool s1 = c.rb >= ph.rb1;
+    c.a = (s1 ? ph.w1 : ph.w0) + strip_offset(ph.fmt, ph.KC, s1 ? c.rb - ph.rb1 : c.rb, kc, 0);
+    c.b = nullptr;
+    c.bytes = 2u * sb;
+  } else {
+    const size_t off = strip_offset(ph.fmt, ph.KC, c.rb >> 1, kc, c.rb & 1);
+    c.a = ph.w0 + off;
+    c.b = ph.w1 + off;
+    c.bytes = (uint32_t)sb;
+  }
+}
 __device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, int G, int cta, int warp) {
   while (c.p < prog.n) {
     const Phase& ph = prog.ph[c.p];
     Slice S;
     slice_of_cta(ph, G, cta, S);
     const int w = (cta - S.cta0) * kWarps + warp;
-    c.u = range_begin(S, w);
-    c.ue = range_begin(S, w + 1);
-    c.kc0 = S.kc0;
-    c.kcn = S.kcn;
-    if (c.u < c.ue) return;
+    const int u = range_begin(S, w);
+    c.left = range_begin(S, w + 1) - u;
+    if (c.left > 0) {
+      c.kc0 = S.kc0;
+      c.kcn = S.kcn;
+      c.rb = u / S.kcn;
+      c.kcl = u - c.rb * S.kcn;
+      cursor_locate(c, prog);
+      return;
+    }
     ++c.p;
   }
 }
 __device__ __forceinline__ void cursor_next(Cursor& c, const Program& prog, int G, int cta, int warp) {
-  if (++c.u == c.ue) {
+  if (--c.left == 0) {
     ++c.p;
     cursor_seek(c, prog, G, cta, warp);
-  }
-}
-// Global address and size of the cursor's unit: one contiguous copy (plain), or two strips.
-struct UnitSrc {
-  const uint8_t* a;
-  const uint8_t* b;  // second strip (interleaved), else nullptr
-  uint32_t bytes;    // per source
-};
-__device__ __forceinline__ UnitSrc unit_src(const Program& prog, const Cursor& c) {
-  const Phase& ph = prog.ph[c.p];
-  const int rb = c.u / c.kcn, kc = c.kc0 + c.u % c.kcn;
-  const int sb = strip_bytes(ph.fmt);
-  UnitSrc r;
-  if (ph.layout == kPlain) {
-    const bool s1 = rb >= ph.rb1;
-    r.a = (s1 ? ph.w1 : ph.w0) + strip_offset(ph.fmt, ph.KC, s1 ? rb - ph.rb1 : rb, kc, 0);
-    r.b = nullptr;
-    r.bytes = 2u * sb;
+  } else if (++c.kcl == c.kcn) {
+    c.kcl = 0;
+    ++c.rb;
+    cursor_locate(c, prog);
   } else {
-    const size_t off = strip_offset(ph.fmt, ph.KC, rb >> 1, kc, rb & 1);
-    r.a = ph.w0 + off;
-    r.b = ph.w1 + off;
-    r.bytes = (uint32_t)sb;
+    c.a += c.step;
+    if (c.b) c.b += c.step;
   }
-  return r;
 }
+struct SmemMisc {
+  uint64_t full[kWarps][kMaxSlots];
+  Cursor cur[kWarps];  // the producer state of each warp (used by its lane 0 only)
+  float red[kThreads / 16];
+  float xscale[kMaxM];
+  int tok[kMaxM];
+  int abort;
+  int flag;
+};
+static_assert(sizeof(SmemMisc) <= (size_t)kMiscBytes, "SmemMisc exceeds its shared-memory budget");
+
 // Bulk copy of the cursor's unit into the slot at shared address dst, completing on bar.
-__device__ __forceinline__ void issue_unit(const Program& prog, const Cursor& c, uint32_t dst, uint64_t* bar,
-                                           uint64_t pol) {
-  const UnitSrc r = unit_src(prog, c);
+__device__ __forceinline__ void issue_unit(const Cursor& c, uint32_t dst, uint64_t* bar, uint64_t pol) {
   const uint32_t b = smem_addr(bar);
-  mbar_arrive_expect_tx(bar, r.b ? 2u * r.bytes : r.bytes);
-  bulk_g2s(dst, r.a, r.bytes, b, pol);
-  if (r.b) bulk_g2s(dst + r.bytes, r.b, r.bytes, b, pol);
+  mbar_arrive_expect_tx(bar, c.b ? 2u * c.bytes : c.bytes);
+  bulk_g2s(dst, c.a, c.bytes, b, pol);
+  if (c.b) bulk_g2s(dst + c.bytes, c.b, c.bytes, b, pol);
 }
 
 // ---------------------------------------------------------------- activation staging
@@ -273,10 +286,7 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
   } else {
     e = exp_of_max(row_reduce(stat, T, true, sm.red));
   }
-  if (active && i == 0) {
-    sm.xexp[n] = e;
-    sm.xscale[n] = pow2f(e);
-  }
+  if (active && i == 0) sm.xscale[n] = pow2f(e);
   if (tid >= M && tid < kMaxM) sm.xscale[tid] = 0.0f;
   // x * 2^-e exactly (two power-of-two steps when 2^-e is not a normal float); for RMSNorm the
   // 2^-e folds into 1/rms: bf16(x * inv) * 2^-e == bf16(x * (inv * 2^-e)) (no under/overflow).
@@ -625,9 +635,10 @@ __device__ __forceinline__ void grid_barrier(const Io& io, int G, SmemMisc& sm) 
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant__ Program prog,
                                                            const __grid_constant__ Io io) {
+  constexpr int kSlots = ring_slots(NT);
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* xs = smem + kRingBytes;
-  SmemMisc& sm = *reinterpret_cast<SmemMisc*>(smem + kRingBytes + kXBytes);
+  uint8_t* xs = smem + ring_bytes(NT);
+  SmemMisc& sm = *reinterpret_cast<SmemMisc*>(smem + ring_bytes(NT) + x_bytes(NT));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -639,14 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
 
   const uint32_t ring_w = smem_addr(smem) + warp * kSlots * kSlotBytes;
   uint64_t pol = 0;
-  Cursor pc;  // next unit to copy into the ring
-  pc.p = 0;
+  Cursor& pc = sm.cur[warp];  // next unit to copy into the ring (lane 0)
   unsigned issued = 0;
   if (lane == 0) {
     pol = l2_evict_first_policy();
+    pc.p = 0;
     cursor_seek(pc, prog, G, cta, warp);
     for (; issued < (unsigned)kSlots && pc.p < prog.n; ++issued) {
-      issue_unit(prog, pc, ring_w + issued * kSlotBytes, &sm.full[warp][issued], pol);
+      issue_unit(pc, ring_w + issued * kSlotBytes, &sm.full[warp][issued], pol);
       cursor_next(pc, prog, G, cta, warp);
     }
   }
@@ -676,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     const int ub = range_begin(S, w), ue = range_begin(S, w + 1);
     const uint32_t xlane = smem_addr(xs) + lane * 16;
     const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
+    int rb = ub < ue ? ub / S.kcn : 0, kcl = ub < ue ? ub - rb * S.kcn : 0;
     float acc[NT][4], acc2[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -683,7 +695,6 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
     int cur = -1;
     for (int u = ub; u < ue; ++u) {
-      const int rb = u / S.kcn, kcl = u - rb * S.kcn;
       if (rb != cur) {
         if (cur >= 0) {
           flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
@@ -707,11 +718,15 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0 && pc.p < prog.n && !sm.abort) {
         fence_proxy_async_smem();
-        issue_unit(prog, pc, ua, &sm.full[warp][slot], pol);
+        issue_unit(pc, ua, &sm.full[warp][slot], pol);
         cursor_next(pc, prog, G, cta, warp);
         ++issued;
       }
       ++seq;
+      if (++kcl == S.kcn) {
+        kcl = 0;
+        ++rb;
+      }
     }
     if (cur >= 0) flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
     if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);

@@ -35,23 +35,31 @@ __host__ __device__ inline size_t strip_offset(int fmt, int KC, int rb, int kc, 
 
 // ---------------------------------------------------------------- executor geometry
 // One persistent CTA per SM, 16 warps.  Every warp streams its own contiguous range of units
-// through a private 3-slot shared-memory ring filled by bulk copies it issues itself, and runs the
+// through a private shared-memory ring filled by bulk copies it issues itself, and runs the
 // dequantisation + warp MMAs of each unit from there.  The rest of shared memory holds the
-// activations of the CTA's K slice as f16 MMA fragments.
+// activations of the CTA's K slice as f16 MMA fragments.  The ring is as deep as the activations
+// leave room for: what a warp has in flight while it computes is what hides the DRAM latency
+// (about 2.5 us when the whole GPU streams).
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSlots = 3;
+constexpr int kMaxSlots = 4;
 constexpr int kSlotBytes = 2304;
-constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;  // 110,592
-constexpr int kMiscBytes = 4096;
-constexpr int kSmemBytes = 232448;                        // 227 KB: the per-CTA maximum
-constexpr int kXBytes = kSmemBytes - kRingBytes - kMiscBytes;
+constexpr int kMiscBytes = 2048;
+constexpr int kSmemBytes = 232448;  // 227 KB: the per-CTA maximum
 constexpr int kMaxGrid = 256;
 constexpr int kWarpsBound = kMaxGrid * kWarps;  // bound on the warps of any slice (fixup slot count)
 
-// Widest K slice whose activations fit in kXBytes as NT n-tiles of 8 tokens (and that the staging
-// threads hold in registers): a multiple of both chunk widths.
-__host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 7168 : NT == 2 ? 3584 : NT == 3 ? 2048 : 1792; }
+// Ring slots per warp for NT n-tiles of 8 tokens, and the shared memory left for activations.
+__host__ __device__ constexpr int ring_slots(int NT) { return NT == 1 ? 4 : 3; }
+__host__ __device__ constexpr int ring_bytes(int NT) { return kWarps * ring_slots(NT) * kSlotBytes; }
+__host__ __device__ constexpr int x_bytes(int NT) { return kSmemBytes - ring_bytes(NT) - kMiscBytes; }
+
+// Widest K slice whose activations fit in x_bytes(NT) (16 NT bytes per k) and that the staging
+// threads hold in registers (128 k per thread of a row): a multiple of both chunk widths.
+__host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 5120 : NT == 2 ? 3584 : NT == 3 ? 2048 : 1792; }
+static_assert(16 * 1 * 5120 <= x_bytes(1) && 16 * 2 * 3584 <= x_bytes(2) && 16 * 3 * 2048 <= x_bytes(3) &&
+                  16 * 4 * 1792 <= x_bytes(4),
+              "activation slices fit the shared memory left by the ring");
 
 enum Layout : int {
   kPlain = 0,        // virtual row blocks = the row blocks of w0, then of w1 (from row block rb1)
