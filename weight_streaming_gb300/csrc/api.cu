@@ -76,16 +76,19 @@ Phase make_phase(const PhaseSpec& s, int NT) {
   ph.s1 = s.s1;
   ph.K = s.K;
   ph.KC = s.K / chunk_k(s.fmt);
+  ph.RB = (s.rows0 + s.rows1) / kRowBlock;
   if (s.layout == kPlain) {
-    ph.RB = (s.rows0 + s.rows1) / kRowBlock;
+    ph.grp = 2;
     ph.rb1 = s.rows0 / kRowBlock;
   } else {
-    ph.RB = s.rows0 / kStripRows;
+    ph.grp = 1;
+    ph.RB = s.rows0 / kRowBlock;
     ph.rb1 = ph.RB;
   }
-  const int per = ks_max(NT) / chunk_k(s.fmt);
-  ph.ks = (int8_t)((ph.KC + per - 1) / per);
-  ph.cmax = phase_cmax(ph.RB, ph.KC, ph.ks);
+  ph.KG = (ph.KC + ph.grp - 1) / ph.grp;
+  const int per = ks_max(NT) / chunk_k(s.fmt) / ph.grp;  // groups per slice at most
+  ph.ks = (int8_t)((ph.KG + per - 1) / per);
+  ph.cmax = phase_cmax(ph.RB, ph.KG, ph.ks);
   ph.fmt = (int8_t)s.fmt;
   ph.layout = (int8_t)s.layout;
   ph.epi = (int8_t)s.epi;
@@ -103,19 +106,24 @@ Phase make_phase(const PhaseSpec& s, int NT) {
 bool slices_ok(const Phase& ph, int G) {
   int prev = 0;
   for (int s = 1; s <= ph.ks; ++s) {
-    const int kc = (int)((long long)s * ph.KC / ph.ks);
-    const int c = s == ph.ks ? G : (int)(((long long)G * kc + ph.KC / 2) / ph.KC);
+    const int kg = (int)((long long)s * ph.KG / ph.ks);
+    const int c = s == ph.ks ? G : (int)(((long long)G * kg + ph.KG / 2) / ph.KG);
     if (c <= prev) return false;
     prev = c;
   }
   return true;
 }
 
+// Fixup slots of a phase, in units of 32 lanes x 4 NT floats (an interleaved phase keeps two sets).
+size_t phase_slots(const Phase& ph) {
+  return (size_t)ph.RB * ph.ks * ph.cmax * (ph.layout == kInterleaved ? 2 : 1);
+}
+
 struct Needs {
   size_t max_rb = 1, max_slots = 1;
   void add(const Phase& ph) {
     max_rb = std::max(max_rb, (size_t)ph.RB);
-    max_slots = std::max(max_slots, (size_t)ph.RB * ph.ks * ph.cmax);
+    max_slots = std::max(max_slots, phase_slots(ph));
   }
 };
 
@@ -285,7 +293,7 @@ void argmax_chunking(int V, int* chunk, int* n_chunks) {
 }
 
 size_t single_ws_bytes(const Phase& ph, int NT) {
-  return ws_layout((size_t)ph.RB, (size_t)ph.RB * ph.ks * ph.cmax, NT).total;
+  return ws_layout((size_t)ph.RB, phase_slots(ph), NT).total;
 }
 
 }  // namespace
@@ -385,7 +393,7 @@ static vp_status run_single(const PhaseSpec& s, int M, const void* x, void* ws, 
                             cudaStream_t stream) {
   const int NT = nt_of(M);
   const Phase ph = make_phase(s, NT);
-  const WsLayout L = ws_layout((size_t)ph.RB, (size_t)ph.RB * ph.ks * ph.cmax, NT);
+  const WsLayout L = ws_layout((size_t)ph.RB, phase_slots(ph), NT);
   if (ws_bytes < L.total) return VP_ERR_WORKSPACE;
   int sms = 0;
   vp_status st = device_sms(&sms);
@@ -517,7 +525,7 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   s.out_ld = N;
   const int NT = nt_of(M);
   const Phase ph = make_phase(s, NT);
-  const WsLayout L = ws_layout((size_t)ph.RB, (size_t)ph.RB * ph.ks * ph.cmax, NT);
+  const WsLayout L = ws_layout((size_t)ph.RB, phase_slots(ph), NT);
   if (L.total > kNoallocScratchBytes) return VP_ERR_WORKSPACE;  // the shape needs more than the fixed scratch
   int sms = 0;
   vp_status st = device_sms(&sms);

@@ -10,12 +10,12 @@
 // projections) and "The bugs a second reviewer found" (one argmax tie rule everywhere).
 //
 // GB300 design (not the pages' Metal tiles):
-//  * One CTA per SM, 16 independent warps.  Each phase's units (16-row block x one K chunk, 2304 B
-//    NVFP4 / 2048 B FP8) are split into equal contiguous ranges, one per warp.  A warp streams its
-//    range through a private 3-slot ring with 1-D bulk copies that its lane 0 issues (evict-first),
-//    so no warp ever waits for another inside a phase, and it keeps prefetching across phase ends:
-//    the next phase's first units are in flight while the grid barrier and the activation staging
-//    of the phase boundary run.
+//  * One CTA per SM, 16 independent warps.  Each phase's units (a virtual row block x a group of K
+//    chunks: 4608 B NVFP4 / 4096 B FP8) are split into equal contiguous ranges, one per warp.  A
+//    warp streams its range through a private 2-slot ring with 1-D bulk copies that its lane 0
+//    issues (evict-first), so no warp ever waits for another inside a phase, and it keeps
+//    prefetching across phase ends: the next phase's first units are in flight while the grid
+//    barrier and the activation staging of the phase boundary run.
 //  * Dequantisation is exact in f16 (E2M1 x E4M3 products have <= 5 significant bits), done in
 //    registers straight into mma.sync.m16n8k16 A fragments; the activations (B) are staged once per
 //    phase as f16 fragments scaled per row by an exact power of two, which un-scales the fp32
@@ -37,7 +37,7 @@ namespace vp {
 
 enum : int { kStatusTimeout = 6 };
 
-static_assert(kSlotBytes >= 2 * 1152 && kSlotBytes >= 2 * 1024, "a slot holds one unit");
+static_assert(kSlotBytes >= 2 * 2304 && kSlotBytes >= 2 * 2048, "a slot holds one unit");
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
@@ -66,23 +66,23 @@ __device__ __forceinline__ void accept_lane(int l, const int* tok, const int32_t
 }
 
 // ---------------------------------------------------------------- phase geometry
-// K slice s of a phase: chunks [kc0, kc0 + kcn), CTAs [cta0, cta0 + ctan) in proportion to the
-// chunks, U = RB * kcn units (row-block major) over W = min(16 ctan, U) warps, so that every warp
-// with a range owns at least one unit (the owners of a row block's units are then exactly its
+// K slice s of a phase: chunk groups [kg0, kg0 + kgn), CTAs [cta0, cta0 + ctan) in proportion to
+// the groups, U = RB * kgn units (row-block major) over W = min(16 ctan, U) warps, so that every
+// warp with a range owns at least one unit (the owners of a row block's units are then exactly its
 // contributors, and consecutive); the slice's other warps idle.
 struct Slice {
-  int kc0, kcn, cta0, ctan, U, W;
+  int kg0, kgn, cta0, ctan, U, W;
 };
 __device__ __forceinline__ Slice slice_geom(const Phase& ph, int G, int s) {
   Slice S;
-  const int kc0 = (int)((long long)s * ph.KC / ph.ks), kc1 = (int)((long long)(s + 1) * ph.KC / ph.ks);
-  const int c0 = (int)(((long long)G * kc0 + ph.KC / 2) / ph.KC);
-  const int c1 = s + 1 == ph.ks ? G : (int)(((long long)G * kc1 + ph.KC / 2) / ph.KC);
-  S.kc0 = kc0;
-  S.kcn = kc1 - kc0;
+  const int kg0 = (int)((long long)s * ph.KG / ph.ks), kg1 = (int)((long long)(s + 1) * ph.KG / ph.ks);
+  const int c0 = (int)(((long long)G * kg0 + ph.KG / 2) / ph.KG);
+  const int c1 = s + 1 == ph.ks ? G : (int)(((long long)G * kg1 + ph.KG / 2) / ph.KG);
+  S.kg0 = kg0;
+  S.kgn = kg1 - kg0;
   S.cta0 = c0;
   S.ctan = c1 - c0;
-  S.U = ph.RB * S.kcn;
+  S.U = ph.RB * S.kgn;
   S.W = min(kWarps * S.ctan, S.U);
   return S;
 }
@@ -105,29 +105,33 @@ __device__ __forceinline__ int owner(const Slice& S, int u) { return (int)(((lon
 // (2 strips further on), so a step is two pointer increments; the phase descriptor is read only
 // when the row block or the phase changes.
 struct Cursor {
-  int p;           // phase (== prog.n when done)
-  int left;        // units left in the phase's range, including the current one
-  int rb, kcl;     // row block and chunk position within the slice of the current unit
-  int kc0, kcn;    // the slice's chunks
+  int p;             // phase (== prog.n when done)
+  int left;          // units left in the phase's range, including the current one
+  int rb, kgl;       // row block and group position within the slice of the current unit
+  int kg0, kgn;      // the slice's groups
+  int kc, KC, grp;   // first chunk of the current unit; the phase's chunks and group width
+  uint32_t chunk;    // bytes of one chunk of one row block (two strips)
   const uint8_t* a;
-  const uint8_t* b;  // second strip (interleaved layout), else nullptr
+  const uint8_t* b;  // the up row block's chunk (interleaved layout), else nullptr
   uint32_t bytes;    // per source
-  uint32_t step;     // bytes from one K chunk to the next of the same row block
 };
+// Source addresses of the cursor's unit (read from the phase descriptor).
 __device__ __forceinline__ void cursor_locate(Cursor& c, const Program& prog) {
   const Phase& ph = prog.ph[c.p];
-  const int sb = strip_bytes(ph.fmt), kc = c.kc0 + c.kcl;
-  c.step = 2u * sb;
+  c.KC = ph.KC;
+  c.grp = ph.grp;
+  c.chunk = 2u * strip_bytes(ph.fmt);
+  c.kc = (c.kg0 + c.kgl) * ph.grp;
   if (ph.layout == kPlain) {
     const bool s1 = c.rb >= ph.rb1;
-    c.a = (s1 ? ph.w1 : ph.w0) + strip_offset(ph.fmt, ph.KC, s1 ? c.rb - ph.rb1 : c.rb, kc, 0);
+    c.a = (s1 ? ph.w1 : ph.w0) + strip_offset(ph.fmt, ph.KC, s1 ? c.rb - ph.rb1 : c.rb, c.kc, 0);
     c.b = nullptr;
-    c.bytes = 2u * sb;
+    c.bytes = (uint32_t)min(ph.grp, ph.KC - c.kc) * c.chunk;
   } else {
-    const size_t off = strip_offset(ph.fmt, ph.KC, c.rb >> 1, kc, c.rb & 1);
+    const size_t off = strip_offset(ph.fmt, ph.KC, c.rb, c.kc, 0);
     c.a = ph.w0 + off;
     c.b = ph.w1 + off;
-    c.bytes = (uint32_t)sb;
+    c.bytes = c.chunk;
   }
 }
 __device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, int G, int cta, int warp) {
@@ -139,31 +143,38 @@ __device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, int 
     const int u = range_begin(S, w);
     c.left = range_begin(S, w + 1) - u;
     if (c.left > 0) {
-      c.kc0 = S.kc0;
-      c.kcn = S.kcn;
-      c.rb = u / S.kcn;
-      c.kcl = u - c.rb * S.kcn;
+      c.kg0 = S.kg0;
+      c.kgn = S.kgn;
+      c.rb = u / S.kgn;
+      c.kgl = u - c.rb * S.kgn;
       cursor_locate(c, prog);
       return;
     }
     ++c.p;
   }
 }
+// Next unit: within a row block the next group follows contiguously (grp chunks further on).
 __device__ __forceinline__ void cursor_next(Cursor& c, const Program& prog, int G, int cta, int warp) {
   if (--c.left == 0) {
     ++c.p;
     cursor_seek(c, prog, G, cta, warp);
-  } else if (++c.kcl == c.kcn) {
-    c.kcl = 0;
+  } else if (++c.kgl == c.kgn) {
+    c.kgl = 0;
     ++c.rb;
     cursor_locate(c, prog);
   } else {
-    c.a += c.step;
-    if (c.b) c.b += c.step;
+    const uint32_t step = (uint32_t)c.grp * c.chunk;
+    c.kc += c.grp;
+    c.a += step;
+    if (c.b)
+      c.b += step;
+    else
+      c.bytes = (uint32_t)min(c.grp, c.KC - c.kc) * c.chunk;
   }
 }
+
 struct SmemMisc {
-  uint64_t full[kWarps][kMaxSlots];
+  uint64_t full[kWarps][kSlots];
   Cursor cur[kWarps];  // the producer state of each warp (used by its lane 0 only)
   float red[kThreads / 16];
   float xscale[kMaxM];
@@ -323,9 +334,10 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
 }
 
 // ---------------------------------------------------------------- one unit of a warp
-// acc[j] (16 rows x 8 tokens, the mma.sync C fragment): rows g, g + 8 of the row block, tokens
-// 8j + 2c, 8j + 2c + 1.  With one n-tile, odd k steps accumulate into acc2 (two independent MMA
-// chains); with more, the n-tiles are the independent chains.  ua: the unit's slot; xa: this lane's fragments of the unit's first k-step pair.
+// One K chunk of one row block.  acc[j] (16 rows x 8 tokens, the mma.sync C fragment): rows g, g + 8
+// of the row block, tokens 8j + 2c, 8j + 2c + 1; even k steps accumulate into acc, odd ones into
+// acc2 (the caller passes the same array twice for one chain).  ua: the chunk in the slot; xa: this
+// lane's fragments of the chunk's first k-step pair.
 template <int NT>
 __device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4], float (&acc2)[NT][4]) {
   const int g = lane >> 2;
@@ -358,7 +370,7 @@ __device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, f
       const uint32_t a0 = hmul2_u32(o0[2], d0), a1 = hmul2_u32(o1[2], d1);
       const uint32_t a2 = hmul2_u32(o0[3], d0), a3 = hmul2_u32(o1[3], d1);
 #pragma unroll
-      for (int j = 0; j < NT; ++j) mma_f16_16816(NT == 1 ? acc2[j] : acc[j], a0, a1, a2, a3, b[j].z, b[j].w);
+      for (int j = 0; j < NT; ++j) mma_f16_16816(acc2[j], a0, a1, a2, a3, b[j].z, b[j].w);
     }
   }
 }
@@ -380,8 +392,7 @@ __device__ __forceinline__ void unit_fp8(uint32_t ua, uint32_t xa, int lane, flo
       e4m3x4_to_f16x2x2(w0[2 * p + h], a0, a2);
       e4m3x4_to_f16x2x2(w1[2 * p + h], a1, a3);
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
-        mma_f16_16816((NT == 1 && h) ? acc2[j] : acc[j], a0, a1, a2, a3, h ? b[j].z : b[j].x, h ? b[j].w : b[j].y);
+      for (int j = 0; j < NT; ++j) mma_f16_16816(h ? acc2[j] : acc[j], a0, a1, a2, a3, h ? b[j].z : b[j].x, h ? b[j].w : b[j].y);
     }
   }
 }
@@ -414,22 +425,26 @@ __device__ __forceinline__ void load_resid(const Phase& ph, const Io& io, int M,
       }
 }
 
-// v: the finished row block (fp32, un-scaled activations, before the weight scale).
+// v: the finished row block (fp32, un-scaled activations, before the weight scale); interleaved
+// layout: v = the gate rows, u = the up rows (else u is unused).
 template <int NT>
 __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const float (&v)[NT][4],
-                         const uint16_t (&hold)[NT][4], HeadBest<NT>& hb, int lane) {
+                         const float (&u)[NT][4], const uint16_t (&hold)[NT][4], HeadBest<NT>& hb, int lane) {
   const int g = lane >> 2, c = lane & 3;
   if (ph.layout == kInterleaved) {  // a = bf16(silu(s0 * gate) * s1 * up)
     uint16_t* out = static_cast<uint16_t*>(io.buf[ph.out]);
-    const int f = rb * kStripRows + g;
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int t = 8 * j + 2 * c + h;
         if (t >= M) continue;
-        const float gt = ph.s0 * v[j][h], up = ph.s1 * v[j][2 + h];
-        out[(size_t)t * ph.out_ld + f] = bf16_bits(gt / (1.0f + expf(-gt)) * up);
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int f = rb * kRowBlock + g + 8 * r;
+          const float gt = ph.s0 * v[j][2 * r + h], up = ph.s1 * u[j][2 * r + h];
+          out[(size_t)t * ph.out_ld + f] = bf16_bits(gt / (1.0f + expf(-gt)) * up);
+        }
       }
     return;
   }
@@ -479,38 +494,45 @@ __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const flo
 }
 
 // Finishes row block rb of the warp's range: directly when the warp computed all of it, else
-// through the fixup slots (the last of its contributors sums them in a fixed order).
+// through the fixup slots (the last of its contributors sums them in a fixed order).  Plain layout:
+// the row block is acc + acc2 (two MMA chains); interleaved: acc = gate rows, acc2 = up rows.
 template <int NT>
 __device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, const Slice& S, int w, int ub, int ue,
                       int rb, const float (&acc)[NT][4], const float (&acc2)[NT][4], const float (&tsc)[NT][2],
                       HeadBest<NT>& hb, int lane) {
-  float v[NT][4];
+  const bool two = ph.layout == kInterleaved;
+  float v[NT][4], u[NT][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    v[j][0] = (acc[j][0] + acc2[j][0]) * tsc[j][0];
-    v[j][1] = (acc[j][1] + acc2[j][1]) * tsc[j][1];
-    v[j][2] = (acc[j][2] + acc2[j][2]) * tsc[j][0];
-    v[j][3] = (acc[j][3] + acc2[j][3]) * tsc[j][1];
-  }
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float sc = tsc[j][r & 1];
+      v[j][r] = (two ? acc[j][r] : acc[j][r] + acc2[j][r]) * sc;
+      u[j][r] = two ? acc2[j][r] * sc : 0.0f;
+    }
   uint16_t hold[NT][4];  // residual inputs, loaded before the fixup round trips
   if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
-  const int uf = rb * S.kcn;
-  if (ph.ks == 1 && uf >= ub && uf + S.kcn <= ue) {
-    epilogue<NT>(ph, io, M, rb, v, hold, hb, lane);
+  const int uf = rb * S.kgn;
+  if (ph.ks == 1 && uf >= ub && uf + S.kgn <= ue) {
+    epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
     return;
   }
-  const size_t slot_floats = 32 * 4 * NT;
+  const int per_lane = 4 * NT * (two ? 2 : 1);
+  const size_t slot_floats = 32 * (size_t)per_lane;
   {
     const int i = w - owner(S, uf);
-    float* slot = io.partials + (((size_t)rb * ph.ks + sidx) * ph.cmax + i) * slot_floats + lane * 4 * NT;
+    float* slot = io.partials + (((size_t)rb * ph.ks + sidx) * ph.cmax + i) * slot_floats + lane * per_lane;
 #pragma unroll
-    for (int j = 0; j < NT; ++j) *reinterpret_cast<float4*>(slot + 4 * j) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+    for (int j = 0; j < NT; ++j) {
+      *reinterpret_cast<float4*>(slot + 4 * j) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+      if (two) *reinterpret_cast<float4*>(slot + 4 * (NT + j)) = make_float4(u[j][0], u[j][1], u[j][2], u[j][3]);
+    }
   }
   __syncwarp();
   int total = 0;
   for (int s = 0; s < ph.ks; ++s) {
     const Slice T = slice_geom(ph, G, s);
-    total += owner(T, rb * T.kcn + T.kcn - 1) - owner(T, rb * T.kcn) + 1;
+    total += owner(T, rb * T.kgn + T.kgn - 1) - owner(T, rb * T.kgn) + 1;
   }
   // Release: the warp's partial (ordered before by the warp barrier) is visible to the CTA that
   // finishes the row block; acquire: that CTA then sees every contributor's partial.
@@ -519,12 +541,14 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, con
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old + 1 != (unsigned)total) return;
 #pragma unroll
-  for (int j = 0; j < NT; ++j) v[j][0] = v[j][1] = v[j][2] = v[j][3] = 0.0f;
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
   for (int s = 0; s < ph.ks; ++s) {
     const Slice T = slice_geom(ph, G, s);
-    const int a = owner(T, rb * T.kcn), nc = owner(T, rb * T.kcn + T.kcn - 1) - a + 1;
+    const int a = owner(T, rb * T.kgn), nc = owner(T, rb * T.kgn + T.kgn - 1) - a + 1;
     for (int ii = 0; ii < nc; ++ii) {
-      const float* sl = io.partials + (((size_t)rb * ph.ks + s) * ph.cmax + ii) * slot_floats + lane * 4 * NT;
+      const float* sl = io.partials + (((size_t)rb * ph.ks + s) * ph.cmax + ii) * slot_floats + lane * per_lane;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const float4 q = ldcg_f4(sl + 4 * j);
@@ -532,11 +556,18 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, con
         v[j][1] += q.y;
         v[j][2] += q.z;
         v[j][3] += q.w;
+        if (two) {
+          const float4 q2 = ldcg_f4(sl + 4 * (NT + j));
+          u[j][0] += q2.x;
+          u[j][1] += q2.y;
+          u[j][2] += q2.z;
+          u[j][3] += q2.w;
+        }
       }
     }
   }
   if (lane == 0) io.rb_cnt[rb] = 0u;
-  epilogue<NT>(ph, io, M, rb, v, hold, hb, lane);
+  epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
 }
 
 // Head phase end: per-token argmax of the CTA, then the last CTA to finish reduces all CTAs in a
@@ -635,10 +666,9 @@ __device__ __forceinline__ void grid_barrier(const Io& io, int G, SmemMisc& sm) 
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant__ Program prog,
                                                            const __grid_constant__ Io io) {
-  constexpr int kSlots = ring_slots(NT);
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* xs = smem + ring_bytes(NT);
-  SmemMisc& sm = *reinterpret_cast<SmemMisc*>(smem + ring_bytes(NT) + x_bytes(NT));
+  uint8_t* xs = smem + kRingBytes;
+  SmemMisc& sm = *reinterpret_cast<SmemMisc*>(smem + kRingBytes + kXBytes);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
   const int G = gridDim.x, cta = blockIdx.x;
 
@@ -667,8 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     const Phase& ph = prog.ph[p];
     Slice S;
     const int sidx = slice_of_cta(ph, G, cta, S);
-    const int ck = chunk_k(ph.fmt);
-    stage_x<NT>(prog, ph, io, S.kc0 * ck, S.kcn * ck, xs, sm);
+    const int ck = chunk_k(ph.fmt), kc0 = S.kg0 * ph.grp;
+    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
     float tsc[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -687,7 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     const int ub = range_begin(S, w), ue = range_begin(S, w + 1);
     const uint32_t xlane = smem_addr(xs) + lane * 16;
     const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
-    int rb = ub < ue ? ub / S.kcn : 0, kcl = ub < ue ? ub - rb * S.kcn : 0;
+    const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
+    const bool two = ph.layout == kInterleaved;
+    int rb = ub < ue ? ub / S.kgn : 0, kgl = ub < ue ? ub - rb * S.kgn : 0;
     float acc[NT][4], acc2[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -710,11 +742,20 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         sm.abort = 1;
         atomicExch(io.status, kStatusTimeout);
       }
-      const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kcl * pair_stride;
-      if (ph.fmt == kFmtNvfp4)
-        unit_nvfp4<NT>(ua, xa, lane, acc, acc2);
-      else
-        unit_fp8<NT>(ua, xa, lane, acc, acc2);
+      const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kgl * ph.grp * pair_stride;
+      if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
+        unit_nvfp4<NT>(ua, xa, lane, acc, acc);
+        unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
+      } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
+        const bool second = (S.kg0 + kgl) * ph.grp + 1 < ph.KC;
+        if (ph.fmt == kFmtNvfp4) {
+          unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+          if (second) unit_nvfp4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
+        } else {
+          unit_fp8<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+          if (second) unit_fp8<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
+        }
+      }
       __syncwarp();
       if (lane == 0 && pc.p < prog.n && !sm.abort) {
         fence_proxy_async_smem();
@@ -723,8 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         ++issued;
       }
       ++seq;
-      if (++kcl == S.kcn) {
-        kcl = 0;
+      if (++kgl == S.kgn) {
+        kgl = 0;
         ++rb;
       }
     }

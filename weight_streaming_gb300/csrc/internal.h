@@ -10,8 +10,8 @@ namespace vp {
 // A matrix [N][K] (N % 16 == 0) is stored as row blocks of 16 rows; each row block as K chunks
 // (256 weights wide for NVFP4, 128 for FP8); each chunk as two 8-row strips (rows 0-7, then 8-15 of
 // the block).  Row block rb, chunk kc, strip t starts at ((rb * KC + kc) * 2 + t) * strip bytes, so
-// a row block's stream along K is contiguous and one chunk of a row block (a "unit") is one
-// 2304-byte (NVFP4) or 2048-byte (FP8) copy.
+// a row block's stream along K is contiguous: one chunk of a row block is 2304 (NVFP4) or 2048
+// (FP8) contiguous bytes, and so is any run of consecutive chunks.
 //
 // Inside a strip, thread (g = lane / 4, c = lane % 4) of a warp owns row g and, in every 16-wide k
 // step s of the chunk, the four weights k = 16 s + 4 c .. + 3 (the mma.sync A fragment with the k
@@ -35,35 +35,34 @@ __host__ __device__ inline size_t strip_offset(int fmt, int KC, int rb, int kc, 
 
 // ---------------------------------------------------------------- executor geometry
 // One persistent CTA per SM, 16 warps.  Every warp streams its own contiguous range of units
-// through a private shared-memory ring filled by bulk copies it issues itself, and runs the
-// dequantisation + warp MMAs of each unit from there.  The rest of shared memory holds the
-// activations of the CTA's K slice as f16 MMA fragments.  The ring is as deep as the activations
-// leave room for: what a warp has in flight while it computes is what hides the DRAM latency
-// (about 2.5 us when the whole GPU streams).
+// through a private 2-slot shared-memory ring filled by bulk copies it issues itself, and runs the
+// dequantisation + warp MMAs of each unit from there.  A unit is one "group" of K chunks of a
+// virtual row block: two consecutive chunks of one row block (plain layout: one 4608 / 4096-byte
+// copy), or one chunk of a gate row block and the same chunk of the matching up row block
+// (interleaved layout: two 2304-byte copies).  Copies of this size keep a warp's ring streaming at
+// full DRAM rate (many smaller copies queue up and lengthen the latency).  The rest of shared
+// memory holds the activations of the CTA's K slice as f16 MMA fragments.
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxSlots = 4;
-constexpr int kSlotBytes = 2304;
+constexpr int kSlots = 2;
+constexpr int kSlotBytes = 4608;
+constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;  // 147,456
 constexpr int kMiscBytes = 2048;
 constexpr int kSmemBytes = 232448;  // 227 KB: the per-CTA maximum
+constexpr int kXBytes = kSmemBytes - kRingBytes - kMiscBytes;
 constexpr int kMaxGrid = 256;
 constexpr int kWarpsBound = kMaxGrid * kWarps;  // bound on the warps of any slice (fixup slot count)
 
-// Ring slots per warp for NT n-tiles of 8 tokens, and the shared memory left for activations.
-__host__ __device__ constexpr int ring_slots(int NT) { return NT == 1 ? 4 : 3; }
-__host__ __device__ constexpr int ring_bytes(int NT) { return kWarps * ring_slots(NT) * kSlotBytes; }
-__host__ __device__ constexpr int x_bytes(int NT) { return kSmemBytes - ring_bytes(NT) - kMiscBytes; }
-
-// Widest K slice whose activations fit in x_bytes(NT) (16 NT bytes per k) and that the staging
-// threads hold in registers (128 k per thread of a row): a multiple of both chunk widths.
-__host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 5120 : NT == 2 ? 3584 : NT == 3 ? 2048 : 1792; }
-static_assert(16 * 1 * 5120 <= x_bytes(1) && 16 * 2 * 3584 <= x_bytes(2) && 16 * 3 * 2048 <= x_bytes(3) &&
-                  16 * 4 * 1792 <= x_bytes(4),
+// Widest K slice whose activations fit in kXBytes (16 NT bytes per k, NT n-tiles of 8 tokens) and
+// that the staging threads hold in registers (128 k per thread of a row): a multiple of 512.
+__host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 5120 : NT == 2 ? 2560 : NT == 3 ? 1536 : 1024; }
+static_assert(16 * 1 * 5120 <= kXBytes && 16 * 2 * 2560 <= kXBytes && 16 * 3 * 1536 <= kXBytes &&
+                  16 * 4 * 1024 <= kXBytes,
               "activation slices fit the shared memory left by the ring");
 
 enum Layout : int {
-  kPlain = 0,        // virtual row blocks = the row blocks of w0, then of w1 (from row block rb1)
-  kInterleaved = 1,  // virtual row block rb = 8-row strip rb of w0 (rows 0-7) + strip rb of w1 (rows 8-15)
+  kPlain = 0,        // virtual row blocks = the row blocks of w0, then of w1 (from row block rb1); groups of 2 chunks
+  kInterleaved = 1,  // virtual row block rb = row block rb of w0 and of w1 (gate and up); groups of 1 chunk
 };
 enum Epi : int {
   kEpiF32 = 0,    // y[m][n] = s * acc
@@ -80,6 +79,7 @@ struct Phase {
   const uint8_t* w1;
   float s0, s1;     // fp32 scale of w0 / w1 (NVFP4 tensor scale or FP8 per-tensor scale)
   int K, KC;        // reduction length and its chunk count
+  int grp, KG;      // chunks per unit (2 plain, 1 interleaved) and groups along K (ceil(KC / grp))
   int RB, rb1;      // virtual row blocks; first row block of w1 (plain; RB if none)
   int cmax;         // fixup slots per (row block, K slice)
   int8_t fmt, layout, epi, ks;  // ks: K slices
@@ -108,7 +108,7 @@ struct Io {
   unsigned* head_cnt;
   float* head_aux;     // [kMaxGrid][kMaxM][2]
   unsigned* rb_cnt;    // [max RB]
-  float* partials;     // fixup slots: [RB][ks][cmax][32 lanes][4 NT]
+  float* partials;     // fixup slots: [RB][ks][cmax][32 lanes][4 NT (plain) or 8 NT (interleaved)]
 };
 
 // ---------------------------------------------------------------- workspace carving
@@ -118,7 +118,8 @@ struct WsLayout {
   size_t status, bar, head_cnt, head_aux, rb_cnt, partials, total;
 };
 
-// max_rb: largest RB of the program's phases; max_slots: largest RB * ks * cmax.
+// max_rb: largest RB of the program's phases; max_slots: largest RB * ks * cmax (in units of
+// 32 lanes x 4 NT floats; an interleaved phase's slots count twice).
 inline WsLayout ws_layout(size_t max_rb, size_t max_slots, int NT) {
   WsLayout L;
   L.status = 0;
@@ -132,15 +133,15 @@ inline WsLayout ws_layout(size_t max_rb, size_t max_slots, int NT) {
 }
 
 // Fixup slots a phase needs per (row block, K slice): the most warps whose unit ranges can meet one
-// row block's kcn units, for any grid of at most kMaxGrid CTAs (every non-empty warp range holds at
+// row block's kgn units, for any grid of at most kMaxGrid CTAs (every non-empty warp range holds at
 // least floor(U / kWarpsBound) units).
-inline int phase_cmax(int RB, int KC, int ks) {
+inline int phase_cmax(int RB, int KG, int ks) {
   int cm = 1;
   for (int s = 0; s < ks; ++s) {
-    const int kcn = (int)((long long)(s + 1) * KC / ks - (long long)s * KC / ks);
-    const long long ufl = (long long)RB * kcn / kWarpsBound;
-    int c = ufl == 0 ? kcn : (int)((kcn + ufl - 1) / ufl) + 1;
-    if (c > kcn) c = kcn;
+    const int kgn = (int)((long long)(s + 1) * KG / ks - (long long)s * KG / ks);
+    const long long ufl = (long long)RB * kgn / kWarpsBound;
+    int c = ufl == 0 ? kgn : (int)((kgn + ufl - 1) / ufl) + 1;
+    if (c > kgn) c = kgn;
     if (c > cm) cm = c;
   }
   return cm;
