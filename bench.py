@@ -69,11 +69,13 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Every rank's value of x (all-gather; CPU tensors under gloo, device tensors under NCCL)."""
     if world <= 1:
         return [x]
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cpu" if dist.get_backend() == "gloo" else "cuda"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     out = [torch.zeros_like(t) for _ in range(world)]
     dist.all_gather(out, t)
     return [float(o.item()) for o in out]

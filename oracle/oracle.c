@@ -26,6 +26,12 @@
  *  - Argmax: NaN is treated as -inf; -0 == +0; the lowest index among equal maxima wins.
  *  - The verify-pass surrogate (mixer cores replaced by slices) -- see orc_verify_pass().
  *
+ * Pins: every building block (formats, linear, bf16 rounding, SiLU*up, RMSNorm, argmax, acceptance,
+ * byte table) is pinned by the tests against page values, closed forms, library routines or brute
+ * force.  orc_verify_pass is pinned through its parts and an independent composition on a tiny model;
+ * the long (64-layer) chain as a whole is parity unpinned -- end-to-end comparisons against it check
+ * only decisions that are unique and report the drift.
+ *
  * Everything is computed in fp64 from the plain definitions, with no blocking or reordering:
  * w[n][k] = e2m1(code) * e4m3(scale) * ts, y[m][n] = sum_k x[m][k] * w[n][k].
  */
