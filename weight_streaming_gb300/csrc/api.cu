@@ -78,7 +78,7 @@ Phase make_phase(const PhaseSpec& s, int NT) {
   ph.KC = s.K / chunk_k(s.fmt);
   ph.RB = (s.rows0 + s.rows1) / kRowBlock;
   if (s.layout == kPlain) {
-    ph.grp = 2;
+    ph.grp = 2;  // units of two chunks: one 4096 / 4608-byte copy (smaller copies stream slower)
     ph.rb1 = s.rows0 / kRowBlock;
   } else {
     ph.grp = 1;

@@ -339,7 +339,8 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
 // acc2 (the caller passes the same array twice for one chain).  ua: the chunk in the slot; xa: this
 // lane's fragments of the chunk's first k-step pair.
 template <int NT>
-__device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4], float (&acc2)[NT][4]) {
+__device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4],
+                                           float (&acc2)[NT][4]) {
   const int g = lane >> 2;
   const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
   const uint4 c1a = lds128(ua + 1152 + lane * 16), c1b = lds128(ua + 1152 + 512 + lane * 16);
@@ -376,7 +377,8 @@ __device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, f
 }
 
 template <int NT>
-__device__ __forceinline__ void unit_fp8(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4], float (&acc2)[NT][4]) {
+__device__ __forceinline__ void unit_fp8(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4],
+                                         float (&acc2)[NT][4]) {
   const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
   const uint4 c1a = lds128(ua + 1024 + lane * 16), c1b = lds128(ua + 1024 + 512 + lane * 16);
   const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
@@ -635,31 +637,35 @@ __device__ __noinline__ void head_finish(const Program& prog, const Io& io, int 
 }
 
 // ---------------------------------------------------------------- grid barrier
-// Sense-free generation barrier on two workspace words (arrivals, generation): the last CTA to
-// arrive resets the count and bumps the generation; the others poll it (bounded).
-__device__ __forceinline__ void grid_barrier(const Io& io, int G, SmemMisc& sm) {
+// One monotonic arrival counter per launch: barrier b releases once it reaches G * (b + 1), so the
+// last CTA to arrive has nothing more to do (its atomic is the release) and the others poll one
+// word.  The last CTA to leave the kernel resets the counter (and the exit counter) for the next
+// launch.
+__device__ __forceinline__ void grid_barrier(const Io& io, int G, unsigned target, SmemMisc& sm) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_gpu(io.bar + 1);
     __threadfence();
-    const unsigned arrived = atomicAdd(io.bar, 1u);
-    if (arrived + 1 == (unsigned)G) {
-      atomicExch(io.bar, 0u);
-      __threadfence();
-      st_release_gpu(io.bar + 1, gen + 1u);
-    } else if (!sm.abort) {
+    const unsigned arrived = atomicAdd(io.bar, 1u) + 1u;
+    if (arrived < target && !sm.abort) {
       uint32_t n = 0;
-      while (ld_acquire_gpu(io.bar + 1) == gen) {
-        if (++n > (1u << 21)) {  // about 1-2 s
+      while (ld_acquire_gpu(io.bar) < target) {
+        if (++n > (1u << 22)) {  // about 1-2 s
           sm.abort = 1;
           atomicExch(io.status, kStatusTimeout);
           break;
         }
-        if (n > 64) __nanosleep(64);
+        if (n > 256) __nanosleep(32);
       }
     }
   }
   __syncthreads();
+}
+__device__ __forceinline__ void grid_exit(const Io& io, int G) {
+  __syncthreads();
+  if (threadIdx.x == 0 && atomicAdd(io.bar + 1, 1u) + 1u == (unsigned)G) {
+    atomicExch(io.bar, 0u);
+    atomicExch(io.bar + 1, 0u);
+  }
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -747,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         unit_nvfp4<NT>(ua, xa, lane, acc, acc);
         unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
       } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
-        const bool second = (S.kg0 + kgl) * ph.grp + 1 < ph.KC;
+        const bool second = ph.grp == 2 && (S.kg0 + kgl) * 2 + 1 < ph.KC;
         if (ph.fmt == kFmtNvfp4) {
           unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
           if (second) unit_nvfp4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
@@ -771,11 +777,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     }
     if (cur >= 0) flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
     if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
-    if (p + 1 < prog.n) grid_barrier(io, G, sm);
+    if (p + 1 < prog.n) grid_barrier(io, G, (unsigned)G * (unsigned)(p + 1), sm);
   }
   // Copies still in flight (only after a timeout): wait for them before the CTA's memory goes away.
   if (lane == 0)
     for (unsigned k = seq; k < issued; ++k) mbar_wait_bounded(&sm.full[warp][k % kSlots], (k / kSlots) & 1u);
+  if (prog.n > 1) grid_exit(io, G);
 }
 
 }  // namespace vp

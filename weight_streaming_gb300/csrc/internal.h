@@ -56,8 +56,8 @@ constexpr int kWarpsBound = kMaxGrid * kWarps;  // bound on the warps of any sli
 // Widest K slice whose activations fit in kXBytes (16 NT bytes per k, NT n-tiles of 8 tokens) and
 // that the staging threads hold in registers (128 k per thread of a row): a multiple of 512.
 __host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 5120 : NT == 2 ? 2560 : NT == 3 ? 1536 : 1024; }
-static_assert(16 * 1 * 5120 <= kXBytes && 16 * 2 * 2560 <= kXBytes && 16 * 3 * 1536 <= kXBytes &&
-                  16 * 4 * 1024 <= kXBytes,
+static_assert(16 * 1 * ks_max(1) <= kXBytes && 16 * 2 * ks_max(2) <= kXBytes && 16 * 3 * ks_max(3) <= kXBytes &&
+                  16 * 4 * ks_max(4) <= kXBytes,
               "activation slices fit the shared memory left by the ring");
 
 enum Layout : int {
@@ -104,7 +104,7 @@ struct Io {
   size_t trace_stride;  // elements between trace slots
   // workspace
   int* status;
-  unsigned* bar;       // [0] arrivals, [1] generation
+  unsigned* bar;       // [0] barrier arrivals (monotonic within a launch), [1] CTAs that finished
   unsigned* head_cnt;
   float* head_aux;     // [kMaxGrid][kMaxM][2]
   unsigned* rb_cnt;    // [max RB]
