@@ -616,20 +616,26 @@ __device__ __noinline__ void head_finish(const Program& prog, const Io& io, int 
   __syncthreads();
   if (!sm.flag) return;
   __threadfence();
-  if (tid < M) {
+  // Warp w reduces tokens w, w + 16 (its lanes stride over the CTAs, then a warp reduction); the
+  // winner (largest value, then lowest index) is the same in any order.
+  for (int t = warp; t < M; t += kWarps) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int c = 0; c < G; ++c) {
-      const float2 e = __ldcg(reinterpret_cast<const float2*>(io.head_aux) + (size_t)c * kMaxM + tid);
+    for (int c = lane; c < G; c += 32) {
+      const float2 e = __ldcg(reinterpret_cast<const float2*>(io.head_aux) + (size_t)c * kMaxM + t);
       const int ei = __float_as_int(e.y);
       if (am_better(e.x, ei, bv, bi)) {
         bv = e.x;
         bi = ei;
       }
     }
-    if (bi == 0x7fffffff) bi = 0;
-    sm.tok[tid] = bi;
-    io.argmax[tid] = bi;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) am_shfl_xor(bv, bi, o);
+    if (lane == 0) {
+      if (bi == 0x7fffffff) bi = 0;
+      sm.tok[t] = bi;
+      io.argmax[t] = bi;
+    }
   }
   __syncthreads();
   if (tid < M / 8) accept_lane(tid, sm.tok, io.pending, io.n_commit, io.committed);
