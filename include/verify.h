@@ -236,6 +236,16 @@ vp_status vp_verify_blocks(const vp_model* model, void* h, int M, int block_begi
  * after one device-to-device copy of x0. */
 int vp_pass_launch_count(const vp_model* model);
 
+/* The executor's phase timeline (no counterpart in the pages: a measurement aid).  Only a library
+ * built with VP_PHASE_TRACE (libverify_trace.so) records it; any other build returns
+ * VP_ERR_UNSUPPORTED.  Copies up to `bytes` of the timeline of the kernels that serve M rows into the
+ * host buffer dst: uint64 [2][160][256][36], indexed [launch parity][phase of the launch][CTA][slot]
+ * with globaltimer stamps in ns -- slot 0 phase start, 1 end of the activation staging, 2 + w warp w
+ * done with its units, 18 + w warp w done with its fixups, 34 grid barrier passed -- and the number
+ * of multi-phase launches completed so far into *launches (a launch writes buffer launches % 2).
+ * Synchronous (waits for the device). */
+vp_status vp_trace_read(int M, void* dst, size_t bytes, unsigned* launches);
+
 #ifdef __cplusplus
 }
 #endif

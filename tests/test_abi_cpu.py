@@ -123,3 +123,16 @@ def test_model_create_validation_without_gpu(V):
     bad.w_up = FAKE + 4
     with pytest.raises(V.VerifyError):
         V.vp_model(256, 512, 1e-6, [bad], head)
+
+
+def test_phase_trace_only_in_traced_build(V):
+    """The phase timeline is recorded only by the VP_PHASE_TRACE build; the product library says so
+    without touching a device."""
+    import numpy as np
+    buf = np.zeros(16, np.uint64)
+    with pytest.raises(V.VerifyError) as e:
+        V.vp_trace_read(8, buf)
+    assert e.value.status == V.VP_ERR_UNSUPPORTED
+    with pytest.raises(V.VerifyError) as e:
+        V.vp_trace_read(0, buf)
+    assert e.value.status == V.VP_ERR_SHAPE

@@ -11,7 +11,8 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libverify.so")
+# VP_LIBVERIFY may name another build of the same library (the phase-traced libverify_trace.so).
+LIB_PATH = os.environ.get("VP_LIBVERIFY") or os.path.join(_PKG, "libverify.so")
 
 VP_OK, VP_ERR_INVALID_ARG, VP_ERR_SHAPE, VP_ERR_ALIGNMENT, VP_ERR_WORKSPACE, VP_ERR_CUDA, VP_ERR_TIMEOUT, \
     VP_ERR_UNSUPPORTED = range(8)
@@ -24,7 +25,7 @@ EXPORTS = [
     "vp_packed_bytes_fp8", "vp_pack_nvfp4", "vp_pack_fp8", "vp_workspace_bytes", "vp_linear_nvfp4",
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
-    "vp_linear_nvfp4_noalloc",
+    "vp_linear_nvfp4_noalloc", "vp_trace_read",
 ]
 
 
@@ -79,6 +80,7 @@ def _load():
         "vp_verify_blocks": (I, [P, P, I, I, I, P, P, S, P]),
         "vp_pass_launch_count": (I, [P]),
         "vp_linear_nvfp4_noalloc": (I, [P, F, P, P, I, I, I, P]),
+        "vp_trace_read": (I, [I, P, S, ctypes.POINTER(ctypes.c_uint)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -233,3 +235,12 @@ def vp_verify_blocks(model: vp_model, h, M: int, block_begin: int, block_end: in
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check("vp_verify_blocks", _L.vp_verify_blocks(model.handle, _ptr(h), M, block_begin, block_end, _ptr(trace),
                                                    _ptr(ws), wb, _stream(stream)))
+
+
+def vp_trace_read(M: int, dst) -> int:
+    """Copies the executor's phase timeline into the numpy array `dst` (uint64, up to
+    [2][160][256][36]) and returns the number of multi-phase launches completed; raises VerifyError
+    (VP_ERR_UNSUPPORTED) unless this is the phase-traced build."""
+    n = ctypes.c_uint(0)
+    _check("vp_trace_read", _L.vp_trace_read(M, dst.ctypes.data, dst.nbytes, ctypes.byref(n)))
+    return n.value

@@ -16,6 +16,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libverify.so")
+# The same library with the executor's phase timeline recorded (trace.cuh): a measurement build.
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libverify_trace.so")
 SOURCES = ["api.cu", "exec_nt12.cu", "exec_nt34.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -35,17 +38,20 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Builds libverify.so (or, with trace=True, libverify_trace.so with the phase timeline) and
+    returns its path; nothing is rebuilt when the library is newer than every source."""
+    lib, bdir = (LIB_TRACE, BUILD_TRACE) if trace else (LIB, BUILD)
     deps = _inputs()
-    if not force and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and not _stale(lib, deps):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = ["nvcc", *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = ["nvcc", *ARCH, *FLAGS, *(["-DVP_PHASE_TRACE"] if trace else []), "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
@@ -58,11 +64,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     subprocess.run(["nvcc", *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -749,6 +749,14 @@ size_t vp_pass_workspace_bytes(const vp_model* model, int M) {
   return pass_ws(model, M).total;
 }
 
+vp_status vp_trace_read(int M, void* dst, size_t bytes, unsigned* launches) {
+  if (!dst || !launches) return VP_ERR_INVALID_ARG;
+  if (M < 1 || M > kMaxM) return VP_ERR_SHAPE;
+  const cudaError_t e = nt_of(M) <= 2 ? trace_read_nt12(dst, bytes, launches) : trace_read_nt34(dst, bytes, launches);
+  if (e == cudaErrorNotSupported) return VP_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
 int vp_pass_launch_count(const vp_model* model) {
   return model ? program_launches((int)model->phases[0].size()) : 0;
 }

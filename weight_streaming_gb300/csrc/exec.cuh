@@ -32,6 +32,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "trace.cuh"
 
 namespace vp {
 
@@ -671,6 +672,7 @@ __device__ __forceinline__ void grid_exit(const Io& io, int G) {
   if (threadIdx.x == 0 && atomicAdd(io.bar + 1, 1u) + 1u == (unsigned)G) {
     atomicExch(io.bar, 0u);
     atomicExch(io.bar + 1, 0u);
+    VP_TRACE_LAUNCH_DONE();
   }
 }
 
@@ -707,10 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
   unsigned seq = 0;
   for (int p = 0; p < prog.n; ++p) {
     const Phase& ph = prog.ph[p];
+    VP_TRACE(threadIdx.x == 0, p, 0);
     Slice S;
     const int sidx = slice_of_cta(ph, G, cta, S);
     const int ck = chunk_k(ph.fmt), kc0 = S.kg0 * ph.grp;
     stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
+    VP_TRACE(threadIdx.x == 0, p, 1);
     float tsc[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -781,9 +785,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         ++rb;
       }
     }
+    VP_TRACE(lane == 0, p, 2 + warp);
     if (cur >= 0) flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
     if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
+    VP_TRACE(lane == 0, p, 18 + warp);
     if (p + 1 < prog.n) grid_barrier(io, G, (unsigned)G * (unsigned)(p + 1), sm);
+    VP_TRACE(threadIdx.x == 0, p, 34);
   }
   // Copies still in flight (only after a timeout): wait for them before the CTA's memory goes away.
   if (lane == 0)

@@ -8,6 +8,10 @@ namespace vp {
 
 cudaError_t launch_exec_nt12(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
 cudaError_t launch_exec_nt34(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
+// Copies the phase timeline of the NT = 1-2 / 3-4 kernels (trace.cuh) and the count of completed
+// launches; cudaErrorNotSupported unless the library was built with VP_PHASE_TRACE.
+cudaError_t trace_read_nt12(void* dst, size_t bytes, unsigned* launches);
+cudaError_t trace_read_nt34(void* dst, size_t bytes, unsigned* launches);
 
 // Runs `prog` (NT = ceil(M / 8) n-tiles of 8 tokens) on `grid` CTAs; cooperative when the program
 // has grid barriers (more than one phase), so that every CTA is resident.

@@ -35,4 +35,20 @@ cudaError_t launch_exec_nt34(const Program& prog, const Io& io, int NT, int grid
   return NT == 3 ? launch_nt<3>(prog, io, grid, s, coop) : launch_nt<4>(prog, io, grid, s, coop);
 }
 
+
+// The phase timeline of the kernels of this translation unit (traced builds only).
+cudaError_t trace_read_nt34(void* dst, size_t bytes, unsigned* launches) {
+#ifdef VP_PHASE_TRACE
+  if (bytes > sizeof(g_trace)) bytes = sizeof(g_trace);
+  cudaError_t e = cudaMemcpyFromSymbol(dst, g_trace, bytes);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(launches, g_trace_launches, sizeof(unsigned));
+  return e;
+#else
+  (void)dst;
+  (void)bytes;
+  (void)launches;
+  return cudaErrorNotSupported;
+#endif
+}
+
 }  // namespace vp

@@ -1,0 +1,35 @@
+// Phase timeline of the streaming executor, compiled in only with -DVP_PHASE_TRACE (the
+// libverify_trace.so build); in the normal build every hook below is empty.
+//
+// For each phase p of a launch and each CTA, globaltimer stamps (ns): [0] phase start, [1] end of the
+// activation staging, [2 + w] warp w done with its units, [18 + w] warp w done with its row-block
+// fixups (and the head's argmax), [34] grid barrier passed.  Two launch buffers alternate (the
+// launch counter's parity), so the two launches of a verify pass keep both halves.
+#pragma once
+#include <cstdint>
+
+#include "internal.h"
+
+namespace vp {
+
+constexpr int kTraceSlots = 36;
+
+#ifdef VP_PHASE_TRACE
+__device__ unsigned long long g_trace[2][kMaxPhases][kMaxGrid][kTraceSlots];
+__device__ unsigned g_trace_launches;  // launches completed (the last CTA to leave counts)
+__device__ __forceinline__ void trace_stamp(int p, int slot) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  g_trace[*reinterpret_cast<volatile unsigned*>(&g_trace_launches) & 1u][p][blockIdx.x][slot] = t;
+}
+#define VP_TRACE(cond, p, slot)                   \
+  do {                                            \
+    if (cond) ::vp::trace_stamp((p), (slot));     \
+  } while (0)
+#define VP_TRACE_LAUNCH_DONE() atomicAdd(&::vp::g_trace_launches, 1u)
+#else
+#define VP_TRACE(cond, p, slot) ((void)0)
+#define VP_TRACE_LAUNCH_DONE() ((void)0)
+#endif
+
+}  // namespace vp

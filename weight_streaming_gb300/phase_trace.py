@@ -1,0 +1,113 @@
+"""Phase timeline of a verify pass: where the time of each phase kind goes.
+
+Builds the phase-traced library (libverify_trace.so: the same kernels with globaltimer stamps at each
+phase start, end of staging, end of each warp's units and fixups, and the grid barrier; see
+csrc/trace.cuh), runs verify passes of a synthetic model on one GPU and prints, per phase kind, the
+mean over the last pass's phases of (us):
+
+  staging        phase start -> activations staged (slowest CTA)
+  stream med/max staging done -> a warp's units done (median / slowest warp)
+  fixup tail     last warp's units done -> last warp's fixups done
+  release        last fixup done -> first CTA past the grid barrier
+  phase          phase start -> next phase start
+
+  python -m weight_streaming_gb300.phase_trace [--layers 16] [--M 8] [--save timeline.npy]
+
+The stamps cost a few global stores per phase and CTA; the traced pass runs within ~2 % of the
+untraced one.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import numpy as np
+
+KINDS = ("mixer in", "mixer out", "gate+up", "down")
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--M", type=int, default=8)
+    ap.add_argument("--passes", type=int, default=5)
+    ap.add_argument("--save", default=None, help="write the last pass's stamps [phase][CTA][slot] (.npy)")
+    args = ap.parse_args(argv)
+
+    from .build import build
+    os.environ["VP_LIBVERIFY"] = build(trace=True)
+    import torch
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import synth
+    from . import _lib as V
+    from .model import Geometry, SyntheticModel
+
+    M = args.M
+    geom = Geometry(n_layers=args.layers)
+    sm = SyntheticModel(geom, seed=0)
+    H = geom.hidden
+    x0 = torch.from_numpy(synth.normal_bf16(0, synth.stream_id(0, synth.T_X0), (M, H)).view(np.int16))
+    x0 = x0.cuda().view(torch.bfloat16)
+    t = synth.uniform_ints(0, synth.stream_id(0, synth.T_PENDING) + 7, 0, M, geom.vocab)
+    pending, _ = synth.planted_pending(0, t, geom.vocab)
+    pend = torch.from_numpy(pending).cuda()
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    nc = torch.empty(M // 8, dtype=torch.int32, device="cuda")
+    cm = torch.empty((M // 8, 8), dtype=torch.int32, device="cuda")
+    ws = sm.workspace(M)
+    for _ in range(args.passes):
+        sm.run(x0, pend, am, nc, cm, ws)
+    torch.cuda.synchronize()
+    assert V.vp_read_status(ws) == V.VP_OK
+
+    n_ph = 4 * args.layers + 1
+    per_launch = 160
+    launches = (n_ph + per_launch - 1) // per_launch
+    buf = np.zeros((2, per_launch, 256, 36), np.uint64)
+    done = V.vp_trace_read(M, buf)
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = []  # the last pass: launch l holds phases [l * n / launches, (l + 1) * n / launches)
+    last_of_launch = set()
+    for l in range(launches):
+        p0, p1 = l * n_ph // launches, (l + 1) * n_ph // launches
+        par = (done - launches + l) & 1
+        for p in range(p1 - p0):
+            rows.append(buf[par, p, :G, :].astype(np.int64))
+        last_of_launch.add(p1 - 1)
+    T = np.stack(rows)
+    if args.save:
+        np.save(args.save, T)
+
+    stats = {}
+    for gp in range(n_ph):
+        kind = "head" if gp == n_ph - 1 else KINDS[gp % 4]
+        S = T[gp]
+        t0, t1, t2, t3, t4 = S[:, 0], S[:, 1], S[:, 2:18], S[:, 18:34], S[:, 34]
+        d = {"staging": (t1 - t0).max(), "stream med": np.median(t2 - t1[:, None]),
+             "stream max": (t2 - t1[:, None]).max(), "fixup tail": t3.max() - t2.max()}
+        if gp not in last_of_launch:  # the last phase of a launch has no barrier after it
+            d["release"] = t4.min() - t3.max()
+            d["phase"] = T[gp + 1][:, 0].min() - t0.min()
+        stats.setdefault(kind, []).append(d)
+    cols = ["staging", "stream med", "stream max", "fixup tail", "release", "phase"]
+    print(f"verify pass, {args.layers} layers, M = {M}: mean per phase kind (us)")
+    print(f"{'phase kind':12s} {'n':>4s} " + " ".join(f"{c:>11s}" for c in cols))
+    for kind in KINDS + ("head",):
+        lst = stats.get(kind, [])
+        if not lst:
+            continue
+        vals = []
+        for c in cols:
+            v = [x[c] for x in lst if c in x]
+            vals.append(f"{np.mean(v) / 1e3:11.2f}" if v else f"{'-':>11s}")
+        print(f"{kind:12s} {len(lst):4d} " + " ".join(vals))
+    total = (T[-1][:, 18:34].max() - T[0][:, 0].min()) / 1e3
+    print(f"first phase start -> last phase done: {total:.1f} us")
+
+
+if __name__ == "__main__":
+    main()
