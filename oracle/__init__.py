@@ -13,6 +13,8 @@ the passage of the pages it follows:
   "The megakernel is per layer, not per step" (greedy acceptance, 1..8 tokens per round).
 * "144 tok/s needs 502 GB/s" (Splash) -- "The engine hard-codes the model" (geometry).
 * "Beating Splash on an M5 Max" -- "The bugs a second reviewer found" (one argmax tie rule).
+* "144 tok/s needs 502 GB/s" -- "The engine hard-codes the model" (the affine 4-bit "Q4" format:
+  per group of 64 inputs, 32 bytes of codes, a bf16 scale and a bf16 bias; ``linear_q4``).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against page values,
 closed forms, library routines or brute force, except the 64-layer surrogate chain, whose
@@ -79,6 +81,11 @@ def lib():
             L.orc_linear.restype = ctypes.c_int
             L.orc_linear.argtypes = [ctypes.c_int, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P,
                                      ctypes.c_double, P, ctypes.c_int64, P, P, ctypes.c_int]
+            L.orc_linear_q4.restype = ctypes.c_int
+            L.orc_linear_q4.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, P, P, ctypes.c_int64,
+                                        P, P, ctypes.c_int]
+            L.orc_q4_bytes.restype = ctypes.c_int64
+            L.orc_q4_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
             L.orc_silu_mul.argtypes = [P, P, ctypes.c_int64, P]
             L.orc_rmsnorm.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
             L.orc_argmax.restype = ctypes.c_int64
@@ -154,6 +161,34 @@ def linear(fmt: int, x_bf16: np.ndarray, codes: np.ndarray, scales: np.ndarray |
     if rc != 0:
         raise ValueError("orc_linear rejected its arguments")
     return (y, a) if with_abs else y
+
+
+def linear_q4(x_bf16: np.ndarray, codes: np.ndarray, scales: np.ndarray, biases: np.ndarray, N: int,
+              rows: np.ndarray | None = None, with_abs: bool = True, nthreads: int | None = None):
+    """Affine INT4 linear: y[m][i] = sum_k x[m][k] (scale * q + bias)[rows[i]][k] (fp64), and
+    a = sum_k |x| (|scale * q| + |bias|) (tolerance scale).  codes uint8 [N][K/2] (low nibble first),
+    scales / biases bf16 bit patterns (uint16) [N][K/64]."""
+    x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    M, K = x_bf16.shape
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.uint16)
+    bi = np.ascontiguousarray(biases, dtype=np.uint16)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        n_rows = rows.size
+    else:
+        n_rows = N
+    y = np.zeros((M, n_rows), np.float64)
+    a = np.zeros((M, n_rows), np.float64) if with_abs else None
+    rc = lib().orc_linear_q4(_p(x_bf16), M, K, N, _p(codes), _p(sc), _p(bi), _p(rows) if rows is not None else None,
+                             n_rows, _p(y), _p(a) if a is not None else None, nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("orc_linear_q4 rejected its arguments")
+    return (y, a) if with_abs else y
+
+
+def q4_bytes(N: int, K: int) -> int:
+    return int(lib().orc_q4_bytes(N, K))
 
 
 def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:

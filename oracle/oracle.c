@@ -18,12 +18,16 @@
  *    geometry (64 layers, hidden 5120, vocab 248320, intermediate 17408, fullAttentionPeriod = 4).
  *  - "Beating Splash on an M5 Max", section "The bugs a second reviewer found": the argmax tie
  *    rule must be the same everywhere (here: lowest index among equal maxima).
+ *  - "144 tok/s needs 502 GB/s", section "The engine hard-codes the model": the other engines'
+ *    affine 4-bit format (32 bytes of codes + a bf16 scale + a bf16 bias per group of 64 inputs) --
+ *    see orc_linear_q4().
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *  - E2M1 bit layout: bit 3 = sign, bits 2..1 = exponent (bias 1), bit 0 = mantissa (OCP MX).
  *  - Packing of two E2M1 codes per byte: element 2j is the LOW nibble of byte j.
  *  - Block scales run along K: scale[n][k/16].
  *  - Argmax: NaN is treated as -inf; -0 == +0; the lowest index among equal maxima wins.
+ *  - Q4: unsigned codes, w = scale * q + bias, groups of 64 along K, low nibble first.
  *  - The verify-pass surrogate (mixer cores replaced by slices) -- see orc_verify_pass().
  *
  * Pins: every building block (formats, linear, bf16 rounding, SiLU*up, RMSNorm, argmax, acceptance,
@@ -210,6 +214,80 @@ int orc_linear(int fmt, const uint16_t* x_bf16, int M, int K, int N, const uint8
     free(x);
     return 0;
 }
+
+/* ------------------------------------------------------------------ affine INT4 ("Q4") linear
+ *
+ * "144 tok/s needs 502 GB/s, and Apple sells two M5 Max chips", section "The engine hard-codes the
+ * model": the other engines' 4-bit format packs nine bytes per sixteen weights -- for every group of
+ * 64 inputs, 32 bytes of 4-bit codes plus a bf16 scale and a bf16 bias.  Readings (the page gives no
+ * formula): the code q is unsigned (0..15) and the weight is the affine map w = scale * q + bias;
+ * groups run along K (scale[n][k/64]); element 2j is the low nibble of byte j (as for NVFP4).
+ * "Beating Splash on an M5 Max", section "What actually moved the needle": the producers emit the
+ * per-group input sums the Q4 tiles need -- that is an implementation route to the same y, not a
+ * different result, so the oracle keeps the plain definition below. */
+
+typedef struct {
+    const double* x; /* [M][K] */
+    int M, K, N;
+    const uint8_t* codes;   /* [N][K/2] */
+    const uint16_t* scales; /* [N][K/64] bf16 */
+    const uint16_t* biases; /* [N][K/64] bf16 */
+    const int32_t* rows;
+    double* y;
+    double* a; /* sum_k |x| (|scale * q| + |bias|): the magnitude of both terms of every weight */
+    int64_t n_rows;
+} orc_q4_ctx;
+
+static void orc_q4_row(void* p, int64_t i) {
+    orc_q4_ctx* c = (orc_q4_ctx*)p;
+    int64_t n = c->rows ? c->rows[i] : i;
+    int K = c->K;
+    double* w = (double*)malloc(sizeof(double) * (size_t)K * 2);
+    if (!w) return;
+    double* wa = w + K;
+    const uint8_t* cr = c->codes + n * (int64_t)(K / 2);
+    const uint16_t* sr = c->scales + n * (int64_t)(K / 64);
+    const uint16_t* br = c->biases + n * (int64_t)(K / 64);
+    for (int k = 0; k < K; ++k) {
+        int byte = cr[k / 2];
+        int q = (k & 1) ? (byte >> 4) : (byte & 15);
+        double sc = orc_bf16_value(sr[k / 64]), bi = orc_bf16_value(br[k / 64]);
+        w[k] = sc * (double)q + bi;
+        wa[k] = fabs(sc * (double)q) + fabs(bi);
+    }
+    for (int m = 0; m < c->M; ++m) {
+        const double* xr = c->x + (int64_t)m * K;
+        double s = 0.0, sa = 0.0;
+        for (int k = 0; k < K; ++k) {
+            s += xr[k] * w[k];
+            sa += fabs(xr[k]) * wa[k];
+        }
+        c->y[(int64_t)m * c->n_rows + i] = s;
+        if (c->a) c->a[(int64_t)m * c->n_rows + i] = sa;
+    }
+    free(w);
+}
+
+/* y[m][i] = sum_k x[m][k] * (scale * q + bias)[rows[i]][k] in fp64 (x: bf16 bit patterns [M][K]).
+ * Returns 0, or -1 on bad arguments (K must be a multiple of 64). */
+int orc_linear_q4(const uint16_t* x_bf16, int M, int K, int N, const uint8_t* codes, const uint16_t* scales,
+                  const uint16_t* biases, const int32_t* rows, int64_t n_rows, double* y, double* a,
+                  int nthreads) {
+    if (M < 0 || K <= 0 || K % 64 != 0 || N <= 0 || !x_bf16 || !codes || !scales || !biases || !y) return -1;
+    if (!rows) n_rows = N;
+    for (int64_t i = 0; rows && i < n_rows; ++i)
+        if (rows[i] < 0 || rows[i] >= N) return -1;
+    double* x = (double*)malloc(sizeof(double) * (size_t)M * (size_t)K + 8);
+    if (!x) return -1;
+    for (int64_t i = 0; i < (int64_t)M * K; ++i) x[i] = orc_bf16_value(x_bf16[i]);
+    orc_q4_ctx c = {x, M, K, N, codes, scales, biases, rows, y, a, n_rows};
+    orc_parallel(nthreads, n_rows, orc_q4_row, &c);
+    free(x);
+    return 0;
+}
+
+/* Packed bytes of an N x K Q4 matrix: per group of 64 weights, 32 bytes of codes + 2 + 2. */
+int64_t orc_q4_bytes(int64_t N, int64_t K) { return N * (K / 64) * (32 + 2 + 2); }
 
 /* ------------------------------------------------------------------ glue */
 

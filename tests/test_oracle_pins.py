@@ -393,3 +393,126 @@ def test_verify_pass_matches_independent_torch_composition():
     logits = (r @ torch.from_numpy(dequant_nvfp4_indep(head[0], head[1], head[2])).T).numpy()
     np.testing.assert_allclose(out["logits"], logits, rtol=1e-12, atol=1e-12)
     assert np.array_equal(out["argmax"], np.argmax(out["logits"], axis=1))
+
+
+# ------------------------------------------------------------------ affine INT4 ("Q4")
+
+def bf16_bits_of(values):
+    """bf16 bit patterns (uint16) of values that bf16 holds exactly."""
+    t = torch.tensor(np.asarray(values, np.float64)).to(torch.bfloat16)
+    assert np.array_equal(t.to(torch.float64).numpy(), np.asarray(values, np.float64))
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def dequant_q4_indep(codes, scales, biases):
+    """w = scale * q + bias per group of 64 along K, with torch's bf16 decoding (not the oracle)."""
+    N, K2 = codes.shape
+    q = np.empty((N, 2 * K2), np.float64)
+    q[:, 0::2] = codes & 15
+    q[:, 1::2] = codes >> 4
+    sv = np.repeat(bf16_vals_torch(scales), 64, axis=1)
+    bv = np.repeat(bf16_vals_torch(biases), 64, axis=1)
+    return sv * q + bv, np.abs(sv * q) + np.abs(bv)
+
+
+def test_q4_bytes_match_page_table():
+    """Nine bytes per sixteen weights reproduce the page's byte table of the 4-bit checkpoint."""
+    t = GOLD["q4_bytes_mb"]
+    shapes = {"gdn_in_16640x5120": (16640, 5120), "gdn_out_5120x6144": (5120, 6144),
+              "attn_in_14336x5120": (14336, 5120), "attn_out_5120x6144": (5120, 6144),
+              "lm_head_248320x5120": (248320, 5120), "token_embedding_248320x5120": (248320, 5120)}
+    for key, (n, k) in shapes.items():
+        assert round(oracle.q4_bytes(n, k) / 1e6, 2) == t[key], key
+        assert oracle.q4_bytes(n, k) * 16 == 9 * n * k
+    g = GOLD["geometry"]
+    mlp = 2 * oracle.q4_bytes(g["intermediate"], g["hidden"]) + oracle.q4_bytes(g["hidden"], g["intermediate"])
+    assert round(mlp / 1e6, 2) == t["swiglu_gate_up_down_per_layer"]
+    tot = GOLD["q4_target_total"]
+    total = (tot["layers_gdn"] * (oracle.q4_bytes(16640, 5120) + oracle.q4_bytes(5120, 6144))
+             + tot["layers_attention"] * (oracle.q4_bytes(14336, 5120) + oracle.q4_bytes(5120, 6144))
+             + g["layers"] * mlp + 2 * oracle.q4_bytes(g["vocab"], g["hidden"]))
+    assert round(total / 1e9 + tot["small_tensors_gb"], 3) == tot["gb"]
+
+
+def test_q4_one_hot_probes_cover_all_codes():
+    """x = e_k reproduces w[n][k] = scale * q + bias exactly: all 16 codes, scales and biases of both
+    signs and very different magnitudes, and the group boundary (k = 63 | 64) of every group."""
+    N, groups = 16, 6
+    K = 64 * groups
+    codes = np.zeros((N, K // 2), np.uint8)
+    for n in range(N):
+        codes[n, :] = n | (n << 4)
+    sv = [0.0078125, -0.5, 3.0, 2.0 ** -20, 96.0, 0.1015625]
+    bv = [-0.0546875, 1.25, -6.0, 2.0 ** -18, 0.0, -1000.0]
+    scales = np.tile(bf16_bits_of(sv), (N, 1))
+    biases = np.tile(bf16_bits_of(bv), (N, 1))
+    probes = []
+    for gi in range(groups):
+        probes += [64 * gi, 64 * gi + 63, 64 * gi + 17]
+    x = np.zeros((len(probes), K), np.uint16)
+    for m, k in enumerate(probes):
+        x[m, k] = 0x3F80  # bf16 1.0
+    y, a = oracle.linear_q4(x, codes, scales, biases, N)
+    for m, k in enumerate(probes):
+        gi = k // 64
+        for n in range(N):
+            assert y[m, n] == sv[gi] * n + bv[gi], (m, n)
+            assert a[m, n] == abs(sv[gi] * n) + abs(bv[gi])
+
+
+def test_q4_group_sum_closed_form():
+    """x = 1 on one whole group: y = scale * (sum of the group's codes) + 64 * bias."""
+    rng = np.random.default_rng(11)
+    N, K = 8, 256
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = bf16_bits_of(np.ldexp(1.0, rng.integers(-8, 2, (N, K // 64))))
+    biases = bf16_bits_of(rng.integers(-40, 40, (N, K // 64)) / 8.0)
+    x = np.zeros((K // 64, K), np.uint16)
+    for gi in range(K // 64):
+        x[gi, 64 * gi:64 * gi + 64] = 0x3F80
+    y = oracle.linear_q4(x, codes, scales, biases, N, with_abs=False)
+    q = np.empty((N, K), np.int64)
+    q[:, 0::2] = codes & 15
+    q[:, 1::2] = codes >> 4
+    for gi in range(K // 64):
+        for n in range(N):
+            s = bf16_vals_torch(scales[n, gi:gi + 1])[0]
+            b = bf16_vals_torch(biases[n, gi:gi + 1])[0]
+            assert y[gi, n] == s * q[n, 64 * gi:64 * gi + 64].sum() + 64 * b
+
+
+def test_q4_matches_numpy_matmul_random():
+    rng = np.random.default_rng(12)
+    M, N, K = 6, 24, 320
+    codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+    scales = rand_bf16(rng, (N, K // 64), 0.05)
+    biases = rand_bf16(rng, (N, K // 64), 0.4)
+    x = rand_bf16(rng, (M, K))
+    y, a = oracle.linear_q4(x, codes, scales, biases, N)
+    w, wa = dequant_q4_indep(codes, scales, biases)
+    xv = bf16_vals_torch(x)
+    np.testing.assert_allclose(y, xv @ w.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(a, np.abs(xv) @ wa.T, rtol=1e-12, atol=1e-12)
+    rows = np.array([23, 1, 9], np.int32)
+    y2, a2 = oracle.linear_q4(x, codes, scales, biases, N, rows=rows)
+    assert np.array_equal(y2, y[:, rows]) and np.array_equal(a2, a[:, rows])
+
+
+def test_q4_nibble_order_low_first():
+    """Element 2j is the low nibble: a code byte 0x50 (low 0, high 5) only reaches x[2j + 1]."""
+    K = 64
+    codes = np.zeros((1, K // 2), np.uint8)
+    codes[0, 4] = 0x50
+    scales = bf16_bits_of([[0.5]])
+    biases = bf16_bits_of([[0.0]])
+    x = np.zeros((2, K), np.uint16)
+    x[0, 8] = 0x3F80
+    x[1, 9] = 0x3F80
+    y = oracle.linear_q4(x, codes, scales, biases, 1, with_abs=False)
+    assert y[0, 0] == 0.0 and y[1, 0] == 2.5
+
+
+def test_q4_rejects_bad_arguments():
+    with pytest.raises(ValueError):
+        oracle.linear_q4(np.zeros((1, 96), np.uint16), np.zeros((1, 48), np.uint8), np.zeros((1, 1), np.uint16),
+                         np.zeros((1, 1), np.uint16), 1)
