@@ -20,6 +20,11 @@
  *   [BS-ties]    "Beating Splash on an M5 Max", section "The bugs a second reviewer found" (GPU and
  *                CPU must break argmax ties the same way) and "The kernels were not the gap"
  *                (split-K for narrow projections).
+ *   [SP-q4]      "144 tok/s needs 502 GB/s" (Splash), section "The engine hard-codes the model": the
+ *                other engines' affine 4-bit format, per group of 64 inputs 32 bytes of codes plus
+ *                a bf16 scale and a bf16 bias (nine bytes per sixteen weights); "Beating Splash on
+ *                an M5 Max", section "What actually moved the needle" (the Q4 tiles use per-group
+ *                input sums).
  *
  * Conventions for every entry point:
  *   - Device pointers are plain CUDA device addresses owned by the caller; the library never
@@ -102,6 +107,18 @@ vp_status vp_pack_nvfp4(const void* codes, const void* scales, int N, int K, voi
 /* w: [N][K] E4M3 bytes -> packed (vp_packed_bytes_fp8(N, K) bytes). */
 vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_bytes, void* stream);
 
+/* Q4 (affine INT4, groups of 64 along K) [SP-q4]: codes [N][K/2] bytes, element 2j of a row is the
+ * LOW nibble of byte j, an unsigned code q in 0..15; scales and biases [N][K/64] bf16;
+ *   w[n][k] = scale[n][k/64] * q[n][k] + bias[n][k/64]
+ * (the pages give the sizes, not the formula: the affine map is this library's reading).  Packed
+ * size N*K/16*9 bytes, the canonical size; the packed layout has the NVFP4 geometry (256-wide
+ * chunks, 1152-byte strips) with the codes in the order of an f16 magic-number conversion and each
+ * row's four (scale, bias) pairs of a chunk in one 16-byte piece.  K % 256 == 0, N % 16 == 0.
+ * codes and packed 16-byte aligned, scales and biases 2-byte aligned. */
+size_t vp_packed_bytes_q4(int N, int K);
+vp_status vp_pack_q4(const void* codes, const void* scales, const void* biases, int N, int K, void* packed,
+                     size_t packed_bytes, void* stream);
+
 /* ------------------------------------------------------------------ skinny linear layers
  *
  * y[m][n] = scale * sum_k x[m][k] * w[n][k], m < M, n < N, fp32 accumulation.  [LM-formats]
@@ -112,7 +129,7 @@ vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_b
  * Shapes: 1 <= M <= 32, N % 16 == 0, K as for the packed layout, N*K < 2^40.
  * Work is split along K across warps and CTAs (split-K) with a fixed-order reduction, so results
  * are bit-identical from run to run.  [BS-ties] (split-K).  */
-enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3 };
+enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3, VP_OP_Q4 = 4 };
 
 /* Workspace bytes for one call of op (VP_OP_*) at the given shape; 0 if the shape is invalid. */
 size_t vp_workspace_bytes(int op, int M, int N, int K);
@@ -121,6 +138,13 @@ vp_status vp_linear_nvfp4(const void* w_packed, float tensor_scale, const void* 
                           int N, int K, void* ws, size_t ws_bytes, void* stream);
 vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float* y, int M, int N,
                         int K, void* ws, size_t ws_bytes, void* stream);
+/* Q4: y[m][n] = sum_k x[m][k] * (scale * q + bias)[n][k] [SP-q4].  Each 64-wide group is computed
+ * as scale * (sum_k q x) + bias * (sum_k x): the codes enter the tensor core as exact f16 integers,
+ * the activation sums of every group are formed while the activations are staged, and both terms
+ * are applied in fp32.  Workspace: vp_workspace_bytes(VP_OP_Q4, M, N, K).  Arguments, shapes and
+ * errors otherwise as for vp_linear_nvfp4. */
+vp_status vp_linear_q4(const void* w_packed, const void* x, float* y, int M, int N, int K, void* ws,
+                       size_t ws_bytes, void* stream);
 
 /* vp_linear_nvfp4 without a caller-provided workspace.  The pages describe no such call: it is
  * a convenience of this library for callers that cannot pass scratch memory -- a plugin or custom-

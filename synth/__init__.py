@@ -24,6 +24,10 @@ Distributions (the input recipe):
 * ``fp8_normal_codes``: E4M3 code of ``x ~ N(0, 1)`` rounded to nearest, by the same integer
   threshold method on the normal CDF (inverse-CDF sampling).
 * ``normal_bf16`` (host only): Box-Muller from two words, rounded to bf16 by torch.
+* ``q4_scales_biases`` (host only): the affine 4-bit format's group scales and biases, bf16 (rounded
+  by torch): scale = 2**u with u ~ U(-8, -4) from one word, bias = -scale * (7.5 + v) with
+  v ~ U(-1/2, 1/2) from the next -- the group minimum that an affine quantiser of zero-centred
+  weights stores, so that weights span about [-7.5, 7.5] scales.
 """
 from __future__ import annotations
 
@@ -162,6 +166,18 @@ def normal_bf16(seed: int, stream: int, shape) -> np.ndarray:
     z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
     t = torch.from_numpy(z).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16).reshape(shape).copy()
+
+
+def q4_scales_biases(seed: int, stream: int, start: int, count: int) -> tuple:
+    """(scales, biases): bf16 bit patterns (uint16) of groups start .. start+count-1."""
+    import torch
+    w = words(seed, stream, 2 * start, 2 * count).reshape(count, 2)
+    u = -8.0 + 4.0 * ((w[:, 0] >> np.uint64(11)).astype(np.float64) + 0.5) / 2.0**53
+    v = ((w[:, 1] >> np.uint64(11)).astype(np.float64) + 0.5) / 2.0**53 - 0.5
+    sc = torch.from_numpy(np.exp2(u)).to(torch.bfloat16)
+    bi = torch.from_numpy(-sc.to(torch.float64).numpy() * (7.5 + v)).to(torch.bfloat16)
+    as_bits = lambda t: t.view(torch.int16).numpy().view(np.uint16).copy()  # noqa: E731
+    return as_bits(sc), as_bits(bi)
 
 
 def uniform_ints(seed: int, stream: int, start: int, count: int, n: int) -> np.ndarray:

@@ -72,6 +72,30 @@ def test_linear_validation_without_gpu(V):
         assert fn(*ok[:8], ws - 1, None) == V.VP_ERR_WORKSPACE
 
 
+def test_q4_sizes_and_validation_without_gpu(V):
+    assert V.vp_packed_bytes_q4(17408, 5120) == 17408 * 5120 * 9 // 16 == 50_135_040
+    assert V.vp_packed_bytes_q4(16, 128) == 0 and V.vp_packed_bytes_q4(24, 256) == 0
+    assert V.vp_workspace_bytes(V.VP_OP_Q4, 8, 17408, 5120) > 0
+    assert V.vp_workspace_bytes(V.VP_OP_Q4, 33, 17408, 5120) == 0
+    L = V.lib()
+    ws = V.vp_workspace_bytes(V.VP_OP_Q4, 8, 256, 1024)
+    ok = (FAKE, FAKE, FAKE, 8, 256, 1024, FAKE, ws, None)
+    assert L.vp_linear_q4(None, *ok[1:]) == V.VP_ERR_INVALID_ARG
+    assert L.vp_linear_q4(*ok[:6], None, *ok[7:]) == V.VP_ERR_INVALID_ARG
+    for M, N, K in ((0, 256, 1024), (33, 256, 1024), (8, 250, 1024), (8, 256, 1000), (8, 256, 65536 + 256)):
+        assert L.vp_linear_q4(FAKE, FAKE, FAKE, M, N, K, FAKE, 1 << 30, None) == V.VP_ERR_SHAPE
+    assert L.vp_linear_q4(FAKE + 8, *ok[1:]) == V.VP_ERR_ALIGNMENT
+    assert L.vp_linear_q4(FAKE, FAKE + 2, *ok[2:]) == V.VP_ERR_ALIGNMENT
+    assert L.vp_linear_q4(*ok[:7], ws - 1, None) == V.VP_ERR_WORKSPACE
+    pb = V.vp_packed_bytes_q4(256, 1024)
+    assert L.vp_pack_q4(None, FAKE, FAKE, 256, 1024, FAKE, pb, None) == V.VP_ERR_INVALID_ARG
+    assert L.vp_pack_q4(FAKE, FAKE, None, 256, 1024, FAKE, pb, None) == V.VP_ERR_INVALID_ARG
+    assert L.vp_pack_q4(FAKE, FAKE, FAKE, 256, 1000, FAKE, pb, None) == V.VP_ERR_SHAPE
+    assert L.vp_pack_q4(FAKE, FAKE, FAKE, 256, 1024, FAKE, pb - 1, None) == V.VP_ERR_INVALID_ARG
+    assert L.vp_pack_q4(FAKE, FAKE + 1, FAKE, 256, 1024, FAKE, pb, None) == V.VP_ERR_ALIGNMENT
+    assert L.vp_pack_q4(FAKE, FAKE, FAKE, 256, 1024, FAKE + 8, pb, None) == V.VP_ERR_ALIGNMENT
+
+
 def test_head_and_argmax_validation_without_gpu(V):
     L = V.lib()
     ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)

@@ -16,7 +16,7 @@ LIB_PATH = os.environ.get("VP_LIBVERIFY") or os.path.join(_PKG, "libverify.so")
 
 VP_OK, VP_ERR_INVALID_ARG, VP_ERR_SHAPE, VP_ERR_ALIGNMENT, VP_ERR_WORKSPACE, VP_ERR_CUDA, VP_ERR_TIMEOUT, \
     VP_ERR_UNSUPPORTED = range(8)
-VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX = range(4)
+VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX, VP_OP_Q4 = range(5)
 VP_LAYER_GDN, VP_LAYER_ATTN = 0, 1
 
 # Every symbol include/verify.h declares.
@@ -25,7 +25,7 @@ EXPORTS = [
     "vp_packed_bytes_fp8", "vp_pack_nvfp4", "vp_pack_fp8", "vp_workspace_bytes", "vp_linear_nvfp4",
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
-    "vp_linear_nvfp4_noalloc", "vp_trace_read",
+    "vp_linear_nvfp4_noalloc", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
 ]
 
 
@@ -81,6 +81,9 @@ def _load():
         "vp_pass_launch_count": (I, [P]),
         "vp_linear_nvfp4_noalloc": (I, [P, F, P, P, I, I, I, P]),
         "vp_trace_read": (I, [I, P, S, ctypes.POINTER(ctypes.c_uint)]),
+        "vp_packed_bytes_q4": (S, [I, I]),
+        "vp_pack_q4": (I, [P, P, P, I, I, P, S, P]),
+        "vp_linear_q4": (I, [P, P, P, I, I, I, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -134,6 +137,10 @@ def vp_packed_bytes_fp8(N: int, K: int) -> int:
     return _L.vp_packed_bytes_fp8(N, K)
 
 
+def vp_packed_bytes_q4(N: int, K: int) -> int:
+    return _L.vp_packed_bytes_q4(N, K)
+
+
 def vp_workspace_bytes(op: int, M: int, N: int, K: int) -> int:
     return _L.vp_workspace_bytes(op, M, N, K)
 
@@ -146,6 +153,17 @@ def vp_pack_nvfp4(codes, scales, N: int, K: int, packed, stream=None, packed_byt
 def vp_pack_fp8(w, N: int, K: int, packed, stream=None, packed_bytes=None):
     pb = packed_bytes if packed_bytes is not None else _nbytes(packed)
     _check("vp_pack_fp8", _L.vp_pack_fp8(_ptr(w), N, K, _ptr(packed), pb, _stream(stream)))
+
+
+def vp_pack_q4(codes, scales, biases, N: int, K: int, packed, stream=None, packed_bytes=None):
+    pb = packed_bytes if packed_bytes is not None else _nbytes(packed)
+    _check("vp_pack_q4", _L.vp_pack_q4(_ptr(codes), _ptr(scales), _ptr(biases), N, K, _ptr(packed), pb,
+                                       _stream(stream)))
+
+
+def vp_linear_q4(w_packed, x, y, M: int, N: int, K: int, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_linear_q4", _L.vp_linear_q4(_ptr(w_packed), _ptr(x), _ptr(y), M, N, K, _ptr(ws), wb, _stream(stream)))
 
 
 def vp_linear_nvfp4(w_packed, tensor_scale: float, x, y, M: int, N: int, K: int, ws, stream=None, ws_bytes=None):

@@ -86,7 +86,7 @@ Phase make_phase(const PhaseSpec& s, int NT) {
     ph.rb1 = ph.RB;
   }
   ph.KG = (ph.KC + ph.grp - 1) / ph.grp;
-  const int per = ks_max(NT) / chunk_k(s.fmt) / ph.grp;  // groups per slice at most
+  const int per = (s.fmt == kFmtQ4 ? ks_max_q4(NT) : ks_max(NT)) / chunk_k(s.fmt) / ph.grp;  // groups per slice at most
   ph.ks = (int8_t)((ph.KG + per - 1) / per);
   ph.cmax = phase_cmax(ph.RB, ph.KG, ph.ks);
   ph.fmt = (int8_t)s.fmt;
@@ -150,7 +150,7 @@ vp_status run_phases(const std::vector<Phase>& phases, int M, float eps, const I
     prog.n = p1 - p0;
     prog.M = M;
     prog.eps = eps;
-    prog.pad = 0;
+    prog.q4 = phases[p0].fmt == kFmtQ4;  // a program is all Q4 or has none (checked by the callers)
     for (int i = p0; i < p1; ++i) prog.ph[i - p0] = phases[i];
     cudaError_t e = launch_exec(prog, io, G, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -210,6 +210,48 @@ __global__ void pack_fp8_kernel(const uint8_t* __restrict__ w, int N, int K, uin
 #pragma unroll
     for (int ss = 0; ss < 4; ++ss) q[ss] = *reinterpret_cast<const uint32_t*>(src + 16 * (4 * h + ss) + 4 * c);
     *reinterpret_cast<uint4*>(out + strip * 1024 + piece * 16) = make_uint4(q[0], q[1], q[2], q[3]);
+  }
+}
+
+// Q4: codes [N][K/2] (low nibble first), scales and biases bf16 [N][K/64].  Code pieces hold, per
+// 32-bit word, steps s and s + 1 of the piece's lane in the nibble order of internal.h; scale piece g
+// holds the four (scale, bias) pairs of row g's groups in the chunk.
+__global__ void pack_q4_kernel(const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                               const uint16_t* __restrict__ biases, int N, int K, uint8_t* __restrict__ out) {
+  const int KC = K / 256;
+  const long long pieces = (long long)(N / 8) * KC * 72;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pieces;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long strip = i / 72;
+    const int piece = (int)(i % 72);
+    const int t = (int)(strip & 1), kc = (int)((strip >> 1) % KC);
+    const long long rb = (strip >> 1) / KC;
+    uint32_t wd[4];
+    if (piece < 64) {
+      const int h = piece >> 5, g = (piece >> 2) & 7, c = piece & 3;
+      const uint8_t* src = codes + (size_t)(rb * 16 + t * 8 + g) * (K / 2) + (size_t)kc * 128;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int s0 = 8 * h + 2 * w;
+        uint32_t q[2][4];  // [step][k within the lane's four]
+#pragma unroll
+        for (int d = 0; d < 2; ++d) {
+          const uint8_t b0 = src[8 * (s0 + d) + 2 * c], b1 = src[8 * (s0 + d) + 2 * c + 1];
+          q[d][0] = b0 & 15u;
+          q[d][1] = b0 >> 4;
+          q[d][2] = b1 & 15u;
+          q[d][3] = b1 >> 4;
+        }
+        wd[w] = q[0][0] | q[1][0] << 4 | q[0][2] << 8 | q[1][2] << 12 | q[0][1] << 16 | q[1][1] << 20 |
+                q[0][3] << 24 | q[1][3] << 28;
+      }
+    } else {
+      const int g = piece - 64;
+      const size_t row = (size_t)(rb * 16 + t * 8 + g) * (K / 64) + (size_t)kc * 4;
+#pragma unroll
+      for (int G = 0; G < 4; ++G) wd[G] = (uint32_t)scales[row + G] | (uint32_t)biases[row + G] << 16;
+    }
+    *reinterpret_cast<uint4*>(out + strip * 1152 + piece * 16) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
   }
 }
 
@@ -373,13 +415,35 @@ vp_status vp_pack_fp8(const void* w, int N, int K, void* packed, size_t packed_b
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
+size_t vp_packed_bytes_q4(int N, int K) {
+  if (!weight_shape_ok(kFmtQ4, N, K)) return 0;
+  return (size_t)N * (size_t)K / 16 * 9;
+}
+
+vp_status vp_pack_q4(const void* codes, const void* scales, const void* biases, int N, int K, void* packed,
+                     size_t packed_bytes, void* stream) {
+  if (!codes || !scales || !biases || !packed) return VP_ERR_INVALID_ARG;
+  const size_t need = vp_packed_bytes_q4(N, K);
+  if (need == 0) return VP_ERR_SHAPE;
+  if (packed_bytes < need) return VP_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(packed, 16))
+    return VP_ERR_ALIGNMENT;
+  int sms = 0;
+  vp_status st = device_sms(&sms);
+  if (st != VP_OK) return st;
+  pack_q4_kernel<<<pack_grid((long long)(N / 8) * (K / 256) * 72), 256, 0, (cudaStream_t)stream>>>(
+      (const uint8_t*)codes, (const uint16_t*)scales, (const uint16_t*)biases, N, K, (uint8_t*)packed);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
 size_t vp_workspace_bytes(int op, int M, int N, int K) {
   if (op == VP_OP_ARGMAX) {
     if (M < 8 || M > kMaxM || M % 8 || N < 1) return 0;
     return ws_layout(1, 1, 1).rb_cnt;  // the counter and the per-chunk maxima
   }
-  if (op != VP_OP_NVFP4 && op != VP_OP_FP8 && op != VP_OP_HEAD) return 0;
-  const int fmt = op == VP_OP_FP8 ? kFmtFp8 : kFmtNvfp4;
+  if (op != VP_OP_NVFP4 && op != VP_OP_FP8 && op != VP_OP_HEAD && op != VP_OP_Q4) return 0;
+  const int fmt = op == VP_OP_FP8 ? kFmtFp8 : op == VP_OP_Q4 ? kFmtQ4 : kFmtNvfp4;
   if (M < 1 || M > kMaxM || !weight_shape_ok(fmt, N, K)) return 0;
   if (op == VP_OP_HEAD && M % 8) return 0;
   PhaseSpec s;
@@ -440,6 +504,11 @@ vp_status vp_linear_nvfp4(const void* w_packed, float tensor_scale, const void* 
 vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float* y, int M, int N, int K, void* ws,
                         size_t ws_bytes, void* stream) {
   return linear_common(kFmtFp8, w_packed, scale, x, y, M, N, K, ws, ws_bytes, stream);
+}
+
+vp_status vp_linear_q4(const void* w_packed, const void* x, float* y, int M, int N, int K, void* ws, size_t ws_bytes,
+                       void* stream) {
+  return linear_common(kFmtQ4, w_packed, 1.0f, x, y, M, N, K, ws, ws_bytes, stream);
 }
 
 vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const void* x, int M, int V, int K,
@@ -545,7 +614,7 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   prog.n = 1;
   prog.M = M;
   prog.eps = 0.0f;
-  prog.pad = 0;
+  prog.q4 = 0;
   prog.ph[0] = ph;
   e = launch_exec(prog, io, sms, cs);
   return e == cudaSuccess ? VP_OK : cuda_fail(e);

@@ -1,4 +1,5 @@
-// Host-side entry of the streaming executor (exec.cuh), instantiated in exec_nt12.cu / exec_nt34.cu.
+// Host-side entry of the streaming executor (exec.cuh), instantiated in exec_nt12.cu / exec_nt34.cu
+// (NVFP4 / FP8 phases) and exec_q4.cu (Q4 phases).
 #pragma once
 #include <cuda_runtime.h>
 
@@ -8,6 +9,7 @@ namespace vp {
 
 cudaError_t launch_exec_nt12(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
 cudaError_t launch_exec_nt34(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
+cudaError_t launch_exec_q4(const Program& prog, const Io& io, int NT, int grid, cudaStream_t s, bool coop);
 // Copies the phase timeline of the NT = 1-2 / 3-4 kernels (trace.cuh) and the count of completed
 // launches; cudaErrorNotSupported unless the library was built with VP_PHASE_TRACE.
 cudaError_t trace_read_nt12(void* dst, size_t bytes, unsigned* launches);
@@ -18,6 +20,7 @@ cudaError_t trace_read_nt34(void* dst, size_t bytes, unsigned* launches);
 inline cudaError_t launch_exec(const Program& prog, const Io& io, int grid, cudaStream_t s) {
   const int NT = (prog.M + 7) / 8;
   const bool coop = prog.n > 1;
+  if (prog.q4) return launch_exec_q4(prog, io, NT, grid, s, coop);
   return NT <= 2 ? launch_exec_nt12(prog, io, NT, grid, s, coop) : launch_exec_nt34(prog, io, NT, grid, s, coop);
 }
 

@@ -20,15 +20,21 @@ namespace vp {
 //                         two bytes per step (k, k+1 in the first byte, low nibble first; k+2, k+3
 //                         in the second) -- then block scales [g][16 B], byte s = E4M3 scale of step s.
 //   FP8 strip (1024 B):   [half h = 0..1][g][c][16 B] -- steps 4h .. 4h + 3, four bytes per step.
+//   Q4 strip (1152 B):    codes [h][g][c][16 B] as NVFP4, but each 32-bit word w of the 16 bytes holds
+//                         steps s = 8h + 2w and s + 1 with its eight 4-bit codes in the order the
+//                         f16 magic-number conversion reads them: nibbles 0, 4 = step s, k + 0 / k + 1;
+//                         nibbles 2, 6 = step s, k + 2 / k + 3; nibbles 1, 5 and 3, 7 = the same of step
+//                         s + 1 -- then [g][16 B]: word G = bf16 scale | bf16 bias << 16 of the 64-wide
+//                         group G of the chunk (steps 4G .. 4G + 3).
 // Every warp-wide 16-byte shared-memory read of a strip is one contiguous 512-byte row.
 constexpr int kRowBlock = 16;
 constexpr int kStripRows = 8;
 constexpr int kMaxM = 32;
 
-enum Fmt : int { kFmtNvfp4 = 0, kFmtFp8 = 1 };
+enum Fmt : int { kFmtNvfp4 = 0, kFmtFp8 = 1, kFmtQ4 = 2 };
 
-__host__ __device__ constexpr int chunk_k(int fmt) { return fmt == kFmtNvfp4 ? 256 : 128; }
-__host__ __device__ constexpr int strip_bytes(int fmt) { return fmt == kFmtNvfp4 ? 1152 : 1024; }
+__host__ __device__ constexpr int chunk_k(int fmt) { return fmt == kFmtFp8 ? 128 : 256; }
+__host__ __device__ constexpr int strip_bytes(int fmt) { return fmt == kFmtFp8 ? 1024 : 1152; }
 __host__ __device__ inline size_t strip_offset(int fmt, int KC, int rb, int kc, int t) {
   return (((size_t)rb * KC + kc) * 2 + t) * (size_t)strip_bytes(fmt);
 }
@@ -59,6 +65,15 @@ __host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 5120 : NT ==
 static_assert(16 * 1 * ks_max(1) <= kXBytes && 16 * 2 * ks_max(2) <= kXBytes && 16 * 3 * ks_max(3) <= kXBytes &&
                   16 * 4 * ks_max(4) <= kXBytes,
               "activation slices fit the shared memory left by the ring");
+// Q4 phases also keep the per-group activation sums of the slice (fp32 [K / 64][8 NT]) after the
+// fragments, so their slices are narrower.
+__host__ __device__ constexpr int ks_max_q4(int NT) { return NT == 1 ? 4608 : NT == 2 ? 2048 : NT == 3 ? 1536 : 1024; }
+__host__ __device__ constexpr int q4_sums_offset(int NT) { return 16 * NT * ks_max_q4(NT); }
+static_assert(q4_sums_offset(1) + ks_max_q4(1) / 64 * 32 * 1 <= kXBytes &&
+                  q4_sums_offset(2) + ks_max_q4(2) / 64 * 32 * 2 <= kXBytes &&
+                  q4_sums_offset(3) + ks_max_q4(3) / 64 * 32 * 3 <= kXBytes &&
+                  q4_sums_offset(4) + ks_max_q4(4) / 64 * 32 * 4 <= kXBytes,
+              "Q4 activation slices and their group sums fit the shared memory left by the ring");
 
 enum Layout : int {
   kPlain = 0,        // virtual row blocks = the row blocks of w0, then of w1 (from row block rb1); groups of 2 chunks
@@ -91,7 +106,7 @@ constexpr int kMaxPhases = 160;
 struct Program {
   int n, M;
   float eps;
-  int pad;
+  int q4;  // 1: every phase is Q4 (the executor instantiation with the Q4 unit)
   Phase ph[kMaxPhases];
 };
 

@@ -84,6 +84,14 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
 }
+__device__ __forceinline__ float2 lds64f(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts32f(uint32_t a, float x) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(x) : "memory");
+}
 __device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(a), "r"(x), "r"(y) : "memory");
 }
@@ -126,6 +134,23 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
   asm("{ .reg .b16 h0, h1;\n mov.b32 {h0, h1}, %2;\n cvt.rn.f16x2.e4m3x2 %0, h0;\n cvt.rn.f16x2.e4m3x2 %1, h1;\n}"
       : "=r"(lo), "=r"(hi)
       : "r"(w));
+}
+// One Q4 word (eight 4-bit codes) -> four f16x2 of the exact integers 0..15: o[0] = nibbles 0 / 4,
+// o[1] = 2 / 6, o[2] = 1 / 5, o[3] = 3 / 7 (first named -> low half).  Each pair is masked into the
+// mantissa of 1024 = 0x6400 (the odd nibbles land 4 bits higher, as 1024 + 16 q), then the offset is
+// removed: q = v - 1024, or q = v / 16 - 64, both exact in f16.
+__device__ __forceinline__ void q4x8_to_f16x2x4(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w8 = w >> 8, lo = 0x000F000Fu, hi = 0x00F000F0u, k1024 = 0x64006400u;
+  const uint32_t k16th = 0x2C002C00u, km64 = 0xD400D400u;
+  uint32_t e0, e1, e2, e3;  // (a & b) | c
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(e0) : "r"(w), "r"(lo), "r"(k1024));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(e1) : "r"(w), "r"(hi), "r"(k1024));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(e2) : "r"(w8), "r"(lo), "r"(k1024));
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(e3) : "r"(w8), "r"(hi), "r"(k1024));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[0]) : "r"(e0), "r"(k1024));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(o[1]) : "r"(e2), "r"(k1024));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[2]) : "r"(e1), "r"(k16th), "r"(km64));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[3]) : "r"(e3), "r"(k16th), "r"(km64));
 }
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   uint32_t r;
