@@ -38,7 +38,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=64)
-    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head"],
+    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
     return ap.parse_args()
@@ -236,10 +236,11 @@ def run_kernel(args):
     from weight_streaming_gb300 import _lib as V
     from weight_streaming_gb300.model import pack_fp8, pack_nvfp4
     shapes = {"gate": ("nvfp4", 17408, 5120), "down": ("nvfp4", 5120, 17408), "gdn_in": ("fp8", 16384, 5120),
-              "head": ("nvfp4", 248320, 5120)}
+              "head": ("nvfp4", 248320, 5120), "q4_gate": ("q4", 17408, 5120), "q4_down": ("q4", 5120, 17408),
+              "q4_head": ("q4", 248320, 5120)}
     fmt, N, K = shapes[args.kernel]
     M = args.M
-    copies = 1 if args.kernel == "head" else 4
+    copies = 1 if args.kernel in ("head", "q4_head") else 4
     ws_list = []
     for c in range(copies):
         if fmt == "nvfp4":
@@ -248,15 +249,27 @@ def run_kernel(args):
             synth.gpu_uniform_bytes(cc, 0, synth.stream_id(c, synth.T_GATE_C))
             synth.gpu_scale_codes(sc, 0, synth.stream_id(c, synth.T_GATE_S))
             ws_list.append(pack_nvfp4(cc, sc))
+        elif fmt == "q4":
+            cc = torch.empty((N, K // 2), dtype=torch.uint8, device="cuda")
+            synth.gpu_uniform_bytes(cc, 0, synth.stream_id(c, synth.T_GATE_C))
+            sb = synth.q4_scales_biases(0, synth.stream_id(c, synth.T_GATE_S), 0, N * K // 64)
+            sc16, bi16 = (torch.from_numpy(a.view("int16")).cuda() for a in sb)
+            packed = torch.empty(V.vp_packed_bytes_q4(N, K), dtype=torch.uint8, device="cuda")
+            V.vp_pack_q4(cc, sc16, bi16, N, K, packed)
+            ws_list.append(packed)
         else:
             w = torch.empty((N, K), dtype=torch.uint8, device="cuda")
             synth.gpu_fp8_normal_codes(w, 0, synth.stream_id(c, synth.T_IN))
             ws_list.append(pack_fp8(w))
     x = torch.randn((M, K), device="cuda").to(torch.bfloat16)
     y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-    op = V.VP_OP_NVFP4 if fmt == "nvfp4" else V.VP_OP_FP8
+    op = {"nvfp4": V.VP_OP_NVFP4, "fp8": V.VP_OP_FP8, "q4": V.VP_OP_Q4}[fmt]
     ws = torch.zeros(V.vp_workspace_bytes(op, M, N, K), dtype=torch.uint8, device="cuda")
-    fn = V.vp_linear_nvfp4 if fmt == "nvfp4" else V.vp_linear_fp8
+    if fmt == "q4":
+        def fn(w, scale, x_, y_, M_, N_, K_, ws_):
+            V.vp_linear_q4(w, x_, y_, M_, N_, K_, ws_)
+    else:
+        fn = V.vp_linear_nvfp4 if fmt == "nvfp4" else V.vp_linear_fp8
     torch.cuda.synchronize()
     for i in range(args.warmup):
         fn(ws_list[i % copies], 1.0, x, y, M, N, K, ws)
@@ -268,9 +281,11 @@ def run_kernel(args):
     e1.record()
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) / 1e3 / args.steps
-    nbytes = N * K * 9 // 16 if fmt == "nvfp4" else N * K
+    nbytes = N * K * 9 // 16 if fmt in ("nvfp4", "q4") else N * K
+    peak = (measured_peaks() or {}).get("hbm_gbs")
     print(json.dumps({"kernel": args.kernel, "fmt": fmt, "M": M, "N": N, "K": K, "us_per_launch": t * 1e6,
-                      "gbps": nbytes / t / 1e9, "bytes_per_launch": nbytes}), flush=True)
+                      "gbps": nbytes / t / 1e9, "bytes_per_launch": nbytes,
+                      "frac_of_measured_copy": (nbytes / t / 1e9 / peak) if peak else None}), flush=True)
 
 
 def main():
