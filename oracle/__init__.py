@@ -14,7 +14,8 @@ the passage of the pages it follows:
 * "144 tok/s needs 502 GB/s" (Splash) -- "The engine hard-codes the model" (geometry).
 * "Beating Splash on an M5 Max" -- "The bugs a second reviewer found" (one argmax tie rule).
 * "144 tok/s needs 502 GB/s" -- "The engine hard-codes the model" (the affine 4-bit "Q4" format:
-  per group of 64 inputs, 32 bytes of codes, a bf16 scale and a bf16 bias; ``linear_q4``).
+  per group of 64 inputs, 32 bytes of codes, a bf16 scale and a bf16 bias; ``linear_q4``) and "Exact,
+  up to top-32" (speculative sampling over the top_k <= 32 target candidates; ``sample_accept``).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against page values,
 closed forms, library routines or brute force, except the 64-layer surrogate chain, whose
@@ -86,6 +87,11 @@ def lib():
                                         P, P, ctypes.c_int]
             L.orc_q4_bytes.restype = ctypes.c_int64
             L.orc_q4_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            L.orc_target_dist.restype = ctypes.c_int
+            L.orc_target_dist.argtypes = [P, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_double, P, P, P]
+            L.orc_sample_accept.restype = ctypes.c_int
+            L.orc_sample_accept.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                                            ctypes.c_double, P, P, P, P, P, P, P]
             L.orc_silu_mul.argtypes = [P, P, ctypes.c_int64, P]
             L.orc_rmsnorm.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
             L.orc_argmax.restype = ctypes.c_int64
@@ -189,6 +195,41 @@ def linear_q4(x_bf16: np.ndarray, codes: np.ndarray, scales: np.ndarray, biases:
 
 def q4_bytes(N: int, K: int) -> int:
     return int(lib().orc_q4_bytes(N, K))
+
+
+def target_dist(logits_row: np.ndarray, temperature: float, top_k: int, top_p: float):
+    """(tokens, probs, margin): one row's sampling distribution -- top_k candidates (larger logit
+    first, lower index among equals), temperature, top_p truncation, renormalised."""
+    v = np.ascontiguousarray(logits_row, dtype=np.float64).reshape(-1)
+    tok = np.zeros(32, np.int32)
+    prob = np.zeros(32, np.float64)
+    mg = np.zeros(1, np.float64)
+    n = lib().orc_target_dist(_p(v), v.size, float(temperature), int(top_k), float(top_p), _p(tok), _p(prob), _p(mg))
+    if n <= 0:
+        raise ValueError("orc_target_dist rejected its arguments")
+    return tok[:n].copy(), prob[:n].copy(), float(mg[0])
+
+
+def sample_accept(logits: np.ndarray, temperature: float, top_k: int, top_p: float, pending: np.ndarray,
+                  draft_tokens: np.ndarray | None, draft_probs: np.ndarray | None, uniforms: np.ndarray):
+    """Speculative sampling per lane (see orc_sample_accept): returns (n_commit [L], committed [L][8],
+    margin [L])."""
+    lg = np.ascontiguousarray(logits, dtype=np.float64)
+    M, V = lg.shape
+    pend = np.ascontiguousarray(pending, dtype=np.int32)
+    dt = np.ascontiguousarray(draft_tokens, dtype=np.int32) if draft_tokens is not None else None
+    dp = np.ascontiguousarray(draft_probs, dtype=np.float64) if draft_probs is not None else None
+    u = np.ascontiguousarray(uniforms, dtype=np.float64)
+    L = M // 8
+    nc = np.zeros(L, np.int32)
+    cm = np.zeros((L, 8), np.int32)
+    mg = np.zeros(L, np.float64)
+    rc = lib().orc_sample_accept(_p(lg), M, V, float(temperature), int(top_k), float(top_p), _p(pend),
+                                 _p(dt) if dt is not None else None, _p(dp) if dp is not None else None, _p(u),
+                                 _p(nc), _p(cm), _p(mg))
+    if rc != 0:
+        raise ValueError("orc_sample_accept rejected its arguments")
+    return nc, cm, mg
 
 
 def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:

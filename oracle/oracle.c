@@ -452,6 +452,139 @@ int64_t orc_nvfp4_code_bytes(int64_t N, int64_t K) { return N * K / 2; }
 int64_t orc_nvfp4_scale_bytes(int64_t N, int64_t K) { return N * K / 16; }
 int64_t orc_fp8_bytes(int64_t N, int64_t K) { return N * K; }
 
+/* Probability the draft gave token t (0 when t is not among its 16 candidates). */
+static double orc_q_of(const int32_t* dt, const double* dp, int32_t t) {
+    for (int i = 0; i < 16; ++i) if (dt[i] == t) return dp[i];
+    return 0.0;
+}
+
+/* ------------------------------------------------------------------ sampled acceptance
+ *
+ * "144 tok/s needs 502 GB/s", section "Exact, up to top-32": the acceptance test is standard
+ * speculative sampling -- accept a draft token when u * q < p, else draw from max(p - q, 0) -- so the
+ * output follows the target's distribution; the target's probabilities are temperature over its first
+ * top_k (<= 32) entries, truncated by top_p, renormalised; a token outside those candidates has
+ * probability zero.  "lithos-metal ...", section "How DSpark is wired in": with a greedy drafter the
+ * draft is a point mass (q = 1 on the drafted token).  "Beating Splash on an M5 Max", section "What
+ * actually moved the needle": one GPU kernel over the verify logits applies top-k and top-p, samples
+ * and runs the acceptance rule.
+ * Readings (the pages give the rule, not these details): candidates are ordered by logit, larger
+ * first, ties to the lower token index; top_p keeps the shortest prefix whose mass reaches top_p; a
+ * draw with uniform u from weights w over that order takes the first i with u * sum(w) < w_0 + .. + w_i;
+ * if the residual max(p - q, 0) is zero everywhere (p == q) the draw is from p; the draft's
+ * distribution for draft j of lane l is given as 16 (token, probability) pairs at row 8l + j, and a
+ * token not among them has q = 0; the uniforms are inputs, two per row: u[r][0] for the test of the
+ * draft checked at row r, u[r][1] for the draw at row r. */
+
+/* The target distribution of one row: its top_k candidates in order, probabilities after
+ * temperature, top_p and renormalisation.  Returns the number kept (1..top_k); *margin = the smallest
+ * distance of a running mass to top_p (how close the truncation was to flipping). */
+int orc_target_dist(const double* logits, int V, double temperature, int top_k, double top_p, int32_t* tok,
+                    double* prob, double* margin) {
+    if (V < 1 || top_k < 1 || top_k > 32 || top_k > V || !(temperature > 0.0) || !(top_p > 0.0)) return 0;
+    int32_t best[32];
+    double bv[32];
+    int n = 0;
+    /* top_k by insertion: larger logit first, the lower index first among equals; NaN as -inf */
+    for (int i = 0; i < V; ++i) {
+        double v = isnan(logits[i]) ? -INFINITY : logits[i];
+        int pos = n;
+        while (pos > 0 && v > bv[pos - 1]) pos--;
+        if (pos >= top_k) continue;
+        if (n < top_k) n++;
+        for (int j = n - 1; j > pos; --j) { bv[j] = bv[j - 1]; best[j] = best[j - 1]; }
+        bv[pos] = v;
+        best[pos] = i;
+    }
+    double e[32], sum = 0.0;
+    for (int i = 0; i < n; ++i) {
+        e[i] = exp((bv[i] - bv[0]) / temperature);
+        sum += e[i];
+    }
+    double cum = 0.0, mg = INFINITY;
+    int keep = n;
+    for (int i = 0; i < n; ++i) {
+        cum += e[i] / sum;
+        double d = fabs(cum - top_p);
+        if (d < mg) mg = d;
+        if (cum >= top_p) { keep = i + 1; break; }
+    }
+    double ksum = 0.0;
+    for (int i = 0; i < keep; ++i) ksum += e[i];
+    for (int i = 0; i < keep; ++i) { tok[i] = best[i]; prob[i] = e[i] / ksum; }
+    if (margin) *margin = top_p >= 1.0 ? INFINITY : mg;
+    return keep;
+}
+
+/* First i with u * W < w_0 + .. + w_i (W = the sum); *margin = distance of u * W to the nearest
+ * boundary, relative to W. */
+static int orc_draw(const double* w, int n, double u, double* margin) {
+    double W = 0.0;
+    for (int i = 0; i < n; ++i) W += w[i];
+    double t = u * W, cum = 0.0;
+    int pick = n - 1;
+    double mg = INFINITY;
+    for (int i = 0; i < n; ++i) {
+        cum += w[i];
+        double d = fabs(cum - t) / W;
+        if (d < mg) mg = d;
+        if (t < cum) { pick = i; break; }
+    }
+    if (margin) *margin = mg;
+    return pick;
+}
+
+/* Per lane: speculative sampling of the 7 drafts against the target rows, then the bonus draw.
+ * logits [M][V] (the GPU's fp32 values, widened); draft_tokens / draft_probs [M][16] or NULL
+ * (point mass on each draft); uniforms [M][2].  margin[l] = the smallest margin of the lane's
+ * decisions (acceptance tests |u q - p|, draws, top_p truncations).  Returns 0, or -1 on bad args. */
+int orc_sample_accept(const double* logits, int M, int V, double temperature, int top_k, double top_p,
+                      const int32_t* pending, const int32_t* draft_tokens, const double* draft_probs,
+                      const double* uniforms, int32_t* n_commit, int32_t* committed, double* margin) {
+    if (M < 8 || M % 8 || V < 1 || top_k < 1 || top_k > 32 || top_k > V || !(temperature > 0.0) ||
+        !(top_p > 0.0) || !logits || !pending || !uniforms || !n_commit || !committed)
+        return -1;
+    for (int l = 0; l < M / 8; ++l) {
+        double mg = INFINITY;
+        int acc = 0, last = -1;
+        for (int j = 0; j <= 7; ++j) {
+            const int r = 8 * l + j;
+            int32_t tok[32];
+            double p[32], tm;
+            const int n = orc_target_dist(logits + (int64_t)r * V, V, temperature, top_k, top_p, tok, p, &tm);
+            if (tm < mg) mg = tm;
+            double w[32], dm;
+            if (j == 7) { /* all drafts accepted: the bonus token from p */
+                last = tok[orc_draw(p, n, uniforms[2 * r + 1], &dm)];
+                if (dm < mg) mg = dm;
+                break;
+            }
+            const int32_t d = pending[8 * l + j + 1];
+            double pd = 0.0, qd;
+            for (int i = 0; i < n; ++i) if (tok[i] == d) pd = p[i];
+            /* q of a token under the draft's distribution at this row */
+            #define ORC_Q(t) (draft_probs ? orc_q_of(draft_tokens + (int64_t)r * 16, draft_probs + (int64_t)r * 16, (t)) \
+                                          : ((t) == d ? 1.0 : 0.0))
+            qd = ORC_Q(d);
+            const double a = uniforms[2 * r] * qd;
+            if (fabs(a - pd) < mg) mg = fabs(a - pd);
+            if (a < pd) { acc++; continue; }
+            double W = 0.0;
+            for (int i = 0; i < n; ++i) { w[i] = fmax(p[i] - ORC_Q(tok[i]), 0.0); W += w[i]; }
+            #undef ORC_Q
+            const int pick = W > 0.0 ? orc_draw(w, n, uniforms[2 * r + 1], &dm) : orc_draw(p, n, uniforms[2 * r + 1], &dm);
+            if (dm < mg) mg = dm;
+            last = tok[pick];
+            break;
+        }
+        n_commit[l] = acc + 1;
+        for (int j = 0; j < 8; ++j)
+            committed[8 * l + j] = j < acc ? pending[8 * l + j + 1] : (j == acc ? last : -1);
+        if (margin) margin[l] = mg;
+    }
+    return 0;
+}
+
 /* Per-pass byte groups of the pass geometry, in the page's table order:
  * out[0] MLP codes, out[1] MLP block scales, out[2] GDN FP8, out[3] attention FP8, out[4] head
  * (codes + scales), out[5] total. */

@@ -516,3 +516,100 @@ def test_q4_rejects_bad_arguments():
     with pytest.raises(ValueError):
         oracle.linear_q4(np.zeros((1, 96), np.uint16), np.zeros((1, 48), np.uint8), np.zeros((1, 1), np.uint16),
                          np.zeros((1, 1), np.uint16), 1)
+
+
+# ------------------------------------------------------------------ sampled acceptance
+
+def test_target_dist_top_p_truncation_closed_form():
+    """Probabilities 0.5 / 0.3 / 0.2 (+ a negligible fourth): top_k = 3, top_p = 0.7 keeps two and
+    renormalises them to 0.625 / 0.375; top_p = 1 keeps all three."""
+    lg = np.log(np.array([0.3, 0.5, 1e-12, 0.2]))
+    tok, p, _ = oracle.target_dist(lg, 1.0, 3, 0.7)
+    assert tok.tolist() == [1, 0] and np.allclose(p, [0.625, 0.375], rtol=1e-14)
+    tok, p, mg = oracle.target_dist(lg, 1.0, 3, 1.0)
+    assert tok.tolist() == [1, 0, 3] and np.allclose(p, [0.5, 0.3, 0.2], rtol=1e-14) and mg == np.inf
+
+
+def test_target_dist_temperature_and_softmax():
+    rng = np.random.default_rng(21)
+    lg = rng.standard_normal(500) * 3
+    for T, k in ((0.6, 20), (1.0, 32), (1.7, 5)):
+        tok, p, _ = oracle.target_dist(lg, T, k, 1.0)
+        order = np.lexsort((np.arange(lg.size), -lg))[:k]  # larger logit first, lower index among equals
+        assert tok.tolist() == order.tolist()
+        ref = torch.softmax(torch.tensor(lg[order] / T, dtype=torch.float64), 0).numpy()
+        np.testing.assert_allclose(p, ref, rtol=1e-13)
+        assert math.isclose(p[0] / p[1], math.exp((lg[order[0]] - lg[order[1]]) / T), rel_tol=1e-12)
+
+
+def test_target_dist_ties_and_top1():
+    lg = np.array([1.0, 3.0, 3.0, -2.0, 3.0])
+    tok, p, _ = oracle.target_dist(lg, 1.0, 4, 1.0)
+    assert tok.tolist() == [1, 2, 4, 0]
+    tok, p, _ = oracle.target_dist(lg, 0.5, 1, 0.9)
+    assert tok.tolist() == [oracle.argmax(lg)] and p.tolist() == [1.0]
+
+
+def test_sample_accept_top1_point_mass_is_greedy_acceptance():
+    """top_k = 1 with point-mass drafts is greedy decoding: the result equals the greedy acceptance
+    rule on the rows' argmax, whatever the uniforms."""
+    rng = np.random.default_rng(22)
+    L, V = 6, 50
+    lg = rng.standard_normal((8 * L, V))
+    t = np.array([oracle.argmax(r) for r in lg], np.int32)
+    pending = rng.integers(0, V, 8 * L).astype(np.int32)
+    for l in range(L):  # planted prefixes of length l
+        pending[8 * l + 1:8 * l + 1 + l] = t[8 * l:8 * l + l]
+    u = rng.random((8 * L, 2))
+    nc, cm, _ = oracle.sample_accept(lg, 0.8, 1, 1.0, pending, None, None, u)
+    nc2, cm2 = oracle.accept(t, pending)
+    assert np.array_equal(nc, nc2) and np.array_equal(cm, cm2)
+
+
+@pytest.mark.parametrize("point_mass", [False, True])
+def test_sample_accept_preserves_target_distribution(point_mass):
+    """Speculative sampling leaves the committed token distributed as the target's: over a grid of
+    the two uniforms and every draft token d (weighted by q(d)), the first committed token of a lane
+    follows row 0's target distribution p, up to the grid's resolution."""
+    V, G = 6, 160
+    lg_row = np.log(np.array([0.05, 0.3, 0.1, 0.25, 0.2, 0.1]))
+    p_tok, p_prob, _ = oracle.target_dist(lg_row, 1.0, 5, 0.95)  # token 0 falls outside top_k
+    p_t = np.zeros(V)
+    p_t[p_tok] = p_prob
+    if point_mass:
+        qs = {d: (1.0 if d == 3 else 0.0) for d in range(V)}
+    else:
+        qv = np.array([0.3, 0.1, 0.2, 0.15, 0.05, 0.2])
+        qs = {d: qv[d] for d in range(V)}
+    uu = (np.arange(G) + 0.5) / G
+    U = np.stack(np.meshgrid(uu, uu, indexing="ij"), -1).reshape(-1, 2)  # (u0, u1) pairs
+    L = U.shape[0]
+    lg = np.tile(lg_row, (8 * L, 1))
+    uni = np.zeros((8 * L, 2))
+    uni[0::8] = U
+    dist = np.zeros(V)
+    for d, qd in qs.items():
+        if qd == 0.0:
+            continue
+        pending = np.zeros(8 * L, np.int32)
+        pending[1::8] = d
+        if point_mass:
+            dt = dp = None
+        else:
+            dt = np.tile(np.arange(16, dtype=np.int32), (8 * L, 1))
+            dp = np.zeros((8 * L, 16))
+            dp[:, :V] = np.array([qs[i] for i in range(V)])
+        nc, cm, _ = oracle.sample_accept(lg, 1.0, 5, 0.95, pending, dt, dp, uni)
+        first = cm[:, 0]
+        dist += qd * np.bincount(first, minlength=V)[:V] / L
+    np.testing.assert_allclose(dist, p_t, atol=3.0 / G)
+    assert dist[0] == 0.0  # outside the target's candidates
+
+
+def test_sample_accept_rejects_bad_arguments():
+    lg = np.zeros((8, 10))
+    pend = np.zeros(8, np.int32)
+    u = np.zeros((8, 2))
+    for T, k, p in ((0.0, 5, 1.0), (1.0, 33, 1.0), (1.0, 11, 1.0), (1.0, 5, 0.0)):
+        with pytest.raises(ValueError):
+            oracle.sample_accept(lg, T, k, p, pend, None, None, u)
