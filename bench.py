@@ -38,7 +38,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=64)
-    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head"],
+    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
     return ap.parse_args()
@@ -227,10 +227,48 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ the GPU arm
 
+def run_sample(args):
+    """vp_sample_accept alone over fp32 logits [M][248320] (top_k 20, top_p 0.95, temperature 0.7,
+    draft distributions of 16 candidates); prints one JSON line with the time per call and the logit
+    bytes read per second."""
+    import torch
+
+    from weight_streaming_gb300 import _lib as V
+    M, Vv = args.M, 248320
+    g = torch.Generator(device="cuda").manual_seed(0)
+    logits = torch.randn((M, Vv), device="cuda", generator=g)
+    pending = torch.randint(0, Vv, (M,), device="cuda", dtype=torch.int32, generator=g)
+    dt = torch.randint(0, Vv, (M, 16), device="cuda", dtype=torch.int32, generator=g)
+    dp = torch.full((M, 16), 1.0 / 16, device="cuda")
+    u = torch.rand((M, 2), device="cuda", generator=g)
+    nc = torch.empty(M // 8, dtype=torch.int32, device="cuda")
+    cm = torch.empty((M // 8, 8), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(V.vp_workspace_bytes(V.VP_OP_SAMPLE, M, Vv, 0), dtype=torch.uint8, device="cuda")
+
+    def call():
+        V.vp_sample_accept(logits, M, Vv, 0.7, 20, 0.95, pending, dt, dp, u, nc, cm, ws)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    nbytes = M * Vv * 4
+    print(json.dumps({"kernel": "sample", "M": M, "V": Vv, "us_per_call": t * 1e6, "launches_per_call": 1,
+                      "logit_gbps": nbytes / t / 1e9, "bytes_per_call": nbytes}), flush=True)
+
+
 def run_kernel(args):
     """One GEMM of the pass alone through the C ABI, rotating over 4 weight copies (> L2) so every
     launch streams from DRAM; prints one JSON line with the average launch time and GB/s."""
     import torch
+    if args.kernel == "sample":
+        run_sample(args)
+        return
 
     import synth
     from weight_streaming_gb300 import _lib as V

@@ -20,6 +20,13 @@
  *   [BS-ties]    "Beating Splash on an M5 Max", section "The bugs a second reviewer found" (GPU and
  *                CPU must break argmax ties the same way) and "The kernels were not the gap"
  *                (split-K for narrow projections).
+ *   [SP-sample]  "144 tok/s needs 502 GB/s" (Splash), section "Exact, up to top-32" (standard
+ *                speculative sampling, accept when u * q < p, else draw from max(p - q, 0); the
+ *                target's probabilities are temperature over its first top_k <= 32 entries,
+ *                truncated by top_p, renormalised); "lithos-metal ...", section "How DSpark is wired
+ *                in" (a greedy drafter is a point mass); "Beating Splash on an M5 Max", section "What
+ *                actually moved the needle" (one GPU kernel over the verify logits applies top-k and
+ *                top-p, samples and runs the acceptance rule).
  *   [SP-q4]      "144 tok/s needs 502 GB/s" (Splash), section "The engine hard-codes the model": the
  *                other engines' affine 4-bit format, per group of 64 inputs 32 bytes of codes plus
  *                a bf16 scale and a bf16 bias (nine bytes per sixteen weights); "Beating Splash on
@@ -129,7 +136,7 @@ vp_status vp_pack_q4(const void* codes, const void* scales, const void* biases, 
  * Shapes: 1 <= M <= 32, N % 16 == 0, K as for the packed layout, N*K < 2^40.
  * Work is split along K across warps and CTAs (split-K) with a fixed-order reduction, so results
  * are bit-identical from run to run.  [BS-ties] (split-K).  */
-enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3, VP_OP_Q4 = 4 };
+enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3, VP_OP_Q4 = 4, VP_OP_SAMPLE = 5 };
 
 /* Workspace bytes for one call of op (VP_OP_*) at the given shape; 0 if the shape is invalid. */
 size_t vp_workspace_bytes(int op, int M, int N, int K);
@@ -140,8 +147,8 @@ vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float*
                         int K, void* ws, size_t ws_bytes, void* stream);
 /* Q4: y[m][n] = sum_k x[m][k] * (scale * q + bias)[n][k] [SP-q4].  Each 64-wide group is computed
  * as scale * (sum_k q x) + bias * (sum_k x): the codes enter the tensor core as exact f16 integers,
- * the activation sums of every group are formed while the activations are staged, and both terms
- * are applied in fp32.  Workspace: vp_workspace_bytes(VP_OP_Q4, M, N, K).  Arguments, shapes and
+ * the group's activation sums come from the same tensor-core pass (a ones operand beside the codes),
+ * and both terms are applied in fp32.  Workspace: vp_workspace_bytes(VP_OP_Q4, M, N, K).  Arguments, shapes and
  * errors otherwise as for vp_linear_nvfp4. */
 vp_status vp_linear_q4(const void* w_packed, const void* x, float* y, int M, int N, int K, void* ws,
                        size_t ws_bytes, void* stream);
@@ -184,6 +191,31 @@ vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const 
  * It runs the same device reduction and acceptance code as vp_head_argmax_accept. */
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending,
                            int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/* Sampled acceptance over given fp32 logits [M][V] (M = 8 * lanes; 1 <= V <= 1,048,576)
+ * [SP-sample].  Per row r, the target distribution p_r: the top_k (1..32, <= V) largest logits
+ * (NaN as -inf; ties to the lower token index), p = exp((l - l_max) / temperature) normalised over
+ * them, then the shortest prefix whose mass reaches top_p (0 < top_p <= 1), renormalised; every other
+ * token has p = 0.  Per lane l, for draft j = 0..6 (d = pending[8l + j + 1], checked at row
+ * r = 8l + j, q = the draft's probability of d):
+ *   accept when uniforms[r][0] * q < p_r(d); otherwise draw the committed token from
+ *   max(p_r - q_r, 0) (from p_r if that is zero everywhere) with uniforms[r][1] and stop;
+ * when all 7 are accepted, draw the bonus token from p at row 8l + 7 with uniforms[8l + 7][1].
+ * A draw with u over weights w in candidate order (larger logit first) takes the first i with
+ * u * sum(w) < w_0 + .. + w_i.  The draft's distribution at row r is draft_tokens[r][0..15] /
+ * draft_probs[r][0..15] (tokens not listed have q = 0); with both NULL each draft is a point mass
+ * (q = 1 on d: a greedy drafter).  n_commit[l] = accepted + 1; committed[l] = the accepted drafts,
+ * the drawn token, then -1.  uniforms: fp32 [M][2] in [0, 1), supplied by the caller (the library
+ * draws no random numbers).  Arithmetic is fp32; decisions within rounding of a boundary may
+ * differ from an fp64 evaluation.  One kernel launch.  Workspace: vp_workspace_bytes(VP_OP_SAMPLE,
+ * M, V, 0), zero-filled once before its first use (its counters return to zero after each call).
+ * Errors: VP_ERR_INVALID_ARG (null pointers, one of draft_tokens / draft_probs without the other,
+ * temperature not finite and > 0, top_p outside (0, 1]), VP_ERR_SHAPE, VP_ERR_ALIGNMENT (4-byte
+ * arrays, 256-byte workspace), VP_ERR_WORKSPACE. */
+vp_status vp_sample_accept(const float* logits, int M, int V, float temperature, int top_k, float top_p,
+                           const int32_t* pending, const int32_t* draft_tokens, const float* draft_probs,
+                           const float* uniforms, int32_t* n_commit, int32_t* committed, void* ws,
                            size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------ the verify pass

@@ -96,6 +96,31 @@ def test_q4_sizes_and_validation_without_gpu(V):
     assert L.vp_pack_q4(FAKE, FAKE, FAKE, 256, 1024, FAKE + 8, pb, None) == V.VP_ERR_ALIGNMENT
 
 
+def test_sample_accept_validation_without_gpu(V):
+    L = V.lib()
+    assert V.vp_workspace_bytes(V.VP_OP_SAMPLE, 8, 248320, 0) > 0
+    ws = V.vp_workspace_bytes(V.VP_OP_SAMPLE, 8, 1000, 0)
+    assert ws > 0 and V.vp_workspace_bytes(V.VP_OP_SAMPLE, 12, 1000, 0) == 0
+    assert V.vp_workspace_bytes(V.VP_OP_SAMPLE, 8, (1 << 20) + 1, 0) == 0
+    F = FAKE
+    ok = [F, 8, 1000, 1.0, 20, 0.9, F, F, F, F, F, F, F, ws, None]
+
+    def call(**kw):
+        a = list(ok)
+        names = ["logits", "M", "V", "T", "k", "p", "pending", "dt", "dp", "u", "nc", "cm", "ws", "wsb", "s"]
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return L.vp_sample_accept(*a)
+    assert call(logits=None) == V.VP_ERR_INVALID_ARG
+    assert call(dt=None) == V.VP_ERR_INVALID_ARG  # draft tokens without probabilities
+    assert call(T=0.0) == V.VP_ERR_INVALID_ARG and call(T=float("inf")) == V.VP_ERR_INVALID_ARG
+    assert call(p=0.0) == V.VP_ERR_INVALID_ARG and call(p=1.5) == V.VP_ERR_INVALID_ARG
+    assert call(M=12) == V.VP_ERR_SHAPE and call(k=33) == V.VP_ERR_SHAPE and call(k=0) == V.VP_ERR_SHAPE
+    assert call(V=10, k=11) == V.VP_ERR_SHAPE
+    assert call(logits=F + 2) == V.VP_ERR_ALIGNMENT and call(ws=F + 16) == V.VP_ERR_ALIGNMENT
+    assert call(wsb=ws - 1) == V.VP_ERR_WORKSPACE
+
+
 def test_head_and_argmax_validation_without_gpu(V):
     L = V.lib()
     ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)

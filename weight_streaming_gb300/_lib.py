@@ -16,7 +16,7 @@ LIB_PATH = os.environ.get("VP_LIBVERIFY") or os.path.join(_PKG, "libverify.so")
 
 VP_OK, VP_ERR_INVALID_ARG, VP_ERR_SHAPE, VP_ERR_ALIGNMENT, VP_ERR_WORKSPACE, VP_ERR_CUDA, VP_ERR_TIMEOUT, \
     VP_ERR_UNSUPPORTED = range(8)
-VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX, VP_OP_Q4 = range(5)
+VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX, VP_OP_Q4, VP_OP_SAMPLE = range(6)
 VP_LAYER_GDN, VP_LAYER_ATTN = 0, 1
 
 # Every symbol include/verify.h declares.
@@ -26,6 +26,7 @@ EXPORTS = [
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
     "vp_linear_nvfp4_noalloc", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
+    "vp_sample_accept",
 ]
 
 
@@ -84,6 +85,7 @@ def _load():
         "vp_packed_bytes_q4": (S, [I, I]),
         "vp_pack_q4": (I, [P, P, P, I, I, P, S, P]),
         "vp_linear_q4": (I, [P, P, P, I, I, I, P, S, P]),
+        "vp_sample_accept": (I, [P, I, I, F, I, F, P, P, P, P, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -197,6 +199,15 @@ def vp_argmax_accept(logits, M: int, V: int, pending, argmax, n_commit, committe
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check("vp_argmax_accept", _L.vp_argmax_accept(_ptr(logits), M, V, _ptr(pending), _ptr(argmax), _ptr(n_commit),
                                                    _ptr(committed), _ptr(ws), wb, _stream(stream)))
+
+
+def vp_sample_accept(logits, M: int, V: int, temperature: float, top_k: int, top_p: float, pending, draft_tokens,
+                     draft_probs, uniforms, n_commit, committed, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_sample_accept",
+           _L.vp_sample_accept(_ptr(logits), M, V, temperature, top_k, top_p, _ptr(pending), _ptr(draft_tokens),
+                               _ptr(draft_probs), _ptr(uniforms), _ptr(n_commit), _ptr(committed), _ptr(ws), wb,
+                               _stream(stream)))
 
 
 def vp_workspace_init(ws, stream=None, ws_bytes=None):

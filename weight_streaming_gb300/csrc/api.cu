@@ -11,6 +11,7 @@
 #include "exec.cuh"
 #include "exec_launch.h"
 #include "internal.h"
+#include "sample.h"
 #include "verify.h"
 
 using namespace vp;
@@ -86,7 +87,7 @@ Phase make_phase(const PhaseSpec& s, int NT) {
     ph.rb1 = ph.RB;
   }
   ph.KG = (ph.KC + ph.grp - 1) / ph.grp;
-  const int per = (s.fmt == kFmtQ4 ? ks_max_q4(NT) : ks_max(NT)) / chunk_k(s.fmt) / ph.grp;  // groups per slice at most
+  const int per = ks_max(NT) / chunk_k(s.fmt) / ph.grp;  // groups per slice at most
   ph.ks = (int8_t)((ph.KG + per - 1) / per);
   ph.cmax = phase_cmax(ph.RB, ph.KG, ph.ks);
   ph.fmt = (int8_t)s.fmt;
@@ -442,6 +443,10 @@ size_t vp_workspace_bytes(int op, int M, int N, int K) {
     if (M < 8 || M > kMaxM || M % 8 || N < 1) return 0;
     return ws_layout(1, 1, 1).rb_cnt;  // the counter and the per-chunk maxima
   }
+  if (op == VP_OP_SAMPLE) {
+    if (M < 8 || M > kMaxM || M % 8 || N < 1 || N > kSampleMaxV) return 0;
+    return sample_ws_layout(M, N).total;
+  }
   if (op != VP_OP_NVFP4 && op != VP_OP_FP8 && op != VP_OP_HEAD && op != VP_OP_Q4) return 0;
   const int fmt = op == VP_OP_FP8 ? kFmtFp8 : op == VP_OP_Q4 ? kFmtQ4 : kFmtNvfp4;
   if (M < 1 || M > kMaxM || !weight_shape_ok(fmt, N, K)) return 0;
@@ -504,6 +509,25 @@ vp_status vp_linear_nvfp4(const void* w_packed, float tensor_scale, const void* 
 vp_status vp_linear_fp8(const void* w_packed, float scale, const void* x, float* y, int M, int N, int K, void* ws,
                         size_t ws_bytes, void* stream) {
   return linear_common(kFmtFp8, w_packed, scale, x, y, M, N, K, ws, ws_bytes, stream);
+}
+
+vp_status vp_sample_accept(const float* logits, int M, int V, float temperature, int top_k, float top_p,
+                           const int32_t* pending, const int32_t* draft_tokens, const float* draft_probs,
+                           const float* uniforms, int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (!logits || !pending || !uniforms || !n_commit || !committed || !ws) return VP_ERR_INVALID_ARG;
+  if ((draft_tokens == nullptr) != (draft_probs == nullptr)) return VP_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !(temperature < INFINITY) || !(top_p > 0.0f) || !(top_p <= 1.0f))
+    return VP_ERR_INVALID_ARG;
+  if (M < 8 || M > kMaxM || M % 8 || V < 1 || V > kSampleMaxV || top_k < 1 || top_k > 32 || top_k > V)
+    return VP_ERR_SHAPE;
+  if (!aligned(logits, 4) || !aligned(pending, 4) || !aligned(uniforms, 4) || !aligned(n_commit, 4) ||
+      !aligned(committed, 4) || !aligned(ws, 256) || (draft_tokens && (!aligned(draft_tokens, 4) || !aligned(draft_probs, 4))))
+    return VP_ERR_ALIGNMENT;
+  if (ws_bytes < sample_ws_layout(M, V).total) return VP_ERR_WORKSPACE;
+  cudaError_t e = launch_sample_accept(logits, M, V, temperature, top_k, top_p, pending, draft_tokens, draft_probs,
+                                       uniforms, n_commit, committed, ws, (cudaStream_t)stream);
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
 vp_status vp_linear_q4(const void* w_packed, const void* x, float* y, int M, int N, int K, void* ws, size_t ws_bytes,

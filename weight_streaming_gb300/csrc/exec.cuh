@@ -244,7 +244,7 @@ __device__ __forceinline__ int exp_of_max(float mx) {
 // Stages the CTA's K slice [kbase, kbase + Ks) of the phase's activation rows: x, or
 // bf16(RMSNorm(x)) (unit weight) when the phase asks for it, with the row statistics taken over
 // the whole row.  Thread t handles row n = t / T, 16-byte chunks i, i + T, ... of the slice.
-template <int NT, bool kQ4>
+template <int NT>
 __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, const Io& io, int kbase, int Ks,
                                      uint8_t* xs, SmemMisc& sm) {
   const int tid = threadIdx.x, M = prog.M;
@@ -261,9 +261,6 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
       const int r = M + e / per_row, q = e % per_row;
       sts128(xb + xfrag_offset<NT>(q >> 2, r, q & 3), make_uint4(0u, 0u, 0u, 0u));
     }
-    if constexpr (kQ4)
-      for (int e = tid; e < zrows * (Ks >> 6); e += kThreads)
-        sts32f(xb + q4_sums_offset(NT) + ((e / zrows) * 8 * NT + M + e % zrows) * 4, 0.0f);
   }
   // All of the thread's chunks are loaded at once (one memory round trip).
   uint4 v[16];
@@ -309,11 +306,9 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
   float sc1 = ne > 127 ? pow2f(127) : ne < -126 ? pow2f(-126) : pow2f(ne);
   const float sc2 = ne > 127 ? pow2f(ne - 127) : ne < -126 ? pow2f(ne + 126) : 1.0f;
   if (rms) sc1 *= inv;
-  float gsum[kQ4 ? 16 : 1];  // Q4: the thread's sum of each of its chunks (8 staged values)
 #pragma unroll
   for (int m = 0; m < 16; ++m) {
     const int q = i + T * m;
-    if constexpr (kQ4) gsum[m] = 0.0f;
     if (!(active && q < nch)) continue;
     const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
     uint32_t h[4];
@@ -329,26 +324,12 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
         b *= sc2;
       }
       const __half2 hh = __floats2half2_rn(a, b);
-      if constexpr (kQ4) gsum[m] += __low2float(hh) + __high2float(hh);  // what the tensor core sees
       h[k] = *reinterpret_cast<const uint32_t*>(&hh);
     }
     const int k0 = 8 * q, st = k0 >> 4, hf = (k0 >> 3) & 1;
     const uint32_t ad = xb + xfrag_offset<NT>(st >> 1, n, 2 * hf) + (st & 1) * 8;
     sts64(ad, h[0], h[1]);
     sts64(ad + 16, h[2], h[3]);
-  }
-  if constexpr (kQ4) {
-    // Sum of each 64-wide group (8 chunks held by 8 consecutive lanes of the row), the same fixed
-    // butterfly order in every lane; stored as fp32 [group][token] after the fragments.
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      float t = gsum[m];
-      t += __shfl_xor_sync(0xffffffffu, t, 1);
-      t += __shfl_xor_sync(0xffffffffu, t, 2);
-      t += __shfl_xor_sync(0xffffffffu, t, 4);
-      const int q = i + T * m;
-      if (active && q < nch && (i & 7) == 0) sts32f(xb + q4_sums_offset(NT) + ((q >> 3) * 8 * NT + n) * 4, t);
-    }
   }
   __syncthreads();
 }
@@ -397,12 +378,12 @@ __device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, f
 }
 
 // One Q4 chunk (w = scale * q + bias per 64-wide group): for each group, the codes q (exact f16
-// integers) times the staged activations on the tensor core into a group accumulator t, then
-// acc += scale * t + bias * (the group's activation sum) in fp32.  sa: this lane's sums of the
-// chunk's first group (tokens 2c, 2c + 1 of n-tile 0); the sums are in the staged (row-scaled)
-// units, like t.
+// integers) times the staged activations on the tensor core into a group accumulator t, and a
+// ones operand times the same activations into sx, the group's activation sums of the C fragment's
+// tokens (every row of that product is the column sum); then acc += scale * t + bias * sx in fp32.
+// t and sx are both in the staged (row-scaled) units.
 template <int NT>
-__device__ __forceinline__ void unit_q4(uint32_t ua, uint32_t xa, uint32_t sa, int lane, float (&acc)[NT][4]) {
+__device__ __forceinline__ void unit_q4(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4]) {
   const int g = lane >> 2;
   const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
   const uint4 c1a = lds128(ua + 1152 + lane * 16), c1b = lds128(ua + 1152 + 512 + lane * 16);
@@ -410,13 +391,14 @@ __device__ __forceinline__ void unit_q4(uint32_t ua, uint32_t xa, uint32_t sa, i
   const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
   const uint32_t w1[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
   const uint32_t sb0[4] = {s0.x, s0.y, s0.z, s0.w}, sb1[4] = {s1.x, s1.y, s1.z, s1.w};
+  constexpr uint32_t kOnes = 0x3C003C00u;  // f16x2 (1, 1)
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
-    float t[NT][4];
+    float t[NT][4], sx[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) t[j][r] = 0.0f;
+      for (int r = 0; r < 4; ++r) t[j][r] = sx[j][r] = 0.0f;
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
       const int p = 2 * G + pp;  // steps 2p, 2p + 1
@@ -430,17 +412,18 @@ __device__ __forceinline__ void unit_q4(uint32_t ua, uint32_t xa, uint32_t sa, i
       for (int j = 0; j < NT; ++j) {
         mma_f16_16816(t[j], o0[0], o1[0], o0[1], o1[1], b[j].x, b[j].y);
         mma_f16_16816(t[j], o0[2], o1[2], o0[3], o1[3], b[j].z, b[j].w);
+        mma_f16_16816(sx[j], kOnes, kOnes, kOnes, kOnes, b[j].x, b[j].y);
+        mma_f16_16816(sx[j], kOnes, kOnes, kOnes, kOnes, b[j].z, b[j].w);
       }
     }
     const float sc0 = __uint_as_float(sb0[G] << 16), bi0 = __uint_as_float(sb0[G] & 0xFFFF0000u);
     const float sc1 = __uint_as_float(sb1[G] << 16), bi1 = __uint_as_float(sb1[G] & 0xFFFF0000u);
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      const float2 sx = lds64f(sa + (G * NT + j) * 32);
-      acc[j][0] = fmaf(bi0, sx.x, fmaf(sc0, t[j][0], acc[j][0]));
-      acc[j][1] = fmaf(bi0, sx.y, fmaf(sc0, t[j][1], acc[j][1]));
-      acc[j][2] = fmaf(bi1, sx.x, fmaf(sc1, t[j][2], acc[j][2]));
-      acc[j][3] = fmaf(bi1, sx.y, fmaf(sc1, t[j][3], acc[j][3]));
+      acc[j][0] = fmaf(bi0, sx[j][0], fmaf(sc0, t[j][0], acc[j][0]));
+      acc[j][1] = fmaf(bi0, sx[j][1], fmaf(sc0, t[j][1], acc[j][1]));
+      acc[j][2] = fmaf(bi1, sx[j][2], fmaf(sc1, t[j][2], acc[j][2]));
+      acc[j][3] = fmaf(bi1, sx[j][3], fmaf(sc1, t[j][3], acc[j][3]));
     }
   }
 }
@@ -781,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     Slice S;
     const int sidx = slice_of_cta(ph, G, cta, S);
     const int ck = chunk_k(ph.fmt), kc0 = S.kg0 * ph.grp;
-    stage_x<NT, kQ4>(prog, ph, io, kc0 * ck, (min(kc0 + S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
+    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
     VP_TRACE(threadIdx.x == 0, p, 1);
     float tsc[NT][2];
 #pragma unroll
@@ -828,9 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       }
       const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kgl * ph.grp * pair_stride;
       if constexpr (kQ4) {  // one or two consecutive chunks of the row block, 4 groups each
-        const uint32_t sa = smem_addr(xs) + q4_sums_offset(NT) + kgl * ph.grp * 4 * 32 * NT + c * 8;
-        unit_q4<NT>(ua, xa, sa, lane, acc);
-        if ((S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, sa + 4 * 32 * NT, lane, acc);
+        unit_q4<NT>(ua, xa, lane, acc);
+        if ((S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
       } else if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
         unit_nvfp4<NT>(ua, xa, lane, acc, acc);
         unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);

@@ -65,15 +65,6 @@ __host__ __device__ constexpr int ks_max(int NT) { return NT == 1 ? 5120 : NT ==
 static_assert(16 * 1 * ks_max(1) <= kXBytes && 16 * 2 * ks_max(2) <= kXBytes && 16 * 3 * ks_max(3) <= kXBytes &&
                   16 * 4 * ks_max(4) <= kXBytes,
               "activation slices fit the shared memory left by the ring");
-// Q4 phases also keep the per-group activation sums of the slice (fp32 [K / 64][8 NT]) after the
-// fragments, so their slices are narrower.
-__host__ __device__ constexpr int ks_max_q4(int NT) { return NT == 1 ? 4608 : NT == 2 ? 2048 : NT == 3 ? 1536 : 1024; }
-__host__ __device__ constexpr int q4_sums_offset(int NT) { return 16 * NT * ks_max_q4(NT); }
-static_assert(q4_sums_offset(1) + ks_max_q4(1) / 64 * 32 * 1 <= kXBytes &&
-                  q4_sums_offset(2) + ks_max_q4(2) / 64 * 32 * 2 <= kXBytes &&
-                  q4_sums_offset(3) + ks_max_q4(3) / 64 * 32 * 3 <= kXBytes &&
-                  q4_sums_offset(4) + ks_max_q4(4) / 64 * 32 * 4 <= kXBytes,
-              "Q4 activation slices and their group sums fit the shared memory left by the ring");
 
 enum Layout : int {
   kPlain = 0,        // virtual row blocks = the row blocks of w0, then of w1 (from row block rb1); groups of 2 chunks
