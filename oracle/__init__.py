@@ -16,6 +16,8 @@ the passage of the pages it follows:
 * "144 tok/s needs 502 GB/s" -- "The engine hard-codes the model" (the affine 4-bit "Q4" format:
   per group of 64 inputs, 32 bytes of codes, a bf16 scale and a bf16 bias; ``linear_q4``) and "Exact,
   up to top-32" (speculative sampling over the top_k <= 32 target candidates; ``sample_accept``).
+* "lithos-metal ..." -- "The megakernel is per layer, not per step" (the attention core over a BF16
+  KV cache with online-softmax partitions and a sigmoid gate; ``attention_verify``).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against page values,
 closed forms, library routines or brute force, except the 64-layer surrogate chain, whose
@@ -92,6 +94,9 @@ def lib():
             L.orc_sample_accept.restype = ctypes.c_int
             L.orc_sample_accept.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
                                             ctypes.c_double, P, P, P, P, P, P, P]
+            L.orc_attention_verify.restype = ctypes.c_int
+            L.orc_attention_verify.argtypes = [P, P, P, P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, P, P]
             L.orc_silu_mul.argtypes = [P, P, ctypes.c_int64, P]
             L.orc_rmsnorm.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
             L.orc_argmax.restype = ctypes.c_int64
@@ -230,6 +235,26 @@ def sample_accept(logits: np.ndarray, temperature: float, top_k: int, top_p: flo
     if rc != 0:
         raise ValueError("orc_sample_accept rejected its arguments")
     return nc, cm, mg
+
+
+def attention_verify(q, k_new, v_new, k_cache, v_cache, ctx, gate=None, with_abs=True):
+    """Causal attention of the verify rows over each lane's cache plus the rows' own appended keys
+    (see orc_attention_verify); bf16 bit patterns in, fp64 [M][Hq][D] out (and the tolerance scale)."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    M, Hq, D = q.shape
+    kc = np.ascontiguousarray(k_cache, dtype=np.uint16)
+    L, Hkv, cap, _ = kc.shape
+    args = [np.ascontiguousarray(x, dtype=np.uint16) for x in (k_new, v_new, v_cache)]
+    ctx = np.ascontiguousarray(ctx, dtype=np.int32)
+    g = np.ascontiguousarray(gate, dtype=np.uint16) if gate is not None else None
+    out = np.zeros((M, Hq, D), np.float64)
+    a = np.zeros((M, Hq, D), np.float64) if with_abs else None
+    rc = lib().orc_attention_verify(_p(q), _p(args[0]), _p(args[1]), _p(kc), _p(args[2]), _p(ctx), cap,
+                                    _p(g) if g is not None else None, M, Hq, Hkv, D, _p(out),
+                                    _p(a) if a is not None else None)
+    if rc != 0:
+        raise ValueError("orc_attention_verify rejected its arguments")
+    return (out, a) if with_abs else out
 
 
 def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:

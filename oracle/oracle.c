@@ -452,6 +452,77 @@ int64_t orc_nvfp4_code_bytes(int64_t N, int64_t K) { return N * K / 2; }
 int64_t orc_nvfp4_scale_bytes(int64_t N, int64_t K) { return N * K / 16; }
 int64_t orc_fp8_bytes(int64_t N, int64_t K) { return N * K; }
 
+/* ------------------------------------------------------------------ verify attention over a KV cache
+ *
+ * "lithos-metal ...", section "The megakernel is per layer, not per step" (the full-attention figure
+ * and the text after it): the attention core reads and appends a BF16 KV cache, runs a causal
+ * softmax of q k^T weighting V, multiplies by the sigmoid of the gate, and the KV range is split
+ * into partitions whose online-softmax partials are merged.  The partitions are an implementation
+ * route to the same result, so the oracle computes the plain definition.  Readings: scores are
+ * q . k / sqrt(D); the verify rows of lane l append their keys / values at positions
+ * ctx[l] .. ctx[l] + 7 and row j sees positions 0 .. ctx[l] + j; q heads h share kv head
+ * h / (Hq / Hkv); q and k arrive normalised and rotated (the page's Q/K RMSNorm and RoPE are
+ * elementwise steps before this one).
+ *
+ * q, gate: bf16 [M][Hq][D]; k_new, v_new: bf16 [M][Hkv][D]; k_cache, v_cache: bf16
+ * [L][Hkv][cap][D] holding positions 0 .. ctx[l] - 1; out, a: fp64 [M][Hq][D] with
+ * a = sum_t p_t |v_t| * |sigmoid(gate)| (tolerance scale).  gate may be NULL (no gating). */
+static double orc_bf(const uint16_t* p, int64_t i) { return orc_bf16_value(p[i]); }
+
+int orc_attention_verify(const uint16_t* q, const uint16_t* k_new, const uint16_t* v_new, const uint16_t* k_cache,
+                         const uint16_t* v_cache, const int32_t* ctx, int cap, const uint16_t* gate, int M, int Hq,
+                         int Hkv, int D, double* out, double* a) {
+    if (M < 8 || M % 8 || Hq < 1 || Hkv < 1 || Hq % Hkv || D < 1 || !q || !k_new || !v_new || !k_cache ||
+        !v_cache || !ctx || !out)
+        return -1;
+    const int G = Hq / Hkv, L = M / 8;
+    for (int l = 0; l < L; ++l)
+        if (ctx[l] < 0 || ctx[l] + 8 > cap) return -1;
+    const double scale = 1.0 / sqrt((double)D);
+    double* sc = (double*)malloc(sizeof(double) * ((size_t)cap + 8));
+    if (!sc) return -1;
+    for (int r = 0; r < M; ++r) {
+        const int l = r / 8, j = r % 8, n = ctx[l] + j + 1;
+        for (int h = 0; h < Hq; ++h) {
+            const int g = h / G;
+            const uint16_t* qr = q + ((int64_t)r * Hq + h) * D;
+            /* key / value of position t for this lane and kv head */
+            #define ORC_K(t, d) ((t) < ctx[l] ? orc_bf(k_cache, (((int64_t)l * Hkv + g) * cap + (t)) * D + (d)) \
+                                              : orc_bf(k_new, ((int64_t)(8 * l + (t) - ctx[l]) * Hkv + g) * D + (d)))
+            #define ORC_V(t, d) ((t) < ctx[l] ? orc_bf(v_cache, (((int64_t)l * Hkv + g) * cap + (t)) * D + (d)) \
+                                              : orc_bf(v_new, ((int64_t)(8 * l + (t) - ctx[l]) * Hkv + g) * D + (d)))
+            double mx = -INFINITY;
+            for (int t = 0; t < n; ++t) {
+                double s = 0.0;
+                for (int d = 0; d < D; ++d) s += orc_bf(qr, d) * ORC_K(t, d);
+                sc[t] = s * scale;
+                if (sc[t] > mx) mx = sc[t];
+            }
+            double den = 0.0;
+            for (int t = 0; t < n; ++t) {
+                sc[t] = exp(sc[t] - mx);
+                den += sc[t];
+            }
+            for (int d = 0; d < D; ++d) {
+                double o = 0.0, oa = 0.0;
+                for (int t = 0; t < n; ++t) {
+                    const double v = ORC_V(t, d);
+                    o += sc[t] * v;
+                    oa += sc[t] * fabs(v);
+                }
+                double gt = 1.0;
+                if (gate) gt = 1.0 / (1.0 + exp(-orc_bf(gate, ((int64_t)r * Hq + h) * D + d)));
+                out[((int64_t)r * Hq + h) * D + d] = o / den * gt;
+                if (a) a[((int64_t)r * Hq + h) * D + d] = oa / den * gt;
+            }
+            #undef ORC_K
+            #undef ORC_V
+        }
+    }
+    free(sc);
+    return 0;
+}
+
 /* Probability the draft gave token t (0 when t is not among its 16 candidates). */
 static double orc_q_of(const int32_t* dt, const double* dp, int32_t t) {
     for (int i = 0; i < 16; ++i) if (dt[i] == t) return dp[i];

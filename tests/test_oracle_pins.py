@@ -613,3 +613,74 @@ def test_sample_accept_rejects_bad_arguments():
     for T, k, p in ((0.0, 5, 1.0), (1.0, 33, 1.0), (1.0, 11, 1.0), (1.0, 5, 0.0)):
         with pytest.raises(ValueError):
             oracle.sample_accept(lg, T, k, p, pend, None, None, u)
+
+
+# ------------------------------------------------------------------ verify attention
+
+def attn_case(rng, L=1, Hq=6, Hkv=1, D=32, cap=40, ctx=None):
+    M = 8 * L
+    q = rand_bf16(rng, (M, Hq, D))
+    kn = rand_bf16(rng, (M, Hkv, D))
+    vn = rand_bf16(rng, (M, Hkv, D))
+    kc = rand_bf16(rng, (L, Hkv, cap, D))
+    vc = rand_bf16(rng, (L, Hkv, cap, D))
+    gate = rand_bf16(rng, (M, Hq, D))
+    ctx = np.array(ctx if ctx is not None else rng.integers(0, cap - 8, L), np.int32)
+    return q, kn, vn, kc, vc, ctx, gate
+
+
+def test_attention_matches_torch_sdpa():
+    """Against torch's scaled_dot_product_attention (fp64) with the causal verify mask and the
+    sigmoid gate applied afterwards."""
+    rng = np.random.default_rng(31)
+    L, Hq, Hkv, D, cap = 2, 6, 2, 32, 40
+    q, kn, vn, kc, vc, ctx, gate = attn_case(rng, L, Hq, Hkv, D, cap, ctx=[13, 0])
+    out, a = oracle.attention_verify(q, kn, vn, kc, vc, ctx, gate)
+    f = lambda x: torch.from_numpy(bf16_vals_torch(x))  # noqa: E731
+    for l in range(L):
+        n = ctx[l] + 8
+        K = torch.cat([f(kc[l][:, :ctx[l]]), f(kn[8 * l:8 * l + 8]).permute(1, 0, 2)], 1)  # [Hkv][n][D]
+        Vv = torch.cat([f(vc[l][:, :ctx[l]]), f(vn[8 * l:8 * l + 8]).permute(1, 0, 2)], 1)
+        Q = f(q[8 * l:8 * l + 8]).permute(1, 0, 2)  # [Hq][8][D]
+        K = K.repeat_interleave(Hq // Hkv, 0)
+        Vv = Vv.repeat_interleave(Hq // Hkv, 0)
+        mask = torch.arange(n)[None, :] <= (ctx[l] + torch.arange(8))[:, None]
+        o = torch.nn.functional.scaled_dot_product_attention(Q, K, Vv, attn_mask=mask)
+        o = o * torch.sigmoid(f(gate[8 * l:8 * l + 8]).permute(1, 0, 2))
+        np.testing.assert_allclose(out[8 * l:8 * l + 8], o.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+    assert np.all(a >= np.abs(out) - 1e-12)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(32)
+    q, kn, vn, kc, vc, ctx, gate = attn_case(rng, ctx=[0])
+    out = oracle.attention_verify(q, kn, vn, kc, vc, ctx, None, with_abs=False)
+    # an empty cache: row 0 sees only its own key, so its output is its own value
+    assert np.array_equal(out[0], np.repeat(bf16_vals_torch(vn[0]), 6, 0))
+    # identical keys: uniform weights, the output is the mean of the visible values
+    kn2 = np.tile(kn[:1], (8, 1, 1))
+    out2 = oracle.attention_verify(q, kn2, vn, kc, vc, ctx, None, with_abs=False)
+    vv = bf16_vals_torch(vn)[:, 0]
+    for j in range(8):
+        np.testing.assert_allclose(out2[j], np.tile(vv[:j + 1].mean(0), (6, 1)), rtol=1e-12, atol=1e-14)
+    # a zero gate halves the output
+    zero = np.zeros_like(gate)
+    out3 = oracle.attention_verify(q, kn, vn, kc, vc, ctx, zero, with_abs=False)
+    np.testing.assert_allclose(out3, out / 2, rtol=1e-15)
+
+
+def test_attention_causal_and_grouped():
+    rng = np.random.default_rng(33)
+    q, kn, vn, kc, vc, ctx, gate = attn_case(rng, Hq=6, Hkv=2, ctx=[20])
+    out = oracle.attention_verify(q, kn, vn, kc, vc, ctx, gate, with_abs=False)
+    kn2, vn2 = kn.copy(), vn.copy()
+    kn2[5:] ^= 0x0040  # perturb the keys / values of rows 5..7
+    vn2[5:] ^= 0x0040
+    out2 = oracle.attention_verify(q, kn2, vn2, kc, vc, ctx, gate, with_abs=False)
+    assert np.array_equal(out[:5], out2[:5]) and not np.array_equal(out[5:], out2[5:])
+    # heads 0..2 read kv head 0, heads 3..5 kv head 1: equal queries and gates give equal outputs
+    q2, g2 = q.copy(), gate.copy()
+    q2[:, 1], g2[:, 1] = q2[:, 0], g2[:, 0]
+    q2[:, 4], g2[:, 4] = q2[:, 0], g2[:, 0]
+    out3 = oracle.attention_verify(q2, kn, vn, kc, vc, ctx, g2, with_abs=False)
+    assert np.array_equal(out3[:, 0], out3[:, 1]) and not np.array_equal(out3[:, 0], out3[:, 4])
