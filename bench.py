@@ -38,9 +38,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=64)
-    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample"],
+    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample", "attn"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
+    ap.add_argument("--ctx", type=int, default=32768, help="context length per lane for --kernel attn")
     return ap.parse_args()
 
 
@@ -268,12 +269,55 @@ def run_sample(args):
                       "logit_gbps": nbytes / t / 1e9, "bytes_per_call": nbytes}), flush=True)
 
 
+def run_attn(args):
+    """vp_attention_verify alone: the pages' attention heads (24 q / 4 kv, head dim 256), every lane
+    at the context --ctx, rotating over 4 cache copies when they fit (so the cache streams from
+    DRAM); prints one JSON line with the time per call and the cache bytes read per second."""
+    import torch
+
+    from weight_streaming_gb300 import _lib as V
+    M, Hq, Hkv, D = args.M, 24, 4, 256
+    L, ctx = M // 8, args.ctx
+    cap = ctx + 8
+    cache_bytes = L * Hkv * cap * D * 2 * 2
+    copies = 4 if 4 * cache_bytes < (16 << 30) else 1
+    g = torch.Generator(device="cuda").manual_seed(0)
+    rnd = lambda *sh: torch.randn(sh, device="cuda", generator=g).to(torch.bfloat16)  # noqa: E731
+    caches = [(rnd(L, Hkv, cap, D), rnd(L, Hkv, cap, D)) for _ in range(copies)]
+    q, kn, vn, gate = rnd(M, Hq, D), rnd(M, Hkv, D), rnd(M, Hkv, D), rnd(M, Hq, D)
+    ctx_d = torch.full((L,), ctx, dtype=torch.int32, device="cuda")
+    out = torch.empty((M, Hq, D), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(V.vp_workspace_bytes(V.VP_OP_ATTN, M, Hkv, cap), dtype=torch.uint8, device="cuda")
+
+    def call(i):
+        kc, vc = caches[i % copies]
+        V.vp_attention_verify(q, kn, vn, kc, vc, ctx_d, cap, gate, out, M, Hq, Hkv, D, ws)
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        call(i)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    nbytes = L * Hkv * (ctx + 8) * D * 2 * 2  # keys and values read once
+    peak = (measured_peaks() or {}).get("hbm_gbs")
+    print(json.dumps({"kernel": "attn", "M": M, "ctx": ctx, "heads": [Hq, Hkv, D], "us_per_call": t * 1e6,
+                      "launches_per_call": 3, "kv_gbps": nbytes / t / 1e9, "bytes_per_call": nbytes, "copies": copies,
+                      "frac_of_measured_copy": (nbytes / t / 1e9 / peak) if peak else None}), flush=True)
+
+
 def run_kernel(args):
     """One GEMM of the pass alone through the C ABI, rotating over 4 weight copies (> L2) so every
     launch streams from DRAM; prints one JSON line with the average launch time and GB/s."""
     import torch
     if args.kernel == "sample":
         run_sample(args)
+        return
+    if args.kernel == "attn":
+        run_attn(args)
         return
 
     import synth

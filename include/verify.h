@@ -27,6 +27,10 @@
  *                in" (a greedy drafter is a point mass); "Beating Splash on an M5 Max", section "What
  *                actually moved the needle" (one GPU kernel over the verify logits applies top-k and
  *                top-p, samples and runs the acceptance rule).
+ *   [LM-attn]    "lithos-metal ...", section "The megakernel is per layer, not per step" (the full-
+ *                attention figure and text: an attention core that reads and appends a BF16 KV cache,
+ *                causal softmax of q k^T weighting V, times the sigmoid of the gate; the KV range split
+ *                into partitions of up to 1,024 keys whose online-softmax partials are merged).
  *   [SP-q4]      "144 tok/s needs 502 GB/s" (Splash), section "The engine hard-codes the model": the
  *                other engines' affine 4-bit format, per group of 64 inputs 32 bytes of codes plus
  *                a bf16 scale and a bf16 bias (nine bytes per sixteen weights); "Beating Splash on
@@ -136,7 +140,8 @@ vp_status vp_pack_q4(const void* codes, const void* scales, const void* biases, 
  * Shapes: 1 <= M <= 32, N % 16 == 0, K as for the packed layout, N*K < 2^40.
  * Work is split along K across warps and CTAs (split-K) with a fixed-order reduction, so results
  * are bit-identical from run to run.  [BS-ties] (split-K).  */
-enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3, VP_OP_Q4 = 4, VP_OP_SAMPLE = 5 };
+enum { VP_OP_NVFP4 = 0, VP_OP_FP8 = 1, VP_OP_HEAD = 2, VP_OP_ARGMAX = 3, VP_OP_Q4 = 4, VP_OP_SAMPLE = 5,
+       VP_OP_ATTN = 6 };
 
 /* Workspace bytes for one call of op (VP_OP_*) at the given shape; 0 if the shape is invalid. */
 size_t vp_workspace_bytes(int op, int M, int N, int K);
@@ -217,6 +222,25 @@ vp_status vp_sample_accept(const float* logits, int M, int V, float temperature,
                            const int32_t* pending, const int32_t* draft_tokens, const float* draft_probs,
                            const float* uniforms, int32_t* n_commit, int32_t* committed, void* ws,
                            size_t ws_bytes, void* stream);
+
+/* Verify attention over a BF16 KV cache [LM-attn], for the attention layers' mixer core.  Lane l
+ * (M = 8 * lanes) has ctx[l] cached positions in k_cache / v_cache [lanes][Hkv][cap][D]; the call
+ * first writes the verify rows' keys / values k_new, v_new [M][Hkv][D] at positions ctx[l] + j
+ * (j = 0..7), then for row r = 8l + j and q head h (kv head h / (Hq / Hkv)):
+ *   out[r][h] = softmax_t(q[r][h] . k_t / sqrt(D)) over t = 0 .. ctx[l] + j, weighting v_t,
+ *               times sigmoid(gate[r][h]) elementwise when gate is not NULL, rounded once to bf16.
+ * q, gate, out: bf16 [M][Hq][D].  q and k are taken as given (after the layer's Q/K RMSNorm and RoPE,
+ * which are elementwise steps before this one).  D = 256; Hq % Hkv == 0, Hq / Hkv <= 8; cap >= 8.
+ * ctx is a device array [lanes] (so a device-resident loop can advance it); a lane with ctx[l] < 0 or
+ * ctx[l] + 8 > cap is skipped (its output is zero and the workspace's status word reads
+ * VP_ERR_SHAPE, see vp_read_status).  Partitions of at most 1,024 keys (shorter, in multiples of 64,
+ * when that fills the GPU's 152 SMs in one wave) run in parallel (one CTA per partition, kv head and
+ * lane) and are merged in a fixed order: bit-reproducible for a given cap.  QK^T runs on the
+ * tensor core in bf16, P V in f16 (values must lie in f16's range, where bf16 values are exact).
+ * Workspace: vp_workspace_bytes(VP_OP_ATTN, M, Hkv, cap), 256-byte aligned.  Three launches. */
+vp_status vp_attention_verify(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                              const int32_t* ctx, int cap, const void* gate, void* out, int M, int Hq, int Hkv, int D,
+                              void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------ the verify pass
  *

@@ -121,6 +121,26 @@ def test_sample_accept_validation_without_gpu(V):
     assert call(wsb=ws - 1) == V.VP_ERR_WORKSPACE
 
 
+def test_attention_validation_without_gpu(V):
+    L = V.lib()
+    ws = V.vp_workspace_bytes(V.VP_OP_ATTN, 8, 4, 4096)
+    assert ws > 0 and V.vp_workspace_bytes(V.VP_OP_ATTN, 9, 4, 4096) == 0 and V.vp_workspace_bytes(V.VP_OP_ATTN, 8, 4, 7) == 0
+    F = FAKE
+    ok = [F, F, F, F, F, F, 4096, F, F, 8, 24, 4, 256, F, ws, None]
+    names = ["q", "kn", "vn", "kc", "vc", "ctx", "cap", "gate", "out", "M", "Hq", "Hkv", "D", "ws", "wsb", "s"]
+
+    def call(**kw):
+        a = list(ok)
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return L.vp_attention_verify(*a)
+    assert call(q=None) == V.VP_ERR_INVALID_ARG and call(ctx=None) == V.VP_ERR_INVALID_ARG
+    assert call(D=128) == V.VP_ERR_SHAPE and call(Hq=25) == V.VP_ERR_SHAPE and call(Hq=40, Hkv=4) == V.VP_ERR_SHAPE
+    assert call(M=12) == V.VP_ERR_SHAPE and call(cap=7) == V.VP_ERR_SHAPE
+    assert call(kc=F + 8) == V.VP_ERR_ALIGNMENT and call(ctx=F + 2) == V.VP_ERR_ALIGNMENT
+    assert call(wsb=ws - 1) == V.VP_ERR_WORKSPACE
+
+
 def test_head_and_argmax_validation_without_gpu(V):
     L = V.lib()
     ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)

@@ -16,7 +16,7 @@ LIB_PATH = os.environ.get("VP_LIBVERIFY") or os.path.join(_PKG, "libverify.so")
 
 VP_OK, VP_ERR_INVALID_ARG, VP_ERR_SHAPE, VP_ERR_ALIGNMENT, VP_ERR_WORKSPACE, VP_ERR_CUDA, VP_ERR_TIMEOUT, \
     VP_ERR_UNSUPPORTED = range(8)
-VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX, VP_OP_Q4, VP_OP_SAMPLE = range(6)
+VP_OP_NVFP4, VP_OP_FP8, VP_OP_HEAD, VP_OP_ARGMAX, VP_OP_Q4, VP_OP_SAMPLE, VP_OP_ATTN = range(7)
 VP_LAYER_GDN, VP_LAYER_ATTN = 0, 1
 
 # Every symbol include/verify.h declares.
@@ -26,7 +26,7 @@ EXPORTS = [
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
     "vp_linear_nvfp4_noalloc", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
-    "vp_sample_accept",
+    "vp_sample_accept", "vp_attention_verify",
 ]
 
 
@@ -86,6 +86,7 @@ def _load():
         "vp_pack_q4": (I, [P, P, P, I, I, P, S, P]),
         "vp_linear_q4": (I, [P, P, P, I, I, I, P, S, P]),
         "vp_sample_accept": (I, [P, I, I, F, I, F, P, P, P, P, P, P, P, S, P]),
+        "vp_attention_verify": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -208,6 +209,14 @@ def vp_sample_accept(logits, M: int, V: int, temperature: float, top_k: int, top
            _L.vp_sample_accept(_ptr(logits), M, V, temperature, top_k, top_p, _ptr(pending), _ptr(draft_tokens),
                                _ptr(draft_probs), _ptr(uniforms), _ptr(n_commit), _ptr(committed), _ptr(ws), wb,
                                _stream(stream)))
+
+
+def vp_attention_verify(q, k_new, v_new, k_cache, v_cache, ctx, cap: int, gate, out, M: int, Hq: int, Hkv: int,
+                        D: int, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_attention_verify",
+           _L.vp_attention_verify(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(ctx), cap,
+                                  _ptr(gate), _ptr(out), M, Hq, Hkv, D, _ptr(ws), wb, _stream(stream)))
 
 
 def vp_workspace_init(ws, stream=None, ws_bytes=None):

@@ -11,6 +11,7 @@
 #include "exec.cuh"
 #include "exec_launch.h"
 #include "internal.h"
+#include "attention.h"
 #include "sample.h"
 #include "verify.h"
 
@@ -443,6 +444,10 @@ size_t vp_workspace_bytes(int op, int M, int N, int K) {
     if (M < 8 || M > kMaxM || M % 8 || N < 1) return 0;
     return ws_layout(1, 1, 1).rb_cnt;  // the counter and the per-chunk maxima
   }
+  if (op == VP_OP_ATTN) {  // N = kv heads, K = cache capacity (positions per lane)
+    if (M < 8 || M > kMaxM || M % 8 || N < 1 || K < 8 || K > (1 << 24)) return 0;
+    return attn_ws_layout(M, N, K).total;
+  }
   if (op == VP_OP_SAMPLE) {
     if (M < 8 || M > kMaxM || M % 8 || N < 1 || N > kSampleMaxV) return 0;
     return sample_ws_layout(M, N).total;
@@ -527,6 +532,37 @@ vp_status vp_sample_accept(const float* logits, int M, int V, float temperature,
   if (ws_bytes < sample_ws_layout(M, V).total) return VP_ERR_WORKSPACE;
   cudaError_t e = launch_sample_accept(logits, M, V, temperature, top_k, top_p, pending, draft_tokens, draft_probs,
                                        uniforms, n_commit, committed, ws, (cudaStream_t)stream);
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
+vp_status vp_attention_verify(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                              const int32_t* ctx, int cap, const void* gate, void* out, int M, int Hq, int Hkv, int D,
+                              void* ws, size_t ws_bytes, void* stream) {
+  if (!q || !k_new || !v_new || !k_cache || !v_cache || !ctx || !out || !ws) return VP_ERR_INVALID_ARG;
+  if (M < 8 || M > kMaxM || M % 8 || D != 256 || Hkv < 1 || Hq < Hkv || Hq % Hkv || Hq / Hkv > 8 || cap < 8 ||
+      cap > (1 << 24))
+    return VP_ERR_SHAPE;
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+      !aligned(v_cache, 16) || !aligned(ctx, 4) || (gate && !aligned(gate, 16)) || !aligned(out, 16) ||
+      !aligned(ws, 256))
+    return VP_ERR_ALIGNMENT;
+  if (ws_bytes < attn_ws_layout(M, Hkv, cap).total) return VP_ERR_WORKSPACE;
+  int sms = 0;
+  vp_status st = device_sms(&sms);
+  if (st != VP_OK) return st;
+  AttnArgs a;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k_new = static_cast<const uint16_t*>(k_new);
+  a.v_new = static_cast<const uint16_t*>(v_new);
+  a.k_cache = static_cast<uint16_t*>(k_cache);
+  a.v_cache = static_cast<uint16_t*>(v_cache);
+  a.ctx = ctx;
+  a.gate = static_cast<const uint16_t*>(gate);
+  a.out = static_cast<uint16_t*>(out);
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.cap = cap;
+  cudaError_t e = launch_attention_verify(a, M, ws, (cudaStream_t)stream);
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
