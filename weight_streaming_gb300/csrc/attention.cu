@@ -18,7 +18,9 @@
 //    ldmatrix is conflict-free); S = Q K^T on the tensor core in bf16 (q and k exact), the online
 //    softmax in fp32 (exp2 with the 1/sqrt(D) log2(e) scale folded in), then O += P V in f16 (P in
 //    [0, 1]; the value tile converted from bf16 to f16 in shared memory once per tile, exact in f16's
-//    range).  Warp w owns m-tile w % 4 and output dims 128 (w / 4) .. + 127.
+//    range).  Warps w and w + 4 share m-tile w % 4: each computes S for half of the tile's keys, they
+//    exchange the row maxima and their halves of P through shared memory (named barrier per pair),
+//    and each accumulates output dims 128 (w / 4) .. + 127 over all keys.
 //  * attn_merge: per output row and head, the partitions' partials in a fixed order, then the sigmoid
 //    gate and one bf16 rounding.
 #include <cuda_bf16.h>
@@ -78,6 +80,12 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// Byte offset of (row, key) in the [rows][64] f16 P tile, 16-byte chunks XOR-swizzled by row.
+__device__ __forceinline__ uint32_t pswz(int r, int key) {
+  return (uint32_t)(r * 128 + ((((key >> 3) ^ (r & 7)) << 4) | ((key & 7) << 1)));
+}
+// The two warps of m-tile mt (warps mt and mt + 4) meet at named barrier 1 + mt.
+__device__ __forceinline__ void pair_sync(int mt) { asm volatile("bar.sync %0, 64;" ::"r"(1 + mt) : "memory"); }
 __device__ __forceinline__ uint32_t pack_f16(float a, float b) {
   const __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -141,6 +149,8 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
   ATTN_ISSUE(0, 0)
   cp_async_commit();  // group 0: Q and tile 0
 
+  __shared__ float xmax[4][2][16];                // per m-tile, per warp of the pair: row maxima, then sums
+  __shared__ __align__(16) uint8_t sP[4 * 16 * 128];  // per m-tile: P [16 rows][64 keys] f16, swizzled
   const int mt = warp & 3, dh = warp >> 2;
   const bool live = mt * 16 < rows;
   const float sl2 = 1.4426950408889634f / sqrtf((float)kD);  // log2(e) / sqrt(D)
@@ -168,28 +178,29 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
     }
     __syncthreads();
     if (live) {
-      // S = Q K^T for the m-tile, 64 keys: 8 n-tiles
-      float s[8][4];
+      // S = Q K^T for the m-tile and this warp's 32 keys of the tile (4 n-tiles); the pair's other
+      // warp takes the other 32.
+      float s[4][4];
 #pragma unroll
-      for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
+      for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.0f;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(sQ + swz(mt * 16 + (lane & 15), 2 * ks + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
+        for (int np = 0; np < 2; ++np) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(sK0 + b * kTileBytes + swz(np * 16 + (lane >> 4) * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1)), b0,
-                  b1, b2, b3);
+          ldsm_x4(sK0 + b * kTileBytes + swz(dh * 32 + np * 16 + (lane >> 4) * 8 + (lane & 7), 2 * ks + ((lane >> 3) & 1)),
+                  b0, b1, b2, b3);
           mma_bf16(s[2 * np], a0, a1, a2, a3, b0, b1);
           mma_bf16(s[2 * np + 1], a0, a1, a2, a3, b2, b3);
         }
       }
-      // online softmax (log2 units), causal mask per row
-      const int base = k0 + t * kTile;
+      // online softmax (log2 units), causal mask per row; the row maximum over both halves
+      const int base = k0 + t * kTile + dh * 32;
       float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int pos = base + n * 8 + 2 * cq + (e & 1), h = e >> 1;
@@ -197,18 +208,26 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
           s[n][e] = v;
           mx[h] = fmaxf(mx[h], v);
         }
-      float alpha[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
         mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
-        const float mn = fmaxf(m_r[h], mx[h]);
+      }
+      if (cq == 0) {
+        xmax[mt][dh][gq] = mx[0];
+        xmax[mt][dh][gq + 8] = mx[1];
+      }
+      pair_sync(mt);
+      float alpha[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float mn = fmaxf(m_r[h], fmaxf(mx[h], xmax[mt][dh ^ 1][gq + 8 * h]));
         alpha[h] = mn == -INFINITY ? 1.0f : exp2f(m_r[h] - mn);
         m_r[h] = mn;
       }
       float rs[2] = {0.0f, 0.0f};
 #pragma unroll
-      for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < 4; ++n)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int h = e >> 1;
@@ -217,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
           rs[h] += p;
         }
 #pragma unroll
-      for (int h = 0; h < 2; ++h) l_r[h] = alpha[h] * l_r[h] + rs[h];
+      for (int h = 0; h < 2; ++h) l_r[h] = alpha[h] * l_r[h] + rs[h];  // this warp's keys only
 #pragma unroll
       for (int n = 0; n < 16; ++n) {
         o[n][0] *= alpha[0];
@@ -225,11 +244,35 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
         o[n][2] *= alpha[1];
         o[n][3] *= alpha[1];
       }
-      // O += P V for this warp's 128 output dims: 4 key steps of 16, 16 n-tiles of 8 dims
+      // this warp's half of P (f16) for the other warp of the pair
+      uint32_t pa[2][4];  // A fragments of this warp's two 16-key steps
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        pa[kk][0] = pack_f16(s[2 * kk][0], s[2 * kk][1]);
+        pa[kk][1] = pack_f16(s[2 * kk][2], s[2 * kk][3]);
+        pa[kk][2] = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        pa[kk][3] = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // n-tile 2 kk + hh: keys dh * 32 + 16 kk + 8 hh + 2 cq
+          const int key = dh * 32 + 16 * kk + 8 * hh + 2 * cq;
+          *reinterpret_cast<uint32_t*>(sP + pswz(mt * 16 + gq, key)) = pa[kk][2 * hh];
+          *reinterpret_cast<uint32_t*>(sP + pswz(mt * 16 + gq + 8, key)) = pa[kk][2 * hh + 1];
+        }
+      }
+      pair_sync(mt);
+      // O += P V for this warp's 128 output dims: 4 key steps of 16 (two from registers, two from the
+      // other warp through shared memory), 16 n-tiles of 8 dims
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t a0 = pack_f16(s[2 * kk][0], s[2 * kk][1]), a1 = pack_f16(s[2 * kk][2], s[2 * kk][3]);
-        const uint32_t a2 = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]), a3 = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+        uint32_t a0, a1, a2, a3;
+        if ((kk >> 1) == dh) {
+          a0 = pa[kk & 1][0];
+          a1 = pa[kk & 1][1];
+          a2 = pa[kk & 1][2];
+          a3 = pa[kk & 1][3];
+        } else {
+          ldsm_x4(smem_u32(sP) + pswz(mt * 16 + (lane & 15), 16 * kk + 8 * (lane >> 4)), a0, a1, a2, a3);
+        }
 #pragma unroll
         for (int np = 0; np < 8; ++np) {
           uint32_t b0, b1, b2, b3;
@@ -244,12 +287,19 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
 #undef ATTN_ISSUE
   cp_async_wait<0>();
   if (!live) return;
-  // partials: m (log2 units), l (the row's full sum), o unnormalised
+  // partials: m (log2 units), l (the row's full sum over both warps of the pair), o unnormalised
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 1);
     l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 2);
   }
+  if (cq == 0) {
+    xmax[mt][dh][gq] = l_r[0];
+    xmax[mt][dh][gq + 8] = l_r[1];
+  }
+  pair_sync(mt);
+  l_r[0] += xmax[mt][dh ^ 1][gq];
+  l_r[1] += xmax[mt][dh ^ 1][gq + 8];
   const int r0 = mt * 16 + gq, r1 = r0 + 8;
   if (cq == 0 && dh == 0) {
     pML[2 * r0] = m_r[0];
