@@ -17,7 +17,9 @@ the passage of the pages it follows:
   per group of 64 inputs, 32 bytes of codes, a bf16 scale and a bf16 bias; ``linear_q4``) and "Exact,
   up to top-32" (speculative sampling over the top_k <= 32 target candidates; ``sample_accept``).
 * "lithos-metal ..." -- "The megakernel is per layer, not per step" (the attention core over a BF16
-  KV cache with online-softmax partitions and a sigmoid gate; ``attention_verify``).
+  KV cache with online-softmax partitions and a sigmoid gate; ``attention_verify``; the GDN commit
+  re-scan) and "Beating Splash ..." -- "What actually moved the needle" (double-buffered GDN state,
+  re-scan of the committed rows; ``gdn_scan``, with the published gated delta rule).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against page values,
 closed forms, library routines or brute force, except the 64-layer surrogate chain, whose
@@ -97,6 +99,9 @@ def lib():
             L.orc_attention_verify.restype = ctypes.c_int
             L.orc_attention_verify.argtypes = [P, P, P, P, P, P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_int, ctypes.c_int, P, P]
+            L.orc_gdn_scan.restype = ctypes.c_int
+            L.orc_gdn_scan.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, P]
             L.orc_silu_mul.argtypes = [P, P, ctypes.c_int64, P]
             L.orc_rmsnorm.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
             L.orc_argmax.restype = ctypes.c_int64
@@ -255,6 +260,27 @@ def attention_verify(q, k_new, v_new, k_cache, v_cache, ctx, gate=None, with_abs
     if rc != 0:
         raise ValueError("orc_attention_verify rejected its arguments")
     return (out, a) if with_abs else out
+
+
+def gdn_scan(state_in, q, k, v, alpha, beta, rows, want_out=True):
+    """Gated delta rule scan of each lane's first rows[l] verify rows from state_in [L][H][dv][dk]
+    (see orc_gdn_scan); returns (state_out fp64, out fp64 [M][H][dv] or None)."""
+    st = np.ascontiguousarray(state_in, dtype=np.float64)
+    L, H, dv, dk = st.shape
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    M = q.shape[0]
+    kk = np.ascontiguousarray(k, dtype=np.uint16)
+    vv = np.ascontiguousarray(v, dtype=np.uint16)
+    a = np.ascontiguousarray(alpha, dtype=np.float64)
+    b = np.ascontiguousarray(beta, dtype=np.float64)
+    rw = np.ascontiguousarray(rows, dtype=np.int32)
+    so = np.zeros_like(st)
+    out = np.zeros((M, H, dv), np.float64) if want_out else None
+    rc = lib().orc_gdn_scan(_p(st), _p(so), _p(q), _p(kk), _p(vv), _p(a), _p(b), _p(rw), M, H, dk, dv,
+                            _p(out) if out is not None else None)
+    if rc != 0:
+        raise ValueError("orc_gdn_scan rejected its arguments")
+    return so, out
 
 
 def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:

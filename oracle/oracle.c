@@ -523,6 +523,67 @@ int orc_attention_verify(const uint16_t* q, const uint16_t* k_new, const uint16_
     return 0;
 }
 
+/* ------------------------------------------------------------------ Gated DeltaNet verify scan
+ *
+ * "Beating Splash on an M5 Max", section "What actually moved the needle": the fused GatedDeltaNet
+ * step writes out of place from parity buffer A to parity buffer B; rejecting part of a round
+ * re-scans only the committed rows from the still-intact A, and the state after every possible
+ * number of kept tokens must match a reference scan exactly.  "lithos-metal ...", sections "What one
+ * token costs the bus" (fp32 state (v_heads, dk, dv), 48 x 128 x 128 per layer) and "The megakernel
+ * is per layer, not per step" (the commit pass recomputes the recurrence over the committed tokens,
+ * whose count the accept scan wrote).  The pages name the layer (Gated DeltaNet) but do not print its
+ * recurrence; the oracle takes the published gated delta rule (Yang, Kautz and Hatamizadeh, "Gated
+ * Delta Networks: Improving Mamba2 with Delta Rule", 2024), per head with S a dv x dk matrix:
+ *   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,   o_t = S_t q_t
+ * (= S_{t-1} alpha_t (I - beta_t k_t k_t^T) + beta_t v_t k_t^T).  Readings: one q / k per v head;
+ * q, k, v arrive after the layer's short convolution, activation and normalisation, and alpha, beta
+ * after their gates (all producer steps); lane l scans its first rows[l] verify rows (8 for the
+ * verify pass, the committed count for the re-scan).
+ *
+ * state_in, state_out: [L][H][dv][dk] (fp64 here); q, k: bf16 [M][H][dk]; v: bf16 [M][H][dv];
+ * alpha, beta: [M][H]; out: [M][H][dv] (rows past rows[l] are left untouched). */
+int orc_gdn_scan(const double* state_in, double* state_out, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                 const double* alpha, const double* beta, const int32_t* rows, int M, int H, int dk, int dv,
+                 double* out) {
+    if (M < 8 || M % 8 || H < 1 || dk < 1 || dv < 1 || !state_in || !state_out || !q || !k || !v || !alpha || !beta ||
+        !rows)
+        return -1;
+    const int L = M / 8;
+    double* u = (double*)malloc(sizeof(double) * (size_t)dv);
+    if (!u) return -1;
+    for (int l = 0; l < L; ++l) {
+        if (rows[l] < 0 || rows[l] > 8) { free(u); return -1; }
+        for (int h = 0; h < H; ++h) {
+            const int64_t so = ((int64_t)l * H + h) * dv * dk;
+            double* S = state_out + so;
+            memcpy(S, state_in + so, sizeof(double) * (size_t)dv * dk);
+            for (int j = 0; j < rows[l]; ++j) {
+                const int r = 8 * l + j;
+                const uint16_t* kr = k + ((int64_t)r * H + h) * dk;
+                const uint16_t* qr = q + ((int64_t)r * H + h) * dk;
+                const uint16_t* vr = v + ((int64_t)r * H + h) * dv;
+                const double a = alpha[(int64_t)r * H + h], b = beta[(int64_t)r * H + h];
+                for (int i = 0; i < dv; ++i) {
+                    double sk = 0.0;
+                    for (int c = 0; c < dk; ++c) sk += S[(int64_t)i * dk + c] * orc_bf16_value(kr[c]);
+                    u[i] = b * (orc_bf16_value(vr[i]) - a * sk);
+                }
+                for (int i = 0; i < dv; ++i)
+                    for (int c = 0; c < dk; ++c)
+                        S[(int64_t)i * dk + c] = a * S[(int64_t)i * dk + c] + u[i] * orc_bf16_value(kr[c]);
+                if (out)
+                    for (int i = 0; i < dv; ++i) {
+                        double o = 0.0;
+                        for (int c = 0; c < dk; ++c) o += S[(int64_t)i * dk + c] * orc_bf16_value(qr[c]);
+                        out[((int64_t)r * H + h) * dv + i] = o;
+                    }
+            }
+        }
+    }
+    free(u);
+    return 0;
+}
+
 /* Probability the draft gave token t (0 when t is not among its 16 candidates). */
 static double orc_q_of(const int32_t* dt, const double* dp, int32_t t) {
     for (int i = 0; i < 16; ++i) if (dt[i] == t) return dp[i];

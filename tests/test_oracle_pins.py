@@ -684,3 +684,67 @@ def test_attention_causal_and_grouped():
     q2[:, 4], g2[:, 4] = q2[:, 0], g2[:, 0]
     out3 = oracle.attention_verify(q2, kn, vn, kc, vc, ctx, g2, with_abs=False)
     assert np.array_equal(out3[:, 0], out3[:, 1]) and not np.array_equal(out3[:, 0], out3[:, 4])
+
+
+# ------------------------------------------------------------------ Gated DeltaNet verify scan
+
+def gdn_case(rng, L=1, H=2, d=16):
+    M = 8 * L
+    st = rng.standard_normal((L, H, d, d)) * 0.3
+    q = rand_bf16(rng, (M, H, d))
+    k = rand_bf16(rng, (M, H, d), 0.25)
+    v = rand_bf16(rng, (M, H, d))
+    a = rng.uniform(0.8, 1.0, (M, H))
+    b = rng.uniform(0.0, 1.0, (M, H))
+    return st, q, k, v, a, b
+
+
+def test_gdn_matches_matrix_form_of_the_delta_rule():
+    """Against the gated delta rule written as matrix products in torch:
+    S_t = S_{t-1} alpha (I - beta k k^T) + beta v k^T, o_t = S_t q_t."""
+    rng = np.random.default_rng(41)
+    st, q, k, v, a, b = gdn_case(rng, L=2)
+    rows = np.array([8, 5], np.int32)
+    so, out = oracle.gdn_scan(st, q, k, v, a, b, rows)
+    f = lambda x: torch.from_numpy(bf16_vals_torch(x))  # noqa: E731
+    for l in range(2):
+        for h in range(2):
+            S = torch.from_numpy(st[l, h].copy())
+            for j in range(rows[l]):
+                r = 8 * l + j
+                kv, vv, qv = f(k[r, h]), f(v[r, h]), f(q[r, h])
+                eye = torch.eye(kv.numel(), dtype=torch.float64)
+                S = S @ (a[r, h] * (eye - b[r, h] * torch.outer(kv, kv))) + b[r, h] * torch.outer(vv, kv)
+                np.testing.assert_allclose(out[r, h], (S @ qv).numpy(), rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(so[l, h], S.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_gdn_closed_forms():
+    rng = np.random.default_rng(42)
+    st, q, k, v, a, b = gdn_case(rng)
+    # no rows: the state passes through unchanged
+    so, _ = oracle.gdn_scan(st, q, k, v, a, b, [0])
+    assert np.array_equal(so, st)
+    # beta = 0: pure decay by the product of the alphas
+    so, _ = oracle.gdn_scan(st, q, k, v, a, np.zeros_like(b), [8])
+    np.testing.assert_allclose(so[0], st[0] * np.prod(a, axis=0)[:, None, None], rtol=1e-13)
+    # alpha = beta = 1 and k = e_c: the delta rule overwrites column c of S with v
+    k1 = np.zeros_like(k)
+    k1[:, :, 3] = 0x3F80  # bf16 1.0
+    so, _ = oracle.gdn_scan(st, q, k1, v, np.ones_like(a), np.ones_like(b), [1])
+    expect = st[0].copy()
+    expect[:, :, 3] = bf16_vals_torch(v[0])
+    np.testing.assert_allclose(so[0], expect, rtol=0, atol=1e-15)
+
+
+def test_gdn_scan_composes_row_by_row():
+    """The re-scan invariant: scanning n rows at once equals n one-row scans in sequence."""
+    rng = np.random.default_rng(43)
+    st, q, k, v, a, b = gdn_case(rng)
+    for n in range(9):
+        full, _ = oracle.gdn_scan(st, q, k, v, a, b, [n])
+        cur = st
+        for j in range(n):
+            sh = lambda x: np.roll(x, -j, axis=0)  # noqa: E731  (row j first)
+            cur, _ = oracle.gdn_scan(cur, sh(q), sh(k), sh(v), sh(a), sh(b), [1])
+        np.testing.assert_array_equal(full, cur)
