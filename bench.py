@@ -38,7 +38,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=64)
-    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample", "attn"],
+    ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample", "attn",
+                             "gdn"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--ctx", type=int, default=32768, help="context length per lane for --kernel attn")
@@ -234,6 +235,31 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ the GPU arm
 
+def graph_time(fn, steps: int, warmup: int) -> float:
+    """Seconds per call of fn (a sequence of library launches on the current stream), captured once
+    in a CUDA graph and replayed, so that the host's launch path is not timed; CUDA events on the
+    capturing stream."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm the library's one-time set-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fn()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(steps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / steps
+
+
 def run_sample(args):
     """vp_sample_accept alone over fp32 logits [M][248320] (top_k 20, top_p 0.95, temperature 0.7,
     draft distributions of 16 candidates); prints one JSON line with the time per call and the logit
@@ -254,16 +280,7 @@ def run_sample(args):
 
     def call():
         V.vp_sample_accept(logits, M, Vv, 0.7, 20, 0.95, pending, dt, dp, u, nc, cm, ws)
-    for _ in range(args.warmup):
-        call()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        call()
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    t = graph_time(call, args.steps, args.warmup)
     nbytes = M * Vv * 4
     print(json.dumps({"kernel": "sample", "M": M, "V": Vv, "us_per_call": t * 1e6, "launches_per_call": 1,
                       "logit_gbps": nbytes / t / 1e9, "bytes_per_call": nbytes}), flush=True)
@@ -289,23 +306,45 @@ def run_attn(args):
     out = torch.empty((M, Hq, D), dtype=torch.bfloat16, device="cuda")
     ws = torch.zeros(V.vp_workspace_bytes(V.VP_OP_ATTN, M, Hkv, cap), dtype=torch.uint8, device="cuda")
 
-    def call(i):
-        kc, vc = caches[i % copies]
-        V.vp_attention_verify(q, kn, vn, kc, vc, ctx_d, cap, gate, out, M, Hq, Hkv, D, ws)
-    for i in range(args.warmup):
-        call(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.steps):
-        call(i)
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / args.steps
+    def calls():  # one call per cache copy
+        for kc, vc in caches:
+            V.vp_attention_verify(q, kn, vn, kc, vc, ctx_d, cap, gate, out, M, Hq, Hkv, D, ws)
+    t = graph_time(calls, args.steps, args.warmup) / copies
     nbytes = L * Hkv * (ctx + 8) * D * 2 * 2  # keys and values read once
     peak = (measured_peaks() or {}).get("hbm_gbs")
     print(json.dumps({"kernel": "attn", "M": M, "ctx": ctx, "heads": [Hq, Hkv, D], "us_per_call": t * 1e6,
-                      "launches_per_call": 3, "kv_gbps": nbytes / t / 1e9, "bytes_per_call": nbytes, "copies": copies,
+                      "launches_per_call": 3, "timing": "CUDA graph of one call per cache copy, replayed", "kv_gbps": nbytes / t / 1e9, "bytes_per_call": nbytes, "copies": copies,
+                      "frac_of_measured_copy": (nbytes / t / 1e9 / peak) if peak else None}), flush=True)
+
+
+def run_gdn(args):
+    """vp_gdn_scan for the 48 Gated DeltaNet layers of one pass (48 heads of 128 x 128 fp32 state per
+    layer and lane, parity A -> B, 8 verify rows), one launch per layer; prints one JSON line with
+    the time per layer and the state bytes read + written per second."""
+    import torch
+
+    from weight_streaming_gb300 import _lib as V
+    M, H, d, layers = args.M, 48, 128, 48
+    L = M // 8
+    g = torch.Generator(device="cuda").manual_seed(0)
+    sa = torch.randn((layers, L, H, d, d), device="cuda", generator=g) * 0.1
+    sb = torch.empty_like(sa)
+    q = torch.randn((M, H, d), device="cuda", generator=g).to(torch.bfloat16)
+    k = (torch.randn((M, H, d), device="cuda", generator=g) / d ** 0.5).to(torch.bfloat16)
+    v = torch.randn((M, H, d), device="cuda", generator=g).to(torch.bfloat16)
+    a = torch.full((M, H), 0.95, device="cuda")
+    b = torch.full((M, H), 0.5, device="cuda")
+    rows = torch.full((L,), 8, dtype=torch.int32, device="cuda")
+    out = torch.empty((M, H, d), device="cuda")
+
+    def step():
+        for layer in range(layers):
+            V.vp_gdn_scan(sa[layer], sb[layer], q, k, v, a, b, rows, M, H, d, d, out)
+    t = graph_time(step, args.steps, args.warmup) / layers
+    nbytes = L * H * d * d * 4 * 2
+    peak = (measured_peaks() or {}).get("hbm_gbs")
+    print(json.dumps({"kernel": "gdn", "M": M, "heads": H, "us_per_layer": t * 1e6, "state_gbps": nbytes / t / 1e9,
+                      "bytes_per_layer": nbytes, "us_per_pass_48_layers": t * 1e6 * layers,
                       "frac_of_measured_copy": (nbytes / t / 1e9 / peak) if peak else None}), flush=True)
 
 
@@ -313,6 +352,9 @@ def run_kernel(args):
     """One GEMM of the pass alone through the C ABI, rotating over 4 weight copies (> L2) so every
     launch streams from DRAM; prints one JSON line with the average launch time and GB/s."""
     import torch
+    if args.kernel == "gdn":
+        run_gdn(args)
+        return
     if args.kernel == "sample":
         run_sample(args)
         return
@@ -359,16 +401,11 @@ def run_kernel(args):
     else:
         fn = V.vp_linear_nvfp4 if fmt == "nvfp4" else V.vp_linear_fp8
     torch.cuda.synchronize()
-    for i in range(args.warmup):
-        fn(ws_list[i % copies], 1.0, x, y, M, N, K, ws)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.steps):
-        fn(ws_list[i % copies], 1.0, x, y, M, N, K, ws)
-    e1.record()
-    torch.cuda.synchronize()
-    t = e0.elapsed_time(e1) / 1e3 / args.steps
+
+    def calls():  # one launch per weight copy
+        for w in ws_list:
+            fn(w, 1.0, x, y, M, N, K, ws)
+    t = graph_time(calls, args.steps, args.warmup) / copies
     nbytes = N * K * 9 // 16 if fmt in ("nvfp4", "q4") else N * K
     peak = (measured_peaks() or {}).get("hbm_gbs")
     print(json.dumps({"kernel": args.kernel, "fmt": fmt, "M": M, "N": N, "K": K, "us_per_launch": t * 1e6,

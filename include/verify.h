@@ -31,6 +31,12 @@
  *                attention figure and text: an attention core that reads and appends a BF16 KV cache,
  *                causal softmax of q k^T weighting V, times the sigmoid of the gate; the KV range split
  *                into partitions of up to 1,024 keys whose online-softmax partials are merged).
+ *   [BS-gdn]     "Beating Splash on an M5 Max", section "What actually moved the needle" (the GDN step
+ *                writes out of place from parity buffer A to B; a partly rejected round re-scans only
+ *                the committed rows from the intact A; the state after every possible number of kept
+ *                tokens matches a reference scan exactly); "lithos-metal ...", sections "What one
+ *                token costs the bus" (fp32 state (v_heads, dk, dv) = 48 x 128 x 128 per layer) and
+ *                "The megakernel is per layer, not per step" (the commit re-scan).
  *   [SP-q4]      "144 tok/s needs 502 GB/s" (Splash), section "The engine hard-codes the model": the
  *                other engines' affine 4-bit format, per group of 64 inputs 32 bytes of codes plus
  *                a bf16 scale and a bf16 bias (nine bytes per sixteen weights); "Beating Splash on
@@ -241,6 +247,22 @@ vp_status vp_sample_accept(const float* logits, int M, int V, float temperature,
 vp_status vp_attention_verify(const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                               const int32_t* ctx, int cap, const void* gate, void* out, int M, int Hq, int Hkv, int D,
                               void* ws, size_t ws_bytes, void* stream);
+
+/* Gated DeltaNet verify scan [BS-gdn]: for lane l (M = 8 * lanes) and head h, from state_in
+ * (fp32 [lanes][H][dv][dk], parity buffer A) over the lane's first rows[l] verify rows
+ * (rows: device int32 [lanes], clamped to 0..8), the gated delta rule
+ *   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,   o_t = S_t q_t
+ * (the published Gated DeltaNet recurrence; the pages name the layer, not the formula), writing the
+ * final state to state_out (parity buffer B; may equal state_in for an in-place update) and, when
+ * out is not NULL, o_t to out (fp32 [M][H][dv], rows past rows[l] untouched).  q, k: bf16 [M][H][dk];
+ * v: bf16 [M][H][dv]; alpha, beta: fp32 [M][H] (after the layer's gates; q, k, v after its short
+ * convolution, activation and normalisation -- producer steps).  Verify: rows = 8 from A to B;
+ * commit after a partial accept: rows = n_commit from A to B again -- the same kernel, so the
+ * re-scan's state equals the verify scan's state after those rows bit for bit.  dk = dv = 128.
+ * One launch, no workspace. */
+vp_status vp_gdn_scan(const float* state_in, float* state_out, const void* q, const void* k, const void* v,
+                      const float* alpha, const float* beta, const int32_t* rows, int M, int H, int dk, int dv,
+                      float* out, void* stream);
 
 /* ------------------------------------------------------------------ the verify pass
  *

@@ -141,6 +141,22 @@ def test_attention_validation_without_gpu(V):
     assert call(wsb=ws - 1) == V.VP_ERR_WORKSPACE
 
 
+def test_gdn_validation_without_gpu(V):
+    L = V.lib()
+    F = FAKE
+    ok = [F, F, F, F, F, F, F, F, 8, 48, 128, 128, F, None]
+    names = ["si", "so", "q", "k", "v", "a", "b", "rows", "M", "H", "dk", "dv", "out", "s"]
+
+    def call(**kw):
+        a = list(ok)
+        for key, val in kw.items():
+            a[names.index(key)] = val
+        return L.vp_gdn_scan(*a)
+    assert call(si=None) == V.VP_ERR_INVALID_ARG and call(rows=None) == V.VP_ERR_INVALID_ARG
+    assert call(M=12) == V.VP_ERR_SHAPE and call(dk=64) == V.VP_ERR_SHAPE and call(H=0) == V.VP_ERR_SHAPE
+    assert call(si=F + 2) == V.VP_ERR_ALIGNMENT and call(a=F + 2) == V.VP_ERR_ALIGNMENT
+
+
 def test_head_and_argmax_validation_without_gpu(V):
     L = V.lib()
     ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)

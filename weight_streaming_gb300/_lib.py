@@ -26,7 +26,7 @@ EXPORTS = [
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
     "vp_linear_nvfp4_noalloc", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
-    "vp_sample_accept", "vp_attention_verify",
+    "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan",
 ]
 
 
@@ -87,6 +87,7 @@ def _load():
         "vp_linear_q4": (I, [P, P, P, I, I, I, P, S, P]),
         "vp_sample_accept": (I, [P, I, I, F, I, F, P, P, P, P, P, P, P, S, P]),
         "vp_attention_verify": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, S, P]),
+        "vp_gdn_scan": (I, [P, P, P, P, P, P, P, P, I, I, I, I, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -217,6 +218,12 @@ def vp_attention_verify(q, k_new, v_new, k_cache, v_cache, ctx, cap: int, gate, 
     _check("vp_attention_verify",
            _L.vp_attention_verify(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(ctx), cap,
                                   _ptr(gate), _ptr(out), M, Hq, Hkv, D, _ptr(ws), wb, _stream(stream)))
+
+
+def vp_gdn_scan(state_in, state_out, q, k, v, alpha, beta, rows, M: int, H: int, dk: int, dv: int, out,
+                stream=None):
+    _check("vp_gdn_scan", _L.vp_gdn_scan(_ptr(state_in), _ptr(state_out), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                         _ptr(beta), _ptr(rows), M, H, dk, dv, _ptr(out), _stream(stream)))
 
 
 def vp_workspace_init(ws, stream=None, ws_bytes=None):

@@ -12,6 +12,7 @@
 #include "exec_launch.h"
 #include "internal.h"
 #include "attention.h"
+#include "errors.h"
 #include "sample.h"
 #include "verify.h"
 
@@ -19,12 +20,6 @@ using namespace vp;
 
 namespace {
 
-thread_local int g_last_cuda_error = 0;
-
-vp_status cuda_fail(cudaError_t e) {
-  g_last_cuda_error = (int)e;
-  return VP_ERR_CUDA;
-}
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
@@ -360,7 +355,7 @@ const char* vp_status_string(int s) {
   }
 }
 
-int vp_get_last_cuda_error(void) { return g_last_cuda_error; }
+int vp_get_last_cuda_error(void) { return vp::last_cuda_error(); }
 
 vp_status vp_workspace_init(void* ws, size_t ws_bytes, void* stream) {
   if (!ws) return VP_ERR_INVALID_ARG;
