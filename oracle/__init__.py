@@ -20,6 +20,9 @@ the passage of the pages it follows:
   KV cache with online-softmax partitions and a sigmoid gate; ``attention_verify``; the GDN commit
   re-scan) and "Beating Splash ..." -- "What actually moved the needle" (double-buffered GDN state,
   re-scan of the committed rows; ``gdn_scan``, with the published gated delta rule).
+* "Speculative decoding" (mlx-dspark) -- "Lookup (no drafter)", "Lookup drafts" (the continuation of
+  an earlier match of the current text is a free draft; ``lookup_drafts``); the embedding gather
+  (``embed_nvfp4``) and the history append (``commit_append``) of a decode loop.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against page values,
 closed forms, library routines or brute force, except the 64-layer surrogate chain, whose
@@ -102,6 +105,10 @@ def lib():
             L.orc_gdn_scan.restype = ctypes.c_int
             L.orc_gdn_scan.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, P]
+            L.orc_embed_nvfp4.argtypes = [P, P, ctypes.c_double, P, ctypes.c_int, ctypes.c_int, P]
+            L.orc_lookup_drafts.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+            L.orc_commit_append.restype = ctypes.c_int
+            L.orc_commit_append.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
             L.orc_silu_mul.argtypes = [P, P, ctypes.c_int64, P]
             L.orc_rmsnorm.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P]
             L.orc_argmax.restype = ctypes.c_int64
@@ -281,6 +288,36 @@ def gdn_scan(state_in, q, k, v, alpha, beta, rows, want_out=True):
     if rc != 0:
         raise ValueError("orc_gdn_scan rejected its arguments")
     return so, out
+
+
+def embed_nvfp4(codes: np.ndarray, scales: np.ndarray, ts: float, tokens: np.ndarray) -> np.ndarray:
+    """Rows of a canonical NVFP4 table as bf16 bit patterns [M][K] (one rounding)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint8)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    K = codes.shape[1] * 2
+    out = np.zeros((tokens.size, K), np.uint16)
+    lib().orc_embed_nvfp4(_p(codes), _p(scales), float(ts), _p(tokens), tokens.size, K, _p(out))
+    return out
+
+
+def lookup_drafts(hist: np.ndarray, hist_len: np.ndarray, max_match: int = 8) -> np.ndarray:
+    """Anchor + 7 lookup drafts per lane (int32 [8 L]) from histories [L][cap]."""
+    hist = np.ascontiguousarray(hist, dtype=np.int32)
+    L, cap = hist.shape
+    hl = np.ascontiguousarray(hist_len, dtype=np.int32)
+    out = np.zeros(8 * L, np.int32)
+    lib().orc_lookup_drafts(_p(hist), _p(hl), L, cap, int(max_match), _p(out))
+    return out
+
+
+def commit_append(hist: np.ndarray, hist_len: np.ndarray, n_commit: np.ndarray, committed: np.ndarray) -> int:
+    """Appends each lane's committed tokens in place; returns 0, or -1 if a lane's history is full."""
+    assert hist.dtype == np.int32 and hist.flags.c_contiguous and hist_len.dtype == np.int32
+    L, cap = hist.shape
+    nc = np.ascontiguousarray(n_commit, dtype=np.int32)
+    cm = np.ascontiguousarray(committed, dtype=np.int32)
+    return int(lib().orc_commit_append(_p(hist), _p(hist_len), L, cap, _p(nc), _p(cm)))
 
 
 def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:

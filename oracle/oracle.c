@@ -584,6 +584,66 @@ int orc_gdn_scan(const double* state_in, double* state_out, const uint16_t* q, c
     return 0;
 }
 
+/* ------------------------------------------------------------------ decode loop pieces
+ *
+ * "lithos-metal ...", section "What one token costs the bus": the embedding is a gather of the
+ * 4-bit table (the pass streams everything else).  "Speculative decoding" (mlx-dspark), sections
+ * "Lookup (no drafter)" and "Lookup drafts": when the text being written already appeared earlier in
+ * the context, the continuation of that earlier match is a free draft.  "The megakernel is per
+ * layer, not per step": a round commits 1..8 tokens.  Readings: the embedding row is NVFP4 in the
+ * canonical layout, x = bf16(e2m1 * e4m3 * ts) rounded once; the lookup takes the earlier position p
+ * (continuation hist[p..]) whose preceding tokens match the history's last tokens for the most
+ * positions (up to max_match), the most recent among equals, a match of at least one token; the 7
+ * drafts are hist[p], hist[p+1], ... while p + j < T, then the last one repeated; with no match the
+ * drafts are the anchor repeated; the anchor is the last committed token hist[T-1]. */
+
+void orc_embed_nvfp4(const uint8_t* codes, const uint8_t* scales, double ts, const int32_t* tokens, int M, int K,
+                     uint16_t* out) {
+    for (int m = 0; m < M; ++m) {
+        const int64_t t = tokens[m];
+        for (int k = 0; k < K; ++k) {
+            int byte = codes[t * (K / 2) + k / 2];
+            int code = (k & 1) ? (byte >> 4) : (byte & 15);
+            out[(int64_t)m * K + k] = orc_bf16_round1(orc_e2m1(code) * orc_e4m3(scales[t * (K / 16) + k / 16]) * ts);
+        }
+    }
+}
+
+/* Lane l: history hist[l * cap .. + T), T = hist_len[l] >= 1; writes pending[8l .. 8l + 7]. */
+void orc_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int L, int cap, int max_match,
+                       int32_t* pending) {
+    for (int l = 0; l < L; ++l) {
+        const int32_t* h = hist + (int64_t)l * cap;
+        const int T = hist_len[l];
+        int best_p = -1, best_len = 0;
+        for (int p = 1; p < T; ++p) {  /* continuation starts at p; match hist[p-1-i] == hist[T-1-i] */
+            int len = 0;
+            while (len < max_match && p - 1 - len >= 0 && h[p - 1 - len] == h[T - 1 - len]) len++;
+            if (len >= 1 && len >= best_len) { best_len = len; best_p = p; }  /* ties: the later p */
+        }
+        const int32_t anchor = h[T - 1];
+        pending[8 * l] = anchor;
+        int32_t last = anchor;
+        for (int j = 0; j < 7; ++j) {
+            if (best_p >= 0 && best_p + j < T) last = h[best_p + j];
+            pending[8 * l + 1 + j] = last;
+        }
+    }
+}
+
+/* Appends committed[l][0 .. n_commit[l]) to lane l's history; returns -1 if one would not fit. */
+int orc_commit_append(int32_t* hist, int32_t* hist_len, int L, int cap, const int32_t* n_commit,
+                      const int32_t* committed) {
+    int rc = 0;
+    for (int l = 0; l < L; ++l) {
+        const int n = n_commit[l];
+        if (hist_len[l] + n > cap) { rc = -1; continue; }
+        for (int j = 0; j < n; ++j) hist[(int64_t)l * cap + hist_len[l] + j] = committed[8 * l + j];
+        hist_len[l] += n;
+    }
+    return rc;
+}
+
 /* Probability the draft gave token t (0 when t is not among its 16 candidates). */
 static double orc_q_of(const int32_t* dt, const double* dp, int32_t t) {
     for (int i = 0; i < 16; ++i) if (dt[i] == t) return dp[i];

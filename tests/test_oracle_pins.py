@@ -748,3 +748,66 @@ def test_gdn_scan_composes_row_by_row():
             sh = lambda x: np.roll(x, -j, axis=0)  # noqa: E731  (row j first)
             cur, _ = oracle.gdn_scan(cur, sh(q), sh(k), sh(v), sh(a), sh(b), [1])
         np.testing.assert_array_equal(full, cur)
+
+
+# ------------------------------------------------------------------ decode loop pieces
+
+def test_lookup_drafts_worked_examples():
+    """Hand-worked continuations: the longest earlier match of the history's suffix wins, the most
+    recent among equals; the continuation is copied while it lasts, then its last token repeats; no
+    match repeats the anchor."""
+    cases = [
+        ([5, 6, 7, 8, 5, 6], [6, 7, 8, 5, 6, 6, 6, 6]),
+        ([1, 2, 9, 2, 3, 1, 2], [2, 9, 2, 3, 1, 2, 2, 2]),  # "1 2" (length 2) beats "2" at position 4
+        ([4, 7, 4, 8, 4], [4, 8, 4, 4, 4, 4, 4, 4]),        # two length-1 matches: the later one
+        ([1, 2, 3], [3, 3, 3, 3, 3, 3, 3, 3]),              # no earlier occurrence of 3
+        ([9], [9] * 8),
+    ]
+    cap = 16
+    hist = np.zeros((len(cases), cap), np.int32)
+    hl = np.zeros(len(cases), np.int32)
+    for i, (h, _) in enumerate(cases):
+        hist[i, :len(h)] = h
+        hl[i] = len(h)
+    out = oracle.lookup_drafts(hist, hl).reshape(-1, 8)
+    for i, (_, want) in enumerate(cases):
+        assert out[i].tolist() == want, (i, out[i].tolist())
+
+
+def test_lookup_drafts_match_cap():
+    """With max_match = 1 only the last token is matched: the most recent earlier occurrence wins."""
+    hist = np.array([[1, 2, 9, 2, 3, 1, 2, 0, 0, 0]], np.int32)
+    out = oracle.lookup_drafts(hist, np.array([7], np.int32), max_match=1)
+    assert out.tolist() == [2, 3, 1, 2, 2, 2, 2, 2]
+
+
+def test_embed_nvfp4_is_the_rounded_table_row():
+    """Row t of the table equals column t of the NVFP4 linear with one-hot activations, rounded once
+    to bf16 (by the single-rounding conversion pinned above)."""
+    rng = np.random.default_rng(51)
+    V, K = 40, 256
+    codes = rng.integers(0, 256, (V, K // 2), dtype=np.uint8)
+    scales = rng.integers(0, 0x7F, (V, K // 16), dtype=np.uint8)
+    toks = np.array([0, 39, 7, 7, 21], np.int32)
+    ts = 0.6
+    emb = oracle.embed_nvfp4(codes, scales, ts, toks)
+    x = np.zeros((K, K), np.uint16)
+    x[np.arange(K), np.arange(K)] = 0x3F80
+    w = oracle.linear(oracle.NVFP4, x, codes, scales, ts, V, with_abs=False)  # w[k][t] = W[t][k]
+    # (values compared, -0 == +0: code 8 is E2M1's -0, which the row keeps and a sum does not)
+    assert np.array_equal(oracle.bf16_value(emb), oracle.bf16_value(oracle.bf16_round(w[:, toks].T.copy())))
+    # with ts = 1 every product is exact in bf16 (<= 5 significant bits): torch's conversion agrees
+    emb1 = oracle.embed_nvfp4(codes, scales, 1.0, toks)
+    w1 = oracle.linear(oracle.NVFP4, x, codes, scales, 1.0, V, with_abs=False)
+    ref1 = torch.from_numpy(w1[:, toks].T.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.bf16_value(emb1), oracle.bf16_value(ref1))
+
+
+def test_commit_append_and_full_history():
+    hist = np.zeros((2, 10), np.int32)
+    hl = np.array([3, 8], np.int32)
+    hist[0, :3] = [1, 2, 3]
+    nc = np.array([2, 3], np.int32)
+    cm = np.array([[7, 8, -1, -1, -1, -1, -1, -1], [4, 5, 6, -1, -1, -1, -1, -1]], np.int32)
+    assert oracle.commit_append(hist, hl, nc, cm) == -1  # lane 1 would overflow: left as it was
+    assert hist[0, :5].tolist() == [1, 2, 3, 7, 8] and hl.tolist() == [5, 8]
