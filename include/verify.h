@@ -37,6 +37,11 @@
  *                tokens matches a reference scan exactly); "lithos-metal ...", sections "What one
  *                token costs the bus" (fp32 state (v_heads, dk, dv) = 48 x 128 x 128 per layer) and
  *                "The megakernel is per layer, not per step" (the commit re-scan).
+ *   [LOOP]       "lithos-metal ...", section "What one token costs the bus" (the embedding is a gather
+ *                of the 4-bit table); "Speculative decoding" (mlx-dspark), sections "Lookup (no
+ *                drafter)" and "Lookup drafts" (the continuation of an earlier match of the current
+ *                text is a free draft); "Beating Splash on an M5 Max", section "The kernels were not
+ *                the gap" (host synchronisations per round were the cost).
  *   [SP-q4]      "144 tok/s needs 502 GB/s" (Splash), section "The engine hard-codes the model": the
  *                other engines' affine 4-bit format, per group of 64 inputs 32 bytes of codes plus
  *                a bf16 scale and a bf16 bias (nine bytes per sixteen weights); "Beating Splash on
@@ -347,6 +352,39 @@ int vp_pass_launch_count(const vp_model* model);
  * of multi-phase launches completed so far into *launches (a launch writes buffer launches % 2).
  * Synchronous (waits for the device). */
 vp_status vp_trace_read(int M, void* dst, size_t bytes, unsigned* launches);
+
+/* ------------------------------------------------------------------ device-resident decode loop [LOOP]
+ *
+ * Per lane l the decode state lives on the device: the token history hist[l][0 .. T_l) (int32
+ * [lanes][cap], T_l = hist_len[l]; the last token is the anchor, already committed) and an optional
+ * status word (set to VP_ERR_SHAPE by a kernel that met an out-of-range token or a full history; the
+ * work it concerns is skipped).  Every call below is asynchronous on `stream`, synchronises nothing
+ * and is CUDA-graph capturable. */
+
+/* x[m][k] = bf16(e2m1(code) * e4m3(scale) * ts) of row tokens[m] of an NVFP4 table in the canonical
+ * layout (codes [V][K/2], scales [V][K/16]), rounded once: the embedding gather.  x: bf16 [M][K].
+ * K % 16 == 0.  An out-of-range token gives a zero row and the status. */
+vp_status vp_embed_nvfp4(const void* codes, const void* scales, float ts, const int32_t* tokens, int M, int V, int K,
+                         void* x, int* status, void* stream);
+/* Lookup drafts: pending[8l] = the anchor hist[l][T-1]; pending[8l + 1 + j] = hist[l][p + j] while
+ * p + j < T, then the last copied token, where p (1 <= p < T) is the earlier position whose preceding
+ * tokens match the history's last tokens for the most positions (at most max_match, at least one),
+ * the latest p among equals; with no match every draft is the anchor. */
+vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
+                           int32_t* pending, int* status, void* stream);
+/* Appends committed[l][0 .. n_commit[l]) to lane l's history (a lane that would overflow cap is left
+ * as it is, with the status). */
+vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap, const int32_t* n_commit,
+                           const int32_t* committed, int* status, void* stream);
+/* `steps` rounds with no host in the loop: x0 = embed(pending) (the embedding table emb_codes /
+ * emb_scales / emb_ts, [vocab][hidden]); vp_verify_pass; append the committed tokens; lookup drafts
+ * into pending.  pending must hold the first round's anchor + drafts (e.g. from vp_lookup_drafts).
+ * x0: bf16 [8 lanes][hidden]; argmax, n_commit, committed, ws as for vp_verify_pass (the last round's
+ * values remain). */
+vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_codes, const void* emb_scales,
+                          float emb_ts, int vocab, int hidden, int32_t* hist, int32_t* hist_len, int cap,
+                          int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,
+                          int32_t* committed, void* ws, size_t ws_bytes, int* status, void* stream);
 
 #ifdef __cplusplus
 }

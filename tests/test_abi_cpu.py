@@ -157,6 +157,21 @@ def test_gdn_validation_without_gpu(V):
     assert call(si=F + 2) == V.VP_ERR_ALIGNMENT and call(a=F + 2) == V.VP_ERR_ALIGNMENT
 
 
+def test_loop_validation_without_gpu(V):
+    L = V.lib()
+    F = FAKE
+    assert L.vp_embed_nvfp4(None, F, 1.0, F, 8, 100, 256, F, None, None) == V.VP_ERR_INVALID_ARG
+    assert L.vp_embed_nvfp4(F, F, 1.0, F, 8, 100, 250, F, None, None) == V.VP_ERR_SHAPE
+    assert L.vp_embed_nvfp4(F, F, 1.0, F + 2, 8, 100, 256, F, None, None) == V.VP_ERR_ALIGNMENT
+    assert L.vp_lookup_drafts(F, F, 5, 100, 8, F, None, None) == V.VP_ERR_SHAPE
+    assert L.vp_lookup_drafts(F, F, 1, 100, 0, F, None, None) == V.VP_ERR_SHAPE
+    assert L.vp_lookup_drafts(F, None, 1, 100, 8, F, None, None) == V.VP_ERR_INVALID_ARG
+    assert L.vp_commit_append(F, F, 0, 100, F, F, None, None) == V.VP_ERR_SHAPE
+    assert L.vp_commit_append(F, F, 1, 100, F, F + 2, None, None) == V.VP_ERR_ALIGNMENT
+    assert L.vp_decode_steps(None, 1, F, F, 1.0, 100, 256, F, F, 100, 1, 8, F, F, F, F, F, F, 256, None,
+                             None) == V.VP_ERR_INVALID_ARG
+
+
 def test_head_and_argmax_validation_without_gpu(V):
     L = V.lib()
     ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)

@@ -26,7 +26,8 @@ EXPORTS = [
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
     "vp_linear_nvfp4_noalloc", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
-    "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan",
+    "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
+    "vp_commit_append", "vp_decode_steps",
 ]
 
 
@@ -88,6 +89,10 @@ def _load():
         "vp_sample_accept": (I, [P, I, I, F, I, F, P, P, P, P, P, P, P, S, P]),
         "vp_attention_verify": (I, [P, P, P, P, P, P, I, P, P, I, I, I, I, P, S, P]),
         "vp_gdn_scan": (I, [P, P, P, P, P, P, P, P, I, I, I, I, P, P]),
+        "vp_embed_nvfp4": (I, [P, P, F, P, I, I, I, P, P, P]),
+        "vp_lookup_drafts": (I, [P, P, I, I, I, P, P, P]),
+        "vp_commit_append": (I, [P, P, I, I, P, P, P, P]),
+        "vp_decode_steps": (I, [P, I, P, P, F, I, I, P, P, I, I, I, P, P, P, P, P, P, S, P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -224,6 +229,32 @@ def vp_gdn_scan(state_in, state_out, q, k, v, alpha, beta, rows, M: int, H: int,
                 stream=None):
     _check("vp_gdn_scan", _L.vp_gdn_scan(_ptr(state_in), _ptr(state_out), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
                                          _ptr(beta), _ptr(rows), M, H, dk, dv, _ptr(out), _stream(stream)))
+
+
+def vp_embed_nvfp4(codes, scales, ts: float, tokens, M: int, V: int, K: int, x, status=None, stream=None):
+    _check("vp_embed_nvfp4", _L.vp_embed_nvfp4(_ptr(codes), _ptr(scales), ts, _ptr(tokens), M, V, K, _ptr(x),
+                                               _ptr(status), _stream(stream)))
+
+
+def vp_lookup_drafts(hist, hist_len, lanes: int, cap: int, max_match: int, pending, status=None, stream=None):
+    _check("vp_lookup_drafts", _L.vp_lookup_drafts(_ptr(hist), _ptr(hist_len), lanes, cap, max_match, _ptr(pending),
+                                                   _ptr(status), _stream(stream)))
+
+
+def vp_commit_append(hist, hist_len, lanes: int, cap: int, n_commit, committed, status=None, stream=None):
+    _check("vp_commit_append", _L.vp_commit_append(_ptr(hist), _ptr(hist_len), lanes, cap, _ptr(n_commit),
+                                                   _ptr(committed), _ptr(status), _stream(stream)))
+
+
+def vp_decode_steps(model: "vp_model", steps: int, emb_codes, emb_scales, emb_ts: float, vocab: int, hidden: int,
+                    hist, hist_len, cap: int, lanes: int, max_match: int, pending, x0, argmax, n_commit, committed,
+                    ws, status=None, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_decode_steps",
+           _L.vp_decode_steps(model.handle, steps, _ptr(emb_codes), _ptr(emb_scales), emb_ts, vocab, hidden,
+                              _ptr(hist), _ptr(hist_len), cap, lanes, max_match, _ptr(pending), _ptr(x0),
+                              _ptr(argmax), _ptr(n_commit), _ptr(committed), _ptr(ws), wb, _ptr(status),
+                              _stream(stream)))
 
 
 def vp_workspace_init(ws, stream=None, ws_bytes=None):

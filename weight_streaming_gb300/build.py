@@ -1,9 +1,9 @@
 """Builds libverify.so (the C-ABI library) in-tree with nvcc for sm_103a.
 
-Eight translation units are compiled in parallel (host API + packers, the streaming executor for
+Nine translation units are compiled in parallel (host API + packers, the streaming executor for
 8/16 token columns, the executor for 24/32 token columns, the executor with the Q4 unit, the
-sampled acceptance, the verify attention, the Gated DeltaNet scan, the error bookkeeping) and
-linked against the shared CUDA runtime.
+sampled acceptance, the verify attention, the Gated DeltaNet scan, the decode loop, the error
+bookkeeping) and linked against the shared CUDA runtime.
 """
 from __future__ import annotations
 
@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libverify.so")
 BUILD_TRACE = os.path.join(PKG, "_build_trace")
 LIB_TRACE = os.path.join(PKG, "libverify_trace.so")
 SOURCES = ["api.cu", "exec_nt12.cu", "exec_nt34.cu", "exec_q4.cu", "sample.cu", "attention.cu", "gdn.cu",
-           "errors.cu"]
+           "loop.cu", "errors.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 
