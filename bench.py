@@ -9,7 +9,7 @@ through the C ABI with host buffers, and the fp64 oracle on the host cores as th
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Multi-GPU: the pass does not shard in this build (replicas only): under torchrun every rank runs its
+Multi-GPU: the library runs the pass on one GPU (replicas only): under torchrun every rank runs its
 own replica on its own GPU; value = total bytes streamed by all ranks / the slowest rank's time.
 """
 from __future__ import annotations
