@@ -62,6 +62,7 @@ struct PhaseSpec {
   float s0 = 1.0f, s1 = 1.0f;
   int rows0 = 0, rows1 = 0, K = 0;
   int epi = kEpiF32, x_src = kBufX, x_ld = 0, x_rms = 0, out = kBufY, out_ld = 0, out_cols = 0, trace_slot = -1;
+  int ss = 0;
 };
 
 Phase make_phase(const PhaseSpec& s, int NT) {
@@ -91,6 +92,7 @@ Phase make_phase(const PhaseSpec& s, int NT) {
   ph.epi = (int8_t)s.epi;
   ph.x_src = (int8_t)s.x_src;
   ph.x_rms = (int8_t)s.x_rms;
+  ph.ss = (int8_t)s.ss;
   ph.out = (int8_t)s.out;
   ph.x_ld = s.x_ld;
   ph.out_ld = s.out_ld;
@@ -737,6 +739,7 @@ void build_pass(vp_model* md, int NT) {
     in.x_src = kBufH;
     in.x_ld = H;
     in.x_rms = 1;
+    in.ss = l > 0 ? kSsRead : 0;  // layer 0 reads x0, which no phase produced
     in.out = kBufZ;
     in.out_ld = d.k_out;
     in.out_cols = d.k_out;
@@ -752,6 +755,7 @@ void build_pass(vp_model* md, int NT) {
     o.x_ld = d.k_out;
     o.out = kBufH;
     o.out_ld = H;
+    o.ss = kSsWrite;
     o.trace_slot = 2 * l;
     out.push_back(make_phase(o, NT));
     PhaseSpec gu;  // MLP gate + up, interleaved strips -> a = bf16(silu(gate) * up)
@@ -767,6 +771,7 @@ void build_pass(vp_model* md, int NT) {
     gu.x_src = kBufH;
     gu.x_ld = H;
     gu.x_rms = 1;
+    gu.ss = kSsRead;
     gu.out = kBufA;
     gu.out_ld = I;
     out.push_back(make_phase(gu, NT));
@@ -781,6 +786,7 @@ void build_pass(vp_model* md, int NT) {
     dn.x_ld = I;
     dn.out = kBufH;
     dn.out_ld = H;
+    dn.ss = kSsWrite;
     dn.trace_slot = 2 * l + 1;
     out.push_back(make_phase(dn, NT));
   }
@@ -794,6 +800,7 @@ void build_pass(vp_model* md, int NT) {
   hd.x_src = kBufH;
   hd.x_ld = H;
   hd.x_rms = 1;
+  hd.ss = kSsRead;
   hd.out = kBufLogits;
   hd.out_ld = md->head.vocab;
   out.push_back(make_phase(hd, NT));
@@ -803,7 +810,7 @@ void build_pass(vp_model* md, int NT) {
 
 struct PassWs {
   WsLayout L;
-  size_t h, z, a, total;
+  size_t h, z, a, rss, total;
 };
 
 PassWs pass_ws(const vp_model* md, int M) {
@@ -817,6 +824,8 @@ PassWs pass_ws(const vp_model* md, int M) {
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->zmax, 256);
   w.a = off;
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->inter, 256);
+  w.rss = off;
+  off = align_up(off + sizeof(float) * (size_t)M * (md->hidden / kRowBlock), 256);
   w.total = off;
   return w;
 }
@@ -906,6 +915,8 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
   io.buf[kBufH] = b + w.h;
   io.buf[kBufZ] = b + w.z;
   io.buf[kBufA] = b + w.a;
+  io.rss = reinterpret_cast<float*>(b + w.rss);
+  io.rss_ld = md->hidden / kRowBlock;
   io.buf[kBufLogits] = logits;
   io.buf[kBufTrace] = trace;
   io.trace_stride = (size_t)M * md->hidden;
@@ -936,12 +947,15 @@ vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, 
     if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
     if (ph.trace_slot >= 0) ph.trace_slot -= block_begin;
   }
+  phases[0].ss &= ~kSsRead;  // the caller's h: no producer left its row-block sums
   const PassWs w = pass_ws(md, M);
   uint8_t* b = (uint8_t*)ws;
   Io io = make_io(ws, w.L);
   io.buf[kBufH] = h;
   io.buf[kBufZ] = b + w.z;
   io.buf[kBufA] = b + w.a;
+  io.rss = reinterpret_cast<float*>(b + w.rss);
+  io.rss_ld = md->hidden / kRowBlock;
   io.buf[kBufTrace] = trace;
   io.trace_stride = (size_t)M * md->hidden;
   return run_phases(phases, M, md->eps, io, sms, (cudaStream_t)stream);

@@ -287,11 +287,18 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
   float inv = 1.0f;
   int e;
   if (rms) {
-    if (Ks < ph.K && active)
+    bool from_rss = false;
+    if constexpr (NT > 1) from_rss = (ph.ss & kSsRead) && Ks < ph.K && io.rss;
+    if (from_rss) {  // the row's statistic from the producer's row-block sums, in a fixed order
+      stat = 0.0f;
+      if (active)
+        for (int q = i; q < (ph.K >> 4); q += T) stat += __ldcg(io.rss + (size_t)n * io.rss_ld + q);
+    } else if (Ks < ph.K && active) {
       for (int q = i; q < (ph.K >> 3); q += T) {
         const int k = 8 * q;
         if (k < kbase || k >= kbase + Ks) stat += sumsq8(ldcg128(row + k));
       }
+    }
     const float tot = row_reduce(stat, T, false, sm.red);
     inv = 1.0f / sqrtf(tot / (float)ph.K + prog.eps);
     e = exp_of_max(1.01f * sqrtf((float)ph.K));
@@ -505,6 +512,9 @@ __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const flo
   const bool seg1 = rb >= ph.rb1;
   const float s = seg1 ? ph.s1 : ph.s0;
   const int nb = (seg1 ? rb - ph.rb1 : rb) * kRowBlock + g;
+  float sq[NT][2];  // kSsWrite: this lane's squares of the stored values, per token
+#pragma unroll
+  for (int j = 0; j < NT; ++j) sq[j][0] = sq[j][1] = 0.0f;
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -527,6 +537,10 @@ __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const flo
             uint16_t* hp = static_cast<uint16_t*>(io.buf[ph.out]);
             const uint16_t nv = bf16_bits(bf16_bits_to_float(hold[j][2 * r + h]) + val);
             hp[o] = nv;
+            if constexpr (NT > 1) {
+              const float f = bf16_bits_to_float(nv);
+              sq[j][h] = fmaf(f, f, sq[j][h]);
+            }
             if (ph.trace_slot >= 0 && io.buf[kBufTrace])
               static_cast<uint16_t*>(io.buf[kBufTrace])[(size_t)ph.trace_slot * io.trace_stride + o] = nv;
             break;
@@ -545,6 +559,21 @@ __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const flo
         }
       }
     }
+  if constexpr (NT > 1) {
+    if (ph.epi == kEpiResid && (ph.ss & kSsWrite)) {  // the row block's 16 rows: lanes g = 0..7 (xor 4, 8, 16)
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float v = sq[j][h];
+          v += __shfl_xor_sync(0xffffffffu, v, 4);
+          v += __shfl_xor_sync(0xffffffffu, v, 8);
+          v += __shfl_xor_sync(0xffffffffu, v, 16);
+          const int t = 8 * j + 2 * c + h;
+          if (g == 0 && t < M) io.rss[(size_t)t * io.rss_ld + (seg1 ? rb - ph.rb1 : rb)] = v;
+        }
+    }
+  }
 }
 
 // Finishes row block rb of the warp's range: directly when the warp computed all of it, else

@@ -77,6 +77,11 @@ enum Epi : int {
   kEpiResid = 3,  // h[m][n] = bf16(h[m][n] + s * acc) (and the trace copy)
   kEpiHead = 4,   // logits -> per-row argmax -> greedy acceptance
 };
+// Row-block sums of squares of the residual stream: a kEpiResid phase with kSsWrite stores, per token
+// and 16-column row block of its output, the sum of the squares of the stored bf16 values; an RMSNorm
+// phase with kSsRead whose K slice is narrower than the row takes the row's statistic from them (a
+// fixed-order sum, the same in every CTA) instead of loading the whole row.  Used at 2+ n-tiles.
+enum : int { kSsRead = 1, kSsWrite = 2 };
 // Buffers a phase reads or writes, resolved per launch through Io::buf.
 enum Buf : int { kBufX = 0, kBufY, kBufH, kBufZ, kBufA, kBufLogits, kBufTrace, kNumBufs };
 
@@ -89,7 +94,7 @@ struct Phase {
   int RB, rb1;      // virtual row blocks; first row block of w1 (plain; RB if none)
   int cmax;         // fixup slots per (row block, K slice)
   int8_t fmt, layout, epi, ks;  // ks: K slices
-  int8_t x_src, x_rms, out, pad;
+  int8_t x_src, x_rms, out, ss;  // ss: kSsRead | kSsWrite (row-block sums of squares, see Io::rss)
   int x_ld, out_ld, out_cols, trace_slot;
 };
 
@@ -115,6 +120,8 @@ struct Io {
   float* head_aux;     // [kMaxGrid][kMaxM][2]
   unsigned* rb_cnt;    // [max RB]
   float* partials;     // fixup slots: [RB][ks][cmax][32 lanes][4 NT (plain) or 8 NT (interleaved)]
+  float* rss;          // row-block sums of squares [kMaxM][rss_ld] (or null)
+  int rss_ld;
 };
 
 // ---------------------------------------------------------------- workspace carving
