@@ -39,7 +39,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample", "attn",
-                             "gdn"],
+                             "gdn", "decode"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--ctx", type=int, default=32768, help="context length per lane for --kernel attn")
@@ -348,12 +348,110 @@ def run_gdn(args):
                       "frac_of_measured_copy": (nbytes / t / 1e9 / peak) if peak else None}), flush=True)
 
 
+def run_decode(args):
+    """The device-resident decode loop (vp_decode_steps: embedding gather, the 64-layer verify pass,
+    history append, lookup drafts) on the full synthetic model, --M rows (M / 8 lanes). Times R rounds
+    captured in one CUDA graph and replayed, the same rounds enqueued one at a time with a host
+    synchronisation and a read of n_commit after each (a host-driven loop), and the pass alone; prints
+    one JSON line with the time per round of each and the tokens committed per round."""
+    import numpy as np
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    from weight_streaming_gb300.model import Geometry, SyntheticModel
+
+    geom = Geometry(n_layers=args.layers)
+    M, R, T0, cap, mm, ts = args.M, 8, 512, 8192, 8, 1.0
+    L = M // 8
+    sm = SyntheticModel(geom, seed=0)
+    ec = torch.empty((geom.vocab, geom.hidden // 2), dtype=torch.uint8, device="cuda")
+    es = torch.empty((geom.vocab, geom.hidden // 16), dtype=torch.uint8, device="cuda")
+    synth.gpu_uniform_bytes(ec, 0, synth.stream_id(synth.HEAD_LAYER + 1, synth.T_HEAD_C))
+    synth.gpu_scale_codes(es, 0, synth.stream_id(synth.HEAD_LAYER + 1, synth.T_HEAD_S))
+    rng = np.random.default_rng(5)
+    hist0 = np.zeros((L, cap), np.int32)
+    for l in range(L):  # a text over a small alphabet with a copied span, so that lookup finds matches
+        base = rng.integers(0, 2000, T0)
+        base[T0 // 2:] = base[:T0 // 2]
+        hist0[l, :T0] = base
+    hl0 = np.full(L, T0, np.int32)
+    ws = sm.workspace(M)
+    x0 = torch.empty((M, geom.hidden), dtype=torch.bfloat16, device="cuda")
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    nc = torch.empty(L, dtype=torch.int32, device="cuda")
+    cm = torch.empty((L, 8), dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pend = torch.empty(M, dtype=torch.int32, device="cuda")
+
+    def state():
+        return torch.from_numpy(hist0).cuda(), torch.from_numpy(hl0).cuda()
+
+    def rounds(h, hl, n, s):
+        V.vp_decode_steps(sm.model, n, ec, es, ts, geom.vocab, geom.hidden, h, hl, cap, L, mm, pend, x0, am, nc,
+                          cm, ws, st, stream=s)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        # R rounds in one graph, replayed
+        h, hl = state()
+        V.vp_lookup_drafts(h, hl, L, cap, mm, pend, st, stream=s)
+        rounds(h, hl, 1, s)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            rounds(h, hl, R, s)
+        for _ in range(args.warmup):
+            g.replay()
+        s.synchronize()
+        before = int(hl.sum().item())
+        e0, e1 = ev(), ev()
+        e0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(s)
+        s.synchronize()
+        t_graph = e0.elapsed_time(e1) / 1e3 / (args.steps * R)
+        tok_graph = (int(hl.sum().item()) - before) / (args.steps * R * L)
+        # the same rounds, one call per round, the host waiting for each round's n_commit
+        h, hl = state()
+        V.vp_lookup_drafts(h, hl, L, cap, mm, pend, st, stream=s)
+        nch = torch.empty(L, dtype=torch.int32).pin_memory()
+        for _ in range(args.warmup):
+            rounds(h, hl, 1, s)
+            nch.copy_(nc, non_blocking=True)
+            s.synchronize()
+        e0, e1 = ev(), ev()
+        e0.record(s)
+        for _ in range(args.steps * R):
+            rounds(h, hl, 1, s)
+            nch.copy_(nc, non_blocking=True)
+            s.synchronize()
+        e1.record(s)
+        s.synchronize()
+        t_host = e0.elapsed_time(e1) / 1e3 / (args.steps * R)
+    assert int(st.item()) == 0 and V.vp_read_status(ws) == V.VP_OK
+    t_pass = graph_time(lambda: sm.run(x0, pend, am, nc, cm, ws), args.steps, args.warmup)
+    launches = sm.launch_count() + 3
+    print(json.dumps({"kernel": "decode", "M": M, "lanes": L, "layers": args.layers, "rounds_per_graph": R,
+                      "ms_per_round_graph": t_graph * 1e3, "ms_per_round_host_sync": t_host * 1e3,
+                      "ms_per_pass_alone": t_pass * 1e3, "loop_overhead_us_graph": (t_graph - t_pass) * 1e6,
+                      "loop_overhead_us_host_sync": (t_host - t_pass) * 1e6,
+                      "tokens_committed_per_lane_round": tok_graph, "launches_per_round": launches,
+                      "history_tokens_at_start": T0, "max_match": mm}), flush=True)
+
+
 def run_kernel(args):
     """One GEMM of the pass alone through the C ABI, rotating over 4 weight copies (> L2) so every
     launch streams from DRAM; prints one JSON line with the average launch time and GB/s."""
     import torch
     if args.kernel == "gdn":
         run_gdn(args)
+        return
+    if args.kernel == "decode":
+        run_decode(args)
         return
     if args.kernel == "sample":
         run_sample(args)
