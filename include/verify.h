@@ -380,7 +380,9 @@ vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap,
  * emb_scales / emb_ts, [vocab][hidden]); vp_verify_pass; append the committed tokens; lookup drafts
  * into pending.  pending must hold the first round's anchor + drafts (e.g. from vp_lookup_drafts).
  * x0: bf16 [8 lanes][hidden]; argmax, n_commit, committed, ws as for vp_verify_pass (the last round's
- * values remain). */
+ * values remain).  hidden must be the model's hidden size (x0 is written with it and read by the pass
+ * with the model's; the library cannot check the caller's buffer).  All arguments are checked before
+ * the first launch: a rejected call enqueues nothing (steps == 0: the checks alone). */
 vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_codes, const void* emb_scales,
                           float emb_ts, int vocab, int hidden, int32_t* hist, int32_t* hist_len, int cap,
                           int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,

@@ -172,6 +172,28 @@ def test_loop_validation_without_gpu(V):
                              None) == V.VP_ERR_INVALID_ARG
 
 
+def test_decode_steps_checks_everything_before_launching(V):
+    """vp_decode_steps rejects a bad argument of any of its four steps before its first launch (every
+    call below either fails a check or has steps == 0, so nothing is enqueued)."""
+    L = V.lib()
+    F = FAKE
+    m = V.vp_model(256, 512, 1e-6, [_layer(V)], V.vp_head_desc(FAKE, 1.0, 2048))
+    need = V.vp_pass_workspace_bytes(m, 8)
+
+    def call(steps=1, vocab=2048, hidden=256, cap=100, lanes=1, mm=8, x0=F, ws=F, ws_bytes=need, hist=F):
+        return L.vp_decode_steps(m.handle, steps, F, F, 1.0, vocab, hidden, hist, F, cap, lanes, mm, F, x0, F, F, F, ws,
+                                 ws_bytes, None, None)
+    assert call(steps=0) == V.VP_OK  # the checks alone
+    assert call(steps=-1) == V.VP_ERR_SHAPE and call(lanes=5) == V.VP_ERR_SHAPE
+    assert call(cap=0) == V.VP_ERR_SHAPE and call(cap=1 << 24) == V.VP_ERR_SHAPE
+    assert call(mm=0) == V.VP_ERR_SHAPE and call(mm=128) == V.VP_ERR_SHAPE
+    assert call(vocab=0) == V.VP_ERR_SHAPE and call(hidden=250) == V.VP_ERR_SHAPE
+    assert call(x0=F + 8) == V.VP_ERR_ALIGNMENT and call(hist=F + 2) == V.VP_ERR_ALIGNMENT
+    assert call(ws=F + 128) == V.VP_ERR_ALIGNMENT
+    assert call(ws_bytes=need - 1) == V.VP_ERR_WORKSPACE
+    m.close()
+
+
 def test_head_and_argmax_validation_without_gpu(V):
     L = V.lib()
     ws = V.vp_workspace_bytes(V.VP_OP_HEAD, 8, 1024, 512)

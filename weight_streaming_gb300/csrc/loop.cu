@@ -162,6 +162,17 @@ vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_code
     return VP_ERR_INVALID_ARG;
   if (steps < 0 || lanes < 1 || lanes > kMaxM / 8) return VP_ERR_SHAPE;
   const int M = 8 * lanes;
+  // Every argument of the four steps is checked before the first launch, so a bad call enqueues
+  // nothing.  (The pass's own per-phase checks still run inside vp_verify_pass.)
+  if (vocab < 1 || hidden < 16 || hidden % 16 || (long long)vocab * hidden >= (1LL << 40) || cap < 1 ||
+      cap >= (1 << 24) || max_match < 1 || max_match > 127)
+    return VP_ERR_SHAPE;
+  if (!al(hist, 4) || !al(hist_len, 4) || !al(pending, 4) || !al(x0, 16) || !al(argmax, 4) || !al(n_commit, 4) ||
+      !al(committed, 4) || !al(ws, 256) || (status && !al(status, 4)))
+    return VP_ERR_ALIGNMENT;
+  const size_t need = vp_pass_workspace_bytes(model, M);
+  if (need == 0) return VP_ERR_SHAPE;
+  if (ws_bytes < need) return VP_ERR_WORKSPACE;
   for (int s = 0; s < steps; ++s) {
     vp_status st = vp_embed_nvfp4(emb_codes, emb_scales, emb_ts, pending, M, vocab, hidden, x0, status, stream);
     if (st != VP_OK) return st;
