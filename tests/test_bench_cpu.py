@@ -51,3 +51,37 @@ def test_aggregate_single_rank():
     import bench
     v, t = bench.aggregate(17555292160, [0.0075])
     assert t == 0.0075 and v == pytest.approx(17555292160 / 0.0075 / 1e9)
+
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _bench(args, env_extra=None):
+    import subprocess
+    import sys
+    env = dict(os.environ, **(env_extra or {}))
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT, env=env,
+                          capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """The oracle arm (bench.py --impl reference) prints one JSON line with the GPU arm's metric and
+    unit, the cpu_baseline it measured and an e2e object, on the host cores alone."""
+    import json
+    r = _bench(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    import bench
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT and d["impl"] == "reference"
+    assert d["value"] > 0 and d["steps"] == 1 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun only rank 0 runs the oracle arm; the others exit 0 without output."""
+    r = _bench(["--impl", "reference", "--steps", "1", "--warmup", "0"], {"RANK": "1", "WORLD_SIZE": "2"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
