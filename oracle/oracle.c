@@ -29,12 +29,23 @@
  *  - Argmax: NaN is treated as -inf; -0 == +0; the lowest index among equal maxima wins.
  *  - Q4: unsigned codes, w = scale * q + bias, groups of 64 along K, low nibble first.
  *  - The verify-pass surrogate (mixer cores replaced by slices) -- see orc_verify_pass().
+ *  - Sampled acceptance: candidates ordered by logit, ties to the lower index; top_p keeps the
+ *    shortest prefix whose mass reaches top_p; a draw takes the first i whose cumulative weight
+ *    exceeds u times the total; a zero residual draws from the target -- see orc_sample_accept().
+ *  - Verify attention: scores q.k / sqrt(D); row j of a lane sees cache positions 0 .. ctx + j after
+ *    the lane's 8 new keys are appended; q head h reads kv head h / (Hq / Hkv) -- see
+ *    orc_attention_verify().
+ *  - Gated DeltaNet: the published gated delta rule; the re-scan count is the lane's n_commit --
+ *    see orc_gdn_scan().
+ *  - Lookup drafts: the longest match of the history's suffix (at most max_match), the latest
+ *    position among equals, its continuation then its last token repeated -- see orc_lookup_drafts().
  *
- * Pins: every building block (formats, linear, bf16 rounding, SiLU*up, RMSNorm, argmax, acceptance,
- * byte table) is pinned by the tests against page values, closed forms, library routines or brute
- * force.  orc_verify_pass is pinned through its parts and an independent composition on a tiny model;
- * the long (64-layer) chain as a whole is parity unpinned -- end-to-end comparisons against it check
- * only decisions that are unique and report the drift.
+ * Pins: every building block (formats, linear, Q4, bf16 rounding, SiLU*up, RMSNorm, argmax,
+ * acceptance, byte tables, the sampled-acceptance distribution, attention, the delta-rule scan,
+ * the decode-loop pieces) is pinned by the tests against page values, closed forms, library
+ * routines or brute force.  orc_verify_pass is pinned through its parts and an independent
+ * composition on a tiny model; the long (64-layer) chain as a whole is parity unpinned -- end-to-end
+ * comparisons against it check only decisions that are unique and report the drift.
  *
  * Everything is computed in fp64 from the plain definitions, with no blocking or reordering:
  * w[n][k] = e2m1(code) * e4m3(scale) * ts, y[m][n] = sum_k x[m][k] * w[n][k].
