@@ -737,6 +737,24 @@ def test_gdn_closed_forms():
     np.testing.assert_allclose(so[0], expect, rtol=0, atol=1e-15)
 
 
+def test_gdn_retrieves_the_written_value():
+    """The delta rule's defining property: after one step with a unit-norm key k, the state maps k to
+    (1 - beta) * alpha * S k + beta * v (with beta = 1 the memory returns exactly v for k), and the
+    output for q = k is that vector.  The key (0.5 on four coordinates) has k^T k = 1 exactly."""
+    rng = np.random.default_rng(44)
+    st, q, k, v, a, b = gdn_case(rng)
+    ku = np.zeros_like(k)
+    ku[:, :, [1, 4, 9, 14]] = 0x3F00  # bf16 0.5
+    kval = bf16_vals_torch(ku[0, 0])
+    assert float(kval @ kval) == 1.0
+    for beta in (b, np.ones_like(b)):
+        so, out = oracle.gdn_scan(st, ku, ku, v, a, beta, [1])
+        for h in range(st.shape[1]):
+            want = (1 - beta[0, h]) * a[0, h] * (st[0, h] @ kval) + beta[0, h] * bf16_vals_torch(v[0, h])
+            np.testing.assert_allclose(so[0, h] @ kval, want, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(out[0, h], want, rtol=1e-12, atol=1e-13)
+
+
 def test_gdn_scan_composes_row_by_row():
     """The re-scan invariant: scanning n rows at once equals n one-row scans in sequence."""
     rng = np.random.default_rng(43)
