@@ -593,10 +593,11 @@ def main():
         t = time_graph(g, s, max(3, args.steps // 2), 3)
         steps_m = max(3, args.steps // 2)
         gbs = pass_bytes * steps_m / t / 1e9
-        also[f"M{M}"] = {"gbps": gbs, "ms_per_pass": 1e3 * t / steps_m,
+        also[f"M{M}"] = {"gbps": gbs, "ms_per_pass": 1e3 * t / steps_m, "passes_per_s": steps_m / t,
                          "implied_tok_s": (M // 8) * 4.8 / (t / steps_m)}
         del g
-    also["M8"] = {"gbps": value / world, "ms_per_pass": ms8, "implied_tok_s": 4.8 / (ms8 / 1e3)}
+    also["M8"] = {"gbps": value / world, "ms_per_pass": ms8, "passes_per_s": 1e3 / ms8,
+                  "implied_tok_s": 4.8 / (ms8 / 1e3)}
 
     # ---- dominant kernel: the pass is two launches of one persistent kernel (exec_kernel<1, 0> at M = 8,
     # 4 phases per layer + the head); its algorithmic bytes are the pass's weight bytes, its duration
