@@ -25,6 +25,45 @@ import sys
 import numpy as np
 
 KINDS = ("mixer in", "mixer out", "gate+up", "down")
+COLS = ("staging", "stream med", "stream max", "fixup tail", "release", "phase")
+
+
+def phase_stats(T: np.ndarray, last_of_launch: set) -> dict:
+    """Per phase kind, the list of per-phase figures (ns) from stamps T[phase][CTA][slot]: slot 0
+    phase start, 1 staging done, 2..17 each warp's units done, 18..33 each warp's fixups done, 34
+    barrier exit.  The last phase of a launch has no barrier after it (no release / phase figure)."""
+    n_ph = T.shape[0]
+    stats = {}
+    for gp in range(n_ph):
+        kind = "head" if gp == n_ph - 1 else KINDS[gp % 4]
+        S = T[gp]
+        t0, t1, t2, t3, t4 = S[:, 0], S[:, 1], S[:, 2:18], S[:, 18:34], S[:, 34]
+        d = {"staging": (t1 - t0).max(), "stream med": np.median(t2 - t1[:, None]),
+             "stream max": (t2 - t1[:, None]).max(), "fixup tail": t3.max() - t2.max()}
+        if gp not in last_of_launch:
+            d["release"] = t4.min() - t3.max()
+            d["phase"] = T[gp + 1][:, 0].min() - t0.min()
+        stats.setdefault(kind, []).append(d)
+    return stats
+
+
+def report(T: np.ndarray, last_of_launch: set, layers: int, M: int) -> list:
+    """The printed table: the mean of each figure per phase kind, in us."""
+    stats = phase_stats(T, last_of_launch)
+    lines = [f"verify pass, {layers} layers, M = {M}: mean per phase kind (us)",
+             f"{'phase kind':12s} {'n':>4s} " + " ".join(f"{c:>11s}" for c in COLS)]
+    for kind in KINDS + ("head",):
+        lst = stats.get(kind, [])
+        if not lst:
+            continue
+        vals = []
+        for c in COLS:
+            v = [x[c] for x in lst if c in x]
+            vals.append(f"{np.mean(v) / 1e3:11.2f}" if v else f"{'-':>11s}")
+        lines.append(f"{kind:12s} {len(lst):4d} " + " ".join(vals))
+    total = (T[-1][:, 18:34].max() - T[0][:, 0].min()) / 1e3
+    lines.append(f"first phase start -> last phase done: {total:.1f} us")
+    return lines
 
 
 def main(argv=None) -> None:
@@ -82,32 +121,7 @@ def main(argv=None) -> None:
     if args.save:
         np.save(args.save, T)
 
-    stats = {}
-    for gp in range(n_ph):
-        kind = "head" if gp == n_ph - 1 else KINDS[gp % 4]
-        S = T[gp]
-        t0, t1, t2, t3, t4 = S[:, 0], S[:, 1], S[:, 2:18], S[:, 18:34], S[:, 34]
-        d = {"staging": (t1 - t0).max(), "stream med": np.median(t2 - t1[:, None]),
-             "stream max": (t2 - t1[:, None]).max(), "fixup tail": t3.max() - t2.max()}
-        if gp not in last_of_launch:  # the last phase of a launch has no barrier after it
-            d["release"] = t4.min() - t3.max()
-            d["phase"] = T[gp + 1][:, 0].min() - t0.min()
-        stats.setdefault(kind, []).append(d)
-    cols = ["staging", "stream med", "stream max", "fixup tail", "release", "phase"]
-    print(f"verify pass, {args.layers} layers, M = {M}: mean per phase kind (us)")
-    print(f"{'phase kind':12s} {'n':>4s} " + " ".join(f"{c:>11s}" for c in cols))
-    for kind in KINDS + ("head",):
-        lst = stats.get(kind, [])
-        if not lst:
-            continue
-        vals = []
-        for c in cols:
-            v = [x[c] for x in lst if c in x]
-            vals.append(f"{np.mean(v) / 1e3:11.2f}" if v else f"{'-':>11s}")
-        print(f"{kind:12s} {len(lst):4d} " + " ".join(vals))
-    total = (T[-1][:, 18:34].max() - T[0][:, 0].min()) / 1e3
-    print(f"first phase start -> last phase done: {total:.1f} us")
-
+    print("\n".join(report(T, last_of_launch, args.layers, M)))
 
 if __name__ == "__main__":
     main()
