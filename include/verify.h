@@ -263,7 +263,8 @@ vp_status vp_attention_verify(const void* q, const void* k_new, const void* v_ne
  * v: bf16 [M][H][dv]; alpha, beta: fp32 [M][H] (after the layer's gates; q, k, v after its short
  * convolution, activation and normalisation -- producer steps).  Verify: rows = 8 from A to B;
  * commit after a partial accept: rows = n_commit from A to B again -- the same kernel, so the
- * re-scan's state equals the verify scan's state after those rows bit for bit.  dk = dv = 128.
+ * re-scan's state equals the verify scan's state after those rows bit for bit.  dk = dv = 128,
+ * H 1..4096.
  * One launch, no workspace. */
 vp_status vp_gdn_scan(const float* state_in, float* state_out, const void* q, const void* k, const void* v,
                       const float* alpha, const float* beta, const int32_t* rows, int M, int H, int dk, int dv,
@@ -363,17 +364,20 @@ vp_status vp_trace_read(int M, void* dst, size_t bytes, unsigned* launches);
 
 /* x[m][k] = bf16(e2m1(code) * e4m3(scale) * ts) of row tokens[m] of an NVFP4 table in the canonical
  * layout (codes [V][K/2], scales [V][K/16]), rounded once: the embedding gather.  x: bf16 [M][K].
- * K % 16 == 0.  An out-of-range token gives a zero row and the status. */
+ * K % 16 == 0, V * K < 2^40.  An out-of-range token gives a zero row and the status. */
 vp_status vp_embed_nvfp4(const void* codes, const void* scales, float ts, const int32_t* tokens, int M, int V, int K,
                          void* x, int* status, void* stream);
 /* Lookup drafts: pending[8l] = the anchor hist[l][T-1]; pending[8l + 1 + j] = hist[l][p + j] while
  * p + j < T, then the last copied token, where p (1 <= p < T) is the earlier position whose preceding
  * tokens match the history's last tokens for the most positions (at most max_match, at least one),
- * the latest p among equals; with no match every draft is the anchor. */
+ * the latest p among equals; with no match every draft is the anchor.  lanes 1..4, cap < 2^24,
+ * max_match 1..127; pending: int32 [8 lanes].  A lane with hist_len outside 1..cap gets all 8
+ * pending entries 0, and the status. */
 vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
                            int32_t* pending, int* status, void* stream);
-/* Appends committed[l][0 .. n_commit[l]) to lane l's history (a lane that would overflow cap is left
- * as it is, with the status). */
+/* Appends committed[l][0 .. n_commit[l]) to lane l's history (a lane that would overflow cap, or whose
+ * n_commit is outside 1..8, is left as it is, with the status).  lanes 1..4; committed: int32
+ * [lanes][8]. */
 vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap, const int32_t* n_commit,
                            const int32_t* committed, int* status, void* stream);
 /* `steps` rounds with no host in the loop: x0 = embed(pending) (the embedding table emb_codes /
