@@ -213,7 +213,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from weight_streaming_gb300.model import Geometry
+    from weight_streaming_gb300.geometry import Geometry  # shapes only: no libverify.so in this process
     geom = Geometry(n_layers=args.layers)
     for _ in range(args.warmup):
         oracle_sample(geom, 0, 8, target_s=0.0)

@@ -187,6 +187,11 @@ vp_status vp_linear_q4(const void* w_packed, const void* x, float* y, int M, int
  * Arguments, shapes and errors otherwise as for vp_linear_nvfp4. */
 vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, const void* x, float* y, int M,
                                   int N, int K, void* stream);
+/* The status word of the last vp_linear_nvfp4_noalloc call on this device (ordered on `stream`):
+ * VP_OK, or VP_ERR_TIMEOUT when one of its bounded device waits gave up (its y is then not valid).
+ * Copies the word to the host int *status and synchronises `stream`.  Each noalloc call clears the
+ * word before its launch, so the status is that of the latest call enqueued before this one. */
+vp_status vp_noalloc_read_status(int* status, void* stream);
 
 /* ------------------------------------------------------------------ head + argmax + accept
  *
@@ -384,9 +389,9 @@ vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap,
  * emb_scales / emb_ts, [vocab][hidden]); vp_verify_pass; append the committed tokens; lookup drafts
  * into pending.  pending must hold the first round's anchor + drafts (e.g. from vp_lookup_drafts).
  * x0: bf16 [8 lanes][hidden]; argmax, n_commit, committed, ws as for vp_verify_pass (the last round's
- * values remain).  hidden must be the model's hidden size (x0 is written with it and read by the pass
- * with the model's; the library cannot check the caller's buffer).  All arguments are checked before
- * the first launch: a rejected call enqueues nothing (steps == 0: the checks alone). */
+ * values remain).  hidden must equal the model's hidden size (the embedding writes x0 rows of `hidden`
+ * values and the pass reads rows of the model's width): VP_ERR_SHAPE otherwise.  All arguments are
+ * checked before the first launch: a rejected call enqueues nothing (steps == 0: the checks alone). */
 vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_codes, const void* emb_scales,
                           float emb_ts, int vocab, int hidden, int32_t* hist, int32_t* hist_len, int cap,
                           int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,

@@ -13,7 +13,7 @@ Sources (web pages, cited by title and section):
    heads of 256; the attention in-projection is queries, keys, values and an output gate,
    6144 + 1024 + 1024 + 6144 rows; norms are small bf16 vectors).
 
-The pages name the steps; the formulas below are readings, each also listed in the design notes:
+The pages name the steps; the formulas below are readings (the plainest ones the names support):
  - the q projection's rows are the queries (Hq heads) then the gate (Hq heads); the kv
    projection's rows are the keys (Hkv heads) then the values (Hkv heads);
  - Q/K RMSNorm: each head of q and k over its root mean square (eps 1e-6), times a per-dimension

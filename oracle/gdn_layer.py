@@ -17,8 +17,7 @@ Sources (web pages, cited by title and section):
    and the convolution window are both double-buffered; a partial accept re-scans the committed
    rows, and the state and window after every possible kept count must match a reference scan).
 
-The pages name the steps; the formulas below are readings (the plainest ones the names support),
-each also listed in the design notes:
+The pages name the steps; the formulas below are readings (the plainest ones the names support):
  - in-projection rows: q (n_qk heads), k (n_qk heads), v (n_v heads), then z (n_v heads), each
    head d wide; the A and B projections give one value per v head;
  - short convolution: causal and depthwise over q, k and v, 4 taps, tap 3 on the current token and

@@ -22,7 +22,7 @@
  *    affine 4-bit format (32 bytes of codes + a bf16 scale + a bf16 bias per group of 64 inputs) --
  *    see orc_linear_q4().
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings where the pages are silent (the plainest choice the passages support):
  *  - E2M1 bit layout: bit 3 = sign, bits 2..1 = exponent (bias 1), bit 0 = mantissa (OCP MX).
  *  - Packing of two E2M1 codes per byte: element 2j is the LOW nibble of byte j.
  *  - Block scales run along K: scale[n][k/16].

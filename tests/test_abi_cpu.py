@@ -188,6 +188,9 @@ def test_decode_steps_checks_everything_before_launching(V):
     assert call(cap=0) == V.VP_ERR_SHAPE and call(cap=1 << 24) == V.VP_ERR_SHAPE
     assert call(mm=0) == V.VP_ERR_SHAPE and call(mm=128) == V.VP_ERR_SHAPE
     assert call(vocab=0) == V.VP_ERR_SHAPE and call(hidden=250) == V.VP_ERR_SHAPE
+    # the embedding's row width must be the model's: a wider or narrower x0 row is refused
+    assert call(hidden=512) == V.VP_ERR_SHAPE and call(hidden=128) == V.VP_ERR_SHAPE
+    assert call(steps=0, hidden=512) == V.VP_ERR_SHAPE
     assert call(x0=F + 8) == V.VP_ERR_ALIGNMENT and call(hist=F + 2) == V.VP_ERR_ALIGNMENT
     assert call(ws=F + 128) == V.VP_ERR_ALIGNMENT
     assert call(ws_bytes=need - 1) == V.VP_ERR_WORKSPACE

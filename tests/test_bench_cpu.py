@@ -85,3 +85,17 @@ def test_reference_arm_other_ranks_exit_quietly():
     """Under torchrun only rank 0 runs the oracle arm; the others exit 0 without output."""
     r = _bench(["--impl", "reference", "--steps", "1", "--warmup", "0"], {"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_does_not_load_the_product_library():
+    """The oracle arm times the fp64 oracle alone: its process maps oracle/liboracle.so and never
+    libverify.so (the shapes come from the library-free geometry module)."""
+    import subprocess
+    import sys
+    code = ("import sys, runpy; sys.argv = ['bench.py', '--impl', 'reference', '--steps', '1', '--warmup', '0', "
+            "'--layers', '1']; runpy.run_path('bench.py', run_name='__main__'); "
+            "maps = open('/proc/self/maps').read(); "
+            "print('LIBVERIFY' if 'libverify' in maps else 'CLEAN', 'ORACLE' if 'liboracle' in maps else 'NO-ORACLE')")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().splitlines()[-1] == "CLEAN ORACLE"

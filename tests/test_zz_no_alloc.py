@@ -1,6 +1,7 @@
 """The no-allocation linear call (vp_linear_nvfp4_noalloc) through the C ABI: on two calls in a row
 it returns bit for bit what vp_linear_nvfp4 returns with a caller workspace (same kernel, same
-reduction order), and a shape whose bookkeeping exceeds its fixed scratch is refused.  This file is
+reduction order) and reports a clean status word through vp_noalloc_read_status, and a shape whose
+bookkeeping exceeds its fixed scratch is refused.  This file is
 collected last so that it also runs after everything else has used the GPU."""
 import numpy as np
 import pytest
@@ -34,6 +35,7 @@ def test_noalloc_matches_workspace_call_twice(V, M, N, K):
         V.vp_linear_nvfp4_noalloc(packed, 0.75, x, y, M, N, K)
         torch.cuda.synchronize()
         assert torch.equal(y, y_ref)
+        assert V.vp_noalloc_read_status() == V.VP_OK
     assert np.isfinite(y.cpu().numpy()).all()
 
 

@@ -25,7 +25,7 @@ EXPORTS = [
     "vp_packed_bytes_fp8", "vp_pack_nvfp4", "vp_pack_fp8", "vp_workspace_bytes", "vp_linear_nvfp4",
     "vp_linear_fp8", "vp_head_argmax_accept", "vp_argmax_accept", "vp_model_create", "vp_model_destroy",
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
-    "vp_linear_nvfp4_noalloc", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
+    "vp_linear_nvfp4_noalloc", "vp_noalloc_read_status", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
     "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
     "vp_commit_append", "vp_decode_steps",
 ]
@@ -82,6 +82,7 @@ def _load():
         "vp_verify_blocks": (I, [P, P, I, I, I, P, P, S, P]),
         "vp_pass_launch_count": (I, [P]),
         "vp_linear_nvfp4_noalloc": (I, [P, F, P, P, I, I, I, P]),
+        "vp_noalloc_read_status": (I, [ctypes.POINTER(I), P]),
         "vp_trace_read": (I, [I, P, S, ctypes.POINTER(ctypes.c_uint)]),
         "vp_packed_bytes_q4": (S, [I, I]),
         "vp_pack_q4": (I, [P, P, P, I, I, P, S, P]),
@@ -186,6 +187,13 @@ def vp_linear_nvfp4_noalloc(w_packed, tensor_scale: float, x, y, M: int, N: int,
     calls must not overlap in time (see include/verify.h)."""
     _check("vp_linear_nvfp4_noalloc", _L.vp_linear_nvfp4_noalloc(_ptr(w_packed), tensor_scale, _ptr(x), _ptr(y), M,
                                                                  N, K, _stream(stream)))
+
+
+def vp_noalloc_read_status(stream=None) -> int:
+    """Status word of the last vp_linear_nvfp4_noalloc call on this device (synchronises the stream)."""
+    out = ctypes.c_int(-1)
+    _check("vp_noalloc_read_status", _L.vp_noalloc_read_status(ctypes.byref(out), _stream(stream)))
+    return out.value
 
 
 def vp_linear_fp8(w_packed, scale: float, x, y, M: int, N: int, K: int, ws, stream=None, ws_bytes=None):

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -612,20 +613,21 @@ constexpr size_t kNoallocScratchBytes = (size_t)8 << 20;  // 8 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 
 // Address of the scratch array on the current device, looked up on the first call per device (with
-// that device current) and kept.
+// that device current) and kept.  Host threads may race on the first call: each lookup yields the
+// same address, and the atomic slot makes the store and the later loads well defined.
 vp_status noalloc_scratch(void** out) {
-  static void* addr[64] = {nullptr};
+  static std::atomic<void*> addr[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= 64) return VP_ERR_UNSUPPORTED;
-  if (!addr[dev]) {
-    void* p = nullptr;
+  void* p = addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e);
-    addr[dev] = p;
+    addr[dev].store(p, std::memory_order_release);
   }
-  *out = addr[dev];
+  *out = p;
   return VP_OK;
 }
 
@@ -677,6 +679,17 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
+vp_status vp_noalloc_read_status(int* status, void* stream) {
+  if (!status) return VP_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  vp_status st = noalloc_scratch(&scratch);
+  if (st != VP_OK) return st;
+  // The status word is the first word of the scratch (the workspace layout's status offset is 0).
+  cudaError_t e = cudaMemcpyAsync(status, scratch, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending, int32_t* argmax,
                            int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes, void* stream) {
   if (!logits || !pending || !argmax || !n_commit || !committed || !ws) return VP_ERR_INVALID_ARG;
@@ -712,6 +725,10 @@ struct vp_model {
   std::vector<Phase> phases[4];  // per NT: 4 phases per layer (in, out, gate+up, down), then the head
   Needs needs[4];
 };
+
+namespace vp {
+int model_hidden(const vp_model* model) { return model ? model->hidden : 0; }
+}  // namespace vp
 
 namespace {
 

@@ -623,6 +623,9 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, con
   if (lane == 0) old = atom_add_acq_rel_gpu(io.rb_cnt + rb, 1u);
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old + 1 != (unsigned)total) return;
+  // The shuffle carries no memory ordering: the warp barrier orders lane 0's acquire before the
+  // other lanes' reads of the partials.
+  __syncwarp();
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll

@@ -4,7 +4,12 @@
 #include <cstddef>
 #include <cstdint>
 
+struct vp_model;
+
 namespace vp {
+
+// Hidden size of a model handle (the width of x0 and of the residual stream); api.cu.
+int model_hidden(const vp_model* model);
 
 // ---------------------------------------------------------------- packed weight layout
 // A matrix [N][K] (N % 16 == 0) is stored as row blocks of 16 rows; each row block as K chunks

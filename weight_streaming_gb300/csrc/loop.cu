@@ -167,6 +167,8 @@ vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_code
   if (vocab < 1 || hidden < 16 || hidden % 16 || (long long)vocab * hidden >= (1LL << 40) || cap < 1 ||
       cap >= (1 << 24) || max_match < 1 || max_match > 127)
     return VP_ERR_SHAPE;
+  // The embedding writes x0 rows of `hidden` values and the pass reads rows of the model's width.
+  if (hidden != vp::model_hidden(model)) return VP_ERR_SHAPE;
   if (!al(hist, 4) || !al(hist_len, 4) || !al(pending, 4) || !al(x0, 16) || !al(argmax, 4) || !al(n_commit, 4) ||
       !al(committed, 4) || !al(ws, 256) || (status && !al(status, 4)))
     return VP_ERR_ALIGNMENT;
