@@ -74,11 +74,17 @@ def _mix64(z: np.ndarray) -> np.ndarray:
 
 
 def words(seed: int, stream: int, start: int, count: int) -> np.ndarray:
-    """uint64 words i = start .. start+count-1 of the stream."""
+    """uint64 words i = start .. start+count-1 of the stream (computed in blocks of 2^20 words, so
+    that the temporaries of a large request stay small)."""
     k = np.uint64(key(seed, stream))
-    i = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    out = np.empty(max(count, 0), np.uint64)
+    blk = 1 << 20
     with np.errstate(over="ignore"):
-        return _mix64(k + i * np.uint64(GOLDEN))
+        for b0 in range(0, count, blk):
+            n = min(blk, count - b0)
+            i = np.arange(start + b0 + 1, start + b0 + n + 1, dtype=np.uint64)
+            out[b0:b0 + n] = _mix64(k + i * np.uint64(GOLDEN))
+    return out
 
 
 def uniform_bytes(seed: int, stream: int, start: int, count: int) -> np.ndarray:
@@ -142,10 +148,16 @@ def fp8_normal_thresholds():
 
 
 def _threshold_codes(seed, stream, start, count, table) -> np.ndarray:
+    """Code of word start + i: the number of thresholds <= its top 32 bits picks it.  Done in blocks
+    of 2^20 words, so that the temporaries stay small (the same values as one whole-array pass)."""
     thr, codes = table
-    r = words(seed, stream, start, count) >> np.uint64(32)
-    idx = np.searchsorted(thr, r, side="right")  # number of thresholds <= r
-    return codes[idx]
+    out = np.empty(count, np.uint8)
+    blk = 1 << 20
+    for b0 in range(0, count, blk):
+        n = min(blk, count - b0)
+        r = words(seed, stream, start + b0, n) >> np.uint64(32)
+        out[b0:b0 + n] = codes[np.searchsorted(thr, r, side="right")]
+    return out
 
 
 def scale_codes(seed: int, stream: int, start: int, count: int) -> np.ndarray:

@@ -12,25 +12,36 @@ from helpers import REL, dev_u8
 DELTA = 2.0 ** -7  # one bf16 ulp, relative to the value (a rounding step may flip by one ulp)
 
 
+def make_layer(G, seed, l, scales=None):
+    """Canonical weights of layer l (the seeded recipe; the same bits as the device fills of
+    weight_streaming_gb300.model.SyntheticModel).  scales: the six per-tensor scales, default 1."""
+    attn = (l % G.period) == G.period - 1
+    n_in = G.attn_q if attn else G.gdn_in
+    kz = G.attn_z if attn else G.gdn_z
+    d = {"attn": attn, "n_in": n_in, "kz": kz,
+         "in": synth.fp8_matrix(seed, l, synth.T_IN, n_in, G.hidden),
+         "kv": synth.fp8_matrix(seed, l, synth.T_KV, G.attn_kv, G.hidden) if attn else None,
+         "out": synth.fp8_matrix(seed, l, synth.T_OUT, G.hidden, kz)}
+    d["gate_c"], d["gate_s"] = synth.nvfp4_matrix(seed, l, synth.T_GATE_C, synth.T_GATE_S, G.inter, G.hidden)
+    d["up_c"], d["up_s"] = synth.nvfp4_matrix(seed, l, synth.T_UP_C, synth.T_UP_S, G.inter, G.hidden)
+    d["down_c"], d["down_s"] = synth.nvfp4_matrix(seed, l, synth.T_DOWN_C, synth.T_DOWN_S, G.hidden, G.inter)
+    for i, k in enumerate(("s_in", "s_kv", "s_out", "ts_gate", "ts_up", "ts_down")):
+        d[k] = 1.0 if scales is None else float(scales[i])
+    return d
+
+
+def make_head(G, seed, ts=1.0):
+    hc, hs = synth.nvfp4_matrix(seed, synth.HEAD_LAYER, synth.T_HEAD_C, synth.T_HEAD_S, G.vocab, G.hidden)
+    return hc, hs, float(ts)
+
+
 def make_layers(G, seed, unit_scales=False):
     rng = np.random.default_rng(seed + 777)
     layers = []
     for l in range(G.n_layers):
-        attn = (l % G.period) == G.period - 1
-        n_in = G.attn_q if attn else G.gdn_in
-        kz = G.attn_z if attn else G.gdn_z
-        d = {"attn": attn, "n_in": n_in, "kz": kz,
-             "in": synth.fp8_matrix(seed, l, synth.T_IN, n_in, G.hidden),
-             "kv": synth.fp8_matrix(seed, l, synth.T_KV, G.attn_kv, G.hidden) if attn else None,
-             "out": synth.fp8_matrix(seed, l, synth.T_OUT, G.hidden, kz)}
-        d["gate_c"], d["gate_s"] = synth.nvfp4_matrix(seed, l, synth.T_GATE_C, synth.T_GATE_S, G.inter, G.hidden)
-        d["up_c"], d["up_s"] = synth.nvfp4_matrix(seed, l, synth.T_UP_C, synth.T_UP_S, G.inter, G.hidden)
-        d["down_c"], d["down_s"] = synth.nvfp4_matrix(seed, l, synth.T_DOWN_C, synth.T_DOWN_S, G.hidden, G.inter)
-        for k in ("s_in", "s_kv", "s_out", "ts_gate", "ts_up", "ts_down"):
-            d[k] = 1.0 if unit_scales else float(rng.uniform(0.5, 1.5))
-        layers.append(d)
-    hc, hs = synth.nvfp4_matrix(seed, synth.HEAD_LAYER, synth.T_HEAD_C, synth.T_HEAD_S, G.vocab, G.hidden)
-    head = (hc, hs, 1.0 if unit_scales else float(rng.uniform(0.5, 1.5)))
+        sc = [1.0 if unit_scales else float(rng.uniform(0.5, 1.5)) for _ in range(6)]
+        layers.append(make_layer(G, seed, l, sc))
+    head = make_head(G, seed, 1.0 if unit_scales else float(rng.uniform(0.5, 1.5)))
     return layers, head
 
 
@@ -73,30 +84,13 @@ class DeviceModel:
 
 # ------------------------------------------------------------------ error budget of one block
 
-_E4 = None
-_E2 = None
-
-
-def _tables():
-    global _E4, _E2
-    if _E4 is None:
-        _E4 = oracle.e4m3_table()
-        _E2 = oracle.e2m1_table()
-    return _E4, _E2
-
-
-def abs_fp8(w8, s):
-    E4, _ = _tables()
-    return np.abs(E4[w8]) * abs(s)
-
-
-def abs_nvfp4(codes, scales, ts):
-    E4, E2 = _tables()
-    N, K2 = codes.shape
-    q = np.empty((N, 2 * K2), np.int64)
-    q[:, 0::2] = codes & 15
-    q[:, 1::2] = codes >> 4
-    return np.abs(E2[q]) * np.repeat(np.abs(E4[scales]), 16, axis=1) * abs(ts)
+def prop_bound(fmt, dx, codes, scales, ts, N):
+    """An upper bound of sum_k dx[m][k] |w[n][k]| (dx >= 0): the oracle's sum |x w| over dx rounded
+    up to bf16.  bf16 keeps 8 significant bits, so rounding dx (1 + 2^-7) to nearest stays above dx;
+    the bound is at most 2^-6 above the exact sum."""
+    v = np.maximum(np.asarray(dx, np.float64), 0.0) * (1.0 + 2.0 ** -7)
+    _, a = oracle.linear(fmt, oracle.bf16_round(v), codes, scales, ts, N)
+    return a
 
 
 def mixer_block_ref(G, d, h_in_bits):
@@ -112,7 +106,7 @@ def mixer_block_ref(G, d, h_in_bits):
     du = (REL + DELTA) * a_u[:, :kz]
     dz = du + DELTA * (np.abs(z) + du)
     y, a_y = oracle.linear(oracle.FP8, z_bits, d["out"], None, d["s_out"], G.hidden)
-    prop = dz @ abs_fp8(d["out"], d["s_out"]).T
+    prop = prop_bound(oracle.FP8, dz, d["out"], None, d["s_out"], G.hidden)
     dy = REL * (a_y + prop) + prop
     h_out = oracle.bf16_round(oracle.bf16_value(h_in_bits) + y)
     hv = oracle.bf16_value(h_out)
@@ -132,7 +126,7 @@ def mlp_block_ref(G, d, h_in_bits):
     ds = 1.1 * dg * (np.abs(u) + du) + (np.abs(silu_g) + 1.1 * dg) * du + 1e-6 * np.abs(s)
     da = ds + DELTA * (np.abs(av) + ds)
     y, a_y = oracle.linear(oracle.NVFP4, a_bits, d["down_c"], d["down_s"], d["ts_down"], G.hidden)
-    prop = da @ abs_nvfp4(d["down_c"], d["down_s"], d["ts_down"]).T
+    prop = prop_bound(oracle.NVFP4, da, d["down_c"], d["down_s"], d["ts_down"], G.hidden)
     dy = REL * (a_y + prop) + prop
     h_out = oracle.bf16_round(oracle.bf16_value(h_in_bits) + y)
     hv = oracle.bf16_value(h_out)
