@@ -20,6 +20,12 @@ LIB = os.path.join(PKG, "libverify.so")
 # The same library with the executor's phase timeline recorded (trace.cuh): a measurement build.
 BUILD_TRACE = os.path.join(PKG, "_build_trace")
 LIB_TRACE = os.path.join(PKG, "libverify_trace.so")
+# The same library with tiny limits on every bounded device wait and a workspace hook that makes
+# one CTA skip its first grid-barrier arrival: the build in which a test makes a wait run out.
+BUILD_WAIT = os.path.join(PKG, "_build_waittest")
+LIB_WAIT = os.path.join(PKG, "libverify_waittest.so")
+VARIANTS = {"": (LIB, BUILD, []), "trace": (LIB_TRACE, BUILD_TRACE, ["-DVP_PHASE_TRACE"]),
+            "waittest": (LIB_WAIT, BUILD_WAIT, ["-DVP_WAIT_TEST"])}
 SOURCES = ["api.cu", "exec_nt12.cu", "exec_nt34.cu", "exec_q4.cu", "sample.cu", "attention.cu", "gdn.cu",
            "loop.cu", "errors.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,10 +46,11 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
-    """Builds libverify.so (or, with trace=True, libverify_trace.so with the phase timeline) and
-    returns its path; nothing is rebuilt when the library is newer than every source."""
-    lib, bdir = (LIB_TRACE, BUILD_TRACE) if trace else (LIB, BUILD)
+def build(force: bool = False, verbose: bool = False, trace: bool = False, variant: str = "") -> str:
+    """Builds libverify.so (or a measurement / test variant of it: "trace" with the phase timeline,
+    "waittest" with tiny wait limits; trace=True is variant "trace") and returns its path; nothing
+    is rebuilt when the library is newer than every source."""
+    lib, bdir, defs = VARIANTS["trace" if trace else variant]
     deps = _inputs()
     if not force and not _stale(lib, deps):
         return lib
@@ -53,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
     for src in SOURCES:
         obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = ["nvcc", *ARCH, *FLAGS, *(["-DVP_PHASE_TRACE"] if trace else []), "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = ["nvcc", *ARCH, *FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
@@ -73,4 +80,5 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False) -> st
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv,
+                variant="waittest" if "--waittest" in sys.argv else ""))

@@ -733,13 +733,19 @@ __device__ __noinline__ void head_finish(const Program& prog, const Io& io, int 
 // launch.
 __device__ __forceinline__ void grid_barrier(const Io& io, int G, unsigned target, SmemMisc& sm) {
   __syncthreads();
-  if (threadIdx.x == 0) {
+  bool skip = false;
+#ifdef VP_WAIT_TEST
+  // Wait-test hook (workspace word kWsTestSkip): CTA (value - 1) leaves its first arrival out, so
+  // that every other CTA's wait runs out.
+  skip = target == (unsigned)G && ((const volatile int*)io.status)[kWsTestSkip / sizeof(int)] == (int)blockIdx.x + 1;
+#endif
+  if (threadIdx.x == 0 && !skip) {
     __threadfence();
     const unsigned arrived = atomicAdd(io.bar, 1u) + 1u;
     if (arrived < target && !sm.abort) {
       uint32_t n = 0;
       while (ld_acquire_gpu(io.bar) < target) {
-        if (++n > (1u << 22)) {  // about 1-2 s
+        if (++n > kBarrierPolls) {  // about 1-2 s (milliseconds in the wait-test build)
           sm.abort = 1;
           atomicExch(io.status, kStatusTimeout);
           break;
@@ -878,9 +884,15 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     if (p + 1 < prog.n) grid_barrier(io, G, (unsigned)G * (unsigned)(p + 1), sm);
     VP_TRACE(threadIdx.x == 0, p, 34);
   }
-  // Copies still in flight (only after a timeout): wait for them before the CTA's memory goes away.
+  // Copies still in flight (only after a timeout, when the units are consumed without waiting):
+  // wait for the last copy issued into each slot before the CTA's memory goes away.  A copy goes
+  // into a slot only after the wait for that slot's previous copy, so the last one is the only one
+  // that can be pending, and waiting on its phase parity is exact whether or not it has landed.
   if (lane == 0)
-    for (unsigned k = seq; k < issued; ++k) mbar_wait_bounded(&sm.full[warp][k % kSlots], (k / kSlots) & 1u);
+    for (unsigned s = 0; s < (unsigned)kSlots && s < issued; ++s) {
+      const unsigned k = issued - 1 - ((issued - 1 - s) % kSlots);  // the last copy into slot s
+      mbar_wait_bounded(&sm.full[warp][s], (k / kSlots) & 1u);
+    }
   if (prog.n > 1) grid_exit(io, G);
 }
 

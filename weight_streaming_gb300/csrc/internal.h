@@ -132,6 +132,11 @@ struct Io {
 // ---------------------------------------------------------------- workspace carving
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Byte offset, from the status word, of the wait-test hook word (read only by the wait-test build:
+// a nonzero value v makes CTA v - 1 leave its first grid-barrier arrival out).  It lies in the
+// padding between the status word and the barrier counters.
+constexpr size_t kWsTestSkip = 32;
+
 struct WsLayout {
   size_t status, bar, head_cnt, head_aux, rb_cnt, partials, total;
 };

@@ -35,10 +35,21 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
       : "memory");
   return ok != 0;
 }
-// Bounded wait for the phase with the given parity: at most 2^16 suspended polls of <= 20 us each
-// (about 1.3 s), after which it returns false and the caller records a timeout.
+// Poll limits of the bounded waits: the mbarrier waits of the weight rings (suspended polls of <= 20
+// us each) and the grid barrier (polls of about 1 us).  The wait-test build makes both tiny, so that
+// a test can make a wait run out in milliseconds; normal waits take microseconds.
+#ifdef VP_WAIT_TEST
+constexpr uint32_t kMbarPolls = 1u << 8;
+constexpr uint32_t kBarrierPolls = 1u << 13;
+#else
+constexpr uint32_t kMbarPolls = 1u << 16;
+constexpr uint32_t kBarrierPolls = 1u << 22;
+#endif
+
+// Bounded wait for the phase with the given parity: at most kMbarPolls suspended polls of <= 20 us
+// each (about 1.3 s), after which it returns false and the caller records a timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < (1u << 16); ++i)
+  for (uint32_t i = 0; i < kMbarPolls; ++i)
     if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
   return false;
 }
