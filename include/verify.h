@@ -180,7 +180,8 @@ vp_status vp_linear_q4(const void* w_packed, const void* x, float* y, int M, int
  *     may initialise the CUDA context); make it before any stream capture.
  *   - Every call clears the scratch's status word and counters on `stream` before its launch.
  *   - Shapes whose split-K bookkeeping needs more than the 8 MiB scratch (roughly: many rows times
- *     a long K, e.g. a 248320 x 5120 head) return VP_ERR_WORKSPACE; use vp_linear_nvfp4 for them.
+ *     a K cut into several K slices, e.g. a 248320 x 5120 head at M = 32) return VP_ERR_WORKSPACE;
+ *     use vp_linear_nvfp4 for them.
  *   - The scratch is shared by all calls on a device: calls that overlap in time (on different
  *     streams, or from different host threads) race and corrupt each other's results.  Order them
  *     on one stream.

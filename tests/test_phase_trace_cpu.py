@@ -42,3 +42,15 @@ def test_report_lists_every_kind_once():
     assert lines[-1].startswith("first phase start -> last phase done:")
     head = lines[-2].split()
     assert head[-2:] == ["-", "-"]
+
+
+def test_k_sliced_phase_reports_its_cross_slice_step():
+    """A phase with cross-slice sums (slot 35 stamped in every CTA) reports them from the last
+    in-CTA fixup to the slowest CTA's sums, and its release from there."""
+    T = stamps()
+    T[1, :, 35] = T[1, :, 18:34].max() + 3_000 + np.arange(T.shape[1]) * 100
+    st = phase_stats(T, last_of_launch={4})
+    d = st["mixer out"][0]
+    assert d["x-slice"] == 3_000 + 100 * (T.shape[1] - 1)
+    assert d["release"] == T[1, :, 34].min() - T[1, :, 35].max()
+    assert "x-slice" not in st["mixer in"][0]

@@ -42,5 +42,5 @@ def test_noalloc_matches_workspace_call_twice(V, M, N, K):
 def test_noalloc_refuses_oversized_shape(V):
     L = V.lib()
     fake = 0x10000000  # never dereferenced: the size check comes first
-    st = L.vp_linear_nvfp4_noalloc(fake, 1.0, fake, fake, 8, 248320, 5120, None)
+    st = L.vp_linear_nvfp4_noalloc(fake, 1.0, fake, fake, 32, 248320, 5120, None)
     assert st == V.VP_ERR_WORKSPACE

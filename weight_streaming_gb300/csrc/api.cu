@@ -87,7 +87,6 @@ Phase make_phase(const PhaseSpec& s, int NT) {
   ph.KG = (ph.KC + ph.grp - 1) / ph.grp;
   const int per = ks_max(NT) / chunk_k(s.fmt) / ph.grp;  // groups per slice at most
   ph.ks = (int8_t)((ph.KG + per - 1) / per);
-  ph.cmax = phase_cmax(ph.RB, ph.KG, ph.ks);
   ph.fmt = (int8_t)s.fmt;
   ph.layout = (int8_t)s.layout;
   ph.epi = (int8_t)s.epi;
@@ -114,20 +113,22 @@ bool slices_ok(const Phase& ph, int G) {
   return true;
 }
 
-// Fixup slots of a phase, in units of 32 lanes x 4 NT floats (an interleaved phase keeps two sets).
-size_t phase_slots(const Phase& ph) {
-  return (size_t)ph.RB * ph.ks * ph.cmax * (ph.layout == kInterleaved ? 2 : 1);
-}
-
+// The split-K bookkeeping a program needs: floats per lane of a partial (4 NT; 8 NT when a phase is
+// interleaved) and the largest cross-slice slot area (RB * ks partials of the phases with ks > 1).
 struct Needs {
-  size_t max_rb = 1, max_slots = 1;
+  int NT = 1;
+  bool two = false;
+  size_t x_parts = 0;
+  explicit Needs(int nt = 1) : NT(nt) {}
   void add(const Phase& ph) {
-    max_rb = std::max(max_rb, (size_t)ph.RB);
-    max_slots = std::max(max_slots, phase_slots(ph));
+    two = two || ph.layout == kInterleaved;
+    if (ph.ks > 1) x_parts = std::max(x_parts, (size_t)ph.RB * ph.ks);
   }
+  int cs_lane() const { return 4 * NT * (two ? 2 : 1); }
+  WsLayout layout() const { return ws_layout(cs_lane(), x_parts * 32 * (size_t)cs_lane()); }
 };
 
-Io make_io(void* ws, const WsLayout& L) {
+Io make_io(void* ws, const WsLayout& L, int cs_lane) {
   Io io;
   memset(&io, 0, sizeof(io));
   uint8_t* b = static_cast<uint8_t*>(ws);
@@ -135,8 +136,9 @@ Io make_io(void* ws, const WsLayout& L) {
   io.bar = reinterpret_cast<unsigned*>(b + L.bar);
   io.head_cnt = reinterpret_cast<unsigned*>(b + L.head_cnt);
   io.head_aux = reinterpret_cast<float*>(b + L.head_aux);
-  io.rb_cnt = reinterpret_cast<unsigned*>(b + L.rb_cnt);
-  io.partials = reinterpret_cast<float*>(b + L.partials);
+  io.cslots = reinterpret_cast<float*>(b + L.cslots);
+  io.xslots = reinterpret_cast<float*>(b + L.xslots);
+  io.cs_lane = cs_lane;
   return io;
 }
 
@@ -334,8 +336,10 @@ void argmax_chunking(int V, int* chunk, int* n_chunks) {
   *n_chunks = (V + ch - 1) / ch;
 }
 
-size_t single_ws_bytes(const Phase& ph, int NT) {
-  return ws_layout((size_t)ph.RB, phase_slots(ph), NT).total;
+Needs single_needs(const Phase& ph, int NT) {
+  Needs n(NT);
+  n.add(ph);
+  return n;
 }
 
 }  // namespace
@@ -440,7 +444,7 @@ vp_status vp_pack_q4(const void* codes, const void* scales, const void* biases, 
 size_t vp_workspace_bytes(int op, int M, int N, int K) {
   if (op == VP_OP_ARGMAX) {
     if (M < 8 || M > kMaxM || M % 8 || N < 1) return 0;
-    return ws_layout(1, 1, 1).rb_cnt;  // the counter and the per-chunk maxima
+    return ws_layout(4, 0).cslots;  // the counter and the per-chunk maxima
   }
   if (op == VP_OP_ATTN) {  // N = kv heads, K = cache capacity (positions per lane)
     if (M < 8 || M > kMaxM || M % 8 || N < 1 || K < 8 || K > (1 << 24)) return 0;
@@ -458,20 +462,21 @@ size_t vp_workspace_bytes(int op, int M, int N, int K) {
   s.fmt = fmt;
   s.rows0 = N;
   s.K = K;
-  return single_ws_bytes(make_phase(s, nt_of(M)), nt_of(M));
+  return single_needs(make_phase(s, nt_of(M)), nt_of(M)).layout().total;
 }
 
 static vp_status run_single(const PhaseSpec& s, int M, const void* x, void* ws, size_t ws_bytes, Io io_extra,
                             cudaStream_t stream) {
   const int NT = nt_of(M);
   const Phase ph = make_phase(s, NT);
-  const WsLayout L = ws_layout((size_t)ph.RB, phase_slots(ph), NT);
+  const Needs nd = single_needs(ph, NT);
+  const WsLayout L = nd.layout();
   if (ws_bytes < L.total) return VP_ERR_WORKSPACE;
   int sms = 0;
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
   if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
-  Io io = make_io(ws, L);
+  Io io = make_io(ws, L, nd.cs_lane());
   for (int b = 0; b < kNumBufs; ++b) io.buf[b] = io_extra.buf[b];
   io.buf[kBufX] = const_cast<void*>(x);
   io.pending = io_extra.pending;
@@ -653,7 +658,8 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   s.out_ld = N;
   const int NT = nt_of(M);
   const Phase ph = make_phase(s, NT);
-  const WsLayout L = ws_layout((size_t)ph.RB, phase_slots(ph), NT);
+  const Needs nd = single_needs(ph, NT);
+  const WsLayout L = nd.layout();
   if (L.total > kNoallocScratchBytes) return VP_ERR_WORKSPACE;  // the shape needs more than the fixed scratch
   int sms = 0;
   vp_status st = device_sms(&sms);
@@ -663,10 +669,10 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   if ((st = noalloc_scratch(&scratch)) != VP_OK) return st;
   cudaStream_t cs = (cudaStream_t)stream;
   // The status word, the barrier and the counters must start at zero: clear them on every call
-  // (the fixup slots and the head maxima are written before they are read).
-  cudaError_t e = cudaMemsetAsync(scratch, 0, L.partials, cs);
+  // (the split-K slots and the head maxima are written before they are read).
+  cudaError_t e = cudaMemsetAsync(scratch, 0, L.head_aux, cs);
   if (e != cudaSuccess) return cuda_fail(e);
-  Io io = make_io(scratch, L);
+  Io io = make_io(scratch, L, nd.cs_lane());
   io.buf[kBufX] = const_cast<void*>(x);
   io.buf[kBufY] = y;
   static thread_local Program prog;
@@ -703,7 +709,7 @@ vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pen
   if (st != VP_OK) return st;
   int chunk = 0, n_chunks = 0;
   argmax_chunking(V, &chunk, &n_chunks);
-  const WsLayout L = ws_layout(1, 1, 1);
+  const WsLayout L = ws_layout(4, 0);
   uint8_t* b = (uint8_t*)ws;
   argmax_accept_kernel<<<dim3(n_chunks, M), 256, 0, (cudaStream_t)stream>>>(
       logits, M, V, chunk, n_chunks, pending, argmax, n_commit, committed, (float*)(b + L.head_aux),
@@ -723,7 +729,7 @@ struct vp_model {
   vp_head_desc head;
   int zmax;
   std::vector<Phase> phases[4];  // per NT: 4 phases per layer (in, out, gate+up, down), then the head
-  Needs needs[4];
+  Needs needs[4] = {Needs(1), Needs(2), Needs(3), Needs(4)};
 };
 
 namespace vp {
@@ -821,7 +827,7 @@ void build_pass(vp_model* md, int NT) {
   hd.out = kBufLogits;
   hd.out_ld = md->head.vocab;
   out.push_back(make_phase(hd, NT));
-  nd = Needs();
+  nd = Needs(NT);
   for (const Phase& ph : out) nd.add(ph);
 }
 
@@ -833,7 +839,7 @@ struct PassWs {
 PassWs pass_ws(const vp_model* md, int M) {
   const int NT = nt_of(M);
   PassWs w;
-  w.L = ws_layout(md->needs[NT - 1].max_rb, md->needs[NT - 1].max_slots, NT);
+  w.L = md->needs[NT - 1].layout();
   size_t off = w.L.total;
   w.h = off;
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->hidden, 256);
@@ -928,7 +934,7 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
   cudaStream_t s = (cudaStream_t)stream;
   const PassWs w = pass_ws(md, M);
   uint8_t* b = (uint8_t*)ws;
-  Io io = make_io(ws, w.L);
+  Io io = make_io(ws, w.L, md->needs[nt_of(M) - 1].cs_lane());
   io.buf[kBufH] = b + w.h;
   io.buf[kBufZ] = b + w.z;
   io.buf[kBufA] = b + w.a;
@@ -967,7 +973,7 @@ vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, 
   phases[0].ss &= ~kSsRead;  // the caller's h: no producer left its row-block sums
   const PassWs w = pass_ws(md, M);
   uint8_t* b = (uint8_t*)ws;
-  Io io = make_io(ws, w.L);
+  Io io = make_io(ws, w.L, md->needs[nt_of(M) - 1].cs_lane());
   io.buf[kBufH] = h;
   io.buf[kBufZ] = b + w.z;
   io.buf[kBufA] = b + w.a;

@@ -68,11 +68,13 @@ __device__ __forceinline__ void accept_lane(int l, const int* tok, const int32_t
 
 // ---------------------------------------------------------------- phase geometry
 // K slice s of a phase: chunk groups [kg0, kg0 + kgn), CTAs [cta0, cta0 + ctan) in proportion to
-// the groups, U = RB * kgn units (row-block major) over W = min(16 ctan, U) warps, so that every
-// warp with a range owns at least one unit (the owners of a row block's units are then exactly its
-// contributors, and consecutive); the slice's other warps idle.
+// the groups.  Within a slice every CTA owns whole row blocks: CTA c of the slice owns row blocks
+// [c RB / ctan, (c + 1) RB / ctan), so a (row block, slice) task never leaves its CTA.  The CTA's
+// units (row-block major, kgn per row block) are cut into equal contiguous ranges over
+// W = min(16, U) warps, so every warp with a range owns at least one unit and the contributors of
+// a row block are consecutive warps.
 struct Slice {
-  int kg0, kgn, cta0, ctan, U, W;
+  int kg0, kgn, cta0, ctan;
 };
 __device__ __forceinline__ Slice slice_geom(const Phase& ph, int G, int s) {
   Slice S;
@@ -83,22 +85,36 @@ __device__ __forceinline__ Slice slice_geom(const Phase& ph, int G, int s) {
   S.kgn = kg1 - kg0;
   S.cta0 = c0;
   S.ctan = c1 - c0;
-  S.U = ph.RB * S.kgn;
-  S.W = min(kWarps * S.ctan, S.U);
   return S;
 }
-__device__ __forceinline__ int slice_of_cta(const Phase& ph, int G, int cta, Slice& S) {
+// A CTA's share of a phase: its slice, its row blocks [rb0, rb0 + nrb), U = nrb * kgn units over W
+// warps.
+struct Part {
+  Slice S;
+  int sidx, rb0, nrb, U, W;
+};
+__device__ __forceinline__ Part part_of_cta(const Phase& ph, int G, int cta) {
+  Part P;
+  P.sidx = ph.ks - 1;
   for (int s = 0; s < ph.ks; ++s) {
-    S = slice_geom(ph, G, s);
-    if (cta < S.cta0 + S.ctan) return s;
+    P.S = slice_geom(ph, G, s);
+    if (cta < P.S.cta0 + P.S.ctan) {
+      P.sidx = s;
+      break;
+    }
   }
-  return ph.ks - 1;
+  const int c = cta - P.S.cta0;
+  P.rb0 = (int)((long long)c * ph.RB / P.S.ctan);
+  P.nrb = (int)((long long)(c + 1) * ph.RB / P.S.ctan) - P.rb0;
+  P.U = P.nrb * P.S.kgn;
+  P.W = min(kWarps, P.U);
+  return P;
 }
-// Warp w of a slice owns units [range_begin(w), range_begin(w + 1)); owner(u) inverts it.
-__device__ __forceinline__ int range_begin(const Slice& S, int w) {
-  return w >= S.W ? S.U : (int)((long long)w * S.U / S.W);
+// Warp w of a CTA owns its units [wbegin(w), wbegin(w + 1)); wowner(u) inverts it.
+__device__ __forceinline__ int wbegin(const Part& P, int w) {
+  return w >= P.W ? P.U : (int)((long long)w * P.U / P.W);
 }
-__device__ __forceinline__ int owner(const Slice& S, int u) { return (int)(((long long)(u + 1) * S.W - 1) / S.U); }
+__device__ __forceinline__ int wowner(const Part& P, int u) { return (int)(((long long)(u + 1) * P.W - 1) / P.U); }
 
 // ---------------------------------------------------------------- weight producer (lane 0 of a warp)
 // Walks the warp's units across all phases of the program, in consumption order, keeping the
@@ -138,16 +154,14 @@ __device__ __forceinline__ void cursor_locate(Cursor& c, const Program& prog) {
 __device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, int G, int cta, int warp) {
   while (c.p < prog.n) {
     const Phase& ph = prog.ph[c.p];
-    Slice S;
-    slice_of_cta(ph, G, cta, S);
-    const int w = (cta - S.cta0) * kWarps + warp;
-    const int u = range_begin(S, w);
-    c.left = range_begin(S, w + 1) - u;
+    const Part P = part_of_cta(ph, G, cta);
+    const int u = wbegin(P, warp);
+    c.left = wbegin(P, warp + 1) - u;
     if (c.left > 0) {
-      c.kg0 = S.kg0;
-      c.kgn = S.kgn;
-      c.rb = u / S.kgn;
-      c.kgl = u - c.rb * S.kgn;
+      c.kg0 = P.S.kg0;
+      c.kgn = P.S.kgn;
+      c.rb = P.rb0 + u / P.S.kgn;
+      c.kgl = u - (c.rb - P.rb0) * P.S.kgn;
       cursor_locate(c, prog);
       return;
     }
@@ -177,6 +191,8 @@ __device__ __forceinline__ void cursor_next(Cursor& c, const Program& prog, int 
 struct SmemMisc {
   uint64_t full[kWarps][kSlots];
   Cursor cur[kWarps];  // the producer state of each warp (used by its lane 0 only)
+  unsigned tcnt[kWarps];  // arrivals at a row block shared by warps, indexed by its first contributor
+  Part part;              // the CTA's share of the current phase
   float red[kThreads / 16];
   float xscale[kMaxM];
   int tok[kMaxM];
@@ -576,13 +592,28 @@ __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const flo
   }
 }
 
-// Finishes row block rb of the warp's range: directly when the warp computed all of it, else
-// through the fixup slots (the last of its contributors sums them in a fixed order).  Plain layout:
-// the row block is acc + acc2 (two MMA chains); interleaved: acc = gate rows, acc2 = up rows.
+// Stores one partial (this lane's v and, interleaved, u) at slot address sl.
 template <int NT>
-__device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, const Slice& S, int w, int ub, int ue,
-                      int rb, const float (&acc)[NT][4], const float (&acc2)[NT][4], const float (&tsc)[NT][2],
-                      HeadBest<NT>& hb, int lane) {
+__device__ __forceinline__ void store_partial(float* sl, bool two, const float (&v)[NT][4], const float (&u)[NT][4]) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    *reinterpret_cast<float4*>(sl + 4 * j) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+    if (two) *reinterpret_cast<float4*>(sl + 4 * (NT + j)) = make_float4(u[j][0], u[j][1], u[j][2], u[j][3]);
+  }
+}
+
+// Finishes the warp's part of row block rb (the task of this CTA's K slice): v = its sum over the
+// slice (plain: acc + acc2, two MMA chains; interleaved: acc = gate rows, acc2 = up rows, in u).
+//  * Several warps of the CTA share the row block: each stores its partial in the CTA's slot of its
+//    first or last row block and arrives on a shared-memory counter (CTA scope); the last to arrive
+//    sums the slots in warp order, so the result does not depend on who arrives last.
+//  * One K slice (ks == 1): the finished row block runs its epilogue here.  Several K slices: its
+//    sum over this slice goes to the cross-slice slot, summed after the next grid barrier.
+template <int NT>
+__device__ void flush(const Phase& ph, const Io& io, int M, int G, int w, int rb, const float (&acc)[NT][4],
+                      const float (&acc2)[NT][4], const float (&tsc)[NT][2], HeadBest<NT>& hb, SmemMisc& sm,
+                      int lane) {
+  const Part& P = sm.part;  // read from shared memory: nothing of it stays live in the unit loop
   const bool two = ph.layout == kInterleaved;
   float v[NT][4], u[NT][4];
 #pragma unroll
@@ -593,48 +624,72 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, con
       v[j][r] = (two ? acc[j][r] : acc[j][r] + acc2[j][r]) * sc;
       u[j][r] = two ? acc2[j][r] * sc : 0.0f;
     }
-  uint16_t hold[NT][4];  // residual inputs, loaded before the fixup round trips
-  if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
-  const int uf = rb * S.kgn;
-  if (ph.ks == 1 && uf >= ub && uf + S.kgn <= ue) {
-    epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
+  const int per_lane = io.cs_lane;
+  const int kgn = P.S.kgn, r0 = (rb - P.rb0) * kgn;
+  const int wf = wowner(P, r0), wl = wowner(P, r0 + kgn - 1);
+  if (wf != wl) {
+    const size_t cta_slots = (size_t)blockIdx.x * kWarps * 2;
+    store_partial<NT>(io.cslots + ((cta_slots + 2 * w + (wbegin(P, w) >= r0 ? 0 : 1)) * 32 + lane) * per_lane, two, v,
+                      u);
+    // Release (CTA scope): the warp's stores, ordered before by the warp barrier, are visible to the
+    // warp that finishes the row block; acquire: that warp then sees every contributor's partial.
+    __syncwarp();
+    unsigned old = 0;
+    if (lane == 0) old = atom_add_acq_rel_cta_smem(&sm.tcnt[wf], 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old + 1 != (unsigned)(wl - wf + 1)) return;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
+    for (int c = wf; c <= wl; ++c) {
+      const float* sl = io.cslots + ((cta_slots + 2 * c + (wbegin(P, c) >= r0 ? 0 : 1)) * 32 + lane) * per_lane;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const float4 q = *reinterpret_cast<const float4*>(sl + 4 * j);
+        v[j][0] += q.x;
+        v[j][1] += q.y;
+        v[j][2] += q.z;
+        v[j][3] += q.w;
+        if (two) {
+          const float4 q2 = *reinterpret_cast<const float4*>(sl + 4 * (NT + j));
+          u[j][0] += q2.x;
+          u[j][1] += q2.y;
+          u[j][2] += q2.z;
+          u[j][3] += q2.w;
+        }
+      }
+    }
+    if (lane == 0) sm.tcnt[wf] = 0u;
+  }
+  if (ph.ks > 1) {
+    store_partial<NT>(io.xslots + (((size_t)rb * ph.ks + P.sidx) * 32 + lane) * per_lane, two, v, u);
     return;
   }
-  const int per_lane = 4 * NT * (two ? 2 : 1);
-  const size_t slot_floats = 32 * (size_t)per_lane;
-  {
-    const int i = w - owner(S, uf);
-    float* slot = io.partials + (((size_t)rb * ph.ks + sidx) * ph.cmax + i) * slot_floats + lane * per_lane;
+  uint16_t hold[NT][4];
+  if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
+  epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
+}
+
+// Phases with several K slices, after the grid barrier that follows the units: row block rb is
+// summed over its slices in slice order (by one warp; consecutive row blocks go to different CTAs)
+// and runs its epilogue.
+template <int NT>
+__device__ void cross_slice_fixup(const Phase& ph, const Io& io, int M, int G, HeadBest<NT>& hb, int warp,
+                                  int lane) {
+  const bool two = ph.layout == kInterleaved;
+  const int per_lane = io.cs_lane;
+  for (int rb = warp * G + (int)blockIdx.x; rb < ph.RB; rb += G * kWarps) {
+    float v[NT][4], u[NT][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      *reinterpret_cast<float4*>(slot + 4 * j) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
-      if (two) *reinterpret_cast<float4*>(slot + 4 * (NT + j)) = make_float4(u[j][0], u[j][1], u[j][2], u[j][3]);
-    }
-  }
-  __syncwarp();
-  int total = 0;
-  for (int s = 0; s < ph.ks; ++s) {
-    const Slice T = slice_geom(ph, G, s);
-    total += owner(T, rb * T.kgn + T.kgn - 1) - owner(T, rb * T.kgn) + 1;
-  }
-  // Release: the warp's partial (ordered before by the warp barrier) is visible to the CTA that
-  // finishes the row block; acquire: that CTA then sees every contributor's partial.
-  unsigned old = 0;
-  if (lane == 0) old = atom_add_acq_rel_gpu(io.rb_cnt + rb, 1u);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old + 1 != (unsigned)total) return;
-  // The shuffle carries no memory ordering: the warp barrier orders lane 0's acquire before the
-  // other lanes' reads of the partials.
-  __syncwarp();
+    for (int j = 0; j < NT; ++j)
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
-  for (int s = 0; s < ph.ks; ++s) {
-    const Slice T = slice_geom(ph, G, s);
-    const int a = owner(T, rb * T.kgn), nc = owner(T, rb * T.kgn + T.kgn - 1) - a + 1;
-    for (int ii = 0; ii < nc; ++ii) {
-      const float* sl = io.partials + (((size_t)rb * ph.ks + s) * ph.cmax + ii) * slot_floats + lane * per_lane;
+      for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
+    uint16_t hold[NT][4];
+    if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
+    for (int s = 0; s < ph.ks; ++s) {
+      const float* sl = io.xslots + (((size_t)rb * ph.ks + s) * 32 + lane) * per_lane;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const float4 q = ldcg_f4(sl + 4 * j);
@@ -651,9 +706,8 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int sidx, con
         }
       }
     }
+    epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
   }
-  if (lane == 0) io.rb_cnt[rb] = 0u;
-  epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
 }
 
 // Head phase end: per-token argmax of the CTA, then the last CTA to finish reduces all CTAs in a
@@ -775,8 +829,10 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
   const int G = gridDim.x, cta = blockIdx.x;
 
-  if (lane == 0)
+  if (lane == 0) {
     for (int s = 0; s < kSlots; ++s) mbar_init(&sm.full[warp][s], 1);
+    sm.tcnt[warp] = 0u;
+  }
   if (threadIdx.x == 0) sm.abort = 0;
   fence_mbar_init();
   __syncthreads();
@@ -795,14 +851,14 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     }
   }
 
-  unsigned seq = 0;
+  unsigned seq = 0, nbar = 0;
   for (int p = 0; p < prog.n; ++p) {
     const Phase& ph = prog.ph[p];
     VP_TRACE(threadIdx.x == 0, p, 0);
-    Slice S;
-    const int sidx = slice_of_cta(ph, G, cta, S);
-    const int ck = chunk_k(ph.fmt), kc0 = S.kg0 * ph.grp;
-    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
+    const Part P = part_of_cta(ph, G, cta);
+    if (threadIdx.x == 0) sm.part = P;  // published by the staging's closing barrier
+    const int ck = chunk_k(ph.fmt), kc0 = P.S.kg0 * ph.grp;
+    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
     VP_TRACE(threadIdx.x == 0, p, 1);
     float tsc[NT][2];
 #pragma unroll
@@ -818,13 +874,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         hb.v[j][h] = -INFINITY;
         hb.i[j][h] = 0x7fffffff;
       }
-    const int w = (cta - S.cta0) * kWarps + warp;
-    const int ub = range_begin(S, w), ue = range_begin(S, w + 1);
+    const int ub = wbegin(P, warp), ue = wbegin(P, warp + 1);
     const uint32_t xlane = smem_addr(xs) + lane * 16;
     const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
     const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
     const bool two = ph.layout == kInterleaved;
-    int rb = ub < ue ? ub / S.kgn : 0, kgl = ub < ue ? ub - rb * S.kgn : 0;
+    int rb = ub < ue ? P.rb0 + ub / P.S.kgn : 0, kgl = ub < ue ? ub % P.S.kgn : 0;
     float acc[NT][4], acc2[NT][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -834,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     for (int u = ub; u < ue; ++u) {
       if (rb != cur) {
         if (cur >= 0) {
-          flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
+          flush<NT>(ph, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
 #pragma unroll
           for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -850,12 +905,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kgl * ph.grp * pair_stride;
       if constexpr (kQ4) {  // one or two consecutive chunks of the row block, 4 groups each
         unit_q4<NT>(ua, xa, lane, acc);
-        if ((S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
+        if ((P.S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
       } else if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
         unit_nvfp4<NT>(ua, xa, lane, acc, acc);
         unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
       } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
-        const bool second = ph.grp == 2 && (S.kg0 + kgl) * 2 + 1 < ph.KC;
+        const bool second = ph.grp == 2 && (P.S.kg0 + kgl) * 2 + 1 < ph.KC;
         if (ph.fmt == kFmtNvfp4) {
           unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
           if (second) unit_nvfp4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
@@ -872,16 +927,21 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         ++issued;
       }
       ++seq;
-      if (++kgl == S.kgn) {
+      if (++kgl == P.S.kgn) {
         kgl = 0;
         ++rb;
       }
     }
     VP_TRACE(lane == 0, p, 2 + warp);
-    if (cur >= 0) flush<NT>(ph, io, prog.M, G, sidx, S, w, ub, ue, cur, acc, acc2, tsc, hb, lane);
-    if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
+    if (cur >= 0) flush<NT>(ph, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
     VP_TRACE(lane == 0, p, 18 + warp);
-    if (p + 1 < prog.n) grid_barrier(io, G, (unsigned)G * (unsigned)(p + 1), sm);
+    if (ph.ks > 1) {  // every row block's slices meet after a grid barrier
+      grid_barrier(io, G, (unsigned)G * ++nbar, sm);
+      cross_slice_fixup<NT>(ph, io, prog.M, G, hb, warp, lane);
+      VP_TRACE(threadIdx.x == 0, p, 35);
+    }
+    if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
+    if (p + 1 < prog.n) grid_barrier(io, G, (unsigned)G * ++nbar, sm);
     VP_TRACE(threadIdx.x == 0, p, 34);
   }
   // Copies still in flight (only after a timeout, when the units are consumed without waiting):

@@ -62,7 +62,6 @@ constexpr int kMiscBytes = 2048;
 constexpr int kSmemBytes = 232448;  // 227 KB: the per-CTA maximum
 constexpr int kXBytes = kSmemBytes - kRingBytes - kMiscBytes;
 constexpr int kMaxGrid = 256;
-constexpr int kWarpsBound = kMaxGrid * kWarps;  // bound on the warps of any slice (fixup slot count)
 
 // Widest K slice whose activations fit in kXBytes (16 NT bytes per k, NT n-tiles of 8 tokens) and
 // that the staging threads hold in registers (128 k per thread of a row): a multiple of 512.
@@ -97,7 +96,6 @@ struct Phase {
   int K, KC;        // reduction length and its chunk count
   int grp, KG;      // chunks per unit (2 plain, 1 interleaved) and groups along K (ceil(KC / grp))
   int RB, rb1;      // virtual row blocks; first row block of w1 (plain; RB if none)
-  int cmax;         // fixup slots per (row block, K slice)
   int8_t fmt, layout, epi, ks;  // ks: K slices
   int8_t x_src, x_rms, out, ss;  // ss: kSsRead | kSsWrite (row-block sums of squares, see Io::rss)
   int x_ld, out_ld, out_cols, trace_slot;
@@ -123,8 +121,11 @@ struct Io {
   unsigned* bar;       // [0] barrier arrivals (monotonic within a launch), [1] CTAs that finished
   unsigned* head_cnt;
   float* head_aux;     // [kMaxGrid][kMaxM][2]
-  unsigned* rb_cnt;    // [max RB]
-  float* partials;     // fixup slots: [RB][ks][cmax][32 lanes][4 NT (plain) or 8 NT (interleaved)]
+  // Split-K partials, in floats of 32 lanes x cs_lane (cs_lane = 4 NT, or 8 NT when the program has an
+  // interleaved phase: its gate and up rows travel together):
+  float* cslots;       // within a CTA: [kMaxGrid][kWarps][2] (a warp's first / last row block)
+  float* xslots;       // across K slices: [RB][ks] (phases with ks > 1)
+  int cs_lane;
   float* rss;          // row-block sums of squares [kMaxM][rss_ld] (or null)
   int rss_ld;
 };
@@ -138,36 +139,21 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t kWsTestSkip = 32;
 
 struct WsLayout {
-  size_t status, bar, head_cnt, head_aux, rb_cnt, partials, total;
+  size_t status, bar, head_cnt, head_aux, cslots, xslots, total;
 };
 
-// max_rb: largest RB of the program's phases; max_slots: largest RB * ks * cmax (in units of
-// 32 lanes x 4 NT floats; an interleaved phase's slots count twice).
-inline WsLayout ws_layout(size_t max_rb, size_t max_slots, int NT) {
+// cs_lane: floats per lane of one partial (4 NT, or 8 NT with an interleaved phase); x_floats: the
+// largest RB * ks * 32 * cs_lane of the program's phases with ks > 1 (0 if none).
+inline WsLayout ws_layout(int cs_lane, size_t x_floats) {
   WsLayout L;
   L.status = 0;
   L.bar = 64;
   L.head_cnt = 128;
   L.head_aux = 256;
-  L.rb_cnt = align_up(L.head_aux + sizeof(float) * 2 * kMaxM * kMaxGrid, 256);
-  L.partials = align_up(L.rb_cnt + sizeof(unsigned) * max_rb, 256);
-  L.total = align_up(L.partials + sizeof(float) * 32 * 4 * (size_t)NT * max_slots, 256);
+  L.cslots = align_up(L.head_aux + sizeof(float) * 2 * kMaxM * kMaxGrid, 256);
+  L.xslots = align_up(L.cslots + sizeof(float) * (size_t)kMaxGrid * kWarps * 2 * 32 * cs_lane, 256);
+  L.total = align_up(L.xslots + sizeof(float) * x_floats, 256);
   return L;
-}
-
-// Fixup slots a phase needs per (row block, K slice): the most warps whose unit ranges can meet one
-// row block's kgn units, for any grid of at most kMaxGrid CTAs (every non-empty warp range holds at
-// least floor(U / kWarpsBound) units).
-inline int phase_cmax(int RB, int KG, int ks) {
-  int cm = 1;
-  for (int s = 0; s < ks; ++s) {
-    const int kgn = (int)((long long)(s + 1) * KG / ks - (long long)s * KG / ks);
-    const long long ufl = (long long)RB * kgn / kWarpsBound;
-    int c = ufl == 0 ? kgn : (int)((kgn + ufl - 1) / ufl) + 1;
-    if (c > kgn) c = kgn;
-    if (c > cm) cm = c;
-  }
-  return cm;
 }
 
 }  // namespace vp

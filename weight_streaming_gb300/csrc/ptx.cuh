@@ -85,6 +85,14 @@ __device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
+// Shared-memory atomic add with acquire-release semantics at CTA scope; returns the old value.  It
+// orders the warp's earlier global stores for the other warps of the CTA without waiting for the
+// SM's outstanding bulk copies (a GPU-scope release waits for them).
+__device__ __forceinline__ unsigned atom_add_acq_rel_cta_smem(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(smem_addr(p)), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

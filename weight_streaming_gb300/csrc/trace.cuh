@@ -2,8 +2,8 @@
 // libverify_trace.so build); in the normal build every hook below is empty.
 //
 // For each phase p of a launch and each CTA, globaltimer stamps (ns): [0] phase start, [1] end of the
-// activation staging, [2 + w] warp w done with its units, [18 + w] warp w done with its row-block
-// fixups (and the head's argmax), [34] grid barrier passed.  Two launch buffers alternate (the
+// activation staging, [2 + w] warp w done with its units, [18 + w] warp w done with its row blocks
+// shared within the CTA, [35] (K-sliced phases) the cross-slice sums done, [34] grid barrier passed.  Two launch buffers alternate (the
 // launch counter's parity), so the two launches of a verify pass keep both halves.
 #pragma once
 #include <cstdint>

@@ -7,8 +7,9 @@ mean over the last pass's phases of (us):
 
   staging        phase start -> activations staged (slowest CTA)
   stream med/max staging done -> a warp's units done (median / slowest warp)
-  fixup tail     last warp's units done -> last warp's fixups done
-  release        last fixup done -> first CTA past the grid barrier
+  fixup tail     last warp's units done -> last warp's row blocks finished within its CTA
+  x-slice        (K-sliced phases) -> grid barrier and the cross-slice sums done (slowest CTA)
+  release        last of those done -> first CTA past the grid barrier
   phase          phase start -> next phase start
 
   python -m weight_streaming_gb300.phase_trace [--layers 16] [--M 8] [--save timeline.npy]
@@ -25,23 +26,27 @@ import sys
 import numpy as np
 
 KINDS = ("mixer in", "mixer out", "gate+up", "down")
-COLS = ("staging", "stream med", "stream max", "fixup tail", "release", "phase")
+COLS = ("staging", "stream med", "stream max", "fixup tail", "x-slice", "release", "phase")
 
 
 def phase_stats(T: np.ndarray, last_of_launch: set) -> dict:
     """Per phase kind, the list of per-phase figures (ns) from stamps T[phase][CTA][slot]: slot 0
-    phase start, 1 staging done, 2..17 each warp's units done, 18..33 each warp's fixups done, 34
-    barrier exit.  The last phase of a launch has no barrier after it (no release / phase figure)."""
+    phase start, 1 staging done, 2..17 each warp's units done, 18..33 each warp's fixups within the
+    CTA done, 34 barrier exit, 35 cross-slice sums done (K-sliced phases; 0 elsewhere).  The last phase of a launch has no barrier after it (no release / phase figure)."""
     n_ph = T.shape[0]
     stats = {}
     for gp in range(n_ph):
         kind = "head" if gp == n_ph - 1 else KINDS[gp % 4]
         S = T[gp]
-        t0, t1, t2, t3, t4 = S[:, 0], S[:, 1], S[:, 2:18], S[:, 18:34], S[:, 34]
+        t0, t1, t2, t3, t4, t5 = S[:, 0], S[:, 1], S[:, 2:18], S[:, 18:34], S[:, 34], S[:, 35]
         d = {"staging": (t1 - t0).max(), "stream med": np.median(t2 - t1[:, None]),
              "stream max": (t2 - t1[:, None]).max(), "fixup tail": t3.max() - t2.max()}
+        done = t3.max()
+        if (t5 > 0).all():  # a K-sliced phase: grid barrier, then the cross-slice sums
+            d["x-slice"] = t5.max() - t3.max()
+            done = t5.max()
         if gp not in last_of_launch:
-            d["release"] = t4.min() - t3.max()
+            d["release"] = t4.min() - done
             d["phase"] = T[gp + 1][:, 0].min() - t0.min()
         stats.setdefault(kind, []).append(d)
     return stats
