@@ -8,11 +8,12 @@ from weight_streaming_gb300.phase_trace import phase_stats, report
 
 
 def stamps(n_ph=5, G=3):
-    T = np.zeros((n_ph, G, 36), np.int64)
+    T = np.zeros((n_ph, G, 37), np.int64)
     for p in range(n_ph):
         base = 100_000 * p
         for c in range(G):
             T[p, c, 0] = base + 10 * c                      # phase start
+            T[p, c, 36] = base + 400 + 100 * c              # loads and statistics done
             T[p, c, 1] = base + 1_000 + 100 * c             # staged: CTA 2 slowest (1,200 after its start 20)
             T[p, c, 2:18] = T[p, c, 1] + 5_000 + np.arange(16) * 10 + 1_000 * (c == 1) * (np.arange(16) == 3)
             T[p, c, 18:34] = T[p, c, 2:18] + 2_000
@@ -26,6 +27,7 @@ def test_phase_stats_figures():
     assert set(st) == {"mixer in", "mixer out", "gate+up", "down", "head"}
     d = st["mixer in"][0]
     assert d["staging"] == 1_180  # CTA 2: 1,200 - 20
+    assert d["stage-ld"] == 580
     assert d["stream max"] == 6_030  # CTA 1, warp 3: 5,000 + 30 + 1,000 after its own staging end
     assert d["stream med"] == np.median(T[0, :, 2:18] - T[0, :, 1:2])
     assert d["fixup tail"] == T[0, :, 18:34].max() - T[0, :, 2:18].max() == 2_000
@@ -41,7 +43,7 @@ def test_report_lists_every_kind_once():
     assert kinds == ["mixer", "mixer", "gate+up", "down", "head"]
     assert lines[-1].startswith("first phase start -> last phase done:")
     head = lines[-2].split()
-    assert head[-2:] == ["-", "-"]
+    assert head[-3:] == ["-", "-", "-"]
 
 
 def test_k_sliced_phase_reports_its_cross_slice_step():

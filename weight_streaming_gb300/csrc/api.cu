@@ -125,7 +125,7 @@ struct Needs {
     if (ph.ks > 1) x_parts = std::max(x_parts, (size_t)ph.RB * ph.ks);
   }
   int cs_lane() const { return 4 * NT * (two ? 2 : 1); }
-  WsLayout layout() const { return ws_layout(cs_lane(), x_parts * 32 * (size_t)cs_lane()); }
+  WsLayout layout(int grid = kMaxGrid) const { return ws_layout(cs_lane(), x_parts * 32 * (size_t)cs_lane(), grid); }
 };
 
 Io make_io(void* ws, const WsLayout& L, int cs_lane) {
@@ -658,12 +658,12 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   s.out_ld = N;
   const int NT = nt_of(M);
   const Phase ph = make_phase(s, NT);
-  const Needs nd = single_needs(ph, NT);
-  const WsLayout L = nd.layout();
-  if (L.total > kNoallocScratchBytes) return VP_ERR_WORKSPACE;  // the shape needs more than the fixed scratch
   int sms = 0;
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
+  const Needs nd = single_needs(ph, NT);
+  const WsLayout L = nd.layout(sms);  // in-CTA slots for this device's grid only
+  if (L.total > kNoallocScratchBytes) return VP_ERR_WORKSPACE;  // the shape needs more than the fixed scratch
   if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != VP_OK) return st;

@@ -230,24 +230,6 @@ __device__ __forceinline__ float sumsq8(uint4 v) {
   return s;
 }
 
-// Reduces x over the T consecutive threads of each row (T a multiple of 16) in a fixed order; every
-// thread of the row gets the result.
-__device__ __forceinline__ float row_reduce(float x, int T, bool is_max, float* red) {
-#pragma unroll
-  for (int o = 8; o; o >>= 1) {
-    const float y = __shfl_xor_sync(0xffffffffu, x, o);
-    x = is_max ? fmaxf(x, y) : x + y;
-  }
-  const int tid = threadIdx.x;
-  if ((tid & 15) == 0) red[tid >> 4] = x;
-  __syncthreads();
-  const int segs = T >> 4, s0 = (tid / T) * segs;
-  float r = red[s0];
-  for (int s = 1; s < segs; ++s) r = is_max ? fmaxf(r, red[s0 + s]) : r + red[s0 + s];
-  __syncthreads();
-  return r;
-}
-
 // Exponent e of a row whose largest magnitude is mx: the row enters the tensor core as x * 2^-e,
 // below 2^15 (f16 holds every bf16 value exactly there, down to 2^-24 of that scale).
 __device__ __forceinline__ int exp_of_max(float mx) {
@@ -259,84 +241,123 @@ __device__ __forceinline__ int exp_of_max(float mx) {
 
 // Stages the CTA's K slice [kbase, kbase + Ks) of the phase's activation rows: x, or
 // bf16(RMSNorm(x)) (unit weight) when the phase asks for it, with the row statistics taken over
-// the whole row.  Thread t handles row n = t / T, 16-byte chunks i, i + T, ... of the slice.
+// the whole row.
+//
+// Work items: (token n, 64-wide k block, its 32-wide half p, h) -> the thread loads the 16-byte chunks
+// k = 32 p + 8 h .. + 7 and 32 p + 16 + 8 h .. + 7 and writes the two whole fragment entries they fill
+// (lanes c = 2 h and 2 h + 1 of token n for k-step pair p: 32 contiguous bytes).  Lane l of a warp
+// takes token 2 (l >> 3) + (l & 1) of an 8-token tile, h = (l >> 1) & 1 and the parity of p
+// (l >> 2) & 1, and writes first the entry c = 2 h + (p & 1): the 8 lanes of a quarter warp then hit
+// 8 different 4-bank groups (token parity x c), so the 16-byte stores have no bank conflicts.  Each
+// warp takes (tile, 64-wide block) pairs warp, warp + 16, ... (at most 5: Ks <= ks_max(NT)).
 template <int NT>
 __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, const Io& io, int kbase, int Ks,
-                                     uint8_t* xs, SmemMisc& sm) {
-  const int tid = threadIdx.x, M = prog.M;
-  const int Mp = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : M <= 16 ? 16 : 32;
-  const int T = kThreads / Mp, n = tid / T, i = tid % T;
-  const bool active = n < M;
-  const uint16_t* row = static_cast<const uint16_t*>(io.buf[ph.x_src]) + (size_t)(active ? n : 0) * ph.x_ld;
-  const int nch = Ks >> 3;
-  const uint32_t xb = smem_addr(xs);
-
-  if (M < 8 * NT) {  // token rows M .. 8 NT - 1 are zero
-    const int per_row = Ks >> 3, zrows = 8 * NT - M;
-    for (int e = tid; e < zrows * per_row; e += kThreads) {
-      const int r = M + e / per_row, q = e % per_row;
-      sts128(xb + xfrag_offset<NT>(q >> 2, r, q & 3), make_uint4(0u, 0u, 0u, 0u));
-    }
-  }
-  // All of the thread's chunks are loaded at once (one memory round trip).
-  uint4 v[16];
-#pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const int q = i + T * m;
-    v[m] = (active && q < nch) ? ldcg128(row + kbase + 8 * q) : make_uint4(0u, 0u, 0u, 0u);
-  }
-  // Row exponent e (the row enters the tensor core as x * 2^-e, below 2^15).  RMSNorm output has
-  // |r| <= sqrt(K) (no element exceeds the root of the row's sum of squares; 1% covers the fp32
-  // 1/rms and the bf16 rounding), so those rows take the exponent of that bound and only their sum
-  // of squares is reduced; other rows take the exponent of their largest magnitude.
+                                        uint8_t* xs, SmemMisc& sm, int trace_phase) {
+  constexpr int kIt = 5;
+  static_assert(NT * ks_max(NT) / 64 <= kIt * kWarps, "every (tile, k block) pair has a warp iteration");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, M = prog.M;
+  const int g = 2 * (lane >> 3) + (lane & 1), h = (lane >> 1) & 1, pp = (lane >> 2) & 1;
+  const int blocks = Ks >> 6, items = NT * blocks;
+  const uint16_t* xsrc = static_cast<const uint16_t*>(io.buf[ph.x_src]);
   const bool rms = ph.x_rms != 0;
-  float stat = 0.0f;
+  uint4 va[kIt], vb[kIt];
+  float stat[NT];
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+  for (int j = 0; j < NT; ++j) stat[j] = 0.0f;
+  // All of the thread's chunks are loaded at once (one memory round trip).
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float a = __uint_as_float(w[k] << 16), b = __uint_as_float(w[k] & 0xFFFF0000u);
-      stat = rms ? fmaf(b, b, fmaf(a, a, stat)) : fmaxf(stat, fmaxf(fabsf(a), fabsf(b)));
-    }
+  for (int it = 0; it < kIt; ++it) {
+    const int item = warp + kWarps * it, tile = item % NT, n = 8 * tile + g, p = 2 * (item / NT) + pp;
+    const bool ok = item < items && n < M;
+    const uint16_t* a = xsrc + (size_t)(ok ? n : 0) * ph.x_ld + kbase + 32 * p + 8 * h;
+    va[it] = ok ? ldcg128(a) : make_uint4(0u, 0u, 0u, 0u);
+    vb[it] = ok ? ldcg128(a + 16) : make_uint4(0u, 0u, 0u, 0u);
   }
-  float inv = 1.0f;
-  int e;
-  if (rms) {
-    bool from_rss = false;
-    if constexpr (NT > 1) from_rss = (ph.ss & kSsRead) && Ks < ph.K && io.rss;
-    if (from_rss) {  // the row's statistic from the producer's row-block sums, in a fixed order
-      stat = 0.0f;
-      if (active)
-        for (int q = i; q < (ph.K >> 4); q += T) stat += __ldcg(io.rss + (size_t)n * io.rss_ld + q);
-    } else if (Ks < ph.K && active) {
-      for (int q = i; q < (ph.K >> 3); q += T) {
-        const int k = 8 * q;
-        if (k < kbase || k >= kbase + Ks) stat += sumsq8(ldcg128(row + k));
+  // The thread's statistic per tile (sum of squares for RMSNorm, else the largest magnitude).
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    const int tile = (warp + kWarps * it) % NT;
+    const uint32_t w[8] = {va[it].x, va[it].y, va[it].z, va[it].w, vb[it].x, vb[it].y, vb[it].z, vb[it].w};
+    float st = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float a = __uint_as_float(w[k] << 16), b = __uint_as_float(w[k] & 0xFFFF0000u);
+      st = rms ? fmaf(b, b, fmaf(a, a, st)) : fmaxf(st, fmaxf(fabsf(a), fabsf(b)));
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+      if (j == tile) stat[j] = rms ? stat[j] + st : fmaxf(stat[j], st);
+  }
+  // The row's statistic, summed in a fixed order (the same in every CTA): per warp over the lanes of
+  // a token (xor 2, 4), then over the warps in order.  Scratch: the start of the activation area,
+  // which the fragments overwrite only after the next barrier.
+  float* red = reinterpret_cast<float*>(xs);  // [kWarps][kMaxM]
+  bool from_rss = false, whole_row = false;
+  if (rms && Ks < ph.K) {
+    if constexpr (NT > 1) from_rss = (ph.ss & kSsRead) && io.rss;
+    whole_row = !from_rss;
+  }
+  if (from_rss || whole_row) {
+    // The statistic of the whole row, not only the slice: lane l of warp w sums token l's 16-wide row
+    // blocks (from the producer's sums of squares) or 8-wide chunks (loaded) w, w + 16, ...
+    float s = 0.0f;
+    if (lane < M) {
+      if (from_rss) {
+        for (int q = warp; q < (ph.K >> 4); q += kWarps) s += __ldcg(io.rss + (size_t)lane * io.rss_ld + q);
+      } else {
+        const uint16_t* row = xsrc + (size_t)lane * ph.x_ld;
+        for (int q = warp; q < (ph.K >> 3); q += kWarps) s += sumsq8(ldcg128(row + 8 * q));
       }
     }
-    const float tot = row_reduce(stat, T, false, sm.red);
-    inv = 1.0f / sqrtf(tot / (float)ph.K + prog.eps);
-    e = exp_of_max(1.01f * sqrtf((float)ph.K));
+    red[warp * kMaxM + lane] = s;
   } else {
-    e = exp_of_max(row_reduce(stat, T, true, sm.red));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float x = stat[j];
+      const float y2 = __shfl_xor_sync(0xffffffffu, x, 2);
+      x = rms ? x + y2 : fmaxf(x, y2);
+      const float y4 = __shfl_xor_sync(0xffffffffu, x, 4);
+      x = rms ? x + y4 : fmaxf(x, y4);
+      // the warp's partial for tile j: its lanes' statistic over the pairs of that tile (zero if none)
+      if ((lane & 6) == 0) red[warp * kMaxM + 8 * j + g] = x;
+    }
+    if (NT * 8 < kMaxM && lane < kMaxM - 8 * NT) red[warp * kMaxM + 8 * NT + lane] = 0.0f;
   }
-  if (active && i == 0) sm.xscale[n] = pow2f(e);
-  if (tid >= M && tid < kMaxM) sm.xscale[tid] = 0.0f;
+  __syncthreads();
+  if (tid < kMaxM) {
+    float tot = 0.0f;
+    for (int w = 0; w < kWarps; ++w) tot = rms ? tot + red[w * kMaxM + tid] : fmaxf(tot, red[w * kMaxM + tid]);
+    int e;
+    float inv = 1.0f;
+    if (rms) {
+      inv = 1.0f / sqrtf(tot / (float)ph.K + prog.eps);
+      // RMSNorm output has |r| <= sqrt(K) (no element exceeds the root of the row's sum of squares;
+      // 1% covers the fp32 1/rms and the bf16 rounding): the exponent of that bound.
+      e = exp_of_max(1.01f * sqrtf((float)ph.K));
+    } else {
+      e = exp_of_max(tot);
+    }
+    sm.xscale[tid] = tid < M ? pow2f(e) : 0.0f;
+    sm.red[tid] = inv;
+    sm.tok[tid] = e;
+  }
+  __syncthreads();
+  VP_TRACE(tid == 0, trace_phase, 36);
   // x * 2^-e exactly (two power-of-two steps when 2^-e is not a normal float); for RMSNorm the
   // 2^-e folds into 1/rms: bf16(x * inv) * 2^-e == bf16(x * (inv * 2^-e)) (no under/overflow).
-  const int ne = -e;
-  float sc1 = ne > 127 ? pow2f(127) : ne < -126 ? pow2f(-126) : pow2f(ne);
-  const float sc2 = ne > 127 ? pow2f(ne - 127) : ne < -126 ? pow2f(ne + 126) : 1.0f;
-  if (rms) sc1 *= inv;
+  const uint32_t xb = smem_addr(xs);
 #pragma unroll
-  for (int m = 0; m < 16; ++m) {
-    const int q = i + T * m;
-    if (!(active && q < nch)) continue;
-    const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
-    uint32_t h[4];
+  for (int it = 0; it < kIt; ++it) {
+    const int item = warp + kWarps * it, tile = item % NT, n = 8 * tile + g, p = 2 * (item / NT) + pp;
+    if (item >= items) continue;
+    const int ne = -sm.tok[n];
+    float sc1 = ne > 127 ? pow2f(127) : ne < -126 ? pow2f(-126) : pow2f(ne);
+    const float sc2 = ne > 127 ? pow2f(ne - 127) : ne < -126 ? pow2f(ne + 126) : 1.0f;
+    if (rms) sc1 *= sm.red[n];
+    const uint32_t w[8] = {va[it].x, va[it].y, va[it].z, va[it].w, vb[it].x, vb[it].y, vb[it].z, vb[it].w};
+    uint32_t o[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 8; ++k) {
       float a = __uint_as_float(w[k] << 16) * sc1, b = __uint_as_float(w[k] & 0xFFFF0000u) * sc1;
       if (rms) {
         const __nv_bfloat162 r = __floats2bfloat162_rn(a, b);  // the RMSNorm output, rounded once
@@ -347,12 +368,19 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
         b *= sc2;
       }
       const __half2 hh = __floats2half2_rn(a, b);
-      h[k] = *reinterpret_cast<const uint32_t*>(&hh);
+      o[k] = *reinterpret_cast<const uint32_t*>(&hh);
     }
-    const int k0 = 8 * q, st = k0 >> 4, hf = (k0 >> 3) & 1;
-    const uint32_t ad = xb + xfrag_offset<NT>(st >> 1, n, 2 * hf) + (st & 1) * 8;
-    sts64(ad, h[0], h[1]);
-    sts64(ad + 16, h[2], h[3]);
+    // entry c = 2h: k = 32p + 8h + 0..3 (chunk a words 0, 1) and 32p + 16 + 8h + 0..3 (chunk b words
+    // 0, 1); entry c = 2h + 1: the upper halves (words 2, 3 of each chunk).
+    const uint32_t e0 = xb + xfrag_offset<NT>(p, n, 2 * h);
+    const uint4 lo = make_uint4(o[0], o[1], o[4], o[5]), hi = make_uint4(o[2], o[3], o[6], o[7]);
+    if (pp) {
+      sts128(e0 + 16, hi);
+      sts128(e0, lo);
+    } else {
+      sts128(e0, lo);
+      sts128(e0 + 16, hi);
+    }
   }
   __syncthreads();
 }
@@ -858,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     const Part P = part_of_cta(ph, G, cta);
     if (threadIdx.x == 0) sm.part = P;  // published by the staging's closing barrier
     const int ck = chunk_k(ph.fmt), kc0 = P.S.kg0 * ph.grp;
-    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm);
+    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm, p);
     VP_TRACE(threadIdx.x == 0, p, 1);
     float tsc[NT][2];
 #pragma unroll

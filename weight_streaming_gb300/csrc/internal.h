@@ -143,15 +143,17 @@ struct WsLayout {
 };
 
 // cs_lane: floats per lane of one partial (4 NT, or 8 NT with an interleaved phase); x_floats: the
-// largest RB * ks * 32 * cs_lane of the program's phases with ks > 1 (0 if none).
-inline WsLayout ws_layout(int cs_lane, size_t x_floats) {
+// largest RB * ks * 32 * cs_lane of the program's phases with ks > 1 (0 if none); grid: the CTAs the
+// in-CTA slots are sized for (kMaxGrid, so that a workspace size does not depend on the device,
+// except where the caller knows the grid).
+inline WsLayout ws_layout(int cs_lane, size_t x_floats, int grid = kMaxGrid) {
   WsLayout L;
   L.status = 0;
   L.bar = 64;
   L.head_cnt = 128;
   L.head_aux = 256;
   L.cslots = align_up(L.head_aux + sizeof(float) * 2 * kMaxM * kMaxGrid, 256);
-  L.xslots = align_up(L.cslots + sizeof(float) * (size_t)kMaxGrid * kWarps * 2 * 32 * cs_lane, 256);
+  L.xslots = align_up(L.cslots + sizeof(float) * (size_t)grid * kWarps * 2 * 32 * cs_lane, 256);
   L.total = align_up(L.xslots + sizeof(float) * x_floats, 256);
   return L;
 }

@@ -3,7 +3,8 @@
 //
 // For each phase p of a launch and each CTA, globaltimer stamps (ns): [0] phase start, [1] end of the
 // activation staging, [2 + w] warp w done with its units, [18 + w] warp w done with its row blocks
-// shared within the CTA, [35] (K-sliced phases) the cross-slice sums done, [34] grid barrier passed.  Two launch buffers alternate (the
+// shared within the CTA, [35] (K-sliced phases) the cross-slice sums done, [34] grid barrier passed,
+// [36] the staging's loads and row statistics done (before the conversion).  Two launch buffers alternate (the
 // launch counter's parity), so the two launches of a verify pass keep both halves.
 #pragma once
 #include <cstdint>
@@ -12,7 +13,7 @@
 
 namespace vp {
 
-constexpr int kTraceSlots = 36;
+constexpr int kTraceSlots = 37;
 
 #ifdef VP_PHASE_TRACE
 __device__ unsigned long long g_trace[2][kMaxPhases][kMaxGrid][kTraceSlots];

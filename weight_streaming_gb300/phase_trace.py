@@ -5,6 +5,7 @@ phase start, end of staging, end of each warp's units and fixups, and the grid b
 csrc/trace.cuh), runs verify passes of a synthetic model on one GPU and prints, per phase kind, the
 mean over the last pass's phases of (us):
 
+  stage-ld       phase start -> the staging's loads and row statistics done (slowest CTA)
   staging        phase start -> activations staged (slowest CTA)
   stream med/max staging done -> a warp's units done (median / slowest warp)
   fixup tail     last warp's units done -> last warp's row blocks finished within its CTA
@@ -26,7 +27,7 @@ import sys
 import numpy as np
 
 KINDS = ("mixer in", "mixer out", "gate+up", "down")
-COLS = ("staging", "stream med", "stream max", "fixup tail", "x-slice", "release", "phase")
+COLS = ("stage-ld", "staging", "stream med", "stream max", "fixup tail", "x-slice", "release", "phase")
 
 
 def phase_stats(T: np.ndarray, last_of_launch: set) -> dict:
@@ -39,7 +40,7 @@ def phase_stats(T: np.ndarray, last_of_launch: set) -> dict:
         kind = "head" if gp == n_ph - 1 else KINDS[gp % 4]
         S = T[gp]
         t0, t1, t2, t3, t4, t5 = S[:, 0], S[:, 1], S[:, 2:18], S[:, 18:34], S[:, 34], S[:, 35]
-        d = {"staging": (t1 - t0).max(), "stream med": np.median(t2 - t1[:, None]),
+        d = {"stage-ld": (S[:, 36] - t0).max(), "staging": (t1 - t0).max(), "stream med": np.median(t2 - t1[:, None]),
              "stream max": (t2 - t1[:, None]).max(), "fixup tail": t3.max() - t2.max()}
         done = t3.max()
         if (t5 > 0).all():  # a K-sliced phase: grid barrier, then the cross-slice sums
@@ -111,7 +112,7 @@ def main(argv=None) -> None:
     n_ph = 4 * args.layers + 1
     per_launch = 160
     launches = (n_ph + per_launch - 1) // per_launch
-    buf = np.zeros((2, per_launch, 256, 36), np.uint64)
+    buf = np.zeros((2, per_launch, 256, 37), np.uint64)  # kTraceSlots stamps per phase and CTA
     done = V.vp_trace_read(M, buf)
     G = torch.cuda.get_device_properties(0).multi_processor_count
     rows = []  # the last pass: launch l holds phases [l * n / launches, (l + 1) * n / launches)
