@@ -298,18 +298,38 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
     whole_row = !from_rss;
   }
   if (from_rss || whole_row) {
-    // The statistic of the whole row, not only the slice: lane l of warp w sums token l's 16-wide row
-    // blocks (from the producer's sums of squares) or 8-wide chunks (loaded) w, w + 16, ...
-    float s = 0.0f;
-    if (lane < M) {
+    // The statistic of the whole row, not only the slice: thread 16 n + i sums its share of token n's
+    // row -- the producer's 16-wide row-block sums of squares, or the row itself -- with 8 loads in
+    // flight at a time, then a fixed xor tree over the token's 16 threads.
+    const int n = tid >> 4, i = tid & 15;
+    float sum = 0.0f;
+    if (n < M) {
       if (from_rss) {
-        for (int q = warp; q < (ph.K >> 4); q += kWarps) s += __ldcg(io.rss + (size_t)lane * io.rss_ld + q);
+        const float4* r4 = reinterpret_cast<const float4*>(io.rss + (size_t)n * io.rss_ld);
+        const int nq = ph.K >> 6;
+        for (int q0 = i; q0 < nq; q0 += 16 * 8) {
+          float4 a[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            a[k] = q0 + 16 * k < nq ? __ldcg(r4 + q0 + 16 * k) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sum += (a[k].x + a[k].y) + (a[k].z + a[k].w);
+        }
       } else {
-        const uint16_t* row = xsrc + (size_t)lane * ph.x_ld;
-        for (int q = warp; q < (ph.K >> 3); q += kWarps) s += sumsq8(ldcg128(row + 8 * q));
+        const uint16_t* row = xsrc + (size_t)n * ph.x_ld;
+        const int nq = ph.K >> 3;
+        for (int q0 = i; q0 < nq; q0 += 16 * 8) {
+          uint4 a[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) a[k] = q0 + 16 * k < nq ? ldcg128(row + 8 * (q0 + 16 * k)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sum += sumsq8(a[k]);
+        }
       }
     }
-    red[warp * kMaxM + lane] = s;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (i == 0) red[n] = sum;
   } else {
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
@@ -326,7 +346,10 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
   __syncthreads();
   if (tid < kMaxM) {
     float tot = 0.0f;
-    for (int w = 0; w < kWarps; ++w) tot = rms ? tot + red[w * kMaxM + tid] : fmaxf(tot, red[w * kMaxM + tid]);
+    if (from_rss || whole_row)
+      tot = red[tid];
+    else
+      for (int w = 0; w < kWarps; ++w) tot = rms ? tot + red[w * kMaxM + tid] : fmaxf(tot, red[w * kMaxM + tid]);
     int e;
     float inv = 1.0f;
     if (rms) {
@@ -509,115 +532,119 @@ struct HeadBest {
   int i[NT][2];
 };
 
-// Residual inputs h[t][n] of the thread's elements of row block rb (plain layout), element
-// [j][2r + h] = row g + 8r, token 8j + 2c + h.
-template <int NT>
-__device__ __forceinline__ void load_resid(const Phase& ph, const Io& io, int M, int rb, uint16_t (&hold)[NT][4],
-                                           int lane) {
+// Residual inputs h[t][n] of the thread's elements of row block rb (plain layout) for token tile j:
+// element [2r + h] = row g + 8r, token 8j + 2c + h.
+__device__ __forceinline__ void load_resid_tile(const Phase& ph, const Io& io, int M, int rb, int j, uint16_t (&hold)[4],
+                                                int lane) {
   const int g = lane >> 2, c = lane & 3;
   const uint16_t* hp = static_cast<const uint16_t*>(io.buf[ph.out]);
   const int nb = rb * kRowBlock + g;
 #pragma unroll
-  for (int j = 0; j < NT; ++j)
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int r = 0; r < 2; ++r) {
+      const int t = 8 * j + 2 * c + h;
+      unsigned short b = 0;
+      if (t < M) asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(b) : "l"(hp + (size_t)t * ph.out_ld + nb + 8 * r));
+      hold[2 * r + h] = b;
+    }
+}
+template <int NT>
+__device__ __forceinline__ void load_resid(const Phase& ph, const Io& io, int M, int rb, uint16_t (&hold)[NT][4],
+                                           int lane) {
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = 8 * j + 2 * c + h;
-        unsigned short b = 0;
-        if (t < M) asm volatile("ld.global.cg.u16 %0, [%1];" : "=h"(b) : "l"(hp + (size_t)t * ph.out_ld + nb + 8 * r));
-        hold[j][2 * r + h] = b;
-      }
+  for (int j = 0; j < NT; ++j) load_resid_tile(ph, io, M, rb, j, hold[j], lane);
 }
 
-// v: the finished row block (fp32, un-scaled activations, before the weight scale); interleaved
-// layout: v = the gate rows, u = the up rows (else u is unused).
+// Token tile j of the finished row block rb: v (fp32, un-scaled activations, before the weight
+// scale); interleaved layout: v = the gate rows, u = the up rows (else u is unused).
 template <int NT>
-__device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const float (&v)[NT][4],
-                         const float (&u)[NT][4], const uint16_t (&hold)[NT][4], HeadBest<NT>& hb, int lane) {
+__device__ __forceinline__ void epilogue_tile(const Phase& ph, const Io& io, int M, int rb, int j, const float (&v)[4],
+                                              const float (&u)[4], const uint16_t (&hold)[4], HeadBest<NT>& hb,
+                                              int lane) {
   const int g = lane >> 2, c = lane & 3;
   if (ph.layout == kInterleaved) {  // a = bf16(silu(s0 * gate) * s1 * up)
     uint16_t* out = static_cast<uint16_t*>(io.buf[ph.out]);
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int t = 8 * j + 2 * c + h;
-        if (t >= M) continue;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int f = rb * kRowBlock + g + 8 * r;
-          const float gt = ph.s0 * v[j][2 * r + h], up = ph.s1 * u[j][2 * r + h];
-          out[(size_t)t * ph.out_ld + f] = bf16_bits(gt / (1.0f + expf(-gt)) * up);
-        }
-      }
-    return;
-  }
-  const bool seg1 = rb >= ph.rb1;
-  const float s = seg1 ? ph.s1 : ph.s0;
-  const int nb = (seg1 ? rb - ph.rb1 : rb) * kRowBlock + g;
-  float sq[NT][2];  // kSsWrite: this lane's squares of the stored values, per token
-#pragma unroll
-  for (int j = 0; j < NT; ++j) sq[j][0] = sq[j][1] = 0.0f;
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int t = 8 * j + 2 * c + h;
       if (t >= M) continue;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const int n = nb + 8 * r;
-        const float val = s * v[j][2 * r + h];
-        const size_t o = (size_t)t * ph.out_ld + n;
-        switch (ph.epi) {
-          case kEpiF32:
-            static_cast<float*>(io.buf[ph.out])[o] = val;
-            break;
-          case kEpiZ:
-            if (!seg1 && n < ph.out_cols) static_cast<uint16_t*>(io.buf[ph.out])[o] = bf16_bits(val);
-            break;
-          case kEpiResid: {
-            uint16_t* hp = static_cast<uint16_t*>(io.buf[ph.out]);
-            const uint16_t nv = bf16_bits(bf16_bits_to_float(hold[j][2 * r + h]) + val);
-            hp[o] = nv;
-            if constexpr (NT > 1) {
-              const float f = bf16_bits_to_float(nv);
-              sq[j][h] = fmaf(f, f, sq[j][h]);
-            }
-            if (ph.trace_slot >= 0 && io.buf[kBufTrace])
-              static_cast<uint16_t*>(io.buf[kBufTrace])[(size_t)ph.trace_slot * io.trace_stride + o] = nv;
-            break;
-          }
-          case kEpiHead: {
-            if (io.buf[kBufLogits]) static_cast<float*>(io.buf[kBufLogits])[o] = val;
-            const float key = isnan(val) ? -INFINITY : val;
-            if (am_better(key, n, hb.v[j][h], hb.i[j][h])) {
-              hb.v[j][h] = key;
-              hb.i[j][h] = n;
-            }
-            break;
-          }
-          default:
-            break;
-        }
+        const int f = rb * kRowBlock + g + 8 * r;
+        const float gt = ph.s0 * v[2 * r + h], up = ph.s1 * u[2 * r + h];
+        out[(size_t)t * ph.out_ld + f] = bf16_bits(gt / (1.0f + expf(-gt)) * up);
       }
     }
+    return;
+  }
+  const bool seg1 = rb >= ph.rb1;
+  const float s = seg1 ? ph.s1 : ph.s0;
+  const int nb = (seg1 ? rb - ph.rb1 : rb) * kRowBlock + g;
+  float sq[2] = {0.0f, 0.0f};  // kSsWrite: this lane's squares of the stored values, per token
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int t = 8 * j + 2 * c + h;
+    if (t >= M) continue;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int n = nb + 8 * r;
+      const float val = s * v[2 * r + h];
+      const size_t o = (size_t)t * ph.out_ld + n;
+      switch (ph.epi) {
+        case kEpiF32:
+          static_cast<float*>(io.buf[ph.out])[o] = val;
+          break;
+        case kEpiZ:
+          if (!seg1 && n < ph.out_cols) static_cast<uint16_t*>(io.buf[ph.out])[o] = bf16_bits(val);
+          break;
+        case kEpiResid: {
+          uint16_t* hp = static_cast<uint16_t*>(io.buf[ph.out]);
+          const uint16_t nv = bf16_bits(bf16_bits_to_float(hold[2 * r + h]) + val);
+          hp[o] = nv;
+          if constexpr (NT > 1) {
+            const float f = bf16_bits_to_float(nv);
+            sq[h] = fmaf(f, f, sq[h]);
+          }
+          if (ph.trace_slot >= 0 && io.buf[kBufTrace])
+            static_cast<uint16_t*>(io.buf[kBufTrace])[(size_t)ph.trace_slot * io.trace_stride + o] = nv;
+          break;
+        }
+        case kEpiHead: {
+          if (io.buf[kBufLogits]) static_cast<float*>(io.buf[kBufLogits])[o] = val;
+          const float key = isnan(val) ? -INFINITY : val;
+          if (am_better(key, n, hb.v[j][h], hb.i[j][h])) {
+            hb.v[j][h] = key;
+            hb.i[j][h] = n;
+          }
+          break;
+        }
+        default:
+          break;
+      }
+    }
+  }
   if constexpr (NT > 1) {
     if (ph.epi == kEpiResid && (ph.ss & kSsWrite)) {  // the row block's 16 rows: lanes g = 0..7 (xor 4, 8, 16)
 #pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float v = sq[j][h];
-          v += __shfl_xor_sync(0xffffffffu, v, 4);
-          v += __shfl_xor_sync(0xffffffffu, v, 8);
-          v += __shfl_xor_sync(0xffffffffu, v, 16);
-          const int t = 8 * j + 2 * c + h;
-          if (g == 0 && t < M) io.rss[(size_t)t * io.rss_ld + (seg1 ? rb - ph.rb1 : rb)] = v;
-        }
+      for (int h = 0; h < 2; ++h) {
+        float q = sq[h];
+        q += __shfl_xor_sync(0xffffffffu, q, 4);
+        q += __shfl_xor_sync(0xffffffffu, q, 8);
+        q += __shfl_xor_sync(0xffffffffu, q, 16);
+        const int t = 8 * j + 2 * c + h;
+        if (g == 0 && t < M) io.rss[(size_t)t * io.rss_ld + (seg1 ? rb - ph.rb1 : rb)] = q;
+      }
     }
   }
+}
+
+// The finished row block rb, every token tile.
+template <int NT>
+__device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const float (&v)[NT][4],
+                         const float (&u)[NT][4], const uint16_t (&hold)[NT][4], HeadBest<NT>& hb, int lane) {
+#pragma unroll
+  for (int j = 0; j < NT; ++j) epilogue_tile<NT>(ph, io, M, rb, j, v[j], u[j], hold[j], hb, lane);
 }
 
 // Stores one partial (this lane's v and, interleaved, u) at slot address sl.
@@ -700,41 +727,42 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int w, int rb
   epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
 }
 
-// Phases with several K slices, after the grid barrier that follows the units: row block rb is
-// summed over its slices in slice order (by one warp; consecutive row blocks go to different CTAs)
-// and runs its epilogue.
+// Phases with several K slices, after the grid barrier that follows the units: token tile j of
+// row block rb is summed over its slices in slice order by one warp (items (rb, j) spread over the
+// CTAs first), its slice partials loaded 8 slices at a time, then its epilogue runs.
 template <int NT>
 __device__ void cross_slice_fixup(const Phase& ph, const Io& io, int M, int G, HeadBest<NT>& hb, int warp,
                                   int lane) {
   const bool two = ph.layout == kInterleaved;
-  const int per_lane = io.cs_lane;
-  for (int rb = warp * G + (int)blockIdx.x; rb < ph.RB; rb += G * kWarps) {
-    float v[NT][4], u[NT][4];
+  const int per_lane = io.cs_lane, ks = ph.ks;
+  for (int item = warp * G + (int)blockIdx.x; item < ph.RB * NT; item += G * kWarps) {
+    const int rb = item / NT, j = item - rb * NT;
+    uint16_t hold[4];
+    if (ph.epi == kEpiResid) load_resid_tile(ph, io, M, rb, j, hold, lane);
+    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f}, u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    const float* base = io.xslots + ((size_t)rb * ks * 32 + lane) * per_lane + 4 * j;
+    for (int s0 = 0; s0 < ks; s0 += 8) {
+      float4 q[8], q2[8];
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+      for (int i = 0; i < 8; ++i) {
+        const float* sl = base + (size_t)(s0 + i) * 32 * per_lane;
+        q[i] = s0 + i < ks ? ldcg_f4(sl) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        q2[i] = two && s0 + i < ks ? ldcg_f4(sl + 4 * NT) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
-    uint16_t hold[NT][4];
-    if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
-    for (int s = 0; s < ph.ks; ++s) {
-      const float* sl = io.xslots + (((size_t)rb * ph.ks + s) * 32 + lane) * per_lane;
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float4 q = ldcg_f4(sl + 4 * j);
-        v[j][0] += q.x;
-        v[j][1] += q.y;
-        v[j][2] += q.z;
-        v[j][3] += q.w;
-        if (two) {
-          const float4 q2 = ldcg_f4(sl + 4 * (NT + j));
-          u[j][0] += q2.x;
-          u[j][1] += q2.y;
-          u[j][2] += q2.z;
-          u[j][3] += q2.w;
-        }
+      for (int i = 0; i < 8; ++i) {
+        if (s0 + i >= ks) break;
+        v[0] += q[i].x;
+        v[1] += q[i].y;
+        v[2] += q[i].z;
+        v[3] += q[i].w;
+        u[0] += q2[i].x;
+        u[1] += q2[i].y;
+        u[2] += q2[i].z;
+        u[3] += q2[i].w;
       }
     }
-    epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
+    epilogue_tile<NT>(ph, io, M, rb, j, v, u, hold, hb, lane);
   }
 }
 
