@@ -647,13 +647,18 @@ __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const flo
   for (int j = 0; j < NT; ++j) epilogue_tile<NT>(ph, io, M, rb, j, v[j], u[j], hold[j], hb, lane);
 }
 
-// Stores one partial (this lane's v and, interleaved, u) at slot address sl.
+// A partial of a row block (one slot: 32 lanes x cs_lane floats) is laid out token tile major:
+// sub-block j (v) and NT + j (u, interleaved) of 32 lanes x 4 floats each, so that one tile's 32
+// lanes read or write 512 contiguous bytes.  slot: the slot's first float; this lane's float4 of
+// sub-block b is at slot + (32 b + lane) * 4.
 template <int NT>
-__device__ __forceinline__ void store_partial(float* sl, bool two, const float (&v)[NT][4], const float (&u)[NT][4]) {
+__device__ __forceinline__ void store_partial(float* slot, int lane, bool two, const float (&v)[NT][4],
+                                              const float (&u)[NT][4]) {
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
-    *reinterpret_cast<float4*>(sl + 4 * j) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
-    if (two) *reinterpret_cast<float4*>(sl + 4 * (NT + j)) = make_float4(u[j][0], u[j][1], u[j][2], u[j][3]);
+    *reinterpret_cast<float4*>(slot + (32 * j + lane) * 4) = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+    if (two)
+      *reinterpret_cast<float4*>(slot + (32 * (NT + j) + lane) * 4) = make_float4(u[j][0], u[j][1], u[j][2], u[j][3]);
   }
 }
 
@@ -679,13 +684,16 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int w, int rb
       v[j][r] = (two ? acc[j][r] : acc[j][r] + acc2[j][r]) * sc;
       u[j][r] = two ? acc2[j][r] * sc : 0.0f;
     }
-  const int per_lane = io.cs_lane;
+  const size_t slot_floats = 32 * (size_t)io.cs_lane;
   const int kgn = P.S.kgn, r0 = (rb - P.rb0) * kgn;
   const int wf = wowner(P, r0), wl = wowner(P, r0 + kgn - 1);
+  // The residual inputs of a row block this warp finishes, loaded ahead of the partials' round trip.
+  uint16_t hold[NT][4];
+  const bool resid = ph.ks == 1 && ph.epi == kEpiResid;
+  if (resid && wf == wl) load_resid<NT>(ph, io, M, rb, hold, lane);
   if (wf != wl) {
     const size_t cta_slots = (size_t)blockIdx.x * kWarps * 2;
-    store_partial<NT>(io.cslots + ((cta_slots + 2 * w + (wbegin(P, w) >= r0 ? 0 : 1)) * 32 + lane) * per_lane, two, v,
-                      u);
+    store_partial<NT>(io.cslots + (cta_slots + 2 * w + (wbegin(P, w) >= r0 ? 0 : 1)) * slot_floats, lane, two, v, u);
     // Release (CTA scope): the warp's stores, ordered before by the warp barrier, are visible to the
     // warp that finishes the row block; acquire: that warp then sees every contributor's partial.
     __syncwarp();
@@ -694,21 +702,22 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int w, int rb
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old + 1 != (unsigned)(wl - wf + 1)) return;
     __syncwarp();
+    if (resid) load_resid<NT>(ph, io, M, rb, hold, lane);
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
       for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
     for (int c = wf; c <= wl; ++c) {
-      const float* sl = io.cslots + ((cta_slots + 2 * c + (wbegin(P, c) >= r0 ? 0 : 1)) * 32 + lane) * per_lane;
+      const float* sl = io.cslots + (cta_slots + 2 * c + (wbegin(P, c) >= r0 ? 0 : 1)) * slot_floats + lane * 4;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const float4 q = *reinterpret_cast<const float4*>(sl + 4 * j);
+        const float4 q = *reinterpret_cast<const float4*>(sl + 128 * j);
         v[j][0] += q.x;
         v[j][1] += q.y;
         v[j][2] += q.z;
         v[j][3] += q.w;
         if (two) {
-          const float4 q2 = *reinterpret_cast<const float4*>(sl + 4 * (NT + j));
+          const float4 q2 = *reinterpret_cast<const float4*>(sl + 128 * (NT + j));
           u[j][0] += q2.x;
           u[j][1] += q2.y;
           u[j][2] += q2.z;
@@ -719,11 +728,9 @@ __device__ void flush(const Phase& ph, const Io& io, int M, int G, int w, int rb
     if (lane == 0) sm.tcnt[wf] = 0u;
   }
   if (ph.ks > 1) {
-    store_partial<NT>(io.xslots + (((size_t)rb * ph.ks + P.sidx) * 32 + lane) * per_lane, two, v, u);
+    store_partial<NT>(io.xslots + ((size_t)rb * ph.ks + P.sidx) * slot_floats, lane, two, v, u);
     return;
   }
-  uint16_t hold[NT][4];
-  if (ph.epi == kEpiResid) load_resid<NT>(ph, io, M, rb, hold, lane);
   epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
 }
 
@@ -734,20 +741,21 @@ template <int NT>
 __device__ void cross_slice_fixup(const Phase& ph, const Io& io, int M, int G, HeadBest<NT>& hb, int warp,
                                   int lane) {
   const bool two = ph.layout == kInterleaved;
-  const int per_lane = io.cs_lane, ks = ph.ks;
+  const size_t slot_floats = 32 * (size_t)io.cs_lane;
+  const int ks = ph.ks;
   for (int item = warp * G + (int)blockIdx.x; item < ph.RB * NT; item += G * kWarps) {
     const int rb = item / NT, j = item - rb * NT;
     uint16_t hold[4];
     if (ph.epi == kEpiResid) load_resid_tile(ph, io, M, rb, j, hold, lane);
     float v[4] = {0.0f, 0.0f, 0.0f, 0.0f}, u[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    const float* base = io.xslots + ((size_t)rb * ks * 32 + lane) * per_lane + 4 * j;
+    const float* base = io.xslots + (size_t)rb * ks * slot_floats + (32 * j + lane) * 4;
     for (int s0 = 0; s0 < ks; s0 += 8) {
       float4 q[8], q2[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float* sl = base + (size_t)(s0 + i) * 32 * per_lane;
+        const float* sl = base + (size_t)(s0 + i) * slot_floats;
         q[i] = s0 + i < ks ? ldcg_f4(sl) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        q2[i] = two && s0 + i < ks ? ldcg_f4(sl + 4 * NT) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        q2[i] = two && s0 + i < ks ? ldcg_f4(sl + 128 * NT) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
