@@ -37,9 +37,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-components", action="store_true", help="skip the one-MLP-layer and head+accept figures")
     ap.add_argument("--layers", type=int, default=64)
     ap.add_argument("--kernel", default=None, choices=["gate", "down", "gdn_in", "head", "q4_gate", "q4_down", "q4_head", "sample", "attn",
-                             "gdn", "decode"],
+                             "gdn", "decode", "mlp", "head_accept", "pass"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
     ap.add_argument("--ctx", type=int, default=32768, help="context length per lane for --kernel attn")
@@ -443,6 +444,109 @@ def run_decode(args):
                       "history_tokens_at_start": T0, "max_match": mm}), flush=True)
 
 
+def measure_mlp_layer(M_list, steps: int, warmup: int, copies: int = 4) -> dict:
+    """One MLP layer of the pass (RMSNorm, gate + up with SiLU(gate) * up, down with the residual) through
+    vp_verify_blocks, as the pass runs it, rotating over `copies` layers' weights (> L2, so every call
+    streams from DRAM); per M: microseconds per layer and weight GB/s (150,405,120 B per layer)."""
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    from weight_streaming_gb300.geometry import Geometry
+    from weight_streaming_gb300.model import SyntheticModel
+    geom = Geometry(n_layers=copies)
+    sm = SyntheticModel(geom, seed=0)
+    H, I = geom.hidden, geom.inter
+    nbytes = 3 * I * H * 9 // 16
+    out = {}
+    for M in M_list:
+        h = torch.from_numpy(synth.normal_bf16(M, synth.stream_id(0, synth.T_X0), (M, H)).view("int16"))
+        h = h.cuda().view(torch.bfloat16)
+        ws = torch.zeros(V.vp_pass_workspace_bytes(sm.model, M), dtype=torch.uint8, device="cuda")
+
+        def calls():  # the MLP block (2l + 1) of every copy
+            for l in range(copies):
+                V.vp_verify_blocks(sm.model, h, M, 2 * l + 1, 2 * l + 2, None, ws)
+        t = graph_time(calls, steps, warmup) / copies
+        assert V.vp_read_status(ws) == V.VP_OK
+        out[f"M{M}"] = {"us_per_layer": t * 1e6, "gbps": nbytes / t / 1e9}
+    del sm
+    torch.cuda.empty_cache()
+    return {"workload": f"one MLP layer (gate, up [5120->17408], down [17408->5120] NVFP4) as the pass runs it, "
+                        f"{copies} rotating copies", "bytes_per_layer": nbytes, **out}
+
+
+def measure_head_accept(lanes_list, steps: int, warmup: int) -> dict:
+    """The NVFP4 vocabulary head [5120 -> 248320] fused with argmax and greedy acceptance
+    (vp_head_argmax_accept) at M = 8 lanes, planted draft prefixes of 0..7; per lane count: microseconds
+    per call and weight GB/s (715,161,600 B; larger than L2, so every call streams from DRAM)."""
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    from weight_streaming_gb300.model import pack_nvfp4
+    V_, K = 248320, 5120
+    c = torch.empty((V_, K // 2), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((V_, K // 16), dtype=torch.uint8, device="cuda")
+    synth.gpu_uniform_bytes(c, 0, synth.stream_id(synth.HEAD_LAYER, synth.T_HEAD_C))
+    synth.gpu_scale_codes(sc, 0, synth.stream_id(synth.HEAD_LAYER, synth.T_HEAD_S))
+    w = pack_nvfp4(c, sc)
+    del c, sc
+    nbytes = V_ * K * 9 // 16
+    out = {}
+    for L in lanes_list:
+        M = 8 * L
+        x = torch.from_numpy(synth.normal_bf16(M, synth.stream_id(0, synth.T_X0), (M, K)).view("int16"))
+        x = x.cuda().view(torch.bfloat16)
+        t_ref = synth.uniform_ints(M, synth.stream_id(0, synth.T_PENDING) + 7, 0, M, V_)
+        pending, planted = synth.planted_pending(M, t_ref, V_)
+        pend = torch.from_numpy(pending).cuda()
+        am = torch.empty(M, dtype=torch.int32, device="cuda")
+        nc = torch.empty(L, dtype=torch.int32, device="cuda")
+        cm = torch.empty((L, 8), dtype=torch.int32, device="cuda")
+        ws = torch.zeros(V.vp_workspace_bytes(V.VP_OP_HEAD, M, V_, K), dtype=torch.uint8, device="cuda")
+
+        def call():
+            V.vp_head_argmax_accept(w, 1.0, x, M, V_, K, pend, am, nc, cm, None, ws)
+        t = graph_time(call, steps, warmup)
+        n = nc.cpu().numpy()
+        assert (n >= 1).all() and (n <= 8).all() and V.vp_read_status(ws) == V.VP_OK
+        out[f"L{L}"] = {"M": M, "us_per_call": t * 1e6, "gbps": nbytes / t / 1e9,
+                        "planted_prefixes": [int(p) for p in planted]}
+    del w
+    torch.cuda.empty_cache()
+    return {"workload": "NVFP4 head [5120->248320] + argmax (lowest index) + greedy accept", "bytes": nbytes, **out}
+
+
+def run_pass_only(args):
+    """The verify pass alone (--layers layers, --M rows), CUDA-graph replays with nothing else on the
+    device: a small case for profiling; prints one JSON line with the time per pass and weight GB/s."""
+    import numpy as np
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    from weight_streaming_gb300.geometry import Geometry
+    from weight_streaming_gb300.model import SyntheticModel
+    geom = Geometry(n_layers=args.layers)
+    sm = SyntheticModel(geom, seed=0)
+    M, H = args.M, geom.hidden
+    x0 = torch.from_numpy(synth.normal_bf16(0, synth.stream_id(0, synth.T_X0), (M, H)).view(np.int16))
+    x0 = x0.cuda().view(torch.bfloat16)
+    t = synth.uniform_ints(0, synth.stream_id(0, synth.T_PENDING) + 7, 0, M, geom.vocab)
+    pend = torch.from_numpy(synth.planted_pending(0, t, geom.vocab)[0]).cuda()
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    nc = torch.empty(M // 8, dtype=torch.int32, device="cuda")
+    cm = torch.empty((M // 8, 8), dtype=torch.int32, device="cuda")
+    ws = sm.workspace(M)
+    tp = graph_time(lambda: sm.run(x0, pend, am, nc, cm, ws), args.steps, args.warmup)
+    assert V.vp_read_status(ws) == V.VP_OK
+    nbytes = geom.pass_bytes()
+    print(json.dumps({"kernel": "pass", "layers": args.layers, "M": M, "ms_per_pass": tp * 1e3,
+                      "gbps": nbytes / tp / 1e9, "bytes_per_pass": nbytes,
+                      "launches_per_pass": sm.launch_count()}), flush=True)
+
+
 def run_kernel(args):
     """One GEMM of the pass alone through the C ABI, rotating over 4 weight copies (> L2) so every
     launch streams from DRAM; prints one JSON line with the average launch time and GB/s."""
@@ -458,6 +562,15 @@ def run_kernel(args):
         return
     if args.kernel == "attn":
         run_attn(args)
+        return
+    if args.kernel == "pass":
+        run_pass_only(args)
+        return
+    if args.kernel == "mlp":
+        print(json.dumps({"kernel": "mlp", **measure_mlp_layer([1, 8, 16, 24, 32], args.steps, args.warmup)}), flush=True)
+        return
+    if args.kernel == "head_accept":
+        print(json.dumps({"kernel": "head_accept", **measure_head_accept([1, 4], args.steps, args.warmup)}), flush=True)
         return
 
     import synth
@@ -598,6 +711,14 @@ def main():
         del g
     also["M8"] = {"gbps": value / world, "ms_per_pass": ms8, "passes_per_s": 1e3 / ms8,
                   "implied_tok_s": 4.8 / (ms8 / 1e3)}
+    # run-to-run spread of the headline: the same graph timed in three more runs of K steps
+    runs = [ms8] + [1e3 * time_graph(g8, s8, args.steps, 3) / args.steps for _ in range(3)]
+    srt = sorted(runs)
+    also["M8_runs_ms_per_pass"] = {"runs": runs, "min": srt[0], "median": 0.5 * (srt[1] + srt[2]), "max": srt[-1]}
+    # the per-component workloads: one MLP layer at M = 1 .. 32, and the head with acceptance at 1 / 4 lanes
+    if not args.no_components:
+        also["config_mlp_layer"] = measure_mlp_layer([1, 8, 16, 24, 32], max(5, args.steps), 3)
+        also["config_head_accept"] = measure_head_accept([1, 4], max(5, args.steps), 3)
 
     # ---- dominant kernel: the pass is two launches of one persistent kernel (exec_kernel<1, 0> at M = 8,
     # 4 phases per layer + the head); its algorithmic bytes are the pass's weight bytes, its duration

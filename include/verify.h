@@ -325,7 +325,8 @@ vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_d
                           int n_layers, const vp_head_desc* head, vp_model** out);
 void vp_model_destroy(vp_model* model);
 
-/* Workspace bytes for vp_verify_pass at M rows (0 if invalid). */
+/* Workspace bytes for vp_verify_pass (M = 8 * lanes) or vp_verify_blocks (M = 1..32) at M rows (0 if
+ * invalid). */
 size_t vp_pass_workspace_bytes(const vp_model* model, int M);
 
 /* One verify pass.  x0: bf16 [M][hidden] (the rows' input hidden states, read-only); pending,
@@ -338,8 +339,9 @@ vp_status vp_verify_pass(const vp_model* model, const void* x0, int M, const int
                          float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16
- * [M][hidden], updated in place); block 2l is the mixer block of layer l and block 2l + 1 its MLP
- * block, computed exactly as inside vp_verify_pass (the same phases of the same kernel).
+ * [M][hidden], M = 1..32: no acceptance runs, so M need not be whole lanes; updated in place); block
+ * 2l is the mixer block of layer l and block 2l + 1 its MLP block, computed exactly as inside
+ * vp_verify_pass (the same phases of the same kernel).
  * trace: optional bf16 [block_end - block_begin][M][hidden], h after each block.  Lets a
  * caller run part of the stream, or check one block against a reference from a known input. */
 vp_status vp_verify_blocks(const vp_model* model, void* h, int M, int block_begin, int block_end, void* trace,
@@ -353,10 +355,12 @@ int vp_pass_launch_count(const vp_model* model);
 /* The executor's phase timeline (no counterpart in the pages: a measurement aid).  Only a library
  * built with VP_PHASE_TRACE (libverify_trace.so) records it; any other build returns
  * VP_ERR_UNSUPPORTED.  Copies up to `bytes` of the timeline of the kernels that serve M rows into the
- * host buffer dst: uint64 [2][160][256][36], indexed [launch parity][phase of the launch][CTA][slot]
- * with globaltimer stamps in ns -- slot 0 phase start, 1 end of the activation staging, 2 + w warp w
- * done with its units, 18 + w warp w done with its fixups, 34 grid barrier passed -- and the number
- * of multi-phase launches completed so far into *launches (a launch writes buffer launches % 2).
+ * host buffer dst: uint64 [2][160][256][37], indexed [launch parity][phase of the launch][CTA][slot]
+ * with globaltimer stamps in ns -- slot 0 phase start, 36 the staging's loads and row statistics
+ * done, 1 end of the activation staging, 2 + w warp w done with its units, 18 + w warp w done with
+ * the row blocks it shares within its CTA, 35 (K-sliced phases) the cross-slice sums done, 34 grid
+ * barrier passed -- and the number of multi-phase launches completed so far into *launches (a
+ * launch writes buffer launches % 2).
  * Synchronous (waits for the device). */
 vp_status vp_trace_read(int M, void* dst, size_t bytes, unsigned* launches);
 

@@ -232,7 +232,13 @@ def test_model_create_validation_without_gpu(V):
     m = V.vp_model(256, 512, 1e-6, [_layer(V), _layer(V, 1, 384, 256, 128)], head)
     assert V.vp_pass_launch_count(m) == 1  # 9 phases: one executor launch
     assert V.vp_pass_workspace_bytes(m, 8) > 0
-    assert V.vp_pass_workspace_bytes(m, 12) == 0
+    assert V.vp_pass_workspace_bytes(m, 1) > 0 and V.vp_pass_workspace_bytes(m, 12) > 0  # block runs take any M
+    assert V.vp_pass_workspace_bytes(m, 0) == 0 and V.vp_pass_workspace_bytes(m, 33) == 0
+    L = V.lib()
+    ws_fake = 1 << 20  # never dereferenced: the row count is checked first
+    # the pass itself needs whole lanes of 8 rows
+    assert L.vp_verify_pass(m.handle, FAKE, 12, FAKE, FAKE, FAKE, FAKE, None, None, ws_fake,
+                            V.vp_pass_workspace_bytes(m, 12), None) == V.VP_ERR_SHAPE
     m.close()
     with pytest.raises(V.VerifyError):
         V.vp_model(256, 512, 1e-6, [_layer(V, k_out=1024)], head)  # k_out > n_in

@@ -62,7 +62,7 @@ def check_block(G, layers, b, h_in, got, what):
                           f"{float(np.max(err / budget)):.3g}"
 
 
-@pytest.mark.parametrize("M", [8, 16, 24, 32])
+@pytest.mark.parametrize("M", [1, 8, 13, 16, 24, 32])
 def test_blocks_at_page_shapes_chain(V, two_layers, M):
     G, layers, head, dm = two_layers
     x0 = synth.normal_bf16(40 + M, synth.stream_id(0, synth.T_X0), (M, G.hidden))

@@ -856,9 +856,10 @@ PassWs pass_ws(const vp_model* md, int M) {
 bool fp8_ok(const void* w, int N, int K) { return w && aligned(w, 16) && vp_packed_bytes_fp8(N, K) > 0; }
 bool nvfp4_ok(const void* w, int N, int K) { return w && aligned(w, 16) && vp_packed_bytes_nvfp4(N, K) > 0; }
 
-vp_status pass_args_ok(const vp_model* md, int M, void* ws, size_t ws_bytes) {
+// lanes: the call ends in the head's acceptance, so M must be whole lanes of 8 rows.
+vp_status pass_args_ok(const vp_model* md, int M, void* ws, size_t ws_bytes, bool lanes) {
   if (!md || !ws) return VP_ERR_INVALID_ARG;
-  if (M < 8 || M > kMaxM || M % 8) return VP_ERR_SHAPE;
+  if (M < 1 || M > kMaxM || (lanes && M % 8)) return VP_ERR_SHAPE;
   if (!aligned(ws, 256)) return VP_ERR_ALIGNMENT;
   if (ws_bytes < pass_ws(md, M).total) return VP_ERR_WORKSPACE;
   return VP_OK;
@@ -901,7 +902,7 @@ vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_d
 void vp_model_destroy(vp_model* model) { delete model; }
 
 size_t vp_pass_workspace_bytes(const vp_model* model, int M) {
-  if (!model || M < 8 || M > kMaxM || M % 8) return 0;
+  if (!model || M < 1 || M > kMaxM) return 0;
   return pass_ws(model, M).total;
 }
 
@@ -920,7 +921,7 @@ int vp_pass_launch_count(const vp_model* model) {
 vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
                          int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, size_t ws_bytes,
                          void* stream) {
-  vp_status st = pass_args_ok(md, M, ws, ws_bytes);
+  vp_status st = pass_args_ok(md, M, ws, ws_bytes, true);
   if (st != VP_OK) return st;
   if (!x0 || !pending || !argmax || !n_commit || !committed) return VP_ERR_INVALID_ARG;
   if (!aligned(x0, 16) || (trace && !aligned(trace, 16)) || (logits && !aligned(logits, 4)) || !aligned(pending, 4) ||
@@ -955,7 +956,7 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
 
 vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, int block_end, void* trace, void* ws,
                            size_t ws_bytes, void* stream) {
-  vp_status st = pass_args_ok(md, M, ws, ws_bytes);
+  vp_status st = pass_args_ok(md, M, ws, ws_bytes, false);
   if (st != VP_OK) return st;
   if (!h) return VP_ERR_INVALID_ARG;
   const int nb = 2 * (int)md->layers.size();
