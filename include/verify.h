@@ -338,6 +338,23 @@ vp_status vp_verify_pass(const vp_model* model, const void* x0, int M, const int
                          int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace,
                          float* logits, void* ws, size_t ws_bytes, void* stream);
 
+/* The verify pass with sampled instead of greedy acceptance [SP-sample]: the pass of
+ * vp_verify_pass, whose head phase writes the fp32 logits [M][vocab] (into `logits` when non-NULL,
+ * else into the workspace) and the argmax, then -- on the same stream, with no host in between -- the
+ * sampled acceptance of vp_sample_accept over those logits (temperature, top_k, top_p, the drafts'
+ * distributions draft_tokens / draft_probs or point masses when both are NULL, the caller's uniforms
+ * [M][2]; see vp_sample_accept), which writes n_commit and committed.  argmax stays the greedy
+ * target token of each row.  One launch more than vp_verify_pass and nothing read back to the host:
+ * capturable into a CUDA graph.  Workspace: vp_pass_sampled_workspace_bytes(model, M) bytes,
+ * zero-filled once.  Errors: as vp_verify_pass and vp_sample_accept (VP_ERR_SHAPE for a vocabulary
+ * above 1,048,576 or top_k outside 1..min(32, vocab)). */
+size_t vp_pass_sampled_workspace_bytes(const vp_model* model, int M);
+vp_status vp_verify_pass_sampled(const vp_model* model, const void* x0, int M, const int32_t* pending,
+                                 float temperature, int top_k, float top_p, const int32_t* draft_tokens,
+                                 const float* draft_probs, const float* uniforms, int32_t* argmax,
+                                 int32_t* n_commit, int32_t* committed, float* logits, void* ws,
+                                 size_t ws_bytes, void* stream);
+
 /* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16
  * [M][hidden], M = 1..32: no acceptance runs, so M need not be whole lanes; updated in place); block
  * 2l is the mixer block of layer l and block 2l + 1 its MLP block, computed exactly as inside

@@ -234,6 +234,18 @@ def test_model_create_validation_without_gpu(V):
     assert V.vp_pass_workspace_bytes(m, 8) > 0
     assert V.vp_pass_workspace_bytes(m, 1) > 0 and V.vp_pass_workspace_bytes(m, 12) > 0  # block runs take any M
     assert V.vp_pass_workspace_bytes(m, 0) == 0 and V.vp_pass_workspace_bytes(m, 33) == 0
+    # the sampled pass: whole lanes only, and more workspace than the greedy pass (its logits)
+    assert V.vp_pass_sampled_workspace_bytes(m, 8) > V.vp_pass_workspace_bytes(m, 8) + 8 * 2048 * 4
+    assert V.vp_pass_sampled_workspace_bytes(m, 12) == 0
+    ps = V.vp_pass_sampled_workspace_bytes(m, 8)
+    bad = lambda **kw: L.vp_verify_pass_sampled(  # noqa: E731
+        m.handle, FAKE, 8, FAKE, kw.get("T", 1.0), kw.get("k", 20), kw.get("p", 0.9), kw.get("dt", None),
+        kw.get("dp", None), FAKE, FAKE, FAKE, FAKE, None, 1 << 20, kw.get("wb", ps), None)
+    L = V.lib()
+    assert bad(T=0.0) == V.VP_ERR_INVALID_ARG and bad(p=1.5) == V.VP_ERR_INVALID_ARG
+    assert bad(dt=FAKE) == V.VP_ERR_INVALID_ARG  # draft tokens without their probabilities
+    assert bad(k=0) == V.VP_ERR_SHAPE and bad(k=33) == V.VP_ERR_SHAPE
+    assert bad(wb=ps - 1) == V.VP_ERR_WORKSPACE
     L = V.lib()
     ws_fake = 1 << 20  # never dereferenced: the row count is checked first
     # the pass itself needs whole lanes of 8 rows

@@ -27,7 +27,7 @@ EXPORTS = [
     "vp_pass_workspace_bytes", "vp_verify_pass", "vp_verify_blocks", "vp_pass_launch_count",
     "vp_linear_nvfp4_noalloc", "vp_noalloc_read_status", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
     "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
-    "vp_commit_append", "vp_decode_steps",
+    "vp_commit_append", "vp_decode_steps", "vp_pass_sampled_workspace_bytes", "vp_verify_pass_sampled",
 ]
 
 
@@ -94,6 +94,8 @@ def _load():
         "vp_lookup_drafts": (I, [P, P, I, I, I, P, P, P]),
         "vp_commit_append": (I, [P, P, I, I, P, P, P, P]),
         "vp_decode_steps": (I, [P, I, P, P, F, I, I, P, P, I, I, I, P, P, P, P, P, P, S, P, P]),
+        "vp_pass_sampled_workspace_bytes": (S, [P, I]),
+        "vp_verify_pass_sampled": (I, [P, P, I, P, F, I, F, P, P, P, P, P, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -312,6 +314,20 @@ def vp_verify_pass(model: vp_model, x0, M: int, pending, argmax, n_commit, commi
     _check("vp_verify_pass", _L.vp_verify_pass(model.handle, _ptr(x0), M, _ptr(pending), _ptr(argmax),
                                                _ptr(n_commit), _ptr(committed), _ptr(trace), _ptr(logits), _ptr(ws),
                                                wb, _stream(stream)))
+
+
+def vp_pass_sampled_workspace_bytes(model: vp_model, M: int) -> int:
+    return _L.vp_pass_sampled_workspace_bytes(model.handle, M)
+
+
+def vp_verify_pass_sampled(model: vp_model, x0, M: int, pending, temperature: float, top_k: int, top_p: float,
+                           draft_tokens, draft_probs, uniforms, argmax, n_commit, committed, logits, ws, stream=None,
+                           ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_verify_pass_sampled",
+           _L.vp_verify_pass_sampled(model.handle, _ptr(x0), M, _ptr(pending), temperature, top_k, top_p,
+                                     _ptr(draft_tokens), _ptr(draft_probs), _ptr(uniforms), _ptr(argmax),
+                                     _ptr(n_commit), _ptr(committed), _ptr(logits), _ptr(ws), wb, _stream(stream)))
 
 
 def vp_verify_blocks(model: vp_model, h, M: int, block_begin: int, block_end: int, trace, ws, stream=None,

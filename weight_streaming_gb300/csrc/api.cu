@@ -918,21 +918,15 @@ int vp_pass_launch_count(const vp_model* model) {
   return model ? program_launches((int)model->phases[0].size()) : 0;
 }
 
-vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
-                         int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, size_t ws_bytes,
-                         void* stream) {
-  vp_status st = pass_args_ok(md, M, ws, ws_bytes, true);
-  if (st != VP_OK) return st;
-  if (!x0 || !pending || !argmax || !n_commit || !committed) return VP_ERR_INVALID_ARG;
-  if (!aligned(x0, 16) || (trace && !aligned(trace, 16)) || (logits && !aligned(logits, 4)) || !aligned(pending, 4) ||
-      !aligned(argmax, 4) || !aligned(n_commit, 4) || !aligned(committed, 4))
-    return VP_ERR_ALIGNMENT;
-  int sms = 0;
-  if ((st = device_sms(&sms)) != VP_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// The pass's launches once its arguments are checked: the x0 copy, then the phase program.
+vp_status enqueue_pass(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
+                       int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, int sms,
+                       cudaStream_t s) {
   const std::vector<Phase>& phases = md->phases[nt_of(M) - 1];
-  for (const Phase& ph : phases)
-    if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
-  cudaStream_t s = (cudaStream_t)stream;
   const PassWs w = pass_ws(md, M);
   uint8_t* b = (uint8_t*)ws;
   Io io = make_io(ws, w.L, md->needs[nt_of(M) - 1].cs_lane());
@@ -952,6 +946,83 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
                                   cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e);
   return run_phases(phases, M, md->eps, io, sms, s);
+}
+
+vp_status pass_io_ok(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
+                     int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, size_t ws_bytes,
+                     int* sms) {
+  vp_status st = pass_args_ok(md, M, ws, ws_bytes, true);
+  if (st != VP_OK) return st;
+  if (!x0 || !pending || !argmax || !n_commit || !committed) return VP_ERR_INVALID_ARG;
+  if (!aligned(x0, 16) || (trace && !aligned(trace, 16)) || (logits && !aligned(logits, 4)) || !aligned(pending, 4) ||
+      !aligned(argmax, 4) || !aligned(n_commit, 4) || !aligned(committed, 4))
+    return VP_ERR_ALIGNMENT;
+  if ((st = device_sms(sms)) != VP_OK) return st;
+  for (const Phase& ph : md->phases[nt_of(M) - 1])
+    if (!slices_ok(ph, *sms)) return VP_ERR_SHAPE;
+  return VP_OK;
+}
+
+// The sampled pass's workspace: the pass's, then the greedy acceptance it does not report (n_commit,
+// committed of up to 4 lanes), the logits [M][vocab] fp32, the sampling kernel's.
+struct SampledWs {
+  size_t greedy, logits, sample, total;
+};
+SampledWs sampled_ws(const vp_model* md, int M) {
+  SampledWs w;
+  w.greedy = align_up(pass_ws(md, M).total, 256);
+  w.logits = align_up(w.greedy + sizeof(int32_t) * 9 * (kMaxM / 8), 256);
+  w.sample = align_up(w.logits + sizeof(float) * (size_t)M * md->head.vocab, 256);
+  w.total = align_up(w.sample + sample_ws_layout(M, md->head.vocab).total, 256);
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
+                         int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, size_t ws_bytes,
+                         void* stream) {
+  int sms = 0;
+  vp_status st = pass_io_ok(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, ws_bytes, &sms);
+  if (st != VP_OK) return st;
+  return enqueue_pass(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, sms, (cudaStream_t)stream);
+}
+
+size_t vp_pass_sampled_workspace_bytes(const vp_model* model, int M) {
+  if (!model || M < 8 || M > kMaxM || M % 8 || model->head.vocab > kSampleMaxV) return 0;
+  return sampled_ws(model, M).total;
+}
+
+vp_status vp_verify_pass_sampled(const vp_model* md, const void* x0, int M, const int32_t* pending, float temperature,
+                                 int top_k, float top_p, const int32_t* draft_tokens, const float* draft_probs,
+                                 const float* uniforms, int32_t* argmax, int32_t* n_commit, int32_t* committed,
+                                 float* logits, void* ws, size_t ws_bytes, void* stream) {
+  if (!md || !uniforms) return VP_ERR_INVALID_ARG;
+  if ((draft_tokens == nullptr) != (draft_probs == nullptr)) return VP_ERR_INVALID_ARG;
+  if (!(temperature > 0.0f) || !(temperature < INFINITY) || !(top_p > 0.0f) || !(top_p <= 1.0f))
+    return VP_ERR_INVALID_ARG;
+  const int V = md->head.vocab;
+  if (top_k < 1 || top_k > 32 || top_k > V || V > kSampleMaxV) return VP_ERR_SHAPE;
+  if (!aligned(uniforms, 4) || (draft_tokens && (!aligned(draft_tokens, 4) || !aligned(draft_probs, 4))))
+    return VP_ERR_ALIGNMENT;
+  if (M >= 8 && M <= kMaxM && M % 8 == 0 && ws_bytes < sampled_ws(md, M).total) return VP_ERR_WORKSPACE;
+  int sms = 0;
+  vp_status st = pass_io_ok(md, x0, M, pending, argmax, n_commit, committed, nullptr, logits, ws, ws_bytes, &sms);
+  if (st != VP_OK) return st;
+  const SampledWs w = sampled_ws(md, M);
+  uint8_t* b = (uint8_t*)ws;
+  float* lg = logits ? logits : reinterpret_cast<float*>(b + w.logits);
+  int32_t* greedy = reinterpret_cast<int32_t*>(b + w.greedy);
+  cudaStream_t s = (cudaStream_t)stream;
+  // The head phase writes the logits (and the argmax); its greedy acceptance goes to scratch, the
+  // sampled acceptance over the same logits to the caller.
+  st = enqueue_pass(md, x0, M, pending, argmax, greedy, greedy + kMaxM / 8, nullptr, lg, ws, sms, s);
+  if (st != VP_OK) return st;
+  cudaError_t e = launch_sample_accept(lg, M, V, temperature, top_k, top_p, pending, draft_tokens, draft_probs,
+                                       uniforms, n_commit, committed, b + w.sample, s);
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
 vp_status vp_verify_blocks(const vp_model* md, void* h, int M, int block_begin, int block_end, void* trace, void* ws,
