@@ -715,6 +715,15 @@ def main():
     runs = [ms8] + [1e3 * time_graph(g8, s8, args.steps, 3) / args.steps for _ in range(3)]
     srt = sorted(runs)
     also["M8_runs_ms_per_pass"] = {"runs": runs, "min": srt[0], "median": 0.5 * (srt[1] + srt[2]), "max": srt[-1]}
+    # the pass with sampled acceptance at M = 8 (top_k 20, top_p 0.95, temperature 0.7, point-mass drafts)
+    x0s, pends, ams, ncs, cms, _ = io8
+    wss = torch.zeros(V.vp_pass_sampled_workspace_bytes(sm.model, 8), dtype=torch.uint8, device="cuda")
+    us = torch.rand((8, 2), device="cuda", generator=torch.Generator(device="cuda").manual_seed(0))
+    t_s = graph_time(lambda: V.vp_verify_pass_sampled(sm.model, x0s, 8, pends, 0.7, 20, 0.95, None, None, us, ams,
+                                                      ncs, cms, None, wss), max(3, args.steps // 2), 3)
+    also["M8_sampled"] = {"ms_per_pass": t_s * 1e3, "gbps": pass_bytes / t_s / 1e9,
+                          "what": "vp_verify_pass_sampled: the pass, its logits written, then sampled acceptance"}
+    del wss
     # the per-component workloads: one MLP layer at M = 1 .. 32, and the head with acceptance at 1 / 4 lanes
     if not args.no_components:
         also["config_mlp_layer"] = measure_mlp_layer([1, 8, 16, 24, 32], max(5, args.steps), 3)
