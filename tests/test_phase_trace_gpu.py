@@ -27,7 +27,8 @@ def test_phase_trace_tool_reports_every_phase_kind():
         assert n == (1 if kind == "head" else 4)
         nums = [float(v) for v in vals if v != "-"]
         assert all(0.0 <= v < 5e4 for v in nums), (kind, vals)
-        staging, med, mx = nums[0], nums[1], nums[2]
-        assert med <= mx
+        # columns: stage-ld, staging, stream med, stream max, fixup tail, x-slice, release, phase
+        stage_ld, staging, med, mx = (float(v) for v in vals[:4])
+        assert stage_ld <= staging and med <= mx
     total = float(re.search(r"last phase done: ([\d.]+) us", out.stdout).group(1))
     assert total > 0.0

@@ -202,6 +202,7 @@ struct SmemMisc {
   unsigned tcnt[kWarps];  // arrivals at a row block shared by warps, indexed by its first contributor
   Part part;              // the CTA's share of the current phase
   uint32_t tmem_base;     // the CTA's tensor memory (parked units)
+  unsigned done;          // warps of the CTA done with the current phase's units
   float red[kThreads / 16];
   float xscale[kMaxM];
   int tok[kMaxM];
@@ -250,7 +251,7 @@ __device__ __forceinline__ int exp_of_max(float mx) {
 
 // Stages the CTA's K slice [kbase, kbase + Ks) of the phase's activation rows: x, or
 // bf16(RMSNorm(x)) (unit weight) when the phase asks for it, with the row statistics taken over
-// the whole row.  park(): each warp's own work, done while the staging loads are in flight.
+// the whole row.
 //
 // Work items: (token n, 64-wide k block, its 32-wide half p, h) -> the thread loads the 16-byte chunks
 // k = 32 p + 8 h .. + 7 and 32 p + 16 + 8 h .. + 7 and writes the two whole fragment entries they fill
@@ -259,9 +260,9 @@ __device__ __forceinline__ int exp_of_max(float mx) {
 // (l >> 2) & 1, and writes first the entry c = 2 h + (p & 1): the 8 lanes of a quarter warp then hit
 // 8 different 4-bank groups (token parity x c), so the 16-byte stores have no bank conflicts.  Each
 // warp takes (tile, 64-wide block) pairs warp, warp + 16, ... (at most 5: Ks <= ks_max(NT)).
-template <int NT, class Park>
+template <int NT>
 __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, const Io& io, int kbase, int Ks,
-                                        uint8_t* xs, SmemMisc& sm, int trace_phase, Park&& park) {
+                                        uint8_t* xs, SmemMisc& sm, int trace_phase) {
   constexpr int kIt = 5;
   static_assert(NT * ks_max(NT) / 64 <= kIt * kWarps, "every (tile, k block) pair has a warp iteration");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, M = prog.M;
@@ -282,7 +283,6 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
     va[it] = ok ? ldcg128(a) : make_uint4(0u, 0u, 0u, 0u);
     vb[it] = ok ? ldcg128(a + 16) : make_uint4(0u, 0u, 0u, 0u);
   }
-  park();  // the warp's own work while the loads are in flight
   // The thread's statistic per tile (sum of squares for RMSNorm, else the largest magnitude).
 #pragma unroll
   for (int it = 0; it < kIt; ++it) {
@@ -976,47 +976,22 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
   }
 
   unsigned seq = 0, nbar = 0;
+  int parked_next = 0;  // units of the next phase this warp parked in tensor memory
   for (int p = 0; p < prog.n; ++p) {
     const Phase& ph = prog.ph[p];
     VP_TRACE(threadIdx.x == 0, p, 0);
     const Part P = part_of_cta(ph, G, cta);
-    if (threadIdx.x == 0) sm.part = P;  // published by the staging's closing barrier
+    if (threadIdx.x == 0) {
+      sm.part = P;  // published by the staging's closing barrier
+      sm.done = 0u;
+    }
     const int ck = chunk_k(ph.fmt), kc0 = P.S.kg0 * ph.grp;
     const int ub = wbegin(P, warp), ue = wbegin(P, warp + 1);
     const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
     const bool fp8 = ph.fmt == kFmtFp8;
-    // While the staging loads are in flight, the warp moves the phase's first units (already in its
-    // ring) into tensor memory and refills the ring with the next ones: the boundary then keeps twice
-    // the bytes in flight.  The parked units are consumed first, from tensor memory.
-    int parked = 0;
-    auto park = [&]() {
-      if constexpr (!kQ4) {
-        const int n = min(kSlots, ue - ub);
-        for (int k = 0; k < n; ++k) {
-          const int slot = (int)(seq % kSlots);
-          if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
-            sm.abort = 1;
-            atomicExch(io.status, kStatusTimeout);
-          }
-          __syncwarp();
-          const uint32_t ua = ring_w + slot * kSlotBytes;
-          chunk_park(tslot + kUnitCols * k, chunk_smem(ua, lane, fp8));
-          chunk_park(tslot + kUnitCols * k + kUnitCols / 2, chunk_smem(ua + chunk_bytes, lane, fp8));
-          __syncwarp();
-          if (lane == 0 && pc.p < prog.n && !sm.abort) {
-            fence_proxy_async_smem();
-            issue_unit(pc, ua, &sm.full[warp][slot], pol);
-            cursor_next(pc, prog, G, cta, warp);
-            ++issued;
-          }
-          ++seq;
-        }
-        parked = n;
-        __syncwarp();
-        tmem_wait_st();
-      }
-    };
-    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm, p, park);
+    const int parked = parked_next;  // this phase's first units, parked at the end of the last one
+    parked_next = 0;
+    stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm, p);
     VP_TRACE(threadIdx.x == 0, p, 1);
     float tsc[NT][2];
 #pragma unroll
@@ -1096,6 +1071,44 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     }
     VP_TRACE(lane == 0, p, 2 + warp);
     if (cur >= 0) flush<NT>(ph, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+    if constexpr (!kQ4) {
+      // A warp done while at least 4 of its CTA's warps still stream is idle until the phase ends: it
+      // moves the next phase's first units (already in its ring) into tensor memory and refills the
+      // ring with the ones after, so that the boundary keeps twice the bytes in flight.  The last
+      // warps to finish do not, so the CTA's arrival at the barrier is not delayed.
+      unsigned order = 0;
+      if (lane == 0) order = atomicAdd(&sm.done, 1u);
+      order = __shfl_sync(0xffffffffu, order, 0);
+      if (p + 1 < prog.n && order + 4 < (unsigned)kWarps) {
+        const Phase& nx = prog.ph[p + 1];
+        const Part Pn = part_of_cta(nx, G, cta);
+        const int n = min(kSlots, wbegin(Pn, warp + 1) - wbegin(Pn, warp));
+        const bool nfp8 = nx.fmt == kFmtFp8;
+        const uint32_t ncb = 2u * strip_bytes(nx.fmt);
+        for (int k = 0; k < n; ++k) {
+          const int slot = (int)(seq % kSlots);
+          if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
+            sm.abort = 1;
+            atomicExch(io.status, kStatusTimeout);
+          }
+          __syncwarp();
+          const uint32_t ua = ring_w + slot * kSlotBytes;
+          chunk_park(tslot + kUnitCols * k, chunk_smem(ua, lane, nfp8));
+          chunk_park(tslot + kUnitCols * k + kUnitCols / 2, chunk_smem(ua + ncb, lane, nfp8));
+          __syncwarp();
+          if (lane == 0 && pc.p < prog.n && !sm.abort) {
+            fence_proxy_async_smem();
+            issue_unit(pc, ua, &sm.full[warp][slot], pol);
+            cursor_next(pc, prog, G, cta, warp);
+            ++issued;
+          }
+          ++seq;
+        }
+        parked_next = n;
+        __syncwarp();
+        tmem_wait_st();
+      }
+    }
     VP_TRACE(lane == 0, p, 18 + warp);
     if (ph.ks > 1) {  // every row block's slices meet after a grid barrier
       grid_barrier(io, G, (unsigned)G * ++nbar, sm);
