@@ -40,14 +40,6 @@ enum : int { kStatusTimeout = 6 };
 
 static_assert(kSlotBytes >= 2 * 2304 && kSlotBytes >= 2 * 2048, "a slot holds one unit");
 
-// Tensor memory: all 512 columns of the SM (one CTA per SM); a parked unit takes 48 columns of a
-// warp's 32 lanes (two chunks of 6 x 16-byte pieces), a warp kSlots units, and the 4 warps that share
-// a lane quarter stack their columns.
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kUnitCols = 48;
-constexpr uint32_t kParkCols = kUnitCols * kSlots;
-static_assert(4 * kParkCols <= kTmemCols, "the parked units of 4 warps fit a lane quarter's columns");
-
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 __device__ __forceinline__ uint16_t bf16_bits(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
@@ -201,8 +193,6 @@ struct SmemMisc {
   Cursor cur[kWarps];  // the producer state of each warp (used by its lane 0 only)
   unsigned tcnt[kWarps];  // arrivals at a row block shared by warps, indexed by its first contributor
   Part part;              // the CTA's share of the current phase
-  uint32_t tmem_base;     // the CTA's tensor memory (parked units)
-  unsigned done;          // warps of the CTA done with the current phase's units
   float red[kThreads / 16];
   float xscale[kMaxM];
   int tok[kMaxM];
@@ -419,58 +409,20 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
 }
 
 // ---------------------------------------------------------------- one unit of a warp
-// A K chunk of a row block as one lane reads it: the 16-byte pieces (g, c) of the codes of strips 0
-// and 1 (rows g and g + 8), halves 0 and 1 (a0, a1 / b0, b1), and, NVFP4, the block scales of rows g
-// and g + 8 (s0, s1).
-struct ChunkW {
-  uint4 a0, a1, b0, b1, s0, s1;
-};
-__device__ __forceinline__ ChunkW chunk_smem(uint32_t ua, int lane, bool fp8) {
-  ChunkW w;
-  const int sb = fp8 ? 1024 : 1152, g = lane >> 2;
-  w.a0 = lds128(ua + lane * 16);
-  w.a1 = lds128(ua + 512 + lane * 16);
-  w.b0 = lds128(ua + sb + lane * 16);
-  w.b1 = lds128(ua + sb + 512 + lane * 16);
-  if (fp8) {
-    w.s0 = w.s1 = make_uint4(0u, 0u, 0u, 0u);
-  } else {
-    w.s0 = lds128(ua + 1024 + g * 16);
-    w.s1 = lds128(ua + 1152 + 1024 + g * 16);
-  }
-  return w;
-}
-// The same pieces parked in tensor memory, 24 columns per chunk (a0, a1, b0, b1, s0, s1).
-__device__ __forceinline__ ChunkW chunk_tmem(uint32_t taddr) {
-  ChunkW w;
-  w.a0 = tmem_ld4(taddr);
-  w.a1 = tmem_ld4(taddr + 4);
-  w.b0 = tmem_ld4(taddr + 8);
-  w.b1 = tmem_ld4(taddr + 12);
-  w.s0 = tmem_ld4(taddr + 16);
-  w.s1 = tmem_ld4(taddr + 20);
-  tmem_wait_ld(w.a0, w.a1, w.b0, w.b1, w.s0, w.s1);
-  return w;
-}
-__device__ __forceinline__ void chunk_park(uint32_t taddr, const ChunkW& w) {
-  tmem_st4(taddr, w.a0);
-  tmem_st4(taddr + 4, w.a1);
-  tmem_st4(taddr + 8, w.b0);
-  tmem_st4(taddr + 12, w.b1);
-  tmem_st4(taddr + 16, w.s0);
-  tmem_st4(taddr + 20, w.s1);
-}
-
-// One NVFP4 K chunk of one row block.  acc[j] (16 rows x 8 tokens, the mma.sync C fragment): rows g,
-// g + 8 of the row block, tokens 8j + 2c, 8j + 2c + 1; even k steps accumulate into acc, odd ones into
-// acc2 (the caller passes the same array twice for one chain).  xa: this lane's fragments of the
-// chunk's first k-step pair.
+// One K chunk of one row block.  acc[j] (16 rows x 8 tokens, the mma.sync C fragment): rows g, g + 8
+// of the row block, tokens 8j + 2c, 8j + 2c + 1; even k steps accumulate into acc, odd ones into
+// acc2 (the caller passes the same array twice for one chain).  ua: the chunk in the slot; xa: this
+// lane's fragments of the chunk's first k-step pair.
 template <int NT>
-__device__ __forceinline__ void unit_nvfp4(const ChunkW& cw, uint32_t xa, int lane, float (&acc)[NT][4],
+__device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4],
                                            float (&acc2)[NT][4]) {
-  const uint32_t w0[8] = {cw.a0.x, cw.a0.y, cw.a0.z, cw.a0.w, cw.a1.x, cw.a1.y, cw.a1.z, cw.a1.w};
-  const uint32_t w1[8] = {cw.b0.x, cw.b0.y, cw.b0.z, cw.b0.w, cw.b1.x, cw.b1.y, cw.b1.z, cw.b1.w};
-  const uint32_t sw0[4] = {cw.s0.x, cw.s0.y, cw.s0.z, cw.s0.w}, sw1[4] = {cw.s1.x, cw.s1.y, cw.s1.z, cw.s1.w};
+  const int g = lane >> 2;
+  const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
+  const uint4 c1a = lds128(ua + 1152 + lane * 16), c1b = lds128(ua + 1152 + 512 + lane * 16);
+  const uint4 s0 = lds128(ua + 1024 + g * 16), s1 = lds128(ua + 1152 + 1024 + g * 16);
+  const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+  const uint32_t w1[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
+  const uint32_t sw0[4] = {s0.x, s0.y, s0.z, s0.w}, sw1[4] = {s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
   for (int p = 0; p < 8; ++p) {
     uint4 b[NT];
@@ -550,12 +502,13 @@ __device__ __forceinline__ void unit_q4(uint32_t ua, uint32_t xa, int lane, floa
   }
 }
 
-// One FP8 K chunk of one row block (accumulators as unit_nvfp4).
 template <int NT>
-__device__ __forceinline__ void unit_fp8(const ChunkW& cw, uint32_t xa, int lane, float (&acc)[NT][4],
+__device__ __forceinline__ void unit_fp8(uint32_t ua, uint32_t xa, int lane, float (&acc)[NT][4],
                                          float (&acc2)[NT][4]) {
-  const uint32_t w0[8] = {cw.a0.x, cw.a0.y, cw.a0.z, cw.a0.w, cw.a1.x, cw.a1.y, cw.a1.z, cw.a1.w};
-  const uint32_t w1[8] = {cw.b0.x, cw.b0.y, cw.b0.z, cw.b0.w, cw.b1.x, cw.b1.y, cw.b1.z, cw.b1.w};
+  const uint4 c0a = lds128(ua + lane * 16), c0b = lds128(ua + 512 + lane * 16);
+  const uint4 c1a = lds128(ua + 1024 + lane * 16), c1b = lds128(ua + 1024 + 512 + lane * 16);
+  const uint32_t w0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+  const uint32_t w1[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     uint4 b[NT];
@@ -945,21 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     sm.tcnt[warp] = 0u;
   }
   if (threadIdx.x == 0) sm.abort = 0;
-  if constexpr (!kQ4) {
-    if (warp == 0) {
-      tmem_alloc(&sm.tmem_base, kTmemCols);
-      tmem_fence_before_sync();
-    }
-  }
   fence_mbar_init();
   __syncthreads();
-  // Tensor memory: warp w parks up to kSlots units in lanes 32 (w % 4) .., columns 96 (w / 4) ..
-  // (48 per unit: 24 per chunk).
-  uint32_t tslot = 0;
-  if constexpr (!kQ4) {
-    tmem_fence_after_sync();
-    tslot = sm.tmem_base + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kParkCols * (warp >> 2));
-  }
 
   const uint32_t ring_w = smem_addr(smem) + warp * kSlots * kSlotBytes;
   uint64_t pol = 0;
@@ -976,21 +916,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
   }
 
   unsigned seq = 0, nbar = 0;
-  int parked_next = 0;  // units of the next phase this warp parked in tensor memory
   for (int p = 0; p < prog.n; ++p) {
     const Phase& ph = prog.ph[p];
     VP_TRACE(threadIdx.x == 0, p, 0);
     const Part P = part_of_cta(ph, G, cta);
-    if (threadIdx.x == 0) {
-      sm.part = P;  // published by the staging's closing barrier
-      sm.done = 0u;
-    }
+    if (threadIdx.x == 0) sm.part = P;  // published by the staging's closing barrier
     const int ck = chunk_k(ph.fmt), kc0 = P.S.kg0 * ph.grp;
-    const int ub = wbegin(P, warp), ue = wbegin(P, warp + 1);
-    const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
-    const bool fp8 = ph.fmt == kFmtFp8;
-    const int parked = parked_next;  // this phase's first units, parked at the end of the last one
-    parked_next = 0;
     stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm, p);
     VP_TRACE(threadIdx.x == 0, p, 1);
     float tsc[NT][2];
@@ -1007,8 +938,10 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         hb.v[j][h] = -INFINITY;
         hb.i[j][h] = 0x7fffffff;
       }
+    const int ub = wbegin(P, warp), ue = wbegin(P, warp + 1);
     const uint32_t xlane = smem_addr(xs) + lane * 16;
     const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
+    const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
     const bool two = ph.layout == kInterleaved;
     int rb = ub < ue ? P.rb0 + ub / P.S.kgn : 0, kgl = ub < ue ? ub % P.S.kgn : 0;
     float acc[NT][4], acc2[NT][4];
@@ -1028,42 +961,36 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         }
         cur = rb;
       }
-      const bool tm = u - ub < parked;  // a parked unit (tensor memory), else the ring's next
       const int slot = (int)(seq % kSlots);
-      if (!tm && !sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
+      if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
         sm.abort = 1;
         atomicExch(io.status, kStatusTimeout);
       }
       const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kgl * ph.grp * pair_stride;
-      const uint32_t tu = tslot + kUnitCols * (u - ub);
-      if (tm) __syncwarp();  // converged for the warp-wide tensor-memory loads
-      auto chunk = [&](int ci) { return tm ? chunk_tmem(tu + ci * (kUnitCols / 2)) : chunk_smem(ua + ci * chunk_bytes, lane, fp8); };
       if constexpr (kQ4) {  // one or two consecutive chunks of the row block, 4 groups each
         unit_q4<NT>(ua, xa, lane, acc);
         if ((P.S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
       } else if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
-        unit_nvfp4<NT>(chunk(0), xa, lane, acc, acc);
-        unit_nvfp4<NT>(chunk(1), xa, lane, acc2, acc2);
+        unit_nvfp4<NT>(ua, xa, lane, acc, acc);
+        unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
       } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
         const bool second = ph.grp == 2 && (P.S.kg0 + kgl) * 2 + 1 < ph.KC;
-        if (!fp8) {
-          unit_nvfp4<NT>(chunk(0), xa, lane, acc, NT == 1 ? acc2 : acc);
-          if (second) unit_nvfp4<NT>(chunk(1), xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
+        if (ph.fmt == kFmtNvfp4) {
+          unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+          if (second) unit_nvfp4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
         } else {
-          unit_fp8<NT>(chunk(0), xa, lane, acc, NT == 1 ? acc2 : acc);
-          if (second) unit_fp8<NT>(chunk(1), xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
+          unit_fp8<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+          if (second) unit_fp8<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
         }
       }
-      if (!tm) {
-        __syncwarp();
-        if (lane == 0 && pc.p < prog.n && !sm.abort) {
-          fence_proxy_async_smem();
-          issue_unit(pc, ua, &sm.full[warp][slot], pol);
-          cursor_next(pc, prog, G, cta, warp);
-          ++issued;
-        }
-        ++seq;
+      __syncwarp();
+      if (lane == 0 && pc.p < prog.n && !sm.abort) {
+        fence_proxy_async_smem();
+        issue_unit(pc, ua, &sm.full[warp][slot], pol);
+        cursor_next(pc, prog, G, cta, warp);
+        ++issued;
       }
+      ++seq;
       if (++kgl == P.S.kgn) {
         kgl = 0;
         ++rb;
@@ -1071,44 +998,6 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     }
     VP_TRACE(lane == 0, p, 2 + warp);
     if (cur >= 0) flush<NT>(ph, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
-    if constexpr (!kQ4) {
-      // A warp done while at least 4 of its CTA's warps still stream is idle until the phase ends: it
-      // moves the next phase's first units (already in its ring) into tensor memory and refills the
-      // ring with the ones after, so that the boundary keeps twice the bytes in flight.  The last
-      // warps to finish do not, so the CTA's arrival at the barrier is not delayed.
-      unsigned order = 0;
-      if (lane == 0) order = atomicAdd(&sm.done, 1u);
-      order = __shfl_sync(0xffffffffu, order, 0);
-      if (p + 1 < prog.n && order + 4 < (unsigned)kWarps) {
-        const Phase& nx = prog.ph[p + 1];
-        const Part Pn = part_of_cta(nx, G, cta);
-        const int n = min(kSlots, wbegin(Pn, warp + 1) - wbegin(Pn, warp));
-        const bool nfp8 = nx.fmt == kFmtFp8;
-        const uint32_t ncb = 2u * strip_bytes(nx.fmt);
-        for (int k = 0; k < n; ++k) {
-          const int slot = (int)(seq % kSlots);
-          if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
-            sm.abort = 1;
-            atomicExch(io.status, kStatusTimeout);
-          }
-          __syncwarp();
-          const uint32_t ua = ring_w + slot * kSlotBytes;
-          chunk_park(tslot + kUnitCols * k, chunk_smem(ua, lane, nfp8));
-          chunk_park(tslot + kUnitCols * k + kUnitCols / 2, chunk_smem(ua + ncb, lane, nfp8));
-          __syncwarp();
-          if (lane == 0 && pc.p < prog.n && !sm.abort) {
-            fence_proxy_async_smem();
-            issue_unit(pc, ua, &sm.full[warp][slot], pol);
-            cursor_next(pc, prog, G, cta, warp);
-            ++issued;
-          }
-          ++seq;
-        }
-        parked_next = n;
-        __syncwarp();
-        tmem_wait_st();
-      }
-    }
     VP_TRACE(lane == 0, p, 18 + warp);
     if (ph.ks > 1) {  // every row block's slices meet after a grid barrier
       grid_barrier(io, G, (unsigned)G * ++nbar, sm);
@@ -1128,15 +1017,6 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       const unsigned k = issued - 1 - ((issued - 1 - s) % kSlots);  // the last copy into slot s
       mbar_wait_bounded(&sm.full[warp][s], (k / kSlots) & 1u);
     }
-  // The tensor memory goes back on every path (a timed-out launch runs to here as well).
-  if constexpr (!kQ4) {
-    tmem_fence_before_sync();
-    __syncthreads();
-    if (warp == 0) {
-      tmem_fence_after_sync();
-      tmem_dealloc(sm.tmem_base, kTmemCols);
-    }
-  }
   if (prog.n > 1) grid_exit(io, G);
 }
 

@@ -180,47 +180,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// ---------------------------------------------------------------- tensor memory (tcgen05)
-// Tensor memory is addressed as (lane << 16) | column; warp w of a CTA reaches lanes 32 (w % 4) ..
-// 32 (w % 4) + 31.  Allocation: one whole warp; the base address is written to the shared word dst.
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst)), "r"(ncols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-// Order tensor-memory operations around a thread barrier (before it in one thread, after it in another).
-__device__ __forceinline__ void tmem_fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tmem_fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// 32 lanes x 4 columns: thread t of the warp writes / reads lane (lane of taddr) + t, columns
-// (column of taddr) .. + 3.
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint4 v) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ uint4 tmem_ld4(uint32_t taddr) {
-  uint4 v;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(taddr)
-               : "memory");
-  return v;
-}
-// Waits for this thread's tensor-memory loads; the loaded registers pass through the instruction, so
-// no use of them can be scheduled before it.
-__device__ __forceinline__ void tmem_wait_ld(uint4& a, uint4& b, uint4& c, uint4& d, uint4& e, uint4& f) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a.x), "+r"(a.y), "+r"(a.z), "+r"(a.w), "+r"(b.x), "+r"(b.y), "+r"(b.z), "+r"(b.w), "+r"(c.x),
-                 "+r"(c.y), "+r"(c.z), "+r"(c.w), "+r"(d.x), "+r"(d.y), "+r"(d.z), "+r"(d.w), "+r"(e.x), "+r"(e.y),
-                 "+r"(e.z), "+r"(e.w), "+r"(f.x), "+r"(f.y), "+r"(f.z), "+r"(f.w)
-               :
-               : "memory");
-}
-
 // ---------------------------------------------------------------- exact powers of two
 // 2^e as a float for e in [-149, 127] (subnormal below -126).
 __device__ __forceinline__ float pow2f(int e) {
