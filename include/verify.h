@@ -355,6 +355,68 @@ vp_status vp_verify_pass_sampled(const vp_model* model, const void* x0, int M, c
                                  int32_t* n_commit, int32_t* committed, float* logits, void* ws,
                                  size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------ the pass with the real mixer cores
+ *
+ * In place of the stand-in slice, each layer runs its own mixer core between its projections, all on
+ * the device [LM-attn] [BS-gdn]:
+ *   Gated DeltaNet: u = FP8(in, r) kept whole (rows: q (n_qk heads), k (n_qk), v (n_v), z (n_v), each
+ *     d wide); a, b = r . A, r . B (BF16 [n_v][hidden] each, fp32 results); the causal depthwise
+ *     4-tap convolution of u's q, k, v part over the lane's 3 earlier rows (window_a) and its 8 rows
+ *     (tap 3 on the current row), SiLU; q, k over their per-head L2 norm (eps 1e-6 inside the root);
+ *     q, k, v rounded to bf16, q / k head i serving v heads i * n_v / n_qk ..; alpha =
+ *     exp(-exp(A_log) softplus(a + dt_bias)), beta = sigmoid(b); the gated delta rule of vp_gdn_scan
+ *     from state_a into state_b over the 8 rows; bf16(o / sqrt(mean(o^2) + 1e-6) * norm_w * silu(z))
+ *     per v head into the out-projection.
+ *   attention: q + gate = FP8(q, r), k + v = FP8(kv, r), kept whole; q and k heads over their root
+ *     mean square (eps 1e-6) times q_norm / k_norm, then the rotary embedding over the whole head at
+ *     cache position ctx[lane] + j (base 10000), bf16; then vp_attention_verify (append k, v at ctx ..
+ *     ctx + 7, causal softmax over the cache, times sigmoid(gate)) into the o-projection.
+ * Rounding: bf16 at the projection outputs, the cores' inputs and outputs, and the residual.
+ * State: the caller owns it (device memory, per layer); the pass reads state_a / window_a / the cache
+ * rows before ctx and writes state_b (the state after all 8 rows), conv_hist (window_a's 3 rows then
+ * the 8 rows' conv inputs: the window after n accepted rows is rows n .. n + 2) and the cache rows ctx
+ * .. ctx + 7.  After a partial accept the caller re-scans the n committed rows from state_a with
+ * vp_gdn_scan and takes the window from conv_hist.  d = 128 (the scan), D = 256 (the attention core),
+ * Hq / Hkv <= 8, ctx[lane] + 8 <= cap. */
+typedef struct {
+  /* Gated DeltaNet layers */
+  const void* w_a;       /* bf16 [n_v][hidden] */
+  const void* w_b;       /* bf16 [n_v][hidden] */
+  const void* conv_taps; /* bf16 [(2 n_qk + n_v) d][4] */
+  const float* a_log;    /* fp32 [n_v] */
+  const float* dt_bias;  /* fp32 [n_v] */
+  const float* norm_w;   /* fp32 [d]: the gated RMSNorm's weight */
+  const float* state_a;  /* fp32 [lanes][n_v][d][d] (parity buffer A: read) */
+  float* state_b;        /* fp32 [lanes][n_v][d][d] (parity buffer B: written) */
+  const void* window_a;  /* bf16 [lanes][3][(2 n_qk + n_v) d] */
+  void* conv_hist;       /* bf16 [lanes][11][(2 n_qk + n_v) d] (written) */
+  /* attention layers */
+  const float* q_norm;   /* fp32 [D] */
+  const float* k_norm;   /* fp32 [D] */
+  void* k_cache;         /* bf16 [lanes][Hkv][cap][D] */
+  void* v_cache;         /* bf16 [lanes][Hkv][cap][D] */
+} vp_core_desc;
+
+typedef struct {
+  int n_qk, n_v, d;      /* Gated DeltaNet heads: q / k heads, v heads, head width */
+  int Hq, Hkv, D, cap;   /* attention: query and key-value heads, head width, cache positions per lane */
+} vp_core_geom;
+
+/* Attaches the mixer cores to a model (one descriptor per layer; the model keeps the pointers).
+ * Checks every layer's projection widths against the geometry: Gated DeltaNet n_in ==
+ * (2 n_qk + 2 n_v) d and k_out == n_v d; attention n_in == 2 Hq D, n_kv == 2 Hkv D, k_out == Hq D. */
+vp_status vp_model_set_cores(vp_model* model, const vp_core_geom* geom, const vp_core_desc* cores, int n_layers);
+/* Workspace bytes of vp_verify_pass_cores at M rows (0 if the model has no cores or M is invalid). */
+size_t vp_pass_cores_workspace_bytes(const vp_model* model, int M);
+/* The verify pass with the real mixer cores (arguments as vp_verify_pass; ctx: device int32 [lanes],
+ * the cached positions per lane).  Launches: one executor program per layer boundary and the cores'
+ * kernels in between, all on `stream`, nothing read back to the host: capturable into a CUDA graph.
+ * The attention core reports a lane whose ctx + 8 exceeds cap in the workspace's status word
+ * (VP_ERR_SHAPE; that lane's cache is left as it is). */
+vp_status vp_verify_pass_cores(const vp_model* model, const void* x0, int M, const int32_t* ctx,
+                               const int32_t* pending, int32_t* argmax, int32_t* n_commit, int32_t* committed,
+                               void* trace, float* logits, void* ws, size_t ws_bytes, void* stream);
+
 /* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16
  * [M][hidden], M = 1..32: no acceptance runs, so M need not be whole lanes; updated in place); block
  * 2l is the mixer block of layer l and block 2l + 1 its MLP block, computed exactly as inside

@@ -55,14 +55,15 @@ def rope(x: np.ndarray, pos: np.ndarray) -> np.ndarray:
 
 
 def attn_block(h_bf16: np.ndarray, g: dict, wts: dict, k_cache: np.ndarray, v_cache: np.ndarray,
-               ctx: np.ndarray):
+               ctx: np.ndarray, core_out: list | None = None):
     """The attention mixer block for M = 8 * lanes verify rows.
 
     h_bf16: uint16 [M][hidden]; g: {"hidden", "Hq", "Hkv", "D"}; wts: "q" FP8 codes [2 Hq D][hidden]
     with scale "s_q", "kv" FP8 codes [2 Hkv D][hidden] with "s_kv", "o" FP8 codes [hidden][Hq D] with
     "s_o", "q_norm" / "k_norm" fp64 [D]; k_cache / v_cache: bf16 bits [lanes][Hkv][cap][D] holding
     ctx[l] positions per lane.  Returns (new residual uint16 [M][hidden], the rows' keys and values
-    as appended (bf16 bits [M][Hkv][D]), the core's q and gate inputs (bf16 bits [M][Hq][D]))."""
+    as appended (bf16 bits [M][Hkv][D]), the core's q and gate inputs (bf16 bits [M][Hq][D])).  core_out:
+    when a list, the o-projection's input (the core's bf16 output bits [M][Hq D]) is appended to it."""
     H, Hq, Hkv, D = g["hidden"], g["Hq"], g["Hkv"], g["D"]
     M = h_bf16.shape[0]
     r = rmsnorm(h_bf16)
@@ -76,5 +77,7 @@ def attn_block(h_bf16: np.ndarray, g: dict, wts: dict, k_cache: np.ndarray, v_ca
     vb, gb = bf16_round(v), bf16_round(gate)
     core = attention_verify(qb, kb, vb, k_cache, v_cache, ctx, gb, with_abs=False)
     ob = bf16_round(core.reshape(M, Hq * D))
+    if core_out is not None:
+        core_out.append(ob)
     y = linear(FP8, ob, wts["o"], None, wts["s_o"], H, with_abs=False)
     return bf16_round(bf16_value(h_bf16) + y), (kb, vb), (qb, gb)

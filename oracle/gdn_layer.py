@@ -79,7 +79,8 @@ def gated_rmsnorm(o: np.ndarray, z: np.ndarray, w: np.ndarray) -> np.ndarray:
     return o / np.sqrt((o * o).mean(axis=-1, keepdims=True) + EPS) * w * silu(z)
 
 
-def gdn_block(h_bf16: np.ndarray, g: dict, wts: dict, state: np.ndarray, window: np.ndarray, rows: int = 8):
+def gdn_block(h_bf16: np.ndarray, g: dict, wts: dict, state: np.ndarray, window: np.ndarray, rows: int = 8,
+              core_out: list | None = None):
     """One lane's Gated DeltaNet mixer block over its 8 verify rows.
 
     h_bf16: uint16 [8][hidden] (the residual); g: {"hidden", "n_qk", "n_v", "d"}; wts: "in" FP8
@@ -90,7 +91,8 @@ def gdn_block(h_bf16: np.ndarray, g: dict, wts: dict, state: np.ndarray, window:
     over all 8 rows; the returned state and window are those after the first `rows` rows (8 after a
     full accept, n_commit for the re-scan after a partial one).
     Returns (new residual uint16 [8][hidden], state after `rows` rows, window after `rows` rows,
-    the recurrence's inputs (q, k, v bf16 bits [8][n_v][d], alpha, beta [8][n_v]))."""
+    the recurrence's inputs (q, k, v bf16 bits [8][n_v][d], alpha, beta [8][n_v])).  core_out: when a
+    list, the out-projection's input (the gated norm's bf16 bits [8][n_v d]) is appended to it."""
     H, nqk, nv, d = g["hidden"], g["n_qk"], g["n_v"], g["d"]
     cq, cv = nqk * d, nv * d
     r = rmsnorm(h_bf16)
@@ -111,6 +113,8 @@ def gdn_block(h_bf16: np.ndarray, g: dict, wts: dict, state: np.ndarray, window:
     if rows != 8:  # the commit re-scan: the state after the committed rows only
         st, _ = gdn_scan(state[None], qe, ke, v, alpha, beta, np.array([rows], np.int32), want_out=False)
     on = bf16_round(gated_rmsnorm(o, z.reshape(8, nv, d), wts["w_norm"]).reshape(8, cv))
+    if core_out is not None:
+        core_out.append(on)
     y_out = linear(FP8, on, wts["out"], None, wts["s_out"], H, with_abs=False)
     h_new = bf16_round(bf16_value(h_bf16) + y_out)
     return h_new, st[0], e[rows:rows + 3], (qe, ke, v, alpha, beta)

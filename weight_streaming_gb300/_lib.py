@@ -28,6 +28,7 @@ EXPORTS = [
     "vp_linear_nvfp4_noalloc", "vp_noalloc_read_status", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
     "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
     "vp_commit_append", "vp_decode_steps", "vp_pass_sampled_workspace_bytes", "vp_verify_pass_sampled",
+    "vp_model_set_cores", "vp_pass_cores_workspace_bytes", "vp_verify_pass_cores",
 ]
 
 
@@ -48,6 +49,19 @@ class vp_layer_desc(ctypes.Structure):
                 ("w_gate", ctypes.c_void_p), ("ts_gate", ctypes.c_float),
                 ("w_up", ctypes.c_void_p), ("ts_up", ctypes.c_float),
                 ("w_down", ctypes.c_void_p), ("ts_down", ctypes.c_float)]
+
+
+class vp_core_desc(ctypes.Structure):
+    _fields_ = [("w_a", ctypes.c_void_p), ("w_b", ctypes.c_void_p), ("conv_taps", ctypes.c_void_p),
+                ("a_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("norm_w", ctypes.c_void_p),
+                ("state_a", ctypes.c_void_p), ("state_b", ctypes.c_void_p), ("window_a", ctypes.c_void_p),
+                ("conv_hist", ctypes.c_void_p), ("q_norm", ctypes.c_void_p), ("k_norm", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p)]
+
+
+class vp_core_geom(ctypes.Structure):
+    _fields_ = [("n_qk", ctypes.c_int), ("n_v", ctypes.c_int), ("d", ctypes.c_int), ("Hq", ctypes.c_int),
+                ("Hkv", ctypes.c_int), ("D", ctypes.c_int), ("cap", ctypes.c_int)]
 
 
 class vp_head_desc(ctypes.Structure):
@@ -96,6 +110,9 @@ def _load():
         "vp_decode_steps": (I, [P, I, P, P, F, I, I, P, P, I, I, I, P, P, P, P, P, P, S, P, P]),
         "vp_pass_sampled_workspace_bytes": (S, [P, I]),
         "vp_verify_pass_sampled": (I, [P, P, I, P, F, I, F, P, P, P, P, P, P, P, P, S, P]),
+        "vp_model_set_cores": (I, [P, ctypes.POINTER(vp_core_geom), ctypes.POINTER(vp_core_desc), I]),
+        "vp_pass_cores_workspace_bytes": (S, [P, I]),
+        "vp_verify_pass_cores": (I, [P, P, I, P, P, P, P, P, P, P, P, S, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -328,6 +345,23 @@ def vp_verify_pass_sampled(model: vp_model, x0, M: int, pending, temperature: fl
            _L.vp_verify_pass_sampled(model.handle, _ptr(x0), M, _ptr(pending), temperature, top_k, top_p,
                                      _ptr(draft_tokens), _ptr(draft_probs), _ptr(uniforms), _ptr(argmax),
                                      _ptr(n_commit), _ptr(committed), _ptr(logits), _ptr(ws), wb, _stream(stream)))
+
+
+def vp_model_set_cores(model: vp_model, geom: vp_core_geom, cores: list):
+    arr = (vp_core_desc * len(cores))(*cores)
+    _check("vp_model_set_cores", _L.vp_model_set_cores(model.handle, ctypes.byref(geom), arr, len(cores)))
+
+
+def vp_pass_cores_workspace_bytes(model: vp_model, M: int) -> int:
+    return _L.vp_pass_cores_workspace_bytes(model.handle, M)
+
+
+def vp_verify_pass_cores(model: vp_model, x0, M: int, ctx, pending, argmax, n_commit, committed, trace, logits, ws,
+                         stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_verify_pass_cores",
+           _L.vp_verify_pass_cores(model.handle, _ptr(x0), M, _ptr(ctx), _ptr(pending), _ptr(argmax), _ptr(n_commit),
+                                   _ptr(committed), _ptr(trace), _ptr(logits), _ptr(ws), wb, _stream(stream)))
 
 
 def vp_verify_blocks(model: vp_model, h, M: int, block_begin: int, block_end: int, trace, ws, stream=None,

@@ -27,7 +27,7 @@ LIB_WAIT = os.path.join(PKG, "libverify_waittest.so")
 VARIANTS = {"": (LIB, BUILD, []), "trace": (LIB_TRACE, BUILD_TRACE, ["-DVP_PHASE_TRACE"]),
             "waittest": (LIB_WAIT, BUILD_WAIT, ["-DVP_WAIT_TEST"])}
 SOURCES = ["api.cu", "exec_nt12.cu", "exec_nt34.cu", "exec_q4.cu", "sample.cu", "attention.cu", "gdn.cu",
-           "loop.cu", "errors.cu"]
+           "loop.cu", "errors.cu", "mixer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -14,6 +14,7 @@
 #include "internal.h"
 #include "attention.h"
 #include "errors.h"
+#include "mixer.h"
 #include "sample.h"
 #include "verify.h"
 
@@ -730,6 +731,13 @@ struct vp_model {
   int zmax;
   std::vector<Phase> phases[4];  // per NT: 4 phases per layer (in, out, gate+up, down), then the head
   Needs needs[4] = {Needs(1), Needs(2), Needs(3), Needs(4)};
+  // the real mixer cores (vp_model_set_cores): the same program with the in-projections kept whole
+  bool has_cores = false;
+  vp_core_geom cg{};
+  std::vector<vp_core_desc> cores;
+  int umax = 0;  // widest in-projection (both segments)
+  std::vector<Phase> cphases[4];
+  Needs cneeds[4] = {Needs(1), Needs(2), Needs(3), Needs(4)};
 };
 
 namespace vp {
@@ -739,11 +747,12 @@ int model_hidden(const vp_model* model) { return model ? model->hidden : 0; }
 namespace {
 
 // The pass's phases at NT n-tiles.  Block 2l (mixer of layer l) = phases 4l, 4l + 1; block 2l + 1
-// (its MLP) = phases 4l + 2, 4l + 3; the head is the last phase.
-void build_pass(vp_model* md, int NT) {
+// (its MLP) = phases 4l + 2, 4l + 3; the head is the last phase.  cores: the in-projections keep
+// every row (kEpiU into the U buffer) for the real mixer cores.
+void build_pass(vp_model* md, int NT, bool cores = false) {
   const int H = md->hidden, I = md->inter;
-  std::vector<Phase>& out = md->phases[NT - 1];
-  Needs& nd = md->needs[NT - 1];
+  std::vector<Phase>& out = cores ? md->cphases[NT - 1] : md->phases[NT - 1];
+  Needs& nd = cores ? md->cneeds[NT - 1] : md->needs[NT - 1];
   out.clear();
   for (int l = 0; l < (int)md->layers.size(); ++l) {
     const vp_layer_desc& d = md->layers[l];
@@ -766,6 +775,11 @@ void build_pass(vp_model* md, int NT) {
     in.out = kBufZ;
     in.out_ld = d.k_out;
     in.out_cols = d.k_out;
+    if (cores) {
+      in.epi = kEpiU;
+      in.out = kBufU;
+      in.out_ld = d.n_in + (d.kind == VP_LAYER_ATTN ? d.n_kv : 0);
+    }
     out.push_back(make_phase(in, NT));
     PhaseSpec o;  // mixer out-projection + residual
     o.fmt = kFmtFp8;
@@ -849,6 +863,41 @@ PassWs pass_ws(const vp_model* md, int M) {
   off = align_up(off + sizeof(uint16_t) * (size_t)M * md->inter, 256);
   w.rss = off;
   off = align_up(off + sizeof(float) * (size_t)M * (md->hidden / kRowBlock), 256);
+  w.total = off;
+  return w;
+}
+
+// The cores pass's workspace: the pass's, then the in-projections kept whole and the cores' scratch.
+struct CoresWs {
+  PassWs P;
+  size_t u, a, b, alpha, beta, q, k, v, o, rows8, aq, ak, av, ag, attn, total;
+};
+CoresWs cores_ws(const vp_model* md, int M) {
+  CoresWs w;
+  w.P = pass_ws(md, M);
+  const vp_core_geom& g = md->cg;
+  const size_t gv = (size_t)M * g.n_v, gd = gv * g.d, hq = (size_t)M * g.Hq * g.D, hk = (size_t)M * g.Hkv * g.D;
+  size_t off = w.P.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  w.u = take(sizeof(uint16_t) * (size_t)M * md->umax);
+  w.a = take(sizeof(float) * gv);
+  w.b = take(sizeof(float) * gv);
+  w.alpha = take(sizeof(float) * gv);
+  w.beta = take(sizeof(float) * gv);
+  w.q = take(sizeof(uint16_t) * gd);
+  w.k = take(sizeof(uint16_t) * gd);
+  w.v = take(sizeof(uint16_t) * gd);
+  w.o = take(sizeof(float) * gd);
+  w.rows8 = take(sizeof(int32_t) * (kMaxM / 8));
+  w.aq = take(sizeof(uint16_t) * hq);
+  w.ag = take(sizeof(uint16_t) * hq);
+  w.ak = take(sizeof(uint16_t) * hk);
+  w.av = take(sizeof(uint16_t) * hk);
+  w.attn = take(g.Hkv > 0 && g.cap >= 8 ? attn_ws_layout(M, g.Hkv, g.cap).total : 0);
   w.total = off;
   return w;
 }
@@ -988,6 +1037,137 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
   vp_status st = pass_io_ok(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, ws_bytes, &sms);
   if (st != VP_OK) return st;
   return enqueue_pass(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, sms, (cudaStream_t)stream);
+}
+
+vp_status vp_model_set_cores(vp_model* md, const vp_core_geom* g, const vp_core_desc* cores, int n_layers) {
+  if (!md || !g || !cores || n_layers != (int)md->layers.size()) return VP_ERR_INVALID_ARG;
+  if (g->d != 128 || g->n_qk < 1 || g->n_v < g->n_qk || g->n_v % g->n_qk || g->n_v > 4096) return VP_ERR_SHAPE;
+  if (g->D != 256 || g->Hkv < 1 || g->Hq < g->Hkv || g->Hq % g->Hkv || g->Hq / g->Hkv > 8 || g->cap < 8 ||
+      g->cap > (1 << 24))
+    return VP_ERR_SHAPE;
+  int umax = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const vp_layer_desc& d = md->layers[l];
+    const vp_core_desc& c = cores[l];
+    if (d.kind == VP_LAYER_GDN) {
+      if (d.n_in != (2 * g->n_qk + 2 * g->n_v) * g->d || d.k_out != g->n_v * g->d) return VP_ERR_SHAPE;
+      if (!c.w_a || !c.w_b || !c.conv_taps || !c.a_log || !c.dt_bias || !c.norm_w || !c.state_a || !c.state_b ||
+          !c.window_a || !c.conv_hist)
+        return VP_ERR_INVALID_ARG;
+      if (!aligned(c.state_a, 16) || !aligned(c.state_b, 16) || !aligned(c.w_a, 2) || !aligned(c.w_b, 2) ||
+          !aligned(c.conv_taps, 2) || !aligned(c.window_a, 2) || !aligned(c.conv_hist, 2))
+        return VP_ERR_ALIGNMENT;
+      umax = std::max(umax, d.n_in);
+    } else {
+      if (d.n_in != 2 * g->Hq * g->D || d.n_kv != 2 * g->Hkv * g->D || d.k_out != g->Hq * g->D) return VP_ERR_SHAPE;
+      if (!c.q_norm || !c.k_norm || !c.k_cache || !c.v_cache) return VP_ERR_INVALID_ARG;
+      if (!aligned(c.k_cache, 16) || !aligned(c.v_cache, 16)) return VP_ERR_ALIGNMENT;
+      umax = std::max(umax, d.n_in + d.n_kv);
+    }
+  }
+  md->cg = *g;
+  md->cores.assign(cores, cores + n_layers);
+  md->umax = umax;
+  for (int nt = 1; nt <= 4; ++nt) build_pass(md, nt, true);
+  md->has_cores = true;
+  return VP_OK;
+}
+
+size_t vp_pass_cores_workspace_bytes(const vp_model* model, int M) {
+  if (!model || !model->has_cores || M < 8 || M > kMaxM || M % 8) return 0;
+  return cores_ws(model, M).total;
+}
+
+vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const int32_t* ctx, const int32_t* pending,
+                               int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace, float* logits,
+                               void* ws, size_t ws_bytes, void* stream) {
+  if (!md || !md->has_cores || !ctx) return VP_ERR_INVALID_ARG;
+  if (!aligned(ctx, 4)) return VP_ERR_ALIGNMENT;
+  if (M >= 8 && M <= kMaxM && M % 8 == 0 && ws_bytes < cores_ws(md, M).total) return VP_ERR_WORKSPACE;
+  int sms = 0;
+  vp_status st = pass_io_ok(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, ws_bytes, &sms);
+  if (st != VP_OK) return st;
+  const int NT = nt_of(M), L = (int)md->layers.size();
+  const std::vector<Phase>& all = md->cphases[NT - 1];
+  for (const Phase& ph : all)
+    if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
+  cudaStream_t s = (cudaStream_t)stream;
+  const CoresWs w = cores_ws(md, M);
+  uint8_t* b = (uint8_t*)ws;
+  Io io = make_io(ws, w.P.L, md->needs[NT - 1].cs_lane());
+  io.buf[kBufH] = b + w.P.h;
+  io.buf[kBufZ] = b + w.P.z;
+  io.buf[kBufA] = b + w.P.a;
+  io.buf[kBufU] = b + w.u;
+  io.rss = reinterpret_cast<float*>(b + w.P.rss);
+  io.rss_ld = md->hidden / kRowBlock;
+  io.buf[kBufLogits] = logits;
+  io.buf[kBufTrace] = trace;
+  io.trace_stride = (size_t)M * md->hidden;
+  io.pending = pending;
+  io.argmax = argmax;
+  io.n_commit = n_commit;
+  io.committed = committed;
+  cudaError_t e = cudaMemcpyAsync(io.buf[kBufH], x0, sizeof(uint16_t) * (size_t)M * md->hidden,
+                                  cudaMemcpyDeviceToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const vp_core_geom& g = md->cg;
+  const uint16_t* h = static_cast<const uint16_t*>(io.buf[kBufH]);
+  const uint16_t* u = reinterpret_cast<const uint16_t*>(b + w.u);
+  uint16_t* zb = static_cast<uint16_t*>(io.buf[kBufZ]);
+  // Program segments: [in(0)], then per layer l: its core, then [out(l), gate+up(l), down(l), in(l + 1)]
+  // (the head after the last layer's down).
+  for (int l = 0; l <= L; ++l) {
+    const int p0 = l == 0 ? 0 : 4 * (l - 1) + 1, p1 = l == 0 ? 1 : 4 * l + 1;
+    std::vector<Phase> seg(all.begin() + p0, all.begin() + p1);
+    if ((st = run_phases(seg, M, md->eps, io, sms, s)) != VP_OK) return st;
+    if (l == L) break;
+    const vp_layer_desc& d = md->layers[l];
+    const vp_core_desc& c = md->cores[l];
+    const int ld_u = d.n_in + (d.kind == VP_LAYER_ATTN ? d.n_kv : 0);
+    if (d.kind == VP_LAYER_GDN) {
+      const int cq = g.n_qk * g.d, cv = g.n_v * g.d;
+      float *fa = reinterpret_cast<float*>(b + w.a), *fb = reinterpret_cast<float*>(b + w.b);
+      float *al = reinterpret_cast<float*>(b + w.alpha), *be = reinterpret_cast<float*>(b + w.beta);
+      uint16_t *q = reinterpret_cast<uint16_t*>(b + w.q), *k = reinterpret_cast<uint16_t*>(b + w.k);
+      uint16_t* v = reinterpret_cast<uint16_t*>(b + w.v);
+      float* o = reinterpret_cast<float*>(b + w.o);
+      int32_t* rows8 = reinterpret_cast<int32_t*>(b + w.rows8);
+      if ((e = launch_ab_proj(h, md->hidden, M, md->eps, static_cast<const uint16_t*>(c.w_a),
+                              static_cast<const uint16_t*>(c.w_b), g.n_v, fa, fb, s)) != cudaSuccess)
+        return cuda_fail(e);
+      if ((e = launch_gdn_prep(u, ld_u, M, static_cast<const uint16_t*>(c.window_a),
+                               static_cast<const uint16_t*>(c.conv_taps), g.n_qk, g.n_v, g.d, q, k, v,
+                               static_cast<uint16_t*>(c.conv_hist), rows8, fa, fb, c.a_log, c.dt_bias, al, be, s)) !=
+          cudaSuccess)
+        return cuda_fail(e);
+      if ((st = vp_gdn_scan(c.state_a, c.state_b, q, k, v, al, be, rows8, M, g.n_v, g.d, g.d, o, stream)) != VP_OK)
+        return st;
+      if ((e = launch_gated_norm(o, u, ld_u, 2 * cq + cv, c.norm_w, M, g.n_v, g.d, zb, s)) != cudaSuccess)
+        return cuda_fail(e);
+    } else {
+      uint16_t *aq = reinterpret_cast<uint16_t*>(b + w.aq), *ag = reinterpret_cast<uint16_t*>(b + w.ag);
+      uint16_t *ak = reinterpret_cast<uint16_t*>(b + w.ak), *av = reinterpret_cast<uint16_t*>(b + w.av);
+      if ((e = launch_attn_prep(u, ld_u, u + d.n_in, ld_u, M, g.Hq, g.Hkv, g.D, c.q_norm, c.k_norm, ctx, aq, ak, av, ag,
+                                s)) != cudaSuccess)
+        return cuda_fail(e);
+      AttnArgs aa;
+      memset(&aa, 0, sizeof(aa));
+      aa.q = aq;
+      aa.k_new = ak;
+      aa.v_new = av;
+      aa.k_cache = static_cast<uint16_t*>(c.k_cache);
+      aa.v_cache = static_cast<uint16_t*>(c.v_cache);
+      aa.ctx = ctx;
+      aa.gate = ag;
+      aa.out = zb;
+      aa.Hq = g.Hq;
+      aa.Hkv = g.Hkv;
+      aa.cap = g.cap;
+      if ((e = launch_attention_verify(aa, M, b + w.attn, s, io.status)) != cudaSuccess) return cuda_fail(e);
+    }
+  }
+  return VP_OK;
 }
 
 size_t vp_pass_sampled_workspace_bytes(const vp_model* model, int M) {

@@ -357,14 +357,14 @@ AttnWs attn_ws_layout(int M, int Hkv, int cap) {
   return L;
 }
 
-cudaError_t launch_attention_verify(AttnArgs a, int M, void* ws, cudaStream_t s) {
+cudaError_t launch_attention_verify(AttnArgs a, int M, void* ws, cudaStream_t s, int* status) {
   const AttnWs L = attn_ws_layout(M, a.Hkv, a.cap);
   uint8_t* b = static_cast<uint8_t*>(ws);
   a.n_part = L.n_part;
   a.part_len = L.part_len;
   a.part_o = reinterpret_cast<float*>(b + L.part_o);
   a.part_ml = reinterpret_cast<float*>(b + L.part_ml);
-  a.status = reinterpret_cast<int*>(b + L.status);
+  a.status = status ? status : reinterpret_cast<int*>(b + L.status);
   static bool attr_done[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

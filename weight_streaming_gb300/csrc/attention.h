@@ -31,6 +31,7 @@ struct AttnWs {
 };
 AttnWs attn_ws_layout(int M, int Hkv, int cap);
 
-cudaError_t launch_attention_verify(AttnArgs a, int M, void* ws, cudaStream_t s);
+// status: the word a lane out of range is reported in (null: the workspace's own status word).
+cudaError_t launch_attention_verify(AttnArgs a, int M, void* ws, cudaStream_t s, int* status = nullptr);
 
 }  // namespace vp

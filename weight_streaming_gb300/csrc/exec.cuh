@@ -598,6 +598,9 @@ __device__ __forceinline__ void epilogue_tile(const Phase& ph, const Io& io, int
         case kEpiZ:
           if (!seg1 && n < ph.out_cols) static_cast<uint16_t*>(io.buf[ph.out])[o] = bf16_bits(val);
           break;
+        case kEpiU:  // column = the virtual row: segment 1 follows segment 0
+          static_cast<uint16_t*>(io.buf[ph.out])[(size_t)t * ph.out_ld + rb * kRowBlock + g + 8 * r] = bf16_bits(val);
+          break;
         case kEpiResid: {
           uint16_t* hp = static_cast<uint16_t*>(io.buf[ph.out]);
           const uint16_t nv = bf16_bits(bf16_bits_to_float(hold[2 * r + h]) + val);

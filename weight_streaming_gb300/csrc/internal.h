@@ -80,6 +80,8 @@ enum Epi : int {
   kEpiSilu = 2,   // a[m][f] = bf16(silu(s0 * gate) * s1 * up) (interleaved)
   kEpiResid = 3,  // h[m][n] = bf16(h[m][n] + s * acc) (and the trace copy)
   kEpiHead = 4,   // logits -> per-row argmax -> greedy acceptance
+  kEpiU = 5,      // u[m][v] = bf16(s * acc) for every virtual row v (both segments): the in-projection
+                  // kept whole for the real mixer cores
 };
 // Row-block sums of squares of the residual stream: a kEpiResid phase with kSsWrite stores, per token
 // and 16-column row block of its output, the sum of the squares of the stored bf16 values; an RMSNorm
@@ -87,7 +89,7 @@ enum Epi : int {
 // fixed-order sum, the same in every CTA) instead of loading the whole row.  Used at 2+ n-tiles.
 enum : int { kSsRead = 1, kSsWrite = 2 };
 // Buffers a phase reads or writes, resolved per launch through Io::buf.
-enum Buf : int { kBufX = 0, kBufY, kBufH, kBufZ, kBufA, kBufLogits, kBufTrace, kNumBufs };
+enum Buf : int { kBufX = 0, kBufY, kBufH, kBufZ, kBufA, kBufLogits, kBufTrace, kBufU, kNumBufs };
 
 struct Phase {
   const uint8_t* w0;
