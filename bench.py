@@ -43,7 +43,9 @@ def parse():
                              "gdn", "decode", "mlp", "head_accept", "pass"],
                     help="time one GEMM shape alone (for profiling) instead of the pass")
     ap.add_argument("--M", type=int, default=8)
-    ap.add_argument("--ctx", type=int, default=32768, help="context length per lane for --kernel attn")
+    ap.add_argument("--ctx", type=int, default=None,
+                    help="context length per lane: --kernel attn (default 32768), --kernel pass --cores (4096)")
+    ap.add_argument("--cores", action="store_true", help="--kernel pass: the pass with the real mixer cores")
     return ap.parse_args()
 
 
@@ -518,6 +520,43 @@ def measure_head_accept(lanes_list, steps: int, warmup: int) -> dict:
     return {"workload": "NVFP4 head [5120->248320] + argmax (lowest index) + greedy accept", "bytes": nbytes, **out}
 
 
+def measure_cores_pass(sm, M_list, ctx: int, steps: int, warmup: int) -> dict:
+    """The verify pass with the real mixer cores (vp_verify_pass_cores) at each M, every lane at
+    context ctx: CUDA-graph replays, CUDA events.  The state the pass writes (state_b, the
+    convolution history, cache rows ctx .. ctx + 7) is the same every replay, so replays repeat the
+    same work.  Weight GB/s counts the projection weights only; the cores' own reads (the
+    key / value cache rows, the delta-rule states) are reported beside it."""
+    import numpy as np
+    import torch
+
+    import synth
+    from weight_streaming_gb300 import _lib as V
+    geom = sm.geom
+    out = {}
+    for M in M_list:
+        lanes = M // 8
+        x0 = torch.from_numpy(synth.normal_bf16(M, synth.stream_id(0, synth.T_X0), (M, geom.hidden)).view(np.int16))
+        x0 = x0.cuda().view(torch.bfloat16)
+        t = synth.uniform_ints(M, synth.stream_id(0, synth.T_PENDING) + 7, 0, M, geom.vocab)
+        pend = torch.from_numpy(synth.planted_pending(M, t, geom.vocab)[0]).cuda()
+        ctx_d = torch.full((lanes,), ctx, dtype=torch.int32, device="cuda")
+        am = torch.empty(M, dtype=torch.int32, device="cuda")
+        nc = torch.empty(lanes, dtype=torch.int32, device="cuda")
+        cm = torch.empty((lanes, 8), dtype=torch.int32, device="cuda")
+        ws = sm.cores_workspace(M)
+        tp = graph_time(lambda: sm.run_cores(x0, ctx_d, pend, am, nc, cm, ws), steps, warmup)
+        assert V.vp_read_status(ws) == V.VP_OK
+        nb = geom.pass_bytes()
+        n_gdn = sum(not geom.is_attn(l) for l in range(geom.n_layers))
+        state = n_gdn * lanes * geom.n_v * geom.d * geom.d * 4 * 2  # read state_a, write state_b
+        out[f"M{M}"] = {"ms_per_pass": tp * 1e3, "weight_gbps": nb / tp / 1e9,
+                        "kv_cache_bytes": lanes * geom.kv_bytes(ctx), "state_bytes": state,
+                        "all_bytes_gbps": (nb + lanes * geom.kv_bytes(ctx) + state) / tp / 1e9,
+                        "launches_per_pass": V.vp_pass_cores_launch_count(sm.model)}
+        del ws
+    return out
+
+
 def run_pass_only(args):
     """The verify pass alone (--layers layers, --M rows), CUDA-graph replays with nothing else on the
     device: a small case for profiling; prints one JSON line with the time per pass and weight GB/s."""
@@ -538,6 +577,11 @@ def run_pass_only(args):
     am = torch.empty(M, dtype=torch.int32, device="cuda")
     nc = torch.empty(M // 8, dtype=torch.int32, device="cuda")
     cm = torch.empty((M // 8, 8), dtype=torch.int32, device="cuda")
+    if args.cores:
+        sm.attach_cores(max(1, M // 8), args.ctx + 8)
+        r = measure_cores_pass(sm, [M], args.ctx, args.steps, args.warmup)[f"M{M}"]
+        print(json.dumps({"kernel": "pass_cores", "layers": args.layers, "M": M, "ctx": args.ctx, **r}), flush=True)
+        return
     ws = sm.workspace(M)
     tp = graph_time(lambda: sm.run(x0, pend, am, nc, cm, ws), args.steps, args.warmup)
     assert V.vp_read_status(ws) == V.VP_OK
@@ -630,6 +674,8 @@ def main():
         run_reference(args)
         return
     if args.kernel:
+        if args.ctx is None:
+            args.ctx = 4096 if args.kernel == "pass" else 32768
         run_kernel(args)
         return
     import numpy as np
@@ -728,6 +774,9 @@ def main():
     if not args.no_components:
         also["config_mlp_layer"] = measure_mlp_layer([1, 8, 16, 24, 32], max(5, args.steps), 3)
         also["config_head_accept"] = measure_head_accept([1, 4], max(5, args.steps), 3)
+        # the pass with the real mixer cores in place of the stand-in slice, every lane at context 4096
+        sm.attach_cores(4, 4096 + 8)
+        also["pass_with_cores_ctx4096"] = measure_cores_pass(sm, [8, 32], 4096, max(5, args.steps // 2), 3)
 
     # ---- dominant kernel: the pass is two launches of one persistent kernel (exec_kernel<1, 0> at M = 8,
     # 4 phases per layer + the head); its algorithmic bytes are the pass's weight bytes, its duration

@@ -380,8 +380,8 @@ vp_status vp_verify_pass_sampled(const vp_model* model, const void* x0, int M, c
  * Hq / Hkv <= 8, ctx[lane] + 8 <= cap. */
 typedef struct {
   /* Gated DeltaNet layers */
-  const void* w_a;       /* bf16 [n_v][hidden] */
-  const void* w_b;       /* bf16 [n_v][hidden] */
+  const void* w_a;       /* bf16 [n_v][hidden], 16-byte aligned */
+  const void* w_b;       /* bf16 [n_v][hidden], 16-byte aligned */
   const void* conv_taps; /* bf16 [(2 n_qk + n_v) d][4] */
   const float* a_log;    /* fp32 [n_v] */
   const float* dt_bias;  /* fp32 [n_v] */
@@ -404,7 +404,9 @@ typedef struct {
 
 /* Attaches the mixer cores to a model (one descriptor per layer; the model keeps the pointers).
  * Checks every layer's projection widths against the geometry: Gated DeltaNet n_in ==
- * (2 n_qk + 2 n_v) d and k_out == n_v d; attention n_in == 2 Hq D, n_kv == 2 Hkv D, k_out == Hq D. */
+ * (2 n_qk + 2 n_v) d and k_out == n_v d; attention n_in == 2 Hq D, n_kv == 2 Hkv D, k_out == Hq D
+ * (VP_ERR_SHAPE); a missing pointer is VP_ERR_INVALID_ARG; w_a, w_b, the states and the caches not
+ * 16-byte aligned (the other bf16 arrays not 2-byte aligned) is VP_ERR_ALIGNMENT. */
 vp_status vp_model_set_cores(vp_model* model, const vp_core_geom* geom, const vp_core_desc* cores, int n_layers);
 /* Workspace bytes of vp_verify_pass_cores at M rows (0 if the model has no cores or M is invalid). */
 size_t vp_pass_cores_workspace_bytes(const vp_model* model, int M);
@@ -416,6 +418,13 @@ size_t vp_pass_cores_workspace_bytes(const vp_model* model, int M);
 vp_status vp_verify_pass_cores(const vp_model* model, const void* x0, int M, const int32_t* ctx,
                                const int32_t* pending, int32_t* argmax, int32_t* n_commit, int32_t* committed,
                                void* trace, float* logits, void* ws, size_t ws_bytes, void* stream);
+
+/* Kernel launches that vp_verify_pass_cores enqueues for a model with cores (0 without): one
+ * executor program per segment (the first in-projection, then the 4 phases after each layer's
+ * core, the last with the head), 5 per Gated DeltaNet core (A/B projections, convolution + norms,
+ * gates, scan, gated norm) and 4 per attention core (prep, cache append, partitions, merge), after
+ * one device-to-device copy of x0. */
+int vp_pass_cores_launch_count(const vp_model* model);
 
 /* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16
  * [M][hidden], M = 1..32: no acceptance runs, so M need not be whole lanes; updated in place); block

@@ -1,7 +1,7 @@
 """GPU parity of the verify attention over a BF16 KV cache (vp_attention_verify) against the fp64
 oracle, through the C ABI: one and several 1,024-key partitions, the pages' 24 / 4 head geometry,
 ragged context lengths per lane, a group of 8 heads, the cache append, an out-of-range length
-reported through the status word, and bit-reproducibility."""
+reported through the status word, bit-reproducibility, and values across bf16's whole range."""
 import numpy as np
 import pytest
 import torch
@@ -98,3 +98,24 @@ def test_attention_out_of_range_context_is_reported(V):
     ref, a = oracle.attention_verify(c["q"][8:], c["kn"][8:], c["vn"][8:], c["kc"][1:], c["vc"][1:], c["ctx"][1:],
                                      c["gate"][8:])
     assert_close(out[8:], ref, a, "good lane")
+
+
+def test_attention_values_over_bf16_range(V):
+    """The cache is BF16: values far outside half precision's range (up to ~1e30 here, half's
+    largest finite is 65504) and tiny ones (~1e-30, below half's smallest subnormal) must pass
+    through the weighted sum exactly as bf16 holds them.  Each key-value head's values get their own
+    scale; queries and keys stay N(0,1) so the softmax weights are ordinary."""
+    c = case(11, 2, 24, 4, 1100, [1000, 37])
+    for name in ("vn", "vc"):
+        x = torch.from_numpy(c[name].view(np.int16)).view(torch.bfloat16).double()
+        axis = 1  # the key-value head axis: [M][Hkv][D] and [L][Hkv][cap][D]
+        scale = torch.tensor([1e30, 1e6, 1e-30, 3.0], dtype=torch.float64)
+        shape = [1] * x.dim()
+        shape[axis] = 4
+        c[name] = (x * scale.view(shape)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    out, _, _, st = run(V, c)
+    assert st == V.VP_OK
+    got = torch.from_numpy(out.view(np.int16)).view(torch.bfloat16).double().numpy()
+    assert np.all(np.isfinite(got))
+    ref, a = oracle.attention_verify(c["q"], c["kn"], c["vn"], c["kc"], c["vc"], c["ctx"], c["gate"])
+    assert_close(out, ref, a, "values over the bf16 range")

@@ -134,3 +134,30 @@ def test_head_matches_oracle(V, M, Vv, K):
     am, nc, cm, lg = run_head(V, codes, scales, ts, x, pending)
     unique = check_head(am, nc, cm, lg, y_ref, a_ref, pending, f"head {M}x{Vv}x{K}")
     assert unique.mean() >= 0.5
+
+
+def test_head_workspace_reused_with_new_inputs(V):
+    """The fused head at M = 32, K = 5120 (a phase cut into K slices) called three times on one
+    workspace with different hidden states: each call's logits match the oracle's for its own
+    input (a barrier left counted by the previous call would let the slices' sums read stale
+    partials)."""
+    M, Vv, K = 32, 2064, 5120
+    codes = synth.uniform_bytes(77, 1, 0, Vv * K // 2).reshape(Vv, K // 2)
+    scales = synth.scale_codes(77, 2, 0, Vv * K // 16).reshape(Vv, K // 16)
+    packed = torch.empty(V.vp_packed_bytes_nvfp4(Vv, K), dtype=torch.uint8, device="cuda")
+    V.vp_pack_nvfp4(dev_u8(codes), dev_u8(scales), Vv, K, packed)
+    ws = workspace(V.vp_workspace_bytes(V.VP_OP_HEAD, M, Vv, K))
+    for i in range(3):
+        x = synth.normal_bf16(300 + i, 3, (M, K))
+        y_ref, a_ref = oracle.linear(oracle.NVFP4, x, codes, scales, 0.8, Vv)
+        pending, _ = synth.planted_pending(i, np.argmax(y_ref, axis=1).astype(np.int32), Vv)
+        am = torch.empty(M, dtype=torch.int32, device="cuda")
+        nc = torch.empty(M // 8, dtype=torch.int32, device="cuda")
+        cm = torch.empty((M // 8, 8), dtype=torch.int32, device="cuda")
+        lg = torch.empty((M, Vv), dtype=torch.float32, device="cuda")
+        V.vp_head_argmax_accept(packed, 0.8, dev_bf16(x), M, Vv, K, dev_i32(pending), am, nc, cm, lg, ws)
+        torch.cuda.synchronize()
+        assert V.vp_read_status(ws) == V.VP_OK
+        assert_linear_close(lg.cpu().numpy(), y_ref, a_ref, f"head call {i}")
+        check_head(am.cpu().numpy(), nc.cpu().numpy(), cm.cpu().numpy(), lg.cpu().numpy(), y_ref, a_ref, pending,
+                   f"head call {i}")

@@ -197,3 +197,34 @@ def test_linear_wide_dynamic_range_rows(V):
     y_ref, a_ref = oracle.linear(oracle.NVFP4, x2, codes, scales, 1.0, N)
     assert_linear_close(y, y_ref, a_ref, "dynamic range")
     assert np.all(y[3] == 0.0)
+
+
+@pytest.mark.parametrize("fmt,M", [("fp8", 16), ("fp8", 32), ("nvfp4", 16), ("nvfp4", 32)])
+def test_workspace_reused_by_k_sliced_calls(V, fmt, M):
+    """One workspace serves several calls without a reset in between (the workspace contract).
+    With K = 5120 at M > 8 the single phase is cut into K slices that meet at a grid barrier, so
+    the barrier's counter must be back at zero when a call ends.  Each call gets different
+    activations: a call whose barrier passed early would sum the previous call's partials."""
+    N, K = 512, 5120
+    if fmt == "fp8":
+        w, _ = fp8_case(70 + M, M, N, K)
+        packed = torch.empty(V.vp_packed_bytes_fp8(N, K), dtype=torch.uint8, device="cuda")
+        V.vp_pack_fp8(dev_u8(w), N, K, packed)
+        op, call, scale = V.VP_OP_FP8, V.vp_linear_fp8, 0.75
+    else:
+        codes, scales, _ = nvfp4_case(70 + M, M, N, K)
+        packed = torch.empty(V.vp_packed_bytes_nvfp4(N, K), dtype=torch.uint8, device="cuda")
+        V.vp_pack_nvfp4(dev_u8(codes), dev_u8(scales), N, K, packed)
+        op, call, scale = V.VP_OP_NVFP4, V.vp_linear_nvfp4, 0.75
+    ws = workspace(V.vp_workspace_bytes(op, M, N, K))
+    for i in range(3):
+        x = synth.normal_bf16(200 + 10 * M + i, 5, (M, K))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        call(packed, scale, dev_bf16(x), y, M, N, K, ws)
+        torch.cuda.synchronize()
+        assert V.vp_read_status(ws) == V.VP_OK
+        if fmt == "fp8":
+            y_ref, a_ref = oracle.linear(oracle.FP8, x, w, None, scale, N)
+        else:
+            y_ref, a_ref = oracle.linear(oracle.NVFP4, x, codes, scales, scale, N)
+        assert_linear_close(y.cpu().numpy(), y_ref, a_ref, f"{fmt} M={M} call {i}")

@@ -160,3 +160,20 @@ def test_linear_q4_mlp_shapes_sampled_rows(V, M, N, K):
     rows = np.unique(np.concatenate([[0, 15, 16, N - 1], rng.integers(0, N, 92)])).astype(np.int32)
     y_ref, a_ref = oracle.linear_q4(x, codes, sc, bi, N, rows=rows)
     assert_linear_close(y[:, rows], y_ref, a_ref, f"q4 {M}x{N}x{K} sampled")
+
+
+def test_linear_q4_workspace_reused_by_k_sliced_calls(V):
+    """M = 32, K = 5120: the phase is cut into K slices that meet at a grid barrier; three calls
+    with different activations on one workspace each match the oracle for their own input."""
+    M, N, K = 32, 512, 5120
+    codes, scales, biases, _ = q4_case(91, M, N, K)
+    packed = pack(V, codes, scales, biases)
+    ws = workspace(V.vp_workspace_bytes(V.VP_OP_Q4, M, N, K))
+    for i in range(3):
+        x = synth.normal_bf16(400 + i, 23, (M, K))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        V.vp_linear_q4(packed, dev_bf16(x), y, M, N, K, ws)
+        torch.cuda.synchronize()
+        assert V.vp_read_status(ws) == V.VP_OK
+        y_ref, a_ref = oracle.linear_q4(x, codes, scales, biases, N)
+        assert_linear_close(y.cpu().numpy(), y_ref, a_ref, f"q4 call {i}")

@@ -28,7 +28,7 @@ EXPORTS = [
     "vp_linear_nvfp4_noalloc", "vp_noalloc_read_status", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
     "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
     "vp_commit_append", "vp_decode_steps", "vp_pass_sampled_workspace_bytes", "vp_verify_pass_sampled",
-    "vp_model_set_cores", "vp_pass_cores_workspace_bytes", "vp_verify_pass_cores",
+    "vp_model_set_cores", "vp_pass_cores_workspace_bytes", "vp_verify_pass_cores", "vp_pass_cores_launch_count",
 ]
 
 
@@ -113,6 +113,7 @@ def _load():
         "vp_model_set_cores": (I, [P, ctypes.POINTER(vp_core_geom), ctypes.POINTER(vp_core_desc), I]),
         "vp_pass_cores_workspace_bytes": (S, [P, I]),
         "vp_verify_pass_cores": (I, [P, P, I, P, P, P, P, P, P, P, P, S, P]),
+        "vp_pass_cores_launch_count": (I, [P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -354,6 +355,10 @@ def vp_model_set_cores(model: vp_model, geom: vp_core_geom, cores: list):
 
 def vp_pass_cores_workspace_bytes(model: vp_model, M: int) -> int:
     return _L.vp_pass_cores_workspace_bytes(model.handle, M)
+
+
+def vp_pass_cores_launch_count(model: vp_model) -> int:
+    return _L.vp_pass_cores_launch_count(model.handle)
 
 
 def vp_verify_pass_cores(model: vp_model, x0, M: int, ctx, pending, argmax, n_commit, committed, trace, logits, ws,

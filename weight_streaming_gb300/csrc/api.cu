@@ -738,6 +738,7 @@ struct vp_model {
   int umax = 0;  // widest in-projection (both segments)
   std::vector<Phase> cphases[4];
   Needs cneeds[4] = {Needs(1), Needs(2), Needs(3), Needs(4)};
+  RopeTable rope{};
 };
 
 namespace vp {
@@ -870,7 +871,7 @@ PassWs pass_ws(const vp_model* md, int M) {
 // The cores pass's workspace: the pass's, then the in-projections kept whole and the cores' scratch.
 struct CoresWs {
   PassWs P;
-  size_t u, a, b, alpha, beta, q, k, v, o, rows8, aq, ak, av, ag, attn, total;
+  size_t u, alpha, beta, q, k, v, o, rows8, aq, ak, av, ag, attn, total;
 };
 CoresWs cores_ws(const vp_model* md, int M) {
   CoresWs w;
@@ -884,8 +885,6 @@ CoresWs cores_ws(const vp_model* md, int M) {
     return at;
   };
   w.u = take(sizeof(uint16_t) * (size_t)M * md->umax);
-  w.a = take(sizeof(float) * gv);
-  w.b = take(sizeof(float) * gv);
   w.alpha = take(sizeof(float) * gv);
   w.beta = take(sizeof(float) * gv);
   w.q = take(sizeof(uint16_t) * gd);
@@ -1042,6 +1041,7 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
 vp_status vp_model_set_cores(vp_model* md, const vp_core_geom* g, const vp_core_desc* cores, int n_layers) {
   if (!md || !g || !cores || n_layers != (int)md->layers.size()) return VP_ERR_INVALID_ARG;
   if (g->d != 128 || g->n_qk < 1 || g->n_v < g->n_qk || g->n_v % g->n_qk || g->n_v > 4096) return VP_ERR_SHAPE;
+  if (md->hidden > 8192) return VP_ERR_SHAPE;  // the A / B projections hold two 16-byte chunks of K per thread
   if (g->D != 256 || g->Hkv < 1 || g->Hq < g->Hkv || g->Hq % g->Hkv || g->Hq / g->Hkv > 8 || g->cap < 8 ||
       g->cap > (1 << 24))
     return VP_ERR_SHAPE;
@@ -1054,7 +1054,7 @@ vp_status vp_model_set_cores(vp_model* md, const vp_core_geom* g, const vp_core_
       if (!c.w_a || !c.w_b || !c.conv_taps || !c.a_log || !c.dt_bias || !c.norm_w || !c.state_a || !c.state_b ||
           !c.window_a || !c.conv_hist)
         return VP_ERR_INVALID_ARG;
-      if (!aligned(c.state_a, 16) || !aligned(c.state_b, 16) || !aligned(c.w_a, 2) || !aligned(c.w_b, 2) ||
+      if (!aligned(c.state_a, 16) || !aligned(c.state_b, 16) || !aligned(c.w_a, 16) || !aligned(c.w_b, 16) ||
           !aligned(c.conv_taps, 2) || !aligned(c.window_a, 2) || !aligned(c.conv_hist, 2))
         return VP_ERR_ALIGNMENT;
       umax = std::max(umax, d.n_in);
@@ -1068,6 +1068,7 @@ vp_status vp_model_set_cores(vp_model* md, const vp_core_geom* g, const vp_core_
   md->cg = *g;
   md->cores.assign(cores, cores + n_layers);
   md->umax = umax;
+  md->rope = rope_table(g->D);
   for (int nt = 1; nt <= 4; ++nt) build_pass(md, nt, true);
   md->has_cores = true;
   return VP_OK;
@@ -1127,19 +1128,18 @@ vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const 
     const int ld_u = d.n_in + (d.kind == VP_LAYER_ATTN ? d.n_kv : 0);
     if (d.kind == VP_LAYER_GDN) {
       const int cq = g.n_qk * g.d, cv = g.n_v * g.d;
-      float *fa = reinterpret_cast<float*>(b + w.a), *fb = reinterpret_cast<float*>(b + w.b);
       float *al = reinterpret_cast<float*>(b + w.alpha), *be = reinterpret_cast<float*>(b + w.beta);
       uint16_t *q = reinterpret_cast<uint16_t*>(b + w.q), *k = reinterpret_cast<uint16_t*>(b + w.k);
       uint16_t* v = reinterpret_cast<uint16_t*>(b + w.v);
       float* o = reinterpret_cast<float*>(b + w.o);
       int32_t* rows8 = reinterpret_cast<int32_t*>(b + w.rows8);
-      if ((e = launch_ab_proj(h, md->hidden, M, md->eps, static_cast<const uint16_t*>(c.w_a),
-                              static_cast<const uint16_t*>(c.w_b), g.n_v, fa, fb, s)) != cudaSuccess)
+      if ((e = launch_ab_gates(h, md->hidden, M, md->eps, static_cast<const uint16_t*>(c.w_a),
+                               static_cast<const uint16_t*>(c.w_b), g.n_v, c.a_log, c.dt_bias, al, be, s)) !=
+          cudaSuccess)
         return cuda_fail(e);
       if ((e = launch_gdn_prep(u, ld_u, M, static_cast<const uint16_t*>(c.window_a),
                                static_cast<const uint16_t*>(c.conv_taps), g.n_qk, g.n_v, g.d, q, k, v,
-                               static_cast<uint16_t*>(c.conv_hist), rows8, fa, fb, c.a_log, c.dt_bias, al, be, s)) !=
-          cudaSuccess)
+                               static_cast<uint16_t*>(c.conv_hist), rows8, s)) != cudaSuccess)
         return cuda_fail(e);
       if ((st = vp_gdn_scan(c.state_a, c.state_b, q, k, v, al, be, rows8, M, g.n_v, g.d, g.d, o, stream)) != VP_OK)
         return st;
@@ -1148,8 +1148,8 @@ vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const 
     } else {
       uint16_t *aq = reinterpret_cast<uint16_t*>(b + w.aq), *ag = reinterpret_cast<uint16_t*>(b + w.ag);
       uint16_t *ak = reinterpret_cast<uint16_t*>(b + w.ak), *av = reinterpret_cast<uint16_t*>(b + w.av);
-      if ((e = launch_attn_prep(u, ld_u, u + d.n_in, ld_u, M, g.Hq, g.Hkv, g.D, c.q_norm, c.k_norm, ctx, aq, ak, av, ag,
-                                s)) != cudaSuccess)
+      if ((e = launch_attn_prep(u, ld_u, u + d.n_in, ld_u, M, g.Hq, g.Hkv, g.D, c.q_norm, c.k_norm, ctx, md->rope, aq,
+                                ak, av, ag, s)) != cudaSuccess)
         return cuda_fail(e);
       AttnArgs aa;
       memset(&aa, 0, sizeof(aa));
@@ -1168,6 +1168,17 @@ vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const 
     }
   }
   return VP_OK;
+}
+
+int vp_pass_cores_launch_count(const vp_model* md) {
+  if (!md || !md->has_cores) return 0;
+  // one executor program per segment (the in-projection of layer 0, then 4 phases per layer, the
+  // last with the head), then per Gated DeltaNet layer the A/B projections, the convolution + norms,
+  // the gates, the scan and the gated norm; per attention layer the prep, the cache append, the
+  // partitions and the merge
+  int n = program_launches(1);
+  for (const vp_layer_desc& d : md->layers) n += program_launches(4) + (d.kind == VP_LAYER_GDN ? 5 : 4);
+  return n;
 }
 
 size_t vp_pass_sampled_workspace_bytes(const vp_model* model, int M) {

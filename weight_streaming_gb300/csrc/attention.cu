@@ -16,15 +16,15 @@
 //    the kv head x 8 verify rows, padded to 64).  Key and value tiles of 64 positions stream through
 //    a two-stage cp.async ring in shared memory (16-byte chunks XOR-swizzled by row, so every
 //    ldmatrix is conflict-free); S = Q K^T on the tensor core in bf16 (q and k exact), the online
-//    softmax in fp32 (exp2 with the 1/sqrt(D) log2(e) scale folded in), then O += P V in f16 (P in
-//    [0, 1]; the value tile converted from bf16 to f16 in shared memory once per tile, exact in f16's
-//    range).  Warps w and w + 4 share m-tile w % 4: each computes S for half of the tile's keys, they
+//    softmax in fp32 (exp2 with the 1/sqrt(D) log2(e) scale folded in), then O += P V on the tensor
+//    core in bf16 with the values as cached (exact over bf16's whole range) and P in [0, 1] split into
+//    two bf16 parts, P = hi + lo (hi = bf16(P), lo = bf16(P - hi): P to about 2^-17 relative), one
+//    MMA each.  Warps w and w + 4 share m-tile w % 4: each computes S for half of the tile's keys, they
 //    exchange the row maxima and their halves of P through shared memory (named barrier per pair),
 //    and each accumulates output dims 128 (w / 4) .. + 127 over all keys.
 //  * attn_merge: per output row and head, the partitions' partials in a fixed order, then the sigmoid
 //    gate and one bf16 rounding.
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 
@@ -74,21 +74,18 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
-                                        uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-// Byte offset of (row, key) in the [rows][64] f16 P tile, 16-byte chunks XOR-swizzled by row.
+// Byte offset of (row, key) in a [rows][64] 16-bit P tile, 16-byte chunks XOR-swizzled by row.
 __device__ __forceinline__ uint32_t pswz(int r, int key) {
   return (uint32_t)(r * 128 + ((((key >> 3) ^ (r & 7)) << 4) | ((key & 7) << 1)));
 }
 // The two warps of m-tile mt (warps mt and mt + 4) meet at named barrier 1 + mt.
 __device__ __forceinline__ void pair_sync(int mt) { asm volatile("bar.sync %0, 64;" ::"r"(1 + mt) : "memory"); }
-__device__ __forceinline__ uint32_t pack_f16(float a, float b) {
-  const __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<const uint32_t*>(&h);
+// Two fp32 values as bf16 pairs: hi = bf16(x) (a in the low half), lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(a - __low2float(h), b - __high2float(h));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 constexpr int kStatusShape = 2;  // VP_ERR_SHAPE
@@ -150,7 +147,9 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
   cp_async_commit();  // group 0: Q and tile 0
 
   __shared__ float xmax[4][2][16];                // per m-tile, per warp of the pair: row maxima, then sums
-  __shared__ __align__(16) uint8_t sP[4 * 16 * 128];  // per m-tile: P [16 rows][64 keys] f16, swizzled
+  // per m-tile: P [16 rows][64 keys] as bf16 hi parts, then (at + kPLo) the lo parts, swizzled
+  constexpr int kPLo = 4 * 16 * 128;
+  __shared__ __align__(16) uint8_t sP[2 * kPLo];
   const int mt = warp & 3, dh = warp >> 2;
   const bool live = mt * 16 < rows;
   const float sl2 = 1.4426950408889634f / sqrtf((float)kD);  // log2(e) / sqrt(D)
@@ -166,17 +165,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
     if (t + 1 < n_tiles) ATTN_ISSUE(t + 1, b ^ 1)
     cp_async_commit();
     cp_async_wait<1>();  // this thread's copies of tile t (and Q) have landed
-    // the value tile to f16 in place (this thread's own chunks)
-    for (int c = tid; c < kTile * 32; c += blockDim.x) {
-      uint4* p = reinterpret_cast<uint4*>(sm + (sV0 - sQ) + b * kTileBytes + swz(c >> 5, c & 31));
-      uint4 v = *p;
-      uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        w[e] = pack_f16(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
-      *p = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    __syncthreads();
+    __syncthreads();     // and every other thread's
     if (live) {
       // S = Q K^T for the m-tile and this warp's 32 keys of the tile (4 n-tiles); the pair's other
       // warp takes the other 32.
@@ -244,41 +233,49 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
         o[n][2] *= alpha[1];
         o[n][3] *= alpha[1];
       }
-      // this warp's half of P (f16) for the other warp of the pair
-      uint32_t pa[2][4];  // A fragments of this warp's two 16-key steps
+      // this warp's half of P (bf16 hi and lo parts) for the other warp of the pair
+      uint32_t ph[2][4], pl[2][4];  // A fragments of this warp's two 16-key steps
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        pa[kk][0] = pack_f16(s[2 * kk][0], s[2 * kk][1]);
-        pa[kk][1] = pack_f16(s[2 * kk][2], s[2 * kk][3]);
-        pa[kk][2] = pack_f16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[kk][3] = pack_f16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+        split_bf16(s[2 * kk][0], s[2 * kk][1], ph[kk][0], pl[kk][0]);
+        split_bf16(s[2 * kk][2], s[2 * kk][3], ph[kk][1], pl[kk][1]);
+        split_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[kk][2], pl[kk][2]);
+        split_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[kk][3], pl[kk][3]);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {  // n-tile 2 kk + hh: keys dh * 32 + 16 kk + 8 hh + 2 cq
           const int key = dh * 32 + 16 * kk + 8 * hh + 2 * cq;
-          *reinterpret_cast<uint32_t*>(sP + pswz(mt * 16 + gq, key)) = pa[kk][2 * hh];
-          *reinterpret_cast<uint32_t*>(sP + pswz(mt * 16 + gq + 8, key)) = pa[kk][2 * hh + 1];
+          const uint32_t o0 = pswz(mt * 16 + gq, key), o1 = pswz(mt * 16 + gq + 8, key);
+          *reinterpret_cast<uint32_t*>(sP + o0) = ph[kk][2 * hh];
+          *reinterpret_cast<uint32_t*>(sP + o1) = ph[kk][2 * hh + 1];
+          *reinterpret_cast<uint32_t*>(sP + kPLo + o0) = pl[kk][2 * hh];
+          *reinterpret_cast<uint32_t*>(sP + kPLo + o1) = pl[kk][2 * hh + 1];
         }
       }
       pair_sync(mt);
-      // O += P V for this warp's 128 output dims: 4 key steps of 16 (two from registers, two from the
-      // other warp through shared memory), 16 n-tiles of 8 dims
+      // O += (P_hi + P_lo) V for this warp's 128 output dims: 4 key steps of 16 (two from registers,
+      // two from the other warp through shared memory), 16 n-tiles of 8 dims
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        uint32_t a0, a1, a2, a3;
+        uint32_t a[4], c[4];
         if ((kk >> 1) == dh) {
-          a0 = pa[kk & 1][0];
-          a1 = pa[kk & 1][1];
-          a2 = pa[kk & 1][2];
-          a3 = pa[kk & 1][3];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            a[e] = ph[kk & 1][e];
+            c[e] = pl[kk & 1][e];
+          }
         } else {
-          ldsm_x4(smem_u32(sP) + pswz(mt * 16 + (lane & 15), 16 * kk + 8 * (lane >> 4)), a0, a1, a2, a3);
+          const uint32_t at = smem_u32(sP) + pswz(mt * 16 + (lane & 15), 16 * kk + 8 * (lane >> 4));
+          ldsm_x4(at, a[0], a[1], a[2], a[3]);
+          ldsm_x4(at + kPLo, c[0], c[1], c[2], c[3]);
         }
 #pragma unroll
         for (int np = 0; np < 8; ++np) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(sV0 + b * kTileBytes + swz(kk * 16 + (lane & 15), dh * 16 + 2 * np + (lane >> 4)), b0, b1, b2, b3);
-          mma_f16(o[2 * np], a0, a1, a2, a3, b0, b1);
-          mma_f16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+          mma_bf16(o[2 * np], a[0], a[1], a[2], a[3], b0, b1);
+          mma_bf16(o[2 * np], c[0], c[1], c[2], c[3], b0, b1);
+          mma_bf16(o[2 * np + 1], a[0], a[1], a[2], a[3], b2, b3);
+          mma_bf16(o[2 * np + 1], c[0], c[1], c[2], c[3], b2, b3);
         }
       }
     }
@@ -315,8 +312,12 @@ __global__ void __launch_bounds__(kThreadsA, 1) attn_partition(const AttnArgs a)
   }
 }
 
-// One CTA per (verify row, q head), one thread per output dim: the partitions in order.
+// One CTA per (verify row, q head), one thread per output dim: the partitions in order.  The
+// partitions' maxima and sums are the same for every thread of the CTA: they are read once per CTA
+// (thread p reads partition p of each chunk of kD) and each partition's weight exp2(m - M) is formed
+// once, in shared memory; every thread then adds the partitions in order.
 __global__ void attn_merge(const AttnArgs a) {
+  __shared__ float sw[kD], sl[kD], red[kD / 32];
   const int r = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const int G = a.Hq / a.Hkv, g = h / G, l = r / 8, i = (h % G) * 8 + r % 8;
   const size_t pb = ((size_t)l * a.Hkv + g) * a.n_part;
@@ -325,14 +326,32 @@ __global__ void attn_merge(const AttnArgs a) {
     return;
   }
   float M = -INFINITY;
-  for (int p = 0; p < a.n_part; ++p) M = fmaxf(M, a.part_ml[((pb + p) * kRows + i) * 2]);
+  for (int p = d; p < a.n_part; p += kD) M = fmaxf(M, a.part_ml[((pb + p) * kRows + i) * 2]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if ((d & 31) == 0) red[d >> 5] = M;
+  __syncthreads();
+  M = red[0];
+  for (int w = 1; w < kD / 32; ++w) M = fmaxf(M, red[w]);
   float den = 0.0f, num = 0.0f;
-  for (int p = 0; p < a.n_part; ++p) {
-    const float m = a.part_ml[((pb + p) * kRows + i) * 2];
-    if (m == -INFINITY) continue;
-    const float w = exp2f(m - M);
-    den += w * a.part_ml[((pb + p) * kRows + i) * 2 + 1];
-    num += w * a.part_o[((pb + p) * kRows + i) * kD + d];
+  for (int p0 = 0; p0 < a.n_part; p0 += kD) {
+    if (p0 + d < a.n_part) {
+      const float* ml = a.part_ml + ((pb + p0 + d) * kRows + i) * 2;
+      const float m = ml[0];
+      sw[d] = m == -INFINITY ? -1.0f : exp2f(m - M);  // -1: an empty partition, skipped
+      sl[d] = ml[1];
+    }
+    __syncthreads();
+    const int n = min(kD, a.n_part - p0);
+    const float* po = a.part_o + ((pb + p0) * kRows + i) * kD + d;
+#pragma unroll 8
+    for (int q = 0; q < n; ++q) {
+      const float w = sw[q];
+      if (w < 0.0f) continue;
+      den += w * sl[q];
+      num += w * po[(size_t)q * kRows * kD];
+    }
+    __syncthreads();
   }
   float v = num / den;
   if (a.gate) v /= 1.0f + expf(-__uint_as_float((uint32_t)a.gate[((size_t)r * a.Hq + h) * kD + d] << 16));

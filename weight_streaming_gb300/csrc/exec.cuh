@@ -1020,7 +1020,9 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       const unsigned k = issued - 1 - ((issued - 1 - s) % kSlots);  // the last copy into slot s
       mbar_wait_bounded(&sm.full[warp][s], (k / kSlots) & 1u);
     }
-  if (prog.n > 1) grid_exit(io, G);
+  // Every CTA takes the same barriers; a program that took any (several phases, or one phase cut
+  // into K slices) resets the counter on the way out, so the workspace is ready for the next call.
+  if (nbar > 0) grid_exit(io, G);
 }
 
 // ---------------------------------------------------------------- launch (host)

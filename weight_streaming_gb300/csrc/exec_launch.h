@@ -16,10 +16,12 @@ cudaError_t trace_read_nt12(void* dst, size_t bytes, unsigned* launches);
 cudaError_t trace_read_nt34(void* dst, size_t bytes, unsigned* launches);
 
 // Runs `prog` (NT = ceil(M / 8) n-tiles of 8 tokens) on `grid` CTAs; cooperative when the program
-// has grid barriers (more than one phase), so that every CTA is resident.
+// has grid barriers (more than one phase, or a phase cut into K slices), so that every CTA is
+// resident.
 inline cudaError_t launch_exec(const Program& prog, const Io& io, int grid, cudaStream_t s) {
   const int NT = (prog.M + 7) / 8;
-  const bool coop = prog.n > 1;
+  bool coop = prog.n > 1;
+  for (int i = 0; i < prog.n && !coop; ++i) coop = prog.ph[i].ks > 1;
   if (prog.q4) return launch_exec_q4(prog, io, NT, grid, s, coop);
   return NT <= 2 ? launch_exec_nt12(prog, io, NT, grid, s, coop) : launch_exec_nt34(prog, io, NT, grid, s, coop);
 }

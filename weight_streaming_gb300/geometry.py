@@ -25,6 +25,14 @@ class Geometry:
     attn_kv: int = 2048
     attn_z: int = 6144
     eps: float = 1e-6
+    # the mixer cores: Gated DeltaNet q/k heads, v heads and head width; attention query and
+    # key-value heads and head width (gdn_in = (2 n_qk + 2 n_v) d, attn_q = 2 Hq D, attn_kv = 2 Hkv D)
+    n_qk: int = 16
+    n_v: int = 48
+    d: int = 128
+    Hq: int = 24
+    Hkv: int = 4
+    D: int = 256
 
     def is_attn(self, l: int) -> bool:
         return (l % self.period) == self.period - 1
@@ -40,3 +48,9 @@ class Geometry:
             b += (2 * I * H + H * I) * 9 // 16
         b += self.vocab * H * 9 // 16
         return b
+
+    def kv_bytes(self, ctx: int) -> int:
+        """Bytes of the key and value cache rows one lane's attention cores read at context ctx (the
+        cached rows and the 8 new ones), over all attention layers."""
+        n_attn = sum(self.is_attn(l) for l in range(self.n_layers))
+        return n_attn * 2 * self.Hkv * (ctx + 8) * self.D * 2

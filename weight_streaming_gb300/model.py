@@ -96,6 +96,58 @@ class SyntheticModel:
         torch.cuda.synchronize()
         self.model = V.vp_model(H, I, geom.eps, layers, head)
 
+    def attach_cores(self, lanes: int, cap: int, seed: int = 7):
+        """Attaches the real mixer cores with synthetic parameters and state, all drawn on the device
+        from one seeded generator: A and B ~ N(0,1)/sqrt(hidden) (bf16), convolution taps U(-0.6, 0.6),
+        A_log U(-2, 0), dt_bias U(-1, 1), the norm weights U(0.5, 1.5), delta-rule states 0.1 N(0,1),
+        convolution windows and cached keys / values N(0,1).  Caches hold `cap` positions per lane."""
+        g = self.geom
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(seed)
+        H, C = g.hidden, (2 * g.n_qk + g.n_v) * g.d
+        self.core_tensors = []
+
+        def keep(t):
+            self.core_tensors.append(t)
+            return t.data_ptr()
+
+        def normal(shape, std=1.0, dtype=torch.bfloat16):
+            return (torch.randn(shape, generator=gen, device="cuda") * std).to(dtype)
+
+        def uniform(shape, lo, hi, dtype=torch.float32):
+            return (torch.rand(shape, generator=gen, device="cuda") * (hi - lo) + lo).to(dtype)
+
+        descs = []
+        for l in range(g.n_layers):
+            c = V.vp_core_desc()
+            if g.is_attn(l):
+                c.q_norm = keep(uniform(g.D, 0.5, 1.5))
+                c.k_norm = keep(uniform(g.D, 0.5, 1.5))
+                c.k_cache = keep(normal((lanes, g.Hkv, cap, g.D)))
+                c.v_cache = keep(normal((lanes, g.Hkv, cap, g.D)))
+            else:
+                c.w_a = keep(normal((g.n_v, H), H ** -0.5))
+                c.w_b = keep(normal((g.n_v, H), H ** -0.5))
+                c.conv_taps = keep(uniform((C, 4), -0.6, 0.6, torch.bfloat16))
+                c.a_log = keep(uniform(g.n_v, -2.0, 0.0))
+                c.dt_bias = keep(uniform(g.n_v, -1.0, 1.0))
+                c.norm_w = keep(uniform(g.d, 0.5, 1.5))
+                c.state_a = keep(normal((lanes, g.n_v, g.d, g.d), 0.1, torch.float32))
+                c.state_b = keep(torch.zeros((lanes, g.n_v, g.d, g.d), device="cuda"))
+                c.window_a = keep(normal((lanes, 3, C)))
+                c.conv_hist = keep(torch.zeros((lanes, 11, C), dtype=torch.bfloat16, device="cuda"))
+            descs.append(c)
+        torch.cuda.synchronize()
+        V.vp_model_set_cores(self.model, V.vp_core_geom(g.n_qk, g.n_v, g.d, g.Hq, g.Hkv, g.D, cap), descs)
+
+    def cores_workspace(self, M: int) -> torch.Tensor:
+        return torch.zeros(V.vp_pass_cores_workspace_bytes(self.model, M), dtype=torch.uint8, device="cuda")
+
+    def run_cores(self, x0, ctx, pending, argmax, n_commit, committed, ws, trace=None, logits=None, stream=None):
+        M = x0.shape[0]
+        V.vp_verify_pass_cores(self.model, x0, M, ctx, pending, argmax, n_commit, committed, trace, logits, ws,
+                               stream)
+
     def workspace(self, M: int) -> torch.Tensor:
         n = V.vp_pass_workspace_bytes(self.model, M)
         return torch.zeros(n, dtype=torch.uint8, device="cuda")
