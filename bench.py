@@ -522,9 +522,9 @@ def measure_head_accept(lanes_list, steps: int, warmup: int) -> dict:
 
 def measure_cores_pass(sm, M_list, ctx: int, steps: int, warmup: int) -> dict:
     """The verify pass with the real mixer cores (vp_verify_pass_cores) at each M, every lane at
-    context ctx: CUDA-graph replays, CUDA events.  The state the pass writes (state_b, the
-    convolution history, cache rows ctx .. ctx + 7) is the same every replay, so replays repeat the
-    same work.  Weight GB/s counts the projection weights only; the cores' own reads (the
+    context ctx: CUDA-graph replays, CUDA events; alone, and followed by the commit of the rows it
+    accepted (vp_commit_cores).  Every replay reads parity buffer A and the same window and cache
+    rows and rewrites the same outputs, so replays repeat the same work.  Weight GB/s counts the projection weights only; the cores' own reads (the
     key / value cache rows, the delta-rule states) are reported beside it."""
     import numpy as np
     import torch
@@ -546,10 +546,16 @@ def measure_cores_pass(sm, M_list, ctx: int, steps: int, warmup: int) -> dict:
         ws = sm.cores_workspace(M)
         tp = graph_time(lambda: sm.run_cores(x0, ctx_d, pend, am, nc, cm, ws), steps, warmup)
         assert V.vp_read_status(ws) == V.VP_OK
+
+        def step():  # the pass, then the commit of the rows it accepted (parity 0 both times)
+            sm.run_cores(x0, ctx_d, pend, am, nc, cm, ws)
+            sm.commit_cores(M, nc, 0, ws)
+        tpc = graph_time(step, steps, warmup)
+        assert V.vp_read_status(ws) == V.VP_OK
         nb = geom.pass_bytes()
         n_gdn = sum(not geom.is_attn(l) for l in range(geom.n_layers))
         state = n_gdn * lanes * geom.n_v * geom.d * geom.d * 4 * 2  # read state_a, write state_b
-        out[f"M{M}"] = {"ms_per_pass": tp * 1e3, "weight_gbps": nb / tp / 1e9,
+        out[f"M{M}"] = {"ms_per_pass": tp * 1e3, "ms_per_pass_and_commit": tpc * 1e3, "weight_gbps": nb / tp / 1e9,
                         "kv_cache_bytes": lanes * geom.kv_bytes(ctx), "state_bytes": state,
                         "all_bytes_gbps": (nb + lanes * geom.kv_bytes(ctx) + state) / tp / 1e9,
                         "launches_per_pass": V.vp_pass_cores_launch_count(sm.model)}

@@ -372,12 +372,14 @@ vp_status vp_verify_pass_sampled(const vp_model* model, const void* x0, int M, c
  *     cache position ctx[lane] + j (base 10000), bf16; then vp_attention_verify (append k, v at ctx ..
  *     ctx + 7, causal softmax over the cache, times sigmoid(gate)) into the o-projection.
  * Rounding: bf16 at the projection outputs, the cores' inputs and outputs, and the residual.
- * State: the caller owns it (device memory, per layer); the pass reads state_a / window_a / the cache
- * rows before ctx and writes state_b (the state after all 8 rows), conv_hist (window_a's 3 rows then
- * the 8 rows' conv inputs: the window after n accepted rows is rows n .. n + 2) and the cache rows ctx
- * .. ctx + 7.  After a partial accept the caller re-scans the n committed rows from state_a with
- * vp_gdn_scan and takes the window from conv_hist.  d = 128 (the scan), D = 256 (the attention core),
- * Hq / Hkv <= 8, ctx[lane] + 8 <= cap. */
+ * State [BS-gdn]: the caller owns it (device memory, per layer).  The recurrent state is
+ * double-buffered by step parity: a pass of parity p reads buffer p (0: state_a, 1: state_b) and writes
+ * the other (the state after all 8 rows); it reads window_a and the cache rows before ctx, and writes
+ * conv_hist (window_a's 3 rows then the 8 rows' conv inputs) and the cache rows ctx .. ctx + 7.  After
+ * the acceptance, vp_commit_cores with the same parity re-scans each lane's n_commit rows from the
+ * intact buffer p into the other one and rewrites window_a with rows n_commit .. n_commit + 2 of
+ * conv_hist; the next pass then runs with parity 1 - p at ctx + n_commit.  d = 128 (the scan), D = 256
+ * (the attention core), Hq / Hkv <= 8, ctx[lane] + 8 <= cap, hidden <= 8192. */
 typedef struct {
   /* Gated DeltaNet layers */
   const void* w_a;       /* bf16 [n_v][hidden], 16-byte aligned */
@@ -386,10 +388,10 @@ typedef struct {
   const float* a_log;    /* fp32 [n_v] */
   const float* dt_bias;  /* fp32 [n_v] */
   const float* norm_w;   /* fp32 [d]: the gated RMSNorm's weight */
-  const float* state_a;  /* fp32 [lanes][n_v][d][d] (parity buffer A: read) */
-  float* state_b;        /* fp32 [lanes][n_v][d][d] (parity buffer B: written) */
-  const void* window_a;  /* bf16 [lanes][3][(2 n_qk + n_v) d] */
-  void* conv_hist;       /* bf16 [lanes][11][(2 n_qk + n_v) d] (written) */
+  float* state_a;        /* fp32 [lanes][n_v][d][d]: parity buffer A (read at parity 0, written at 1) */
+  float* state_b;        /* fp32 [lanes][n_v][d][d]: parity buffer B (written at parity 0, read at 1) */
+  void* window_a;        /* bf16 [lanes][3][(2 n_qk + n_v) d] (read by the pass, rewritten by the commit) */
+  void* conv_hist;       /* bf16 [lanes][11][(2 n_qk + n_v) d] (written by the pass) */
   /* attention layers */
   const float* q_norm;   /* fp32 [D] */
   const float* k_norm;   /* fp32 [D] */
@@ -411,19 +413,31 @@ vp_status vp_model_set_cores(vp_model* model, const vp_core_geom* geom, const vp
 /* Workspace bytes of vp_verify_pass_cores at M rows (0 if the model has no cores or M is invalid). */
 size_t vp_pass_cores_workspace_bytes(const vp_model* model, int M);
 /* The verify pass with the real mixer cores (arguments as vp_verify_pass; ctx: device int32 [lanes],
- * the cached positions per lane).  Launches: one executor program per layer boundary and the cores'
- * kernels in between, all on `stream`, nothing read back to the host: capturable into a CUDA graph.
- * The attention core reports a lane whose ctx + 8 exceeds cap in the workspace's status word
- * (VP_ERR_SHAPE; that lane's cache is left as it is). */
-vp_status vp_verify_pass_cores(const vp_model* model, const void* x0, int M, const int32_t* ctx,
+ * the cached positions per lane; parity 0 or 1, see above, else VP_ERR_INVALID_ARG).  Launches: one
+ * executor program per layer boundary and the cores' kernels in between, all on `stream`, nothing read
+ * back to the host: capturable into a CUDA graph.  The workspace keeps each Gated DeltaNet layer's scan
+ * inputs (q, k, v, alpha, beta of the 8 rows) for vp_commit_cores.  The attention core reports a lane
+ * whose ctx + 8 exceeds cap in the workspace's status word (VP_ERR_SHAPE; that lane's cache is left as
+ * it is). */
+vp_status vp_verify_pass_cores(const vp_model* model, const void* x0, int M, const int32_t* ctx, int parity,
                                const int32_t* pending, int32_t* argmax, int32_t* n_commit, int32_t* committed,
                                void* trace, float* logits, void* ws, size_t ws_bytes, void* stream);
+/* The commit of a pass of the given parity [BS-gdn]: for every Gated DeltaNet layer and lane, the
+ * gated delta rule over the lane's first n_commit[lane] rows (device int32 [M / 8], clamped to 0..8)
+ * from the intact parity buffer into the other, from the inputs the pass kept in `ws` (the same
+ * arithmetic as the pass's scan: n_commit = 8 reproduces the pass's state bit for bit), and the next
+ * window, rows n .. n + 2 of conv_hist, into window_a.  Run it after vp_verify_pass_cores on the same
+ * stream and workspace, before the next pass.  One launch per 48 Gated DeltaNet layers; nothing read
+ * back to the host.  Errors: VP_ERR_INVALID_ARG (no cores, NULL, parity), VP_ERR_SHAPE (M),
+ * VP_ERR_ALIGNMENT, VP_ERR_WORKSPACE. */
+vp_status vp_commit_cores(const vp_model* model, int M, const int32_t* n_commit, int parity, void* ws,
+                          size_t ws_bytes, void* stream);
 
 /* Kernel launches that vp_verify_pass_cores enqueues for a model with cores (0 without): one
  * executor program per segment (the first in-projection, then the 4 phases after each layer's
- * core, the last with the head), 5 per Gated DeltaNet core (A/B projections, convolution + norms,
- * gates, scan, gated norm) and 4 per attention core (prep, cache append, partitions, merge), after
- * one device-to-device copy of x0. */
+ * core, the last with the head), 1 per Gated DeltaNet core (A/B projections and gates, convolution
+ * and norms, the scan and the gated norm in one launch of 4-CTA clusters) and 4 per attention core
+ * (prep, cache append, partitions, merge), after one device-to-device copy of x0. */
 int vp_pass_cores_launch_count(const vp_model* model);
 
 /* Blocks [block_begin, block_end) of the pass on a caller-owned residual stream h (bf16

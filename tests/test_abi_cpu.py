@@ -268,6 +268,61 @@ def test_model_create_validation_without_gpu(V):
         V.vp_model(256, 512, 1e-6, [bad], head)
 
 
+def _core(V, gdn=True, **kw):
+    c = V.vp_core_desc()
+    names = ("w_a", "w_b", "conv_taps", "a_log", "dt_bias", "norm_w", "state_a", "state_b", "window_a", "conv_hist") \
+        if gdn else ("q_norm", "k_norm", "k_cache", "v_cache")
+    for n in names:
+        setattr(c, n, kw.get(n, FAKE))
+    return c
+
+
+def test_cores_validation_without_gpu(V):
+    """vp_model_set_cores checks the widths against the core geometry, the pointers and their
+    alignment; the cores pass and its commit check parity, rows and workspace before launching."""
+    L = V.lib()
+    head = V.vp_head_desc(FAKE, 1.0, 2048)
+    # layer 0 Gated DeltaNet (n_qk = n_v = 1, d = 128), layer 1 attention (Hq = Hkv = 1, D = 256)
+    layers = [_layer(V, 0, 512, 128), _layer(V, 1, 512, 256, 512)]
+    m = V.vp_model(256, 512, 1e-6, layers, head)
+    geom = V.vp_core_geom(1, 1, 128, 1, 1, 256, 64)
+    assert V.vp_pass_cores_workspace_bytes(m, 8) == 0  # no cores yet
+    assert L.vp_verify_pass_cores(m.handle, FAKE, 8, FAKE, 0, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 30,
+                                  None) == V.VP_ERR_INVALID_ARG
+    arr = lambda cs: (V.vp_core_desc * 2)(*cs)  # noqa: E731
+    set_cores = lambda g, cs, n=2: L.vp_model_set_cores(m.handle, ctypes.byref(g), arr(cs), n)  # noqa: E731
+    good = [_core(V), _core(V, gdn=False)]
+    assert set_cores(geom, good, 1) == V.VP_ERR_INVALID_ARG                       # one descriptor per layer
+    assert set_cores(V.vp_core_geom(1, 2, 128, 1, 1, 256, 64), good) == V.VP_ERR_SHAPE  # GDN widths
+    assert set_cores(V.vp_core_geom(1, 1, 64, 1, 1, 256, 64), good) == V.VP_ERR_SHAPE   # d != 128
+    assert set_cores(V.vp_core_geom(1, 1, 128, 2, 1, 256, 64), good) == V.VP_ERR_SHAPE  # attention widths
+    assert set_cores(geom, [_core(V, w_b=None), good[1]]) == V.VP_ERR_INVALID_ARG
+    assert set_cores(geom, [_core(V, w_a=FAKE + 2), good[1]]) == V.VP_ERR_ALIGNMENT    # A / B need 16 bytes
+    assert set_cores(geom, [good[0], _core(V, gdn=False, k_cache=FAKE + 8)]) == V.VP_ERR_ALIGNMENT
+    assert set_cores(geom, good) == V.VP_OK
+    wb = V.vp_pass_cores_workspace_bytes(m, 8)
+    assert wb > V.vp_pass_workspace_bytes(m, 8)
+    assert V.vp_pass_cores_workspace_bytes(m, 12) == 0 and V.vp_pass_cores_workspace_bytes(m, 40) == 0
+    # launches: 3 executor programs ([in 0], then 4 phases after each core), 1 GDN core, 4 attention
+    assert V.vp_pass_cores_launch_count(m) == 3 + 1 + 4
+    pc = lambda **kw: L.vp_verify_pass_cores(  # noqa: E731
+        m.handle, FAKE, kw.get("M", 8), FAKE, kw.get("parity", 0), FAKE, FAKE, FAKE, FAKE, None, None, FAKE,
+        kw.get("wb", wb), None)
+    assert pc(parity=2) == V.VP_ERR_INVALID_ARG and pc(parity=-1) == V.VP_ERR_INVALID_ARG
+    assert pc(wb=wb - 1) == V.VP_ERR_WORKSPACE
+    assert pc(M=12, wb=1 << 30) == V.VP_ERR_SHAPE
+    cc = lambda **kw: L.vp_commit_cores(m.handle, kw.get("M", 8), kw.get("nc", FAKE), kw.get("parity", 0),  # noqa: E731
+                                         kw.get("ws", FAKE), kw.get("wb", wb), None)
+    assert cc(parity=2) == V.VP_ERR_INVALID_ARG and cc(nc=None) == V.VP_ERR_INVALID_ARG
+    assert cc(M=12) == V.VP_ERR_SHAPE and cc(M=0) == V.VP_ERR_SHAPE
+    assert cc(ws=FAKE + 16) == V.VP_ERR_ALIGNMENT and cc(nc=FAKE + 2) == V.VP_ERR_ALIGNMENT
+    assert cc(wb=wb - 1) == V.VP_ERR_WORKSPACE
+    m.close()
+    m2 = V.vp_model(256, 512, 1e-6, layers, head)  # a model without cores has nothing to commit
+    assert L.vp_commit_cores(m2.handle, 8, FAKE, 0, FAKE, 1 << 30, None) == V.VP_ERR_INVALID_ARG
+    m2.close()
+
+
 def test_phase_trace_only_in_traced_build(V):
     """The phase timeline is recorded only by the VP_PHASE_TRACE build; the product library says so
     without touching a device."""

@@ -134,7 +134,7 @@ def test_cores_pass_matches_oracle_blocks(V, cfg, lanes, cap, ctx):
     lg = torch.empty((M, G.vocab), dtype=torch.float32, device="cuda")
     trace = torch.empty((4, M, H), dtype=torch.bfloat16, device="cuda")
     ws = workspace(V.vp_pass_cores_workspace_bytes(dm.model, M))
-    V.vp_verify_pass_cores(dm.model, dev_bf16(x0), M, dev_i32(ctx), dev_i32(pending), am, nc, cm, trace, lg, ws)
+    V.vp_verify_pass_cores(dm.model, dev_bf16(x0), M, dev_i32(ctx), 0, dev_i32(pending), am, nc, cm, trace, lg, ws)
     torch.cuda.synchronize()
     assert V.vp_read_status(ws) == V.VP_OK
     tr = host_bf16_bits(trace)
@@ -213,7 +213,74 @@ def test_cores_pass_is_deterministic(V):
         cm = torch.empty((lanes, 8), dtype=torch.int32, device="cuda")
         lg = torch.empty((M, G.vocab), dtype=torch.float32, device="cuda")
         ws = workspace(V.vp_pass_cores_workspace_bytes(dm.model, M))
-        V.vp_verify_pass_cores(dm.model, x0, M, ctx, pend, am, nc, cm, None, lg, ws)
+        V.vp_verify_pass_cores(dm.model, x0, M, ctx, 0, pend, am, nc, cm, None, lg, ws)
         torch.cuda.synchronize()
         outs.append((lg.clone(), dg["state_b"].clone()))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("cfg,lanes,cap,ctx,keep", [(SMALL, 2, 64, [5, 40], [3, 8]),
+                                                   (PAGES, 4, 1100, [0, 77, 1030, 500], [1, 8, 5, 2])])
+def test_cores_commit_then_next_pass(V, cfg, lanes, cap, ctx, keep):
+    """A pass of parity 0, the commit of `keep` rows per lane, then a pass of parity 1 at ctx + keep."""
+    M = 8 * lanes
+    G, layers, head, gd, at, dm, dg, da, _ = build(V, cfg, lanes, cap, seed=71 + lanes)
+    H, nqk, nv = cfg["hidden"], cfg["n_qk"], cfg["n_v"]
+    g = {"hidden": H, "n_qk": nqk, "n_v": nv, "d": D_GDN}
+    d0 = layers[0]
+    wts = {"in": d0["in"], "s_in": d0["s_in"], "out": d0["out"], "s_out": d0["s_out"], "A": gd["A"], "B": gd["B"],
+           "taps": bfv(gd["taps"]), "A_log": gd["A_log"].astype(np.float64),
+           "dt_bias": gd["dt_bias"].astype(np.float64), "w_norm": gd["w_norm"].astype(np.float64)}
+    ws = workspace(V.vp_pass_cores_workspace_bytes(dm.model, M))
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    nc = torch.empty(lanes, dtype=torch.int32, device="cuda")
+    cm = torch.empty((lanes, 8), dtype=torch.int32, device="cuda")
+    pend = dev_i32(np.zeros(M, np.int32))
+    x0 = synth.normal_bf16(90 + M, synth.stream_id(0, synth.T_X0), (M, H))
+    V.vp_verify_pass_cores(dm.model, dev_bf16(x0), M, dev_i32(np.asarray(ctx, np.int32)), 0, pend, am, nc, cm, None,
+                           None, ws)
+    torch.cuda.synchronize()
+    assert V.vp_read_status(ws) == V.VP_OK
+    state_a0 = dg["state_a"].clone()
+    sb_pass = dg["state_b"].cpu().numpy()
+    hist = dg["hist"].cpu().numpy().view(np.uint16)
+    V.vp_commit_cores(dm.model, M, dev_i32(np.asarray(keep, np.int32)), 0, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(dg["state_a"], state_a0)  # the intact buffer
+    sb = dg["state_b"].cpu().numpy()
+    win = dg["window"].cpu().numpy().view(np.uint16)
+    for l in range(lanes):
+        n = keep[l]
+        assert np.array_equal(win[l], hist[l, n:n + 3]), ("window", l)
+        if n == 8:
+            assert np.array_equal(sb[l], sb_pass[l]), ("a full commit reproduces the pass's state", l)
+        _, st, wref, _ = gdn_block(x0[8 * l:8 * l + 8], g, wts, gd["state"][l].astype(np.float64),
+                                   bfv(gd["window"][l]), rows=n)
+        tol = 2.0 ** -6 * np.abs(st).max()
+        assert np.abs(sb[l] - st).max() <= tol, ("state after the committed rows", l, n)
+        _, a_u = oracle.linear(oracle.FP8, oracle.rmsnorm(x0[8 * l:8 * l + 8], G.eps), d0["in"], None, d0["s_in"],
+                               (2 * nqk + nv) * D_GDN)
+        rows_w = [r - 3 for r in range(n, n + 3) if r >= 3]  # window rows that come from the pass's u
+        if rows_w:
+            ww = bfv(win[l][3 - len(rows_w):])
+            wr = wref[3 - len(rows_w):]
+            bound = REL * a_u[rows_w] + 2.0 ** -7 * np.abs(wr) + 1e-30
+            assert np.all(np.abs(ww - wr) <= bound), ("window against the oracle", l)
+    # the next pass, parity 1: reads state_b and the new window, writes state_a
+    sb_t = dg["state_b"].clone()
+    ctx1 = np.asarray(ctx, np.int32) + np.asarray(keep, np.int32)
+    x1 = synth.normal_bf16(95 + M, synth.stream_id(0, synth.T_X0), (M, H))
+    trace = torch.empty((4, M, H), dtype=torch.bfloat16, device="cuda")
+    V.vp_verify_pass_cores(dm.model, dev_bf16(x1), M, dev_i32(ctx1), 1, pend, am, nc, cm, trace, None, ws)
+    torch.cuda.synchronize()
+    assert V.vp_read_status(ws) == V.VP_OK
+    assert torch.equal(dg["state_b"], sb_t)  # read only at parity 1
+    tr = host_bf16_bits(trace)
+    sa = dg["state_a"].cpu().numpy()
+    for l in range(lanes):
+        rows = slice(8 * l, 8 * l + 8)
+        on = []
+        h_ref, st, _, _ = gdn_block(x1[rows], g, wts, sb[l].astype(np.float64), bfv(win[l]), core_out=on)
+        within(tr[0][rows], h_ref, core_budget(on[0], d0["out"], d0["s_out"], H, h_ref, D_GDN, 8),
+               f"GDN block of the parity-1 pass, lane {l}")
+        assert np.abs(sa[l] - st).max() <= 2.0 ** -6 * np.abs(st).max(), ("state after the parity-1 pass", l)

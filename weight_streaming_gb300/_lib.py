@@ -28,7 +28,7 @@ EXPORTS = [
     "vp_linear_nvfp4_noalloc", "vp_noalloc_read_status", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
     "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
     "vp_commit_append", "vp_decode_steps", "vp_pass_sampled_workspace_bytes", "vp_verify_pass_sampled",
-    "vp_model_set_cores", "vp_pass_cores_workspace_bytes", "vp_verify_pass_cores", "vp_pass_cores_launch_count",
+    "vp_model_set_cores", "vp_pass_cores_workspace_bytes", "vp_verify_pass_cores", "vp_pass_cores_launch_count", "vp_commit_cores",
 ]
 
 
@@ -112,7 +112,8 @@ def _load():
         "vp_verify_pass_sampled": (I, [P, P, I, P, F, I, F, P, P, P, P, P, P, P, P, S, P]),
         "vp_model_set_cores": (I, [P, ctypes.POINTER(vp_core_geom), ctypes.POINTER(vp_core_desc), I]),
         "vp_pass_cores_workspace_bytes": (S, [P, I]),
-        "vp_verify_pass_cores": (I, [P, P, I, P, P, P, P, P, P, P, P, S, P]),
+        "vp_verify_pass_cores": (I, [P, P, I, P, I, P, P, P, P, P, P, P, S, P]),
+        "vp_commit_cores": (I, [P, I, P, I, P, S, P]),
         "vp_pass_cores_launch_count": (I, [P]),
     }
     for name, (res, args) in sig.items():
@@ -361,12 +362,19 @@ def vp_pass_cores_launch_count(model: vp_model) -> int:
     return _L.vp_pass_cores_launch_count(model.handle)
 
 
-def vp_verify_pass_cores(model: vp_model, x0, M: int, ctx, pending, argmax, n_commit, committed, trace, logits, ws,
-                         stream=None, ws_bytes=None):
+def vp_verify_pass_cores(model: vp_model, x0, M: int, ctx, parity: int, pending, argmax, n_commit, committed, trace,
+                         logits, ws, stream=None, ws_bytes=None):
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check("vp_verify_pass_cores",
-           _L.vp_verify_pass_cores(model.handle, _ptr(x0), M, _ptr(ctx), _ptr(pending), _ptr(argmax), _ptr(n_commit),
-                                   _ptr(committed), _ptr(trace), _ptr(logits), _ptr(ws), wb, _stream(stream)))
+           _L.vp_verify_pass_cores(model.handle, _ptr(x0), M, _ptr(ctx), parity, _ptr(pending), _ptr(argmax),
+                                   _ptr(n_commit), _ptr(committed), _ptr(trace), _ptr(logits), _ptr(ws), wb,
+                                   _stream(stream)))
+
+
+def vp_commit_cores(model: vp_model, M: int, n_commit, parity: int, ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_commit_cores", _L.vp_commit_cores(model.handle, M, _ptr(n_commit), parity, _ptr(ws), wb,
+                                                 _stream(stream)))
 
 
 def vp_verify_blocks(model: vp_model, h, M: int, block_begin: int, block_end: int, trace, ws, stream=None,

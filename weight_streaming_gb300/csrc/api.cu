@@ -871,13 +871,13 @@ PassWs pass_ws(const vp_model* md, int M) {
 // The cores pass's workspace: the pass's, then the in-projections kept whole and the cores' scratch.
 struct CoresWs {
   PassWs P;
-  size_t u, alpha, beta, q, k, v, o, rows8, aq, ak, av, ag, attn, total;
+  size_t u, aq, ak, av, ag, attn, rec, rec_qk, rec_v, rec_ab, rec_layer, total;
 };
 CoresWs cores_ws(const vp_model* md, int M) {
   CoresWs w;
   w.P = pass_ws(md, M);
   const vp_core_geom& g = md->cg;
-  const size_t gv = (size_t)M * g.n_v, gd = gv * g.d, hq = (size_t)M * g.Hq * g.D, hk = (size_t)M * g.Hkv * g.D;
+  const size_t hq = (size_t)M * g.Hq * g.D, hk = (size_t)M * g.Hkv * g.D;
   size_t off = w.P.total;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -885,18 +885,19 @@ CoresWs cores_ws(const vp_model* md, int M) {
     return at;
   };
   w.u = take(sizeof(uint16_t) * (size_t)M * md->umax);
-  w.alpha = take(sizeof(float) * gv);
-  w.beta = take(sizeof(float) * gv);
-  w.q = take(sizeof(uint16_t) * gd);
-  w.k = take(sizeof(uint16_t) * gd);
-  w.v = take(sizeof(uint16_t) * gd);
-  w.o = take(sizeof(float) * gd);
-  w.rows8 = take(sizeof(int32_t) * (kMaxM / 8));
   w.aq = take(sizeof(uint16_t) * hq);
   w.ag = take(sizeof(uint16_t) * hq);
   w.ak = take(sizeof(uint16_t) * hk);
   w.av = take(sizeof(uint16_t) * hk);
   w.attn = take(g.Hkv > 0 && g.cap >= 8 ? attn_ws_layout(M, g.Hkv, g.cap).total : 0);
+  // per Gated DeltaNet layer, the scan's recorded inputs for the commit re-scan
+  w.rec_qk = 0;
+  w.rec_v = align_up(sizeof(uint16_t) * (size_t)M * 2 * g.n_qk * g.d, 256);
+  w.rec_ab = align_up(w.rec_v + sizeof(uint16_t) * (size_t)M * g.n_v * g.d, 256);
+  w.rec_layer = align_up(w.rec_ab + sizeof(float) * (size_t)M * g.n_v * 2, 256);
+  int n_gdn = 0;
+  for (const vp_layer_desc& d : md->layers) n_gdn += d.kind == VP_LAYER_GDN;
+  w.rec = take(w.rec_layer * n_gdn);
   w.total = off;
   return w;
 }
@@ -1079,10 +1080,10 @@ size_t vp_pass_cores_workspace_bytes(const vp_model* model, int M) {
   return cores_ws(model, M).total;
 }
 
-vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const int32_t* ctx, const int32_t* pending,
-                               int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace, float* logits,
-                               void* ws, size_t ws_bytes, void* stream) {
-  if (!md || !md->has_cores || !ctx) return VP_ERR_INVALID_ARG;
+vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const int32_t* ctx, int parity,
+                               const int32_t* pending, int32_t* argmax, int32_t* n_commit, int32_t* committed,
+                               void* trace, float* logits, void* ws, size_t ws_bytes, void* stream) {
+  if (!md || !md->has_cores || !ctx || (parity != 0 && parity != 1)) return VP_ERR_INVALID_ARG;
   if (!aligned(ctx, 4)) return VP_ERR_ALIGNMENT;
   if (M >= 8 && M <= kMaxM && M % 8 == 0 && ws_bytes < cores_ws(md, M).total) return VP_ERR_WORKSPACE;
   int sms = 0;
@@ -1118,6 +1119,7 @@ vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const 
   uint16_t* zb = static_cast<uint16_t*>(io.buf[kBufZ]);
   // Program segments: [in(0)], then per layer l: its core, then [out(l), gate+up(l), down(l), in(l + 1)]
   // (the head after the last layer's down).
+  int gdn_index = 0;
   for (int l = 0; l <= L; ++l) {
     const int p0 = l == 0 ? 0 : 4 * (l - 1) + 1, p1 = l == 0 ? 1 : 4 * l + 1;
     std::vector<Phase> seg(all.begin() + p0, all.begin() + p1);
@@ -1127,24 +1129,31 @@ vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const 
     const vp_core_desc& c = md->cores[l];
     const int ld_u = d.n_in + (d.kind == VP_LAYER_ATTN ? d.n_kv : 0);
     if (d.kind == VP_LAYER_GDN) {
-      const int cq = g.n_qk * g.d, cv = g.n_v * g.d;
-      float *al = reinterpret_cast<float*>(b + w.alpha), *be = reinterpret_cast<float*>(b + w.beta);
-      uint16_t *q = reinterpret_cast<uint16_t*>(b + w.q), *k = reinterpret_cast<uint16_t*>(b + w.k);
-      uint16_t* v = reinterpret_cast<uint16_t*>(b + w.v);
-      float* o = reinterpret_cast<float*>(b + w.o);
-      int32_t* rows8 = reinterpret_cast<int32_t*>(b + w.rows8);
-      if ((e = launch_ab_gates(h, md->hidden, M, md->eps, static_cast<const uint16_t*>(c.w_a),
-                               static_cast<const uint16_t*>(c.w_b), g.n_v, c.a_log, c.dt_bias, al, be, s)) !=
-          cudaSuccess)
-        return cuda_fail(e);
-      if ((e = launch_gdn_prep(u, ld_u, M, static_cast<const uint16_t*>(c.window_a),
-                               static_cast<const uint16_t*>(c.conv_taps), g.n_qk, g.n_v, g.d, q, k, v,
-                               static_cast<uint16_t*>(c.conv_hist), rows8, s)) != cudaSuccess)
-        return cuda_fail(e);
-      if ((st = vp_gdn_scan(c.state_a, c.state_b, q, k, v, al, be, rows8, M, g.n_v, g.d, g.d, o, stream)) != VP_OK)
-        return st;
-      if ((e = launch_gated_norm(o, u, ld_u, 2 * cq + cv, c.norm_w, M, g.n_v, g.d, zb, s)) != cudaSuccess)
-        return cuda_fail(e);
+      GdnCoreArgs ga;
+      ga.h = h;
+      ga.hidden = md->hidden;
+      ga.eps = md->eps;
+      ga.u = u;
+      ga.ld_u = ld_u;
+      ga.z0 = (2 * g.n_qk + g.n_v) * g.d;
+      ga.window_a = static_cast<const uint16_t*>(c.window_a);
+      ga.taps = static_cast<const uint16_t*>(c.conv_taps);
+      ga.wa = static_cast<const uint16_t*>(c.w_a);
+      ga.wb = static_cast<const uint16_t*>(c.w_b);
+      ga.a_log = c.a_log;
+      ga.dt_bias = c.dt_bias;
+      ga.norm_w = c.norm_w;
+      ga.state_in = parity ? c.state_b : c.state_a;
+      ga.state_out = parity ? c.state_a : c.state_b;
+      ga.conv_hist = static_cast<uint16_t*>(c.conv_hist);
+      ga.out = zb;
+      uint8_t* rec = b + w.rec + w.rec_layer * gdn_index++;
+      ga.rec_qk = reinterpret_cast<uint16_t*>(rec + w.rec_qk);
+      ga.rec_v = reinterpret_cast<uint16_t*>(rec + w.rec_v);
+      ga.rec_ab = reinterpret_cast<float*>(rec + w.rec_ab);
+      ga.n_qk = g.n_qk;
+      ga.n_v = g.n_v;
+      if ((e = launch_gdn_core(ga, M / 8, s)) != cudaSuccess) return cuda_fail(e);
     } else {
       uint16_t *aq = reinterpret_cast<uint16_t*>(b + w.aq), *ag = reinterpret_cast<uint16_t*>(b + w.ag);
       uint16_t *ak = reinterpret_cast<uint16_t*>(b + w.ak), *av = reinterpret_cast<uint16_t*>(b + w.av);
@@ -1170,14 +1179,52 @@ vp_status vp_verify_pass_cores(const vp_model* md, const void* x0, int M, const 
   return VP_OK;
 }
 
+vp_status vp_commit_cores(const vp_model* md, int M, const int32_t* n_commit, int parity, void* ws, size_t ws_bytes,
+                          void* stream) {
+  if (!md || !md->has_cores || !n_commit || !ws || (parity != 0 && parity != 1)) return VP_ERR_INVALID_ARG;
+  if (M < 8 || M > kMaxM || M % 8) return VP_ERR_SHAPE;
+  if (!aligned(ws, 256) || !aligned(n_commit, 4)) return VP_ERR_ALIGNMENT;
+  const CoresWs w = cores_ws(md, M);
+  if (ws_bytes < w.total) return VP_ERR_WORKSPACE;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  static thread_local GdnCommitArgs ca;  // ~2.7 KB: kept off the stack
+  ca.n_commit = n_commit;
+  ca.lanes = M / 8;
+  ca.n_qk = md->cg.n_qk;
+  ca.n_v = md->cg.n_v;
+  int n = 0, gdn_index = 0;
+  for (int l = 0; l < (int)md->layers.size(); ++l) {
+    if (md->layers[l].kind != VP_LAYER_GDN) continue;
+    const vp_core_desc& c = md->cores[l];
+    GdnCommitLayer& L = ca.layer[n++];
+    L.state_in = parity ? c.state_b : c.state_a;
+    L.state_out = parity ? c.state_a : c.state_b;
+    L.conv_hist = static_cast<const uint16_t*>(c.conv_hist);
+    L.window = static_cast<uint16_t*>(c.window_a);
+    const uint8_t* rec = b + w.rec + w.rec_layer * gdn_index++;
+    L.rec_qk = reinterpret_cast<const uint16_t*>(rec + w.rec_qk);
+    L.rec_v = reinterpret_cast<const uint16_t*>(rec + w.rec_v);
+    L.rec_ab = reinterpret_cast<const float*>(rec + w.rec_ab);
+    if (n == kCommitLayers) {
+      const cudaError_t e = launch_gdn_commit(ca, n, (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(e);
+      n = 0;
+    }
+  }
+  if (n > 0) {
+    const cudaError_t e = launch_gdn_commit(ca, n, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return VP_OK;
+}
+
 int vp_pass_cores_launch_count(const vp_model* md) {
   if (!md || !md->has_cores) return 0;
   // one executor program per segment (the in-projection of layer 0, then 4 phases per layer, the
-  // last with the head), then per Gated DeltaNet layer the A/B projections, the convolution + norms,
-  // the gates, the scan and the gated norm; per attention layer the prep, the cache append, the
-  // partitions and the merge
+  // last with the head), then per Gated DeltaNet layer its whole core (one cluster launch); per
+  // attention layer the prep, the cache append, the partitions and the merge
   int n = program_launches(1);
-  for (const vp_layer_desc& d : md->layers) n += program_launches(4) + (d.kind == VP_LAYER_GDN ? 5 : 4);
+  for (const vp_layer_desc& d : md->layers) n += program_launches(4) + (d.kind == VP_LAYER_GDN ? 1 : 4);
   return n;
 }
 

@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "errors.h"
+#include "gdn_step.cuh"
 #include "internal.h"
 #include "verify.h"
 
@@ -32,11 +33,11 @@ namespace vp {
 
 namespace {
 
-constexpr int kDk = 128, kDv = 128;
+constexpr int kDk = kGdnDk, kDv = kGdnDv;
 constexpr int kRowsPerCta = 32;   // rows of S per CTA
-constexpr int kSeg = 16;          // entries of a row per thread (8 threads per row)
+constexpr int kSeg = kGdnSeg;     // entries of a row per thread (8 threads per row)
 constexpr int kThreadsG = kRowsPerCta * (kDk / kSeg);  // 256
-constexpr int kTpr = kDk / kSeg;  // threads per row
+constexpr int kTpr = kGdnTpr;     // threads per row
 
 __device__ __forceinline__ float bf(const uint16_t* p, size_t i) { return __uint_as_float((uint32_t)p[i] << 16); }
 
@@ -74,27 +75,9 @@ __global__ void __launch_bounds__(kThreadsG) gdn_scan_kernel(const float* __rest
 #pragma unroll
   for (int e = 0; e < kSeg; ++e) s[e] = state_in[so + kTpr * e];
   __syncthreads();
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j >= n) break;
-    const size_t rh = (size_t)(8 * l + j) * H + h;
-    const float a = sab[j][0], b = sab[j][1];
-    float u = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kSeg; ++e) u = fmaf(s[e], sk[j][c0 + kTpr * e], u);
-#pragma unroll
-    for (int m = 1; m < kTpr; m <<= 1) u += __shfl_xor_sync(0xffffffffu, u, m);
-    const float d = b * (vi[j] - a * u);
-    float o = 0.0f;
-#pragma unroll
-    for (int e = 0; e < kSeg; ++e) {
-      s[e] = fmaf(d, sk[j][c0 + kTpr * e], a * s[e]);
-      o = fmaf(s[e], sq[j][c0 + kTpr * e], o);
-    }
-#pragma unroll
-    for (int m = 1; m < kTpr; m <<= 1) o += __shfl_xor_sync(0xffffffffu, o, m);
-    if (out && c0 == 0) out[rh * kDv + i] = o;
-  }
+  gdn_scan_rows(s, sk, sq, sab, vi, n, c0, [&](int j, float o) {
+    if (out && c0 == 0) out[((size_t)(8 * l + j) * H + h) * kDv + i] = o;
+  });
 #pragma unroll
   for (int e = 0; e < kSeg; ++e) state_out[so + kTpr * e] = s[e];
 }

@@ -1,7 +1,7 @@
-// Producer and consumer steps of the pass's real mixer cores, between the executor's projections:
-// the Gated DeltaNet layer's A / B projections, short convolution, Q / K normalisation and gates
-// ahead of its delta-rule scan (gdn.cu) and its gated RMSNorm after it; the attention layer's Q / K
-// RMSNorm and rotary embedding ahead of its core over the KV cache (attention.cu).
+// The pass's real mixer cores between the executor's projections: the whole Gated DeltaNet core in one
+// launch (A / B projections and gates, short convolution, Q / K normalisation, the delta-rule scan of
+// gdn_step.cuh, the gated RMSNorm), and the attention layer's Q / K RMSNorm and rotary embedding
+// ahead of its core over the KV cache (attention.cu).
 //
 // Sources: "lithos-metal: per-layer megakernels for Qwen3.8-27B on an M5 Max" -- "The megakernel is
 // per layer, not per step" (the GDN layer: RMSNorm, FP8 QKV and Z projections, BF16 A / B
@@ -18,6 +18,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "gdn_step.cuh"
+
 #include <cstdint>
 
 #include "mixer.h"
@@ -30,168 +32,280 @@ __device__ __forceinline__ float bfv(uint16_t b) { return __uint_as_float((uint3
 __device__ __forceinline__ uint16_t to_bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
-// Sum of x over the block's threads (blockDim.x a multiple of 32, at most 1024), in a fixed order;
-// every thread gets the result.
-__device__ __forceinline__ float block_sum(float x, float* red) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[w] = x;
-  __syncthreads();
-  float s = 0.0f;
-  for (int i = 0; i < nw; ++i) s += red[i];
-  return s;
-}
+// ---------------------------------------------------------------- the Gated DeltaNet core
+// One cluster of 4 CTAs per (v head hv, lane); CTA rank rb of the cluster owns rows rb * 32 .. + 31
+// of the head's 128 x 128 state and quarter rb of K for the A / B projections.  The CTAs exchange
+// partial sums through distributed shared memory at cluster barriers (every CTA then adds the four
+// partials in rank order, so all four hold the same values):
+//  1. r_t = bf16(RMSNorm(h_t)) (unit weight): sums of squares of the rows' K quarters, exchanged;
+//     then the K quarter's dot products with A[hv] and B[hv], exchanged; alpha_t = exp(-exp(A_log)
+//     softplus(a + dt_bias)), beta_t = sigmoid(b);
+//  2. the causal depthwise 4-tap convolution of u's q, k, v channels over the lane's window (3 earlier
+//     rows) and its 8 rows (tap 3 on the current row), SiLU; q, k of q/k head hv / (n_v / n_qk) over
+//     their L2 norm (eps 1e-6 inside the root), bf16; v of the CTA's 32 channels, bf16; the
+//     convolution history (the window, then the 8 rows' inputs) of the channels the CTA owns;
+//  3. the delta rule over the 8 rows (gdn_step.cuh) from state_in into state_out; the scan's inputs
+//     (q, k per q/k head, v, alpha, beta) are recorded for the commit re-scan;
+//  4. the gated RMSNorm per row and head: o / sqrt(mean(o^2) + 1e-6) * norm_w * silu(z), the sum of
+//     squares over the head's 128 outputs exchanged, then bf16 into the out-projection's input.
+constexpr int kCoreThreads = 256, kCoreRows = 32, kCoreCta = 4;
 
-// A / B projections of a Gated DeltaNet layer on r = bf16(RMSNorm(h)) (unit weight), with the gates:
-// alpha[t][j] = exp(-exp(A_log[j]) softplus(r_t . A[j] + dt_bias[j])), beta[t][j] = sigmoid(r_t . B[j])
-// (fp32 [M][n_v]).  Block (j, g): weight row j (rows 0 .. n_v - 1 of A, then those of B) against rows
-// 4g .. 4g + 3.  Thread i holds 16-byte chunks i and i + 512 of K of the 4 rows in registers (all
-// loads issued at once), so the rows' statistic and the dot products read h once; both sums meet in a
-// fixed order (shuffle tree, then the 16 warps in order).  hidden % 8 == 0, hidden <= 8192.
-constexpr int kAbThreads = 512, kAbPer = 2, kAbRows = 4;
-__device__ __forceinline__ void ab_block_sum(float (&v)[kAbRows], float (*red)[kAbRows], float* out) {
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of all CTAs of the cluster: writes to shared memory before it are visible after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// p in CTA rank's shared memory (the same variable as p in this CTA's).
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+  const uint32_t a = (uint32_t)__cvta_generic_to_shared(p);
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
+  return v;
+}
+// Per-warp partial sums of n values (n <= 24) into red[warp][.], then thread i < n adds the warps
+// [w0, w1) in order; the caller synchronises before reading the result.
+template <int N>
+__device__ __forceinline__ void warp_partials(const float (&v)[N], float (*red)[24]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int t = 0; t < kAbRows; ++t) {
-    float x = v[t];
+  for (int e = 0; e < N; ++e) {
+    float x = v[e];
 #pragma unroll
     for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) red[warp][t] = x;
+    if (lane == 0) red[warp][e] = x;
   }
-  __syncthreads();
-  if (threadIdx.x < kAbRows) {
-    float x = 0.0f;
-    for (int w = 0; w < kAbThreads / 32; ++w) x += red[w][threadIdx.x];
-    out[threadIdx.x] = x;
-  }
-  __syncthreads();
 }
-__global__ void __launch_bounds__(kAbThreads) ab_gates_kernel(
-    const uint16_t* __restrict__ h, int hidden, int M, float eps, const uint16_t* __restrict__ wa,
-    const uint16_t* __restrict__ wb, int n_v, const float* __restrict__ a_log, const float* __restrict__ dt_bias,
-    float* __restrict__ alpha, float* __restrict__ beta) {
-  __shared__ float red[kAbThreads / 32][kAbRows];
-  __shared__ float sums[kAbRows];
-  const int j = blockIdx.x, t0 = blockIdx.y * kAbRows, tid = threadIdx.x, chunks = hidden / 8;
-  const uint16_t* w = j < n_v ? wa + (size_t)j * hidden : wb + (size_t)(j - n_v) * hidden;
-  uint4 hv[kAbPer][kAbRows], wv[kAbPer];
+
+__global__ void __cluster_dims__(kCoreCta, 1, 1) __launch_bounds__(kCoreThreads) gdn_core_kernel(const GdnCoreArgs a) {
+  __shared__ float sk[8][kGdnDk], sq[8][kGdnDk], sab[8][2], sv[8][kCoreRows], so[8][kCoreRows];
+  __shared__ float red[kCoreThreads / 32][24];
+  __shared__ float xp[8 + 16 + 8];  // exchanged partials: sums of squares of h, a and b, sums of o^2
+  __shared__ float inv[8], onorm[8];
+  const uint32_t rb = cluster_rank();
+  const int hv = blockIdx.y, l = blockIdx.z, tid = threadIdx.x, warp = tid >> 5;
+  const int n_qk = a.n_qk, n_v = a.n_v, C = (2 * n_qk + n_v) * kGdnDk, head_qk = hv / (n_v / n_qk);
+  const int i = rb * kCoreRows + tid / kGdnTpr, c0 = tid % kGdnTpr;  // state row and column phase
+  const size_t so_off = (((size_t)l * n_v + hv) * kGdnDv + i) * kGdnDk + c0;
+  float s[kGdnSeg];
 #pragma unroll
-  for (int p = 0; p < kAbPer; ++p) {
-    const int c = tid + p * kAbThreads;
-    const bool ok = c < chunks;
-    wv[p] = ok ? *reinterpret_cast<const uint4*>(w + 8 * c) : make_uint4(0, 0, 0, 0);
+  for (int e = 0; e < kGdnSeg; ++e) s[e] = a.state_in[so_off + kGdnTpr * e];
+
+  // 1. A / B projections and gates: chunk (8 values) rb * qc + tid of K, for the lane's 8 rows
+  const int qc = a.hidden / 32, ch = rb * qc + tid;
+  const bool kin = tid < qc;
+  uint4 hx[8];
 #pragma unroll
-    for (int t = 0; t < kAbRows; ++t)
-      hv[p][t] = ok && t0 + t < M ? *reinterpret_cast<const uint4*>(h + (size_t)(t0 + t) * hidden + 8 * c)
-                                  : make_uint4(0, 0, 0, 0);
-  }
-  float acc[kAbRows];
+  for (int t = 0; t < 8; ++t)
+    hx[t] = kin ? *reinterpret_cast<const uint4*>(a.h + (size_t)(8 * l + t) * a.hidden + 8 * ch) : make_uint4(0, 0, 0, 0);
+  {
+    float p[8];
 #pragma unroll
-  for (int t = 0; t < kAbRows; ++t) {
-    acc[t] = 0.0f;
-#pragma unroll
-    for (int p = 0; p < kAbPer; ++p) {
-      const uint32_t x4[4] = {hv[p][t].x, hv[p][t].y, hv[p][t].z, hv[p][t].w};
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t x4[4] = {hx[t].x, hx[t].y, hx[t].z, hx[t].w};
+      p[t] = 0.0f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float lo = __uint_as_float(x4[e] << 16), hi = __uint_as_float(x4[e] & 0xFFFF0000u);
-        acc[t] = fmaf(lo, lo, acc[t]);
-        acc[t] = fmaf(hi, hi, acc[t]);
+        p[t] = fmaf(lo, lo, p[t]);
+        p[t] = fmaf(hi, hi, p[t]);
       }
     }
+    warp_partials(p, red);
   }
-  ab_block_sum(acc, red, sums);
-  float inv[kAbRows];
+  __syncthreads();
+  if (tid < 8) {
+    float x = 0.0f;
+    for (int w = 0; w < kCoreThreads / 32; ++w) x += red[w][tid];
+    xp[tid] = x;
+  }
+  cluster_sync();
+  if (tid < 8) {
+    float x = 0.0f;
+    for (uint32_t r = 0; r < kCoreCta; ++r) x += ld_cluster(&xp[tid], r);
+    inv[tid] = 1.0f / sqrtf(x / (float)a.hidden + a.eps);
+  }
+  __syncthreads();
+  {
+    const uint4 wa = kin ? *reinterpret_cast<const uint4*>(a.wa + (size_t)hv * a.hidden + 8 * ch) : make_uint4(0, 0, 0, 0);
+    const uint4 wb = kin ? *reinterpret_cast<const uint4*>(a.wb + (size_t)hv * a.hidden + 8 * ch) : make_uint4(0, 0, 0, 0);
+    const uint32_t a4[4] = {wa.x, wa.y, wa.z, wa.w}, b4[4] = {wb.x, wb.y, wb.z, wb.w};
+    float p[16];
 #pragma unroll
-  for (int t = 0; t < kAbRows; ++t) inv[t] = 1.0f / sqrtf(sums[t] / (float)hidden + eps);
-  __syncthreads();  // sums is rewritten below
-#pragma unroll
-  for (int t = 0; t < kAbRows; ++t) {
-    acc[t] = 0.0f;
-#pragma unroll
-    for (int p = 0; p < kAbPer; ++p) {
-      const uint32_t x4[4] = {hv[p][t].x, hv[p][t].y, hv[p][t].z, hv[p][t].w};
-      const uint32_t w4[4] = {wv[p].x, wv[p].y, wv[p].z, wv[p].w};
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t x4[4] = {hx[t].x, hx[t].y, hx[t].z, hx[t].w};
+      p[t] = p[8 + t] = 0.0f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float r0 = bfv(to_bf(__uint_as_float(x4[e] << 16) * inv[t]));
         const float r1 = bfv(to_bf(__uint_as_float(x4[e] & 0xFFFF0000u) * inv[t]));
-        acc[t] = fmaf(r0, __uint_as_float(w4[e] << 16), acc[t]);
-        acc[t] = fmaf(r1, __uint_as_float(w4[e] & 0xFFFF0000u), acc[t]);
+        p[t] = fmaf(r0, __uint_as_float(a4[e] << 16), p[t]);
+        p[t] = fmaf(r1, __uint_as_float(a4[e] & 0xFFFF0000u), p[t]);
+        p[8 + t] = fmaf(r0, __uint_as_float(b4[e] << 16), p[8 + t]);
+        p[8 + t] = fmaf(r1, __uint_as_float(b4[e] & 0xFFFF0000u), p[8 + t]);
+      }
+    }
+    __syncthreads();  // red is reused
+    warp_partials(p, red);
+  }
+  __syncthreads();
+  if (tid < 16) {
+    float x = 0.0f;
+    for (int w = 0; w < kCoreThreads / 32; ++w) x += red[w][tid];
+    xp[8 + tid] = x;
+  }
+  cluster_sync();
+  if (tid < 16) {
+    float x = 0.0f;
+    for (uint32_t r = 0; r < kCoreCta; ++r) x += ld_cluster(&xp[8 + tid], r);
+    float g;
+    if (tid < 8) {
+      const float z = x + a.dt_bias[hv];
+      const float sp = z > 20.0f ? z : log1pf(expf(z));
+      g = expf(-expf(a.a_log[hv]) * sp);
+    } else {
+      g = 1.0f / (1.0f + expf(-x));
+    }
+    sab[tid & 7][tid >> 3] = g;
+    if (rb == 0) a.rec_ab[((size_t)(8 * l + (tid & 7)) * n_v + hv) * 2 + (tid >> 3)] = g;
+  }
+
+  // 2. convolution: threads 0..127 the q channel, 128..255 the k channel of q/k head head_qk;
+  //    threads 0..31 also the CTA's 32 v channels
+  const uint16_t* win = a.window_a + (size_t)l * 3 * C;
+  uint16_t* hist = a.conv_hist + (size_t)l * 11 * C;
+  auto conv = [&](int c, float (&y)[8], bool keep) {
+    float e[11];
+    uint16_t eb[11];
+#pragma unroll
+    for (int r = 0; r < 11; ++r) {
+      eb[r] = r < 3 ? win[(size_t)r * C + c] : a.u[(size_t)(8 * l + r - 3) * a.ld_u + c];
+      e[r] = bfv(eb[r]);
+    }
+    float tp[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tp[j] = bfv(a.taps[(size_t)c * 4 + j]);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc = fmaf(tp[j], e[t + j], acc);
+      y[t] = silu(acc);
+    }
+    if (keep)
+#pragma unroll
+      for (int r = 0; r < 11; ++r) hist[(size_t)r * C + c] = eb[r];
+  };
+  {
+    const bool isk = tid >= kGdnDk;
+    const int c = (isk ? n_qk + head_qk : head_qk) * kGdnDk + (tid & (kGdnDk - 1));
+    float y[8];
+    conv(c, y, rb == 0 && hv % (n_v / n_qk) == 0);  // one CTA keeps each q / k channel's history
+    float p[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) p[t] = y[t] * y[t];
+    warp_partials(p, red);
+    __syncthreads();
+    const bool rec_qk = rb == 0 && hv % (n_v / n_qk) == 0;  // one CTA records each q / k head
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const int w0 = isk ? 4 : 0;
+      const float n2 = red[w0][t] + red[w0 + 1][t] + red[w0 + 2][t] + red[w0 + 3][t];
+      const uint16_t b = to_bf(y[t] / sqrtf(n2 + 1e-6f));
+      (isk ? sk : sq)[t][tid & (kGdnDk - 1)] = bfv(b);
+      if (rec_qk) a.rec_qk[(((size_t)(8 * l + t) * 2 + isk) * n_qk + head_qk) * kGdnDk + (tid & (kGdnDk - 1))] = b;
+    }
+    if (tid < kCoreRows) {
+      float yv[8];
+      conv((2 * n_qk + hv) * kGdnDv + rb * kCoreRows + tid, yv, true);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint16_t b = to_bf(yv[t]);
+        sv[t][tid] = bfv(b);
+        a.rec_v[((size_t)(8 * l + t) * n_v + hv) * kGdnDv + rb * kCoreRows + tid] = b;
       }
     }
   }
-  ab_block_sum(acc, red, sums);
-  if (tid < kAbRows && t0 + tid < M) {
-    const float x = sums[tid];
-    const int t = t0 + tid;
-    if (j < n_v) {
-      const float z = x + dt_bias[j];
-      const float sp = z > 20.0f ? z : log1pf(expf(z));
-      alpha[(size_t)t * n_v + j] = expf(-expf(a_log[j]) * sp);
-    } else {
-      beta[(size_t)t * n_v + (j - n_v)] = 1.0f / (1.0f + expf(-x));
-    }
+  __syncthreads();
+
+  // 3. the delta rule over the 8 rows
+  float vi[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) vi[t] = sv[t][tid / kGdnTpr];
+  gdn_scan_rows(s, sk, sq, sab, vi, 8, c0, [&](int t, float o) {
+    if (c0 == 0) so[t][tid / kGdnTpr] = o;
+  });
+#pragma unroll
+  for (int e = 0; e < kGdnSeg; ++e) a.state_out[so_off + kGdnTpr * e] = s[e];
+  __syncthreads();
+
+  // 4. gated RMSNorm: the head's sum of o^2 per row from the four CTAs' 32 rows each
+  if (tid < 8) {
+    float x = 0.0f;
+    for (int r = 0; r < kCoreRows; ++r) x = fmaf(so[tid][r], so[tid][r], x);
+    xp[24 + tid] = x;
   }
+  cluster_sync();
+  if (tid < 8) {
+    float x = 0.0f;
+    for (uint32_t r = 0; r < kCoreCta; ++r) x += ld_cluster(&xp[24 + tid], r);
+    onorm[tid] = x / (float)kGdnDv;
+  }
+  __syncthreads();
+  {
+    const int t = tid / kCoreRows, r = tid % kCoreRows, ch = rb * kCoreRows + r;
+    const float z = bfv(a.u[(size_t)(8 * l + t) * a.ld_u + a.z0 + hv * kGdnDv + ch]);
+    a.out[(size_t)(8 * l + t) * n_v * kGdnDv + hv * kGdnDv + ch] =
+        to_bf(so[t][r] / sqrtf(onorm[t] + 1e-6f) * a.norm_w[ch] * silu(z));
+  }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
-// The Gated DeltaNet producer steps, block (row t, head) of d threads (one channel each):
-//  * the conv input of channel c: e = [window_a rows 0..2 (the lane's three earlier rows), the
-//    lane's 8 rows of u (the in-projection's q, k, v part)]; row t's output is
-//    y = silu(sum_j taps[c][j] e[t + j]) (tap 3 on the current row), in fp32 in tap order;
-//  * q and k heads: y over its L2 norm (eps 1e-6 inside the root), then bf16; v: bf16(y);
-//  * q / k head i serves v heads i * rep .. (i + 1) * rep - 1 (rep = n_v / n_qk): written there;
-//  * conv_hist[lane] = e (11 rows): the window after n accepted rows is rows n .. n + 2.
-// Heads: 0 .. n_qk - 1 q, n_qk .. 2 n_qk - 1 k, then n_v v heads.
-__global__ void gdn_prep_kernel(const uint16_t* __restrict__ u, int ld_u, const uint16_t* __restrict__ window_a,
-                                const uint16_t* __restrict__ taps, int n_qk, int n_v, int d,
-                                uint16_t* __restrict__ q, uint16_t* __restrict__ k, uint16_t* __restrict__ v,
-                                uint16_t* __restrict__ conv_hist, int32_t* __restrict__ rows8) {
-  __shared__ float red[8];
-  const int t = blockIdx.x, head = blockIdx.y, i = threadIdx.x;
-  const int lane = t >> 3, tl = t & 7, C = (2 * n_qk + n_v) * d;
-  const int c = head * d + i;
-  const uint16_t* wa = window_a + (size_t)lane * 3 * C;
-  float e[4];
+// The commit re-scan of every Gated DeltaNet layer: CTA (rb, hv, layer x lane) re-runs the delta
+// rule of gdn_step.cuh over the lane's first n = n_commit[lane] rows from the intact state_in into
+// state_out, from the inputs the pass recorded (the same values, the same arithmetic: n = 8
+// reproduces the pass's state bit for bit), and writes the next pass's window, rows n .. n + 2 of
+// the convolution history, for the channels it owns (its 32 v channels; the q / k head's channels
+// in the CTAs with rb == 0 and hv % (n_v / n_qk) == 0).
+__global__ void __launch_bounds__(kCoreThreads) gdn_commit_kernel(const __grid_constant__ GdnCommitArgs a) {
+  __shared__ float sk[8][kGdnDk], sq[8][kGdnDk], sab[8][2];
+  const int rb = blockIdx.x, hv = blockIdx.y, li = blockIdx.z / a.lanes, l = blockIdx.z % a.lanes, tid = threadIdx.x;
+  const int n_qk = a.n_qk, n_v = a.n_v, C = (2 * n_qk + n_v) * kGdnDk, head_qk = hv / (n_v / n_qk);
+  const GdnCommitLayer& L = a.layer[li];
+  int n = a.n_commit[l];
+  n = n < 0 ? 0 : (n > 8 ? 8 : n);
+  const int i = rb * kCoreRows + tid / kGdnTpr, c0 = tid % kGdnTpr;
+  const size_t so_off = (((size_t)l * n_v + hv) * kGdnDv + i) * kGdnDk + c0;
+  const uint16_t* rqk = L.rec_qk;
+  for (int t = 0; t < n; ++t) {
+    const int isk = tid >> 7, c = tid & (kGdnDk - 1);
+    (isk ? sk : sq)[t][c] = bfv(rqk[(((size_t)(8 * l + t) * 2 + isk) * n_qk + head_qk) * kGdnDk + c]);
+    if (tid < 2) sab[t][tid] = L.rec_ab[((size_t)(8 * l + t) * n_v + hv) * 2 + tid];
+  }
+  float vi[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int r = tl + j;  // row of e
-    e[j] = r < 3 ? bfv(wa[(size_t)r * C + c]) : bfv(u[(size_t)(8 * lane + r - 3) * ld_u + c]);
-  }
-  float acc = 0.0f;
+  for (int t = 0; t < 8; ++t) vi[t] = t < n ? bfv(L.rec_v[((size_t)(8 * l + t) * n_v + hv) * kGdnDv + i]) : 0.0f;
+  float s[kGdnSeg];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) acc = fmaf(bfv(taps[(size_t)c * 4 + j]), e[j], acc);
-  const float y = silu(acc);
-  if (tl == 0) {  // the lane's conv history: its window, then its 8 rows
-    uint16_t* hist = conv_hist + (size_t)lane * 11 * C;
-    for (int r = 0; r < 3; ++r) hist[(size_t)r * C + c] = wa[(size_t)r * C + c];
-    for (int r = 0; r < 8; ++r) hist[(size_t)(3 + r) * C + c] = u[(size_t)(8 * lane + r) * ld_u + c];
-    if (head == 0 && i == 0) rows8[lane] = 8;
-  }
-  const int rep = n_v / n_qk;
-  if (head < 2 * n_qk) {
-    const float n2 = block_sum(y * y, red);
-    const uint16_t o = to_bf(y / sqrtf(n2 + 1e-6f));
-    uint16_t* dst = head < n_qk ? q : k;
-    const int qh = head < n_qk ? head : head - n_qk;
-    for (int r = 0; r < rep; ++r) dst[((size_t)t * n_v + qh * rep + r) * d + i] = o;
-  } else {
-    v[((size_t)t * n_v + (head - 2 * n_qk)) * d + i] = to_bf(y);
-  }
-}
-
-// Gated RMSNorm, block (row t, v head) of d threads: bf16(o / sqrt(mean(o^2) + eps) * w * silu(z)),
-// o the scan's output (fp32 [M][n_v][d]), z = u[t][z0 + head * d + i] (bf16 in-projection output).
-__global__ void gated_norm_kernel(const float* __restrict__ o, const uint16_t* __restrict__ u, int ld_u, int z0,
-                                  const float* __restrict__ w, int n_v, int d, uint16_t* __restrict__ out) {
-  __shared__ float red[8];
-  const int t = blockIdx.x, hh = blockIdx.y, i = threadIdx.x;
-  const float x = o[((size_t)t * n_v + hh) * d + i];
-  const float ms = block_sum(x * x, red) / (float)d;
-  const float z = bfv(u[(size_t)t * ld_u + z0 + hh * d + i]);
-  out[(size_t)t * n_v * d + hh * d + i] = to_bf(x / sqrtf(ms + 1e-6f) * w[i] * silu(z));
+  for (int e = 0; e < kGdnSeg; ++e) s[e] = L.state_in[so_off + kGdnTpr * e];
+  __syncthreads();
+  gdn_scan_rows(s, sk, sq, sab, vi, n, c0, [](int, float) {});
+#pragma unroll
+  for (int e = 0; e < kGdnSeg; ++e) L.state_out[so_off + kGdnTpr * e] = s[e];
+  // the window after n rows
+  const uint16_t* hist = L.conv_hist + (size_t)l * 11 * C;
+  uint16_t* win = L.window + (size_t)l * 3 * C;
+  auto copy = [&](int c) {
+#pragma unroll
+    for (int r = 0; r < 3; ++r) win[(size_t)r * C + c] = hist[(size_t)(n + r) * C + c];
+  };
+  if (tid < kCoreRows) copy((2 * n_qk + hv) * kGdnDv + rb * kCoreRows + tid);
+  if (rb == 0 && hv % (n_v / n_qk) == 0) copy(((tid >> 7) ? n_qk + head_qk : head_qk) * kGdnDk + (tid & (kGdnDk - 1)));
 }
 
 // Attention producer steps, block (row t, group of kPrepHeads heads) of D threads: heads 0 .. Hq - 1
@@ -265,25 +379,13 @@ __global__ void attn_prep_kernel(const uint16_t* __restrict__ uq, int ld_q, cons
 
 }  // namespace
 
-cudaError_t launch_ab_gates(const uint16_t* h, int hidden, int M, float eps, const uint16_t* wa, const uint16_t* wb,
-                            int n_v, const float* a_log, const float* dt_bias, float* alpha, float* beta,
-                            cudaStream_t s) {
-  ab_gates_kernel<<<dim3(2 * n_v, (M + kAbRows - 1) / kAbRows), kAbThreads, 0, s>>>(h, hidden, M, eps, wa, wb, n_v,
-                                                                                    a_log, dt_bias, alpha, beta);
+cudaError_t launch_gdn_commit(const GdnCommitArgs& a, int n_layers, cudaStream_t s) {
+  gdn_commit_kernel<<<dim3(kCoreCta, (unsigned)a.n_v, (unsigned)(n_layers * a.lanes)), kCoreThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
-cudaError_t launch_gdn_prep(const uint16_t* u, int ld_u, int M, const uint16_t* window_a, const uint16_t* taps,
-                            int n_qk, int n_v, int d, uint16_t* q, uint16_t* k, uint16_t* v, uint16_t* conv_hist,
-                            int32_t* rows8, cudaStream_t s) {
-  gdn_prep_kernel<<<dim3(M, 2 * n_qk + n_v), d, 0, s>>>(u, ld_u, window_a, taps, n_qk, n_v, d, q, k, v, conv_hist,
-                                                        rows8);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_gated_norm(const float* o, const uint16_t* u, int ld_u, int z0, const float* w, int M, int n_v,
-                              int d, uint16_t* out, cudaStream_t s) {
-  gated_norm_kernel<<<dim3(M, n_v), d, 0, s>>>(o, u, ld_u, z0, w, n_v, d, out);
+cudaError_t launch_gdn_core(const GdnCoreArgs& a, int lanes, cudaStream_t s) {
+  gdn_core_kernel<<<dim3(kCoreCta, (unsigned)a.n_v, (unsigned)lanes), kCoreThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -7,20 +7,48 @@
 
 namespace vp {
 
-// The gates alpha[t][j] = exp(-exp(a_log[j]) softplus(a + dt_bias[j])), beta[t][j] = sigmoid(b) of
-// a = bf16(RMSNorm(h_t)) . wa[j], b = ... . wb[j] (fp32 [M][n_v]); h bf16 [M][hidden], hidden % 8 == 0,
-// hidden <= 8192, h / wa / wb 16-byte aligned.
-cudaError_t launch_ab_gates(const uint16_t* h, int hidden, int M, float eps, const uint16_t* wa, const uint16_t* wb,
-                            int n_v, const float* a_log, const float* dt_bias, float* alpha, float* beta,
-                            cudaStream_t s);
-// Short convolution + SiLU + Q / K L2 norm (q, k expanded to the n_v heads, v) bf16 [M][n_v][d], the
-// conv history [lanes][11][C] and rows8[lane] = 8.
-cudaError_t launch_gdn_prep(const uint16_t* u, int ld_u, int M, const uint16_t* window_a, const uint16_t* taps,
-                            int n_qk, int n_v, int d, uint16_t* q, uint16_t* k, uint16_t* v, uint16_t* conv_hist,
-                            int32_t* rows8, cudaStream_t s);
-// out[t][h d + i] = bf16(gated RMSNorm of the scan output o with silu(z)), z = u[t][z0 + h d + i].
-cudaError_t launch_gated_norm(const float* o, const uint16_t* u, int ld_u, int z0, const float* w, int M, int n_v,
-                              int d, uint16_t* out, cudaStream_t s);
+// The Gated DeltaNet core of one layer for all lanes (8 rows each), one launch (mixer.cu).
+struct GdnCoreArgs {
+  const uint16_t* h;         // bf16 [M][hidden]: the residual (the A / B projections' input)
+  int hidden;                // % 128 == 0, <= 8192
+  float eps;                 // RMSNorm eps of the A / B projections' input
+  const uint16_t* u;         // bf16 [M][ld_u]: the in-projection (q, k, v, z)
+  int ld_u, z0;              // row stride; first column of z
+  const uint16_t* window_a;  // bf16 [lanes][3][C], C = (2 n_qk + n_v) 128
+  const uint16_t* taps;      // bf16 [C][4]
+  const uint16_t* wa;        // bf16 [n_v][hidden], 16-byte aligned
+  const uint16_t* wb;        // bf16 [n_v][hidden], 16-byte aligned
+  const float* a_log;        // fp32 [n_v]
+  const float* dt_bias;      // fp32 [n_v]
+  const float* norm_w;       // fp32 [128]
+  const float* state_in;     // fp32 [lanes][n_v][128][128]
+  float* state_out;          // fp32 [lanes][n_v][128][128]
+  uint16_t* conv_hist;       // bf16 [lanes][11][C]
+  uint16_t* out;             // bf16 [M][n_v 128]: the out-projection's input
+  uint16_t* rec_qk;          // bf16 [M][2][n_qk][128]: the scan's q then k per q/k head (recorded)
+  uint16_t* rec_v;           // bf16 [M][n_v][128]: the scan's v (recorded)
+  float* rec_ab;             // fp32 [M][n_v][2]: alpha, beta (recorded)
+  int n_qk, n_v;
+};
+cudaError_t launch_gdn_core(const GdnCoreArgs& a, int lanes, cudaStream_t s);
+
+// The commit re-scan of up to kCommitLayers Gated DeltaNet layers in one launch (mixer.cu).
+constexpr int kCommitLayers = 48;
+struct GdnCommitLayer {
+  const float* state_in;     // the intact parity buffer
+  float* state_out;          // the other one: the state after the committed rows
+  const uint16_t* conv_hist; // bf16 [lanes][11][C] of the pass
+  uint16_t* window;          // bf16 [lanes][3][C]: rows n .. n + 2 of the history
+  const uint16_t* rec_qk;    // the pass's record (GdnCoreArgs)
+  const uint16_t* rec_v;
+  const float* rec_ab;
+};
+struct GdnCommitArgs {
+  GdnCommitLayer layer[kCommitLayers];
+  const int32_t* n_commit;   // int32 [lanes], rows kept per lane (clamped to 0 .. 8)
+  int lanes, n_qk, n_v;
+};
+cudaError_t launch_gdn_commit(const GdnCommitArgs& a, int n_layers, cudaStream_t s);
 // The rotary embedding's inverse frequencies 10000^(-2j / D), j < D / 2 (formed on the host in fp64).
 struct RopeTable {
   double inv_freq[256];

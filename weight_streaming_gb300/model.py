@@ -143,10 +143,14 @@ class SyntheticModel:
     def cores_workspace(self, M: int) -> torch.Tensor:
         return torch.zeros(V.vp_pass_cores_workspace_bytes(self.model, M), dtype=torch.uint8, device="cuda")
 
-    def run_cores(self, x0, ctx, pending, argmax, n_commit, committed, ws, trace=None, logits=None, stream=None):
+    def run_cores(self, x0, ctx, pending, argmax, n_commit, committed, ws, parity=0, trace=None, logits=None,
+                  stream=None):
         M = x0.shape[0]
-        V.vp_verify_pass_cores(self.model, x0, M, ctx, pending, argmax, n_commit, committed, trace, logits, ws,
-                               stream)
+        V.vp_verify_pass_cores(self.model, x0, M, ctx, parity, pending, argmax, n_commit, committed, trace, logits,
+                               ws, stream)
+
+    def commit_cores(self, M, n_commit, parity, ws, stream=None):
+        V.vp_commit_cores(self.model, M, n_commit, parity, ws, stream)
 
     def workspace(self, M: int) -> torch.Tensor:
         n = V.vp_pass_workspace_bytes(self.model, M)
