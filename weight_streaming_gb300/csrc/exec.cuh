@@ -76,11 +76,17 @@ __device__ __forceinline__ void accept_lane(int l, const int* tok, const int32_t
 struct Slice {
   int kg0, kgn, cta0, ctan;
 };
+// (a * b + d) / c for non-negative ints with a quotient that fits an int: 32-bit unsigned division
+// when the dividend fits (the usual case), else 64-bit.
+__device__ __forceinline__ int muldiv(int a, int b, int d, int c) {
+  const long long n = (long long)a * b + d;
+  return n < (1LL << 32) ? (int)((unsigned)n / (unsigned)c) : (int)(n / c);
+}
 __device__ __forceinline__ Slice slice_geom(const Phase& ph, int G, int s) {
   Slice S;
-  const int kg0 = (int)((long long)s * ph.KG / ph.ks), kg1 = (int)((long long)(s + 1) * ph.KG / ph.ks);
-  const int c0 = (int)(((long long)G * kg0 + ph.KG / 2) / ph.KG);
-  const int c1 = s + 1 == ph.ks ? G : (int)(((long long)G * kg1 + ph.KG / 2) / ph.KG);
+  const int kg0 = muldiv(s, ph.KG, 0, ph.ks), kg1 = muldiv(s + 1, ph.KG, 0, ph.ks);
+  const int c0 = muldiv(G, kg0, ph.KG / 2, ph.KG);
+  const int c1 = s + 1 == ph.ks ? G : muldiv(G, kg1, ph.KG / 2, ph.KG);
   S.kg0 = kg0;
   S.kgn = kg1 - kg0;
   S.cta0 = c0;
@@ -104,17 +110,47 @@ __device__ __forceinline__ Part part_of_cta(const Phase& ph, int G, int cta) {
     }
   }
   const int c = cta - P.S.cta0;
-  P.rb0 = (int)((long long)c * ph.RB / P.S.ctan);
-  P.nrb = (int)((long long)(c + 1) * ph.RB / P.S.ctan) - P.rb0;
+  P.rb0 = muldiv(c, ph.RB, 0, P.S.ctan);
+  P.nrb = muldiv(c + 1, ph.RB, 0, P.S.ctan) - P.rb0;
   P.U = P.nrb * P.S.kgn;
   P.W = min(kWarps, P.U);
   return P;
 }
 // Warp w of a CTA owns its units [wbegin(w), wbegin(w + 1)); wowner(u) inverts it.
-__device__ __forceinline__ int wbegin(const Part& P, int w) {
-  return w >= P.W ? P.U : (int)((long long)w * P.U / P.W);
+__device__ __forceinline__ int wbegin(const Part& P, int w) { return w >= P.W ? P.U : muldiv(w, P.U, 0, P.W); }
+__device__ __forceinline__ int wowner(const Part& P, int u) { return muldiv(u + 1, P.W, -1, P.U); }
+
+// A phase's descriptor, the CTA's share of it and the warps' unit ranges, kept in shared memory.
+// Slot p % 3 holds phase p.  Phases 0 and 1 are filled at the start; phase p + 2 by the first warp
+// of the CTA to finish its units of phase p, so that neither the phase loop nor the weight
+// producers (which cross into the next phase while the current one streams) read the kernel
+// parameters or divide on their critical paths.  The slot's phase index is written last with a
+// CTA-scope release and read with an acquire.
+constexpr int kPhaseSlots = 3;
+struct PhaseSlot {
+  Phase ph;
+  Part part;
+  int idx;                // the phase held (-1: none)
+  int wb[kWarps + 1];     // warp w's units: [wb[w], wb[w + 1])
+  const void* x;          // the phase's activation source
+};
+static __device__ __noinline__ void fill_slot(PhaseSlot& sl, const Program& prog, const Io& io, int p, int G, int cta,
+                                          int lane) {
+  static_assert(sizeof(Phase) % 4 == 0 && sizeof(Phase) <= 32 * 4, "a phase descriptor is at most 32 words");
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(&prog.ph[p]);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(&sl.ph);
+  if (lane < (int)(sizeof(Phase) / 4)) dst[lane] = src[lane];
+  __syncwarp();
+  const Part P = part_of_cta(sl.ph, G, cta);
+  if (lane <= kWarps) sl.wb[lane] = wbegin(P, lane);
+  if (lane == 0) {
+    sl.part = P;
+    sl.x = io.buf[sl.ph.x_src];
+  }
+  __syncwarp();
+  if (lane == 0) st_release_cta_smem(&sl.idx, p);
 }
-__device__ __forceinline__ int wowner(const Part& P, int u) { return (int)(((long long)(u + 1) * P.W - 1) / P.U); }
+__device__ __forceinline__ bool slot_holds(const PhaseSlot& sl, int p) { return ld_acquire_cta_smem(&sl.idx) == p; }
 
 // ---------------------------------------------------------------- weight producer (lane 0 of a warp)
 // Walks the warp's units across all phases of the program, in consumption order, keeping the
@@ -133,8 +169,7 @@ struct Cursor {
   uint32_t bytes;    // per source
 };
 // Source addresses of the cursor's unit (read from the phase descriptor).
-__device__ __forceinline__ void cursor_locate(Cursor& c, const Program& prog) {
-  const Phase& ph = prog.ph[c.p];
+__device__ __forceinline__ void cursor_locate_in(Cursor& c, const Phase& ph) {
   c.KC = ph.KC;
   c.grp = ph.grp;
   c.chunk = 2u * strip_bytes(ph.fmt);
@@ -151,32 +186,47 @@ __device__ __forceinline__ void cursor_locate(Cursor& c, const Program& prog) {
     c.bytes = c.chunk;
   }
 }
-__device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, int G, int cta, int warp) {
+// Out of line: called when the row block or the phase changes, which keeps the unit loop's
+// registers for the unit.
+__device__ __forceinline__ void cursor_locate(Cursor& c, const Program& prog, const PhaseSlot*) {
+  cursor_locate_in(c, prog.ph[c.p]);
+}
+__device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, const PhaseSlot* slots, int G, int cta,
+                                            int warp) {
   while (c.p < prog.n) {
-    const Phase& ph = prog.ph[c.p];
-    const Part P = part_of_cta(ph, G, cta);
-    const int u = wbegin(P, warp);
-    c.left = wbegin(P, warp + 1) - u;
+    const PhaseSlot& sl = slots[c.p % kPhaseSlots];
+    Part P;
+    int u;
+    if (slot_holds(sl, c.p)) {
+      P = sl.part;
+      u = sl.wb[warp];
+      c.left = sl.wb[warp + 1] - u;
+    } else {
+      P = part_of_cta(prog.ph[c.p], G, cta);
+      u = wbegin(P, warp);
+      c.left = wbegin(P, warp + 1) - u;
+    }
     if (c.left > 0) {
       c.kg0 = P.S.kg0;
       c.kgn = P.S.kgn;
       c.rb = P.rb0 + u / P.S.kgn;
       c.kgl = u - (c.rb - P.rb0) * P.S.kgn;
-      cursor_locate(c, prog);
+      cursor_locate(c, prog, slots);
       return;
     }
     ++c.p;
   }
 }
 // Next unit: within a row block the next group follows contiguously (grp chunks further on).
-__device__ __forceinline__ void cursor_next(Cursor& c, const Program& prog, int G, int cta, int warp) {
+__device__ __forceinline__ void cursor_next(Cursor& c, const Program& prog, const PhaseSlot* slots, int G, int cta,
+                                            int warp) {
   if (--c.left == 0) {
     ++c.p;
-    cursor_seek(c, prog, G, cta, warp);
+    cursor_seek(c, prog, slots, G, cta, warp);
   } else if (++c.kgl == c.kgn) {
     c.kgl = 0;
     ++c.rb;
-    cursor_locate(c, prog);
+    cursor_locate(c, prog, slots);
   } else {
     const uint32_t step = (uint32_t)c.grp * c.chunk;
     c.kc += c.grp;
@@ -192,7 +242,8 @@ struct SmemMisc {
   uint64_t full[kWarps][kSlots];
   Cursor cur[kWarps];  // the producer state of each warp (used by its lane 0 only)
   unsigned tcnt[kWarps];  // arrivals at a row block shared by warps, indexed by its first contributor
-  Part part;              // the CTA's share of the current phase
+  PhaseSlot ps[kPhaseSlots];  // phase p in slot p % 3
+  int fillp;                  // the phase whose slot is filled next, minus 2
   float red[kThreads / 16];
   float xscale[kMaxM];
   int tok[kMaxM];
@@ -239,7 +290,7 @@ __device__ __forceinline__ int exp_of_max(float mx) {
   return ex - 1 - 14;
 }
 
-// Stages the CTA's K slice [kbase, kbase + Ks) of the phase's activation rows: x, or
+// Stages the CTA's K slice [kbase, kbase + Ks) of phase `trace_phase`'s activation rows: x, or
 // bf16(RMSNorm(x)) (unit weight) when the phase asks for it, with the row statistics taken over
 // the whole row.
 //
@@ -258,7 +309,7 @@ __device__ __forceinline__ void stage_x(const Program& prog, const Phase& ph, co
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, M = prog.M;
   const int g = 2 * (lane >> 3) + (lane & 1), h = (lane >> 1) & 1, pp = (lane >> 2) & 1;
   const int blocks = Ks >> 6, items = NT * blocks;
-  const uint16_t* xsrc = static_cast<const uint16_t*>(io.buf[ph.x_src]);
+  const uint16_t* xsrc = static_cast<const uint16_t*>(sm.ps[trace_phase % kPhaseSlots].x);
   const bool rms = ph.x_rms != 0;
   uint4 va[kIt], vb[kIt];
   float stat[NT];
@@ -673,10 +724,10 @@ __device__ __forceinline__ void store_partial(float* slot, int lane, bool two, c
 //  * One K slice (ks == 1): the finished row block runs its epilogue here.  Several K slices: its
 //    sum over this slice goes to the cross-slice slot, summed after the next grid barrier.
 template <int NT>
-__device__ void flush(const Phase& ph, const Io& io, int M, int G, int w, int rb, const float (&acc)[NT][4],
+__device__ void flush(const Phase& ph, const Part& P, const Io& io, int M, int G, int w, int rb, const float (&acc)[NT][4],
                       const float (&acc2)[NT][4], const float (&tsc)[NT][2], HeadBest<NT>& hb, SmemMisc& sm,
                       int lane) {
-  const Part& P = sm.part;  // read from shared memory: nothing of it stays live in the unit loop
+  // P is the shared-memory copy: nothing of it stays live in the unit loop
   const bool two = ph.layout == kInterleaved;
   float v[NT][4], u[NT][4];
 #pragma unroll
@@ -900,7 +951,18 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     for (int s = 0; s < kSlots; ++s) mbar_init(&sm.full[warp][s], 1);
     sm.tcnt[warp] = 0u;
   }
-  if (threadIdx.x == 0) sm.abort = 0;
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    sm.fillp = 0;
+    sm.ps[2].idx = -1;
+  }
+  if (warp == 1) fill_slot(sm.ps[0], prog, io, 0, G, cta, lane);
+  if (warp == 2) {
+    if (prog.n > 1)
+      fill_slot(sm.ps[1], prog, io, 1, G, cta, lane);
+    else if (lane == 0)
+      sm.ps[1].idx = -1;
+  }
   fence_mbar_init();
   __syncthreads();
 
@@ -911,19 +973,19 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
   if (lane == 0) {
     pol = l2_evict_first_policy();
     pc.p = 0;
-    cursor_seek(pc, prog, G, cta, warp);
+    cursor_seek(pc, prog, sm.ps, G, cta, warp);
     for (; issued < (unsigned)kSlots && pc.p < prog.n; ++issued) {
       issue_unit(pc, ring_w + issued * kSlotBytes, &sm.full[warp][issued], pol);
-      cursor_next(pc, prog, G, cta, warp);
+      cursor_next(pc, prog, sm.ps, G, cta, warp);
     }
   }
 
   unsigned seq = 0, nbar = 0;
   for (int p = 0; p < prog.n; ++p) {
+    const PhaseSlot& sl = sm.ps[p % kPhaseSlots];
     const Phase& ph = prog.ph[p];
     VP_TRACE(threadIdx.x == 0, p, 0);
-    const Part P = part_of_cta(ph, G, cta);
-    if (threadIdx.x == 0) sm.part = P;  // published by the staging's closing barrier
+    const Part P = sl.part;
     const int ck = chunk_k(ph.fmt), kc0 = P.S.kg0 * ph.grp;
     stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm, p);
     VP_TRACE(threadIdx.x == 0, p, 1);
@@ -941,7 +1003,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
         hb.v[j][h] = -INFINITY;
         hb.i[j][h] = 0x7fffffff;
       }
-    const int ub = wbegin(P, warp), ue = wbegin(P, warp + 1);
+    const int ub = sl.wb[warp], ue = sl.wb[warp + 1];
     const uint32_t xlane = smem_addr(xs) + lane * 16;
     const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
     const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
@@ -956,7 +1018,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     for (int u = ub; u < ue; ++u) {
       if (rb != cur) {
         if (cur >= 0) {
-          flush<NT>(ph, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+          flush<NT>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
 #pragma unroll
           for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -990,7 +1052,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       if (lane == 0 && pc.p < prog.n && !sm.abort) {
         fence_proxy_async_smem();
         issue_unit(pc, ua, &sm.full[warp][slot], pol);
-        cursor_next(pc, prog, G, cta, warp);
+        cursor_next(pc, prog, sm.ps, G, cta, warp);
         ++issued;
       }
       ++seq;
@@ -1000,7 +1062,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       }
     }
     VP_TRACE(lane == 0, p, 2 + warp);
-    if (cur >= 0) flush<NT>(ph, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+    if (cur >= 0) flush<NT>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+    if (p + 2 < prog.n) {  // the first warp of the CTA done with this phase fills phase p + 2's slot
+      int won = 0;
+      if (lane == 0) won = atomicCAS(&sm.fillp, p, p + 1) == p;
+      if (__shfl_sync(0xffffffffu, won, 0)) fill_slot(sm.ps[(p + 2) % kPhaseSlots], prog, io, p + 2, G, cta, lane);
+    }
     VP_TRACE(lane == 0, p, 18 + warp);
     if (ph.ks > 1) {  // every row block's slices meet after a grid barrier
       grid_barrier(io, G, (unsigned)G * ++nbar, sm);

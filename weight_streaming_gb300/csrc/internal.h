@@ -58,7 +58,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kSlots = 2;
 constexpr int kSlotBytes = 4608;
 constexpr int kRingBytes = kWarps * kSlots * kSlotBytes;  // 147,456
-constexpr int kMiscBytes = 2048;
+constexpr int kMiscBytes = 2560;
 constexpr int kSmemBytes = 232448;  // 227 KB: the per-CTA maximum
 constexpr int kXBytes = kSmemBytes - kRingBytes - kMiscBytes;
 constexpr int kMaxGrid = 256;
