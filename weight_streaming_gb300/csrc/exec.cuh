@@ -250,7 +250,7 @@ struct SmemMisc {
   int abort;
   int flag;
 };
-static_assert(sizeof(SmemMisc) <= (size_t)kMiscBytes, "SmemMisc exceeds its shared-memory budget");
+static_assert(sizeof(SmemMisc) + 16 <= (size_t)kMiscBytes, "SmemMisc exceeds its shared-memory budget (the last word is the trace parity)");
 
 // Bulk copy of the cursor's unit into the slot at shared address dst, completing on bar.
 __device__ __forceinline__ void issue_unit(const Cursor& c, uint32_t dst, uint64_t* bar, uint64_t pol) {
@@ -956,6 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     sm.fillp = 0;
     sm.ps[2].idx = -1;
   }
+  VP_TRACE_INIT();
   if (warp == 1) fill_slot(sm.ps[0], prog, io, 0, G, cta, lane);
   if (warp == 2) {
     if (prog.n > 1)
