@@ -609,7 +609,7 @@ __device__ __forceinline__ void load_resid(const Phase& ph, const Io& io, int M,
 
 // Token tile j of the finished row block rb: v (fp32, un-scaled activations, before the weight
 // scale); interleaved layout: v = the gate rows, u = the up rows (else u is unused).
-template <int NT>
+template <int NT, bool kHead>
 __device__ __forceinline__ void epilogue_tile(const Phase& ph, const Io& io, int M, int rb, int j, const float (&v)[4],
                                               const float (&u)[4], const uint16_t (&hold)[4], HeadBest<NT>& hb,
                                               int lane) {
@@ -665,11 +665,13 @@ __device__ __forceinline__ void epilogue_tile(const Phase& ph, const Io& io, int
           break;
         }
         case kEpiHead: {
-          if (io.buf[kBufLogits]) static_cast<float*>(io.buf[kBufLogits])[o] = val;
-          const float key = isnan(val) ? -INFINITY : val;
-          if (am_better(key, n, hb.v[j][h], hb.i[j][h])) {
-            hb.v[j][h] = key;
-            hb.i[j][h] = n;
+          if constexpr (kHead) {  // only the head phase's instantiation carries the argmax state
+            if (io.buf[kBufLogits]) static_cast<float*>(io.buf[kBufLogits])[o] = val;
+            const float key = isnan(val) ? -INFINITY : val;
+            if (am_better(key, n, hb.v[j][h], hb.i[j][h])) {
+              hb.v[j][h] = key;
+              hb.i[j][h] = n;
+            }
           }
           break;
         }
@@ -694,11 +696,11 @@ __device__ __forceinline__ void epilogue_tile(const Phase& ph, const Io& io, int
 }
 
 // The finished row block rb, every token tile.
-template <int NT>
+template <int NT, bool kHead>
 __device__ void epilogue(const Phase& ph, const Io& io, int M, int rb, const float (&v)[NT][4],
                          const float (&u)[NT][4], const uint16_t (&hold)[NT][4], HeadBest<NT>& hb, int lane) {
 #pragma unroll
-  for (int j = 0; j < NT; ++j) epilogue_tile<NT>(ph, io, M, rb, j, v[j], u[j], hold[j], hb, lane);
+  for (int j = 0; j < NT; ++j) epilogue_tile<NT, kHead>(ph, io, M, rb, j, v[j], u[j], hold[j], hb, lane);
 }
 
 // A partial of a row block (one slot: 32 lanes x cs_lane floats) is laid out token tile major:
@@ -723,18 +725,28 @@ __device__ __forceinline__ void store_partial(float* slot, int lane, bool two, c
 //    sums the slots in warp order, so the result does not depend on who arrives last.
 //  * One K slice (ks == 1): the finished row block runs its epilogue here.  Several K slices: its
 //    sum over this slice goes to the cross-slice slot, summed after the next grid barrier.
+// Register budget: at 3-4 token tiles the per-token scales are read from shared memory here (tsc is
+// unused), so that they do not stay live through the unit loop; at 1-2 tiles the caller's copy is
+// cheaper.
 template <int NT>
+constexpr bool kScalesFromSmem = NT >= 3;
+template <int NT, bool kHead>
 __device__ void flush(const Phase& ph, const Part& P, const Io& io, int M, int G, int w, int rb, const float (&acc)[NT][4],
                       const float (&acc2)[NT][4], const float (&tsc)[NT][2], HeadBest<NT>& hb, SmemMisc& sm,
                       int lane) {
   // P is the shared-memory copy: nothing of it stays live in the unit loop
   const bool two = ph.layout == kInterleaved;
+  const int c = lane & 3;
   float v[NT][4], u[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const float sc = tsc[j][r & 1];
+      float sc;
+      if constexpr (kScalesFromSmem<NT>)
+        sc = sm.xscale[8 * j + 2 * c + (r & 1)];
+      else
+        sc = tsc[j][r & 1];
       v[j][r] = (two ? acc[j][r] : acc[j][r] + acc2[j][r]) * sc;
       u[j][r] = two ? acc2[j][r] * sc : 0.0f;
     }
@@ -785,13 +797,13 @@ __device__ void flush(const Phase& ph, const Part& P, const Io& io, int M, int G
     store_partial<NT>(io.xslots + ((size_t)rb * ph.ks + P.sidx) * slot_floats, lane, two, v, u);
     return;
   }
-  epilogue<NT>(ph, io, M, rb, v, u, hold, hb, lane);
+  epilogue<NT, kHead>(ph, io, M, rb, v, u, hold, hb, lane);
 }
 
 // Phases with several K slices, after the grid barrier that follows the units: token tile j of
 // row block rb is summed over its slices in slice order by one warp (items (rb, j) spread over the
 // CTAs first), its slice partials loaded 8 slices at a time, then its epilogue runs.
-template <int NT>
+template <int NT, bool kHead>
 __device__ void cross_slice_fixup(const Phase& ph, const Io& io, int M, int G, HeadBest<NT>& hb, int warp,
                                   int lane) {
   const bool two = ph.layout == kInterleaved;
@@ -824,7 +836,7 @@ __device__ void cross_slice_fixup(const Phase& ph, const Io& io, int M, int G, H
         u[3] += q2[i].w;
       }
     }
-    epilogue_tile<NT>(ph, io, M, rb, j, v, u, hold, hb, lane);
+    epilogue_tile<NT, kHead>(ph, io, M, rb, j, v, u, hold, hb, lane);
   }
 }
 
@@ -937,6 +949,109 @@ __device__ __forceinline__ void grid_exit(const Io& io, int G) {
   }
 }
 
+// The streaming part of phase p (after its staging): the warp's units, its row blocks' fixups, the
+// cross-slice sums and the head's argmax and acceptance.  Instantiated twice: only the head phase's
+// copy (kHead) keeps the running argmax in registers through the unit loop.
+template <int NT, bool kQ4, bool kHead>
+__device__ __forceinline__ void phase_units(const Program& prog, const Io& io, const Phase& ph, const PhaseSlot& sl,
+                                            int p, uint8_t* xs, SmemMisc& sm, uint32_t ring_w, uint64_t pol,
+                                            unsigned& issued, unsigned& seq, unsigned& nbar) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, cta = blockIdx.x;
+  Cursor& pc = sm.cur[warp];
+  const Part P = sl.part;
+  const int ck = chunk_k(ph.fmt);
+  float tsc[NT][2];  // per-token scales (unused at 3-4 tiles: see flush)
+  if constexpr (!kScalesFromSmem<NT>) {
+    const int c = lane & 3;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      tsc[j][0] = sm.xscale[8 * j + 2 * c];
+      tsc[j][1] = sm.xscale[8 * j + 2 * c + 1];
+    }
+  }
+  HeadBest<NT> hb;
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      hb.v[j][h] = -INFINITY;
+      hb.i[j][h] = 0x7fffffff;
+    }
+  const int ub = sl.wb[warp], ue = sl.wb[warp + 1];
+  const uint32_t xlane = smem_addr(xs) + lane * 16;
+  const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
+  const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
+  const bool two = ph.layout == kInterleaved;
+  int rb = ub < ue ? P.rb0 + ub / P.S.kgn : 0, kgl = ub < ue ? ub % P.S.kgn : 0;
+  float acc[NT][4], acc2[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
+  int cur = -1;
+  for (int u = ub; u < ue; ++u) {
+    if (rb != cur) {
+      if (cur >= 0) {
+        flush<NT, kHead>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
+      }
+      cur = rb;
+    }
+    const int slot = (int)(seq % kSlots);
+    if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
+      sm.abort = 1;
+      atomicExch(io.status, kStatusTimeout);
+    }
+    const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kgl * ph.grp * pair_stride;
+    if constexpr (kQ4) {  // one or two consecutive chunks of the row block, 4 groups each
+      unit_q4<NT>(ua, xa, lane, acc);
+      if ((P.S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
+    } else if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
+      unit_nvfp4<NT>(ua, xa, lane, acc, acc);
+      unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
+    } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
+      const bool second = ph.grp == 2 && (P.S.kg0 + kgl) * 2 + 1 < ph.KC;
+      if (ph.fmt == kFmtNvfp4) {
+        unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+        if (second) unit_nvfp4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
+      } else {
+        unit_fp8<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+        if (second) unit_fp8<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
+      }
+    }
+    __syncwarp();
+    if (lane == 0 && pc.p < prog.n && !sm.abort) {
+      fence_proxy_async_smem();
+      issue_unit(pc, ua, &sm.full[warp][slot], pol);
+      cursor_next(pc, prog, sm.ps, G, cta, warp);
+      ++issued;
+    }
+    ++seq;
+    if (++kgl == P.S.kgn) {
+      kgl = 0;
+      ++rb;
+    }
+  }
+  VP_TRACE(lane == 0, p, 2 + warp);
+  if (cur >= 0) flush<NT, kHead>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+  if (p + 2 < prog.n) {  // the first warp of the CTA done with this phase fills phase p + 2's slot
+    int won = 0;
+    if (lane == 0) won = atomicCAS(&sm.fillp, p, p + 1) == p;
+    if (__shfl_sync(0xffffffffu, won, 0)) fill_slot(sm.ps[(p + 2) % kPhaseSlots], prog, io, p + 2, G, cta, lane);
+  }
+  VP_TRACE(lane == 0, p, 18 + warp);
+  if (ph.ks > 1) {  // every row block's slices meet after a grid barrier
+    grid_barrier(io, G, (unsigned)G * ++nbar, sm);
+    cross_slice_fixup<NT, kHead>(ph, io, prog.M, G, hb, warp, lane);
+    VP_TRACE(threadIdx.x == 0, p, 35);
+  }
+  if (kHead && ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
+}
+
 // ---------------------------------------------------------------- the kernel
 template <int NT, bool kQ4>
 __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant__ Program prog,
@@ -990,92 +1105,12 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     const int ck = chunk_k(ph.fmt), kc0 = P.S.kg0 * ph.grp;
     stage_x<NT>(prog, ph, io, kc0 * ck, (min(kc0 + P.S.kgn * ph.grp, ph.KC) - kc0) * ck, xs, sm, p);
     VP_TRACE(threadIdx.x == 0, p, 1);
-    float tsc[NT][2];
-#pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      tsc[j][0] = sm.xscale[8 * j + 2 * c];
-      tsc[j][1] = sm.xscale[8 * j + 2 * c + 1];
-    }
-    HeadBest<NT> hb;
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        hb.v[j][h] = -INFINITY;
-        hb.i[j][h] = 0x7fffffff;
-      }
-    const int ub = sl.wb[warp], ue = sl.wb[warp + 1];
-    const uint32_t xlane = smem_addr(xs) + lane * 16;
-    const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
-    const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
-    const bool two = ph.layout == kInterleaved;
-    int rb = ub < ue ? P.rb0 + ub / P.S.kgn : 0, kgl = ub < ue ? ub % P.S.kgn : 0;
-    float acc[NT][4], acc2[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
-    int cur = -1;
-    for (int u = ub; u < ue; ++u) {
-      if (rb != cur) {
-        if (cur >= 0) {
-          flush<NT>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
-#pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
-        }
-        cur = rb;
-      }
-      const int slot = (int)(seq % kSlots);
-      if (!sm.abort && !mbar_wait_bounded(&sm.full[warp][slot], (seq / kSlots) & 1u)) {
-        sm.abort = 1;
-        atomicExch(io.status, kStatusTimeout);
-      }
-      const uint32_t ua = ring_w + slot * kSlotBytes, xa = xlane + kgl * ph.grp * pair_stride;
-      if constexpr (kQ4) {  // one or two consecutive chunks of the row block, 4 groups each
-        unit_q4<NT>(ua, xa, lane, acc);
-        if ((P.S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
-      } else if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
-        unit_nvfp4<NT>(ua, xa, lane, acc, acc);
-        unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
-      } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
-        const bool second = ph.grp == 2 && (P.S.kg0 + kgl) * 2 + 1 < ph.KC;
-        if (ph.fmt == kFmtNvfp4) {
-          unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
-          if (second) unit_nvfp4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
-        } else {
-          unit_fp8<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
-          if (second) unit_fp8<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc, NT == 1 ? acc2 : acc);
-        }
-      }
-      __syncwarp();
-      if (lane == 0 && pc.p < prog.n && !sm.abort) {
-        fence_proxy_async_smem();
-        issue_unit(pc, ua, &sm.full[warp][slot], pol);
-        cursor_next(pc, prog, sm.ps, G, cta, warp);
-        ++issued;
-      }
-      ++seq;
-      if (++kgl == P.S.kgn) {
-        kgl = 0;
-        ++rb;
-      }
-    }
-    VP_TRACE(lane == 0, p, 2 + warp);
-    if (cur >= 0) flush<NT>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
-    if (p + 2 < prog.n) {  // the first warp of the CTA done with this phase fills phase p + 2's slot
-      int won = 0;
-      if (lane == 0) won = atomicCAS(&sm.fillp, p, p + 1) == p;
-      if (__shfl_sync(0xffffffffu, won, 0)) fill_slot(sm.ps[(p + 2) % kPhaseSlots], prog, io, p + 2, G, cta, lane);
-    }
-    VP_TRACE(lane == 0, p, 18 + warp);
-    if (ph.ks > 1) {  // every row block's slices meet after a grid barrier
-      grid_barrier(io, G, (unsigned)G * ++nbar, sm);
-      cross_slice_fixup<NT>(ph, io, prog.M, G, hb, warp, lane);
-      VP_TRACE(threadIdx.x == 0, p, 35);
-    }
-    if (ph.epi == kEpiHead) head_finish<NT>(prog, io, G, hb, xs, sm, warp, lane);
+    // the streaming part of the phase
+    // (at 4 tiles the other phases use an instantiation without the running argmax: registers)
+    if (NT == 4 && ph.epi != kEpiHead)
+      phase_units<NT, kQ4, false>(prog, io, ph, sl, p, xs, sm, ring_w, pol, issued, seq, nbar);
+    else
+      phase_units<NT, kQ4, true>(prog, io, ph, sl, p, xs, sm, ring_w, pol, issued, seq, nbar);
     if (p + 1 < prog.n) grid_barrier(io, G, (unsigned)G * ++nbar, sm);
     VP_TRACE(threadIdx.x == 0, p, 34);
   }
