@@ -502,6 +502,58 @@ __device__ __forceinline__ void unit_nvfp4(uint32_t ua, uint32_t xa, int lane, f
   }
 }
 
+// The same K chunk of two row blocks (chunk u0 -> acc0, chunk u1 -> acc1) against the same
+// activations: each B fragment is loaded from shared memory once for both row blocks' MMAs.  The
+// code words are loaded per half chunk (steps 0-7, then 8-15) to keep fewer registers live.
+template <int NT>
+__device__ __forceinline__ void unit_nvfp4_pair(uint32_t u0, uint32_t u1, uint32_t xa, int lane, float (&acc0)[NT][4],
+                                                float (&acc1)[NT][4]) {
+  const int g = lane >> 2;
+  const uint4 s00 = lds128(u0 + 1024 + g * 16), s01 = lds128(u0 + 1152 + 1024 + g * 16);
+  const uint4 s10 = lds128(u1 + 1024 + g * 16), s11 = lds128(u1 + 1152 + 1024 + g * 16);
+  const uint32_t sw00[4] = {s00.x, s00.y, s00.z, s00.w}, sw01[4] = {s01.x, s01.y, s01.z, s01.w};
+  const uint32_t sw10[4] = {s10.x, s10.y, s10.z, s10.w}, sw11[4] = {s11.x, s11.y, s11.z, s11.w};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const uint4 c00 = lds128(u0 + 512 * half + lane * 16), c01 = lds128(u0 + 1152 + 512 * half + lane * 16);
+    const uint4 c10 = lds128(u1 + 512 * half + lane * 16), c11 = lds128(u1 + 1152 + 512 * half + lane * 16);
+    const uint32_t w00[4] = {c00.x, c00.y, c00.z, c00.w}, w01[4] = {c01.x, c01.y, c01.z, c01.w};
+    const uint32_t w10[4] = {c10.x, c10.y, c10.z, c10.w}, w11[4] = {c11.x, c11.y, c11.z, c11.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int p = 4 * half + q;
+      uint4 b[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) b[j] = lds128(xa + (p * NT + j) * 512);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {  // row block r of the pair
+        const uint32_t* sa = r ? sw10 : sw00;
+        const uint32_t* sb = r ? sw11 : sw01;
+        const uint32_t sc0 = e4m3x2_to_f16x2((p & 1) ? (sa[p >> 1] >> 16) : sa[p >> 1]);
+        const uint32_t sc1 = e4m3x2_to_f16x2((p & 1) ? (sb[p >> 1] >> 16) : sb[p >> 1]);
+        uint32_t o0[4], o1[4];
+        e2m1x8_to_f16x2x4(r ? w10[q] : w00[q], o0);
+        e2m1x8_to_f16x2x4(r ? w11[q] : w01[q], o1);
+        float (&acc)[NT][4] = r ? acc1 : acc0;
+        {
+          const uint32_t d0 = dup_lo16(sc0), d1 = dup_lo16(sc1);
+          const uint32_t a0 = hmul2_u32(o0[0], d0), a1 = hmul2_u32(o1[0], d1);
+          const uint32_t a2 = hmul2_u32(o0[1], d0), a3 = hmul2_u32(o1[1], d1);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma_f16_16816(acc[j], a0, a1, a2, a3, b[j].x, b[j].y);
+        }
+        {
+          const uint32_t d0 = dup_hi16(sc0), d1 = dup_hi16(sc1);
+          const uint32_t a0 = hmul2_u32(o0[2], d0), a1 = hmul2_u32(o1[2], d1);
+          const uint32_t a2 = hmul2_u32(o0[3], d0), a3 = hmul2_u32(o1[3], d1);
+#pragma unroll
+          for (int j = 0; j < NT; ++j) mma_f16_16816(acc[j], a0, a1, a2, a3, b[j].z, b[j].w);
+        }
+      }
+    }
+  }
+}
+
 // One Q4 chunk (w = scale * q + bias per 64-wide group): for each group, the codes q (exact f16
 // integers) times the staged activations on the tensor core into a group accumulator t, and a
 // ones operand times the same activations into sx, the group's activation sums of the C fragment's
@@ -1011,8 +1063,7 @@ __device__ __forceinline__ void phase_units(const Program& prog, const Io& io, c
       unit_q4<NT>(ua, xa, lane, acc);
       if ((P.S.kg0 + kgl) * 2 + 1 < ph.KC) unit_q4<NT>(ua + chunk_bytes, xa + pair_stride, lane, acc);
     } else if (two) {  // gate chunk -> acc, up chunk -> acc2, same activations (NVFP4 only)
-      unit_nvfp4<NT>(ua, xa, lane, acc, acc);
-      unit_nvfp4<NT>(ua + chunk_bytes, xa, lane, acc2, acc2);
+      unit_nvfp4_pair<NT>(ua, ua + chunk_bytes, xa, lane, acc, acc2);
     } else {  // one or two consecutive chunks of the row block (one chain per n-tile, two if NT = 1)
       const bool second = ph.grp == 2 && (P.S.kg0 + kgl) * 2 + 1 < ph.KC;
       if (ph.fmt == kFmtNvfp4) {
