@@ -24,8 +24,12 @@ LIB_TRACE = os.path.join(PKG, "libverify_trace.so")
 # one CTA skip its first grid-barrier arrival: the build in which a test makes a wait run out.
 BUILD_WAIT = os.path.join(PKG, "_build_waittest")
 LIB_WAIT = os.path.join(PKG, "libverify_waittest.so")
+# A measurement build of the executor's unit loop alone (csrc/unit_bench.cu; unit_bench.py runs it).
+BUILD_UNIT = os.path.join(PKG, "_build_unitbench")
+LIB_UNIT = os.path.join(PKG, "libverify_unitbench.so")
 VARIANTS = {"": (LIB, BUILD, []), "trace": (LIB_TRACE, BUILD_TRACE, ["-DVP_PHASE_TRACE"]),
-            "waittest": (LIB_WAIT, BUILD_WAIT, ["-DVP_WAIT_TEST"])}
+            "waittest": (LIB_WAIT, BUILD_WAIT, ["-DVP_WAIT_TEST"]), "unitbench": (LIB_UNIT, BUILD_UNIT, [])}
+UNIT_SOURCES = ["unit_bench.cu"]
 SOURCES = ["api.cu", "exec_nt12.cu", "exec_nt34.cu", "exec_q4.cu", "sample.cu", "attention.cu", "gdn.cu",
            "loop.cu", "errors.cu", "mixer.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -48,8 +52,9 @@ def _stale(target: str, deps) -> bool:
 
 def build(force: bool = False, verbose: bool = False, trace: bool = False, variant: str = "") -> str:
     """Builds libverify.so (or a measurement / test variant of it: "trace" with the phase timeline,
-    "waittest" with tiny wait limits; trace=True is variant "trace") and returns its path; nothing
-    is rebuilt when the library is newer than every source."""
+    "waittest" with tiny wait limits, "unitbench" the unit-loop breakdown alone; trace=True is
+    variant "trace") and returns its path; nothing is rebuilt when the library is newer than every
+    source."""
     lib, bdir, defs = VARIANTS["trace" if trace else variant]
     deps = _inputs()
     if not force and not _stale(lib, deps):
@@ -57,7 +62,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False, varia
     os.makedirs(bdir, exist_ok=True)
     procs = []
     objs = []
-    for src in SOURCES:
+    for src in UNIT_SOURCES if variant == "unitbench" else SOURCES:
         obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = ["nvcc", *ARCH, *FLAGS, *defs, "-c", os.path.join(CSRC, src), "-o", obj]
