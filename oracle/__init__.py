@@ -114,6 +114,10 @@ def lib():
             L.orc_argmax.restype = ctypes.c_int64
             L.orc_argmax.argtypes = [P, ctypes.c_int64]
             L.orc_accept.argtypes = [P, P, ctypes.c_int, P, P]
+            L.orc_accept_rows.argtypes = [P, P, ctypes.c_int, ctypes.c_int, P, P]
+            L.orc_lookup_drafts_rows.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
+            L.orc_commit_append_rows.restype = ctypes.c_int
+            L.orc_commit_append_rows.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P]
             L.orc_verify_pass.restype = ctypes.c_int
             L.orc_verify_pass.argtypes = [ctypes.POINTER(Geom), P, P, P, P, ctypes.c_double, P,
                                           ctypes.c_int, P, P, P, P, P, P, P, ctypes.c_int]
@@ -301,23 +305,30 @@ def embed_nvfp4(codes: np.ndarray, scales: np.ndarray, ts: float, tokens: np.nda
     return out
 
 
-def lookup_drafts(hist: np.ndarray, hist_len: np.ndarray, max_match: int = 8) -> np.ndarray:
-    """Anchor + 7 lookup drafts per lane (int32 [8 L]) from histories [L][cap]."""
+def lookup_drafts(hist: np.ndarray, hist_len: np.ndarray, max_match: int = 8, rows: int = 8) -> np.ndarray:
+    """Anchor + rows - 1 lookup drafts per lane (int32 [rows L]) from histories [L][cap]."""
     hist = np.ascontiguousarray(hist, dtype=np.int32)
     L, cap = hist.shape
     hl = np.ascontiguousarray(hist_len, dtype=np.int32)
-    out = np.zeros(8 * L, np.int32)
-    lib().orc_lookup_drafts(_p(hist), _p(hl), L, cap, int(max_match), _p(out))
+    out = np.zeros(rows * L, np.int32)
+    if rows == 8:
+        lib().orc_lookup_drafts(_p(hist), _p(hl), L, cap, int(max_match), _p(out))
+    else:
+        lib().orc_lookup_drafts_rows(_p(hist), _p(hl), L, cap, int(max_match), int(rows), _p(out))
     return out
 
 
 def commit_append(hist: np.ndarray, hist_len: np.ndarray, n_commit: np.ndarray, committed: np.ndarray) -> int:
-    """Appends each lane's committed tokens in place; returns 0, or -1 if a lane's history is full."""
+    """Appends each lane's committed tokens (committed [L][rows]) in place; returns 0, or -1 if a lane's
+    history is full."""
     assert hist.dtype == np.int32 and hist.flags.c_contiguous and hist_len.dtype == np.int32
     L, cap = hist.shape
     nc = np.ascontiguousarray(n_commit, dtype=np.int32)
     cm = np.ascontiguousarray(committed, dtype=np.int32)
-    return int(lib().orc_commit_append(_p(hist), _p(hist_len), L, cap, _p(nc), _p(cm)))
+    rows = cm.size // L
+    if rows == 8:
+        return int(lib().orc_commit_append(_p(hist), _p(hist_len), L, cap, _p(nc), _p(cm)))
+    return int(lib().orc_commit_append_rows(_p(hist), _p(hist_len), L, cap, int(rows), _p(nc), _p(cm)))
 
 
 def silu_mul(g: np.ndarray, u: np.ndarray) -> np.ndarray:
@@ -341,13 +352,18 @@ def argmax(v: np.ndarray) -> int:
     return int(lib().orc_argmax(_p(v), v.size))
 
 
-def accept(t: np.ndarray, pending: np.ndarray):
+def accept(t: np.ndarray, pending: np.ndarray, rows: int = 8):
+    """Greedy acceptance per lane of `rows` verify rows (anchor + rows - 1 drafts): n_commit [lanes],
+    committed [lanes][rows]."""
     t = np.ascontiguousarray(t, dtype=np.int32)
     pending = np.ascontiguousarray(pending, dtype=np.int32)
-    lanes = t.size // 8
+    lanes = t.size // rows
     nc = np.zeros(lanes, np.int32)
-    cm = np.zeros((lanes, 8), np.int32)
-    lib().orc_accept(_p(t), _p(pending), lanes, _p(nc), _p(cm))
+    cm = np.zeros((lanes, rows), np.int32)
+    if rows == 8:
+        lib().orc_accept(_p(t), _p(pending), lanes, _p(nc), _p(cm))
+    else:
+        lib().orc_accept_rows(_p(t), _p(pending), lanes, int(rows), _p(nc), _p(cm))
     return nc, cm
 
 

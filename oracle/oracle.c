@@ -335,19 +335,24 @@ int64_t orc_argmax(const double* v, int64_t n) {
     return best;
 }
 
-/* Greedy acceptance per lane (8 rows: the committed anchor token + 7 drafts).
- * t[8l + j] is the target's token at verify row j; pending[8l + j + 1] is draft j.
- * acc = number of leading drafts equal to the target's tokens (0..7);
- * n_commit = acc + 1 and committed[l][0..acc] = t[8l .. 8l + acc] (accepted drafts, then the
- * target's own token); committed[l][acc+1..7] = -1. */
+/* Greedy acceptance per lane of R verify rows (the committed anchor token + R - 1 drafts).
+ * t[R l + j] is the target's token at verify row j; pending[R l + j + 1] is draft j.
+ * acc = number of leading drafts equal to the target's tokens (0..R-1);
+ * n_commit = acc + 1 and committed[l][0..acc] = t[R l .. R l + acc] (accepted drafts, then the
+ * target's own token); committed[l][acc+1..R-1] = -1.  The pages' verify has R = 8; lookup drafts
+ * ("mlx-dspark", section "Lookup drafts") verify 16-32 rows. */
+void orc_accept_rows(const int32_t* t, const int32_t* pending, int lanes, int R, int32_t* n_commit,
+                     int32_t* committed) {
+    for (int l = 0; l < lanes; ++l) {
+        int base = R * l, acc = 0;
+        while (acc < R - 1 && t[base + acc] == pending[base + acc + 1]) acc++;
+        n_commit[l] = acc + 1;
+        for (int j = 0; j < R; ++j) committed[R * l + j] = (j <= acc) ? t[base + j] : -1;
+    }
+}
 void orc_accept(const int32_t* t, const int32_t* pending, int lanes, int32_t* n_commit,
                 int32_t* committed) {
-    for (int l = 0; l < lanes; ++l) {
-        int base = 8 * l, acc = 0;
-        while (acc < 7 && t[base + acc] == pending[base + acc + 1]) acc++;
-        n_commit[l] = acc + 1;
-        for (int j = 0; j < 8; ++j) committed[8 * l + j] = (j <= acc) ? t[base + j] : -1;
-    }
+    orc_accept_rows(t, pending, lanes, 8, n_commit, committed);
 }
 
 /* ------------------------------------------------------------------ verify-pass surrogate */
@@ -620,9 +625,10 @@ void orc_embed_nvfp4(const uint8_t* codes, const uint8_t* scales, double ts, con
     }
 }
 
-/* Lane l: history hist[l * cap .. + T), T = hist_len[l] >= 1; writes pending[8l .. 8l + 7]. */
-void orc_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int L, int cap, int max_match,
-                       int32_t* pending) {
+/* Lane l: history hist[l * cap .. + T), T = hist_len[l] >= 1; writes pending[R l .. R l + R - 1]:
+ * the anchor, then R - 1 drafts. */
+void orc_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, int L, int cap, int max_match, int R,
+                            int32_t* pending) {
     for (int l = 0; l < L; ++l) {
         const int32_t* h = hist + (int64_t)l * cap;
         const int T = hist_len[l];
@@ -633,26 +639,35 @@ void orc_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int L, int 
             if (len >= 1 && len >= best_len) { best_len = len; best_p = p; }  /* ties: the later p */
         }
         const int32_t anchor = h[T - 1];
-        pending[8 * l] = anchor;
+        pending[R * l] = anchor;
         int32_t last = anchor;
-        for (int j = 0; j < 7; ++j) {
+        for (int j = 0; j < R - 1; ++j) {
             if (best_p >= 0 && best_p + j < T) last = h[best_p + j];
-            pending[8 * l + 1 + j] = last;
+            pending[R * l + 1 + j] = last;
         }
     }
 }
+void orc_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int L, int cap, int max_match,
+                       int32_t* pending) {
+    orc_lookup_drafts_rows(hist, hist_len, L, cap, max_match, 8, pending);
+}
 
-/* Appends committed[l][0 .. n_commit[l]) to lane l's history; returns -1 if one would not fit. */
-int orc_commit_append(int32_t* hist, int32_t* hist_len, int L, int cap, const int32_t* n_commit,
-                      const int32_t* committed) {
+/* Appends committed[l][0 .. n_commit[l]) (rows of R entries) to lane l's history; returns -1 if one
+ * would not fit. */
+int orc_commit_append_rows(int32_t* hist, int32_t* hist_len, int L, int cap, int R, const int32_t* n_commit,
+                           const int32_t* committed) {
     int rc = 0;
     for (int l = 0; l < L; ++l) {
         const int n = n_commit[l];
         if (hist_len[l] + n > cap) { rc = -1; continue; }
-        for (int j = 0; j < n; ++j) hist[(int64_t)l * cap + hist_len[l] + j] = committed[8 * l + j];
+        for (int j = 0; j < n; ++j) hist[(int64_t)l * cap + hist_len[l] + j] = committed[R * l + j];
         hist_len[l] += n;
     }
     return rc;
+}
+int orc_commit_append(int32_t* hist, int32_t* hist_len, int L, int cap, const int32_t* n_commit,
+                      const int32_t* committed) {
+    return orc_commit_append_rows(hist, hist_len, L, cap, 8, n_commit, committed);
 }
 
 /* Probability the draft gave token t (0 when t is not among its 16 candidates). */

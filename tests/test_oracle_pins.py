@@ -829,3 +829,81 @@ def test_commit_append_and_full_history():
     cm = np.array([[7, 8, -1, -1, -1, -1, -1, -1], [4, 5, 6, -1, -1, -1, -1, -1]], np.int32)
     assert oracle.commit_append(hist, hl, nc, cm) == -1  # lane 1 would overflow: left as it was
     assert hist[0, :5].tolist() == [1, 2, 3, 7, 8] and hl.tolist() == [5, 8]
+
+
+# ------------------------------------------------------------------ wider verify (R rows per lane)
+# "mlx-dspark" -- "Lookup drafts": deep lookup matches verify 16-32 rows; the acceptance rule is the
+# same longest prefix over R - 1 drafts.
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5])
+def test_accept_rows_brute_force_binary_vocab(R):
+    """Every target pattern (R tokens) x every draft pattern (R - 1 tokens) over V = 2, against the
+    definition: 1 + the length of the longest common prefix of the drafts and the first R - 1
+    targets, the committed row the targets up to it and -1 after."""
+    tp = np.array(list(itertools.product([0, 1], repeat=R)), np.int32)
+    drafts = list(itertools.product([0, 1], repeat=R - 1))
+    dp = np.array(drafts, np.int32).reshape(len(drafts), R - 1)
+    T = np.repeat(tp, len(dp), axis=0)
+    D = np.tile(dp, (len(tp), 1))
+    pending = np.concatenate([np.full((T.shape[0], 1), 7, np.int32), D], axis=1)
+    nc, cm = oracle.accept(T.reshape(-1), pending.reshape(-1), rows=R)
+    for i in range(T.shape[0]):
+        lcp = next((j for j in range(R - 1) if T[i, j] != D[i, j]), R - 1)
+        assert nc[i] == lcp + 1
+        assert cm[i].tolist() == [int(T[i, j]) if j <= lcp else -1 for j in range(R)]
+    assert nc.min() == 1 and nc.max() == R
+
+
+@pytest.mark.parametrize("R", [16, 32])
+def test_accept_rows_planted_prefixes(R):
+    """Random targets with every prefix length 0 .. R - 1 planted once per lane (the draft after the
+    prefix differs): n_commit is the planted length + 1; R = 8 equals the 8-row function."""
+    rng = np.random.default_rng(R)
+    L = R
+    T = rng.integers(0, 1000, (L, R)).astype(np.int32)
+    D = rng.integers(0, 1000, (L, R - 1)).astype(np.int32)
+    for l in range(L):
+        n = l % R
+        D[l, :n] = T[l, :n]
+        if n < R - 1:
+            D[l, n] = (T[l, n] + 1) % 1000
+    pending = np.concatenate([np.zeros((L, 1), np.int32), D], axis=1)
+    nc, cm = oracle.accept(T.reshape(-1), pending.reshape(-1), rows=R)
+    assert nc.tolist() == [l % R + 1 for l in range(L)]
+    T8 = T[:, :8].copy()
+    P8 = pending[:, :8].copy()
+    assert [np.array_equal(a, b) for a, b in zip(oracle.accept(T8.reshape(-1), P8.reshape(-1), rows=8),
+                                                   oracle.accept(T8.reshape(-1), P8.reshape(-1)))] == [True, True]
+
+
+def test_lookup_drafts_rows_worked_examples():
+    """16-row lookups of the worked examples above: the continuation copied while it lasts, then its
+    last token repeated to fill 15 drafts; the first 8 entries equal the 8-row lookup."""
+    cases = [
+        ([5, 6, 7, 8, 5, 6], [6, 7, 8, 5, 6] + [6] * 11),
+        ([1, 2, 9, 2, 3, 1, 2], [2, 9, 2, 3, 1, 2] + [2] * 10),
+        ([1, 2, 3], [3] * 16),
+    ]
+    cap = 16
+    hist = np.zeros((len(cases), cap), np.int32)
+    hl = np.zeros(len(cases), np.int32)
+    for i, (h, _) in enumerate(cases):
+        hist[i, :len(h)] = h
+        hl[i] = len(h)
+    out = oracle.lookup_drafts(hist, hl, rows=16).reshape(-1, 16)
+    out8 = oracle.lookup_drafts(hist, hl).reshape(-1, 8)
+    for i, (_, want) in enumerate(cases):
+        assert out[i].tolist() == want, (i, out[i].tolist())
+        assert out[i, :8].tolist() == out8[i].tolist()
+
+
+def test_commit_append_rows():
+    hist = np.zeros((2, 40), np.int32)
+    hl = np.array([2, 0], np.int32)
+    hist[0, :2] = [9, 9]
+    cm = np.full((2, 16), -1, np.int32)
+    cm[0, :11] = np.arange(11)
+    cm[1, :1] = [42]
+    assert oracle.commit_append(hist, hl, np.array([11, 1], np.int32), cm) == 0
+    assert hist[0, :13].tolist() == [9, 9] + list(range(11)) and hist[1, :1].tolist() == [42]
+    assert hl.tolist() == [13, 1]
