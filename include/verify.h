@@ -42,6 +42,9 @@
  *                drafter)" and "Lookup drafts" (the continuation of an earlier match of the current
  *                text is a free draft); "Beating Splash on an M5 Max", section "The kernels were not
  *                the gap" (host synchronisations per round were the cost).
+ *   [WIDE]       "Speculative decoding" (mlx-dspark), section "Lookup drafts": when the current text's
+ *                match runs deep, drafts grow (to 32 tokens) and 16-32 rows are verified in one pass;
+ *                the acceptance rule is the same longest prefix [LM-accept] over R - 1 drafts.
  *   [SP-q4]      "144 tok/s needs 502 GB/s" (Splash), section "The engine hard-codes the model": the
  *                other engines' affine 4-bit format, per group of 64 inputs 32 bytes of codes plus
  *                a bf16 scale and a bf16 bias (nine bytes per sixteen weights); "Beating Splash on
@@ -214,6 +217,14 @@ vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const 
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending,
                            int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws,
                            size_t ws_bytes, void* stream);
+/* The same with R = rows verify rows per lane [WIDE] (1 <= rows <= 32, M = rows * lanes <= 32):
+ *   acc = 0; while (acc < R - 1 && argmax[R l + acc] == pending[R l + acc + 1]) acc++;
+ *   n_commit[l] = acc + 1 (1..R);  committed[l][j] = argmax[R l + j] for j <= acc, -1 after.
+ * n_commit: int32 [M / R]; committed: int32 [M / R][R].  rows = 8 is vp_argmax_accept.
+ * VP_ERR_SHAPE for rows or M out of range, or M % rows != 0. */
+vp_status vp_argmax_accept_rows(const float* logits, int M, int V, int rows, const int32_t* pending,
+                                int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws,
+                                size_t ws_bytes, void* stream);
 
 /* Sampled acceptance over given fp32 logits [M][V] (M = 8 * lanes; 1 <= V <= 1,048,576)
  * [SP-sample].  Per row r, the target distribution p_r: the top_k (1..32, <= V) largest logits
@@ -337,6 +348,14 @@ size_t vp_pass_workspace_bytes(const vp_model* model, int M);
 vp_status vp_verify_pass(const vp_model* model, const void* x0, int M, const int32_t* pending,
                          int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace,
                          float* logits, void* ws, size_t ws_bytes, void* stream);
+/* The verify pass with R = rows verify rows per lane [WIDE]: the same weight stream and logits for
+ * the M rows (M = rows * lanes <= 32, 1 <= rows <= 32), the acceptance of vp_argmax_accept_rows in
+ * the head (n_commit: int32 [M / R]; committed: int32 [M / R][R]).  One lane of 16 or 32 rows, or two
+ * of 16, verify a deep lookup draft in one pass.  rows = 8 is vp_verify_pass; the workspace is
+ * vp_pass_workspace_bytes(model, M). */
+vp_status vp_verify_pass_rows(const vp_model* model, const void* x0, int M, int rows, const int32_t* pending,
+                              int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace,
+                              float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* The verify pass with sampled instead of greedy acceptance [SP-sample]: the pass of
  * vp_verify_pass, whose head phase writes the fp32 logits [M][vocab] (into `logits` when non-NULL,
@@ -487,11 +506,19 @@ vp_status vp_embed_nvfp4(const void* codes, const void* scales, float ts, const 
  * pending entries 0, and the status. */
 vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
                            int32_t* pending, int* status, void* stream);
+/* The same with R = rows entries per lane [WIDE]: pending[R l] = the anchor, then R - 1 drafts;
+ * 1 <= rows <= 32, lanes * rows <= 32; pending: int32 [R lanes].  rows = 8 is vp_lookup_drafts. */
+vp_status vp_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, int lanes, int rows, int cap,
+                                int max_match, int32_t* pending, int* status, void* stream);
 /* Appends committed[l][0 .. n_commit[l]) to lane l's history (a lane that would overflow cap, or whose
  * n_commit is outside 1..8, is left as it is, with the status).  lanes 1..4; committed: int32
  * [lanes][8]. */
 vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap, const int32_t* n_commit,
                            const int32_t* committed, int* status, void* stream);
+/* The same with committed rows of R = rows entries [WIDE] (n_commit outside 1..R: left as it is,
+ * with the status); 1 <= rows <= 32, lanes * rows <= 32; committed: int32 [lanes][R]. */
+vp_status vp_commit_append_rows(int32_t* hist, int32_t* hist_len, int lanes, int rows, int cap,
+                                const int32_t* n_commit, const int32_t* committed, int* status, void* stream);
 /* `steps` rounds with no host in the loop: x0 = embed(pending) (the embedding table emb_codes /
  * emb_scales / emb_ts, [vocab][hidden]); vp_verify_pass; append the committed tokens; lookup drafts
  * into pending.  pending must hold the first round's anchor + drafts (e.g. from vp_lookup_drafts).
@@ -503,6 +530,14 @@ vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_code
                           float emb_ts, int vocab, int hidden, int32_t* hist, int32_t* hist_len, int cap,
                           int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,
                           int32_t* committed, void* ws, size_t ws_bytes, int* status, void* stream);
+/* The decode loop with R = rows verify rows per lane [WIDE] (the pass, append and lookup of the
+ * _rows calls above; 1 <= rows <= 32, lanes * rows <= 32; x0: bf16 [R lanes][hidden]; pending,
+ * committed as there).  rows = 8 is vp_decode_steps. */
+vp_status vp_decode_steps_rows(const vp_model* model, int steps, int rows, const void* emb_codes,
+                               const void* emb_scales, float emb_ts, int vocab, int hidden, int32_t* hist,
+                               int32_t* hist_len, int cap, int lanes, int max_match, int32_t* pending, void* x0,
+                               int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes,
+                               int* status, void* stream);
 
 #ifdef __cplusplus
 }

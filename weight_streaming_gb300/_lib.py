@@ -28,6 +28,8 @@ EXPORTS = [
     "vp_linear_nvfp4_noalloc", "vp_noalloc_read_status", "vp_trace_read", "vp_packed_bytes_q4", "vp_pack_q4", "vp_linear_q4",
     "vp_sample_accept", "vp_attention_verify", "vp_gdn_scan", "vp_embed_nvfp4", "vp_lookup_drafts",
     "vp_commit_append", "vp_decode_steps", "vp_pass_sampled_workspace_bytes", "vp_verify_pass_sampled",
+    "vp_argmax_accept_rows", "vp_verify_pass_rows", "vp_lookup_drafts_rows", "vp_commit_append_rows",
+    "vp_decode_steps_rows",
     "vp_model_set_cores", "vp_pass_cores_workspace_bytes", "vp_verify_pass_cores", "vp_pass_cores_launch_count", "vp_commit_cores",
 ]
 
@@ -88,6 +90,11 @@ def _load():
         "vp_linear_fp8": (I, [P, F, P, P, I, I, I, P, S, P]),
         "vp_head_argmax_accept": (I, [P, F, P, I, I, I, P, P, P, P, P, P, S, P]),
         "vp_argmax_accept": (I, [P, I, I, P, P, P, P, P, S, P]),
+        "vp_argmax_accept_rows": (I, [P, I, I, I, P, P, P, P, P, S, P]),
+        "vp_verify_pass_rows": (I, [P, P, I, I, P, P, P, P, P, P, P, S, P]),
+        "vp_lookup_drafts_rows": (I, [P, P, I, I, I, I, P, P, P]),
+        "vp_commit_append_rows": (I, [P, P, I, I, I, P, P, P, P]),
+        "vp_decode_steps_rows": (I, [P, I, I, P, P, F, I, I, P, P, I, I, I, P, P, P, P, P, P, S, P, P]),
         "vp_model_create": (I, [I, I, F, ctypes.POINTER(vp_layer_desc), I, ctypes.POINTER(vp_head_desc),
                                 ctypes.POINTER(P)]),
         "vp_model_destroy": (None, [P]),
@@ -237,6 +244,14 @@ def vp_argmax_accept(logits, M: int, V: int, pending, argmax, n_commit, committe
                                                    _ptr(committed), _ptr(ws), wb, _stream(stream)))
 
 
+def vp_argmax_accept_rows(logits, M: int, V: int, rows: int, pending, argmax, n_commit, committed, ws, stream=None,
+                          ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_argmax_accept_rows", _L.vp_argmax_accept_rows(_ptr(logits), M, V, rows, _ptr(pending), _ptr(argmax),
+                                                             _ptr(n_commit), _ptr(committed), _ptr(ws), wb,
+                                                             _stream(stream)))
+
+
 def vp_sample_accept(logits, M: int, V: int, temperature: float, top_k: int, top_p: float, pending, draft_tokens,
                      draft_probs, uniforms, n_commit, committed, ws, stream=None, ws_bytes=None):
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
@@ -270,6 +285,19 @@ def vp_lookup_drafts(hist, hist_len, lanes: int, cap: int, max_match: int, pendi
                                                    _ptr(status), _stream(stream)))
 
 
+def vp_lookup_drafts_rows(hist, hist_len, lanes: int, rows: int, cap: int, max_match: int, pending, status=None,
+                          stream=None):
+    _check("vp_lookup_drafts_rows", _L.vp_lookup_drafts_rows(_ptr(hist), _ptr(hist_len), lanes, rows, cap, max_match,
+                                                             _ptr(pending), _ptr(status), _stream(stream)))
+
+
+def vp_commit_append_rows(hist, hist_len, lanes: int, rows: int, cap: int, n_commit, committed, status=None,
+                          stream=None):
+    _check("vp_commit_append_rows", _L.vp_commit_append_rows(_ptr(hist), _ptr(hist_len), lanes, rows, cap,
+                                                             _ptr(n_commit), _ptr(committed), _ptr(status),
+                                                             _stream(stream)))
+
+
 def vp_commit_append(hist, hist_len, lanes: int, cap: int, n_commit, committed, status=None, stream=None):
     _check("vp_commit_append", _L.vp_commit_append(_ptr(hist), _ptr(hist_len), lanes, cap, _ptr(n_commit),
                                                    _ptr(committed), _ptr(status), _stream(stream)))
@@ -284,6 +312,17 @@ def vp_decode_steps(model: "vp_model", steps: int, emb_codes, emb_scales, emb_ts
                               _ptr(hist), _ptr(hist_len), cap, lanes, max_match, _ptr(pending), _ptr(x0),
                               _ptr(argmax), _ptr(n_commit), _ptr(committed), _ptr(ws), wb, _ptr(status),
                               _stream(stream)))
+
+
+def vp_decode_steps_rows(model: "vp_model", steps: int, rows: int, emb_codes, emb_scales, emb_ts: float, vocab: int,
+                         hidden: int, hist, hist_len, cap: int, lanes: int, max_match: int, pending, x0, argmax,
+                         n_commit, committed, ws, status=None, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_decode_steps_rows",
+           _L.vp_decode_steps_rows(model.handle, steps, rows, _ptr(emb_codes), _ptr(emb_scales), emb_ts, vocab,
+                                   hidden, _ptr(hist), _ptr(hist_len), cap, lanes, max_match, _ptr(pending),
+                                   _ptr(x0), _ptr(argmax), _ptr(n_commit), _ptr(committed), _ptr(ws), wb,
+                                   _ptr(status), _stream(stream)))
 
 
 def vp_workspace_init(ws, stream=None, ws_bytes=None):
@@ -333,6 +372,14 @@ def vp_verify_pass(model: vp_model, x0, M: int, pending, argmax, n_commit, commi
     _check("vp_verify_pass", _L.vp_verify_pass(model.handle, _ptr(x0), M, _ptr(pending), _ptr(argmax),
                                                _ptr(n_commit), _ptr(committed), _ptr(trace), _ptr(logits), _ptr(ws),
                                                wb, _stream(stream)))
+
+
+def vp_verify_pass_rows(model: vp_model, x0, M: int, rows: int, pending, argmax, n_commit, committed, trace, logits,
+                        ws, stream=None, ws_bytes=None):
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check("vp_verify_pass_rows", _L.vp_verify_pass_rows(model.handle, _ptr(x0), M, rows, _ptr(pending),
+                                                         _ptr(argmax), _ptr(n_commit), _ptr(committed), _ptr(trace),
+                                                         _ptr(logits), _ptr(ws), wb, _stream(stream)))
 
 
 def vp_pass_sampled_workspace_bytes(model: vp_model, M: int) -> int:

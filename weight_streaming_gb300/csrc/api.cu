@@ -144,7 +144,8 @@ Io make_io(void* ws, const WsLayout& L, int cs_lane) {
 }
 
 // Launches phases [0, n) of `phases` as programs of at most kMaxPhases phases each.
-vp_status run_phases(const std::vector<Phase>& phases, int M, float eps, const Io& io, int G, cudaStream_t s) {
+vp_status run_phases(const std::vector<Phase>& phases, int M, float eps, const Io& io, int G, cudaStream_t s,
+                     int rows = 8) {
   const int n = (int)phases.size();
   const int launches = (n + kMaxPhases - 1) / kMaxPhases;
   static thread_local Program prog;  // ~12 KB: kept off the stack
@@ -154,6 +155,7 @@ vp_status run_phases(const std::vector<Phase>& phases, int M, float eps, const I
     prog.M = M;
     prog.eps = eps;
     prog.q4 = phases[p0].fmt == kFmtQ4;  // a program is all Q4 or has none (checked by the callers)
+    prog.rows = rows;
     for (int i = p0; i < p1; ++i) prog.ph[i - p0] = phases[i];
     cudaError_t e = launch_exec(prog, io, G, s);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -268,7 +270,7 @@ int pack_grid(long long total) {
 // Grid (chunks, M): each CTA reduces one chunk of one row, the last CTA reduces the chunks in order
 // and runs the acceptance.
 __global__ void __launch_bounds__(256) argmax_accept_kernel(const float* __restrict__ logits, int M, int V, int chunk,
-                                                            int n_chunks, const int32_t* pending, int32_t* argmax,
+                                                            int n_chunks, int rows, const int32_t* pending, int32_t* argmax,
                                                             int32_t* n_commit, int32_t* committed, float* aux,
                                                             unsigned* cnt) {
   __shared__ float red_v[8];
@@ -326,7 +328,7 @@ __global__ void __launch_bounds__(256) argmax_accept_kernel(const float* __restr
     argmax[threadIdx.x] = i0;
   }
   __syncthreads();
-  if ((int)threadIdx.x < M / 8) accept_lane(threadIdx.x, tok, pending, n_commit, committed);
+  if ((int)threadIdx.x < M / rows) accept_lane(threadIdx.x, rows, tok, pending, n_commit, committed);
   if (threadIdx.x == 0) *cnt = 0u;
 }
 
@@ -681,6 +683,7 @@ vp_status vp_linear_nvfp4_noalloc(const void* w_packed, float tensor_scale, cons
   prog.M = M;
   prog.eps = 0.0f;
   prog.q4 = 0;
+  prog.rows = 8;
   prog.ph[0] = ph;
   e = launch_exec(prog, io, sms, cs);
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
@@ -697,10 +700,11 @@ vp_status vp_noalloc_read_status(int* status, void* stream) {
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
-vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending, int32_t* argmax,
-                           int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes, void* stream) {
+vp_status vp_argmax_accept_rows(const float* logits, int M, int V, int rows, const int32_t* pending,
+                                int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes,
+                                void* stream) {
   if (!logits || !pending || !argmax || !n_commit || !committed || !ws) return VP_ERR_INVALID_ARG;
-  if (M < 8 || M > kMaxM || M % 8 || V < 1) return VP_ERR_SHAPE;
+  if (rows < 1 || rows > kMaxM || M < rows || M > kMaxM || M % rows || V < 1) return VP_ERR_SHAPE;
   if (!aligned(logits, 4) || !aligned(ws, 256) || !aligned(pending, 4) || !aligned(argmax, 4) ||
       !aligned(n_commit, 4) || !aligned(committed, 4))
     return VP_ERR_ALIGNMENT;
@@ -713,10 +717,16 @@ vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pen
   const WsLayout L = ws_layout(4, 0);
   uint8_t* b = (uint8_t*)ws;
   argmax_accept_kernel<<<dim3(n_chunks, M), 256, 0, (cudaStream_t)stream>>>(
-      logits, M, V, chunk, n_chunks, pending, argmax, n_commit, committed, (float*)(b + L.head_aux),
+      logits, M, V, chunk, n_chunks, rows, pending, argmax, n_commit, committed, (float*)(b + L.head_aux),
       (unsigned*)(b + L.head_cnt));
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
+vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending, int32_t* argmax,
+                           int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes, void* stream) {
+  if (M < 8 || M % 8) return VP_ERR_SHAPE;
+  return vp_argmax_accept_rows(logits, M, V, 8, pending, argmax, n_commit, committed, ws, ws_bytes, stream);
 }
 
 }  // extern "C"
@@ -974,7 +984,7 @@ namespace {
 // The pass's launches once its arguments are checked: the x0 copy, then the phase program.
 vp_status enqueue_pass(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
                        int32_t* n_commit, int32_t* committed, void* trace, float* logits, void* ws, int sms,
-                       cudaStream_t s) {
+                       cudaStream_t s, int rows = 8) {
   const std::vector<Phase>& phases = md->phases[nt_of(M) - 1];
   const PassWs w = pass_ws(md, M);
   uint8_t* b = (uint8_t*)ws;
@@ -994,7 +1004,7 @@ vp_status enqueue_pass(const vp_model* md, const void* x0, int M, const int32_t*
   cudaError_t e = cudaMemcpyAsync(io.buf[kBufH], x0, sizeof(uint16_t) * (size_t)M * md->hidden,
                                   cudaMemcpyDeviceToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  return run_phases(phases, M, md->eps, io, sms, s);
+  return run_phases(phases, M, md->eps, io, sms, s, rows);
 }
 
 vp_status pass_io_ok(const vp_model* md, const void* x0, int M, const int32_t* pending, int32_t* argmax,
@@ -1037,6 +1047,25 @@ vp_status vp_verify_pass(const vp_model* md, const void* x0, int M, const int32_
   vp_status st = pass_io_ok(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, ws_bytes, &sms);
   if (st != VP_OK) return st;
   return enqueue_pass(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, sms, (cudaStream_t)stream);
+}
+
+vp_status vp_verify_pass_rows(const vp_model* md, const void* x0, int M, int rows, const int32_t* pending,
+                              int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace, float* logits,
+                              void* ws, size_t ws_bytes, void* stream) {
+  if (!md || !ws) return VP_ERR_INVALID_ARG;
+  if (rows < 1 || rows > kMaxM || M < rows || M > kMaxM || M % rows) return VP_ERR_SHAPE;
+  int sms = 0;
+  vp_status st = pass_args_ok(md, M, ws, ws_bytes, false);
+  if (st != VP_OK) return st;
+  if (!x0 || !pending || !argmax || !n_commit || !committed) return VP_ERR_INVALID_ARG;
+  if (!aligned(x0, 16) || (trace && !aligned(trace, 16)) || (logits && !aligned(logits, 4)) || !aligned(pending, 4) ||
+      !aligned(argmax, 4) || !aligned(n_commit, 4) || !aligned(committed, 4))
+    return VP_ERR_ALIGNMENT;
+  if ((st = device_sms(&sms)) != VP_OK) return st;
+  for (const Phase& ph : md->phases[nt_of(M) - 1])
+    if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
+  return enqueue_pass(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, sms, (cudaStream_t)stream,
+                      rows);
 }
 
 vp_status vp_model_set_cores(vp_model* md, const vp_core_geom* g, const vp_core_desc* cores, int n_layers) {

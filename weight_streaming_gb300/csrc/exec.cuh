@@ -55,15 +55,15 @@ __device__ __forceinline__ void am_shfl_xor(float& v, int& i, int off) {
     i = i2;
   }
 }
-// Greedy acceptance of lane l given the target tokens tok[8l .. 8l + 7] (the anchor pending[8l] is
-// not compared): the longest prefix of drafts equal to the target's tokens plus the target's token
-// after it.
-__device__ __forceinline__ void accept_lane(int l, const int* tok, const int32_t* pending, int32_t* n_commit,
+// Greedy acceptance of lane l of R verify rows given the target tokens tok[R l .. R l + R - 1] (the
+// anchor pending[R l] is not compared): the longest prefix of drafts equal to the target's tokens
+// plus the target's token after it.  The pages' verify has R = 8; lookup drafts verify up to 32.
+__device__ __forceinline__ void accept_lane(int l, int R, const int* tok, const int32_t* pending, int32_t* n_commit,
                                             int32_t* committed) {
   int acc = 0;
-  while (acc < 7 && tok[8 * l + acc] == pending[8 * l + acc + 1]) ++acc;
+  while (acc < R - 1 && tok[R * l + acc] == pending[R * l + acc + 1]) ++acc;
   n_commit[l] = acc + 1;
-  for (int j = 0; j < 8; ++j) committed[8 * l + j] = j <= acc ? tok[8 * l + j] : -1;
+  for (int j = 0; j < R; ++j) committed[R * l + j] = j <= acc ? tok[R * l + j] : -1;
 }
 
 // ---------------------------------------------------------------- phase geometry
@@ -958,7 +958,7 @@ __device__ __noinline__ void head_finish(const Program& prog, const Io& io, int 
     }
   }
   __syncthreads();
-  if (tid < M / 8) accept_lane(tid, sm.tok, io.pending, io.n_commit, io.committed);
+  if (tid < M / prog.rows) accept_lane(tid, prog.rows, sm.tok, io.pending, io.n_commit, io.committed);
   if (tid == 0) *io.head_cnt = 0u;
 }
 

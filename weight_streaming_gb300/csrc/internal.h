@@ -108,6 +108,7 @@ struct Program {
   int n, M;
   float eps;
   int q4;  // 1: every phase is Q4 (the executor instantiation with the Q4 unit)
+  int rows;  // verify rows per lane of the head's acceptance (anchor + rows - 1 drafts)
   Phase ph[kMaxPhases];
 };
 

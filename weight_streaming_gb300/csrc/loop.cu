@@ -57,34 +57,35 @@ __global__ void embed_kernel(const uint8_t* __restrict__ codes, const uint8_t* _
   }
 }
 
-// Appends committed[l][0 .. n_commit[l]) to lane l's history (one thread per lane); a lane whose
-// history would overflow is left as it is and VP_ERR_SHAPE is reported.
-__global__ void append_kernel(int32_t* __restrict__ hist, int32_t* __restrict__ hist_len, int L, int cap,
+// Appends committed[l][0 .. n_commit[l]) (rows of R entries) to lane l's history (one thread per
+// lane); a lane whose history would overflow is left as it is and VP_ERR_SHAPE is reported.
+__global__ void append_kernel(int32_t* __restrict__ hist, int32_t* __restrict__ hist_len, int L, int cap, int R,
                               const int32_t* __restrict__ n_commit, const int32_t* __restrict__ committed,
                               int* status) {
   const int l = threadIdx.x;
   if (l >= L) return;
   const int n = n_commit[l], T = hist_len[l];
-  if (n < 1 || n > 8 || T < 0 || T + n > cap) {
+  if (n < 1 || n > R || T < 0 || T + n > cap) {
     if (status) atomicExch(status, kStatusShapeL);
     return;
   }
-  for (int j = 0; j < n; ++j) hist[(size_t)l * cap + T + j] = committed[8 * l + j];
+  for (int j = 0; j < n; ++j) hist[(size_t)l * cap + T + j] = committed[R * l + j];
   hist_len[l] = T + n;
 }
 
 // Lookup drafts, one CTA per lane: every earlier position p (continuation hist[p..]) scores the
 // number of tokens before it that match the history's last tokens (up to max_match); the best score
 // wins, the latest p among equals (one key: score * 2^24 + p, reduced by maximum).
+// The anchor and R - 1 drafts go to pending[R l .. R l + R - 1].
 __global__ void __launch_bounds__(256) lookup_kernel(const int32_t* __restrict__ hist,
                                                     const int32_t* __restrict__ hist_len, int cap, int max_match,
-                                                    int32_t* __restrict__ pending, int* status) {
+                                                    int R, int32_t* __restrict__ pending, int* status) {
   __shared__ int red[8];
   const int l = blockIdx.x, tid = threadIdx.x;
   const int32_t* h = hist + (size_t)l * cap;
   const int T = hist_len[l];
   if (T < 1 || T > cap) {
-    if (tid < 8) pending[8 * l + tid] = 0;
+    if (tid < R) pending[R * l + tid] = 0;
     if (tid == 0 && status) atomicExch(status, kStatusShapeL);
     return;
   }
@@ -101,11 +102,11 @@ __global__ void __launch_bounds__(256) lookup_kernel(const int32_t* __restrict__
   for (int w = 1; w < (int)(blockDim.x >> 5); ++w) best = max(best, red[w]);
   const int p = best ? (best & 0xFFFFFF) : -1;
   const int32_t anchor = h[T - 1];
-  pending[8 * l] = anchor;
+  pending[R * l] = anchor;
   int32_t last = anchor;
-  for (int j = 0; j < 7; ++j) {
+  for (int j = 0; j < R - 1; ++j) {
     if (p >= 0 && p + j < T) last = h[p + j];
-    pending[8 * l + 1 + j] = last;
+    pending[R * l + 1 + j] = last;
   }
 }
 
@@ -131,37 +132,49 @@ vp_status vp_embed_nvfp4(const void* codes, const void* scales, float ts, const 
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
-vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
-                           int32_t* pending, int* status, void* stream) {
+vp_status vp_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, int lanes, int rows, int cap,
+                                int max_match, int32_t* pending, int* status, void* stream) {
   if (!hist || !hist_len || !pending) return VP_ERR_INVALID_ARG;
-  if (lanes < 1 || lanes > kMaxM / 8 || cap < 1 || cap >= (1 << 24) || max_match < 1 || max_match > 127)
+  if (rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxM || cap < 1 || cap >= (1 << 24) ||
+      max_match < 1 || max_match > 127)
     return VP_ERR_SHAPE;
   if (!al(hist, 4) || !al(hist_len, 4) || !al(pending, 4) || (status && !al(status, 4))) return VP_ERR_ALIGNMENT;
-  lookup_kernel<<<lanes, 256, 0, (cudaStream_t)stream>>>(hist, hist_len, cap, max_match, pending, status);
+  lookup_kernel<<<lanes, 256, 0, (cudaStream_t)stream>>>(hist, hist_len, cap, max_match, rows, pending, status);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+}
+
+vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
+                           int32_t* pending, int* status, void* stream) {
+  return vp_lookup_drafts_rows(hist, hist_len, lanes, 8, cap, max_match, pending, status, stream);
+}
+
+vp_status vp_commit_append_rows(int32_t* hist, int32_t* hist_len, int lanes, int rows, int cap,
+                                const int32_t* n_commit, const int32_t* committed, int* status, void* stream) {
+  if (!hist || !hist_len || !n_commit || !committed) return VP_ERR_INVALID_ARG;
+  if (rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxM || cap < 1) return VP_ERR_SHAPE;
+  if (!al(hist, 4) || !al(hist_len, 4) || !al(n_commit, 4) || !al(committed, 4) || (status && !al(status, 4)))
+    return VP_ERR_ALIGNMENT;
+  append_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(hist, hist_len, lanes, cap, rows, n_commit, committed, status);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? VP_OK : cuda_fail(e);
 }
 
 vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap, const int32_t* n_commit,
                            const int32_t* committed, int* status, void* stream) {
-  if (!hist || !hist_len || !n_commit || !committed) return VP_ERR_INVALID_ARG;
-  if (lanes < 1 || lanes > kMaxM / 8 || cap < 1) return VP_ERR_SHAPE;
-  if (!al(hist, 4) || !al(hist_len, 4) || !al(n_commit, 4) || !al(committed, 4) || (status && !al(status, 4)))
-    return VP_ERR_ALIGNMENT;
-  append_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(hist, hist_len, lanes, cap, n_commit, committed, status);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+  return vp_commit_append_rows(hist, hist_len, lanes, 8, cap, n_commit, committed, status, stream);
 }
 
-vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_codes, const void* emb_scales,
-                          float emb_ts, int vocab, int hidden, int32_t* hist, int32_t* hist_len, int cap,
-                          int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,
-                          int32_t* committed, void* ws, size_t ws_bytes, int* status, void* stream) {
+vp_status vp_decode_steps_rows(const vp_model* model, int steps, int rows, const void* emb_codes,
+                               const void* emb_scales, float emb_ts, int vocab, int hidden, int32_t* hist,
+                               int32_t* hist_len, int cap, int lanes, int max_match, int32_t* pending, void* x0,
+                               int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes,
+                               int* status, void* stream) {
   if (!model || !emb_codes || !emb_scales || !hist || !hist_len || !pending || !x0 || !argmax || !n_commit ||
       !committed || !ws)
     return VP_ERR_INVALID_ARG;
-  if (steps < 0 || lanes < 1 || lanes > kMaxM / 8) return VP_ERR_SHAPE;
-  const int M = 8 * lanes;
+  if (steps < 0 || rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxM) return VP_ERR_SHAPE;
+  const int M = rows * lanes;
   // Every argument of the four steps is checked before the first launch, so a bad call enqueues
   // nothing.  (The pass's own per-phase checks still run inside vp_verify_pass.)
   if (vocab < 1 || hidden < 16 || hidden % 16 || (long long)vocab * hidden >= (1LL << 40) || cap < 1 ||
@@ -178,14 +191,25 @@ vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_code
   for (int s = 0; s < steps; ++s) {
     vp_status st = vp_embed_nvfp4(emb_codes, emb_scales, emb_ts, pending, M, vocab, hidden, x0, status, stream);
     if (st != VP_OK) return st;
-    st = vp_verify_pass(model, x0, M, pending, argmax, n_commit, committed, nullptr, nullptr, ws, ws_bytes, stream);
+    st = vp_verify_pass_rows(model, x0, M, rows, pending, argmax, n_commit, committed, nullptr, nullptr, ws,
+                             ws_bytes, stream);
     if (st != VP_OK) return st;
-    st = vp_commit_append(hist, hist_len, lanes, cap, n_commit, committed, status, stream);
+    st = vp_commit_append_rows(hist, hist_len, lanes, rows, cap, n_commit, committed, status, stream);
     if (st != VP_OK) return st;
-    st = vp_lookup_drafts(hist, hist_len, lanes, cap, max_match, pending, status, stream);
+    st = vp_lookup_drafts_rows(hist, hist_len, lanes, rows, cap, max_match, pending, status, stream);
     if (st != VP_OK) return st;
   }
   return VP_OK;
+}
+
+vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_codes, const void* emb_scales,
+                          float emb_ts, int vocab, int hidden, int32_t* hist, int32_t* hist_len, int cap,
+                          int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,
+                          int32_t* committed, void* ws, size_t ws_bytes, int* status, void* stream) {
+  if (lanes > kMaxM / 8) return VP_ERR_SHAPE;
+  return vp_decode_steps_rows(model, steps, 8, emb_codes, emb_scales, emb_ts, vocab, hidden, hist, hist_len, cap,
+                              lanes, max_match, pending, x0, argmax, n_commit, committed, ws, ws_bytes, status,
+                              stream);
 }
 
 }  // extern "C"
