@@ -217,11 +217,13 @@ vp_status vp_head_argmax_accept(const void* w_packed, float tensor_scale, const 
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending,
                            int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws,
                            size_t ws_bytes, void* stream);
-/* The same with R = rows verify rows per lane [WIDE] (1 <= rows <= 32, M = rows * lanes <= 32):
+/* The same with R = rows verify rows per lane [WIDE] (1 <= rows <= 32, M = rows * lanes <= 128;
+ * M > 32 only as runs of 32 rows, so M % 32 == 0 and 32 % rows == 0):
  *   acc = 0; while (acc < R - 1 && argmax[R l + acc] == pending[R l + acc + 1]) acc++;
  *   n_commit[l] = acc + 1 (1..R);  committed[l][j] = argmax[R l + j] for j <= acc, -1 after.
- * n_commit: int32 [M / R]; committed: int32 [M / R][R].  rows = 8 is vp_argmax_accept.
- * VP_ERR_SHAPE for rows or M out of range, or M % rows != 0. */
+ * n_commit: int32 [M / R]; committed: int32 [M / R][R].  rows = 8 is vp_argmax_accept.  The
+ * workspace is vp_workspace_bytes(VP_OP_ARGMAX, min(M, 32), V, 0) (runs of 32 rows reuse it, in
+ * stream order).  VP_ERR_SHAPE for rows or M out of range, or M % rows != 0. */
 vp_status vp_argmax_accept_rows(const float* logits, int M, int V, int rows, const int32_t* pending,
                                 int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws,
                                 size_t ws_bytes, void* stream);
@@ -337,7 +339,8 @@ vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_d
 void vp_model_destroy(vp_model* model);
 
 /* Workspace bytes for vp_verify_pass (M = 8 * lanes) or vp_verify_blocks (M = 1..32) at M rows (0 if
- * invalid). */
+ * invalid); for vp_verify_pass_rows also M = 64, 96, 128 (the workspace of 32 rows, which its passes
+ * of 32 rows share). */
 size_t vp_pass_workspace_bytes(const vp_model* model, int M);
 
 /* One verify pass.  x0: bf16 [M][hidden] (the rows' input hidden states, read-only); pending,
@@ -352,7 +355,9 @@ vp_status vp_verify_pass(const vp_model* model, const void* x0, int M, const int
  * the M rows (M = rows * lanes <= 32, 1 <= rows <= 32), the acceptance of vp_argmax_accept_rows in
  * the head (n_commit: int32 [M / R]; committed: int32 [M / R][R]).  One lane of 16 or 32 rows, or two
  * of 16, verify a deep lookup draft in one pass.  rows = 8 is vp_verify_pass; the workspace is
- * vp_pass_workspace_bytes(model, M). */
+ * vp_pass_workspace_bytes(model, M).  M up to 128 (M % 32 == 0, 32 % rows == 0, trace NULL) runs as
+ * M / 32 consecutive passes of 32 rows (whole lanes each) on the stream, sharing the workspace of
+ * vp_pass_workspace_bytes(model, M) (= that of 32 rows): every pass streams the weights again. */
 vp_status vp_verify_pass_rows(const vp_model* model, const void* x0, int M, int rows, const int32_t* pending,
                               int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace,
                               float* logits, void* ws, size_t ws_bytes, void* stream);
@@ -507,7 +512,8 @@ vp_status vp_embed_nvfp4(const void* codes, const void* scales, float ts, const 
 vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
                            int32_t* pending, int* status, void* stream);
 /* The same with R = rows entries per lane [WIDE]: pending[R l] = the anchor, then R - 1 drafts;
- * 1 <= rows <= 32, lanes * rows <= 32; pending: int32 [R lanes].  rows = 8 is vp_lookup_drafts. */
+ * 1 <= rows <= 32, 1 <= lanes <= 32, lanes * rows <= 128; pending: int32 [R lanes].  rows = 8 is
+ * vp_lookup_drafts. */
 vp_status vp_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, int lanes, int rows, int cap,
                                 int max_match, int32_t* pending, int* status, void* stream);
 /* Appends committed[l][0 .. n_commit[l]) to lane l's history (a lane that would overflow cap, or whose
@@ -516,7 +522,8 @@ vp_status vp_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, in
 vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap, const int32_t* n_commit,
                            const int32_t* committed, int* status, void* stream);
 /* The same with committed rows of R = rows entries [WIDE] (n_commit outside 1..R: left as it is,
- * with the status); 1 <= rows <= 32, lanes * rows <= 32; committed: int32 [lanes][R]. */
+ * with the status); 1 <= rows <= 32, 1 <= lanes <= 32, lanes * rows <= 128; committed: int32
+ * [lanes][R]. */
 vp_status vp_commit_append_rows(int32_t* hist, int32_t* hist_len, int lanes, int rows, int cap,
                                 const int32_t* n_commit, const int32_t* committed, int* status, void* stream);
 /* `steps` rounds with no host in the loop: x0 = embed(pending) (the embedding table emb_codes /
@@ -531,8 +538,9 @@ vp_status vp_decode_steps(const vp_model* model, int steps, const void* emb_code
                           int lanes, int max_match, int32_t* pending, void* x0, int32_t* argmax, int32_t* n_commit,
                           int32_t* committed, void* ws, size_t ws_bytes, int* status, void* stream);
 /* The decode loop with R = rows verify rows per lane [WIDE] (the pass, append and lookup of the
- * _rows calls above; 1 <= rows <= 32, lanes * rows <= 32; x0: bf16 [R lanes][hidden]; pending,
- * committed as there).  rows = 8 is vp_decode_steps. */
+ * _rows calls above; 1 <= rows <= 32, lanes * rows <= 128, above 32 rows as vp_verify_pass_rows
+ * takes them; x0: bf16 [R lanes][hidden]; pending, committed as there).  rows = 8 is
+ * vp_decode_steps. */
 vp_status vp_decode_steps_rows(const vp_model* model, int steps, int rows, const void* emb_codes,
                                const void* emb_scales, float emb_ts, int vocab, int hidden, int32_t* hist,
                                int32_t* hist_len, int cap, int lanes, int max_match, int32_t* pending, void* x0,

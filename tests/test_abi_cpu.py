@@ -337,29 +337,38 @@ def test_phase_trace_only_in_traced_build(V):
 
 
 def test_wide_verify_validation_without_gpu(V):
-    """The R-rows entry points refuse rows outside 1..32, M not a multiple of rows, or more than 32
-    rows in all, before any launch."""
+    """The R-rows entry points refuse rows outside 1..32, M not a multiple of rows, more than 128 rows
+    in all, or more than 32 rows that do not split into runs of 32 rows of whole lanes, before any
+    launch."""
     L = V.lib()
     F = FAKE
     arg = lambda M, Vv, rows, lg=F: L.vp_argmax_accept_rows(lg, M, Vv, rows, F, F, F, F, F, 1 << 20, None)
     assert arg(32, 100, 0) == V.VP_ERR_SHAPE and arg(32, 100, 33) == V.VP_ERR_SHAPE
-    assert arg(24, 100, 16) == V.VP_ERR_SHAPE and arg(64, 100, 32) == V.VP_ERR_SHAPE and arg(8, 100, 16) == V.VP_ERR_SHAPE
+    assert arg(24, 100, 16) == V.VP_ERR_SHAPE and arg(8, 100, 16) == V.VP_ERR_SHAPE
+    assert arg(48, 100, 16) == V.VP_ERR_SHAPE and arg(96, 100, 12) == V.VP_ERR_SHAPE  # runs of 32: M % 32, 32 % R
+    assert arg(160, 100, 32) == V.VP_ERR_SHAPE
     assert arg(32, 0, 16) == V.VP_ERR_SHAPE and arg(32, 100, 16, lg=F + 2) == V.VP_ERR_ALIGNMENT
     assert L.vp_argmax_accept_rows(None, 32, 100, 16, F, F, F, F, F, 1 << 20, None) == V.VP_ERR_INVALID_ARG
-    assert L.vp_lookup_drafts_rows(F, F, 2, 32, 100, 8, F, None, None) == V.VP_ERR_SHAPE   # 64 rows
+    assert L.vp_lookup_drafts_rows(F, F, 5, 32, 100, 8, F, None, None) == V.VP_ERR_SHAPE   # 160 rows
+    assert L.vp_lookup_drafts_rows(F, F, 33, 1, 100, 8, F, None, None) == V.VP_ERR_SHAPE   # 33 lanes
     assert L.vp_lookup_drafts_rows(F, F, 1, 0, 100, 8, F, None, None) == V.VP_ERR_SHAPE
     assert L.vp_lookup_drafts_rows(F, F, 1, 32, 100, 8, F + 2, None, None) == V.VP_ERR_ALIGNMENT
-    assert L.vp_commit_append_rows(F, F, 3, 16, 100, F, F, None, None) == V.VP_ERR_SHAPE   # 48 rows
+    assert L.vp_commit_append_rows(F, F, 9, 16, 100, F, F, None, None) == V.VP_ERR_SHAPE   # 144 rows
+    assert L.vp_commit_append_rows(F, F, 33, 1, 100, F, F, None, None) == V.VP_ERR_SHAPE   # 33 lanes
     assert L.vp_commit_append_rows(F, F, 1, 33, 100, F, F, None, None) == V.VP_ERR_SHAPE
     assert L.vp_commit_append_rows(F, None, 1, 16, 100, F, F, None, None) == V.VP_ERR_INVALID_ARG
 
     m = V.vp_model(256, 512, 1e-6, [_layer(V)], V.vp_head_desc(FAKE, 1.0, 2048))
     need = V.vp_pass_workspace_bytes(m, 32)
+    assert all(V.vp_pass_workspace_bytes(m, M) == need for M in (64, 96, 128))  # passes of 32 rows share it
+    assert V.vp_pass_workspace_bytes(m, 48) == 0 and V.vp_pass_workspace_bytes(m, 160) == 0
 
     def vp(M=32, rows=16, x0=F, ws=F, wb=need):
         return L.vp_verify_pass_rows(m.handle, x0, M, rows, F, F, F, F, None, None, ws, wb, None)
     assert vp(rows=0) == V.VP_ERR_SHAPE and vp(rows=33) == V.VP_ERR_SHAPE and vp(M=24) == V.VP_ERR_SHAPE
     assert vp(M=8, rows=16) == V.VP_ERR_SHAPE and vp(M=40, rows=8) == V.VP_ERR_SHAPE
+    assert vp(M=96, rows=12) == V.VP_ERR_SHAPE and vp(M=160, rows=32) == V.VP_ERR_SHAPE
+    assert L.vp_verify_pass_rows(m.handle, F, 64, 16, F, F, F, F, F, None, F, need, None) == V.VP_ERR_SHAPE  # trace
     assert vp(x0=F + 8) == V.VP_ERR_ALIGNMENT and vp(ws=F + 128) == V.VP_ERR_ALIGNMENT
     assert vp(wb=need - 1) == V.VP_ERR_WORKSPACE
     assert L.vp_verify_pass_rows(m.handle, None, 32, 16, F, F, F, F, None, None, F, need, None) == V.VP_ERR_INVALID_ARG
@@ -368,6 +377,8 @@ def test_wide_verify_validation_without_gpu(V):
         return L.vp_decode_steps_rows(m.handle, steps, rows, F, F, 1.0, 2048, hidden, F, F, 100, lanes, 8, F, F, F, F,
                                       F, F, need, None, None)
     assert ds() == V.VP_OK  # the checks alone
-    assert ds(lanes=3) == V.VP_ERR_SHAPE and ds(rows=0) == V.VP_ERR_SHAPE and ds(rows=32, lanes=2) == V.VP_ERR_SHAPE
+    assert ds(rows=32, lanes=2) == V.VP_OK and ds(rows=16, lanes=8) == V.VP_OK  # 64, 128 rows
+    assert ds(lanes=3) == V.VP_ERR_SHAPE and ds(rows=0) == V.VP_ERR_SHAPE and ds(rows=12, lanes=8) == V.VP_ERR_SHAPE
+    assert ds(rows=32, lanes=5) == V.VP_ERR_SHAPE
     assert ds(hidden=512) == V.VP_ERR_SHAPE
     m.close()

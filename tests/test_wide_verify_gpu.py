@@ -1,6 +1,7 @@
 """The wider verify through the C ABI: R verify rows per lane (anchor + R - 1 drafts; 1 lane of 16 or
-32 rows, 2 lanes of 16, 8 lanes of 4), for the deep lookup drafts of "Speculative decoding"
-(mlx-dspark), section "Lookup drafts" (drafts grow to 32 tokens, 16-32 rows verified in one pass).
+32 rows, 2 lanes of 16, 8 lanes of 4; above 32 rows, runs of 32: 2 lanes of 32, 8 of 16), for the deep
+lookup drafts of "Speculative decoding" (mlx-dspark), section "Lookup drafts" (drafts grow to 32
+tokens, 16-32 rows verified in one pass).
 
 - vp_argmax_accept_rows over given logits: argmax and acceptance bit-exact against the oracle's
   lowest-index argmax and its R-row acceptance, with every prefix length planted;
@@ -48,7 +49,7 @@ def planted(t, rows, rng, vocab):
     return pend
 
 
-@pytest.mark.parametrize("M,rows", [(32, 32), (32, 16), (16, 16), (32, 4), (24, 8)])
+@pytest.mark.parametrize("M,rows", [(32, 32), (32, 16), (16, 16), (32, 4), (24, 8), (64, 32), (128, 16)])
 def test_argmax_accept_rows_matches_oracle(V, M, rows):
     rng = np.random.default_rng(M + rows)
     Vv = 5003
@@ -59,7 +60,7 @@ def test_argmax_accept_rows_matches_oracle(V, M, rows):
     am = torch.empty(M, dtype=torch.int32, device="cuda")
     nc = torch.empty(M // rows, dtype=torch.int32, device="cuda")
     cm = torch.empty((M // rows, rows), dtype=torch.int32, device="cuda")
-    ws = workspace(V.vp_workspace_bytes(V.VP_OP_ARGMAX, M, Vv, 0))
+    ws = workspace(V.vp_workspace_bytes(V.VP_OP_ARGMAX, min(M, 32), Vv, 0))
     V.vp_argmax_accept_rows(torch.from_numpy(lg).cuda(), M, Vv, rows, i32(pend), am, nc, cm, ws)
     torch.cuda.synchronize()
     assert np.array_equal(am.cpu().numpy(), t)
@@ -102,9 +103,39 @@ def test_verify_pass_rows(V, small_model, M, rows):
     assert nc_o.max() > 8 or rows <= 8  # a lane commits more tokens than an 8-row verify can
 
 
+@pytest.mark.parametrize("M,rows", [(64, 32), (128, 16), (96, 8)])
+def test_verify_pass_rows_beyond_32_rows(V, small_model, M, rows):
+    """Above 32 rows the call runs passes of 32 rows: logits and argmax equal to 8-row passes over the
+    same 32-row slices, the acceptance equal to the oracle's over all lanes."""
+    G, dm, _, _ = small_model
+    rng = np.random.default_rng(200 + M + rows)
+    x0 = torch.from_numpy(synth.normal_bf16(9 + M, synth.stream_id(0, synth.T_X0), (M, G.hidden)).view(np.int16)).cuda()
+    ws = workspace(V.vp_pass_workspace_bytes(dm.model, M))
+    assert V.vp_pass_workspace_bytes(dm.model, M) == V.vp_pass_workspace_bytes(dm.model, 32)
+    lg8 = torch.empty((M, G.vocab), dtype=torch.float32, device="cuda")
+    am8 = torch.empty(M, dtype=torch.int32, device="cuda")
+    nc8 = torch.empty(4, dtype=torch.int32, device="cuda")
+    cm8 = torch.empty((4, 8), dtype=torch.int32, device="cuda")
+    z = i32(np.zeros(32, np.int32))
+    for r0 in range(0, M, 32):
+        V.vp_verify_pass(dm.model, x0[r0:r0 + 32], 32, z, am8[r0:r0 + 32], nc8, cm8, None, lg8[r0:r0 + 32], ws)
+    torch.cuda.synchronize()
+    t = am8.cpu().numpy()
+    pend = planted(t, rows, rng, G.vocab)
+    lg = torch.empty((M, G.vocab), dtype=torch.float32, device="cuda")
+    am = torch.empty(M, dtype=torch.int32, device="cuda")
+    nc = torch.empty(M // rows, dtype=torch.int32, device="cuda")
+    cm = torch.empty((M // rows, rows), dtype=torch.int32, device="cuda")
+    V.vp_verify_pass_rows(dm.model, x0, M, rows, i32(pend), am, nc, cm, None, lg, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(lg, lg8) and np.array_equal(am.cpu().numpy(), t)
+    nc_o, cm_o = oracle.accept(t, pend, rows=rows)
+    assert np.array_equal(nc.cpu().numpy(), nc_o) and np.array_equal(cm.cpu().numpy(), cm_o)
+
+
 def test_lookup_and_append_rows_match_oracle(V):
     rng = np.random.default_rng(71)
-    for L, rows in ((1, 32), (2, 16), (4, 8), (8, 4)):
+    for L, rows in ((1, 32), (2, 16), (4, 8), (8, 4), (4, 32), (16, 8), (32, 4)):
         cap = 900
         hist = np.zeros((L, cap), np.int32)
         hl = rng.integers(1, 800, L).astype(np.int32)
@@ -128,7 +159,7 @@ def test_lookup_and_append_rows_match_oracle(V):
         assert np.array_equal(h_d.cpu().numpy(), h2) and np.array_equal(hl_d.cpu().numpy(), hl2) and st.item() == 0
 
 
-@pytest.mark.parametrize("lanes,rows", [(1, 32), (2, 16)])
+@pytest.mark.parametrize("lanes,rows", [(1, 32), (2, 16), (2, 32), (8, 16)])
 def test_decode_steps_rows_equal_host_driven_rounds(V, small_model, lanes, rows):
     G, dm, ec, es = small_model
     M, cap, steps, mm, ts = rows * lanes, 600, 3, 8, 0.5

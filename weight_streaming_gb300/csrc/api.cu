@@ -704,11 +704,13 @@ vp_status vp_argmax_accept_rows(const float* logits, int M, int V, int rows, con
                                 int32_t* argmax, int32_t* n_commit, int32_t* committed, void* ws, size_t ws_bytes,
                                 void* stream) {
   if (!logits || !pending || !argmax || !n_commit || !committed || !ws) return VP_ERR_INVALID_ARG;
-  if (rows < 1 || rows > kMaxM || M < rows || M > kMaxM || M % rows || V < 1) return VP_ERR_SHAPE;
+  if (rows < 1 || rows > kMaxM || M < rows || M > kMaxRows || M % rows || V < 1) return VP_ERR_SHAPE;
+  if (M > kMaxM && (M % kMaxM || kMaxM % rows)) return VP_ERR_SHAPE;  // runs of 32 rows, whole lanes each
   if (!aligned(logits, 4) || !aligned(ws, 256) || !aligned(pending, 4) || !aligned(argmax, 4) ||
       !aligned(n_commit, 4) || !aligned(committed, 4))
     return VP_ERR_ALIGNMENT;
-  if (ws_bytes < vp_workspace_bytes(VP_OP_ARGMAX, M, V, 0)) return VP_ERR_WORKSPACE;
+  const int Mp = M > kMaxM ? kMaxM : M;
+  if (ws_bytes < vp_workspace_bytes(VP_OP_ARGMAX, Mp, V, 0)) return VP_ERR_WORKSPACE;
   int sms = 0;
   vp_status st = device_sms(&sms);
   if (st != VP_OK) return st;
@@ -716,11 +718,15 @@ vp_status vp_argmax_accept_rows(const float* logits, int M, int V, int rows, con
   argmax_chunking(V, &chunk, &n_chunks);
   const WsLayout L = ws_layout(4, 0);
   uint8_t* b = (uint8_t*)ws;
-  argmax_accept_kernel<<<dim3(n_chunks, M), 256, 0, (cudaStream_t)stream>>>(
-      logits, M, V, chunk, n_chunks, rows, pending, argmax, n_commit, committed, (float*)(b + L.head_aux),
-      (unsigned*)(b + L.head_cnt));
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? VP_OK : cuda_fail(e);
+  for (int r0 = 0; r0 < M; r0 += Mp) {  // runs of at most 32 rows, whole lanes each
+    const int l0 = r0 / rows;
+    argmax_accept_kernel<<<dim3(n_chunks, Mp), 256, 0, (cudaStream_t)stream>>>(
+        logits + (size_t)r0 * V, Mp, V, chunk, n_chunks, rows, pending + r0, argmax + r0, n_commit + l0,
+        committed + (size_t)l0 * rows, (float*)(b + L.head_aux), (unsigned*)(b + L.head_cnt));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return VP_OK;
 }
 
 vp_status vp_argmax_accept(const float* logits, int M, int V, const int32_t* pending, int32_t* argmax,
@@ -961,8 +967,8 @@ vp_status vp_model_create(int hidden, int inter, float rms_eps, const vp_layer_d
 void vp_model_destroy(vp_model* model) { delete model; }
 
 size_t vp_pass_workspace_bytes(const vp_model* model, int M) {
-  if (!model || M < 1 || M > kMaxM) return 0;
-  return pass_ws(model, M).total;
+  if (!model || M < 1 || M > kMaxRows || (M > kMaxM && M % kMaxM)) return 0;
+  return pass_ws(model, M > kMaxM ? kMaxM : M).total;  // more rows run as passes of 32
 }
 
 vp_status vp_trace_read(int M, void* dst, size_t bytes, unsigned* launches) {
@@ -1053,19 +1059,28 @@ vp_status vp_verify_pass_rows(const vp_model* md, const void* x0, int M, int row
                               int32_t* argmax, int32_t* n_commit, int32_t* committed, void* trace, float* logits,
                               void* ws, size_t ws_bytes, void* stream) {
   if (!md || !ws) return VP_ERR_INVALID_ARG;
-  if (rows < 1 || rows > kMaxM || M < rows || M > kMaxM || M % rows) return VP_ERR_SHAPE;
+  if (rows < 1 || rows > kMaxM || M < rows || M > kMaxRows || M % rows) return VP_ERR_SHAPE;
+  // More than 32 rows: passes of 32 rows (whole lanes each) one after the other on the stream.
+  if (M > kMaxM && (M % kMaxM || kMaxM % rows || trace)) return VP_ERR_SHAPE;
+  const int Mp = M > kMaxM ? kMaxM : M;
   int sms = 0;
-  vp_status st = pass_args_ok(md, M, ws, ws_bytes, false);
+  vp_status st = pass_args_ok(md, Mp, ws, ws_bytes, false);
   if (st != VP_OK) return st;
   if (!x0 || !pending || !argmax || !n_commit || !committed) return VP_ERR_INVALID_ARG;
   if (!aligned(x0, 16) || (trace && !aligned(trace, 16)) || (logits && !aligned(logits, 4)) || !aligned(pending, 4) ||
       !aligned(argmax, 4) || !aligned(n_commit, 4) || !aligned(committed, 4))
     return VP_ERR_ALIGNMENT;
   if ((st = device_sms(&sms)) != VP_OK) return st;
-  for (const Phase& ph : md->phases[nt_of(M) - 1])
+  for (const Phase& ph : md->phases[nt_of(Mp) - 1])
     if (!slices_ok(ph, sms)) return VP_ERR_SHAPE;
-  return enqueue_pass(md, x0, M, pending, argmax, n_commit, committed, trace, logits, ws, sms, (cudaStream_t)stream,
-                      rows);
+  for (int r0 = 0; r0 < M; r0 += Mp) {
+    const int l0 = r0 / rows;
+    st = enqueue_pass(md, static_cast<const uint16_t*>(x0) + (size_t)r0 * md->hidden, Mp, pending + r0, argmax + r0,
+                      n_commit + l0, committed + (size_t)l0 * rows, trace, logits ? logits + (size_t)r0 * md->head.vocab : nullptr,
+                      ws, sms, (cudaStream_t)stream, rows);
+    if (st != VP_OK) return st;
+  }
+  return VP_OK;
 }
 
 vp_status vp_model_set_cores(vp_model* md, const vp_core_geom* g, const vp_core_desc* cores, int n_layers) {

@@ -35,6 +35,9 @@ int model_hidden(const vp_model* model);
 constexpr int kRowBlock = 16;
 constexpr int kStripRows = 8;
 constexpr int kMaxM = 32;
+// Rows a wide verify call takes (vp_verify_pass_rows and its kin): more than kMaxM run as passes of
+// kMaxM rows, whole lanes each.
+constexpr int kMaxRows = 128;
 
 enum Fmt : int { kFmtNvfp4 = 0, kFmtFp8 = 1, kFmtQ4 = 2 };
 

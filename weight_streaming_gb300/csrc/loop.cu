@@ -135,8 +135,8 @@ vp_status vp_embed_nvfp4(const void* codes, const void* scales, float ts, const 
 vp_status vp_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, int lanes, int rows, int cap,
                                 int max_match, int32_t* pending, int* status, void* stream) {
   if (!hist || !hist_len || !pending) return VP_ERR_INVALID_ARG;
-  if (rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxM || cap < 1 || cap >= (1 << 24) ||
-      max_match < 1 || max_match > 127)
+  if (rows < 1 || rows > kMaxM || lanes < 1 || lanes > kMaxM || lanes * rows > kMaxRows || cap < 1 ||
+      cap >= (1 << 24) || max_match < 1 || max_match > 127)
     return VP_ERR_SHAPE;
   if (!al(hist, 4) || !al(hist_len, 4) || !al(pending, 4) || (status && !al(status, 4))) return VP_ERR_ALIGNMENT;
   lookup_kernel<<<lanes, 256, 0, (cudaStream_t)stream>>>(hist, hist_len, cap, max_match, rows, pending, status);
@@ -146,13 +146,14 @@ vp_status vp_lookup_drafts_rows(const int32_t* hist, const int32_t* hist_len, in
 
 vp_status vp_lookup_drafts(const int32_t* hist, const int32_t* hist_len, int lanes, int cap, int max_match,
                            int32_t* pending, int* status, void* stream) {
+  if (lanes > kMaxM / 8) return VP_ERR_SHAPE;
   return vp_lookup_drafts_rows(hist, hist_len, lanes, 8, cap, max_match, pending, status, stream);
 }
 
 vp_status vp_commit_append_rows(int32_t* hist, int32_t* hist_len, int lanes, int rows, int cap,
                                 const int32_t* n_commit, const int32_t* committed, int* status, void* stream) {
   if (!hist || !hist_len || !n_commit || !committed) return VP_ERR_INVALID_ARG;
-  if (rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxM || cap < 1) return VP_ERR_SHAPE;
+  if (rows < 1 || rows > kMaxM || lanes < 1 || lanes > kMaxM || lanes * rows > kMaxRows || cap < 1) return VP_ERR_SHAPE;
   if (!al(hist, 4) || !al(hist_len, 4) || !al(n_commit, 4) || !al(committed, 4) || (status && !al(status, 4)))
     return VP_ERR_ALIGNMENT;
   append_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(hist, hist_len, lanes, cap, rows, n_commit, committed, status);
@@ -162,6 +163,7 @@ vp_status vp_commit_append_rows(int32_t* hist, int32_t* hist_len, int lanes, int
 
 vp_status vp_commit_append(int32_t* hist, int32_t* hist_len, int lanes, int cap, const int32_t* n_commit,
                            const int32_t* committed, int* status, void* stream) {
+  if (lanes > kMaxM / 8) return VP_ERR_SHAPE;
   return vp_commit_append_rows(hist, hist_len, lanes, 8, cap, n_commit, committed, status, stream);
 }
 
@@ -173,8 +175,9 @@ vp_status vp_decode_steps_rows(const vp_model* model, int steps, int rows, const
   if (!model || !emb_codes || !emb_scales || !hist || !hist_len || !pending || !x0 || !argmax || !n_commit ||
       !committed || !ws)
     return VP_ERR_INVALID_ARG;
-  if (steps < 0 || rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxM) return VP_ERR_SHAPE;
+  if (steps < 0 || rows < 1 || rows > kMaxM || lanes < 1 || lanes * rows > kMaxRows) return VP_ERR_SHAPE;
   const int M = rows * lanes;
+  if (M > kMaxM && (M % kMaxM || kMaxM % rows)) return VP_ERR_SHAPE;  // passes of 32 rows, whole lanes
   // Every argument of the four steps is checked before the first launch, so a bad call enqueues
   // nothing.  (The pass's own per-phase checks still run inside vp_verify_pass.)
   if (vocab < 1 || hidden < 16 || hidden % 16 || (long long)vocab * hidden >= (1LL << 40) || cap < 1 ||
