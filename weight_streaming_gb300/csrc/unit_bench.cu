@@ -156,8 +156,107 @@ cudaError_t dispatch_variant(int variant, const uint8_t* units, int reps, float*
   }
 }
 
+// The ring alone, streaming from device memory: W warps per CTA, each streaming its own contiguous
+// range of `src` through S slots of B bytes (one bulk copy per slot, evict-first, mbarrier
+// completion), refilling a slot as soon as it is consumed -- the executor's producer.  kUnit = 0:
+// consuming a slot is one shared-memory load (the ring's own rate); kUnit = 1: the executor's NVFP4
+// unit at NT n-tiles on the slot's two 2304-byte chunks (B = 4608), activations resident in shared
+// memory.  A wait that runs out sets *err and ends the warp's stream.
+template <int NT, int kUnit>
+__global__ void __launch_bounds__(kThreads, 1) ring_bench_kernel(const uint8_t* src, long long units_per_warp, int S,
+                                                                  int B, int* err, float* out) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t bars[kWarps][8];
+  const int W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0)
+    for (int s = 0; s < S; ++s) mbar_init(&bars[warp][s], 1);
+  uint8_t* xs = smem + (size_t)W * S * B;
+  if (kUnit)
+    for (int i = threadIdx.x; i < NT * 512; i += blockDim.x)
+      reinterpret_cast<uint4*>(xs)[i] = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+  fence_mbar_init();
+  __syncthreads();
+  const uint8_t* base = src + ((long long)blockIdx.x * W + warp) * units_per_warp * B;
+  const uint32_t ring = smem_addr(smem) + warp * S * B, xa = smem_addr(xs) + lane * 16;
+  const uint64_t pol = l2_evict_first_policy();
+  long long issued = 0;
+  if (lane == 0)
+    for (; issued < S && issued < units_per_warp; ++issued) {
+      mbar_arrive_expect_tx(&bars[warp][issued], (uint32_t)B);
+      bulk_g2s(ring + (uint32_t)issued * B, base + issued * B, (uint32_t)B, smem_addr(&bars[warp][issued]), pol);
+    }
+  float acc[NT][4], acc2[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) acc[j][r] = acc2[j][r] = 0.0f;
+  uint32_t sink = 0;
+  for (long long u = 0; u < units_per_warp; ++u) {
+    const int s = (int)(u % S);
+    if (!mbar_wait_bounded(&bars[warp][s], (uint32_t)((u / S) & 1))) {
+      if (lane == 0) atomicExch(err, 1);
+      break;
+    }
+    const uint32_t ua = ring + s * B;
+    if constexpr (kUnit) {
+      unit_nvfp4<NT>(ua, xa, lane, acc, NT == 1 ? acc2 : acc);
+      unit_nvfp4<NT>(ua + 2304, xa + 8 * NT * 512, lane, acc, NT == 1 ? acc2 : acc);
+    } else {
+      sink += lds128(ua + lane * 16).x;
+    }
+    __syncwarp();
+    if (lane == 0 && issued < units_per_warp) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bars[warp][s], (uint32_t)B);
+      bulk_g2s(ua, base + issued * B, (uint32_t)B, smem_addr(&bars[warp][s]), pol);
+      ++issued;
+    }
+  }
+  float v = __uint_as_float(sink & 0x007FFFFFu);
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) v += acc[j][r] + acc2[j][r];
+  out[blockIdx.x * kThreads + threadIdx.x] = v;
+}
+
+template <int NT, int kUnit>
+cudaError_t launch_ring(const uint8_t* src, long long upw, int W, int S, int B, int grid, int* err, float* out,
+                        cudaStream_t st) {
+  const int smem = W * S * B + (kUnit ? NT * 8192 : 0);
+  cudaError_t e =
+      cudaFuncSetAttribute(ring_bench_kernel<NT, kUnit>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  ring_bench_kernel<NT, kUnit><<<grid, W * 32, smem, st>>>(src, upw, S, B, err, out);
+  return cudaGetLastError();
+}
+
 }  // namespace
 }  // namespace vp
+
+// src: device, src_bytes (16-byte aligned); warps W (1..16), slots S (1..8) of B bytes (multiple of
+// 16; unit mode: B = 4608); grid CTAs each stream W ranges of src_bytes / (grid W B) slots.  nt = 0:
+// the ring alone; nt = 1..4: the NVFP4 unit at nt n-tiles per slot.  out: device float [grid][512];
+// err: device int, set to 1 if a wait ran out.  Returns a cudaError_t.
+extern "C" int vp_ring_bench(int nt, int warps, int slots, int slot_bytes, const void* src, long long src_bytes,
+                             int grid, int* err, float* out, void* stream) {
+  if (!src || !err || !out || warps < 1 || warps > vp::kWarps || slots < 1 || slots > 8 || slot_bytes < 16 ||
+      slot_bytes % 16 || grid < 1 || grid > 1024 || nt < 0 || nt > 4 || (nt > 0 && slot_bytes != 4608))
+    return (int)cudaErrorInvalidValue;
+  const long long smem = (long long)warps * slots * slot_bytes + (nt ? nt * 8192 : 0);
+  if (smem > vp::kSmemBytes - 1024) return (int)cudaErrorInvalidValue;
+  const long long upw = src_bytes / ((long long)grid * warps * slot_bytes);
+  if (upw < 1) return (int)cudaErrorInvalidValue;
+  const uint8_t* s = static_cast<const uint8_t*>(src);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  switch (nt) {
+    case 0: return (int)vp::launch_ring<1, 0>(s, upw, warps, slots, slot_bytes, grid, err, out, st);
+    case 1: return (int)vp::launch_ring<1, 1>(s, upw, warps, slots, slot_bytes, grid, err, out, st);
+    case 2: return (int)vp::launch_ring<2, 1>(s, upw, warps, slots, slot_bytes, grid, err, out, st);
+    case 3: return (int)vp::launch_ring<3, 1>(s, upw, warps, slots, slot_bytes, grid, err, out, st);
+    default: return (int)vp::launch_ring<4, 1>(s, upw, warps, slots, slot_bytes, grid, err, out, st);
+  }
+}
 
 // units: device, 9216 bytes (two packed NVFP4 units); out: device float [grid][512]; one launch of
 // `grid` CTAs of 16 warps, each warp running 4 x reps unit chunks.  Returns a cudaError_t.
