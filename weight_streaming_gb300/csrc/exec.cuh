@@ -24,7 +24,9 @@
 //  * K slices: when a phase's activations do not fit shared memory, its K chunks are cut into ks
 //    slices with CTAs assigned in proportion.  Row blocks that several warps share are reduced by
 //    the last contributor (atomic counter, no waiting) in a fixed order, so every result is
-//    bit-reproducible; it then runs the epilogue.
+//    bit-reproducible; it then runs the epilogue.  The partials pass through tensor memory between
+//    warps of one lane quarter (the warps' ranges are handed out quarter by quarter), else through
+//    L2.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,6 +39,16 @@
 namespace vp {
 
 enum : int { kStatusTimeout = 6 };
+
+// ---------------------------------------------------------------- tensor memory (the in-CTA fixups)
+// Warp w reaches lanes 32 (w % 4) .. + 31 of the SM's tensor memory.  The fixups keep each warp's
+// partials there too, in its lane quarter, so that a warp of the same quarter can sum them without
+// an L2 round trip: 4 warps x 2 slots x cs_lane columns (cs_lane <= 8 NT).
+template <int NT>
+constexpr uint32_t kTmemCols = NT == 1 ? 64u : NT == 2 ? 128u : 256u;
+// The range of units a warp takes within its CTA: warps 0, 4, 8, 12 the first four, then 1, 5, 9,
+// 13, ...: consecutive ranges (which share row blocks) then mostly sit in one lane quarter.
+__device__ __forceinline__ int range_of(int warp) { return 4 * (warp & 3) + (warp >> 2); }
 
 static_assert(kSlotBytes >= 2 * 2304 && kSlotBytes >= 2 * 2048, "a slot holds one unit");
 
@@ -197,14 +209,15 @@ __device__ __forceinline__ void cursor_seek(Cursor& c, const Program& prog, cons
     const PhaseSlot& sl = slots[c.p % kPhaseSlots];
     Part P;
     int u;
+    const int q = range_of(warp);
     if (slot_holds(sl, c.p)) {
       P = sl.part;
-      u = sl.wb[warp];
-      c.left = sl.wb[warp + 1] - u;
+      u = sl.wb[q];
+      c.left = sl.wb[q + 1] - u;
     } else {
       P = part_of_cta(prog.ph[c.p], G, cta);
-      u = wbegin(P, warp);
-      c.left = wbegin(P, warp + 1) - u;
+      u = wbegin(P, q);
+      c.left = wbegin(P, q + 1) - u;
     }
     if (c.left > 0) {
       c.kg0 = P.S.kg0;
@@ -249,6 +262,7 @@ struct SmemMisc {
   int tok[kMaxM];
   int abort;
   int flag;
+  uint32_t tmem;  // the CTA's tensor-memory allocation
 };
 static_assert(sizeof(SmemMisc) + 16 <= (size_t)kMiscBytes, "SmemMisc exceeds its shared-memory budget (the last word is the trace parity)");
 
@@ -811,7 +825,20 @@ __device__ void flush(const Phase& ph, const Part& P, const Io& io, int M, int G
   if (resid && wf == wl) load_resid<NT>(ph, io, M, rb, hold, lane);
   if (wf != wl) {
     const size_t cta_slots = (size_t)blockIdx.x * kWarps * 2;
-    store_partial<NT>(io.cslots + (cta_slots + 2 * w + (wbegin(P, w) >= r0 ? 0 : 1)) * slot_floats, lane, two, v, u);
+    const int sel = wbegin(P, w) >= r0 ? 0 : 1;
+    store_partial<NT>(io.cslots + (cta_slots + 2 * w + sel) * slot_floats, lane, two, v, u);
+    // the same partial in the warp's lane quarter of tensor memory, for a contributor of that quarter
+    const uint32_t tq = sm.tmem + ((uint32_t)(32 * (w >> 2)) << 16);
+    {
+      const uint32_t col = (uint32_t)((2 * (w & 3) + sel) * io.cs_lane);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        tmem_st4(tq + col + 4 * j, v[j]);
+        if (two) tmem_st4(tq + col + 4 * (NT + j), u[j]);
+      }
+      tmem_wait_st();
+      tmem_fence_before();
+    }
     // Release (CTA scope): the warp's stores, ordered before by the warp barrier, are visible to the
     // warp that finishes the row block; acquire: that warp then sees every contributor's partial.
     __syncwarp();
@@ -820,26 +847,57 @@ __device__ void flush(const Phase& ph, const Part& P, const Io& io, int M, int G
     old = __shfl_sync(0xffffffffu, old, 0);
     if (old + 1 != (unsigned)(wl - wf + 1)) return;
     __syncwarp();
+    tmem_fence_after();
     if (resid) load_resid<NT>(ph, io, M, rb, hold, lane);
+    float ov[NT][4], ou[NT][4];  // this warp's own partial
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) v[j][r] = u[j][r] = 0.0f;
+      for (int r = 0; r < 4; ++r) {
+        ov[j][r] = v[j][r];
+        ou[j][r] = u[j][r];
+        v[j][r] = u[j][r] = 0.0f;
+      }
     for (int c = wf; c <= wl; ++c) {
-      const float* sl = io.cslots + (cta_slots + 2 * c + (wbegin(P, c) >= r0 ? 0 : 1)) * slot_floats + lane * 4;
+      const int sel_c = wbegin(P, c) >= r0 ? 0 : 1;
+      if (c == w) {
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const float4 q = *reinterpret_cast<const float4*>(sl + 128 * j);
-        v[j][0] += q.x;
-        v[j][1] += q.y;
-        v[j][2] += q.z;
-        v[j][3] += q.w;
-        if (two) {
-          const float4 q2 = *reinterpret_cast<const float4*>(sl + 128 * (NT + j));
-          u[j][0] += q2.x;
-          u[j][1] += q2.y;
-          u[j][2] += q2.z;
-          u[j][3] += q2.w;
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            v[j][r] += ov[j][r];
+            if (two) u[j][r] += ou[j][r];
+          }
+      } else if ((c >> 2) == (w >> 2)) {  // the same lane quarter: from tensor memory
+        const uint32_t col = (uint32_t)((2 * (c & 3) + sel_c) * io.cs_lane);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          float q[4];
+          tmem_ld4(tq + col + 4 * j, q);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) v[j][r] += q[r];
+          if (two) {
+            tmem_ld4(tq + col + 4 * (NT + j), q);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) u[j][r] += q[r];
+          }
+        }
+      } else {
+        const float* sl = io.cslots + (cta_slots + 2 * c + sel_c) * slot_floats + lane * 4;
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          const float4 q = *reinterpret_cast<const float4*>(sl + 128 * j);
+          v[j][0] += q.x;
+          v[j][1] += q.y;
+          v[j][2] += q.z;
+          v[j][3] += q.w;
+          if (two) {
+            const float4 q2 = *reinterpret_cast<const float4*>(sl + 128 * (NT + j));
+            u[j][0] += q2.x;
+            u[j][1] += q2.y;
+            u[j][2] += q2.z;
+            u[j][3] += q2.w;
+          }
         }
       }
     }
@@ -1030,7 +1088,8 @@ __device__ __forceinline__ void phase_units(const Program& prog, const Io& io, c
       hb.v[j][h] = -INFINITY;
       hb.i[j][h] = 0x7fffffff;
     }
-  const int ub = sl.wb[warp], ue = sl.wb[warp + 1];
+  const int wr = range_of(warp);  // the warp's range index within the CTA
+  const int ub = sl.wb[wr], ue = sl.wb[wr + 1];
   const uint32_t xlane = smem_addr(xs) + lane * 16;
   const int pair_stride = (ck / 32) * NT * 512;  // bytes of fragments per chunk
   const uint32_t chunk_bytes = 2u * strip_bytes(ph.fmt);
@@ -1045,7 +1104,7 @@ __device__ __forceinline__ void phase_units(const Program& prog, const Io& io, c
   for (int u = ub; u < ue; ++u) {
     if (rb != cur) {
       if (cur >= 0) {
-        flush<NT, kHead>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+        flush<NT, kHead>(ph, sl.part, io, prog.M, G, wr, cur, acc, acc2, tsc, hb, sm, lane);
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -1088,7 +1147,7 @@ __device__ __forceinline__ void phase_units(const Program& prog, const Io& io, c
     }
   }
   VP_TRACE(lane == 0, p, 2 + warp);
-  if (cur >= 0) flush<NT, kHead>(ph, sl.part, io, prog.M, G, warp, cur, acc, acc2, tsc, hb, sm, lane);
+  if (cur >= 0) flush<NT, kHead>(ph, sl.part, io, prog.M, G, wr, cur, acc, acc2, tsc, hb, sm, lane);
   if (p + 2 < prog.n) {  // the first warp of the CTA done with this phase fills phase p + 2's slot
     int won = 0;
     if (lane == 0) won = atomicCAS(&sm.fillp, p, p + 1) == p;
@@ -1123,6 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
     sm.ps[2].idx = -1;
   }
   VP_TRACE_INIT();
+  if (warp == 0) tmem_alloc(&sm.tmem, kTmemCols<NT>);
   if (warp == 1) fill_slot(sm.ps[0], prog, io, 0, G, cta, lane);
   if (warp == 2) {
     if (prog.n > 1)
@@ -1131,7 +1191,9 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
       sm.ps[1].idx = -1;
   }
   fence_mbar_init();
+  tmem_fence_before();
   __syncthreads();
+  tmem_fence_after();
 
   const uint32_t ring_w = smem_addr(smem) + warp * kSlots * kSlotBytes;
   uint64_t pol = 0;
@@ -1177,6 +1239,10 @@ __global__ void __launch_bounds__(kThreads, 1) exec_kernel(const __grid_constant
   // Every CTA takes the same barriers; a program that took any (several phases, or one phase cut
   // into K slices) resets the counter on the way out, so the workspace is ready for the next call.
   if (nbar > 0) grid_exit(io, G);
+  tmem_fence_before();
+  __syncthreads();  // no warp touches tensor memory any more
+  tmem_fence_after();
+  if (warp == 0) tmem_dealloc(sm.tmem, kTmemCols<NT>);
 }
 
 // ---------------------------------------------------------------- launch (host)
