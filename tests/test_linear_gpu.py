@@ -176,6 +176,32 @@ def test_linear_fp8_dyadic_is_exact(V):
     assert np.array_equal(y.astype(np.float64), y_ref)
 
 
+@pytest.mark.parametrize("fmt,M,N,K", [("nvfp4", 8, 2432, 5120), ("nvfp4", 16, 2432, 17408), ("nvfp4", 24, 2432, 5120),
+                                         ("nvfp4", 32, 2432, 5120), ("fp8", 8, 2432, 6144), ("fp8", 16, 2432, 6144)])
+def test_linear_dyadic_shared_row_blocks_exact(V, fmt, M, N, K):
+    """Shapes whose row blocks are split among several warps of a CTA (one row block of 10 units per
+    CTA over 10 warps at M = 8, K = 5120; pairs and triples of warps in K-sliced phases), so that the
+    in-CTA fixups sum partials from warps of the same tensor-memory lane quarter and of other
+    quarters, with one K slice and with several.  Integer activations and power-of-two scales make
+    every partial sum exact in fp32: the result equals the oracle bit for bit."""
+    rng = np.random.default_rng(M * 7 + K)
+    if fmt == "nvfp4":
+        codes = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
+        scales = np.array([0x30, 0x38, 0x40], np.uint8)[rng.integers(0, 3, (N, K // 16))]
+        xi = rng.integers(-4, 5, (M, K)).astype(np.float32)
+    else:
+        w = np.array([0x38, 0xB8, 0x40, 0x30, 0x00, 0x48], np.uint8)[rng.integers(0, 6, (N, K))]
+        xi = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    x = torch.from_numpy(xi).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if fmt == "nvfp4":
+        y = run_nvfp4(V, codes, scales, x, 1.0)
+        y_ref = oracle.linear(oracle.NVFP4, x, codes, scales, 1.0, N, with_abs=False)
+    else:
+        y = run_fp8(V, w, x, 1.0)
+        y_ref = oracle.linear(oracle.FP8, x, w, None, 1.0, N, with_abs=False)
+    assert np.array_equal(y.astype(np.float64), y_ref)
+
+
 def test_linear_is_deterministic(V):
     codes, scales, x = nvfp4_case(11, 16, 2048, 2048)
     y1 = run_nvfp4(V, codes, scales, x, 1.0)
