@@ -169,7 +169,7 @@ __device__ __forceinline__ bool slot_holds(const PhaseSlot& sl, int p) { return 
 // source addresses of the current unit: within a row block the next unit is the next K chunk
 // (2 strips further on), so a step is two pointer increments; the phase descriptor is read only
 // when the row block or the phase changes.
-struct Cursor {
+struct __align__(16) Cursor {
   int p;             // phase (== prog.n when done)
   int left;          // units left in the phase's range, including the current one
   int rb, kgl;       // row block and group position within the slice of the current unit
@@ -180,6 +180,14 @@ struct Cursor {
   const uint8_t* b;  // the up row block's chunk (interleaved layout), else nullptr
   uint32_t bytes;    // per source
 };
+static_assert(sizeof(Cursor) == 64, "a cursor is four 16-byte words");
+// The warp's cursor moves between shared memory and registers as four 16-byte words.
+__device__ __forceinline__ void cursor_load(Cursor& dst, const Cursor& src) {
+  const uint4* s = reinterpret_cast<const uint4*>(&src);
+  uint4* d = reinterpret_cast<uint4*>(&dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = s[i];
+}
 // Source addresses of the cursor's unit (read from the phase descriptor).
 __device__ __forceinline__ void cursor_locate_in(Cursor& c, const Phase& ph) {
   c.KC = ph.KC;
@@ -1134,11 +1142,16 @@ __device__ __forceinline__ void phase_units(const Program& prog, const Io& io, c
       }
     }
     __syncwarp();
-    if (lane == 0 && pc.p < prog.n && !sm.abort) {
-      fence_proxy_async_smem();
-      issue_unit(pc, ua, &sm.full[warp][slot], pol);
-      cursor_next(pc, prog, sm.ps, G, cta, warp);
-      ++issued;
+    if (lane == 0) {  // the producer works on a register copy of its cursor
+      Cursor c;
+      cursor_load(c, pc);
+      if (c.p < prog.n && !sm.abort) {
+        fence_proxy_async_smem();
+        issue_unit(c, ua, &sm.full[warp][slot], pol);
+        cursor_next(c, prog, sm.ps, G, cta, warp);
+        ++issued;
+        cursor_load(pc, c);
+      }
     }
     ++seq;
     if (++kgl == P.S.kgn) {
